@@ -1,0 +1,186 @@
+"""Plain CPU oracle for the AWQ W4A16 GEMM-layout linear.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline / reference leg may import this module.  The
+product path (the CUDA library and its binding) never imports, links or
+calls it, and this module imports nothing from the product path.
+
+What it computes, and where each step comes from:
+
+* Unpack (tensref.org/formats/awq, "Reader", function ``unpack_awq_gemm``):
+  nibble ``i`` of int32 word ``c`` in a row holds output column
+  ``8*c + ORDER[i]`` with ``ORDER = [0, 2, 4, 6, 1, 3, 5, 7]``; the code is
+  ``(word >> 4*i) & 0xF``.  Zeros are unpacked the same way.  Words are read
+  as their unsigned 32-bit pattern; with the ``& 0xF`` mask an arithmetic
+  right shift of the signed word would give the same nibbles.
+* Dequantize (same function): for input row ``k`` the scale/zero row is
+  ``g = k // G``; ``w = (code - zero) * scale`` evaluated in fp32.  Zeros
+  are used as stored, with no +1 (same page, reject rule AWQ-005; GPTQModel
+  wiki "AWQ", "Group quantization and zero points").  ``group_size == -1``
+  means one group spanning all of K (GPTQModel wiki "AWQ", same section).
+  The page returns the transpose ``[out_features, in_features]``;
+  :func:`dequant_page_layout` reproduces that, :func:`dequant_f32` gives the
+  ``[K, N]`` orientation used by ``x @ W``.
+* fp16 dequant output: one round-to-nearest-even conversion of the exact
+  fp32 value (the fp32 value is exact: |code - zero| <= 15 times an fp16
+  scale fits in 24 bits).
+* GEMM: ``y = x @ W (+ bias)`` in fp64, ``x`` fp16 [M, K] widened exactly,
+  ``W`` the fp32 dequant widened exactly; bias broadcast over rows as in a
+  linear layer (format page, "bias ... optional, shape [out_features]").
+
+Pins (tests/test_oracle.py, run without a GPU): ORDER and its inverse from
+the wiki's "Saved formats and packing" section, a hand-packed word, AWQ-004
+(sequential-nibble decode differs), AWQ-005 (zero equal to code gives an
+exact 0), group_size -1 equals group_size K, symmetric zero 8, exact
+rational dequant values, a pure-Python brute-force GEMM written separately,
+and an exact-arithmetic GEMM case.  Every function here has at least one pin.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# Nibble i of a packed word holds column 8*c + ORDER[i]
+# (tensref.org/formats/awq, "Reader"; GPTQModel wiki "AWQ", "Saved formats
+# and packing").
+ORDER = (0, 2, 4, 6, 1, 3, 5, 7)
+# Inverse permutation, as printed in the wiki's "Saved formats and packing".
+REVERSE_ORDER = (0, 4, 1, 5, 2, 6, 3, 7)
+
+
+def resolve_group_size(K: int, group_size: int) -> int:
+    """G = K for group_size -1, else group_size; K must split into whole groups.
+
+    GPTQModel wiki "AWQ", "Group quantization and zero points": positive
+    values need compatible dimensions, -1 is one group across the row.
+    """
+    G = K if group_size == -1 else int(group_size)
+    if G <= 0 or K % G != 0:
+        raise ValueError(f"group_size {group_size} incompatible with K={K}")
+    return G
+
+
+def unpack_codes(packed: np.ndarray) -> np.ndarray:
+    """[R, C] int32 words -> [R, 8C] int64 codes in 0..15 (format page, "Reader")."""
+    packed = np.ascontiguousarray(packed)
+    assert packed.dtype == np.int32 and packed.ndim == 2
+    u = packed.view(np.uint32).astype(np.uint64)
+    R, C = packed.shape
+    out = np.empty((R, 8 * C), dtype=np.int64)
+    for i in range(8):
+        # every word c of the row: column 8*c + ORDER[i] <- (word >> 4i) & 0xF
+        out[:, ORDER[i]::8] = ((u >> np.uint64(4 * i)) & np.uint64(0xF)).astype(np.int64)
+    return out
+
+
+def pack_codes(codes: np.ndarray) -> np.ndarray:
+    """Inverse of :func:`unpack_codes`: [R, 8C] codes 0..15 -> [R, C] int32.
+
+    The wiki's ``pack_awq`` (section "Saved formats and packing") rejects
+    INT4 widths that are not a multiple of eight; so does this.
+    """
+    codes = np.asarray(codes)
+    R, N = codes.shape
+    if N % 8 != 0:
+        raise ValueError("INT4 AWQ packing needs a width divisible by 8")
+    if codes.min(initial=0) < 0 or codes.max(initial=0) > 15:
+        raise ValueError("codes must lie in 0..15")
+    c = codes.astype(np.uint64)
+    word = np.zeros((R, N // 8), dtype=np.uint64)
+    for i in range(8):
+        word |= c[:, ORDER[i]::8] << np.uint64(4 * i)
+    return word.astype(np.uint32).view(np.int32)
+
+
+def dequant_f32(qweight, qzeros, scales, group_size) -> np.ndarray:
+    """W[k, n] = (code[k, n] - zero[k // G, n]) * scale[k // G, n], fp32, [K, N]."""
+    K = qweight.shape[0]
+    G = resolve_group_size(K, group_size)
+    codes = unpack_codes(qweight).astype(np.float32)
+    zeros = unpack_codes(qzeros).astype(np.float32)
+    sc = np.asarray(scales).astype(np.float32)
+    n_groups = K // G
+    assert zeros.shape[0] == n_groups and sc.shape[0] == n_groups
+    assert zeros.shape[1] == codes.shape[1] == sc.shape[1]
+    g_of_k = np.arange(K) // G
+    return ((codes - zeros[g_of_k]) * sc[g_of_k]).astype(np.float32)
+
+
+def dequant_f16(qweight, qzeros, scales, group_size) -> np.ndarray:
+    """fp16 [K, N]: round-to-nearest-even of :func:`dequant_f32`."""
+    return dequant_f32(qweight, qzeros, scales, group_size).astype(np.float16)
+
+
+def dequant_page_layout(qweight, qzeros, scales, group_size) -> np.ndarray:
+    """fp32 [N, K] ([out_features, in_features]) exactly as the format page
+    returns it: column k of the output is filled from input row k."""
+    K = qweight.shape[0]
+    G = resolve_group_size(K, group_size)
+    w = unpack_codes(qweight)
+    z = unpack_codes(qzeros)
+    sc = np.asarray(scales)
+    out = np.empty((w.shape[1], K), dtype=np.float32)
+    for k in range(K):
+        g = k // G
+        out[:, k] = (w[k].astype(np.float32) - z[g].astype(np.float32)) * sc[g].astype(np.float32)
+    return out
+
+
+def gemm(x, qweight, qzeros, scales, bias, group_size) -> np.ndarray:
+    """y[m, n] = sum_k x[m, k] * W[k, n] (+ bias[n]) in fp64, [M, N]."""
+    W = dequant_f32(qweight, qzeros, scales, group_size).astype(np.float64)
+    y = np.asarray(x).astype(np.float64) @ W
+    if bias is not None:
+        y = y + np.asarray(bias).astype(np.float64)[None, :]
+    return y
+
+
+def dequant_columns_f32(qweight, qzeros, scales, group_size, cols) -> np.ndarray:
+    """fp32 [K, len(cols)]: :func:`dequant_f32` restricted to output columns
+    ``cols`` (column n sits in word n // 8, nibble REVERSE_ORDER[n % 8])."""
+    K = qweight.shape[0]
+    G = resolve_group_size(K, group_size)
+    cols = np.asarray(cols, dtype=np.int64)
+    words = np.ascontiguousarray(qweight).view(np.uint32)[:, cols // 8].astype(np.uint64)
+    zwords = np.ascontiguousarray(qzeros).view(np.uint32)[:, cols // 8].astype(np.uint64)
+    shift = (4 * np.asarray(REVERSE_ORDER, dtype=np.int64)[cols % 8]).astype(np.uint64)
+    codes = ((words >> shift[None, :]) & np.uint64(0xF)).astype(np.float32)
+    zeros = ((zwords >> shift[None, :]) & np.uint64(0xF)).astype(np.float32)
+    sc = np.asarray(scales)[:, cols].astype(np.float32)
+    g_of_k = np.arange(K) // G
+    return ((codes - zeros[g_of_k]) * sc[g_of_k]).astype(np.float32)
+
+
+def gemm_sampled(x, qweight, qzeros, scales, bias, group_size, rows, cols) -> np.ndarray:
+    """fp64 y[rows[i], cols[i]] for each sampled pair i (same definition as
+    :func:`gemm`, evaluated only where asked)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    ucols, inv = np.unique(cols, return_inverse=True)
+    Wc = dequant_columns_f32(qweight, qzeros, scales, group_size, ucols).astype(np.float64)
+    xr = np.asarray(x)[rows].astype(np.float64)           # [S, K]
+    y = np.einsum("sk,sk->s", xr, Wc[:, inv].T)
+    if bias is not None:
+        y = y + np.asarray(bias).astype(np.float64)[cols]
+    return y
+
+
+def gemm_rows(x, qweight, qzeros, scales, bias, group_size, rows) -> np.ndarray:
+    """fp64 y[rows, :] for a subset of activation rows (full N)."""
+    W = dequant_f32(qweight, qzeros, scales, group_size).astype(np.float64)
+    y = np.asarray(x)[np.asarray(rows)].astype(np.float64) @ W
+    if bias is not None:
+        y = y + np.asarray(bias).astype(np.float64)[None, :]
+    return y
+
+
+def within_tolerance(y, y_ref, rel: float = 1e-2):
+    """Elementwise |y - y_ref| <= rel * max(1, |y_ref|); returns (ok, worst ratio)."""
+    y = np.asarray(y, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    bound = rel * np.maximum(1.0, np.abs(y_ref))
+    err = np.abs(y - y_ref)
+    finite = bool(np.all(np.isfinite(y)))
+    ratio = err / bound
+    worst = float(np.max(ratio)) if (ratio.size and finite) else (0.0 if finite else float("inf"))
+    ok = bool(finite and np.all(err <= bound))
+    return ok, worst

@@ -1,0 +1,101 @@
+"""Seeded synthetic inputs for the AWQ W4A16 GEMM-layout linear.
+
+This module only draws random numbers.  It contains none of the method's
+arithmetic: no nibble order, no unpacking, no dequantization, no matmul.
+Both the oracle (test side) and the CUDA path (through tests and the
+benchmark) consume what it produces, and nothing else is shared between
+them.
+
+Why the packed words can be drawn directly: in the AWQ GEMM layout
+(tensref.org/formats/awq, "Reader" pseudo-code) every int32 word of
+``qweight`` / ``qzeros`` holds eight 4-bit codes, one per nibble.  A word
+whose 32 bits are uniform and independent holds eight independent codes,
+each uniform on 0..15, whatever nibble order a reader applies.  Drawing
+uniform 32-bit words therefore has exactly the distribution "codes and
+zeros uniform 0..15, packed with ORDER" that the workloads ask for, without
+this module having to know ORDER.
+
+Workload recipe (per linear, draw order x, codes, zeros, scales, bias):
+  * x      fp16 [M, K]     standard normal drawn in fp32, rounded to fp16
+  * qweight int32 [K, N/8] uniform 32-bit words
+  * qzeros int32 [K/G, N/8] uniform 32-bit words (0x88888888 when sym: every
+           nibble 8, the symmetric zero point of GPTQModel wiki "AWQ",
+           "Group quantization and zero points")
+  * scales fp16 [K/G, N]   uniform [1e-3, 1e-2) drawn in fp32, rounded to fp16
+  * bias   fp16 [N]        normal(0, 0.02) drawn in fp32, rounded to fp16
+G = K when group_size == -1.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = ["awq_linear", "seed_for", "SYM_ZERO_WORD"]
+
+# Every nibble equal to 8.  A word with all nibbles equal is invariant under
+# any nibble permutation, so no ordering knowledge is needed to write it.
+SYM_ZERO_WORD = np.uint32(0x88888888).view(np.int32)
+
+
+def seed_for(config_index: int, shape_index: int) -> int:
+    """Seed of one (config, shape) workload: 1000 + 100*config + shape."""
+    return 1000 + 100 * int(config_index) + int(shape_index)
+
+
+def _groups(K: int, group_size: int) -> int:
+    G = K if group_size == -1 else group_size
+    if G <= 0 or K % G != 0:
+        raise ValueError(f"group_size={group_size} does not divide K={K}")
+    return K // G
+
+
+def awq_linear(seed: int, M: int, K: int, N: int, group_size: int = 128,
+               bias: bool = False, sym: bool = False,
+               x_kind: str = "normal", scale_kind: str = "uniform",
+               bias_kind: str = "normal") -> dict:
+    """Draw one synthetic AWQ linear plus an activation batch.
+
+    Returns a dict of numpy arrays: ``x`` fp16 [M,K], ``qweight`` int32
+    [K,N/8], ``qzeros`` int32 [K/G,N/8], ``scales`` fp16 [K/G,N], ``bias``
+    fp16 [N] or None, plus ``group_size``.
+
+    ``x_kind``: "normal" (N(0,1)) or "smallint" (integers in [-4, 4], used by
+    the exact-arithmetic cases).  ``scale_kind``: "uniform" ([1e-3,1e-2)) or
+    "pow2" (2**-p with p uniform in 4..9, also for exact cases).
+    ``bias_kind``: "normal" or "dyadic" (multiples of 1/64 in [-1, 1]).
+    """
+    if N % 8 != 0:
+        raise ValueError("N must be a multiple of 8 (eight codes per int32 word)")
+    n_groups = _groups(K, group_size)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if x_kind == "normal":
+        x = rng.standard_normal((M, K), dtype=np.float32).astype(np.float16)
+    elif x_kind == "smallint":
+        x = rng.integers(-4, 5, size=(M, K)).astype(np.float16)
+    else:
+        raise ValueError(x_kind)
+    qweight = rng.integers(0, 1 << 32, size=(K, N // 8), dtype=np.uint64)
+    qweight = qweight.astype(np.uint32).view(np.int32)
+    if sym:
+        qzeros = np.full((n_groups, N // 8), SYM_ZERO_WORD, dtype=np.int32)
+    else:
+        qzeros = rng.integers(0, 1 << 32, size=(n_groups, N // 8), dtype=np.uint64)
+        qzeros = qzeros.astype(np.uint32).view(np.int32)
+    if scale_kind == "uniform":
+        scales = rng.uniform(1e-3, 1e-2, size=(n_groups, N)).astype(np.float32)
+        scales = scales.astype(np.float16)
+    elif scale_kind == "pow2":
+        p = rng.integers(4, 10, size=(n_groups, N))
+        scales = np.ldexp(np.ones((n_groups, N), np.float32), -p).astype(np.float16)
+    else:
+        raise ValueError(scale_kind)
+    b = None
+    if bias:
+        if bias_kind == "normal":
+            b = rng.normal(0.0, 0.02, size=N).astype(np.float32).astype(np.float16)
+        elif bias_kind == "dyadic":
+            b = (rng.integers(-64, 65, size=N) / 64.0).astype(np.float16)
+        else:
+            raise ValueError(bias_kind)
+    return {"x": np.ascontiguousarray(x), "qweight": np.ascontiguousarray(qweight),
+            "qzeros": np.ascontiguousarray(qzeros), "scales": np.ascontiguousarray(scales),
+            "bias": b, "group_size": int(group_size), "M": M, "K": K, "N": N}

@@ -1,0 +1,266 @@
+"""Pins for the CPU oracle: each check rests on something other than the oracle
+itself -- values worked by hand from the pages, closed forms, exact rational
+arithmetic, or a pure-Python brute force written separately below."""
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from synth import awq_linear, SYM_ZERO_WORD
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "awq_word_layout.txt")
+
+# Restated literally from the format page (tensref.org/formats/awq, "Reader")
+# and from GPTQModel wiki "AWQ", "Saved formats and packing".
+PAGE_ORDER = [0, 2, 4, 6, 1, 3, 5, 7]
+PAGE_REVERSE_ORDER = [0, 4, 1, 5, 2, 6, 3, 7]
+
+
+def _golden_rows():
+    rows = []
+    with open(GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, word, cols, seq = line.split()
+            rows.append((name, int(word, 16), [int(v) for v in cols.split(",")],
+                         [int(v) for v in seq.split(",")]))
+    return rows
+
+
+def _word(u32):
+    return np.array([[np.uint32(u32)]], dtype=np.uint32).view(np.int32)
+
+
+# ---------------------------------------------------------------- ORDER ----
+
+def test_order_tables_match_pages_and_are_inverse():
+    assert list(oracle.ORDER) == PAGE_ORDER
+    assert list(oracle.REVERSE_ORDER) == PAGE_REVERSE_ORDER
+    for i in range(8):
+        assert oracle.REVERSE_ORDER[oracle.ORDER[i]] == i
+        assert oracle.ORDER[oracle.REVERSE_ORDER[i]] == i
+
+
+@pytest.mark.parametrize("row", _golden_rows(), ids=lambda r: r[0])
+def test_golden_words_unpack(row):
+    name, word, cols, _ = row
+    assert oracle.unpack_codes(_word(word))[0].tolist() == cols
+
+
+@pytest.mark.parametrize("row", _golden_rows(), ids=lambda r: r[0])
+def test_golden_words_pack(row):
+    name, word, cols, _ = row
+    packed = oracle.pack_codes(np.array([cols]))
+    assert int(packed.view(np.uint32)[0, 0]) == word
+
+
+def test_awq004_sequential_decode_differs():
+    """AWQ-004: sequential nibbles are not the AWQ order."""
+    for name, word, cols, seq in _golden_rows():
+        sequential = [(word >> (4 * j)) & 0xF for j in range(8)]
+        assert sequential == seq
+        if len(set(cols)) > 1 and name != "sign_nibble":
+            assert sequential != cols
+    # and the oracle does not decode sequentially
+    assert oracle.unpack_codes(_word(0x75316420))[0].tolist() != [0, 2, 4, 6, 1, 3, 5, 7]
+
+
+def test_pack_unpack_round_trip_random_words():
+    rng = np.random.default_rng(7)
+    q = rng.integers(0, 1 << 32, size=(37, 19), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    codes = oracle.unpack_codes(q)
+    assert codes.shape == (37, 152) and codes.min() >= 0 and codes.max() <= 15
+    assert np.array_equal(oracle.pack_codes(codes), q)
+
+
+def test_pack_rejects_width_not_multiple_of_8():
+    with pytest.raises(ValueError):
+        oracle.pack_codes(np.zeros((2, 12), dtype=np.int64))
+
+
+def test_half2_pair_property():
+    """(q >> 4j) & 0x000F000F holds columns 2j (low half) and 2j+1 (high half):
+    a property of ORDER that the CUDA kernels rely on; checked here against the
+    oracle's unpack on random words."""
+    rng = np.random.default_rng(3)
+    words = rng.integers(0, 1 << 32, size=4096, dtype=np.uint64).astype(np.uint32)
+    codes = oracle.unpack_codes(words.view(np.int32).reshape(-1, 1))
+    for j in range(4):
+        pair = (words >> np.uint32(4 * j)) & np.uint32(0x000F000F)
+        assert np.array_equal(pair & 0xF, codes[:, 2 * j])
+        assert np.array_equal(pair >> 16, codes[:, 2 * j + 1])
+
+
+# ------------------------------------------------------------- dequant ----
+
+def test_awq005_no_plus_one_on_zeros():
+    """AWQ-005: code == zero gives exactly 0; zero 0 and code 1 gives the scale."""
+    K, N = 4, 8
+    codes = np.full((K, N), 3)
+    codes[1] = 1
+    zeros = np.full((1, N), 3)
+    zeros_row1 = np.zeros((1, N), dtype=np.int64)
+    scales = np.full((1, N), 0.25, dtype=np.float16)
+    W = oracle.dequant_f32(oracle.pack_codes(codes), oracle.pack_codes(zeros), scales, -1)
+    assert np.all(W[0] == 0.0) and np.all(W[2:] == 0.0)
+    assert np.all(W[1] == np.float32(-0.5))            # (1 - 3) * 0.25
+    W2 = oracle.dequant_f32(oracle.pack_codes(codes), oracle.pack_codes(zeros_row1), scales, -1)
+    assert np.all(W2[1] == np.float32(0.25))            # (1 - 0) * 0.25, no +1
+
+
+def test_group_index_is_k_div_G():
+    """Rows 0..G-1 use scale row 0, rows G..2G-1 scale row 1 (k // G)."""
+    K, N, G = 8, 8, 4
+    codes = np.full((K, N), 5)
+    zeros = np.stack([np.full(N, 1), np.full(N, 2)])
+    scales = np.stack([np.full(N, 1.0), np.full(N, 2.0)]).astype(np.float16)
+    W = oracle.dequant_f32(oracle.pack_codes(codes), oracle.pack_codes(zeros), scales, G)
+    assert np.all(W[:4] == 4.0) and np.all(W[4:] == 6.0)   # (5-1)*1, (5-2)*2
+
+
+def test_group_minus_one_equals_group_K():
+    d = awq_linear(11, 2, 64, 32, group_size=-1, bias=True)
+    a = oracle.dequant_f32(d["qweight"], d["qzeros"], d["scales"], -1)
+    b = oracle.dequant_f32(d["qweight"], d["qzeros"], d["scales"], 64)
+    assert np.array_equal(a, b)
+    assert d["scales"].shape == (1, 32) and d["qzeros"].shape == (1, 4)
+
+
+def test_symmetric_zero_eight():
+    d = awq_linear(12, 1, 32, 16, group_size=16, sym=True)
+    assert np.all(d["qzeros"] == SYM_ZERO_WORD)
+    codes = oracle.unpack_codes(d["qweight"]).astype(np.float32)
+    W = oracle.dequant_f32(d["qweight"], d["qzeros"], d["scales"], 16)
+    s = d["scales"].astype(np.float32)[np.arange(32) // 16]
+    assert np.array_equal(W, (codes - 8.0) * s)
+
+
+def test_dequant_exact_rational_and_fp16_rne():
+    d = awq_linear(13, 1, 256, 64, group_size=32)
+    W32 = oracle.dequant_f32(d["qweight"], d["qzeros"], d["scales"], 32)
+    W16 = oracle.dequant_f16(d["qweight"], d["qzeros"], d["scales"], 32)
+    rng = np.random.default_rng(0)
+    for _ in range(400):
+        k, n = int(rng.integers(256)), int(rng.integers(64))
+        word = int(d["qweight"].view(np.uint32)[k, n // 8])
+        zword = int(d["qzeros"].view(np.uint32)[k // 32, n // 8])
+        nib = PAGE_ORDER.index(n % 8)
+        c, z = (word >> 4 * nib) & 15, (zword >> 4 * nib) & 15
+        exact = Fraction(c - z) * Fraction(float(d["scales"][k // 32, n]))
+        assert Fraction(float(W32[k, n])) == exact
+        # one round-to-nearest-even to fp16 (Python's half packing rounds half-even)
+        assert struct.pack("<e", float(exact)) == W16[k, n].tobytes()
+
+
+def test_page_layout_is_transpose():
+    d = awq_linear(14, 1, 64, 24, group_size=16)
+    P = oracle.dequant_page_layout(d["qweight"], d["qzeros"], d["scales"], 16)
+    assert P.shape == (24, 64)
+    assert np.array_equal(P, oracle.dequant_f32(d["qweight"], d["qzeros"], d["scales"], 16).T)
+
+
+def test_dequant_columns_matches_full():
+    d = awq_linear(15, 1, 128, 80, group_size=32)
+    W = oracle.dequant_f32(d["qweight"], d["qzeros"], d["scales"], 32)
+    cols = np.array([0, 1, 7, 8, 13, 42, 79, 79, 3])
+    assert np.array_equal(oracle.dequant_columns_f32(d["qweight"], d["qzeros"], d["scales"], 32, cols),
+                          W[:, cols])
+
+
+def test_bad_group_size_rejected():
+    with pytest.raises(ValueError):
+        oracle.resolve_group_size(100, 48)
+    with pytest.raises(ValueError):
+        oracle.resolve_group_size(64, 0)
+
+
+# ---------------------------------------------------------------- GEMM ----
+
+def _brute_force_gemm(d):
+    """Pure-Python restatement: for every (m, n) find the nibble holding column
+    n by searching the page's ORDER list, decode code and zero with explicit
+    shifts, and sum x * ((code - zero) * scale) with math.fsum."""
+    x, qw, qz, sc, b = d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"]
+    M, K = x.shape
+    N = qw.shape[1] * 8
+    G = K if d["group_size"] == -1 else d["group_size"]
+    y = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            nib = [i for i in range(8) if PAGE_ORDER[i] == n % 8][0]
+            terms = []
+            for k in range(K):
+                word = int(qw[k, n // 8]) & 0xFFFFFFFF
+                zword = int(qz[k // G, n // 8]) & 0xFFFFFFFF
+                code = (word >> (4 * nib)) & 0xF
+                zero = (zword >> (4 * nib)) & 0xF
+                terms.append(float(x[m, k]) * ((code - zero) * float(sc[k // G, n])))
+            if b is not None:
+                terms.append(float(b[n]))
+            y[m, n] = math.fsum(terms)
+    return y
+
+
+@pytest.mark.parametrize("M,K,N,G,bias", [(3, 32, 16, 8, True), (2, 48, 24, -1, False),
+                                          (1, 64, 8, 16, True), (4, 16, 32, 16, False)])
+def test_gemm_brute_force(M, K, N, G, bias):
+    d = awq_linear(100 + M + K + N, M, K, N, group_size=G, bias=bias)
+    y = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    yb = _brute_force_gemm(d)
+    np.testing.assert_allclose(y, yb, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_exact_dyadic_case():
+    """x small integers, scales powers of two, dyadic bias: every product and
+    sum is exact, so the fp64 oracle equals exact rational arithmetic."""
+    d = awq_linear(21, 3, 64, 16, group_size=16, bias=True, x_kind="smallint",
+                   scale_kind="pow2", bias_kind="dyadic")
+    y = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 16)
+    codes = oracle.unpack_codes(d["qweight"])
+    zeros = oracle.unpack_codes(d["qzeros"])
+    for m in range(3):
+        for n in range(16):
+            acc = Fraction(float(d["bias"][n]))
+            for k in range(64):
+                acc += Fraction(int(d["x"][m, k])) * (codes[k, n] - zeros[k // 16, n]) * \
+                    Fraction(float(d["scales"][k // 16, n]))
+            assert Fraction(float(y[m, n])) == acc
+
+
+def test_gemm_sampled_and_rows_match_full():
+    d = awq_linear(22, 5, 96, 40, group_size=32, bias=True)
+    args = (d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 32)
+    y = oracle.gemm(*args)
+    rows = np.array([0, 4, 2, 2, 1])
+    cols = np.array([0, 39, 17, 18, 8])
+    np.testing.assert_allclose(oracle.gemm_sampled(*args, rows, cols), y[rows, cols], rtol=1e-13)
+    np.testing.assert_allclose(oracle.gemm_rows(*args, [1, 3]), y[[1, 3]], rtol=1e-13)
+
+
+def test_within_tolerance_definition():
+    ok, worst = oracle.within_tolerance([1.0, 200.0], [1.009, 201.0])
+    assert ok and worst < 1.0
+    ok, _ = oracle.within_tolerance([0.0], [0.011])
+    assert not ok
+    ok, _ = oracle.within_tolerance([np.nan], [0.0])
+    assert not ok
+
+
+def test_synth_is_seeded_and_shaped():
+    a = awq_linear(5, 2, 256, 64, group_size=128, bias=True)
+    b = awq_linear(5, 2, 256, 64, group_size=128, bias=True)
+    for key in ("x", "qweight", "qzeros", "scales", "bias"):
+        assert np.array_equal(a[key], b[key])
+    assert a["qweight"].shape == (256, 8) and a["qzeros"].shape == (2, 8)
+    assert a["scales"].shape == (2, 64) and a["scales"].dtype == np.float16
+    s = a["scales"].astype(np.float32)
+    assert s.min() >= 9.99e-4 and s.max() <= 1.0001e-2
+    codes = oracle.unpack_codes(awq_linear(6, 1, 512, 512)["qweight"])
+    counts = np.bincount(codes.ravel(), minlength=16)
+    assert counts.min() > 0.9 * codes.size / 16   # uniform codes 0..15
