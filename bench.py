@@ -1,0 +1,383 @@
+#!/usr/bin/env python
+"""Benchmark: AWQ W4A16 awq_gemm on the 7B-shaped decode workload (M = 1, the three
+linears 4096x4096, 4096x11008, 11008x4096, group size 128, fp16 bias).
+
+A step is one pass of the hot path over one batch: three awq_gemm calls, one per
+linear (one kernel launch each).  Inputs are seeded synthetic tensors resident in HBM.
+Weights rotate over R independent sets whose total (R * 55.7 MB) exceeds the 129 MB L2,
+so every step streams its weights from HBM.  Steps are replayed from CUDA graphs and
+timed with CUDA events on the replay stream, after W warm-up steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain restatement of the method the tests
+check against) on the host cores on a bounded column sample of the same workload.
+Prints one JSON line (rank 0).  Multi-GPU (torchrun): each rank runs an independent
+replica; the reported value is the sum over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = ("awq_gemm GB/s (decode, % HBM roofline) and TFLOP/s (prefill, % fp16 peak) "
+          "on 1 GB300")
+UNIT = "GB/s"
+LINEARS = ["7b_decode_m1_4096x4096_bias", "7b_decode_m1_4096x11008_bias",
+           "7b_decode_m1_11008x4096_bias"]
+WORKLOAD_NAME = ("7B decode GEMV M=1: linears 4096x4096, 4096x11008, 11008x4096; "
+                 "group_size 128; fp16 bias")
+L2_BYTES = 129e6
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(M, K, N, G, bias):
+    """Bytes the method must move once: packed weights, zeros, scales, x, y, bias."""
+    G = K if G == -1 else G
+    ng = K // G
+    return K * N // 2 + ng * N // 2 + 2 * ng * N + 2 * M * K + 2 * M * N + (2 * N if bias else 0)
+
+
+def workload_linears(set_index: int):
+    out = []
+    for name in LINEARS:
+        cfg, si, _, M, K, N, G, b = synth.workload(name)
+        seed = synth.seed_for(cfg, si) + 100000 * set_index
+        out.append(synth.awq_linear(seed, M, K, N, group_size=G, bias=b))
+    return out
+
+
+def step_bytes(lins):
+    return sum(algorithmic_bytes(d["M"], d["K"], d["N"], d["group_size"], d["bias"] is not None)
+               for d in lins)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples; keeps those taken inside [start, end]."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", str(index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def start(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.05)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except Exception:
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.02 <= r[0] <= self.t1 + 0.02]
+        used = inside
+        if not used and rows:
+            mid = 0.5 * (self.t0 + self.t1)
+            used = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median([r[1] for r in used]) if used else None,
+                "sm_max_mhz": max(r[2] for r in used) if used else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------- CPU oracle ----
+
+def oracle_sample(width: int):
+    """Column sample of the workload: for each linear, its first `width` output columns
+    (itself a valid AWQ linear of N = width).  Returns (inputs, algorithmic bytes)."""
+    lins = workload_linears(0)
+    sub = []
+    for d in lins:
+        w = min(width, d["N"])
+        sub.append({"x": d["x"], "qweight": np.ascontiguousarray(d["qweight"][:, :w // 8]),
+                    "qzeros": np.ascontiguousarray(d["qzeros"][:, :w // 8]),
+                    "scales": np.ascontiguousarray(d["scales"][:, :w]),
+                    "bias": None if d["bias"] is None else d["bias"][:w],
+                    "group_size": d["group_size"], "M": d["M"], "K": d["K"], "N": w})
+    return sub, step_bytes(sub)
+
+
+def oracle_step(sub):
+    import oracle
+    for d in sub:
+        oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], d["group_size"])
+
+
+def cpu_baseline(seconds: float = 12.0):
+    width = 1024
+    sub, nbytes = oracle_sample(width)
+    oracle_step(sub)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(sub)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": nbytes * n / el / 1e9, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {width} output columns of each of the three linears (M=1), "
+                      f"{n} passes in {el:.1f} s; numpy fp64 matmul (BLAS threads), "
+                      "unpack/dequant single-threaded"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    # size each step so that warm-up + timed steps end within about two minutes
+    probe_sub, _ = oracle_sample(512)
+    t0 = time.perf_counter()
+    oracle_step(probe_sub)
+    per512 = max(time.perf_counter() - t0, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    width = int(max(8, min(28672, 512 * budget / per512)) // 8 * 8)
+    sub, nbytes = oracle_sample(width)
+    for _ in range(args.warmup):
+        oracle_step(sub)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sub)
+    el = time.perf_counter() - t0
+    value = nbytes * args.steps / el / 1e9
+    desc = (f"first {width} output columns of each of the three linears (M=1) per step; "
+            "numpy fp64 matmul (BLAS threads), unpack/dequant single-threaded")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME + " (column sample)", "sample_width": min(width, 11008)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------- GPU path ----
+
+def run_ours(args, rank, world, local):
+    import torch
+    from w4a16_weight_only_gb300 import build as _build
+    _build.build()
+    import w4a16_weight_only_gb300 as awq
+
+    torch.cuda.set_device(local)
+    if not awq.runtime_available():
+        raise RuntimeError("awq runtime unavailable: " + awq.last_error())
+    lins0 = workload_linears(0)
+    per_set = sum(d["qweight"].nbytes + d["qzeros"].nbytes + d["scales"].nbytes for d in lins0)
+    R = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)))
+    sets = []
+    for r in range(R):
+        lins = lins0 if r == 0 else workload_linears(r)
+        dev = []
+        for d in lins:
+            t = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "qweight", "qzeros", "scales")}
+            t["bias"] = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
+            t["y"] = torch.empty((d["M"], d["N"]), dtype=torch.float16, device="cuda")
+            t["G"] = d["group_size"]
+            dev.append(t)
+        sets.append(dev)
+    nbytes = step_bytes(lins0)
+    launches_per_step = len(LINEARS)
+
+    def step(r):
+        for t in sets[r]:
+            awq.awq_gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], t["bias"],
+                         group_size=t["G"], out=t["y"])
+
+    # eager warm-up (first calls set kernel attributes), then capture
+    for r in range(R):
+        step(r)
+    torch.cuda.synchronize()
+    cycle = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cycle):
+        for r in range(R):
+            step(r)
+    singles = []
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(r)
+        singles.append(g)
+
+    def run_steps(k):
+        full, rem = divmod(k, R)
+        for _ in range(full):
+            cycle.replay()
+        for r in range(rem):
+            singles[r].replay()
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    run_steps(max(args.warmup, 3))
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start()
+    ev0.record(stream)
+    run_steps(args.steps)
+    ev1.record(stream)
+    ev1.synchronize()
+    clocks.end()
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    clk = clocks.finish()
+    elapsed_max = reduce_max(elapsed, world)
+    awq.device_status()
+
+    # end to end through the public API: pinned host x in, y read back, every step
+    host = []
+    for t in sets[0]:
+        host.append((t["x"].cpu().pin_memory(), torch.empty_like(t["y"], device="cpu").pin_memory()))
+    h2d = sum(h[0].numel() * 2 for h in host)
+    d2h = sum(h[1].numel() * 2 for h in host)
+    xs = [[torch.empty_like(t["x"]) for t in s] for s in sets]
+
+    def e2e_step(r):
+        for (hx, hy), t, xd in zip(host, sets[r], xs[r]):
+            xd.copy_(hx, non_blocking=True)
+            awq.awq_gemm(xd, t["qweight"], t["qzeros"], t["scales"], t["bias"],
+                         group_size=t["G"], out=t["y"])
+            hy.copy_(t["y"], non_blocking=True)
+        stream.synchronize()
+
+    e2e_steps = min(args.steps, 2000)
+    for i in range(max(args.warmup, 3)):
+        e2e_step(i % R)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i % R)
+    e1.record(stream)
+    e1.synchronize()
+    e2e_el = reduce_max(e0.elapsed_time(e1) / 1e3, world)
+
+    peak, peak_kind = peaks()
+    achieved = nbytes * args.steps / elapsed / 1e9
+    value = world * nbytes * args.steps / elapsed_max / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "M": 1, "group_size": 128, "bias": True,
+                   "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {R} rotating weight sets, "
+                         f"{R * per_set / 1e6:.0f} MB > 129 MB",
+                   "bytes_per_step": nbytes, "launch": "CUDA graph replays"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "kernel": "decode_kernel (awq_gemm decode path)",
+                     "traffic": None},
+        "e2e": {"value": world * nbytes * e2e_steps / e2e_el / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    return line if rank == 0 else None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

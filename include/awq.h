@@ -1,0 +1,147 @@
+/*
+ * awq.h -- C ABI of libawq_gb300.so: AWQ W4A16 weight-only linear on GB300 (sm_103a).
+ *
+ * The weight layout is the AWQ "GEMM" checkpoint pack (tensref.org/formats/awq,
+ * "Reader" pseudo-code; GPTQModel wiki "AWQ", "Saved formats and packing"):
+ *
+ *   qweight int32 [K, N/8]    row-major; nibble i (bits 4i..4i+3) of word c in row k
+ *                             holds the 4-bit code of output column 8c + ORDER[i],
+ *                             ORDER = {0,2,4,6,1,3,5,7}
+ *   qzeros  int32 [K/G, N/8]  zero points, packed exactly like qweight
+ *   scales  fp16  [K/G, N]    row-major
+ *   bias    fp16  [N]         optional
+ *
+ * with K = in_features, N = out_features, G = group_size (G = K when group_size is -1:
+ * one group across the row, GPTQModel wiki "AWQ", "Group quantization and zero points").
+ * Every weight is  w[k][n] = (code[k][n] - zero[k/G][n]) * scale[k/G][n]  with the zero
+ * used as stored (no +1; format page, reject rule AWQ-005).
+ *
+ * Conventions shared by every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller, dense and row-major.  The
+ *    library never frees or retains them and allocates no device memory per call.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream) and never
+ *    synchronize.  Argument errors are found on the host BEFORE any launch and returned
+ *    synchronously; nothing is launched then.
+ *  - On failure the call returns a non-zero awq_status_t and awq_last_error() holds a
+ *    message for the calling thread.  On success awq_last_error() returns "".
+ *  - Launch failures (cudaGetLastError after the launch) return AWQ_ERR_CUDA with the CUDA
+ *    error string.
+ *  - The library is built for compute capability 10.3 only; on another device every
+ *    compute entry point returns AWQ_ERR_UNSUPPORTED_DEVICE.
+ *  - Sizes are int64; each of M, K, N must be below 2^31, and M*N, K*N below 2^40.
+ */
+#ifndef AWQ_GB300_H
+#define AWQ_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* awq_stream_t;
+
+typedef enum awq_status {
+  AWQ_OK = 0,
+  AWQ_ERR_INVALID_ARGUMENT = 1,  /* null pointer, negative size, bad group_size, bad enum */
+  AWQ_ERR_UNSUPPORTED_SHAPE = 2, /* N not a multiple of 8, K not a multiple of G, size limits */
+  AWQ_ERR_MISALIGNED = 3,        /* a pointer below its element alignment */
+  AWQ_ERR_UNSUPPORTED_DEVICE = 4,/* current device is not compute capability 10.3 */
+  AWQ_ERR_CUDA = 5,              /* a CUDA runtime call or launch failed */
+  AWQ_ERR_TIMEOUT = 6            /* a bounded device-side wait gave up (see awq_device_status) */
+} awq_status_t;
+
+typedef enum awq_dtype { AWQ_DTYPE_F16 = 0, AWQ_DTYPE_F32 = 1 } awq_dtype_t;
+
+/* Kernel family used by awq_gemm_ex.  AUTO picks by M, K, N, G and alignment. */
+typedef enum awq_path {
+  AWQ_PATH_AUTO = 0,
+  AWQ_PATH_DECODE = 1,   /* split-K streaming kernel for small M (tensor-core m16n8k16) */
+  AWQ_PATH_PREFILL = 2,  /* tcgen05/TMEM tensor-core kernel with TMA-fed tiles, large M */
+  AWQ_PATH_GENERIC = 3   /* any valid shape and alignment; slow, used for ragged shapes */
+} awq_path_t;
+
+/* 1 when the current CUDA device is compute capability 10.3 and this library's kernels
+ * load on it, else 0 (the reason is then in awq_last_error()).  Mirrors the wiki's
+ * awq_runtime_available() / awq_runtime_error() pair (GPTQModel wiki "AWQ",
+ * "Native AWQ runtime helpers"). */
+int awq_runtime_available(void);
+
+/* Thread-local message of the last failing call on this thread; "" after a success. */
+const char* awq_last_error(void);
+
+/* Static name of a status code ("AWQ_OK", ...). */
+const char* awq_status_string(awq_status_t status);
+
+/*
+ * awq_dequant -- unpack and dequantize the whole weight (format page, "Reader"; the
+ * wiki's awq_dequantize_weights in "Native AWQ runtime helpers").
+ *
+ *   w_out[k][n] = (code[k][n] - zero[k/G][n]) * scale[k/G][n]     row-major [K, N]
+ *
+ * out_dtype AWQ_DTYPE_F32: the exact fp32 value (it is always representable).
+ * out_dtype AWQ_DTYPE_F16: that value rounded once, to nearest even.
+ * Note the orientation: [K, N] (what x @ W needs); the format page's pseudo-code returns
+ * the transpose [N, K].
+ * Requirements: K > 0, N >= 0, N % 8 == 0, group_size == -1 or (> 0 and K % group_size
+ * == 0); qweight/qzeros 4-byte aligned, scales 2-byte aligned, w_out aligned to its
+ * element size.  N == 0 returns AWQ_OK without a launch.  One kernel launch otherwise.
+ */
+awq_status_t awq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
+                         int64_t K, int64_t N, int64_t group_size,
+                         void* w_out, awq_dtype_t out_dtype, awq_stream_t stream);
+
+/*
+ * awq_gemm -- fused W4A16 linear (the wiki's awq_gemm_forward in "Native GEMM" /
+ * "Native AWQ runtime helpers"; fp32 accumulation always, as with its default
+ * GPTQMODEL_FP32_ACCUM):
+ *
+ *   y[m][n] = fp16_rne( sum_k x[m][k] * w[k][n]  (+ bias[n]) )
+ *
+ *   x_f16     fp16 [M, K] activations
+ *   qweight   int32 [K, N/8], qzeros int32 [K/G, N/8], scales_f16 fp16 [K/G, N]
+ *   bias_f16  fp16 [N] or NULL
+ *   y_f16     fp16 [M, N] output; must not overlap any input
+ *
+ * Argument order is x, qweight, qzeros, scales, bias: qzeros BEFORE scales.  (The wiki's
+ * Python wrappers pass scales before qzeros; bindings must not copy that order here.)
+ * The dense weight is never written to memory.  The dequantized values never leave
+ * registers or shared memory.  Accumulation is fp32 with a fixed summation order for a
+ * given (M, K, N, G): repeated calls give bitwise-identical y.
+ * Requirements: as awq_dequant, plus x/y/bias 2-byte aligned.  M == 0 or N == 0 returns
+ * AWQ_OK without a launch (the wiki's "Empty input returns an appropriately shaped output
+ * without launching").  Exactly one kernel launch otherwise.
+ * Accuracy: |y - y_exact| <= 1e-2 * max(1, |y_exact|) elementwise, y_exact being the
+ * same sum in exact arithmetic.
+ */
+awq_status_t awq_gemm(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                      const void* scales_f16, const void* bias_f16,
+                      int64_t M, int64_t K, int64_t N, int64_t group_size,
+                      void* y_f16, awq_stream_t stream);
+
+/* awq_gemm with an explicit kernel family (tests and benchmarks).  A family that cannot
+ * take the shape or alignment returns AWQ_ERR_UNSUPPORTED_SHAPE / AWQ_ERR_MISALIGNED. */
+awq_status_t awq_gemm_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                         const void* scales_f16, const void* bias_f16,
+                         int64_t M, int64_t K, int64_t N, int64_t group_size,
+                         void* y_f16, awq_path_t path, awq_stream_t stream);
+
+/* The family awq_gemm would pick for this shape and these pointers (no launch, no
+ * device access).  Returns AWQ_PATH_AUTO (0) on an invalid shape. */
+awq_path_t awq_gemm_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size,
+                                const void* x_f16, const int32_t* qweight,
+                                const int32_t* qzeros, const void* scales_f16,
+                                const void* bias_f16, const void* y_f16);
+
+/* Synchronizes `stream`, then reads and clears the library's device status word on the
+ * current device.  Returns AWQ_ERR_TIMEOUT if a kernel gave up a bounded wait since the
+ * last check (its output is then unspecified), AWQ_OK otherwise. */
+awq_status_t awq_device_status(awq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AWQ_GB300_H */

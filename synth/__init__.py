@@ -99,3 +99,53 @@ def awq_linear(seed: int, M: int, K: int, N: int, group_size: int = 128,
     return {"x": np.ascontiguousarray(x), "qweight": np.ascontiguousarray(qweight),
             "qzeros": np.ascontiguousarray(qzeros), "scales": np.ascontiguousarray(scales),
             "bias": b, "group_size": int(group_size), "M": M, "K": K, "N": N}
+
+
+# Workloads shaped like the 7B / 70B linears the pages discuss.  Each entry:
+# (config index, shape index, name, M, K, N, group_size, bias).  Shapes only; seeds
+# come from seed_for(config, shape).
+_L7 = [(4096, 4096), (4096, 11008), (11008, 4096)]
+_L70 = [(8192, 8192), (8192, 28672), (28672, 8192)]
+
+
+def _workloads():
+    out = [(0, 0, "tiny_m1_256x256", 1, 256, 256, 128, False)]
+    si = 0
+    for K, N in _L7:
+        for b in (False, True):
+            out.append((1, si, f"7b_decode_m1_{K}x{N}{'_bias' if b else ''}", 1, K, N, 128, b))
+            si += 1
+    si = 0
+    for M in (4, 8, 16, 32):
+        for K, N in _L7:
+            out.append((2, si, f"7b_smallbatch_m{M}_{K}x{N}", M, K, N, 128, False))
+            si += 1
+    for K, N in _L7:
+        out.append((2, si, f"7b_smallbatch_m8_{K}x{N}_g-1", 8, K, N, -1, False))
+        si += 1
+    si = 0
+    for M in (512, 2048):
+        for K, N in [(4096, 11008), (11008, 4096)]:
+            out.append((3, si, f"7b_prefill_m{M}_{K}x{N}", M, K, N, 128, False))
+            si += 1
+    si = 0
+    for M in (1, 16, 4096):
+        for K, N in _L70:
+            out.append((4, si, f"70b_m{M}_{K}x{N}", M, K, N, 128, True))
+            si += 1
+    return out
+
+
+WORKLOADS = _workloads()
+
+
+def workload(name: str):
+    for w in WORKLOADS:
+        if w[2] == name:
+            return w
+    raise KeyError(name)
+
+
+def workload_inputs(name: str) -> dict:
+    cfg, si, _, M, K, N, G, b = workload(name)
+    return awq_linear(seed_for(cfg, si), M, K, N, group_size=G, bias=b)

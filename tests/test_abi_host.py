@@ -1,0 +1,129 @@
+"""Host-only checks of the C ABI (no GPU needed): the library loads, exports every entry
+point include/awq.h declares, and rejects bad arguments on the host before touching a
+device.  No call here reaches a kernel launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "awq.h")
+
+INVALID, SHAPE, MISALIGNED, DEVICE = 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a16_weight_only_gb300 import build
+    build.build()
+    from w4a16_weight_only_gb300 import _binding
+    return _binding.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(awq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    for n in ("awq_gemm", "awq_dequant", "awq_runtime_available", "awq_last_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_header(lib):
+    from w4a16_weight_only_gb300 import _binding
+    assert set(_declared_functions()) == set(_binding.SIGNATURES)
+
+
+def test_status_strings(lib):
+    assert lib.awq_status_string(0) == b"AWQ_OK"
+    assert lib.awq_status_string(6) == b"AWQ_ERR_TIMEOUT"
+
+
+P = ctypes.c_void_p
+A = P(0x100000)        # fake, 256-byte aligned "device" addresses: never dereferenced
+B = P(0x200000)
+ODD = P(0x100001)
+
+
+def gemm(lib, M=1, K=256, N=256, G=128, x=A, qw=A, qz=A, sc=A, bias=None, y=B, path=0):
+    return lib.awq_gemm_ex(x, qw, qz, sc, bias, M, K, N, G, y, path, None)
+
+
+def test_gemm_shape_validation(lib):
+    assert gemm(lib, K=0) == INVALID
+    assert gemm(lib, K=-16) == INVALID
+    assert gemm(lib, N=-8) == INVALID
+    assert gemm(lib, M=-1) == INVALID
+    assert gemm(lib, G=0) == INVALID
+    assert gemm(lib, G=-2) == INVALID
+    assert gemm(lib, N=12) == SHAPE            # not a multiple of 8
+    assert gemm(lib, K=256, G=96) == SHAPE     # K % G != 0
+    assert gemm(lib, K=1 << 31) == SHAPE       # size limit
+    assert gemm(lib, path=7) == INVALID
+    msg = lib.awq_last_error().decode()
+    assert "path" in msg
+
+
+def test_gemm_empty_is_ok_without_device(lib):
+    # M == 0 or N == 0: nothing to compute, no launch, even with null pointers.
+    assert lib.awq_gemm(None, None, None, None, None, 0, 256, 256, 128, None, None) == 0
+    assert lib.awq_gemm(None, None, None, None, None, 4, 256, 0, 128, None, None) == 0
+    assert lib.awq_last_error() == b""
+
+
+def test_gemm_null_and_alignment(lib):
+    assert gemm(lib, x=None) == INVALID
+    assert gemm(lib, y=None) == INVALID
+    assert gemm(lib, qz=None) == INVALID
+    assert gemm(lib, x=ODD) == MISALIGNED
+    assert gemm(lib, sc=ODD) == MISALIGNED
+    assert gemm(lib, bias=ODD) == MISALIGNED
+    assert gemm(lib, qw=P(0x100002)) == MISALIGNED
+
+
+def test_dequant_validation(lib):
+    d = lib.awq_dequant
+    assert d(A, A, A, 0, 256, 128, B, 0, None) == INVALID
+    assert d(A, A, A, 256, 20, 128, B, 0, None) == SHAPE
+    assert d(A, A, A, 256, 256, 100, B, 0, None) == SHAPE
+    assert d(A, A, A, 256, 256, 128, B, 5, None) == INVALID        # bad dtype
+    assert d(A, A, A, 256, 256, 128, P(0x100002), 1, None) == MISALIGNED  # f32 out
+    assert d(A, A, A, 256, 0, 128, B, 0, None) == 0                 # N == 0: no launch
+    assert d(None, A, A, 256, 256, 128, B, 0, None) == INVALID
+
+
+def test_path_selection_is_host_only(lib):
+    sel = lib.awq_gemm_select_path
+    # decode shapes
+    assert sel(1, 4096, 4096, 128, A, A, A, A, None, B) == 1
+    assert sel(32, 11008, 4096, 128, A, A, A, A, None, B) == 1
+    # K not a multiple of 16 -> generic kernel
+    assert sel(1, 200, 64, 8, A, A, A, A, None, B) == 3
+    # group size not a multiple of 16 -> generic kernel
+    assert sel(4, 256, 64, 8, A, A, A, A, None, B) == 3
+    # invalid shape -> 0
+    assert sel(1, 256, 12, 128, A, A, A, A, None, B) == 0
+
+
+def test_valid_call_without_sm103_device_is_refused(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present; covered by the GPU tests")
+    assert gemm(lib) == DEVICE
+    assert lib.awq_runtime_available() == 0
+    assert lib.awq_last_error() != b""
+
+
+def test_binding_raises_loudly_without_library(tmp_path):
+    from w4a16_weight_only_gb300 import _binding
+    with pytest.raises(RuntimeError, match="missing"):
+        _binding.load_library(str(tmp_path / "nope.so"))

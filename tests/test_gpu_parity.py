@@ -1,0 +1,181 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same
+seeded inputs.  awq_dequant must be bit-exact; awq_gemm must satisfy
+|y - y_ref| <= 1e-2 * max(1, |y_ref|) elementwise (y fp16 with fp32 accumulation,
+y_ref fp64), and bit-exact on inputs where every partial sum is exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def awq():
+    from w4a16_weight_only_gb300 import build
+    build.build()
+    import w4a16_weight_only_gb300 as awq
+    assert awq.runtime_available(), awq.last_error()
+    return awq
+
+
+def to_dev(d):
+    t = {k: torch.from_numpy(np.ascontiguousarray(d[k])).cuda()
+         for k in ("x", "qweight", "qzeros", "scales")}
+    t["bias"] = None if d["bias"] is None else torch.from_numpy(d["bias"]).cuda()
+    return t
+
+
+def run_gemm(awq, d, path="auto", t=None):
+    t = t or to_dev(d)
+    y = awq.awq_gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], t["bias"],
+                     group_size=d["group_size"], path=path)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def assert_close(y, y_ref, what):
+    ok, worst = oracle.within_tolerance(y.astype(np.float64), y_ref, REL_TOL)
+    assert ok, f"{what}: worst |err|/(1e-2*max(1,|ref|)) = {worst:.3f}"
+
+
+def decode_ok(K, G):
+    G = K if G == -1 else G
+    return K % 16 == 0 and G % 16 == 0
+
+
+# ------------------------------------------------------------------ dequant ----
+
+@pytest.mark.parametrize("K,N,G", [(256, 256, 128), (48, 24, 16), (96, 40, 32), (4096, 4096, 128),
+                                   (11008, 4096, -1), (64, 8, 8), (136, 1032, 8)])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32])
+def test_dequant_bit_exact(awq, K, N, G, dtype):
+    d = synth.awq_linear(7000 + K + N, 1, K, N, group_size=G)
+    t = to_dev(d)
+    w = awq.awq_dequant(t["qweight"], t["qzeros"], t["scales"], group_size=G, out_dtype=dtype)
+    torch.cuda.synchronize()
+    ref = (oracle.dequant_f16 if dtype == torch.float16 else oracle.dequant_f32)(
+        d["qweight"], d["qzeros"], d["scales"], G)
+    got = w.cpu().numpy()
+    assert got.shape == (K, N)
+    assert np.array_equal(got.view(np.uint16 if dtype == torch.float16 else np.uint32),
+                          ref.view(np.uint16 if dtype == torch.float16 else np.uint32))
+
+
+def test_dequant_unaligned_output_uses_scalar_path(awq):
+    d = synth.awq_linear(7100, 1, 64, 32, group_size=32)
+    t = to_dev(d)
+    buf = torch.empty(64 * 32 + 1, dtype=torch.float16, device="cuda")
+    out = buf[1:].view(64, 32)      # 2-byte aligned, not 16-byte aligned
+    awq.awq_dequant(t["qweight"], t["qzeros"], t["scales"], group_size=32, out=out)
+    torch.cuda.synchronize()
+    ref = oracle.dequant_f16(d["qweight"], d["qzeros"], d["scales"], 32)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), ref.view(np.uint16))
+
+
+# ---------------------------------------------------- GEMM, small and ragged ----
+
+SMALL = [(1, 256, 256, 128, False), (3, 512, 192, 64, True), (8, 1024, 520, 32, True),
+         (13, 768, 264, 128, False), (17, 2048, 1032, 256, True), (32, 4096, 128, -1, False),
+         (33, 256, 64, 16, True), (100, 512, 136, 64, False), (5, 200, 64, 8, True),
+         (2, 48, 8, 16, False), (64, 1024, 2048, 128, True)]
+
+
+@pytest.mark.parametrize("M,K,N,G,bias", SMALL)
+@pytest.mark.parametrize("path", ["auto", "decode", "generic"])
+def test_gemm_small_vs_oracle(awq, M, K, N, G, bias, path):
+    if path == "decode" and not decode_ok(K, G):
+        pytest.skip("shape outside the decode kernel's contract")
+    d = synth.awq_linear(8000 + M + K + N, M, K, N, group_size=G, bias=bias)
+    y = run_gemm(awq, d, path)
+    y_ref = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    assert_close(y, y_ref, f"{path} M={M} K={K} N={N} G={G}")
+
+
+@pytest.mark.parametrize("M", [1, 5, 8, 12, 16, 30, 32, 40])
+@pytest.mark.parametrize("path", ["decode", "generic"])
+def test_gemm_exact_case_bitwise(awq, M, path):
+    """Small-integer x, power-of-two scales, dyadic bias: every product and partial sum
+    is exact in fp32, so y must equal the fp16 rounding of the exact result bit for bit
+    whatever the summation order."""
+    d = synth.awq_linear(9000 + M, M, 2048, 384, group_size=128, bias=True, x_kind="smallint",
+                         scale_kind="pow2", bias_kind="dyadic")
+    y = run_gemm(awq, d, path)
+    y_ref = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128)
+    assert np.array_equal(y.view(np.uint16), y_ref.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [1, 16, 32, 96])
+def test_gemm_deterministic(awq, M):
+    d = synth.awq_linear(9100 + M, M, 4096, 1024, group_size=128, bias=True)
+    t = to_dev(d)
+    a = run_gemm(awq, d, t=t)
+    b = run_gemm(awq, d, t=t)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_gemm_symmetric_checkpoint(awq):
+    d = synth.awq_linear(9200, 4, 1024, 512, group_size=64, sym=True)
+    y = run_gemm(awq, d)
+    assert_close(y, oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 64), "sym")
+
+
+def test_gemm_empty_batch(awq):
+    d = synth.awq_linear(9300, 0, 256, 64, group_size=128)
+    t = to_dev(d)
+    y = awq.awq_gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], None, group_size=128)
+    assert tuple(y.shape) == (0, 64)
+
+
+def test_gemm_leading_dims_flattened(awq):
+    d = synth.awq_linear(9400, 6, 256, 64, group_size=128)
+    t = to_dev(d)
+    y = awq.awq_gemm(t["x"].view(2, 3, 256), t["qweight"], t["qzeros"], t["scales"], None,
+                     group_size=128)
+    torch.cuda.synchronize()
+    assert tuple(y.shape) == (2, 3, 64)
+    assert_close(y.cpu().numpy().reshape(6, 64),
+                 oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 128), "3d")
+
+
+def test_binding_rejects_wrong_dtype_and_layout(awq):
+    d = synth.awq_linear(9500, 2, 256, 64, group_size=128)
+    t = to_dev(d)
+    with pytest.raises(TypeError):
+        awq.awq_gemm(t["x"].float(), t["qweight"], t["qzeros"], t["scales"], None, group_size=128)
+    with pytest.raises(ValueError):
+        awq.awq_gemm(t["x"], t["qweight"], t["qzeros"], t["scales"][:, :32], None, group_size=128)
+    with pytest.raises(ValueError):
+        xt = torch.empty(256, 2, dtype=torch.float16, device="cuda").t()
+        awq.awq_gemm(xt, t["qweight"], t["qzeros"], t["scales"], None, group_size=128)
+
+
+def test_device_status_clean(awq):
+    awq.device_status()
+
+
+# --------------------------------------------- every workload at full size ----
+
+def _sample(M, N, rng, n=2048):
+    rows = np.concatenate([rng.integers(0, M, n), np.zeros(256, np.int64), np.full(256, M - 1)])
+    cols = np.concatenate([rng.integers(0, N, n), rng.integers(0, N, 512)])
+    return rows, cols
+
+
+@pytest.mark.parametrize("name", [w[2] for w in synth.WORKLOADS])
+def test_workload_parity(awq, name):
+    d = synth.workload_inputs(name)
+    M, K, N, G = d["M"], d["K"], d["N"], d["group_size"]
+    y = run_gemm(awq, d)
+    args = (d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    if M * K * N <= 32 * 4096 * 11008 and K * N <= 64 * 1024 * 1024:
+        assert_close(y, oracle.gemm(*args), name)
+    else:
+        rng = np.random.default_rng(1)
+        rows, cols = _sample(M, N, rng)
+        assert_close(y[rows, cols], oracle.gemm_sampled(*args, rows, cols), name)
+    assert np.all(np.isfinite(y.astype(np.float32)))

@@ -1,0 +1,11 @@
+"""AWQ W4A16 weight-only linear for GB300 (sm_103a).
+
+The computation lives in ``libawq_gb300.so`` (C ABI in ``include/awq.h``, CUDA sources
+in ``csrc/``).  This package only builds it (``build.py``) and marshals arguments
+(``_binding.py``); PyTorch supplies device memory and streams.
+"""
+from ._binding import (AwqError, PATHS, awq_dequant, awq_gemm, device_status, last_error,
+                       load_library, runtime_available, select_path)
+
+__all__ = ["AwqError", "PATHS", "awq_dequant", "awq_gemm", "device_status", "last_error",
+           "load_library", "runtime_available", "select_path"]

@@ -1,0 +1,170 @@
+"""ctypes binding over libawq_gb300.so (include/awq.h).  Argument marshalling only:
+every step of the computation runs in the library's CUDA kernels.  There is no CPU or
+PyTorch fallback: if the library is missing or the device is not sm_103a, calls raise."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libawq_gb300.so")
+
+AWQ_OK = 0
+STATUS_NAMES = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARGUMENT", 2: "AWQ_ERR_UNSUPPORTED_SHAPE",
+                3: "AWQ_ERR_MISALIGNED", 4: "AWQ_ERR_UNSUPPORTED_DEVICE", 5: "AWQ_ERR_CUDA",
+                6: "AWQ_ERR_TIMEOUT"}
+PATHS = {"auto": 0, "decode": 1, "prefill": 2, "generic": 3}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+DTYPE_F16, DTYPE_F32 = 0, 1
+
+# Every entry point of include/awq.h: name -> (restype, argtypes)
+_i64, _vp, _i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+SIGNATURES = {
+    "awq_runtime_available": (_i32, []),
+    "awq_last_error": (ctypes.c_char_p, []),
+    "awq_status_string": (ctypes.c_char_p, [_i32]),
+    "awq_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "awq_gemm": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "awq_gemm_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "awq_gemm_select_path": (_i32, [_i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "awq_device_status": (_i32, [_vp]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class AwqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libawq_gb300.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build it first (python -m w4a16_weight_only_gb300.build or "
+                "__graft_entry__.build()); there is no fallback implementation")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load_library().awq_last_error().decode()
+
+
+def runtime_available() -> bool:
+    return bool(load_library().awq_runtime_available())
+
+
+def _check(status: int):
+    if status != AWQ_OK:
+        raise AwqError(status, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, name, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major)")
+    if t.numel() and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _groups(K, group_size):
+    G = K if group_size == -1 else group_size
+    return K // G if (G > 0 and K % G == 0) else 1
+
+
+def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, path="auto",
+             stream=None):
+    """y = x @ dequant(qweight, qzeros, scales) (+ bias) via the library's awq_gemm.
+
+    x fp16 [M, K] (leading dims are flattened), qweight int32 [K, N/8], qzeros int32
+    [K/G, N/8], scales fp16 [K/G, N], bias fp16 [N] or None.  Returns fp16 [..., N].
+    """
+    lib = load_library()
+    lead = x.shape[:-1]
+    K = x.shape[-1]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    N = qweight.shape[1] * 8
+    dev = x.device
+    _need(x2, "x", torch.float16, (M, K), dev)
+    _need(qweight, "qweight", torch.int32, (K, N // 8), dev)
+    ng = _groups(K, group_size)
+    _need(qzeros, "qzeros", torch.int32, (ng, N // 8), dev)
+    _need(scales, "scales", torch.float16, (ng, N), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.float16, (N,), dev)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    else:
+        _need(out, "out", torch.float16, (M, N), dev)
+    st = lib.awq_gemm_ex(_ptr(x2), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
+                         M, K, N, group_size, _ptr(out), PATHS[path], _stream(stream))
+    _check(st)
+    return out.reshape(*lead, N)
+
+
+def awq_dequant(qweight, qzeros, scales, group_size=128, out_dtype=torch.float16, out=None,
+                stream=None):
+    """Dense W [K, N] = (code - zero) * scale via the library's awq_dequant."""
+    lib = load_library()
+    K, C = qweight.shape
+    N = 8 * C
+    dev = qweight.device
+    _need(qweight, "qweight", torch.int32, (K, C), dev)
+    ng = _groups(K, group_size)
+    _need(qzeros, "qzeros", torch.int32, (ng, C), dev)
+    _need(scales, "scales", torch.float16, (ng, N), dev)
+    if out_dtype not in (torch.float16, torch.float32):
+        raise TypeError("out_dtype must be torch.float16 or torch.float32")
+    if out is None:
+        out = torch.empty((K, N), dtype=out_dtype, device=dev)
+    else:
+        _need(out, "out", out_dtype, (K, N), dev)
+    st = lib.awq_dequant(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size, _ptr(out),
+                         DTYPE_F32 if out_dtype == torch.float32 else DTYPE_F16, _stream(stream))
+    _check(st)
+    return out
+
+
+def select_path(x, qweight, qzeros, scales, bias=None, group_size=128, out=None) -> str:
+    lib = load_library()
+    M, K = x.reshape(-1, x.shape[-1]).shape
+    N = qweight.shape[1] * 8
+    r = lib.awq_gemm_select_path(M, K, N, group_size, _ptr(x), _ptr(qweight), _ptr(qzeros),
+                                 _ptr(scales), _ptr(bias), _ptr(out) if out is not None else _ptr(x))
+    return PATH_NAMES.get(r, "auto")
+
+
+def device_status(stream=None):
+    _check(load_library().awq_device_status(_stream(stream)))

@@ -1,0 +1,241 @@
+// C ABI of libawq_gb300.so (declared in include/awq.h): host-side validation, error
+// reporting and kernel-family dispatch.  All argument checks run on the host before any
+// CUDA call, so an invalid call touches no device.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/awq.h"
+#include "awq_internal.cuh"
+
+namespace {
+
+thread_local std::string g_err;
+
+awq_status_t fail(awq_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+awq_status_t ok() {
+  g_err.clear();
+  return AWQ_OK;
+}
+
+awq_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(AWQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int64_t kDimLimit = (int64_t{1} << 31) - 1;
+constexpr int64_t kProdLimit = int64_t{1} << 40;
+
+// Shape rules shared by awq_dequant and awq_gemm.  Returns AWQ_OK and the resolved G.
+awq_status_t check_weight_shape(int64_t K, int64_t N, int64_t group_size, int* G_out) {
+  if (K <= 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "K must be positive (got %lld)", (long long)K);
+  if (N < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "N must be >= 0 (got %lld)", (long long)N);
+  if (group_size == 0 || group_size < -1)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "group_size must be -1 or positive (got %lld)",
+                (long long)group_size);
+  if (K > kDimLimit || N > kDimLimit)
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "K and N must be below 2^31");
+  if (K * N >= kProdLimit) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "K*N must be below 2^40");
+  if (N % 8 != 0)
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE,
+                "N=%lld is not a multiple of 8 (eight 4-bit codes per int32 word)", (long long)N);
+  const int64_t G = group_size == -1 ? K : group_size;
+  if (K % G != 0)
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "K=%lld is not a multiple of group_size=%lld",
+                (long long)K, (long long)G);
+  *G_out = static_cast<int>(G);
+  return AWQ_OK;
+}
+
+// Current device must be compute capability 10.3 (the only code this library carries).
+awq_status_t check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(AWQ_ERR_UNSUPPORTED_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+  int major = 0, minor = 0;
+  e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(AWQ_ERR_UNSUPPORTED_DEVICE,
+                "device %d is compute capability %d.%d; this library is built for 10.3 (sm_103a)",
+                dev, major, minor);
+  return AWQ_OK;
+}
+
+bool al(const void* p, uintptr_t a) { return awq::aligned(p, a); }
+
+awq_status_t build_problem(const void* x, const int32_t* qweight, const int32_t* qzeros,
+                           const void* scales, const void* bias, int64_t M, int64_t K, int64_t N,
+                           int64_t group_size, void* y, awq_stream_t stream, awq::GemmProblem* p,
+                           bool* empty) {
+  if (M < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "M must be >= 0 (got %lld)", (long long)M);
+  int G = 0;
+  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  if (st != AWQ_OK) return st;
+  if (M > kDimLimit) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "M must be below 2^31");
+  if (M * N >= kProdLimit || M * K >= kProdLimit)
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "M*N and M*K must be below 2^40");
+  *empty = (M == 0 || N == 0);
+  if (*empty) return AWQ_OK;
+  if (!x || !qweight || !qzeros || !scales || !y)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "null pointer among x, qweight, qzeros, scales, y");
+  if (!al(x, 2) || !al(scales, 2) || !al(y, 2) || (bias && !al(bias, 2)))
+    return fail(AWQ_ERR_MISALIGNED, "fp16 tensors must be 2-byte aligned");
+  if (!al(qweight, 4) || !al(qzeros, 4))
+    return fail(AWQ_ERR_MISALIGNED, "qweight and qzeros must be 4-byte aligned");
+  p->x = static_cast<const __half*>(x);
+  p->qw = reinterpret_cast<const uint32_t*>(qweight);
+  p->qz = reinterpret_cast<const uint32_t*>(qzeros);
+  p->sc = static_cast<const __half*>(scales);
+  p->bias = static_cast<const __half*>(bias);
+  p->y = static_cast<__half*>(y);
+  p->M = static_cast<int>(M);
+  p->K = static_cast<int>(K);
+  p->N = static_cast<int>(N);
+  p->G = G;
+  p->stream = reinterpret_cast<cudaStream_t>(stream);
+  return AWQ_OK;
+}
+
+awq::Path choose_path(const awq::GemmProblem& p) {
+  if (p.M <= 32 && awq::decode_supported(p, nullptr)) return awq::kDecode;
+  if (awq::prefill_supported(p, nullptr)) return awq::kPrefill;
+  if (awq::decode_supported(p, nullptr)) return awq::kDecode;
+  return awq::kGeneric;
+}
+
+awq_status_t run(const awq::GemmProblem& p, awq::Path path) {
+  const char* why = "";
+  cudaError_t e = cudaSuccess;
+  switch (path) {
+    case awq::kDecode:
+      if (!awq::decode_supported(p, &why)) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "decode path: %s", why);
+      e = awq::launch_decode(p);
+      break;
+    case awq::kPrefill:
+      if (!awq::prefill_supported(p, &why)) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "prefill path: %s", why);
+      e = awq::launch_prefill(p);
+      break;
+    case awq::kGeneric:
+      e = awq::launch_generic(p);
+      break;
+    default:
+      return fail(AWQ_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int awq_runtime_available(void) {
+  if (check_device() != AWQ_OK) return 0;
+  cudaFuncAttributes attr;
+  const cudaError_t e = awq::probe_kernel_image(&attr);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "loading sm_103a kernels");
+    return 0;
+  }
+  ok();
+  return 1;
+}
+
+const char* awq_last_error(void) { return g_err.c_str(); }
+
+const char* awq_status_string(awq_status_t s) {
+  switch (s) {
+    case AWQ_OK: return "AWQ_OK";
+    case AWQ_ERR_INVALID_ARGUMENT: return "AWQ_ERR_INVALID_ARGUMENT";
+    case AWQ_ERR_UNSUPPORTED_SHAPE: return "AWQ_ERR_UNSUPPORTED_SHAPE";
+    case AWQ_ERR_MISALIGNED: return "AWQ_ERR_MISALIGNED";
+    case AWQ_ERR_UNSUPPORTED_DEVICE: return "AWQ_ERR_UNSUPPORTED_DEVICE";
+    case AWQ_ERR_CUDA: return "AWQ_ERR_CUDA";
+    case AWQ_ERR_TIMEOUT: return "AWQ_ERR_TIMEOUT";
+  }
+  return "AWQ_ERR_UNKNOWN";
+}
+
+awq_status_t awq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
+                         int64_t K, int64_t N, int64_t group_size, void* w_out,
+                         awq_dtype_t out_dtype, awq_stream_t stream) {
+  int G = 0;
+  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  if (st != AWQ_OK) return st;
+  if (out_dtype != AWQ_DTYPE_F16 && out_dtype != AWQ_DTYPE_F32)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "out_dtype must be AWQ_DTYPE_F16 or AWQ_DTYPE_F32");
+  if (N == 0) return ok();
+  if (!qweight || !qzeros || !scales_f16 || !w_out)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "null pointer among qweight, qzeros, scales, w_out");
+  if (!al(qweight, 4) || !al(qzeros, 4)) return fail(AWQ_ERR_MISALIGNED, "qweight/qzeros must be 4-byte aligned");
+  if (!al(scales_f16, 2)) return fail(AWQ_ERR_MISALIGNED, "scales must be 2-byte aligned");
+  if (!al(w_out, out_dtype == AWQ_DTYPE_F32 ? 4 : 2)) return fail(AWQ_ERR_MISALIGNED, "w_out misaligned for its dtype");
+  st = check_device();
+  if (st != AWQ_OK) return st;
+  const cudaError_t e = awq::launch_dequant(
+      reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
+      static_cast<const __half*>(scales_f16), static_cast<int>(K), static_cast<int>(N), G, w_out,
+      out_dtype == AWQ_DTYPE_F32, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "awq_dequant launch");
+  return ok();
+}
+
+awq_status_t awq_gemm_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                         const void* scales_f16, const void* bias_f16, int64_t M, int64_t K,
+                         int64_t N, int64_t group_size, void* y_f16, awq_path_t path,
+                         awq_stream_t stream) {
+  if (path < AWQ_PATH_AUTO || path > AWQ_PATH_GENERIC)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
+  awq::GemmProblem p{};
+  bool empty = false;
+  awq_status_t st = build_problem(x_f16, qweight, qzeros, scales_f16, bias_f16, M, K, N,
+                                  group_size, y_f16, stream, &p, &empty);
+  if (st != AWQ_OK) return st;
+  if (empty) return ok();
+  st = check_device();
+  if (st != AWQ_OK) return st;
+  const awq::Path use = path == AWQ_PATH_AUTO ? choose_path(p) : static_cast<awq::Path>(path);
+  return run(p, use);
+}
+
+awq_status_t awq_gemm(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                      const void* scales_f16, const void* bias_f16, int64_t M, int64_t K,
+                      int64_t N, int64_t group_size, void* y_f16, awq_stream_t stream) {
+  return awq_gemm_ex(x_f16, qweight, qzeros, scales_f16, bias_f16, M, K, N, group_size, y_f16,
+                     AWQ_PATH_AUTO, stream);
+}
+
+awq_path_t awq_gemm_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size,
+                                const void* x_f16, const int32_t* qweight,
+                                const int32_t* qzeros, const void* scales_f16,
+                                const void* bias_f16, const void* y_f16) {
+  awq::GemmProblem p{};
+  bool empty = false;
+  if (build_problem(x_f16, qweight, qzeros, scales_f16, bias_f16, M, K, N, group_size,
+                    const_cast<void*>(y_f16), nullptr, &p, &empty) != AWQ_OK || empty)
+    return AWQ_PATH_AUTO;
+  ok();
+  return static_cast<awq_path_t>(choose_path(p));
+}
+
+awq_status_t awq_device_status(awq_stream_t stream) {
+  awq_status_t st = check_device();
+  if (st != AWQ_OK) return st;
+  unsigned int v = 0u;
+  const cudaError_t e = awq::read_and_clear_status(reinterpret_cast<cudaStream_t>(stream), &v);
+  if (e != cudaSuccess) return cuda_fail(e, "reading device status");
+  if (v != 0u) return fail(AWQ_ERR_TIMEOUT, "a kernel gave up a bounded wait (code 0x%x)", v);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,154 @@
+// awq_dequant: full unpack + dequant of an AWQ GEMM-layout weight to a dense [K, N]
+// matrix, and the generic (any-shape) fused GEMM used for ragged shapes.
+//
+// Unpack and dequant follow tensref.org/formats/awq, "Reader": nibble i of packed word c
+// holds column 8c + ORDER[i]; w = (code - zero) * scale with the scale/zero row k / G and
+// no +1 on the zero (reject rule AWQ-005 on the same page).
+#include "awq_internal.cuh"
+
+namespace awq {
+namespace {
+
+// Each thread handles one packed word (8 output columns of one row) per iteration.
+// The fp32 value (code - zero) * scale is exact (a 5-bit integer times an 11-bit
+// significand); the fp16 output is that value rounded once to nearest even.
+template <bool kF32, bool kVec>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ qw,
+                                                      const uint32_t* __restrict__ qz,
+                                                      const __half* __restrict__ sc, int K, int C,
+                                                      int G, void* __restrict__ out) {
+  const long long total = (long long)K * C;
+  const long long N = 8LL * C;
+  for (long long w = blockIdx.x * (long long)blockDim.x + threadIdx.x; w < total;
+       w += (long long)gridDim.x * blockDim.x) {
+    const int k = (int)(w / C);
+    const int cw = (int)(w - (long long)k * C);
+    const int g = k / G;
+    const uint32_t q = __ldcs(qw + w);
+    const uint32_t z = __ldg(qz + (long long)g * C + cw);
+    const __half* srow = sc + (long long)g * N + 8LL * cw;
+    __half s[8];
+    if (kVec) {
+      *reinterpret_cast<uint4*>(s) = __ldg(reinterpret_cast<const uint4*>(srow));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[j] = srow[j];
+    }
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int code = (int)((q >> (4 * i)) & 0xFu);
+      const int zero = (int)((z >> (4 * i)) & 0xFu);
+      v[nibble_column(i)] = __fmul_rn((float)(code - zero), __half2float(s[nibble_column(i)]));
+    }
+    const long long o = (long long)k * N + 8LL * cw;
+    if (kF32) {
+      float* dst = static_cast<float*>(out) + o;
+      if (kVec) {
+        __stcs(reinterpret_cast<float4*>(dst), make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(reinterpret_cast<float4*>(dst) + 1, make_float4(v[4], v[5], v[6], v[7]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[j] = v[j];
+      }
+    } else {
+      __half* dst = static_cast<__half*>(out) + o;
+      __half h[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[j] = __float2half_rn(v[j]);
+      if (kVec) {
+        __stcs(reinterpret_cast<uint4*>(dst), *reinterpret_cast<uint4*>(h));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[j] = h[j];
+      }
+    }
+  }
+}
+
+// Generic fused GEMM: one thread per output column, kMT activation rows per block row,
+// activations staged through shared memory in kKT-wide slices.  fp32 accumulation in
+// increasing k order.  Used for shapes the fast kernels do not take (K or G not a
+// multiple of 16, N not a multiple of the decode tile, unaligned pointers).
+constexpr int kMT = 8;
+constexpr int kKT = 64;
+
+__global__ void __launch_bounds__(128) generic_gemm_kernel(GemmProblem p) {
+  __shared__ float xs[kMT][kKT];
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  const int C = p.N >> 3;
+  const bool active = n < p.N;
+  const int cw = n >> 3;
+  const int j = n & 7;
+  const int nib = ((j & 1) << 2) | (j >> 1);  // nibble holding column j (inverse of ORDER)
+  for (int m0 = blockIdx.y * kMT; m0 < p.M; m0 += gridDim.y * kMT) {
+  float acc[kMT];
+#pragma unroll
+  for (int m = 0; m < kMT; ++m) acc[m] = 0.f;
+  for (int k0 = 0; k0 < p.K; k0 += kKT) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kMT * kKT; e += blockDim.x) {
+      const int m = e / kKT, kk = e % kKT;
+      const int gm = m0 + m, gk = k0 + kk;
+      xs[m][kk] = (gm < p.M && gk < p.K) ? __half2float(p.x[(long long)gm * p.K + gk]) : 0.f;
+    }
+    __syncthreads();
+    if (active) {
+      const int kend = min(kKT, p.K - k0);
+      for (int kk = 0; kk < kend; ++kk) {
+        const int k = k0 + kk;
+        const int g = k / p.G;
+        const uint32_t q = p.qw[(long long)k * C + cw];
+        const uint32_t z = p.qz[(long long)g * C + cw];
+        const int code = (int)((q >> (4 * nib)) & 0xFu);
+        const int zero = (int)((z >> (4 * nib)) & 0xFu);
+        const float w = __fmul_rn((float)(code - zero), __half2float(p.sc[(long long)g * p.N + n]));
+#pragma unroll
+        for (int m = 0; m < kMT; ++m) acc[m] = __fmaf_rn(xs[m][kk], w, acc[m]);
+      }
+    }
+  }
+  if (active) {
+    const float b = p.bias ? __half2float(p.bias[n]) : 0.f;
+#pragma unroll
+    for (int m = 0; m < kMT; ++m) {
+      const int gm = m0 + m;
+      if (gm < p.M) p.y[(long long)gm * p.N + n] = __float2half_rn(acc[m] + b);
+    }
+  }
+  }  // m0
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
+                           int G, void* out, bool out_f32, cudaStream_t stream) {
+  const int C = N / 8;
+  const long long total = (long long)K * C;
+  if (total == 0) return cudaSuccess;
+  const bool vec = aligned(sc, 16) && aligned(out, out_f32 ? 16 : 16);
+  int blocks = (int)((total + 255) / 256);
+  const int cap = 152 * 16;
+  if (blocks > cap) blocks = cap;
+  if (out_f32) {
+    if (vec) dequant_kernel<true, true><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+    else dequant_kernel<true, false><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+  } else {
+    if (vec) dequant_kernel<false, true><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+    else dequant_kernel<false, false><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t probe_kernel_image(cudaFuncAttributes* attr) {
+  return cudaFuncGetAttributes(attr, dequant_kernel<false, true>);
+}
+
+cudaError_t launch_generic(const GemmProblem& p) {
+  const int mtiles = (p.M + kMT - 1) / kMT;
+  dim3 grid((p.N + 127) / 128, mtiles < 65535 ? mtiles : 65535);
+  generic_gemm_kernel<<<grid, 128, 0, p.stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace awq
