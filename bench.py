@@ -359,6 +359,26 @@ def run_ours(args, rank, world, local):
     return line if rank == 0 else None
 
 
+def run_case(args, local):
+    """Profiling driver: one workload linear, --steps eager awq_gemm calls after --warmup
+    calls, nothing else on the GPU (for ncu launch lists and captures)."""
+    import torch
+    from w4a16_weight_only_gb300 import build as _build
+    _build.build()
+    import w4a16_weight_only_gb300 as awq
+    torch.cuda.set_device(local)
+    d = synth.workload_inputs(args.case)
+    t = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "qweight", "qzeros", "scales")}
+    b = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
+    y = torch.empty((d["M"], d["N"]), dtype=torch.float16, device="cuda")
+    for i in range(args.warmup + args.steps):
+        awq.awq_gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], b, group_size=d["group_size"],
+                     out=y, path=args.path)
+    torch.cuda.synchronize()
+    awq.device_status()
+    print(json.dumps({"case": args.case, "path": args.path, "launches": args.warmup + args.steps}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -366,8 +386,14 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="profiling mode: run only this workload linear (see synth.WORKLOADS)")
+    ap.add_argument("--path", default="auto", choices=["auto", "decode", "prefill", "generic"])
     args = ap.parse_args(argv)
     rank, world, local = dist_setup(args)
+    if args.case:
+        run_case(args, local)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
     else:

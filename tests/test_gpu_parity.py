@@ -82,7 +82,10 @@ def test_dequant_unaligned_output_uses_scalar_path(awq):
 SMALL = [(1, 256, 256, 128, False), (3, 512, 192, 64, True), (8, 1024, 520, 32, True),
          (13, 768, 264, 128, False), (17, 2048, 1032, 256, True), (32, 4096, 128, -1, False),
          (33, 256, 64, 16, True), (100, 512, 136, 64, False), (5, 200, 64, 8, True),
-         (2, 48, 8, 16, False), (64, 1024, 2048, 128, True)]
+         (2, 48, 8, 16, False), (64, 1024, 2048, 128, True),
+         # TMA decode: ragged column tile, 16- and 32-token tiles, two 32-token tiles, K = 64
+         (9, 1024, 160, 128, True), (24, 2048, 96, 64, False), (40, 4096, 4096, 128, True),
+         (1, 64, 32, -1, False), (7, 192, 32, 64, True), (16, 8192, 544, 256, True)]
 
 
 @pytest.mark.parametrize("M,K,N,G,bias", SMALL)

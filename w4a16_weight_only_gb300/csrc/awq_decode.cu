@@ -437,7 +437,7 @@ bool make_plan(const GemmProblem& p, Plan* plan, const char** why) {
 
 }  // namespace
 
-bool decode_supported(const GemmProblem& p, const char** why) {
+bool decode_ldg_supported(const GemmProblem& p, const char** why) {
   static const char* dummy;
   if (!why) why = &dummy;
   if (p.K % 16 != 0) { *why = "decode needs K % 16 == 0"; return false; }
@@ -450,7 +450,7 @@ bool decode_supported(const GemmProblem& p, const char** why) {
   return make_plan(p, &plan, why);
 }
 
-cudaError_t launch_decode(const GemmProblem& p) {
+cudaError_t launch_decode_ldg(const GemmProblem& p) {
   Plan plan;
   const char* why = nullptr;
   if (!make_plan(p, &plan, &why)) return cudaErrorInvalidValue;
@@ -463,6 +463,16 @@ cudaError_t launch_decode(const GemmProblem& p) {
   if (v.TB == 1 && v.CWL == 1) return launch_variant<1, 1, true>(dp, plan.grid, plan.cs, plan.smem, p.stream);
   if (v.TB == 2) return launch_variant<2, 1, true>(dp, plan.grid, plan.cs, plan.smem, p.stream);
   return launch_variant<4, 1, false>(dp, plan.grid, plan.cs, plan.smem, p.stream);
+}
+
+bool decode_supported(const GemmProblem& p, const char** why) {
+  if (decode_tma_supported(p, nullptr)) return true;
+  return decode_ldg_supported(p, why);
+}
+
+cudaError_t launch_decode(const GemmProblem& p) {
+  if (decode_tma_supported(p, nullptr)) return launch_decode_tma(p);
+  return launch_decode_ldg(p);
 }
 
 }  // namespace awq

@@ -2,6 +2,7 @@
 // Nothing here is part of the public C ABI (include/awq.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -30,9 +31,24 @@ cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const __half*
 // Any valid shape / alignment.
 cudaError_t launch_generic(const GemmProblem& p);
 
-// Split-K tensor-core streaming kernel.  decode_supported() is a pure host check.
+// Split-K tensor-core streaming kernels for small M.  decode_supported() is a pure host
+// check; launch_decode() uses the TMA-fed kernel when it takes the shape, else the
+// register-streaming one.
 bool decode_supported(const GemmProblem& p, const char** why);
 cudaError_t launch_decode(const GemmProblem& p);
+bool decode_ldg_supported(const GemmProblem& p, const char** why);
+cudaError_t launch_decode_ldg(const GemmProblem& p);
+bool decode_tma_supported(const GemmProblem& p, const char** why);
+cudaError_t launch_decode_tma(const GemmProblem& p);
+
+// Row-major 2D tensor map: dim0 contiguous elements per row, dim1 rows.
+bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                  const void* base, uint64_t dim0, uint64_t dim1, uint32_t box0, uint32_t box1,
+                  CUtensorMapSwizzle swizzle, const char** why);
+
+// Device address of the status word on the current device (bounded waits that give up
+// OR a code into it).
+cudaError_t status_word_ptr(unsigned int** ptr);
 
 // tcgen05/TMEM kernel for large M.
 bool prefill_supported(const GemmProblem& p, const char** why);

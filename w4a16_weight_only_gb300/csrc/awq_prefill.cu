@@ -14,6 +14,23 @@ bool prefill_supported(const GemmProblem&, const char** why) {
 
 cudaError_t launch_prefill(const GemmProblem&) { return cudaErrorNotSupported; }
 
+cudaError_t status_word_ptr(unsigned int** ptr) {
+  static unsigned int* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cache[dev]) {
+    *ptr = cache[dev];
+    return cudaSuccess;
+  }
+  void* a = nullptr;
+  e = cudaGetSymbolAddress(&a, g_status_word);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev] = static_cast<unsigned int*>(a);
+  *ptr = static_cast<unsigned int*>(a);
+  return cudaSuccess;
+}
+
 cudaError_t read_and_clear_status(cudaStream_t stream, unsigned int* value) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return e;
