@@ -8,9 +8,10 @@
 // GB300 design.  Every warp owns a contiguous run of 64-row stages of one column tile and
 // streams it through its own two-slot shared-memory ring: lane 0 issues the bulk tensor
 // copies (packed weights, activations, the stage's zero and scale rows) on an mbarrier,
-// the warp waits with a bounded try-wait, computes, and refills the slot.  Weight and
-// activation tiles land 128-byte swizzled so the fragment reads below are bank-conflict
-// free.  No register or instruction is spent on address streams for the weights, and a
+// the warp waits with a bounded try-wait, computes, and refills the slot.  The activation
+// tile lands 128-byte swizzled; the weight tile is unswizzled and the row order of the
+// fragment reads (row parity swapped on odd lanes of a quad) spreads each read over all
+// 32 banks, so both need the minimum number of shared-memory wavefronts.  No register or instruction is spent on address streams for the weights, and a
 // CTA keeps 16 stages (64 KB of packed weights) in flight.
 //
 // Unpack without shifts: two rows (k, k+1) of one packed column are byte-permuted (prmt)
@@ -45,7 +46,7 @@ constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 constexpr unsigned int kStatusDecodeTimeout = 0x1u;
 
 struct __align__(64) TmaDecodeParams {
-  CUtensorMap tm_w;  // qweight [K][C] u32, box {CW_W, 64}, 128B swizzle
+  CUtensorMap tm_w;  // qweight [K][C] u32, box {CW_W, 64}, unswizzled
   CUtensorMap tm_x;  // x [M][K] f16, box {64, 8*TB}, 128B swizzle
   CUtensorMap tm_z;  // qzeros [K/G][C] u32, box {CW_W, 1}
   CUtensorMap tm_s;  // scales [K/G][N] f16, box {8*CW_W, 1}
@@ -152,6 +153,9 @@ __global__ void __launch_bounds__(kNW * 32, 2)
     }
     done = j + 1;
     const unsigned char* b = my_slots + slot * GE::SLOT;
+#ifdef AWQ_DECODE_DEBUG_DUMP
+    AWQ_DECODE_DEBUG_DUMP(b, GE::SLOT);
+#endif
     const uint32_t* Z = reinterpret_cast<const uint32_t*>(b + GE::Z_OFF);
     const uint4* S = reinterpret_cast<const uint4*>(b + GE::S_OFF);
 
@@ -187,39 +191,45 @@ __global__ void __launch_bounds__(kNW * 32, 2)
     }
 
     float accg[kFactor ? NMMA : 1][TB][4];
+    // prmt selectors: low (high) 16 bits of row 2q in the low half, of row 2q+1 in the high.
+    const uint32_t sel_lo = (q & 1) ? 0x1054u : 0x5410u;
+    const uint32_t sel_hi = (q & 1) ? 0x3276u : 0x7632u;
 #pragma unroll
     for (int ks = 0; ks < kRS / 16; ++ks) {
-      // Packed words: rows 16ks + 4q + r, column-words g8*CWL .. +CWL-1.
+      // Packed words of lane (g8, q), column-words g8*CWL .. +CWL-1, rows
+      //   r = 0, 1 -> 16ks + 2q + {0, 1},   r = 2, 3 -> 16ks + 2q + 8 + {0, 1},
+      // the row parity swapped for odd q so that, with 64-byte rows, the four q-lanes of a
+      // read cover both halves of the bank space (the prmt selectors undo the swap).
       uint32_t w[4][CWL];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const uint32_t off = swz128(static_cast<uint32_t>((16 * ks + 4 * q + r) * GE::CW_W * 4 +
-                                                          g8 * CWL * 4));
+        const int row = 16 * ks + 2 * q + ((r ^ q) & 1) + 8 * (r >> 1);
         if constexpr (CWL == 2) {
+          const uint32_t off = static_cast<uint32_t>(row * 64 + g8 * 8);
           const uint2 v = *reinterpret_cast<const uint2*>(b + off);
           w[r][0] = v.x;
           w[r][1] = v.y;
         } else {
+          const uint32_t off = static_cast<uint32_t>(row * 32 + g8 * 4);
           w[r][0] = *reinterpret_cast<const uint32_t*>(b + off);
         }
       }
-      // Activations: token 8tb + g8, k = 16ks + 4q .. +3.
+      // Activations: token 8tb + g8, k = 16ks + 2q + {0,1} and 16ks + 2q + 8 + {0,1}.
       uint32_t bx[TB][2];
 #pragma unroll
       for (int tb = 0; tb < TB; ++tb) {
-        const uint32_t off = swz128(static_cast<uint32_t>((8 * tb + g8) * (kRS * 2) + (16 * ks + 4 * q) * 2));
-        const uint2 v = *reinterpret_cast<const uint2*>(b + GE::X_OFF + off);
-        bx[tb][0] = v.x;
-        bx[tb][1] = v.y;
+        const uint32_t base = static_cast<uint32_t>((8 * tb + g8) * (kRS * 2) + (16 * ks + 2 * q) * 2);
+        bx[tb][0] = *reinterpret_cast<const uint32_t*>(b + GE::X_OFF + swz128(base));
+        bx[tb][1] = *reinterpret_cast<const uint32_t*>(b + GE::X_OFF + swz128(base + 16));
       }
-      // Half2 operands v[c][rp][i]: rows (4q+2rp, 4q+2rp+1), nibble i of column-word c.
+      // Half2 operands v[c][rp][i]: rows (2q + 8rp, 2q + 8rp + 1), nibble i of word c.
       uint32_t v[CWL][2][8];
 #pragma unroll
       for (int c = 0; c < CWL; ++c)
 #pragma unroll
         for (int rp = 0; rp < 2; ++rp) {
-          const uint32_t plo = prmt(w[2 * rp][c], w[2 * rp + 1][c], 0x5410u);
-          const uint32_t phi = prmt(w[2 * rp][c], w[2 * rp + 1][c], 0x7632u);
+          const uint32_t plo = prmt(w[2 * rp][c], w[2 * rp + 1][c], sel_lo);
+          const uint32_t phi = prmt(w[2 * rp][c], w[2 * rp + 1][c], sel_hi);
           const uint32_t plo8 = plo >> 8, phi8 = phi >> 8;
           uint32_t h[8];
           if (kFactor) {
@@ -251,6 +261,9 @@ __global__ void __launch_bounds__(kNW * 32, 2)
             v[c][rp][i] = d;
           }
         }
+#ifdef AWQ_DECODE_DEBUG_OPS
+      AWQ_DECODE_DEBUG_OPS(ks, bx, v, w);
+#endif
 #pragma unroll
       for (int mi = 0; mi < NMMA; ++mi) {
         const int ca = mma_cw<CWL>(mi, 0), ia = mma_nib<CWL>(mi, 0);
@@ -291,6 +304,9 @@ __global__ void __launch_bounds__(kNW * 32, 2)
           }
         }
     }
+#ifdef AWQ_DECODE_DEBUG_ACC
+    AWQ_DECODE_DEBUG_ACC(acc);
+#endif
     __syncwarp();
     if (lane == 0 && j + kSlots < j1) issue(slot, j + kSlots);
   }
@@ -371,7 +387,7 @@ cudaError_t launch_v(const GemmProblem& p, const Variant&) {
   const int C = p.N / 8;
   const int ngrp = p.K / p.G;
   if (!make_tmap_2d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, GE::CW_W, kRS,
-                    CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
+                    CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
       !make_tmap_2d(&dp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kRS, 8 * TB,
                     CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
       !make_tmap_2d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, GE::CW_W, 1,

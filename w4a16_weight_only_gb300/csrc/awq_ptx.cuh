@@ -157,6 +157,9 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
 // Byte offset inside a tile written by TMA with CU_TENSOR_MAP_SWIZZLE_128B (tile base
 // 1024-byte aligned): the 16-byte chunk index (bits 4-6) is XORed with bits 7-9.
 __device__ __forceinline__ uint32_t swz128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
+// Same for CU_TENSOR_MAP_SWIZZLE_64B (bits 4-5 ^= bits 7-8) and _32B (bit 4 ^= bit 7).
+__device__ __forceinline__ uint32_t swz64(uint32_t off) { return off ^ (((off >> 7) & 3u) << 4); }
+__device__ __forceinline__ uint32_t swz32(uint32_t off) { return off ^ (((off >> 7) & 1u) << 4); }
 
 }  // namespace ptx
 }  // namespace awq
