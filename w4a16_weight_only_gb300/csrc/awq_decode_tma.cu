@@ -5,29 +5,33 @@
 // (tensref.org/formats/awq, "Reader"; GPTQModel wiki "AWQ", "Native GEMM": fused
 // dequant-GEMM, fp32 accumulation, split over K.)
 //
-// GB300 design.  Every warp owns a contiguous run of 64-row stages of one column tile and
+// Streaming.  Every warp owns a contiguous run of 64-row stages of one column tile and
 // streams it through its own two-slot shared-memory ring: lane 0 issues the bulk tensor
-// copies (packed weights, activations, the stage's zero and scale rows) on an mbarrier,
-// the warp waits with a bounded try-wait, computes, and refills the slot.  The activation
-// tile lands 128-byte swizzled; the weight tile is unswizzled and the row order of the
-// fragment reads (row parity swapped on odd lanes of a quad) spreads each read over all
-// 32 banks, so both need the minimum number of shared-memory wavefronts.  No register or instruction is spent on address streams for the weights, and a
-// CTA keeps 16 stages (64 KB of packed weights) in flight.
+// copies (packed weights, the stage's zero and scale rows, the activations) on an
+// mbarrier, the warp waits with a bounded try-wait, computes, and refills the slot.  The
+// weight copies are issued before the kernel waits on the preceding grid (programmatic
+// dependent launch): only the activation copy and the output stores are ordered after
+// it, so the weight stream of one linear overlaps the tail of the previous kernel.
 //
-// Unpack without shifts: two rows (k, k+1) of one packed column are byte-permuted (prmt)
-// so each 16-bit half holds one row's four low (or high) nibbles; then one LOP3 with the
-// fp16 exponent pattern 0x6400 per nibble pair yields (1024 + c) (even nibbles, bits
-// 0-3) or (1024 + 16c) (odd nibbles, bits 4-7) for both rows, and one HSUB2 with the same
-// construction applied to the zero word gives exactly (c - z) or 16 (c - z).  Those half2
-// pairs are the A operand of m16n8k16 tensor-core MMAs (weights on the 16-row side,
-// activations on the 8-wide side).  With kFactor the MMA accumulates x * (c - z) over a
-// stage (one quantization group) and the scale (divided by 16 for odd nibbles, exact) is
-// applied once per output element per stage; without it the exact fp16 weight
-// (c - z) * scale is formed with HMUL2 first.
+// Unpack (kSub mode, up to 16 activation rows).  Two rows (k, k+1) of one packed column
+// are byte-permuted (prmt) so each 16-bit half holds one row's nibbles; one AND per
+// nibble pair leaves the code in the low mantissa bits of an fp16, i.e. the exact
+// subnormal value c * 2^-24 (even nibbles, bits 0-3) or c * 2^-20 (odd nibbles, bits
+// 4-7), for both rows at once.  Those half2 pairs are the A operand of m16n8k16
+// tensor-core MMAs (weights on the 16-row side, activations on the 8-wide side) that
+// accumulate sum_k x * c per quantization group in fp32 (tensor cores take fp16
+// subnormals exactly).  One more MMA with an all-ones A operand accumulates sum_k x.
+// When the group ends, each output element gets
+//     acc += scale * (2^24 (or 2^20) * sum x c  -  zero * sum x)
+// which is sum x (c - zero) * scale with no per-weight zero subtraction or scaling.
+// (kExact mode, 17..32 rows: the A operand is the exact fp16 weight (c - zero) * scale,
+// formed with the 0x6400 exponent trick, HSUB2 and HMUL2; accumulators go straight to
+// the output sums.)
 //
-// Split-K: warps of a CTA and CTAs of a thread-block cluster take consecutive K ranges;
-// partial sums are reduced in a fixed order through shared memory and distributed shared
-// memory (no global workspace, no atomics), so repeated calls are bitwise identical.
+// Split-K: the warps of a CTA and the CTAs of a thread-block cluster take consecutive K
+// ranges; partial sums are reduced in a fixed order through shared memory and then
+// distributed shared memory (no global workspace, no atomics), so repeated calls are
+// bitwise identical.
 #include <mutex>
 
 #include "awq_internal.cuh"
@@ -38,10 +42,12 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kNW = 8;        // warps per CTA
-constexpr int kSlots = 2;     // ring slots per warp
-constexpr int kRS = 64;       // rows of K per stage
-constexpr uint32_t kMagic = 0x64006400u;
+constexpr int kNW = 4;       // warps per CTA
+constexpr int kSlots = 2;    // ring slots per warp
+constexpr int kRS = 64;      // rows of K per stage
+constexpr int kMaxCluster = 16;
+constexpr uint32_t kMagic = 0x64006400u;     // fp16 1024 in both halves
+constexpr uint32_t kOnes = 0x3C003C00u;      // fp16 1.0 in both halves
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 constexpr unsigned int kStatusDecodeTimeout = 0x1u;
 
@@ -74,6 +80,8 @@ struct Geo {
   static_assert((size_t)kNW * E * 4 <= (size_t)kNW * kSlots * SLOT, "reduction buffer");
 };
 
+// Packed column-word (within the lane's CWL words) and nibble that feed A row g (rs = 0)
+// or g + 8 (rs = 1) of MMA mi.
 template <int CWL>
 __device__ __forceinline__ constexpr int mma_cw(int mi, int rs) {
   return CWL == 1 ? 0 : 2 * (mi >> 3) + rs;
@@ -83,8 +91,26 @@ __device__ __forceinline__ constexpr int mma_nib(int mi, int rs) {
   return CWL == 1 ? mi + 4 * rs : (mi & 7);
 }
 
-template <int TB, int CWL, bool kFactor>
-__global__ void __launch_bounds__(kNW * 32, 2)
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
+template <int TB, int CWL, bool kSub>
+__global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
     decode_tma_kernel(const __grid_constant__ TmaDecodeParams p) {
   using GE = Geo<TB, CWL>;
   constexpr int NMMA = GE::NMMA;
@@ -110,6 +136,7 @@ __global__ void __launch_bounds__(kNW * 32, 2)
 
   unsigned char* my_slots = smem + (size_t)warp * kSlots * GE::SLOT;
   uint64_t* my_bars = bars + warp * kSlots;
+  const uint32_t slots_u32 = smem_u32(my_slots);
 
   if (lane == 0) {
     prefetch_tmap(&p.tm_w);
@@ -119,20 +146,50 @@ __global__ void __launch_bounds__(kNW * 32, 2)
   }
   __syncwarp();
 
-  auto issue = [&](int slot, int j) {
+  auto issue_weights = [&](int slot, int j) {
     unsigned char* b = my_slots + slot * GE::SLOT;
     uint64_t* bar = &my_bars[slot];
     mbar_arrive_expect_tx(bar, GE::TX);
     const int grp = (j * kRS) / p.G;
     tma_load_2d(b, &p.tm_w, bar, cw0, j * kRS);
-    tma_load_2d(b + GE::X_OFF, &p.tm_x, bar, j * kRS, m0);
     tma_load_2d(b + GE::Z_OFF, &p.tm_z, bar, cw0, grp);
     tma_load_2d(b + GE::S_OFF, &p.tm_s, bar, 8 * cw0, grp);
   };
+  auto issue_x = [&](int slot, int j) {
+    tma_load_2d(my_slots + slot * GE::SLOT + GE::X_OFF, &p.tm_x, &my_bars[slot], j * kRS, m0);
+  };
 
-  if (lane == 0) {
-    for (int s = 0; s < kSlots && j0 + s < j1; ++s) issue(s, j0 + s);
-  }
+  // Weights do not depend on the preceding grid: stream them first.  Activations (and the
+  // output stores at the end) are ordered after it.
+  if (lane == 0)
+    for (int s = 0; s < kSlots && j0 + s < j1; ++s) issue_weights(s, j0 + s);
+  grid_dependency_wait();
+  if (lane == 0)
+    for (int s = 0; s < kSlots && j0 + s < j1; ++s) issue_x(s, j0 + s);
+  launch_dependents();
+
+  // Per-lane shared-memory offsets inside a slot.  Packed words of lane (g8, q):
+  // column-words g8*CWL .. +CWL-1, rows r = 0,1 -> 2q + {0,1} and r = 2,3 -> 2q + 8 + {0,1}
+  // (+16 per k16-step), the row parity swapped for odd q so the four q-lanes of a read
+  // cover both halves of the bank space; the prmt selectors undo the swap.
+  uint32_t w_off[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    w_off[r] = static_cast<uint32_t>((2 * q + ((r ^ q) & 1) + 8 * (r >> 1)) * GE::CW_W * 4 +
+                                     g8 * CWL * 4);
+  const uint32_t sel_lo = (q & 1) ? 0x1054u : 0x5410u;
+  const uint32_t sel_hi = (q & 1) ? 0x3276u : 0x7632u;
+  // ldmatrix row addresses for the activation tile (128-byte rows, 128B swizzle): lane l
+  // addresses row (l & 7) of 16-byte chunk 4*pair + (l >> 3).
+  uint32_t x_off[TB][2];
+#pragma unroll
+  for (int tb = 0; tb < TB; ++tb)
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const int rr = lane & 7;
+      const int chunk = 4 * pr + (lane >> 3);
+      x_off[tb][pr] = static_cast<uint32_t>(GE::X_OFF + (8 * tb + rr) * 128 + ((chunk ^ rr) << 4));
+    }
 
   float acc[NMMA][TB][4];
 #pragma unroll
@@ -141,6 +198,38 @@ __global__ void __launch_bounds__(kNW * 32, 2)
     for (int b = 0; b < TB; ++b)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[i][b][e] = 0.f;
+  float accg[kSub ? NMMA : 1][TB][4];
+  float xs[TB][4];
+  uint32_t zw[CWL];
+  uint32_t sv[CWL][4];
+  uint32_t zp[kSub ? 1 : CWL][8];
+  int cur = -1;
+
+  auto fold = [&]() {
+    // acc += scale * (2^24 or 2^20 * sum x c - zero * sum x) for the group just finished.
+#pragma unroll
+    for (int mi = 0; mi < NMMA; ++mi)
+#pragma unroll
+      for (int rs = 0; rs < 2; ++rs) {
+        const int c = mma_cw<CWL>(mi, rs);
+        const int nib = mma_nib<CWL>(mi, rs);
+        const int col = nibble_column(nib);
+        const uint32_t pr = sv[c][col >> 1];
+        const float s = __half2float(__ushort_as_half(
+            static_cast<unsigned short>((col & 1) ? (pr >> 16) : (pr & 0xFFFFu))));
+        const float zf =
+            __int_as_float(static_cast<int>(((zw[c] >> (4 * nib)) & 0xFu) | 0x4B000000u)) - 8388608.f;
+        const float sa = s * ((nib & 1) ? 1048576.f : 16777216.f);
+        const float sz = -s * zf;
+#pragma unroll
+        for (int tb = 0; tb < TB; ++tb)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float a = __fmaf_rn(sz, xs[tb][e], acc[mi][tb][2 * rs + e]);
+            acc[mi][tb][2 * rs + e] = __fmaf_rn(sa, accg[mi][tb][2 * rs + e], a);
+          }
+      }
+  };
 
   int done = j0;  // first stage not yet waited for
   bool failed = false;
@@ -152,164 +241,121 @@ __global__ void __launch_bounds__(kNW * 32, 2)
       break;
     }
     done = j + 1;
-    const unsigned char* b = my_slots + slot * GE::SLOT;
-#ifdef AWQ_DECODE_DEBUG_DUMP
-    AWQ_DECODE_DEBUG_DUMP(b, GE::SLOT);
-#endif
-    const uint32_t* Z = reinterpret_cast<const uint32_t*>(b + GE::Z_OFF);
-    const uint4* S = reinterpret_cast<const uint4*>(b + GE::S_OFF);
-
-    // Zero pairs for this stage's group: (1024 + z) for even nibbles, (1024 + 16 z) for odd.
-    uint32_t zp[CWL][8];
-    uint32_t sv[CWL][4];
+    const uint32_t sb = slots_u32 + slot * GE::SLOT;
+    const int grp = (j * kRS) / p.G;
+    if (grp != cur) {
+      if (kSub && cur >= 0) fold();
+      cur = grp;
 #pragma unroll
-    for (int c = 0; c < CWL; ++c) {
-      const uint32_t zw = Z[g8 * CWL + c];
-      const uint32_t lo = prmt(zw, zw, 0x5410u), hi = prmt(zw, zw, 0x7632u);
-      const uint32_t lo8 = lo >> 8, hi8 = hi >> 8;
-      if (kFactor) {
-        zp[c][0] = and_or(lo, 0x000F000Fu, kMagic);
-        zp[c][1] = and_or(lo, 0x00F000F0u, kMagic);
-        zp[c][2] = and_or(lo8, 0x000F000Fu, kMagic);
-        zp[c][3] = and_or(lo8, 0x00F000F0u, kMagic);
-        zp[c][4] = and_or(hi, 0x000F000Fu, kMagic);
-        zp[c][5] = and_or(hi, 0x00F000F0u, kMagic);
-        zp[c][6] = and_or(hi8, 0x000F000Fu, kMagic);
-        zp[c][7] = and_or(hi8, 0x00F000F0u, kMagic);
+      for (int c = 0; c < CWL; ++c) {
+        zw[c] = lds32(sb + GE::Z_OFF + (g8 * CWL + c) * 4);
+        const uint4 s4 = lds128(sb + GE::S_OFF + (g8 * CWL + c) * 16);
+        sv[c][0] = s4.x; sv[c][1] = s4.y; sv[c][2] = s4.z; sv[c][3] = s4.w;
+      }
+      if (kSub) {
+#pragma unroll
+        for (int i = 0; i < NMMA; ++i)
+#pragma unroll
+          for (int b = 0; b < TB; ++b)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accg[i][b][e] = 0.f;
+#pragma unroll
+        for (int b = 0; b < TB; ++b)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) xs[b][e] = 0.f;
       } else {
-        zp[c][0] = and_or(lo, 0x000F000Fu, kMagic);
-        zp[c][1] = and_or(lo >> 4, 0x000F000Fu, kMagic);
-        zp[c][2] = and_or(lo8, 0x000F000Fu, kMagic);
-        zp[c][3] = and_or(lo8 >> 4, 0x000F000Fu, kMagic);
-        zp[c][4] = and_or(hi, 0x000F000Fu, kMagic);
-        zp[c][5] = and_or(hi >> 4, 0x000F000Fu, kMagic);
-        zp[c][6] = and_or(hi8, 0x000F000Fu, kMagic);
-        zp[c][7] = and_or(hi8 >> 4, 0x000F000Fu, kMagic);
+        // Zero pairs (1024 + z) in both halves, one per nibble.
+#pragma unroll
+        for (int c = 0; c < CWL; ++c) {
+          const uint32_t lo = prmt(zw[c], zw[c], 0x5410u), hi = prmt(zw[c], zw[c], 0x7632u);
+          zp[kSub ? 0 : c][0] = and_or(lo, 0x000F000Fu, kMagic);
+          zp[kSub ? 0 : c][1] = and_or(lo >> 4, 0x000F000Fu, kMagic);
+          zp[kSub ? 0 : c][2] = and_or(lo >> 8, 0x000F000Fu, kMagic);
+          zp[kSub ? 0 : c][3] = and_or(lo >> 12, 0x000F000Fu, kMagic);
+          zp[kSub ? 0 : c][4] = and_or(hi, 0x000F000Fu, kMagic);
+          zp[kSub ? 0 : c][5] = and_or(hi >> 4, 0x000F000Fu, kMagic);
+          zp[kSub ? 0 : c][6] = and_or(hi >> 8, 0x000F000Fu, kMagic);
+          zp[kSub ? 0 : c][7] = and_or(hi >> 12, 0x000F000Fu, kMagic);
+        }
       }
-      const uint4 s4 = S[g8 * CWL + c];
-      sv[c][0] = s4.x; sv[c][1] = s4.y; sv[c][2] = s4.z; sv[c][3] = s4.w;
     }
 
-    float accg[kFactor ? NMMA : 1][TB][4];
-    // prmt selectors: low (high) 16 bits of row 2q in the low half, of row 2q+1 in the high.
-    const uint32_t sel_lo = (q & 1) ? 0x1054u : 0x5410u;
-    const uint32_t sel_hi = (q & 1) ? 0x3276u : 0x7632u;
 #pragma unroll
-    for (int ks = 0; ks < kRS / 16; ++ks) {
-      // Packed words of lane (g8, q), column-words g8*CWL .. +CWL-1, rows
-      //   r = 0, 1 -> 16ks + 2q + {0, 1},   r = 2, 3 -> 16ks + 2q + 8 + {0, 1},
-      // the row parity swapped for odd q so that, with 64-byte rows, the four q-lanes of a
-      // read cover both halves of the bank space (the prmt selectors undo the swap).
-      uint32_t w[4][CWL];
+    for (int pr = 0; pr < 2; ++pr) {
+      // Activation fragments for k16-steps 2pr and 2pr+1: xr[tb][2kk + h] holds token
+      // 8tb + g8, k = 16(2pr+kk) + 2q + 8h .. +1.
+      uint32_t xr[TB][4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int row = 16 * ks + 2 * q + ((r ^ q) & 1) + 8 * (r >> 1);
-        if constexpr (CWL == 2) {
-          const uint32_t off = static_cast<uint32_t>(row * 64 + g8 * 8);
-          const uint2 v = *reinterpret_cast<const uint2*>(b + off);
-          w[r][0] = v.x;
-          w[r][1] = v.y;
-        } else {
-          const uint32_t off = static_cast<uint32_t>(row * 32 + g8 * 4);
-          w[r][0] = *reinterpret_cast<const uint32_t*>(b + off);
-        }
-      }
-      // Activations: token 8tb + g8, k = 16ks + 2q + {0,1} and 16ks + 2q + 8 + {0,1}.
-      uint32_t bx[TB][2];
+      for (int tb = 0; tb < TB; ++tb) ldmatrix_x4(xr[tb], sb + x_off[tb][pr]);
 #pragma unroll
-      for (int tb = 0; tb < TB; ++tb) {
-        const uint32_t base = static_cast<uint32_t>((8 * tb + g8) * (kRS * 2) + (16 * ks + 2 * q) * 2);
-        bx[tb][0] = *reinterpret_cast<const uint32_t*>(b + GE::X_OFF + swz128(base));
-        bx[tb][1] = *reinterpret_cast<const uint32_t*>(b + GE::X_OFF + swz128(base + 16));
-      }
-      // Half2 operands v[c][rp][i]: rows (2q + 8rp, 2q + 8rp + 1), nibble i of word c.
-      uint32_t v[CWL][2][8];
+      for (int kk = 0; kk < 2; ++kk) {
+        const int ks = 2 * pr + kk;
+        uint32_t w[4][CWL];
 #pragma unroll
-      for (int c = 0; c < CWL; ++c)
-#pragma unroll
-        for (int rp = 0; rp < 2; ++rp) {
-          const uint32_t plo = prmt(w[2 * rp][c], w[2 * rp + 1][c], sel_lo);
-          const uint32_t phi = prmt(w[2 * rp][c], w[2 * rp + 1][c], sel_hi);
-          const uint32_t plo8 = plo >> 8, phi8 = phi >> 8;
-          uint32_t h[8];
-          if (kFactor) {
-            h[0] = and_or(plo, 0x000F000Fu, kMagic);
-            h[1] = and_or(plo, 0x00F000F0u, kMagic);
-            h[2] = and_or(plo8, 0x000F000Fu, kMagic);
-            h[3] = and_or(plo8, 0x00F000F0u, kMagic);
-            h[4] = and_or(phi, 0x000F000Fu, kMagic);
-            h[5] = and_or(phi, 0x00F000F0u, kMagic);
-            h[6] = and_or(phi8, 0x000F000Fu, kMagic);
-            h[7] = and_or(phi8, 0x00F000F0u, kMagic);
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t a = sb + w_off[r] + ks * 16 * GE::CW_W * 4;
+          if constexpr (CWL == 2) {
+            const uint2 v = lds64(a);
+            w[r][0] = v.x;
+            w[r][1] = v.y;
           } else {
-            h[0] = and_or(plo, 0x000F000Fu, kMagic);
-            h[1] = and_or(plo >> 4, 0x000F000Fu, kMagic);
-            h[2] = and_or(plo8, 0x000F000Fu, kMagic);
-            h[3] = and_or(plo8 >> 4, 0x000F000Fu, kMagic);
-            h[4] = and_or(phi, 0x000F000Fu, kMagic);
-            h[5] = and_or(phi >> 4, 0x000F000Fu, kMagic);
-            h[6] = and_or(phi8, 0x000F000Fu, kMagic);
-            h[7] = and_or(phi8 >> 4, 0x000F000Fu, kMagic);
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t d = hsub2(h[i], zp[c][i]);
-            if (!kFactor) {
-              const int col = nibble_column(i);
-              d = hmul2(d, prmt(sv[c][col >> 1], 0u, (col & 1) ? 0x3232u : 0x1010u));
-            }
-            v[c][rp][i] = d;
+            w[r][0] = lds32(a);
           }
         }
-#ifdef AWQ_DECODE_DEBUG_OPS
-      AWQ_DECODE_DEBUG_OPS(ks, bx, v, w);
-#endif
+        // src[c][rp][h]: rows (2q + 8rp, +1) of column-word c, nibbles 2h and 2h+1 in the
+        // low byte of each half.
+        uint32_t src[CWL][2][4];
 #pragma unroll
-      for (int mi = 0; mi < NMMA; ++mi) {
-        const int ca = mma_cw<CWL>(mi, 0), ia = mma_nib<CWL>(mi, 0);
-        const int cb = mma_cw<CWL>(mi, 1), ib = mma_nib<CWL>(mi, 1);
+        for (int c = 0; c < CWL; ++c)
 #pragma unroll
-        for (int tb = 0; tb < TB; ++tb) {
-          if (kFactor) {
-            if (ks == 0)
-              mma16816_zero(accg[mi][tb], v[ca][0][ia], v[cb][0][ib], v[ca][1][ia], v[cb][1][ib],
-                            bx[tb][0], bx[tb][1]);
-            else
-              mma16816(accg[mi][tb], v[ca][0][ia], v[cb][0][ib], v[ca][1][ia], v[cb][1][ib],
-                       bx[tb][0], bx[tb][1]);
+          for (int rp = 0; rp < 2; ++rp) {
+            const uint32_t plo = prmt(w[2 * rp][c], w[2 * rp + 1][c], sel_lo);
+            const uint32_t phi = prmt(w[2 * rp][c], w[2 * rp + 1][c], sel_hi);
+            src[c][rp][0] = plo;
+            src[c][rp][1] = plo >> 8;
+            src[c][rp][2] = phi;
+            src[c][rp][3] = phi >> 8;
+          }
+        auto operand = [&](int c, int rp, int nib) -> uint32_t {
+          const uint32_t s = src[c][rp][nib >> 1];
+          if (kSub) {
+            // exact fp16 subnormals c * 2^-24 (even nibble) or c * 2^-20 (odd nibble)
+            return s & ((nib & 1) ? 0x00F000F0u : 0x000F000Fu);
           } else {
-            mma16816(acc[mi][tb], v[ca][0][ia], v[cb][0][ib], v[ca][1][ia], v[cb][1][ib],
-                     bx[tb][0], bx[tb][1]);
+            const uint32_t h = and_or((nib & 1) ? (s >> 4) : s, 0x000F000Fu, kMagic);
+            const int col = nibble_column(nib);
+            const uint32_t spair = prmt(sv[c][col >> 1], 0u, (col & 1) ? 0x3232u : 0x1010u);
+            return hmul2(hsub2(h, zp[kSub ? 0 : c][nib]), spair);
           }
-        }
-      }
-    }
-    if (kFactor) {
-      // acc += scale * accg; odd nibbles carry a factor 16, removed exactly.
+        };
 #pragma unroll
-      for (int mi = 0; mi < NMMA; ++mi)
-#pragma unroll
-        for (int rs = 0; rs < 2; ++rs) {
-          const int c = mma_cw<CWL>(mi, rs);
-          const int nib = mma_nib<CWL>(mi, rs);
-          const int col = nibble_column(nib);
-          const uint32_t pr = sv[c][col >> 1];
-          float s = __half2float(__ushort_as_half(
-              static_cast<unsigned short>((col & 1) ? (pr >> 16) : (pr & 0xFFFFu))));
-          if (nib & 1) s *= 0.0625f;
+        for (int mi = 0; mi < NMMA; ++mi) {
+          const int ca = mma_cw<CWL>(mi, 0), ia = mma_nib<CWL>(mi, 0);
+          const int cb = mma_cw<CWL>(mi, 1), ib = mma_nib<CWL>(mi, 1);
+          const uint32_t a0 = operand(ca, 0, ia), a1 = operand(cb, 0, ib);
+          const uint32_t a2 = operand(ca, 1, ia), a3 = operand(cb, 1, ib);
 #pragma unroll
           for (int tb = 0; tb < TB; ++tb) {
-            acc[mi][tb][2 * rs] = __fmaf_rn(s, accg[mi][tb][2 * rs], acc[mi][tb][2 * rs]);
-            acc[mi][tb][2 * rs + 1] = __fmaf_rn(s, accg[mi][tb][2 * rs + 1], acc[mi][tb][2 * rs + 1]);
+            if (kSub)
+              mma16816(accg[mi][tb], a0, a1, a2, a3, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
+            else
+              mma16816(acc[mi][tb], a0, a1, a2, a3, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
           }
         }
+        if (kSub) {
+#pragma unroll
+          for (int tb = 0; tb < TB; ++tb)
+            mma16816(xs[tb], kOnes, kOnes, kOnes, kOnes, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
+        }
+      }
     }
-#ifdef AWQ_DECODE_DEBUG_ACC
-    AWQ_DECODE_DEBUG_ACC(acc);
-#endif
     __syncwarp();
-    if (lane == 0 && j + kSlots < j1) issue(slot, j + kSlots);
+    if (lane == 0 && j + kSlots < j1) {
+      issue_weights(slot, j + kSlots);
+      issue_x(slot, j + kSlots);
+    }
   }
+  if (kSub && cur >= 0 && !failed) fold();
   if (failed) {
     // Let copies already issued land (bounded) before the slots are reused below.
     const int issued_end = min(j1, done + kSlots);
@@ -342,11 +388,11 @@ __global__ void __launch_bounds__(kNW * 32, 2)
   const int e_hi = static_cast<int>((long long)GE::E * (rank + 1) / cs);
   for (int e = e_lo + threadIdx.x; e < e_hi; e += kNW * 32) {
     const int ln = e & 31;
-    const int j = (e >> 5) & 3;
+    const int jj = (e >> 5) & 3;
     const int tb = (e >> 7) % TB;
     const int mi = (e >> 7) / TB;
-    const int rs = j >> 1;
-    const int tok = m0 + 8 * tb + 2 * (ln & 3) + (j & 1);
+    const int rs = jj >> 1;
+    const int tok = m0 + 8 * tb + 2 * (ln & 3) + (jj & 1);
     const int cw = cw0 + (ln >> 2) * CWL + mma_cw<CWL>(mi, rs);
     if (tok < p.M && cw < p.C) {
       float s = 0.f;
@@ -361,7 +407,7 @@ __global__ void __launch_bounds__(kNW * 32, 2)
 
 struct Variant {
   int TB, CWL;
-  bool factor;
+  bool sub;
 };
 
 Variant pick(const GemmProblem& p) {
@@ -370,17 +416,64 @@ Variant pick(const GemmProblem& p) {
   return Variant{4, 1, false};
 }
 
-template <int TB, int CWL, bool F>
-cudaError_t launch_v(const GemmProblem& p, const Variant&) {
+// Largest number of co-resident clusters of each size (index = cluster size), measured
+// once per kernel variant with the occupancy API.
+template <int TB, int CWL, bool S>
+const int* cluster_capacity() {
   using GE = Geo<TB, CWL>;
-  auto kern = decode_tma_kernel<TB, CWL, F>;
+  static int cap[kMaxCluster + 1] = {};
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(GE::SMEM));
+  std::call_once(once, [] {
+    auto kern = decode_tma_kernel<TB, CWL, S>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(GE::SMEM)) != cudaSuccess)
+      return;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (int cs = 1; cs <= kMaxCluster; ++cs) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cs, 1, 1);
+      cfg.blockDim = dim3(kNW * 32, 1, 1);
+      cfg.dynamicSmemBytes = GE::SMEM;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cs;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+      cap[cs] = n;
+    }
+    (void)cudaGetLastError();
   });
-  if (attr_err != cudaSuccess) return attr_err;
+  return cap;
+}
+
+// Cluster size: the largest resident CTA count in one wave, each warp keeping at least one
+// 64-row stage; ties go to the smaller cluster (less reduction traffic).
+int choose_cluster(long long tiles, int ts, const int* cap) {
+  int best = 1;
+  long long best_resident = -1;
+  for (int cs = 1; cs <= kMaxCluster; ++cs) {
+    if (cap[cs] <= 0) continue;
+    if ((long long)cs * kNW > ts && cs > 1) break;
+    const long long grid = tiles * cs;
+    const long long slots = (long long)cap[cs] * cs;
+    const long long resident = grid <= slots ? grid : -1;  // single wave only
+    if (resident > best_resident) {
+      best_resident = resident;
+      best = cs;
+    }
+  }
+  return best;
+}
+
+template <int TB, int CWL, bool S>
+cudaError_t launch_v(const GemmProblem& p) {
+  using GE = Geo<TB, CWL>;
+  const int* cap = cluster_capacity<TB, CWL, S>();
+  if (cap[1] <= 0) return cudaErrorInvalidConfiguration;
 
   TmaDecodeParams dp;
   const char* why = nullptr;
@@ -403,23 +496,23 @@ cudaError_t launch_v(const GemmProblem& p, const Variant&) {
 
   const int nt = (C + GE::CW_W - 1) / GE::CW_W;
   const int mz = (p.M + 8 * TB - 1) / (8 * TB);
-  const int ts = p.K / kRS;
-  int cs = 1;
-  while (cs < 8 && (long long)nt * mz * cs * 2 <= 2 * 152 && ts >= 2 * cs * kNW) cs *= 2;
+  const int cs = choose_cluster((long long)nt * mz, p.K / kRS, cap);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nt * cs), static_cast<unsigned>(mz), 1);
   cfg.blockDim = dim3(kNW * 32, 1, 1);
   cfg.dynamicSmemBytes = GE::SMEM;
   cfg.stream = p.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, dp);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S>, dp);
 }
 
 }  // namespace
@@ -440,9 +533,9 @@ bool decode_tma_supported(const GemmProblem& p, const char** why) {
 
 cudaError_t launch_decode_tma(const GemmProblem& p) {
   const Variant v = pick(p);
-  if (v.TB == 1) return launch_v<1, 2, true>(p, v);
-  if (v.TB == 2) return launch_v<2, 1, true>(p, v);
-  return launch_v<4, 1, false>(p, v);
+  if (v.TB == 1) return launch_v<1, 2, true>(p);
+  if (v.TB == 2) return launch_v<2, 1, true>(p);
+  return launch_v<4, 1, false>(p);
 }
 
 }  // namespace awq

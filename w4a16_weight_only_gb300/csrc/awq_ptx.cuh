@@ -161,5 +161,24 @@ __device__ __forceinline__ uint32_t swz128(uint32_t off) { return off ^ (((off >
 __device__ __forceinline__ uint32_t swz64(uint32_t off) { return off ^ (((off >> 7) & 3u) << 4); }
 __device__ __forceinline__ uint32_t swz32(uint32_t off) { return off ^ (((off >> 7) & 1u) << 4); }
 
+// ldmatrix: four 8x8 b16 matrices; lane l supplies the row address of row (l % 8) of
+// matrix (l / 8); register j receives row (lane / 4), columns 2 (lane % 4) .. +1 of
+// matrix j.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr)
+               : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's memory to be visible /
+// let the next grid in the stream start launching.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace ptx
 }  // namespace awq
