@@ -43,7 +43,6 @@ namespace {
 using namespace ptx;
 
 constexpr int kNW = 4;       // warps per CTA
-constexpr int kSlots = 2;    // ring slots per warp
 constexpr int kRS = 64;      // rows of K per stage
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kMagic = 0x64006400u;     // fp16 1024 in both halves
@@ -53,31 +52,38 @@ constexpr unsigned int kStatusDecodeTimeout = 0x1u;
 
 struct __align__(64) TmaDecodeParams {
   CUtensorMap tm_w;  // qweight [K][C] u32, box {CW_W, 64}, unswizzled
-  CUtensorMap tm_x;  // x [M][K] f16, box {64, 8*TB}, 128B swizzle
+  CUtensorMap tm_x;  // x [M][K] f16, box {64, x_rows}, 128B swizzle
   CUtensorMap tm_z;  // qzeros [K/G][C] u32, box {CW_W, 1}
   CUtensorMap tm_s;  // scales [K/G][N] f16, box {8*CW_W, 1}
   const __half* bias;
   __half* y;
   unsigned int* status;
   int M, K, N, C, G;
+  int x_rows;  // rows of the activation box: min(M, 8*TB)
 };
 
 template <int TB, int CWL>
 struct Geo {
   static constexpr int CW_W = 8 * CWL;              // packed column-words per warp / CTA
   static constexpr int W_BYTES = kRS * CW_W * 4;    // packed weight tile per stage
-  static constexpr int X_BYTES = 8 * TB * kRS * 2;  // activation tile per stage
+  static constexpr int SLOTS = TB == 4 ? 2 : 3;     // ring slots per warp
+  static constexpr int X_BYTES = 8 * TB * kRS * 2;  // activation tile per stage (max)
   static constexpr int Z_BYTES = CW_W * 4;
   static constexpr int S_BYTES = 8 * CW_W * 2;
   static constexpr int X_OFF = W_BYTES;             // both multiples of 1024
   static constexpr int Z_OFF = W_BYTES + X_BYTES;
   static constexpr int S_OFF = Z_OFF + 128;
   static constexpr int SLOT = ((S_OFF + S_BYTES + 1023) / 1024) * 1024;
-  static constexpr uint32_t TX = W_BYTES + X_BYTES + Z_BYTES + S_BYTES;
+  static constexpr uint32_t META_TX = Z_BYTES + S_BYTES;
   static constexpr int NMMA = 4 * CWL;
   static constexpr int E = NMMA * TB * 4 * 32;      // partial sums per warp
-  static constexpr size_t SMEM = 1024 + (size_t)kNW * kSlots * SLOT + kNW * kSlots * 8;
-  static_assert((size_t)kNW * E * 4 <= (size_t)kNW * kSlots * SLOT, "reduction buffer");
+  static constexpr int RING = kNW * SLOTS * SLOT;   // all warps' rings
+  static constexpr int ZERO_OFF = RING;              // one 128-byte zero line per warp
+  static constexpr int BIAS_OFF = RING + kNW * 128;  // bias of the CTA's columns (fp32)
+  static constexpr int COUNT_OFF = BIAS_OFF + 8 * CW_W * 4;  // per-warp counters
+  static constexpr int BAR_OFF = COUNT_OFF + kNW * 4 + 16;
+  static constexpr size_t SMEM = 1024 + (size_t)BAR_OFF + kNW * SLOTS * 8 + 8;
+  static_assert((size_t)(kNW * E + E + kMaxCluster) * 4 <= (size_t)RING, "reduction buffers");
 };
 
 // Packed column-word (within the lane's CWL words) and nibble that feed A row g (rs = 0)
@@ -110,14 +116,15 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 }
 
 template <int TB, int CWL, bool kSub>
-__global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
+__global__ void __launch_bounds__(kNW * 32, 3)
     decode_tma_kernel(const __grid_constant__ TmaDecodeParams p) {
   using GE = Geo<TB, CWL>;
   constexpr int NMMA = GE::NMMA;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kNW * kSlots * GE::SLOT);
+  constexpr int kSlots = GE::SLOTS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GE::BAR_OFF);
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -128,32 +135,52 @@ __global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
   const int cw0 = static_cast<int>(blockIdx.x / cs) * GE::CW_W;
   const int m0 = blockIdx.y * 8 * TB;
 
-  const int TS = p.K / kRS;
-  const int P = static_cast<int>(cs) * kNW;
-  const int wid = static_cast<int>(rank) * kNW + warp;
-  const int j0 = static_cast<int>((long long)TS * wid / P);
-  const int j1 = static_cast<int>((long long)TS * (wid + 1) / P);
+  // 32-bit arithmetic throughout: TS * P < 2^31 (checked on the host).
+  const uint32_t TS = static_cast<uint32_t>(p.K / kRS);
+  const uint32_t P = cs * kNW;
+  const uint32_t wid = rank * kNW + static_cast<uint32_t>(warp);
+  const int j0 = static_cast<int>(TS * wid / P);
+  const int j1 = static_cast<int>(TS * (wid + 1) / P);
 
   unsigned char* my_slots = smem + (size_t)warp * kSlots * GE::SLOT;
   uint64_t* my_bars = bars + warp * kSlots;
   const uint32_t slots_u32 = smem_u32(my_slots);
 
+#ifdef AWQ_DECODE_DEBUG_TIME
+  AWQ_DECODE_DEBUG_TIME(0);
+#endif
+  // Reduction mbarrier (after all ring barriers): counts the bytes other CTAs push here.
+  uint64_t* red_bar = bars + kNW * kSlots;
   if (lane == 0) {
     prefetch_tmap(&p.tm_w);
     prefetch_tmap(&p.tm_x);
     for (int s = 0; s < kSlots; ++s) mbar_init(&my_bars[s], 1);
+    if (warp == 0) mbar_init(red_bar, 1);
     fence_mbar_init();
   }
   __syncwarp();
 
+  // Stage j of this warp: packed weights always, the group's zero and scale rows only when
+  // stage j opens a group (or is the warp's first stage), activations separately.
+  const int spg = p.G / kRS;  // stages per quantization group
+  const uint32_t x_tx = static_cast<uint32_t>(p.x_rows) * kRS * 2;
+  // Issue-side stage/group counters (advanced by lane 0 only; no division per stage).
+  int iss_grp = j0 / spg;
+  int iss_left = spg - (j0 - iss_grp * spg);  // stages left in iss_grp, counting the next
   auto issue_weights = [&](int slot, int j) {
     unsigned char* b = my_slots + slot * GE::SLOT;
     uint64_t* bar = &my_bars[slot];
-    mbar_arrive_expect_tx(bar, GE::TX);
-    const int grp = (j * kRS) / p.G;
+    const bool meta = (j == j0) || (iss_left == spg);
+    mbar_arrive_expect_tx(bar, GE::W_BYTES + x_tx + (meta ? GE::META_TX : 0u));
     tma_load_2d(b, &p.tm_w, bar, cw0, j * kRS);
-    tma_load_2d(b + GE::Z_OFF, &p.tm_z, bar, cw0, grp);
-    tma_load_2d(b + GE::S_OFF, &p.tm_s, bar, 8 * cw0, grp);
+    if (meta) {
+      tma_load_2d(b + GE::Z_OFF, &p.tm_z, bar, cw0, iss_grp);
+      tma_load_2d(b + GE::S_OFF, &p.tm_s, bar, 8 * cw0, iss_grp);
+    }
+    if (--iss_left == 0) {
+      ++iss_grp;
+      iss_left = spg;
+    }
   };
   auto issue_x = [&](int slot, int j) {
     tma_load_2d(my_slots + slot * GE::SLOT + GE::X_OFF, &p.tm_x, &my_bars[slot], j * kRS, m0);
@@ -180,16 +207,33 @@ __global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
   const uint32_t sel_lo = (q & 1) ? 0x1054u : 0x5410u;
   const uint32_t sel_hi = (q & 1) ? 0x3276u : 0x7632u;
   // ldmatrix row addresses for the activation tile (128-byte rows, 128B swizzle): lane l
-  // addresses row (l & 7) of 16-byte chunk 4*pair + (l >> 3).
+  // addresses row (l & 7) of 16-byte chunk 4*pair + (l >> 3).  Rows past the activation
+  // box (fewer than 8 tokens) read this warp's zero line instead.
+  const uint32_t zero_line = smem_u32(smem + GE::ZERO_OFF + warp * 128);
+  if (lane < 32) reinterpret_cast<uint32_t*>(smem + GE::ZERO_OFF + warp * 128)[lane] = 0u;
+  __syncwarp();
+  // Bias of this CTA's columns, read now (off the critical path) for the epilogue.
+  {
+    float* bias_s = reinterpret_cast<float*>(smem + GE::BIAS_OFF);
+    for (int i = threadIdx.x; i < 8 * GE::CW_W; i += kNW * 32) {
+      const int n = 8 * cw0 + i;
+      bias_s[i] = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+    }
+  }
   uint32_t x_off[TB][2];
+  bool x_real[TB];
 #pragma unroll
-  for (int tb = 0; tb < TB; ++tb)
+  for (int tb = 0; tb < TB; ++tb) {
+    const int rr = lane & 7;
+    x_real[tb] = (8 * tb + rr) < p.x_rows;
 #pragma unroll
     for (int pr = 0; pr < 2; ++pr) {
-      const int rr = lane & 7;
       const int chunk = 4 * pr + (lane >> 3);
-      x_off[tb][pr] = static_cast<uint32_t>(GE::X_OFF + (8 * tb + rr) * 128 + ((chunk ^ rr) << 4));
+      x_off[tb][pr] = x_real[tb]
+                          ? static_cast<uint32_t>(GE::X_OFF + (8 * tb + rr) * 128 + ((chunk ^ rr) << 4))
+                          : static_cast<uint32_t>(chunk << 4);
     }
+  }
 
   float acc[NMMA][TB][4];
 #pragma unroll
@@ -204,45 +248,69 @@ __global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
   uint32_t sv[CWL][4];
   uint32_t zp[kSub ? 1 : CWL][8];
   int cur = -1;
+  // Group of stage j is j / spg; tracked incrementally (one division per warp).
+  int grp_of = j0 / spg;
+  int grp_left = spg - (j0 - grp_of * spg);  // stages left in grp_of, counting j0
 
   auto fold = [&]() {
+#ifdef AWQ_ABL_NOFOLD
+    return;
+#endif
     // acc += scale * (2^24 or 2^20 * sum x c - zero * sum x) for the group just finished.
+    // Nibbles i and i+4 of a packed word are columns 2(i&3) and 2(i&3)+1: their scales are
+    // the two halves of sv[c][i&3] and their zeros come out of one shift-and.
 #pragma unroll
-    for (int mi = 0; mi < NMMA; ++mi)
+    for (int c = 0; c < CWL; ++c)
 #pragma unroll
-      for (int rs = 0; rs < 2; ++rs) {
-        const int c = mma_cw<CWL>(mi, rs);
-        const int nib = mma_nib<CWL>(mi, rs);
-        const int col = nibble_column(nib);
-        const uint32_t pr = sv[c][col >> 1];
-        const float s = __half2float(__ushort_as_half(
-            static_cast<unsigned short>((col & 1) ? (pr >> 16) : (pr & 0xFFFFu))));
-        const float zf =
-            __int_as_float(static_cast<int>(((zw[c] >> (4 * nib)) & 0xFu) | 0x4B000000u)) - 8388608.f;
-        const float sa = s * ((nib & 1) ? 1048576.f : 16777216.f);
-        const float sz = -s * zf;
+      for (int i = 0; i < 4; ++i) {
+        const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&sv[c][i]));
+        const uint32_t zz = (zw[c] >> (4 * i)) & 0x000F000Fu;
+        const float z_lo = static_cast<float>(zz & 0xFFFFu), z_hi = static_cast<float>(zz >> 16);
 #pragma unroll
-        for (int tb = 0; tb < TB; ++tb)
+        for (int h = 0; h < 2; ++h) {
+          const int nib = i + 4 * h;
+          const float s = h ? s2.y : s2.x;
+          const float sa = s * ((nib & 1) ? 1048576.f : 16777216.f);
+          const float sz = -s * (h ? z_hi : z_lo);
+          // the MMA row holding (column-word c, nibble nib) for this lane
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float a = __fmaf_rn(sz, xs[tb][e], acc[mi][tb][2 * rs + e]);
-            acc[mi][tb][2 * rs + e] = __fmaf_rn(sa, accg[mi][tb][2 * rs + e], a);
-          }
+          for (int mi = 0; mi < NMMA; ++mi)
+#pragma unroll
+            for (int rs = 0; rs < 2; ++rs) {
+              if (mma_cw<CWL>(mi, rs) != c || mma_nib<CWL>(mi, rs) != nib) continue;
+#pragma unroll
+              for (int tb = 0; tb < TB; ++tb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const float a = __fmaf_rn(sz, xs[tb][e], acc[mi][tb][2 * rs + e]);
+                  acc[mi][tb][2 * rs + e] = __fmaf_rn(sa, accg[mi][tb][2 * rs + e], a);
+                }
+            }
+        }
       }
   };
 
   int done = j0;  // first stage not yet waited for
   bool failed = false;
+  int slot = 0;
+  uint32_t parity = 0u;
   for (int j = j0; j < j1; ++j) {
-    const int slot = (j - j0) % kSlots;
-    const uint32_t parity = static_cast<uint32_t>(((j - j0) / kSlots) & 1);
     if (!mbar_wait_bounded(&my_bars[slot], parity, p.status, kStatusDecodeTimeout, kWaitLimitNs)) {
       failed = true;
       break;
     }
     done = j + 1;
+#ifdef AWQ_DECODE_DEBUG_TIME
+    if (j == j0) AWQ_DECODE_DEBUG_TIME(1);
+    if (j == j1 - 1) AWQ_DECODE_DEBUG_TIME(4);
+#endif
     const uint32_t sb = slots_u32 + slot * GE::SLOT;
-    const int grp = (j * kRS) / p.G;
+    if (grp_left == 0) {
+      ++grp_of;
+      grp_left = spg;
+    }
+    --grp_left;
+    const int grp = grp_of;
     if (grp != cur) {
       if (kSub && cur >= 0) fold();
       cur = grp;
@@ -286,7 +354,8 @@ __global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
       // 8tb + g8, k = 16(2pr+kk) + 2q + 8h .. +1.
       uint32_t xr[TB][4];
 #pragma unroll
-      for (int tb = 0; tb < TB; ++tb) ldmatrix_x4(xr[tb], sb + x_off[tb][pr]);
+      for (int tb = 0; tb < TB; ++tb)
+        ldmatrix_x4(xr[tb], (x_real[tb] ? sb : zero_line) + x_off[tb][pr]);
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int ks = 2 * pr + kk;
@@ -319,6 +388,9 @@ __global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
         auto operand = [&](int c, int rp, int nib) -> uint32_t {
           const uint32_t s = src[c][rp][nib >> 1];
           if (kSub) {
+#ifdef AWQ_ABL_NOUNPACK
+            return s;
+#endif
             // exact fp16 subnormals c * 2^-24 (even nibble) or c * 2^-20 (odd nibble)
             return s & ((nib & 1) ? 0x00F000F0u : 0x000F000Fu);
           } else {
@@ -342,17 +414,23 @@ __global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
               mma16816(acc[mi][tb], a0, a1, a2, a3, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
           }
         }
+#ifndef AWQ_ABL_NOONES
         if (kSub) {
 #pragma unroll
           for (int tb = 0; tb < TB; ++tb)
             mma16816(xs[tb], kOnes, kOnes, kOnes, kOnes, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
         }
+#endif
       }
     }
     __syncwarp();
     if (lane == 0 && j + kSlots < j1) {
       issue_weights(slot, j + kSlots);
       issue_x(slot, j + kSlots);
+    }
+    if (++slot == kSlots) {
+      slot = 0;
+      parity ^= 1u;
     }
   }
   if (kSub && cur >= 0 && !failed) fold();
@@ -366,8 +444,20 @@ __global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
     }
   }
 
+#ifdef AWQ_DECODE_DEBUG_TIME
+  AWQ_DECODE_DEBUG_TIME(2);
+#endif
   // Reduce: warps of the CTA (fixed order), then CTAs of the cluster (fixed order).
-  __syncthreads();  // the ring is reused as the reduction buffer
+  // Each thread signals the cluster as soon as its ring is idle, so the barrier wait below
+  // overlaps the CTA-level sum; partials are then pushed into the owning CTA's shared
+  // memory (no round-trip loads) and summed there after one more barrier.
+  // This CTA's ring is idle: all its copies were waited for and its fragment reads are
+  // consumed.  (red_bar's initialisation was published by the init fence at the start.)
+  cluster_arrive_relaxed();
+#ifdef AWQ_DECODE_DEBUG_TIME
+  AWQ_DECODE_DEBUG_TIME(5);
+#endif
+  __syncthreads();           // the ring is reused as the reduction buffer
   float* red = reinterpret_cast<float*>(smem);
   float* mine = red + warp * GE::E;
 #pragma unroll
@@ -377,32 +467,73 @@ __global__ void __launch_bounds__(kNW * 32, kSub ? 4 : 3)
 #pragma unroll
       for (int e = 0; e < 4; ++e) mine[((mi * TB + tb) * 4 + e) * 32 + lane] = acc[mi][tb][e];
   __syncthreads();
-  for (int e = threadIdx.x; e < GE::E; e += kNW * 32) {
-    float s = red[e];
+  // Output element e (warp-fragment order): token and column, valid when both exist.
+  auto token_of = [&](int e) { return m0 + 8 * ((e >> 7) % TB) + 2 * (e & 3) + ((e >> 5) & 1); };
+  auto col_of = [&](int e) {  // column offset inside the CTA tile
+    const int mi = (e >> 7) / TB, rs = ((e >> 5) & 3) >> 1;
+    return (((e & 31) >> 2) * CWL + mma_cw<CWL>(mi, rs)) * 8 + nibble_column(mma_nib<CWL>(mi, rs));
+  };
+  auto valid = [&](int e) { return token_of(e) < p.M && cw0 + (col_of(e) >> 3) < p.C; };
+  constexpr int kPer = (GE::E + kNW * 32 - 1) / (kNW * 32);
+  const int slice = (GE::E + static_cast<int>(cs) - 1) / static_cast<int>(cs);
+  const int my_lo = static_cast<int>(rank) * slice;
+  const int my_hi = min(GE::E, my_lo + slice);
+  float part[kPer];
+  int my_count = 0;  // this thread's share of the valid elements of this CTA's slice
 #pragma unroll
-    for (int w = 1; w < kNW; ++w) s += red[w * GE::E + e];
-    red[e] = s;
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x + i * kNW * 32;
+    part[i] = 0.f;
+    if (e < GE::E && valid(e)) {
+#pragma unroll
+      for (int w = 0; w < kNW; ++w) part[i] += red[w * GE::E + e];
+    }
+    my_count += (e >= my_lo && e < my_hi && valid(e)) ? 1 : 0;
   }
-  cluster_sync_all();
-  const int e_lo = static_cast<int>((long long)GE::E * rank / cs);
-  const int e_hi = static_cast<int>((long long)GE::E * (rank + 1) / cs);
-  for (int e = e_lo + threadIdx.x; e < e_hi; e += kNW * 32) {
-    const int ln = e & 31;
-    const int jj = (e >> 5) & 3;
-    const int tb = (e >> 7) % TB;
-    const int mi = (e >> 7) / TB;
-    const int rs = jj >> 1;
-    const int tok = m0 + 8 * tb + 2 * (ln & 3) + (jj & 1);
-    const int cw = cw0 + (ln >> 2) * CWL + mma_cw<CWL>(mi, rs);
-    if (tok < p.M && cw < p.C) {
-      float s = 0.f;
-      for (uint32_t r = 0; r < cs; ++r) s += ld_dsmem_f32(red + e, r);
-      const int n = 8 * cw + nibble_column(mma_nib<CWL>(mi, rs));
-      if (p.bias) s += __half2float(p.bias[n]);
-      p.y[(long long)tok * p.N + n] = __float2half_rn(s);
+  // Valid elements of the slice (each arrives from cs CTAs): warp sums, then warp 0.
+  int* counts = reinterpret_cast<int*>(smem + GE::COUNT_OFF);
+  float* recv = red + kNW * GE::E;  // [cs][slice], disjoint from red
+  {
+    const int wsum = __reduce_add_sync(0xffffffffu, my_count);
+    if (lane == 0) counts[warp] = wsum;
+  }
+  __syncthreads();
+  int mine_valid = 0;
+#pragma unroll
+  for (int w = 0; w < kNW; ++w) mine_valid += counts[w];
+#ifdef AWQ_DECODE_DEBUG_TIME
+  AWQ_DECODE_DEBUG_TIME(6);
+#endif
+  if (threadIdx.x == 0)
+    mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(mine_valid) * cs * 4u);
+  cluster_wait_acquire();  // every CTA of the cluster is past its main loop
+#ifdef AWQ_DECODE_DEBUG_TIME
+  AWQ_DECODE_DEBUG_TIME(7);
+#endif
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x + i * kNW * 32;
+    if (e < GE::E && valid(e)) {
+      const int owner = e / slice;
+      st_async_dsmem_f32(recv + rank * slice + (e - owner * slice), red_bar,
+                         static_cast<uint32_t>(owner), part[i]);
     }
   }
-  cluster_sync_all();
+  const bool got = mbar_wait_bounded(red_bar, 0u, p.status, kStatusDecodeTimeout, kWaitLimitNs);
+#ifdef AWQ_DECODE_DEBUG_TIME
+  AWQ_DECODE_DEBUG_TIME(1);
+#endif
+  const float* bias_s = reinterpret_cast<const float*>(smem + GE::BIAS_OFF);
+  for (int e = my_lo + threadIdx.x; got && e < my_hi; e += kNW * 32) {
+    if (!valid(e)) continue;
+    float sum = 0.f;
+    for (uint32_t r = 0; r < cs; ++r) sum += recv[r * slice + (e - my_lo)];
+    const int col = col_of(e);
+    p.y[(long long)token_of(e) * p.N + 8 * cw0 + col] = __float2half_rn(sum + bias_s[col]);
+  }
+#ifdef AWQ_DECODE_DEBUG_TIME
+  AWQ_DECODE_DEBUG_TIME(3);
+#endif
 }
 
 struct Variant {
@@ -481,8 +612,8 @@ cudaError_t launch_v(const GemmProblem& p) {
   const int ngrp = p.K / p.G;
   if (!make_tmap_2d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, GE::CW_W, kRS,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
-      !make_tmap_2d(&dp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kRS, 8 * TB,
-                    CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
+      !make_tmap_2d(&dp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kRS,
+                    p.M < 8 * TB ? p.M : 8 * TB, CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
       !make_tmap_2d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, GE::CW_W, 1,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
       !make_tmap_2d(&dp.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.sc, p.N, ngrp, 8 * GE::CW_W, 1,
@@ -493,6 +624,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   cudaError_t e = status_word_ptr(&dp.status);
   if (e != cudaSuccess) return e;
   dp.M = p.M; dp.K = p.K; dp.N = p.N; dp.C = C; dp.G = p.G;
+  dp.x_rows = p.M < 8 * TB ? p.M : 8 * TB;
 
   const int nt = (C + GE::CW_W - 1) / GE::CW_W;
   const int mz = (p.M + 8 * TB - 1) / (8 * TB);
@@ -528,6 +660,7 @@ bool decode_tma_supported(const GemmProblem& p, const char** why) {
     return false;
   }
   if ((p.M + 31) / 32 > 65535) { *why = "M too large for the decode grid"; return false; }
+  if ((long long)(p.K / kRS) * kMaxCluster * kNW >= (1LL << 31)) { *why = "K too large for the decode kernel"; return false; }
   return true;
 }
 
