@@ -48,6 +48,11 @@ def decode_ok(K, G):
     return K % 16 == 0 and G % 16 == 0
 
 
+def prefill_ok(K, N, G):
+    G = K if G == -1 else G
+    return K % 64 == 0 and G % 64 == 0 and N % 32 == 0
+
+
 # ------------------------------------------------------------------ dequant ----
 
 @pytest.mark.parametrize("K,N,G", [(256, 256, 128), (48, 24, 16), (96, 40, 32), (4096, 4096, 128),
@@ -89,18 +94,20 @@ SMALL = [(1, 256, 256, 128, False), (3, 512, 192, 64, True), (8, 1024, 520, 32, 
 
 
 @pytest.mark.parametrize("M,K,N,G,bias", SMALL)
-@pytest.mark.parametrize("path", ["auto", "decode", "generic"])
+@pytest.mark.parametrize("path", ["auto", "decode", "prefill", "generic"])
 def test_gemm_small_vs_oracle(awq, M, K, N, G, bias, path):
     if path == "decode" and not decode_ok(K, G):
         pytest.skip("shape outside the decode kernel's contract")
+    if path == "prefill" and not prefill_ok(K, N, G):
+        pytest.skip("shape outside the prefill kernel's contract")
     d = synth.awq_linear(8000 + M + K + N, M, K, N, group_size=G, bias=bias)
     y = run_gemm(awq, d, path)
     y_ref = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
     assert_close(y, y_ref, f"{path} M={M} K={K} N={N} G={G}")
 
 
-@pytest.mark.parametrize("M", [1, 5, 8, 12, 16, 30, 32, 40])
-@pytest.mark.parametrize("path", ["decode", "generic"])
+@pytest.mark.parametrize("M", [1, 5, 8, 12, 16, 30, 32, 40, 300])
+@pytest.mark.parametrize("path", ["decode", "prefill", "generic"])
 def test_gemm_exact_case_bitwise(awq, M, path):
     """Small-integer x, power-of-two scales, dyadic bias: every product and partial sum
     is exact in fp32, so y must equal the fp16 rounding of the exact result bit for bit
@@ -112,7 +119,7 @@ def test_gemm_exact_case_bitwise(awq, M, path):
     assert np.array_equal(y.view(np.uint16), y_ref.astype(np.float16).view(np.uint16))
 
 
-@pytest.mark.parametrize("M", [1, 16, 32, 96])
+@pytest.mark.parametrize("M", [1, 16, 32, 96, 600])
 def test_gemm_deterministic(awq, M):
     d = synth.awq_linear(9100 + M, M, 4096, 1024, group_size=128, bias=True)
     t = to_dev(d)

@@ -1,18 +1,430 @@
-// Prefill path of awq_gemm (large M): tcgen05/TMEM tensor-core kernel.  Placeholder
-// until the kernel lands: prefill_supported() reports the path unavailable, and the
-// device status word used by bounded waits lives here.
+// Prefill path of awq_gemm (large M): persistent tcgen05 / TMEM tensor-core kernel.
+//
+//   y[m][n] = sum_k x[m][k] * (code[k][n] - zero[k/G][n]) * scale[k/G][n]  (+ bias[n])
+//
+// (tensref.org/formats/awq, "Reader"; GPTQModel wiki "AWQ", "Native GEMM": fused
+// dequant-GEMM with fp32 accumulation.)
+//
+// Tiling (operands swapped so the dequantized side is the small one): one UMMA tile is
+// 128 output columns (the MMA's M side, A operand = dequantized W^T) by 256 activation
+// rows (the MMA's N side, B operand = x), K = 64 per pipeline stage, four
+// tcgen05.mma.kind::f16 (K = 16) per stage, fp32 accumulators in TMEM.  Each dequantized
+// 128 x 64 weight tile therefore feeds 256 activation rows.
+//
+// Warp roles (320 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: activation tile (256 x 64 fp16, 128B swizzle), packed weight
+//               tile (64 rows x 16 words), the stage's zero and scale rows -> 4-deep ring
+//   warp 1      TMEM allocation (512 columns = two 128 x 256 fp32 accumulators) and the
+//               single MMA-issuing thread
+//   warps 2-5   dequantize the packed tile into the K-major, 128B-swizzled fp16 A tile:
+//               w = (c - z) * s exactly (fp16 exponent trick, HSUB2, HMUL2) -> 2-deep ring
+//   warps 6-9   epilogue: tcgen05.ld (32 lanes x 32 columns), + bias, fp16, store; the
+//               second accumulator lets the next tile's MMAs run meanwhile
+// Every wait is an mbarrier try-wait bounded in wall time; on give-up the kernel sets the
+// device status word, all roles leave their loops, in-flight copies and MMAs are drained
+// (bounded) and TMEM is freed before exit.
+#include <mutex>
+
 #include "awq_internal.cuh"
+#include "awq_ptx.cuh"
 
 namespace awq {
 
 __device__ unsigned int g_status_word = 0u;
 
-bool prefill_supported(const GemmProblem&, const char** why) {
-  if (why) *why = "prefill kernel not built";
-  return false;
+namespace {
+
+using namespace ptx;
+
+constexpr int kBN = 128;   // output columns per tile (UMMA M)
+constexpr int kBT = 256;   // activation rows per tile (UMMA N)
+constexpr int kBK = 64;    // K per stage
+constexpr int kST = 4;     // TMA ring depth
+constexpr int kSA = 2;     // dequantized-A ring depth
+constexpr int kThreads = 320;
+constexpr uint32_t kMagic = 0x64006400u;
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
+constexpr unsigned int kStatusPrefillTimeout = 0x2u;
+
+// shared memory layout (offsets from a 1024-aligned base)
+constexpr int X_BYTES = kBT * kBK * 2;       // 32 KB
+constexpr int A_BYTES = kBN * kBK * 2;       // 16 KB
+constexpr int W_BYTES = kBK * 16 * 4;        // 4 KB
+constexpr int X_OFF = 0;
+constexpr int A_OFF = X_OFF + kST * X_BYTES;
+constexpr int W_OFF = A_OFF + kSA * A_BYTES;
+constexpr int Z_OFF = W_OFF + kST * W_BYTES;  // 128 B per stage
+constexpr int S_OFF = Z_OFF + kST * 128;      // 256 B per stage
+constexpr int BAR_OFF = S_OFF + kST * 256;
+// barriers: full_t[kST], empty_t[kST], full_a[kSA], empty_a[kSA], tfull[2], tempty[2], drain
+constexpr int NBARS = 2 * kST + 2 * kSA + 4 + 1;
+constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base (u32), abort flag (u32)
+constexpr size_t SMEM = 1024 + MISC_OFF + 16;
+constexpr uint32_t STAGE_TX = X_BYTES + W_BYTES + 16 * 4 + 128 * 2;
+
+struct __align__(64) PrefillParams {
+  CUtensorMap tm_x;  // x [M][K] f16, box {64, 256}, 128B swizzle
+  CUtensorMap tm_w;  // qweight [K][C] u32, box {16, 64}
+  CUtensorMap tm_z;  // qzeros [K/G][C] u32, box {16, 1}
+  CUtensorMap tm_s;  // scales [K/G][N] f16, box {128, 1}
+  const __half* bias;
+  __half* y;
+  unsigned int* status;
+  int M, K, N, C, G;
+  int tiles_t, tiles;  // activation-row tiles, total tiles
+};
+
+// tcgen05 shared-memory matrix descriptor: K-major operand, 128B swizzle, rows of 128 B
+// grouped by 8 (1024 B between groups).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);  // start address / 16
+  d |= static_cast<uint64_t>(1u) << 16;                 // leading byte offset (unused, 16 B)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;         // stride byte offset: 8 rows x 128 B
+  d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                 // layout: 128-byte swizzle
+  return d;
 }
 
-cudaError_t launch_prefill(const GemmProblem&) { return cudaErrorNotSupported; }
+// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B, both K-major,
+// N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) |
+                            (static_cast<uint32_t>(kBT >> 3) << 17) |
+                            (static_cast<uint32_t>(kBN >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t lds32p(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128p(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* full_t = bars;
+  uint64_t* empty_t = bars + kST;
+  uint64_t* full_a = bars + 2 * kST;
+  uint64_t* empty_a = bars + 2 * kST + kSA;
+  uint64_t* tfull = bars + 2 * kST + 2 * kSA;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + MISC_OFF);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KB = p.K / kBK;  // stages per tile
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kST; ++s) {
+      mbar_init(&full_t[s], 1);
+      mbar_init(&empty_t[s], 4 + 1);  // four dequant warps + one MMA commit
+    }
+    for (int s = 0; s < kSA; ++s) {
+      mbar_init(&full_a[s], 4);       // four dequant warps
+      mbar_init(&empty_a[s], 1);      // MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);        // MMA commit
+      mbar_init(&tempty[b], 4);       // four epilogue warps
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot)))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(bar, parity, p.status, kStatusPrefillTimeout, kWaitLimitNs)) return true;
+    *abort_flag = 1u;
+    return false;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_x);
+      prefetch_tmap(&p.tm_w);
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+        const int m0 = (tile % p.tiles_t) * kBT;
+        const int cw0 = (tile / p.tiles_t) * (kBN / 8);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait(&empty_t[s], ph ^ 1u)) { ok = false; break; }
+          const int k0 = kb * kBK;
+          const int grp = k0 / p.G;
+          mbar_arrive_expect_tx(&full_t[s], STAGE_TX);
+          tma_load_2d(smem + X_OFF + s * X_BYTES, &p.tm_x, &full_t[s], k0, m0);
+          tma_load_2d(smem + W_OFF + s * W_BYTES, &p.tm_w, &full_t[s], cw0, k0);
+          tma_load_2d(smem + Z_OFF + s * 128, &p.tm_z, &full_t[s], cw0, grp);
+          tma_load_2d(smem + S_OFF + s * 256, &p.tm_s, &full_t[s], 8 * cw0, grp);
+          ++issued;
+          if (++s == kST) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // drain: every issued stage's copies must land before the CTA can exit
+        for (int i = 0; i < kST && i < issued; ++i) {
+          if (--s < 0) { s = kST - 1; ph ^= 1u; }
+          mbar_wait_bounded(&full_t[s], ph, p.status, kStatusPrefillTimeout, kWaitLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int s = 0, sa = 0;
+      uint32_t ph = 0, pha = 0;
+      int li = 0;
+      bool ok = true;
+      bool any = false;
+      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x, ++li) {
+        const int b = li & 1;
+        if (!wait(&tempty[b], static_cast<uint32_t>(((li >> 1) & 1) ^ 1))) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(b * kBT);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait(&full_t[s], ph) || !wait(&full_a[sa], pha)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t adesc = sw128_desc(sbase + A_OFF + sa * A_BYTES);
+          const uint64_t bdesc = sw128_desc(sbase + X_OFF + s * X_BYTES);
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks)  // +32 B (16 fp16) along K per step
+            mma_f16(d, adesc + 2 * ks, bdesc + 2 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
+          any = true;
+          mma_commit(&empty_t[s]);
+          mma_commit(&empty_a[sa]);
+          if (++s == kST) { s = 0; ph ^= 1u; }
+          if (++sa == kSA) { sa = 0; pha ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[b]);
+      }
+      if (any) {
+        // all MMAs issued by this thread complete before TMEM is released
+        mma_commit(drain);
+        mbar_wait_bounded(drain, 0u, p.status, kStatusPrefillTimeout, kWaitLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- dequant
+    // thread -> (column-word cw, 8-row block kc) of the stage; chunk kc of output row n
+    // (= column 8cw + ORDER position) receives rows 8kc..8kc+7.
+    const int dq = threadIdx.x - 64;
+    const int kc = dq & 7;
+    const int cw = dq >> 3;  // 0..15
+    int s = 0, sa = 0;
+    uint32_t ph = 0, pha = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!wait(&full_t[s], ph) || !wait(&empty_a[sa], pha ^ 1u)) { ok = false; break; }
+        const uint32_t wb = sbase + W_OFF + s * W_BYTES;
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = lds32p(wb + ((8 * kc + j) * 16 + cw) * 4);
+        const uint32_t zw = lds32p(sbase + Z_OFF + s * 128 + cw * 4);
+        const uint4 s4 = lds128p(sbase + S_OFF + s * 256 + cw * 16);
+        const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+        // (1024 + zero) in both halves, per nibble; scale of the nibble's column in both
+        uint32_t zp[8], sp[8];
+        {
+          const uint32_t lo = prmt(zw, zw, 0x5410u), hi = prmt(zw, zw, 0x7632u);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            zp[i] = and_or(lo >> (4 * i), 0x000F000Fu, kMagic);
+            zp[i + 4] = and_or(hi >> (4 * i), 0x000F000Fu, kMagic);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int col = nibble_column(i);
+            sp[i] = prmt(sv[col >> 1], 0u, (col & 1) ? 0x3232u : 0x1010u);
+          }
+        }
+        // v[i][r]: rows (8kc + 2r, +1) of the nibble-i column, exact fp16 weights
+        uint32_t v[8][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const uint32_t plo = prmt(w[2 * r], w[2 * r + 1], 0x5410u);
+          const uint32_t phi = prmt(w[2 * r], w[2 * r + 1], 0x7632u);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t src = (i < 4 ? plo : phi) >> (4 * (i & 3));
+            v[i][r] = hmul2(hsub2(and_or(src, 0x000F000Fu, kMagic), zp[i]), sp[i]);
+          }
+        }
+        const uint32_t ab = sbase + A_OFF + sa * A_BYTES;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int n = 8 * cw + nibble_column(i);  // A row (output column in the tile)
+          sts128(ab + n * 128 + ((kc ^ (n & 7)) << 4), v[i][0], v[i][1], v[i][2], v[i][3]);
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&full_a[sa]);
+          mbar_arrive(&empty_t[s]);
+        }
+        if (++s == kST) { s = 0; ph ^= 1u; }
+        if (++sa == kSA) { sa = 0; pha ^= 1u; }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
+    const int nl = quad * 32 + lane;     // output column inside the tile
+    int li = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++li) {
+      const int b = li & 1;
+      const int m0 = (tile % p.tiles_t) * kBT;
+      const int n = (tile / p.tiles_t) * kBN + nl;
+      const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+      if (!wait(&tfull[b], static_cast<uint32_t>((li >> 1) & 1))) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(b * kBT);
+#pragma unroll 1
+      for (int c = 0; c < kBT / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(taddr + c * 32, v);
+        const int t0 = m0 + c * 32;
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (t0 + j < p.M)
+              p.y[(long long)(t0 + j) * p.N + n] = __float2half_rn(__uint_as_float(v[j]) + bias);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
+  }
+}
+
+std::once_flag g_attr_once;
+cudaError_t g_attr_err = cudaSuccess;
+
+}  // namespace
+
+bool prefill_supported(const GemmProblem& p, const char** why) {
+  static const char* dummy;
+  if (!why) why = &dummy;
+  if (p.K % kBK != 0) { *why = "prefill needs K % 64 == 0"; return false; }
+  if (p.G % kBK != 0) { *why = "prefill needs group_size % 64 == 0"; return false; }
+  if (p.N % 32 != 0) { *why = "prefill needs N % 32 == 0"; return false; }
+  if (!aligned(p.x, 16) || !aligned(p.qw, 16) || !aligned(p.qz, 16) || !aligned(p.sc, 16)) {
+    *why = "prefill needs 16-byte aligned x, qweight, qzeros, scales";
+    return false;
+  }
+  return true;
+}
+
+cudaError_t launch_prefill(const GemmProblem& p) {
+  std::call_once(g_attr_once, [] {
+    g_attr_err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(SMEM));
+  });
+  if (g_attr_err != cudaSuccess) return g_attr_err;
+  PrefillParams pp;
+  const char* why = nullptr;
+  const int C = p.N / 8;
+  const int ngrp = p.K / p.G;
+  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kBK, kBT,
+                    CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
+      !make_tmap_2d(&pp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, 16, kBK,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
+      !make_tmap_2d(&pp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, 16, 1,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
+      !make_tmap_2d(&pp.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.sc, p.N, ngrp, 128, 1,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, &why))
+    return cudaErrorInvalidValue;
+  pp.bias = p.bias;
+  pp.y = p.y;
+  cudaError_t e = status_word_ptr(&pp.status);
+  if (e != cudaSuccess) return e;
+  pp.M = p.M; pp.K = p.K; pp.N = p.N; pp.C = C; pp.G = p.G;
+  pp.tiles_t = (p.M + kBT - 1) / kBT;
+  const long long tiles = (long long)pp.tiles_t * ((p.N + kBN - 1) / kBN);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  pp.tiles = static_cast<int>(tiles);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = pp.tiles < sms ? pp.tiles : sms;
+  prefill_kernel<<<grid, kThreads, SMEM, p.stream>>>(pp);
+  return cudaGetLastError();
+}
 
 cudaError_t status_word_ptr(unsigned int** ptr) {
   static unsigned int* cache[64] = {};
