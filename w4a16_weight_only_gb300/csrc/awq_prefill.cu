@@ -16,7 +16,8 @@
 //               tile (64 rows x 16 words), the stage's zero and scale rows -> 4-deep ring
 //   warp 1      TMEM allocation (512 columns = two 128 x 256 fp32 accumulators) and the
 //               single MMA-issuing thread
-//   warps 2-5   dequantize the packed tile into the K-major, 128B-swizzled fp16 A tile:
+//   warps 2-5   dequantize the packed tile into the MN-major, 128B-swizzled fp16 A tile
+//               (one packed word = one 16-byte chunk of 8 adjacent columns, no transpose):
 //               w = (c - z) * s exactly (fp16 exponent trick, HSUB2, HMUL2) -> 2-deep ring
 //   warps 6-9   epilogue: tcgen05.ld (32 lanes x 32 columns), + bias, fp16, store; the
 //               second accumulator lets the next tile's MMAs run meanwhile
@@ -74,21 +75,29 @@ struct __align__(64) PrefillParams {
   int tiles_t, tiles;  // activation-row tiles, total tiles
 };
 
-// tcgen05 shared-memory matrix descriptor: K-major operand, 128B swizzle, rows of 128 B
-// grouped by 8 (1024 B between groups).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+// tcgen05 shared-memory matrix descriptor with 128-byte swizzle.
+//   K-major operand (B = activations): rows of 128 B (64 fp16 along K), 8-row groups
+//     1024 B apart (stride byte offset); the leading byte offset is unused.
+//   MN-major operand (A = dequantized weights): 1024-byte atoms of 8 K-rows x 64 columns;
+//     leading byte offset = distance between atoms along MN, stride byte offset =
+//     distance between atoms along K.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);  // start address / 16
-  d |= static_cast<uint64_t>(1u) << 16;                 // leading byte offset (unused, 16 B)
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;         // stride byte offset: 8 rows x 128 B
-  d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version
-  d |= static_cast<uint64_t>(2u) << 61;                 // layout: 128-byte swizzle
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);       // start address / 16
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;   // leading byte offset / 16
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;   // stride byte offset / 16
+  d |= static_cast<uint64_t>(1u) << 46;                     // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                     // layout: 128-byte swizzle
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B, both K-major,
+// A tile (MN-major): atom (column half ma, K group kg) at (ma * 8 + kg) * 1024.
+constexpr uint32_t kA_LBO = 8 * 1024;  // between the two 64-column halves
+constexpr uint32_t kA_SBO = 1024;      // between 8-row K groups
+
+// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B, A MN-major, B K-major,
 // N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) |
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (1u << 15) | (0u << 16) |
                             (static_cast<uint32_t>(kBT >> 3) << 17) |
                             (static_cast<uint32_t>(kBN >> 4) << 24);
 
@@ -247,11 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait(&full_t[s], ph) || !wait(&full_a[sa], pha)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t adesc = sw128_desc(sbase + A_OFF + sa * A_BYTES);
-          const uint64_t bdesc = sw128_desc(sbase + X_OFF + s * X_BYTES);
+          const uint64_t adesc = sw128_desc(sbase + A_OFF + sa * A_BYTES, kA_LBO, kA_SBO);
+          const uint64_t bdesc = sw128_desc(sbase + X_OFF + s * X_BYTES, 16u, 1024u);
 #pragma unroll
-          for (int ks = 0; ks < kBK / 16; ++ks)  // +32 B (16 fp16) along K per step
-            mma_f16(d, adesc + 2 * ks, bdesc + 2 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kBK / 16; ++ks)  // K += 16: A two atoms (2048 B), B 32 B
+            mma_f16(d, adesc + (2u * kA_SBO >> 4) * ks, bdesc + 2 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
           any = true;
           mma_commit(&empty_t[s]);
           mma_commit(&empty_a[sa]);
@@ -270,11 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __syncwarp();
   } else if (warp < 6) {
     // ---------------------------------------------------------------- dequant
-    // thread -> (column-word cw, 8-row block kc) of the stage; chunk kc of output row n
-    // (= column 8cw + ORDER position) receives rows 8kc..8kc+7.
+    // thread -> rows (2rp, 2rp+1) x column-words 4cg .. 4cg+3 of the stage.  Each packed
+    // word becomes one 16-byte chunk (its 8 columns in order) of the MN-major A tile.
     const int dq = threadIdx.x - 64;
-    const int kc = dq & 7;
-    const int cw = dq >> 3;  // 0..15
+    const int rp = dq >> 2;
+    const int cg = dq & 3;
     int s = 0, sa = 0;
     uint32_t ph = 0, pha = 0;
     bool ok = true;
@@ -282,44 +291,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       for (int kb = 0; kb < KB; ++kb) {
         if (!wait(&full_t[s], ph) || !wait(&empty_a[sa], pha ^ 1u)) { ok = false; break; }
         const uint32_t wb = sbase + W_OFF + s * W_BYTES;
-        uint32_t w[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = lds32p(wb + ((8 * kc + j) * 16 + cw) * 4);
-        const uint32_t zw = lds32p(sbase + Z_OFF + s * 128 + cw * 4);
-        const uint4 s4 = lds128p(sbase + S_OFF + s * 256 + cw * 16);
-        const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
-        // (1024 + zero) in both halves, per nibble; scale of the nibble's column in both
-        uint32_t zp[8], sp[8];
-        {
-          const uint32_t lo = prmt(zw, zw, 0x5410u), hi = prmt(zw, zw, 0x7632u);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            zp[i] = and_or(lo >> (4 * i), 0x000F000Fu, kMagic);
-            zp[i + 4] = and_or(hi >> (4 * i), 0x000F000Fu, kMagic);
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int col = nibble_column(i);
-            sp[i] = prmt(sv[col >> 1], 0u, (col & 1) ? 0x3232u : 0x1010u);
-          }
-        }
-        // v[i][r]: rows (8kc + 2r, +1) of the nibble-i column, exact fp16 weights
-        uint32_t v[8][4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const uint32_t plo = prmt(w[2 * r], w[2 * r + 1], 0x5410u);
-          const uint32_t phi = prmt(w[2 * r], w[2 * r + 1], 0x7632u);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t src = (i < 4 ? plo : phi) >> (4 * (i & 3));
-            v[i][r] = hmul2(hsub2(and_or(src, 0x000F000Fu, kMagic), zp[i]), sp[i]);
-          }
-        }
+        const uint4 r0 = lds128p(wb + (2 * rp) * 64 + cg * 16);
+        const uint4 r1 = lds128p(wb + (2 * rp + 1) * 64 + cg * 16);
+        const uint4 z4 = lds128p(sbase + Z_OFF + s * 128 + cg * 16);
+        const uint32_t w[2][4] = {{r0.x, r0.y, r0.z, r0.w}, {r1.x, r1.y, r1.z, r1.w}};
+        const uint32_t zw[4] = {z4.x, z4.y, z4.z, z4.w};
         const uint32_t ab = sbase + A_OFF + sa * A_BYTES;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int n = 8 * cw + nibble_column(i);  // A row (output column in the tile)
-          sts128(ab + n * 128 + ((kc ^ (n & 7)) << 4), v[i][0], v[i][1], v[i][2], v[i][3]);
+        for (int c = 0; c < 4; ++c) {
+          const int cw = 4 * cg + c;
+          const uint4 s4 = lds128p(sbase + S_OFF + s * 256 + cw * 16);
+          const uint32_t sp[4] = {s4.x, s4.y, s4.z, s4.w};  // (s[2j], s[2j+1])
+          uint32_t zp[4];                                    // (1024+z[2j], 1024+z[2j+1])
+#pragma unroll
+          for (int j = 0; j < 4; ++j) zp[j] = and_or(zw[c] >> (4 * j), 0x000F000Fu, kMagic);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            uint32_t v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              v[j] = hmul2(hsub2(and_or(w[e][c] >> (4 * j), 0x000F000Fu, kMagic), zp[j]), sp[j]);
+            const int k = 2 * rp + e;
+            const int off = ((cw >> 3) * 8 + (k >> 3)) * 1024 + (k & 7) * 128 +
+                            (((cw & 7) ^ (k & 7)) << 4);
+            sts128(ab + off, v[0], v[1], v[2], v[3]);
+          }
         }
         fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
         __syncwarp();
