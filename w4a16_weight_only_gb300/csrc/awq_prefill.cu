@@ -11,15 +11,15 @@
 // tcgen05.mma.kind::f16 (K = 16) per stage, fp32 accumulators in TMEM.  Each dequantized
 // 128 x 64 weight tile therefore feeds 256 activation rows.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over tiles):
+// Warp roles (448 threads, one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer: activation tile (256 x 64 fp16, 128B swizzle), packed weight
 //               tile (64 rows x 16 words), the stage's zero and scale rows -> 4-deep ring
 //   warp 1      TMEM allocation (512 columns = two 128 x 256 fp32 accumulators) and the
 //               single MMA-issuing thread
-//   warps 2-5   dequantize the packed tile into the MN-major, 128B-swizzled fp16 A tile
+//   warps 2-9   dequantize the packed tile into the MN-major, 128B-swizzled fp16 A tile
 //               (one packed word = one 16-byte chunk of 8 adjacent columns, no transpose):
 //               w = (c - z) * s exactly (fp16 exponent trick, HSUB2, HMUL2) -> 2-deep ring
-//   warps 6-9   epilogue: tcgen05.ld (32 lanes x 32 columns), + bias, fp16, store; the
+//   warps 10-13 epilogue: tcgen05.ld (32 lanes x 32 columns), + bias, fp16, store; the
 //               second accumulator lets the next tile's MMAs run meanwhile
 // Every wait is an mbarrier try-wait bounded in wall time; on give-up the kernel sets the
 // device status word, all roles leave their loops, in-flight copies and MMAs are drained
@@ -41,8 +41,9 @@ constexpr int kBN = 128;   // output columns per tile (UMMA M)
 constexpr int kBT = 256;   // activation rows per tile (UMMA N)
 constexpr int kBK = 64;    // K per stage
 constexpr int kST = 4;     // TMA ring depth
-constexpr int kSA = 2;     // dequantized-A ring depth
-constexpr int kThreads = 320;
+constexpr int kSA = 4;     // dequantized-A ring depth
+constexpr int kDQ = 8;                        // dequant warps
+constexpr int kThreads = (2 + kDQ + 4) * 32;  // producer, MMA, dequant, epilogue
 constexpr uint32_t kMagic = 0x64006400u;
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
 constexpr unsigned int kStatusPrefillTimeout = 0x2u;
@@ -61,7 +62,12 @@ constexpr int BAR_OFF = S_OFF + kST * 256;
 constexpr int NBARS = 2 * kST + 2 * kSA + 4 + 1;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base (u32), abort flag (u32)
 constexpr size_t SMEM = 1024 + MISC_OFF + 16;
-constexpr uint32_t STAGE_TX = X_BYTES + W_BYTES + 16 * 4 + 128 * 2;
+#ifdef AWQ_PREFILL_ABL_HALFX
+constexpr int kXRows = kBT / 2;
+#else
+constexpr int kXRows = kBT;
+#endif
+constexpr uint32_t STAGE_TX = kXRows * kBK * 2 + W_BYTES + 16 * 4 + 128 * 2;
 
 struct __align__(64) PrefillParams {
   CUtensorMap tm_x;  // x [M][K] f16, box {64, 256}, 128B swizzle
@@ -147,6 +153,11 @@ __device__ __forceinline__ uint32_t lds32p(uint32_t a) {
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
+__device__ __forceinline__ uint2 lds64p(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
 __device__ __forceinline__ uint4 lds128p(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
@@ -172,14 +183,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int KB = p.K / kBK;  // stages per tile
+#ifdef AWQ_PREFILL_DEBUG_DECL
+  AWQ_PREFILL_DEBUG_DECL
+#endif
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kST; ++s) {
       mbar_init(&full_t[s], 1);
-      mbar_init(&empty_t[s], 4 + 1);  // four dequant warps + one MMA commit
+      mbar_init(&empty_t[s], kDQ + 1);  // dequant warps + one MMA commit
     }
     for (int s = 0; s < kSA; ++s) {
-      mbar_init(&full_a[s], 4);       // four dequant warps
+      mbar_init(&full_a[s], kDQ);     // dequant warps
       mbar_init(&empty_a[s], 1);      // MMA commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -220,7 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int m0 = (tile % p.tiles_t) * kBT;
         const int cw0 = (tile / p.tiles_t) * (kBN / 8);
         for (int kb = 0; kb < KB; ++kb) {
+#ifdef AWQ_PREFILL_DEBUG_ROLE
+          AWQ_PREFILL_DEBUG_ROLE(0, 0);
+#endif
           if (!wait(&empty_t[s], ph ^ 1u)) { ok = false; break; }
+#ifdef AWQ_PREFILL_DEBUG_ROLE
+          AWQ_PREFILL_DEBUG_ROLE(0, 1);
+#endif
           const int k0 = kb * kBK;
           const int grp = k0 / p.G;
           mbar_arrive_expect_tx(&full_t[s], STAGE_TX);
@@ -243,6 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
+#ifdef AWQ_PREFILL_DEBUG_WAIT
+      unsigned long long dbg_t0 = 0;
+#endif
       int s = 0, sa = 0;
       uint32_t ph = 0, pha = 0;
       int li = 0;
@@ -250,11 +273,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       bool any = false;
       for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x, ++li) {
         const int b = li & 1;
+#ifdef AWQ_PREFILL_DEBUG_WAIT
+        AWQ_PREFILL_DEBUG_WAIT(0);
+#endif
         if (!wait(&tempty[b], static_cast<uint32_t>(((li >> 1) & 1) ^ 1))) { ok = false; break; }
+#ifdef AWQ_PREFILL_DEBUG_WAIT
+        AWQ_PREFILL_DEBUG_WAIT(1);
+#endif
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(b * kBT);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!wait(&full_t[s], ph) || !wait(&full_a[sa], pha)) { ok = false; break; }
+#ifdef AWQ_PREFILL_DEBUG_WAIT
+          AWQ_PREFILL_DEBUG_WAIT(2);
+          AWQ_PREFILL_DEBUG_WAIT(3);
+#endif
+          // full_a completes only after every dequant warp has seen full_t[s], so the
+          // activation tile of stage s is in place as well (one wait per stage).
+          if (!wait(&full_a[sa], pha)) { ok = false; break; }
+#ifdef AWQ_PREFILL_DEBUG_WAIT
+          AWQ_PREFILL_DEBUG_WAIT(4);
+#endif
           tc_fence_after();
           const uint64_t adesc = sw128_desc(sbase + A_OFF + sa * A_BYTES, kA_LBO, kA_SBO);
           const uint64_t bdesc = sw128_desc(sbase + X_OFF + s * X_BYTES, 16u, 1024u);
@@ -277,29 +315,48 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 2 + kDQ) {
     // ---------------------------------------------------------------- dequant
-    // thread -> rows (2rp, 2rp+1) x column-words 4cg .. 4cg+3 of the stage.  Each packed
+    // thread -> rows (2rp, 2rp+1) x column-words 2cg, 2cg+1 of the stage.  Each packed
     // word becomes one 16-byte chunk (its 8 columns in order) of the MN-major A tile.
     const int dq = threadIdx.x - 64;
-    const int rp = dq >> 2;
-    const int cg = dq & 3;
+    const int rp = dq >> 3;
+    const int cg = dq & 7;
     int s = 0, sa = 0;
     uint32_t ph = 0, pha = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
       for (int kb = 0; kb < KB; ++kb) {
-        if (!wait(&full_t[s], ph) || !wait(&empty_a[sa], pha ^ 1u)) { ok = false; break; }
+#ifdef AWQ_PREFILL_DEBUG_ROLE
+        AWQ_PREFILL_DEBUG_ROLE(1, 0);
+#endif
+        if (!wait(&full_t[s], ph)) { ok = false; break; }
+#ifdef AWQ_PREFILL_DEBUG_ROLE
+        AWQ_PREFILL_DEBUG_ROLE(1, 1);
+#endif
+        if (!wait(&empty_a[sa], pha ^ 1u)) { ok = false; break; }
+#ifdef AWQ_PREFILL_DEBUG_ROLE
+        AWQ_PREFILL_DEBUG_ROLE(1, 2);
+#endif
         const uint32_t wb = sbase + W_OFF + s * W_BYTES;
-        const uint4 r0 = lds128p(wb + (2 * rp) * 64 + cg * 16);
-        const uint4 r1 = lds128p(wb + (2 * rp + 1) * 64 + cg * 16);
-        const uint4 z4 = lds128p(sbase + Z_OFF + s * 128 + cg * 16);
-        const uint32_t w[2][4] = {{r0.x, r0.y, r0.z, r0.w}, {r1.x, r1.y, r1.z, r1.w}};
-        const uint32_t zw[4] = {z4.x, z4.y, z4.z, z4.w};
+#ifdef AWQ_PREFILL_ABL_NODQ
+        if (true) {
+          __syncwarp();
+          if (lane == 0) { mbar_arrive(&full_a[sa]); mbar_arrive(&empty_t[s]); }
+          if (++s == kST) { s = 0; ph ^= 1u; }
+          if (++sa == kSA) { sa = 0; pha ^= 1u; }
+          continue;
+        }
+#endif
+        const uint2 r0 = lds64p(wb + (2 * rp) * 64 + cg * 8);
+        const uint2 r1 = lds64p(wb + (2 * rp + 1) * 64 + cg * 8);
+        const uint2 z2 = lds64p(sbase + Z_OFF + s * 128 + cg * 8);
+        const uint32_t w[2][2] = {{r0.x, r0.y}, {r1.x, r1.y}};
+        const uint32_t zw[2] = {z2.x, z2.y};
         const uint32_t ab = sbase + A_OFF + sa * A_BYTES;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int cw = 4 * cg + c;
+        for (int c = 0; c < 2; ++c) {
+          const int cw = 2 * cg + c;
           const uint4 s4 = lds128p(sbase + S_OFF + s * 256 + cw * 16);
           const uint32_t sp[4] = {s4.x, s4.y, s4.z, s4.w};  // (s[2j], s[2j+1])
           uint32_t zp[4];                                    // (1024+z[2j], 1024+z[2j+1])
@@ -323,6 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           mbar_arrive(&full_a[sa]);
           mbar_arrive(&empty_t[s]);
         }
+#ifdef AWQ_PREFILL_DEBUG_ROLE
+        AWQ_PREFILL_DEBUG_ROLE(1, 3);
+#endif
         if (++s == kST) { s = 0; ph ^= 1u; }
         if (++sa == kSA) { sa = 0; pha ^= 1u; }
       }
@@ -395,7 +455,7 @@ cudaError_t launch_prefill(const GemmProblem& p) {
   const char* why = nullptr;
   const int C = p.N / 8;
   const int ngrp = p.K / p.G;
-  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kBK, kBT,
+  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kBK, kXRows,
                     CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
       !make_tmap_2d(&pp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, 16, kBK,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
