@@ -5,13 +5,15 @@
 // (tensref.org/formats/awq, "Reader"; GPTQModel wiki "AWQ", "Native GEMM": fused
 // dequant-GEMM, fp32 accumulation, split over K.)
 //
-// Streaming.  Every warp owns a contiguous run of 64-row stages of one column tile and
-// streams it through its own two-slot shared-memory ring: lane 0 issues the bulk tensor
-// copies (packed weights, the stage's zero and scale rows, the activations) on an
-// mbarrier, the warp waits with a bounded try-wait, computes, and refills the slot.  The
-// weight copies are issued before the kernel waits on the preceding grid (programmatic
-// dependent launch): only the activation copy and the output stores are ordered after
-// it, so the weight stream of one linear overlaps the tail of the previous kernel.
+// Streaming.  Every warp owns a contiguous run of 64-row stages of one column tile (16
+// packed words, 64-byte rows) and streams it through its own ring of S slots (S set at
+// launch from the shared memory each CTA gets): lane 0 issues the bulk tensor copies
+// (packed weights, the group's zero and scale rows when a stage opens a group, the
+// activations) on the slot's mbarrier, the warp waits with a bounded try-wait, computes,
+// and refills the slot.  The weight copies are issued before the kernel waits on the
+// preceding grid (programmatic dependent launch): only the activation copies and the
+// output stores are ordered after it, so the weight stream of one linear overlaps the
+// tail of the previous kernel.
 //
 // Unpack (kSub mode, up to 16 activation rows).  Two rows (k, k+1) of one packed column
 // are byte-permuted (prmt) so each 16-bit half holds one row's nibbles; one AND per
@@ -29,10 +31,14 @@
 // the output sums.)
 //
 // Split-K: the warps of a CTA and the CTAs of a thread-block cluster take consecutive K
-// ranges; partial sums are reduced in a fixed order through shared memory and then
-// distributed shared memory (no global workspace, no atomics), so repeated calls are
-// bitwise identical.
+// ranges.  Each CTA sums its warps' partials in a fixed order in shared memory and pushes
+// the result (st.async into distributed shared memory, counted on an mbarrier) to the
+// cluster's rank-0 CTA, which adds the partials in rank order, adds the bias and stores
+// y; the other CTAs exit right after their push.  No global workspace, no atomics:
+// repeated calls are bitwise identical.
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "awq_internal.cuh"
 #include "awq_ptx.cuh"
@@ -59,31 +65,25 @@ struct __align__(64) TmaDecodeParams {
   __half* y;
   unsigned int* status;
   int M, K, N, C, G;
-  int x_rows;  // rows of the activation box: min(M, 8*TB)
+  int x_rows;   // rows of the activation box: min(M, 8*TB)
+  int slots;    // ring slots per warp
+  int x_pitch;  // bytes per activation slot: 128 (one row, unswizzled) or 1024*TB
+  // Byte offsets inside the 1024-aligned dynamic shared memory (activation rings at 0).
+  int w_off, m_off, zl_off, bias_off, bar_off, recv_off;
 };
 
 template <int TB, int CWL>
 struct Geo {
   static constexpr int CW_W = 8 * CWL;              // packed column-words per warp / CTA
   static constexpr int W_BYTES = kRS * CW_W * 4;    // packed weight tile per stage
-  static constexpr int SLOTS = TB == 4 ? 2 : 3;     // ring slots per warp
-  static constexpr int X_BYTES = 8 * TB * kRS * 2;  // activation tile per stage (max)
   static constexpr int Z_BYTES = CW_W * 4;
   static constexpr int S_BYTES = 8 * CW_W * 2;
-  static constexpr int X_OFF = W_BYTES;             // both multiples of 1024
-  static constexpr int Z_OFF = W_BYTES + X_BYTES;
-  static constexpr int S_OFF = Z_OFF + 128;
-  static constexpr int SLOT = ((S_OFF + S_BYTES + 1023) / 1024) * 1024;
+  static constexpr int META_SLOT = ((128 + S_BYTES + 127) / 128) * 128;  // zeros at 0, scales at 128
   static constexpr uint32_t META_TX = Z_BYTES + S_BYTES;
   static constexpr int NMMA = 4 * CWL;
   static constexpr int E = NMMA * TB * 4 * 32;      // partial sums per warp
-  static constexpr int RING = kNW * SLOTS * SLOT;   // all warps' rings
-  static constexpr int ZERO_OFF = RING;              // one 128-byte zero line per warp
-  static constexpr int BIAS_OFF = RING + kNW * 128;  // bias of the CTA's columns (fp32)
-  static constexpr int COUNT_OFF = BIAS_OFF + 8 * CW_W * 4;  // per-warp counters
-  static constexpr int BAR_OFF = COUNT_OFF + kNW * 4 + 16;
-  static constexpr size_t SMEM = 1024 + (size_t)BAR_OFF + kNW * SLOTS * 8 + 8;
-  static_assert((size_t)(kNW * E + E + kMaxCluster) * 4 <= (size_t)RING, "reduction buffers");
+  static constexpr int PACK = 8 * TB * 8 * CW_W;    // packed partial: tokens x columns
+  static constexpr int RED_BYTES = (kNW * E + PACK) * 4;  // reuses the activation+weight rings
 };
 
 // Packed column-word (within the lane's CWL words) and nibble that feed A row g (rs = 0)
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(kNW * 32, 3)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kSlots = GE::SLOTS;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + GE::BAR_OFF);
+  const int S = p.slots;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -142,23 +142,35 @@ __global__ void __launch_bounds__(kNW * 32, 3)
   const int j0 = static_cast<int>(TS * wid / P);
   const int j1 = static_cast<int>(TS * (wid + 1) / P);
 
-  unsigned char* my_slots = smem + (size_t)warp * kSlots * GE::SLOT;
-  uint64_t* my_bars = bars + warp * kSlots;
-  const uint32_t slots_u32 = smem_u32(my_slots);
+  unsigned char* x_ring = smem + (size_t)warp * S * p.x_pitch;
+  unsigned char* w_ring = smem + p.w_off + (size_t)warp * S * GE::W_BYTES;
+  unsigned char* m_ring = smem + p.m_off + (size_t)warp * S * GE::META_SLOT;
+  uint64_t* my_bars = bars + warp * S;
+  const uint32_t x_ring_u32 = smem_u32(x_ring);
+  const uint32_t w_ring_u32 = smem_u32(w_ring);
+  const uint32_t m_ring_u32 = smem_u32(m_ring);
 
 #ifdef AWQ_DECODE_DEBUG_TIME
   AWQ_DECODE_DEBUG_TIME(0);
 #endif
-  // Reduction mbarrier (after all ring barriers): counts the bytes other CTAs push here.
-  uint64_t* red_bar = bars + kNW * kSlots;
+  // Reduction mbarrier (after all ring barriers): in the cluster's rank-0 CTA it counts
+  // the bytes of the partial sums every CTA of the cluster pushes (its own included).
+  uint64_t* red_bar = bars + kNW * S;
+  const int pack_n = p.x_rows * 8 * GE::CW_W;  // floats of one packed partial
   if (lane == 0) {
     prefetch_tmap(&p.tm_w);
     prefetch_tmap(&p.tm_x);
-    for (int s = 0; s < kSlots; ++s) mbar_init(&my_bars[s], 1);
-    if (warp == 0) mbar_init(red_bar, 1);
+    for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
+    if (warp == 0) {
+      mbar_init(red_bar, 1);
+      if (rank == 0) mbar_arrive_expect_tx(red_bar, cs * static_cast<uint32_t>(pack_n) * 4u);
+    }
     fence_mbar_init();
   }
   __syncwarp();
+  // Publish the barrier initialisation to the cluster; the matching wait comes right
+  // before the first push, long after every CTA has arrived here.
+  cluster_arrive_relaxed();
 
   // Stage j of this warp: packed weights always, the group's zero and scale rows only when
   // stage j opens a group (or is the warp's first stage), activations separately.
@@ -168,14 +180,13 @@ __global__ void __launch_bounds__(kNW * 32, 3)
   int iss_grp = j0 / spg;
   int iss_left = spg - (j0 - iss_grp * spg);  // stages left in iss_grp, counting the next
   auto issue_weights = [&](int slot, int j) {
-    unsigned char* b = my_slots + slot * GE::SLOT;
     uint64_t* bar = &my_bars[slot];
     const bool meta = (j == j0) || (iss_left == spg);
     mbar_arrive_expect_tx(bar, GE::W_BYTES + x_tx + (meta ? GE::META_TX : 0u));
-    tma_load_2d(b, &p.tm_w, bar, cw0, j * kRS);
+    tma_load_2d(w_ring + slot * GE::W_BYTES, &p.tm_w, bar, cw0, j * kRS);
     if (meta) {
-      tma_load_2d(b + GE::Z_OFF, &p.tm_z, bar, cw0, iss_grp);
-      tma_load_2d(b + GE::S_OFF, &p.tm_s, bar, 8 * cw0, iss_grp);
+      tma_load_2d(m_ring + slot * GE::META_SLOT, &p.tm_z, bar, cw0, iss_grp);
+      tma_load_2d(m_ring + slot * GE::META_SLOT + 128, &p.tm_s, bar, 8 * cw0, iss_grp);
     }
     if (--iss_left == 0) {
       ++iss_grp;
@@ -183,17 +194,19 @@ __global__ void __launch_bounds__(kNW * 32, 3)
     }
   };
   auto issue_x = [&](int slot, int j) {
-    tma_load_2d(my_slots + slot * GE::SLOT + GE::X_OFF, &p.tm_x, &my_bars[slot], j * kRS, m0);
+    tma_load_2d(x_ring + slot * p.x_pitch, &p.tm_x, &my_bars[slot], j * kRS, m0);
   };
 
   // Weights do not depend on the preceding grid: stream them first.  Activations (and the
   // output stores at the end) are ordered after it.
   if (lane == 0)
-    for (int s = 0; s < kSlots && j0 + s < j1; ++s) issue_weights(s, j0 + s);
+    for (int s = 0; s < S && j0 + s < j1; ++s) issue_weights(s, j0 + s);
   grid_dependency_wait();
   if (lane == 0)
-    for (int s = 0; s < kSlots && j0 + s < j1; ++s) issue_x(s, j0 + s);
+    for (int s = 0; s < S && j0 + s < j1; ++s) issue_x(s, j0 + s);
+#if !AWQ_DECODE_LATE_TRIGGER
   launch_dependents();
+#endif
 
   // Per-lane shared-memory offsets inside a slot.  Packed words of lane (g8, q):
   // column-words g8*CWL .. +CWL-1, rows r = 0,1 -> 2q + {0,1} and r = 2,3 -> 2q + 8 + {0,1}
@@ -209,12 +222,12 @@ __global__ void __launch_bounds__(kNW * 32, 3)
   // ldmatrix row addresses for the activation tile (128-byte rows, 128B swizzle): lane l
   // addresses row (l & 7) of 16-byte chunk 4*pair + (l >> 3).  Rows past the activation
   // box (fewer than 8 tokens) read this warp's zero line instead.
-  const uint32_t zero_line = smem_u32(smem + GE::ZERO_OFF + warp * 128);
-  if (lane < 32) reinterpret_cast<uint32_t*>(smem + GE::ZERO_OFF + warp * 128)[lane] = 0u;
+  const uint32_t zero_line = smem_u32(smem + p.zl_off + warp * 128);
+  if (lane < 32) reinterpret_cast<uint32_t*>(smem + p.zl_off + warp * 128)[lane] = 0u;
   __syncwarp();
   // Bias of this CTA's columns, read now (off the critical path) for the epilogue.
   {
-    float* bias_s = reinterpret_cast<float*>(smem + GE::BIAS_OFF);
+    float* bias_s = reinterpret_cast<float*>(smem + p.bias_off);
     for (int i = threadIdx.x; i < 8 * GE::CW_W; i += kNW * 32) {
       const int n = 8 * cw0 + i;
       bias_s[i] = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
@@ -230,7 +243,7 @@ __global__ void __launch_bounds__(kNW * 32, 3)
     for (int pr = 0; pr < 2; ++pr) {
       const int chunk = 4 * pr + (lane >> 3);
       x_off[tb][pr] = x_real[tb]
-                          ? static_cast<uint32_t>(GE::X_OFF + (8 * tb + rr) * 128 + ((chunk ^ rr) << 4))
+                          ? static_cast<uint32_t>((8 * tb + rr) * 128 + ((chunk ^ rr) << 4))
                           : static_cast<uint32_t>(chunk << 4);
     }
   }
@@ -304,7 +317,9 @@ __global__ void __launch_bounds__(kNW * 32, 3)
     if (j == j0) AWQ_DECODE_DEBUG_TIME(1);
     if (j == j1 - 1) AWQ_DECODE_DEBUG_TIME(4);
 #endif
-    const uint32_t sb = slots_u32 + slot * GE::SLOT;
+    const uint32_t xb = x_ring_u32 + slot * p.x_pitch;
+    const uint32_t wb = w_ring_u32 + slot * GE::W_BYTES;
+    const uint32_t mb = m_ring_u32 + slot * GE::META_SLOT;
     if (grp_left == 0) {
       ++grp_of;
       grp_left = spg;
@@ -316,8 +331,8 @@ __global__ void __launch_bounds__(kNW * 32, 3)
       cur = grp;
 #pragma unroll
       for (int c = 0; c < CWL; ++c) {
-        zw[c] = lds32(sb + GE::Z_OFF + (g8 * CWL + c) * 4);
-        const uint4 s4 = lds128(sb + GE::S_OFF + (g8 * CWL + c) * 16);
+        zw[c] = lds32(mb + (g8 * CWL + c) * 4);
+        const uint4 s4 = lds128(mb + 128 + (g8 * CWL + c) * 16);
         sv[c][0] = s4.x; sv[c][1] = s4.y; sv[c][2] = s4.z; sv[c][3] = s4.w;
       }
       if (kSub) {
@@ -355,14 +370,14 @@ __global__ void __launch_bounds__(kNW * 32, 3)
       uint32_t xr[TB][4];
 #pragma unroll
       for (int tb = 0; tb < TB; ++tb)
-        ldmatrix_x4(xr[tb], (x_real[tb] ? sb : zero_line) + x_off[tb][pr]);
+        ldmatrix_x4(xr[tb], (x_real[tb] ? xb : zero_line) + x_off[tb][pr]);
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int ks = 2 * pr + kk;
         uint32_t w[4][CWL];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const uint32_t a = sb + w_off[r] + ks * 16 * GE::CW_W * 4;
+          const uint32_t a = wb + w_off[r] + ks * 16 * GE::CW_W * 4;
           if constexpr (CWL == 2) {
             const uint2 v = lds64(a);
             w[r][0] = v.x;
@@ -424,11 +439,11 @@ __global__ void __launch_bounds__(kNW * 32, 3)
       }
     }
     __syncwarp();
-    if (lane == 0 && j + kSlots < j1) {
-      issue_weights(slot, j + kSlots);
-      issue_x(slot, j + kSlots);
+    if (lane == 0 && j + S < j1) {
+      issue_weights(slot, j + S);
+      issue_x(slot, j + S);
     }
-    if (++slot == kSlots) {
+    if (++slot == S) {
       slot = 0;
       parity ^= 1u;
     }
@@ -436,10 +451,10 @@ __global__ void __launch_bounds__(kNW * 32, 3)
   if (kSub && cur >= 0 && !failed) fold();
   if (failed) {
     // Let copies already issued land (bounded) before the slots are reused below.
-    const int issued_end = min(j1, done + kSlots);
+    const int issued_end = min(j1, done + S);
     for (int j = done; j < issued_end; ++j) {
-      const int slot = (j - j0) % kSlots;
-      const uint32_t parity = static_cast<uint32_t>(((j - j0) / kSlots) & 1);
+      const int slot = (j - j0) % S;
+      const uint32_t parity = static_cast<uint32_t>(((j - j0) / S) & 1);
       mbar_wait_bounded(&my_bars[slot], parity, p.status, kStatusDecodeTimeout, kWaitLimitNs);
     }
   }
@@ -447,17 +462,14 @@ __global__ void __launch_bounds__(kNW * 32, 3)
 #ifdef AWQ_DECODE_DEBUG_TIME
   AWQ_DECODE_DEBUG_TIME(2);
 #endif
-  // Reduce: warps of the CTA (fixed order), then CTAs of the cluster (fixed order).
-  // Each thread signals the cluster as soon as its ring is idle, so the barrier wait below
-  // overlaps the CTA-level sum; partials are then pushed into the owning CTA's shared
-  // memory (no round-trip loads) and summed there after one more barrier.
-  // This CTA's ring is idle: all its copies were waited for and its fragment reads are
-  // consumed.  (red_bar's initialisation was published by the init fence at the start.)
-  cluster_arrive_relaxed();
-#ifdef AWQ_DECODE_DEBUG_TIME
-  AWQ_DECODE_DEBUG_TIME(5);
+#if AWQ_DECODE_LATE_TRIGGER
+  launch_dependents();
 #endif
-  __syncthreads();           // the ring is reused as the reduction buffer
+  // Reduce: the warps of the CTA in a fixed order into a packed partial [token][column],
+  // pushed (st.async, counted on the rank-0 CTA's mbarrier) into the rank-0 CTA, which
+  // adds the cluster's partials in rank order, adds the bias and stores y.  Other CTAs
+  // exit right after their push.
+  __syncthreads();  // the ring is reused as the reduction buffer
   float* red = reinterpret_cast<float*>(smem);
   float* mine = red + warp * GE::E;
 #pragma unroll
@@ -467,69 +479,50 @@ __global__ void __launch_bounds__(kNW * 32, 3)
 #pragma unroll
       for (int e = 0; e < 4; ++e) mine[((mi * TB + tb) * 4 + e) * 32 + lane] = acc[mi][tb][e];
   __syncthreads();
-  // Output element e (warp-fragment order): token and column, valid when both exist.
-  auto token_of = [&](int e) { return m0 + 8 * ((e >> 7) % TB) + 2 * (e & 3) + ((e >> 5) & 1); };
-  auto col_of = [&](int e) {  // column offset inside the CTA tile
+  // Output element e (warp-fragment order): token and column inside the CTA tile.
+  auto token_of = [&](int e) { return 8 * ((e >> 7) % TB) + 2 * (e & 3) + ((e >> 5) & 1); };
+  auto col_of = [&](int e) {
     const int mi = (e >> 7) / TB, rs = ((e >> 5) & 3) >> 1;
     return (((e & 31) >> 2) * CWL + mma_cw<CWL>(mi, rs)) * 8 + nibble_column(mma_nib<CWL>(mi, rs));
   };
-  auto valid = [&](int e) { return token_of(e) < p.M && cw0 + (col_of(e) >> 3) < p.C; };
-  constexpr int kPer = (GE::E + kNW * 32 - 1) / (kNW * 32);
-  const int slice = (GE::E + static_cast<int>(cs) - 1) / static_cast<int>(cs);
-  const int my_lo = static_cast<int>(rank) * slice;
-  const int my_hi = min(GE::E, my_lo + slice);
-  float part[kPer];
-  int my_count = 0;  // this thread's share of the valid elements of this CTA's slice
+  float* pack = red + kNW * GE::E;
+  for (int e = threadIdx.x; e < GE::E; e += kNW * 32) {
+    const int t = token_of(e);
+    if (t >= p.x_rows) continue;
+    float v = 0.f;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = threadIdx.x + i * kNW * 32;
-    part[i] = 0.f;
-    if (e < GE::E && valid(e)) {
-#pragma unroll
-      for (int w = 0; w < kNW; ++w) part[i] += red[w * GE::E + e];
-    }
-    my_count += (e >= my_lo && e < my_hi && valid(e)) ? 1 : 0;
-  }
-  // Valid elements of the slice (each arrives from cs CTAs): warp sums, then warp 0.
-  int* counts = reinterpret_cast<int*>(smem + GE::COUNT_OFF);
-  float* recv = red + kNW * GE::E;  // [cs][slice], disjoint from red
-  {
-    const int wsum = __reduce_add_sync(0xffffffffu, my_count);
-    if (lane == 0) counts[warp] = wsum;
+    for (int w = 0; w < kNW; ++w) v += red[w * GE::E + e];
+    pack[t * 8 * GE::CW_W + col_of(e)] = v;
   }
   __syncthreads();
-  int mine_valid = 0;
-#pragma unroll
-  for (int w = 0; w < kNW; ++w) mine_valid += counts[w];
 #ifdef AWQ_DECODE_DEBUG_TIME
   AWQ_DECODE_DEBUG_TIME(6);
 #endif
-  if (threadIdx.x == 0)
-    mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(mine_valid) * cs * 4u);
-  cluster_wait_acquire();  // every CTA of the cluster is past its main loop
+  float* recv = reinterpret_cast<float*>(smem + p.recv_off);
+  cluster_wait_acquire();  // rank 0's receive barrier is initialised
 #ifdef AWQ_DECODE_DEBUG_TIME
   AWQ_DECODE_DEBUG_TIME(7);
 #endif
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = threadIdx.x + i * kNW * 32;
-    if (e < GE::E && valid(e)) {
-      const int owner = e / slice;
-      st_async_dsmem_f32(recv + rank * slice + (e - owner * slice), red_bar,
-                         static_cast<uint32_t>(owner), part[i]);
-    }
+  for (int v = threadIdx.x; v < pack_n / 4; v += kNW * 32)
+    st_async_dsmem_v4(recv + rank * pack_n + 4 * v, red_bar, 0u,
+                      *reinterpret_cast<const float4*>(pack + 4 * v));
+  if (rank != 0) {
+#ifdef AWQ_DECODE_DEBUG_TIME
+    AWQ_DECODE_DEBUG_TIME(3);
+#endif
+    return;
   }
   const bool got = mbar_wait_bounded(red_bar, 0u, p.status, kStatusDecodeTimeout, kWaitLimitNs);
 #ifdef AWQ_DECODE_DEBUG_TIME
-  AWQ_DECODE_DEBUG_TIME(1);
+  AWQ_DECODE_DEBUG_TIME(8);
 #endif
-  const float* bias_s = reinterpret_cast<const float*>(smem + GE::BIAS_OFF);
-  for (int e = my_lo + threadIdx.x; got && e < my_hi; e += kNW * 32) {
-    if (!valid(e)) continue;
+  const float* bias_s = reinterpret_cast<const float*>(smem + p.bias_off);
+  for (int i = threadIdx.x; got && i < pack_n; i += kNW * 32) {
+    const int t = i / (8 * GE::CW_W), col = i - t * 8 * GE::CW_W;
+    if (m0 + t >= p.M || 8 * cw0 + col >= p.N) continue;
     float sum = 0.f;
-    for (uint32_t r = 0; r < cs; ++r) sum += recv[r * slice + (e - my_lo)];
-    const int col = col_of(e);
-    p.y[(long long)token_of(e) * p.N + 8 * cw0 + col] = __float2half_rn(sum + bias_s[col]);
+    for (uint32_t r = 0; r < cs; ++r) sum += recv[r * pack_n + i];
+    p.y[(long long)(m0 + t) * p.N + 8 * cw0 + col] = __float2half_rn(sum + bias_s[col]);
   }
 #ifdef AWQ_DECODE_DEBUG_TIME
   AWQ_DECODE_DEBUG_TIME(3);
@@ -547,64 +540,187 @@ Variant pick(const GemmProblem& p) {
   return Variant{4, 1, false};
 }
 
-// Largest number of co-resident clusters of each size (index = cluster size), measured
-// once per kernel variant with the occupancy API.
-template <int TB, int CWL, bool S>
-const int* cluster_capacity() {
+constexpr int kRecvCap = 64 * 1024;  // bytes of the rank-0 receive region
+// Launch-plan limits (compile-time; overridable for tuning builds).
+#ifndef AWQ_DECODE_LATE_TRIGGER
+#define AWQ_DECODE_LATE_TRIGGER 0
+#endif
+#ifndef AWQ_DECODE_WIDE_X
+#define AWQ_DECODE_WIDE_X 0
+#endif
+#ifndef AWQ_DECODE_MAX_SLOTS
+#define AWQ_DECODE_MAX_SLOTS 4
+#endif
+#ifndef AWQ_DECODE_WAVE_FILL_PCT
+#define AWQ_DECODE_WAVE_FILL_PCT 90
+#endif
+#ifndef AWQ_DECODE_MAX_CTAS_PER_SM
+#define AWQ_DECODE_MAX_CTAS_PER_SM 2
+#endif
+constexpr int kMaxSlots = AWQ_DECODE_MAX_SLOTS;             // ring slots per warp
+constexpr int kWaveFillPct = AWQ_DECODE_WAVE_FILL_PCT;      // share of the slots one wave may fill
+constexpr int kMaxCtasPerSm = AWQ_DECODE_MAX_CTAS_PER_SM;   // CTAs of one launch per SM
+
+// Cluster size, ring depth and shared memory layout of one launch.
+struct Plan {
+  int cs = 0, slots = 0, x_pitch = 0;
+  int w_off = 0, m_off = 0, zl_off = 0, bias_off = 0, bar_off = 0, recv_off = 0, smem = 0;
+};
+
+template <int TB, int CWL>
+Plan layout(int cs, int slots, int x_rows) {
   using GE = Geo<TB, CWL>;
-  static int cap[kMaxCluster + 1] = {};
-  static std::once_flag once;
-  std::call_once(once, [] {
-    auto kern = decode_tma_kernel<TB, CWL, S>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(GE::SMEM)) != cudaSuccess)
-      return;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    for (int cs = 1; cs <= kMaxCluster; ++cs) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(cs, 1, 1);
-      cfg.blockDim = dim3(kNW * 32, 1, 1);
-      cfg.dynamicSmemBytes = GE::SMEM;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = cs;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
-      cap[cs] = n;
-    }
-    (void)cudaGetLastError();
-  });
-  return cap;
+  Plan pl;
+  pl.cs = cs;
+  pl.slots = slots;
+  pl.x_pitch = (x_rows == 1 && !AWQ_DECODE_WIDE_X) ? 128 : 1024 * TB;
+  pl.w_off = kNW * slots * pl.x_pitch;
+  pl.m_off = pl.w_off + kNW * slots * GE::W_BYTES;
+  pl.zl_off = pl.m_off + kNW * slots * GE::META_SLOT;
+  pl.bias_off = pl.zl_off + kNW * 128;
+  pl.bar_off = pl.bias_off + 8 * GE::CW_W * 4;
+  pl.recv_off = ((pl.bar_off + (kNW * slots + 1) * 8 + 15) / 16) * 16;
+  pl.smem = 1024 + pl.recv_off + cs * x_rows * 8 * GE::CW_W * 4;
+  return pl;
 }
 
-// Cluster size: the largest resident CTA count in one wave, each warp keeping at least one
-// 64-row stage; ties go to the smaller cluster (less reduction traffic).
-int choose_cluster(long long tiles, int ts, const int* cap) {
-  int best = 1;
-  long long best_resident = -1;
+struct DevLimits {
+  int sms = 0, smem_per_sm = 0, smem_optin = 0, reserved = 0;
+};
+
+cudaError_t dev_limits(DevLimits* out) {
+  static std::mutex mu;
+  static DevLimits cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  DevLimits& d = cache[dev];
+  if (d.sms == 0) {
+    DevLimits t;
+    e = cudaDeviceGetAttribute(&t.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&t.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&t.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&t.reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return e;
+    d = t;
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+// Co-resident clusters of size cs at `smem` bytes per CTA (occupancy API).
+template <int TB, int CWL, bool S>
+int max_clusters(int cs, int smem) {
+  auto kern = decode_tma_kernel<TB, CWL, S>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, 1, 1);
+  cfg.blockDim = dim3(kNW * 32, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  return n;
+}
+
+// Plan: the cluster size giving the largest grid that is resident in one wave while
+// leaving some slots free (the next kernel's clusters can start while this one drains),
+// each warp keeping at least one 64-row stage; ties go to the smaller cluster.  Ring
+// depth: as many slots as the shared memory left per CTA allows, up to the warp's stage
+// count.  Cached per shape.
+template <int TB, int CWL, bool S>
+cudaError_t plan_for(const GemmProblem& p, Plan* out) {
+  using GE = Geo<TB, CWL>;
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int>, Plan> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
+  const int C = p.N / 8;
+  const int nt = (C + GE::CW_W - 1) / GE::CW_W;
+  const long long mz = (p.M + 8 * TB - 1) / (8 * TB);
+  const auto key = std::make_tuple(dev, p.K, nt * (int)mz, x_rows);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  DevLimits dl;
+  e = dev_limits(&dl);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    auto kern = decode_tma_kernel<TB, CWL, S>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dl.smem_optin);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const long long tiles = (long long)nt * mz;
+  const int TS = p.K / kRS;
+  const int x_pitch = (x_rows == 1 && !AWQ_DECODE_WIDE_X) ? 128 : 1024 * TB;
+  const int red_slots = (GE::RED_BYTES + kNW * (x_pitch + GE::W_BYTES) - 1) / (kNW * (x_pitch + GE::W_BYTES));
+  Plan best;
+  long long best_grid = -1;
   for (int cs = 1; cs <= kMaxCluster; ++cs) {
-    if (cap[cs] <= 0) continue;
-    if ((long long)cs * kNW > ts && cs > 1) break;
+    if (cs > 1 && cs * kNW > TS) break;
+    if ((long long)cs * x_rows * 8 * GE::CW_W * 4 > kRecvCap) break;
     const long long grid = tiles * cs;
-    const long long slots = (long long)cap[cs] * cs;
-    const long long resident = grid <= slots ? grid : -1;  // single wave only
-    if (resident > best_resident) {
-      best_resident = resident;
-      best = cs;
+    long long per_sm = (grid + dl.sms - 1) / dl.sms;
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > kMaxCtasPerSm && cs > 1) continue;
+    const int budget = static_cast<int>(dl.smem_per_sm / per_sm) - dl.reserved - 256;
+    const int spw = (TS + cs * kNW - 1) / (cs * kNW);  // stages of the busiest warp
+    int slots = spw < kMaxSlots ? spw : kMaxSlots;
+    while (slots > 1 && layout<TB, CWL>(cs, slots, x_rows).smem > budget) --slots;
+    if (slots < red_slots) slots = red_slots;
+    Plan pl = layout<TB, CWL>(cs, slots, x_rows);
+    if (pl.smem > dl.smem_optin) continue;
+    // single wave with slack, checked against the occupancy API at this size
+    bool fits = false;
+    while (true) {
+      long long cap = (long long)max_clusters<TB, CWL, S>(cs, pl.smem) * cs;
+      if (cap > (long long)kMaxCtasPerSm * dl.sms) cap = (long long)kMaxCtasPerSm * dl.sms;
+      if (grid * 100 <= cap * kWaveFillPct) { fits = true; break; }
+      if (pl.slots <= red_slots || pl.slots <= 1) break;
+      pl = layout<TB, CWL>(cs, pl.slots - 1, x_rows);
+    }
+    if (!fits && cs > 1) continue;
+    const long long score = fits ? grid : 0;
+    if (score > best_grid) {
+      best_grid = score;
+      best = pl;
     }
   }
-  return best;
+  if (best.cs == 0) return cudaErrorInvalidConfiguration;
+  cache[key] = best;
+  *out = best;
+  return cudaSuccess;
 }
 
 template <int TB, int CWL, bool S>
 cudaError_t launch_v(const GemmProblem& p) {
   using GE = Geo<TB, CWL>;
-  const int* cap = cluster_capacity<TB, CWL, S>();
-  if (cap[1] <= 0) return cudaErrorInvalidConfiguration;
+  Plan pl;
+  cudaError_t e = plan_for<TB, CWL, S>(p, &pl);
+  if (e != cudaSuccess) return e;
+  const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
 
   TmaDecodeParams dp;
   const char* why = nullptr;
@@ -612,8 +728,8 @@ cudaError_t launch_v(const GemmProblem& p) {
   const int ngrp = p.K / p.G;
   if (!make_tmap_2d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, GE::CW_W, kRS,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
-      !make_tmap_2d(&dp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kRS,
-                    p.M < 8 * TB ? p.M : 8 * TB, CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
+      !make_tmap_2d(&dp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kRS, x_rows,
+                    (x_rows == 1 && !AWQ_DECODE_WIDE_X) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
       !make_tmap_2d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, GE::CW_W, 1,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
       !make_tmap_2d(&dp.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.sc, p.N, ngrp, 8 * GE::CW_W, 1,
@@ -621,23 +737,25 @@ cudaError_t launch_v(const GemmProblem& p) {
     return cudaErrorInvalidValue;
   dp.bias = p.bias;
   dp.y = p.y;
-  cudaError_t e = status_word_ptr(&dp.status);
+  e = status_word_ptr(&dp.status);
   if (e != cudaSuccess) return e;
   dp.M = p.M; dp.K = p.K; dp.N = p.N; dp.C = C; dp.G = p.G;
-  dp.x_rows = p.M < 8 * TB ? p.M : 8 * TB;
+  dp.x_rows = x_rows;
+  dp.slots = pl.slots;
+  dp.x_pitch = pl.x_pitch;
+  dp.w_off = pl.w_off; dp.m_off = pl.m_off; dp.zl_off = pl.zl_off;
+  dp.bias_off = pl.bias_off; dp.bar_off = pl.bar_off; dp.recv_off = pl.recv_off;
 
   const int nt = (C + GE::CW_W - 1) / GE::CW_W;
   const int mz = (p.M + 8 * TB - 1) / (8 * TB);
-  const int cs = choose_cluster((long long)nt * mz, p.K / kRS, cap);
-
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(nt * cs), static_cast<unsigned>(mz), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(nt * pl.cs), static_cast<unsigned>(mz), 1);
   cfg.blockDim = dim3(kNW * 32, 1, 1);
-  cfg.dynamicSmemBytes = GE::SMEM;
+  cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
   cfg.stream = p.stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.x = pl.cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -67,6 +67,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Suspend-time hint (ns) of the polling try-wait in mbar_wait_bounded; 0 polls with the
+// plain try-wait (hardware-chosen suspend time).
+#ifndef AWQ_MBAR_SUSPEND_HINT_NS
+#define AWQ_MBAR_SUSPEND_HINT_NS 20000u
+#endif
+
 // Waits for phase `parity` of `bar`, giving up after `limit_ns` of wall time.  On give-up
 // it ORs `code` into the device status word and returns false; the caller must not touch
 // the guarded data.  Never spins without bound.
@@ -76,7 +82,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (AWQ_MBAR_SUSPEND_HINT_NS == 0u ? mbar_try_wait(bar, parity)
+                                       : mbar_try_wait_hint(bar, parity, AWQ_MBAR_SUSPEND_HINT_NS))
+      return true;
     if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(status, code);
       return false;
@@ -188,6 +196,18 @@ __device__ __forceinline__ void st_async_dsmem_f32(float* local, uint64_t* local
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
                "r"(__float_as_uint(v)), "r"(rb)
                : "memory");
+}
+
+// Same for four consecutive floats (16 bytes; both addresses 16-byte aligned).
+__device__ __forceinline__ void st_async_dsmem_v4(float* local, uint64_t* local_bar, uint32_t rank,
+                                                  float4 v) {
+  uint32_t ra, rb;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(local_bar)), "r"(rank));
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(ra),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rb)
+      : "memory");
 }
 
 __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
