@@ -83,19 +83,9 @@ struct Geo {
   static constexpr int NMMA = 4 * CWL;
   static constexpr int E = NMMA * TB * 4 * 32;      // partial sums per warp
   static constexpr int PACK = 8 * TB * 8 * CW_W;    // packed partial: tokens x columns
-  static constexpr int RED_BYTES = (kNW * E + PACK) * 4;  // reuses the activation+weight rings
+  static constexpr int EP = E + E / 128;            // partials per warp, padded
+  static constexpr int RED_BYTES = (kNW * EP + PACK) * 4;  // reuses the activation+weight rings
 };
-
-// Packed column-word (within the lane's CWL words) and nibble that feed A row g (rs = 0)
-// or g + 8 (rs = 1) of MMA mi.
-template <int CWL>
-__device__ __forceinline__ constexpr int mma_cw(int mi, int rs) {
-  return CWL == 1 ? 0 : 2 * (mi >> 3) + rs;
-}
-template <int CWL>
-__device__ __forceinline__ constexpr int mma_nib(int mi, int rs) {
-  return CWL == 1 ? mi + 4 * rs : (mi & 7);
-}
 
 __device__ __forceinline__ uint2 lds64(uint32_t a) {
   uint2 v;
@@ -115,8 +105,16 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
   return v;
 }
 
+#ifndef AWQ_DECODE_MIN_BLOCKS_M8
+#define AWQ_DECODE_MIN_BLOCKS_M8 4
+#endif
+// CTAs per SM the register budget must allow: up to 8 tokens 4 (so the next launch's CTAs
+// fit beside this one's), the wider variants 3.
+template <int TB>
+constexpr int kMinBlocks = TB == 1 ? AWQ_DECODE_MIN_BLOCKS_M8 : 3;
+
 template <int TB, int CWL, bool kSub>
-__global__ void __launch_bounds__(kNW * 32, 3)
+__global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
     decode_tma_kernel(const __grid_constant__ TmaDecodeParams p) {
   using GE = Geo<TB, CWL>;
   constexpr int NMMA = GE::NMMA;
@@ -208,17 +206,30 @@ __global__ void __launch_bounds__(kNW * 32, 3)
   launch_dependents();
 #endif
 
-  // Per-lane shared-memory offsets inside a slot.  Packed words of lane (g8, q):
-  // column-words g8*CWL .. +CWL-1, rows r = 0,1 -> 2q + {0,1} and r = 2,3 -> 2q + 8 + {0,1}
-  // (+16 per k16-step), the row parity swapped for odd q so the four q-lanes of a read
-  // cover both halves of the bank space; the prmt selectors undo the swap.
-  uint32_t w_off[4];
+  // Weight fragments: ldmatrix.trans on the 16-bit view of the packed tile.  An 8x8
+  // matrix of half-words (8 rows of K x 8 half-words), transposed, hands lane (g8, q) the
+  // register (row 2q, row 2q+1) of half-word g8: four nibbles (columns) of two
+  // consecutive K rows, paired as the MMA A operand wants.  Per k16-step the warp's tile
+  // is row blocks rb (rows 0-7, 8-15) x half-word blocks hb (8 half-words = 4 words);
+  // the lane holds half-word 8hb + g8 of every block: word 4hb + g8/2, half g8 % 2.
+  // Rows are 64 bytes (TMA 64-byte swizzle) or 32 bytes (32-byte swizzle); the swizzle
+  // puts the 8 row reads of every matrix in distinct banks.
+  constexpr int HB = GE::CW_W / 4;  // half-word blocks per row
+  uint32_t w_lds[2];
+  {
+    const int rr = lane & 7, jm = lane >> 3;
+    if constexpr (CWL == 2) {  // ldmatrix rb: matrices (rb, hb = jm)
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
-    w_off[r] = static_cast<uint32_t>((2 * q + ((r ^ q) & 1) + 8 * (r >> 1)) * GE::CW_W * 4 +
-                                     g8 * CWL * 4);
-  const uint32_t sel_lo = (q & 1) ? 0x1054u : 0x5410u;
-  const uint32_t sel_hi = (q & 1) ? 0x3276u : 0x7632u;
+      for (int rb = 0; rb < 2; ++rb)
+        w_lds[rb] = static_cast<uint32_t>((8 * rb + rr) * 64 + 16 * (jm ^ ((rr >> 1) & 3)));
+    } else {  // one ldmatrix: matrix jm = (rb, hb) = (jm / 2, jm % 2)
+      w_lds[0] = static_cast<uint32_t>((8 * (jm >> 1) + rr) * 32 + 16 * ((jm & 1) ^ ((rr >> 2) & 1)));
+      w_lds[1] = w_lds[0];
+    }
+  }
+  const int hh = g8 & 1;  // half of its word each of the lane's half-words is
+  const int wq = g8 >> 1;  // word of the lane inside every 4-word block
+  const uint32_t sc_sel = hh ? 0x7632u : 0x5410u;  // scales of columns 2n + hh
   // ldmatrix row addresses for the activation tile (128-byte rows, 128B swizzle): lane l
   // addresses row (l & 7) of 16-byte chunk 4*pair + (l >> 3).  Rows past the activation
   // box (fewer than 8 tokens) read this warp's zero line instead.
@@ -257,47 +268,40 @@ __global__ void __launch_bounds__(kNW * 32, 3)
       for (int e = 0; e < 4; ++e) acc[i][b][e] = 0.f;
   float accg[kSub ? NMMA : 1][TB][4];
   float xs[TB][4];
-  uint32_t zw[CWL];
-  uint32_t sv[CWL][4];
-  uint32_t zp[kSub ? 1 : CWL][8];
+  uint32_t zh[HB];         // the lane's zero half-word (4 nibbles) of every block
+  uint32_t sv[HB][2];      // its scales: nibbles (0, 1) and (2, 3) as half2
+  uint32_t zp[kSub ? 1 : HB][4];  // kExact: 1024 + zero, per nibble, both halves
+  uint32_t sp[kSub ? 1 : HB][4];  // kExact: scale, per nibble, both halves
   int cur = -1;
   // Group of stage j is j / spg; tracked incrementally (one division per warp).
   int grp_of = j0 / spg;
   int grp_left = spg - (j0 - grp_of * spg);  // stages left in grp_of, counting j0
 
+  const bool one_row = p.x_rows == 1;
   auto fold = [&]() {
-#ifdef AWQ_ABL_NOFOLD
-    return;
-#endif
     // acc += scale * (2^24 or 2^20 * sum x c - zero * sum x) for the group just finished.
-    // Nibbles i and i+4 of a packed word are columns 2(i&3) and 2(i&3)+1: their scales are
-    // the two halves of sv[c][i&3] and their zeros come out of one shift-and.
+    // Nibble nib of block hb is MMA mi = 4 (hb / 2) + nib, A rows g8 + 8 (hb % 2).
 #pragma unroll
-    for (int c = 0; c < CWL; ++c)
+    for (int hb = 0; hb < HB; ++hb)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&sv[c][i]));
-        const uint32_t zz = (zw[c] >> (4 * i)) & 0x000F000Fu;
-        const float z_lo = static_cast<float>(zz & 0xFFFFu), z_hi = static_cast<float>(zz >> 16);
+      for (int pp = 0; pp < 2; ++pp) {
+        const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&sv[hb][pp]));
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int nib = i + 4 * h;
-          const float s = h ? s2.y : s2.x;
-          const float sa = s * ((nib & 1) ? 1048576.f : 16777216.f);
-          const float sz = -s * (h ? z_hi : z_lo);
-          // the MMA row holding (column-word c, nibble nib) for this lane
+        for (int n2 = 0; n2 < 2; ++n2) {
+          const int nib = 2 * pp + n2;
+          const float sc = n2 ? s2.y : s2.x;
+          // zero nibble as a float: 2^23 + z read as an fp32 bit pattern, minus 2^23
+          const float z = __uint_as_float(((zh[hb] >> (4 * nib)) & 0xFu) | 0x4B000000u) - 8388608.f;
+          const float sa = sc * ((nib & 1) ? 1048576.f : 16777216.f);
+          const float sz = -sc * z;
+          const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
 #pragma unroll
-          for (int mi = 0; mi < NMMA; ++mi)
+          for (int tb = 0; tb < TB; ++tb)
 #pragma unroll
-            for (int rs = 0; rs < 2; ++rs) {
-              if (mma_cw<CWL>(mi, rs) != c || mma_nib<CWL>(mi, rs) != nib) continue;
-#pragma unroll
-              for (int tb = 0; tb < TB; ++tb)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const float a = __fmaf_rn(sz, xs[tb][e], acc[mi][tb][2 * rs + e]);
-                  acc[mi][tb][2 * rs + e] = __fmaf_rn(sa, accg[mi][tb][2 * rs + e], a);
-                }
+            for (int e = 0; e < 2; ++e) {
+              if (TB == 1 && e == 1 && one_row) continue;  // token 2q+1 does not exist
+              const float a = __fmaf_rn(sz, xs[tb][e], acc[mi][tb][2 * rs + e]);
+              acc[mi][tb][2 * rs + e] = __fmaf_rn(sa, accg[mi][tb][2 * rs + e], a);
             }
         }
       }
@@ -330,10 +334,12 @@ __global__ void __launch_bounds__(kNW * 32, 3)
       if (kSub && cur >= 0) fold();
       cur = grp;
 #pragma unroll
-      for (int c = 0; c < CWL; ++c) {
-        zw[c] = lds32(mb + (g8 * CWL + c) * 4);
-        const uint4 s4 = lds128(mb + 128 + (g8 * CWL + c) * 16);
-        sv[c][0] = s4.x; sv[c][1] = s4.y; sv[c][2] = s4.z; sv[c][3] = s4.w;
+      for (int hb = 0; hb < HB; ++hb) {
+        const uint32_t wofs = 4u * static_cast<uint32_t>(4 * hb + wq);  // word offset, bytes
+        zh[hb] = lds32(mb + wofs) >> (16 * hh);
+        const uint4 v = lds128(mb + 128 + 4 * wofs);  // the word's 8 scales, column order
+        sv[hb][0] = prmt(v.x, v.y, sc_sel);
+        sv[hb][1] = prmt(v.z, v.w, sc_sel);
       }
       if (kSub) {
 #pragma unroll
@@ -347,18 +353,14 @@ __global__ void __launch_bounds__(kNW * 32, 3)
 #pragma unroll
           for (int e = 0; e < 4; ++e) xs[b][e] = 0.f;
       } else {
-        // Zero pairs (1024 + z) in both halves, one per nibble.
 #pragma unroll
-        for (int c = 0; c < CWL; ++c) {
-          const uint32_t lo = prmt(zw[c], zw[c], 0x5410u), hi = prmt(zw[c], zw[c], 0x7632u);
-          zp[kSub ? 0 : c][0] = and_or(lo, 0x000F000Fu, kMagic);
-          zp[kSub ? 0 : c][1] = and_or(lo >> 4, 0x000F000Fu, kMagic);
-          zp[kSub ? 0 : c][2] = and_or(lo >> 8, 0x000F000Fu, kMagic);
-          zp[kSub ? 0 : c][3] = and_or(lo >> 12, 0x000F000Fu, kMagic);
-          zp[kSub ? 0 : c][4] = and_or(hi, 0x000F000Fu, kMagic);
-          zp[kSub ? 0 : c][5] = and_or(hi >> 4, 0x000F000Fu, kMagic);
-          zp[kSub ? 0 : c][6] = and_or(hi >> 8, 0x000F000Fu, kMagic);
-          zp[kSub ? 0 : c][7] = and_or(hi >> 12, 0x000F000Fu, kMagic);
+        for (int hb = 0; hb < HB; ++hb) {
+          const uint32_t zd = prmt(zh[hb], zh[hb], 0x1010u);  // zero half-word in both halves
+#pragma unroll
+          for (int nib = 0; nib < 4; ++nib) {
+            zp[kSub ? 0 : hb][nib] = and_or(zd >> (4 * nib), 0x000F000Fu, kMagic);
+            sp[kSub ? 0 : hb][nib] = prmt(sv[hb][nib >> 1], 0u, (nib & 1) ? 0x3232u : 0x1010u);
+          }
         }
       }
     }
@@ -374,53 +376,37 @@ __global__ void __launch_bounds__(kNW * 32, 3)
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int ks = 2 * pr + kk;
-        uint32_t w[4][CWL];
+        // wr[rb][hb]: rows (2q + 8rb, +1) of the lane's half-word in block hb
+        uint32_t wr[2][HB];
+        if constexpr (CWL == 2) {
+          uint32_t t0[4], t1[4];
+          ldmatrix_x4_trans(t0, wb + w_lds[0] + ks * 16 * 64);
+          ldmatrix_x4_trans(t1, wb + w_lds[1] + ks * 16 * 64);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const uint32_t a = wb + w_off[r] + ks * 16 * GE::CW_W * 4;
-          if constexpr (CWL == 2) {
-            const uint2 v = lds64(a);
-            w[r][0] = v.x;
-            w[r][1] = v.y;
-          } else {
-            w[r][0] = lds32(a);
+          for (int hb = 0; hb < HB; ++hb) {
+            wr[0][hb] = t0[hb];
+            wr[1][hb] = t1[hb];
           }
+        } else {
+          uint32_t t0[4];
+          ldmatrix_x4_trans(t0, wb + w_lds[0] + ks * 16 * 32);
+          wr[0][0] = t0[0]; wr[0][1] = t0[1]; wr[1][0] = t0[2]; wr[1][1] = t0[3];
         }
-        // src[c][rp][h]: rows (2q + 8rp, +1) of column-word c, nibbles 2h and 2h+1 in the
-        // low byte of each half.
-        uint32_t src[CWL][2][4];
-#pragma unroll
-        for (int c = 0; c < CWL; ++c)
-#pragma unroll
-          for (int rp = 0; rp < 2; ++rp) {
-            const uint32_t plo = prmt(w[2 * rp][c], w[2 * rp + 1][c], sel_lo);
-            const uint32_t phi = prmt(w[2 * rp][c], w[2 * rp + 1][c], sel_hi);
-            src[c][rp][0] = plo;
-            src[c][rp][1] = plo >> 8;
-            src[c][rp][2] = phi;
-            src[c][rp][3] = phi >> 8;
-          }
-        auto operand = [&](int c, int rp, int nib) -> uint32_t {
-          const uint32_t s = src[c][rp][nib >> 1];
-          if (kSub) {
-#ifdef AWQ_ABL_NOUNPACK
-            return s;
-#endif
+        auto operand = [&](int rb, int hb, int nib) -> uint32_t {
+          const uint32_t s = wr[rb][hb];
+          if constexpr (kSub) {
             // exact fp16 subnormals c * 2^-24 (even nibble) or c * 2^-20 (odd nibble)
-            return s & ((nib & 1) ? 0x00F000F0u : 0x000F000Fu);
+            return ((nib & 2) ? (s >> 8) : s) & ((nib & 1) ? 0x00F000F0u : 0x000F000Fu);
           } else {
-            const uint32_t h = and_or((nib & 1) ? (s >> 4) : s, 0x000F000Fu, kMagic);
-            const int col = nibble_column(nib);
-            const uint32_t spair = prmt(sv[c][col >> 1], 0u, (col & 1) ? 0x3232u : 0x1010u);
-            return hmul2(hsub2(h, zp[kSub ? 0 : c][nib]), spair);
+            const uint32_t h = and_or(s >> (4 * nib), 0x000F000Fu, kMagic);
+            return hmul2(hsub2(h, zp[kSub ? 0 : hb][nib]), sp[kSub ? 0 : hb][nib]);
           }
         };
 #pragma unroll
         for (int mi = 0; mi < NMMA; ++mi) {
-          const int ca = mma_cw<CWL>(mi, 0), ia = mma_nib<CWL>(mi, 0);
-          const int cb = mma_cw<CWL>(mi, 1), ib = mma_nib<CWL>(mi, 1);
-          const uint32_t a0 = operand(ca, 0, ia), a1 = operand(cb, 0, ib);
-          const uint32_t a2 = operand(ca, 1, ia), a3 = operand(cb, 1, ib);
+          const int hb0 = 2 * (mi >> 2), nib = mi & 3;
+          const uint32_t a0 = operand(0, hb0, nib), a1 = operand(0, hb0 + 1, nib);
+          const uint32_t a2 = operand(1, hb0, nib), a3 = operand(1, hb0 + 1, nib);
 #pragma unroll
           for (int tb = 0; tb < TB; ++tb) {
             if (kSub)
@@ -429,13 +415,11 @@ __global__ void __launch_bounds__(kNW * 32, 3)
               mma16816(acc[mi][tb], a0, a1, a2, a3, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
           }
         }
-#ifndef AWQ_ABL_NOONES
         if (kSub) {
 #pragma unroll
           for (int tb = 0; tb < TB; ++tb)
             mma16816(xs[tb], kOnes, kOnes, kOnes, kOnes, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
         }
-#endif
       }
     }
     __syncwarp();
@@ -470,29 +454,36 @@ __global__ void __launch_bounds__(kNW * 32, 3)
   // adds the cluster's partials in rank order, adds the bias and stores y.  Other CTAs
   // exit right after their push.
   __syncthreads();  // the ring is reused as the reduction buffer
+  // Per-warp partials in fragment order (row X = (mi*TB + tb)*4 + e, 32 lanes), one float
+  // of padding per 4 rows so the packed-order reads below spread over the banks.
   float* red = reinterpret_cast<float*>(smem);
-  float* mine = red + warp * GE::E;
+  float* mine = red + warp * GE::EP;
 #pragma unroll
   for (int mi = 0; mi < NMMA; ++mi)
 #pragma unroll
     for (int tb = 0; tb < TB; ++tb)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) mine[((mi * TB + tb) * 4 + e) * 32 + lane] = acc[mi][tb][e];
+      for (int e = 0; e < 4; ++e) {
+        const int X = (mi * TB + tb) * 4 + e;
+        mine[X * 32 + lane + (X >> 2)] = acc[mi][tb][e];
+      }
   __syncthreads();
-  // Output element e (warp-fragment order): token and column inside the CTA tile.
-  auto token_of = [&](int e) { return 8 * ((e >> 7) % TB) + 2 * (e & 3) + ((e >> 5) & 1); };
-  auto col_of = [&](int e) {
-    const int mi = (e >> 7) / TB, rs = ((e >> 5) & 3) >> 1;
-    return (((e & 31) >> 2) * CWL + mma_cw<CWL>(mi, rs)) * 8 + nibble_column(mma_nib<CWL>(mi, rs));
-  };
-  float* pack = red + kNW * GE::E;
-  for (int e = threadIdx.x; e < GE::E; e += kNW * 32) {
-    const int t = token_of(e);
-    if (t >= p.x_rows) continue;
+  // Packed partial: element (token t, column col) of the tile, summed over the warps.
+  // Column col = 32 hb + 8 (g8 / 2) + 2 nib + g8 % 2 comes from lane group g8, nibble nib
+  // of block hb, i.e. MMA mi = 4 (hb / 2) + nib, rows g8 + 8 (hb % 2); g8 varies fastest
+  // across threads, the token slowest.
+  float* pack = red + kNW * GE::EP;
+  for (int i = threadIdx.x; i < pack_n; i += kNW * 32) {
+    const int g8i = i & 7, r = i >> 3;
+    const int nib = r & 3, hb = (r >> 2) % HB, t = (r >> 2) / HB;
+    const int col = 32 * hb + 8 * (g8i >> 1) + 2 * nib + (g8i & 1);
+    const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
+    const int X = (mi * TB + (t >> 3)) * 4 + 2 * rs + (t & 1);
+    const int e = X * 32 + g8i * 4 + ((t & 7) >> 1) + (X >> 2);
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kNW; ++w) v += red[w * GE::E + e];
-    pack[t * 8 * GE::CW_W + col_of(e)] = v;
+    for (int w = 0; w < kNW; ++w) v += red[w * GE::EP + e];
+    pack[t * 8 * GE::CW_W + col] = v;
   }
   __syncthreads();
 #ifdef AWQ_DECODE_DEBUG_TIME
@@ -727,7 +718,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   const int C = p.N / 8;
   const int ngrp = p.K / p.G;
   if (!make_tmap_2d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, GE::CW_W, kRS,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
+                    CWL == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B, &why) ||
       !make_tmap_2d(&dp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kRS, x_rows,
                     (x_rows == 1 && !AWQ_DECODE_WIDE_X) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
       !make_tmap_2d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, GE::CW_W, 1,

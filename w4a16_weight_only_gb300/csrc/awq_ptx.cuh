@@ -82,6 +82,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
+#ifdef AWQ_MBAR_WAIT_PROBE
+    AWQ_MBAR_WAIT_PROBE();  // debug builds: one call per polling round
+#endif
     if (AWQ_MBAR_SUSPEND_HINT_NS == 0u ? mbar_try_wait(bar, parity)
                                        : mbar_try_wait_hint(bar, parity, AWQ_MBAR_SUSPEND_HINT_NS))
       return true;
@@ -230,6 +233,15 @@ __device__ __forceinline__ uint32_t swz32(uint32_t off) { return off ^ (((off >>
 // matrix j.
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr)
+               : "memory");
+}
+
+// Same with .trans: register j receives column (lane / 4), rows 2 (lane % 4) .. +1 of
+// matrix j (the lower row in the low 16 bits).
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(saddr)
                : "memory");
