@@ -65,6 +65,32 @@ def step_bytes(lins):
                for d in lins)
 
 
+# DRAM traffic of the decode kernel per launch (dram__bytes_read.sum + dram__bytes_write.sum),
+# averaged over the three linears of one step, from the ncu launch list of
+# `python bench.py --steps 60 --warmup 3 --no-cpu-baseline` summarised in
+# profiles/decode_tma_7b_m1_bench_launches.md; valid only for the kernel source it was
+# measured on (SHA-256 of the files below), else reported as null.
+TRAFFIC_BYTES_PER_LAUNCH = 18_588_000
+TRAFFIC_SOURCES = {
+    "w4a16_weight_only_gb300/csrc/awq_decode_tma.cu":
+        "db83bb2f95d1f41e60a5e109f3867befabcd39e753f70b93bb68e66e979aa70c",
+    "w4a16_weight_only_gb300/csrc/awq_ptx.cuh":
+        "594d27bfcdf987daf3de5b15bf561a524931a1ca3859ce6920e4c94921cfbf09",
+}
+
+
+def measured_traffic():
+    import hashlib
+    for rel, digest in TRAFFIC_SOURCES.items():
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
+    return TRAFFIC_BYTES_PER_LAUNCH
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -216,13 +242,15 @@ def run_reference(args, rank, world):
         oracle_step(sub)
     el = time.perf_counter() - t0
     value = nbytes * args.steps / el / 1e9
-    desc = (f"first {width} output columns of each of the three linears (M=1) per step; "
-            "numpy fp64 matmul (BLAS threads), unpack/dequant single-threaded")
+    widths = ", ".join(f"{d['K']}x{d['N']}" for d in sub)
+    desc = (f"first min({width}, N) output columns of each of the three linears (M=1) per step "
+            f"(K x columns: {widths}); numpy fp64 matmul (BLAS threads), unpack/dequant "
+            "single-threaded")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAME + " (column sample)", "sample_width": min(width, 11008)},
+            "config": {"workload": WORKLOAD_NAME + " (column sample)", "sample_width": width},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -348,7 +376,8 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "kernel": "decode_kernel (awq_gemm decode path)",
-                     "traffic": None},
+                     "traffic": measured_traffic(),
+                     "traffic_unit": "bytes per launch (mean of the three linears)"},
         "e2e": {"value": world * nbytes * e2e_steps / e2e_el / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
