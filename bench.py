@@ -408,6 +408,94 @@ def run_case(args, local):
     print(json.dumps({"case": args.case, "path": args.path, "launches": args.warmup + args.steps}))
 
 
+def run_sweep(args, local):
+    """Per-workload table (one JSON line per synth.WORKLOADS entry): small-M shapes as HBM
+    GB/s over CUDA-graph replays of rotating weight copies (together > 3x L2), large-M
+    shapes as TFLOP/s over back-to-back launches, beside cuBLAS fp16 on the dense weight
+    and awq_dequant + cuBLAS for the large ones.  Not the bench contract line."""
+    import torch
+    from w4a16_weight_only_gb300 import build as _build
+    _build.build()
+    import w4a16_weight_only_gb300 as awq
+    torch.cuda.set_device(local)
+    hbm, hbm_kind = peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tflops = float(json.load(f)["bf16_tflops"])
+        tf_kind = "measured bf16 burst (fp16 nominal rate equal)"
+    except Exception:
+        tflops, tf_kind = 1900.0, "fallback"
+    names = [w[2] for w in synth.WORKLOADS]
+    if args.case:
+        names = [n for n in names if args.case in n]
+    stream = torch.cuda.Stream()
+
+    def timed(fn, reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / reps * 1e3  # us
+
+    for name in names:
+        d = synth.workload_inputs(name)
+        M, K, N, G = d["M"], d["K"], d["N"], d["group_size"]
+        x = torch.from_numpy(d["x"]).cuda()
+        qw = torch.from_numpy(d["qweight"]).cuda()
+        qz = torch.from_numpy(d["qzeros"]).cuda()
+        sc = torch.from_numpy(d["scales"]).cuda()
+        bias = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
+        y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        nbytes = algorithmic_bytes(M, K, N, G, bias is not None)
+        flop = 2.0 * M * N * K
+        line = {"workload": name, "M": M, "K": K, "N": N, "group_size": G, "bias": bias is not None,
+                "path": awq.select_path(x, qw, qz, sc, bias, G, y)}
+        if M <= 32:
+            R = max(2, min(16, int(3 * L2_BYTES // nbytes) + 1))
+            sets = [(qw.clone(), qz.clone(), sc.clone()) for _ in range(R)]
+            calls = max(R, (240 // R) * R)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for i in range(3 * R):
+                    w = sets[i % R]
+                    awq.awq_gemm(x, w[0], w[1], w[2], bias, group_size=G, out=y, stream=stream)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(calls):
+                        w = sets[i % R]
+                        awq.awq_gemm(x, w[0], w[1], w[2], bias, group_size=G, out=y, stream=stream)
+            times = sorted(timed(g.replay, 1) / calls for _ in range(5))
+            t = times[2]
+            line.update({"us": t, "GB_s": nbytes / t / 1e3, "frac_hbm": nbytes / t / 1e3 / hbm,
+                         "weight_copies": R, "launches_per_graph": calls})
+            del sets, g
+        else:
+            fn = lambda: awq.awq_gemm(x, qw, qz, sc, bias, group_size=G, out=y, stream=stream)
+            timed(fn, 3)
+            t = timed(fn, 10)
+            wd = awq.awq_dequant(qw, qz, sc, group_size=G)
+            torch.cuda.synchronize()
+            mm = lambda: torch.matmul(x, wd, out=y)
+            timed(mm, 3)
+            t_mm = timed(mm, 10)
+            dq = lambda: awq.awq_dequant(qw, qz, sc, group_size=G, out=wd, stream=stream)
+            timed(dq, 3)
+            t_dq = timed(dq, 10)
+            line.update({"us": t, "TFLOP_s": flop / t / 1e6, "frac_tensor": flop / t / 1e6 / tflops,
+                         "cublas_fp16_dense_us": t_mm, "cublas_fp16_dense_TFLOP_s": flop / t_mm / 1e6,
+                         "dequant_plus_cublas_us": t_dq + t_mm})
+            del wd
+        awq.device_status()
+        line.update({"hbm_peak_GB_s": hbm, "hbm_peak": hbm_kind, "tensor_peak_TFLOP_s": tflops,
+                     "tensor_peak": tf_kind})
+        print(json.dumps(line), flush=True)
+        del x, qw, qz, sc, bias, y
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -418,8 +506,13 @@ def main(argv=None):
     ap.add_argument("--case", default=None,
                     help="profiling mode: run only this workload linear (see synth.WORKLOADS)")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "prefill", "generic"])
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-workload table (one JSON line per workload), not the bench line")
     args = ap.parse_args(argv)
     rank, world, local = dist_setup(args)
+    if args.sweep:
+        run_sweep(args, local)
+        return
     if args.case:
         run_case(args, local)
         return

@@ -115,6 +115,12 @@ awq_status_t awq_dequant(const int32_t* qweight, const int32_t* qzeros, const vo
  * without launching").  Exactly one kernel launch otherwise.
  * Accuracy: |y - y_exact| <= 1e-2 * max(1, |y_exact|) elementwise, y_exact being the
  * same sum in exact arithmetic.
+ * Stream ordering: the small-M kernel is launched as a programmatic dependent launch and
+ * starts reading qweight, qzeros, scales and bias before the kernel issued just before
+ * it on `stream` has finished; x is read and y written only after that kernel's results
+ * are visible.  So those four weight tensors must be complete before the preceding
+ * kernel launch on the same stream (not written by that kernel); any earlier work, copy
+ * or event dependency is ordered as usual.
  */
 awq_status_t awq_gemm(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
                       const void* scales_f16, const void* bias_f16,
