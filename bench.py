@@ -178,6 +178,12 @@ def reduce_max(value: float, world: int) -> float:
     return float(t.item())
 
 
+def job_gbs(bytes_per_step: int, steps: int, world: int, elapsed_max_s: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of `bytes_per_step` algorithmic
+    bytes; the job took the slowest rank's time."""
+    return world * bytes_per_step * steps / elapsed_max_s / 1e9
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -362,7 +368,7 @@ def run_ours(args, rank, world, local):
 
     peak, peak_kind = peaks()
     achieved = nbytes * args.steps / elapsed / 1e9
-    value = world * nbytes * args.steps / elapsed_max / 1e9
+    value = job_gbs(nbytes, args.steps, world, elapsed_max)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3,

@@ -18,7 +18,7 @@
 //               single MMA-issuing thread
 //   warps 2-9   dequantize the packed tile into the MN-major, 128B-swizzled fp16 A tile
 //               (one packed word = one 16-byte chunk of 8 adjacent columns, no transpose):
-//               w = (c - z) * s exactly (fp16 exponent trick, HSUB2, HMUL2) -> 2-deep ring
+//               w = (c - z) * s exactly (fp16 exponent trick, HSUB2, HMUL2) -> 4-deep ring
 //   warps 10-13 epilogue: tcgen05.ld (32 lanes x 32 columns), + bias, fp16, store; the
 //               second accumulator lets the next tile's MMAs run meanwhile
 // Every wait is an mbarrier try-wait bounded in wall time; on give-up the kernel sets the
