@@ -48,7 +48,10 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kNW = 4;       // warps per CTA
+#ifndef AWQ_DECODE_WARPS
+#define AWQ_DECODE_WARPS 4
+#endif
+constexpr int kNW = AWQ_DECODE_WARPS;  // warps per CTA
 constexpr int kRS = 64;      // rows of K per stage
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kMagic = 0x64006400u;     // fp16 1024 in both halves
@@ -106,12 +109,15 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 }
 
 #ifndef AWQ_DECODE_MIN_BLOCKS_M8
-#define AWQ_DECODE_MIN_BLOCKS_M8 4
+#define AWQ_DECODE_MIN_BLOCKS_M8 3
 #endif
-// CTAs per SM the register budget must allow: up to 8 tokens 4 (so the next launch's CTAs
-// fit beside this one's), the wider variants 3.
+// CTAs per SM the register budget must allow (3: up to 168 registers a thread; tighter
+// budgets measured slower, the extra registers buy instruction-level parallelism).
+#ifndef AWQ_DECODE_MIN_BLOCKS_WIDE
+#define AWQ_DECODE_MIN_BLOCKS_WIDE 3
+#endif
 template <int TB>
-constexpr int kMinBlocks = TB == 1 ? AWQ_DECODE_MIN_BLOCKS_M8 : 3;
+constexpr int kMinBlocks = TB == 1 ? AWQ_DECODE_MIN_BLOCKS_M8 : AWQ_DECODE_MIN_BLOCKS_WIDE;
 
 template <int TB, int CWL, bool kSub>
 __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)

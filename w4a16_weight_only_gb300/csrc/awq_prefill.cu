@@ -62,11 +62,7 @@ constexpr int BAR_OFF = S_OFF + kST * 256;
 constexpr int NBARS = 2 * kST + 2 * kSA + 4 + 1;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base (u32), abort flag (u32)
 constexpr size_t SMEM = 1024 + MISC_OFF + 16;
-#ifdef AWQ_PREFILL_ABL_HALFX
-constexpr int kXRows = kBT / 2;
-#else
 constexpr int kXRows = kBT;
-#endif
 constexpr uint32_t STAGE_TX = kXRows * kBK * 2 + W_BYTES + 16 * 4 + 128 * 2;
 
 struct __align__(64) PrefillParams {
@@ -317,11 +313,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __syncwarp();
   } else if (warp < 2 + kDQ) {
     // ---------------------------------------------------------------- dequant
-    // thread -> rows (2rp, 2rp+1) x column-words 2cg, 2cg+1 of the stage.  Each packed
-    // word becomes one 16-byte chunk (its 8 columns in order) of the MN-major A tile.
+    // thread -> rows rp, rp + 32 x column-words 2cg, 2cg+1 of the stage.  Each packed word
+    // becomes one 16-byte chunk (its 8 columns in order) of the MN-major A tile.  A warp
+    // reads four consecutive 64-byte rows (each half-warp two whole rows: no bank
+    // conflict) and, per store, lanes cg >= 4 take their odd word first so the eight
+    // 16-byte chunks of one store phase land in eight different bank groups.
     const int dq = threadIdx.x - 64;
     const int rp = dq >> 3;
     const int cg = dq & 7;
+    const int csel = (cg >> 2) & 1;
     int s = 0, sa = 0;
     uint32_t ph = 0, pha = 0;
     bool ok = true;
@@ -339,36 +339,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         AWQ_PREFILL_DEBUG_ROLE(1, 2);
 #endif
         const uint32_t wb = sbase + W_OFF + s * W_BYTES;
-#ifdef AWQ_PREFILL_ABL_NODQ
-        if (true) {
-          __syncwarp();
-          if (lane == 0) { mbar_arrive(&full_a[sa]); mbar_arrive(&empty_t[s]); }
-          if (++s == kST) { s = 0; ph ^= 1u; }
-          if (++sa == kSA) { sa = 0; pha ^= 1u; }
-          continue;
-        }
-#endif
-        const uint2 r0 = lds64p(wb + (2 * rp) * 64 + cg * 8);
-        const uint2 r1 = lds64p(wb + (2 * rp + 1) * 64 + cg * 8);
+        const uint2 r0 = lds64p(wb + rp * 64 + cg * 8);
+        const uint2 r1 = lds64p(wb + (rp + 32) * 64 + cg * 8);
         const uint2 z2 = lds64p(sbase + Z_OFF + s * 128 + cg * 8);
         const uint32_t w[2][2] = {{r0.x, r0.y}, {r1.x, r1.y}};
         const uint32_t zw[2] = {z2.x, z2.y};
         const uint32_t ab = sbase + A_OFF + sa * A_BYTES;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const int cw = 2 * cg + c;
+          const int cc = c ^ csel;
+          const int cw = 2 * cg + cc;
           const uint4 s4 = lds128p(sbase + S_OFF + s * 256 + cw * 16);
           const uint32_t sp[4] = {s4.x, s4.y, s4.z, s4.w};  // (s[2j], s[2j+1])
           uint32_t zp[4];                                    // (1024+z[2j], 1024+z[2j+1])
+          const uint32_t zc = cc ? zw[1] : zw[0];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) zp[j] = and_or(zw[c] >> (4 * j), 0x000F000Fu, kMagic);
+          for (int j = 0; j < 4; ++j) zp[j] = and_or(zc >> (4 * j), 0x000F000Fu, kMagic);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             uint32_t v[4];
+            const uint32_t wc = cc ? w[e][1] : w[e][0];
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              v[j] = hmul2(hsub2(and_or(w[e][c] >> (4 * j), 0x000F000Fu, kMagic), zp[j]), sp[j]);
-            const int k = 2 * rp + e;
+              v[j] = hmul2(hsub2(and_or(wc >> (4 * j), 0x000F000Fu, kMagic), zp[j]), sp[j]);
+            const int k = rp + 32 * e;
             const int off = ((cw >> 3) * 8 + (k >> 3)) * 1024 + (k & 7) * 128 +
                             (((cw & 7) ^ (k & 7)) << 4);
             sts128(ab + off, v[0], v[1], v[2], v[3]);
