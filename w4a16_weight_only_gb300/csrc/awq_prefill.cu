@@ -24,6 +24,12 @@
 // Every wait is an mbarrier try-wait bounded in wall time; on give-up the kernel sets the
 // device status word, all roles leave their loops, in-flight copies and MMAs are drained
 // (bounded) and TMEM is freed before exit.
+//
+// Pair variant (kPair, compile-time option): a cluster of two CTAs shares a 256 x 256
+// tile through tcgen05.mma.cta_group::2 (M = 256: each CTA dequantizes its own 128
+// columns; N = 256: each CTA loads its own 128 activation rows, no TMA multicast); the
+// even CTA issues the MMAs and commits to both CTAs' barriers, the odd CTA's dequant warps
+// signal readiness with a counted st.async into the even CTA's barrier.
 #include <mutex>
 
 #include "awq_internal.cuh"
@@ -44,26 +50,50 @@ constexpr int kST = 4;     // TMA ring depth
 constexpr int kSA = 4;     // dequantized-A ring depth
 constexpr int kDQ = 8;                        // dequant warps
 constexpr int kThreads = (2 + kDQ + 4) * 32;  // producer, MMA, dequant, epilogue
+#ifndef AWQ_PREFILL_ACC_BUFS
+#define AWQ_PREFILL_ACC_BUFS 2
+#endif
+constexpr int kAccBufs = AWQ_PREFILL_ACC_BUFS;      // TMEM accumulators (tile overlap)
+constexpr int kTmemCols = kAccBufs * kBT;           // 256 or 512 fp32 columns
+static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation size");
 constexpr uint32_t kMagic = 0x64006400u;
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
 constexpr unsigned int kStatusPrefillTimeout = 0x2u;
 
-// shared memory layout (offsets from a 1024-aligned base)
-constexpr int X_BYTES = kBT * kBK * 2;       // 32 KB
+// Shared memory layout (offsets from a 1024-aligned base).  Pair mode loads half the
+// activation rows per CTA, and its stages wait on a cross-SM round trip (remote barrier
+// arrivals, multicast commits), so it spends the room on deeper rings.
+#ifndef AWQ_PREFILL_PAIR_ST
+#define AWQ_PREFILL_PAIR_ST 7
+#endif
+#ifndef AWQ_PREFILL_PAIR_SA
+#define AWQ_PREFILL_PAIR_SA 5
+#endif
 constexpr int A_BYTES = kBN * kBK * 2;       // 16 KB
 constexpr int W_BYTES = kBK * 16 * 4;        // 4 KB
-constexpr int X_OFF = 0;
-constexpr int A_OFF = X_OFF + kST * X_BYTES;
-constexpr int W_OFF = A_OFF + kSA * A_BYTES;
-constexpr int Z_OFF = W_OFF + kST * W_BYTES;  // 128 B per stage
-constexpr int S_OFF = Z_OFF + kST * 128;      // 256 B per stage
-constexpr int BAR_OFF = S_OFF + kST * 256;
-// barriers: full_t[kST], empty_t[kST], full_a[kSA], empty_a[kSA], tfull[2], tempty[2], drain
-constexpr int NBARS = 2 * kST + 2 * kSA + 4 + 1;
-constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base (u32), abort flag (u32)
-constexpr size_t SMEM = 1024 + MISC_OFF + 16;
 constexpr int kXRows = kBT;
-constexpr uint32_t STAGE_TX = kXRows * kBK * 2 + W_BYTES + 16 * 4 + 128 * 2;
+template <bool kPair>
+struct Layout {
+  static constexpr int ST = kPair ? AWQ_PREFILL_PAIR_ST : kST;  // TMA ring depth
+  static constexpr int SA = kPair ? AWQ_PREFILL_PAIR_SA : kSA;  // dequantized-A ring depth
+  static constexpr int X_BYTES = (kPair ? kBT / 2 : kBT) * kBK * 2;  // 16 or 32 KB
+  static constexpr int X_OFF = 0;
+  static constexpr int A_OFF = X_OFF + ST * X_BYTES;
+  static constexpr int W_OFF = A_OFF + SA * A_BYTES;
+  static constexpr int Z_OFF = W_OFF + ST * W_BYTES;  // 128 B per stage
+  static constexpr int S_OFF = Z_OFF + ST * 128;      // 256 B per stage
+  static constexpr int BAR_OFF = S_OFF + ST * 256;
+  // barriers: full_t[ST], empty_t[ST], full_a[SA], empty_a[SA], tfull[2], tempty[2], drain
+  static constexpr int NBARS = 2 * ST + 2 * SA + 4 + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base (u32), abort flag (u32)
+  static constexpr int SIG_OFF = MISC_OFF + 16;         // pair: targets of the peer's signals
+  static constexpr size_t SMEM = 1024 + SIG_OFF + 64;
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// Bytes one CTA's stage copies land: its activation rows, packed tile, zero and scale rows.
+template <bool kPair>
+constexpr uint32_t stage_tx() { return (kPair ? kXRows / 2 : kXRows) * kBK * 2 + W_BYTES + 16 * 4 + 128 * 2; }
 
 struct __align__(64) PrefillParams {
   CUtensorMap tm_x;  // x [M][K] f16, box {64, 256}, 128B swizzle
@@ -103,21 +133,81 @@ constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (1u << 15) | (0
                             (static_cast<uint32_t>(kBT >> 3) << 17) |
                             (static_cast<uint32_t>(kBN >> 4) << 24);
 
+// Pair mode (cta_group::2): the MMA spans the two CTAs of a cluster, M = 256 (128 A rows
+// from each CTA's shared memory), N = 256 (128 B rows from each); every CTA's TMEM holds
+// the accumulator rows of its own A half.
+constexpr uint32_t kIdescPair = (kIdesc & ~(0x1Fu << 24)) | (static_cast<uint32_t>((2 * kBN) >> 4) << 24);
+
+template <bool kPair>
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
+  if constexpr (kPair) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kIdescPair), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
+// Arrive on `bar` once the MMAs issued so far complete: in pair mode on the barrier at the
+// same offset in both CTAs of the cluster.
+template <bool kPair>
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  if constexpr (kPair) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(static_cast<unsigned short>(0x3))
+        : "memory");
+  } else {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+  }
+}
+
+// Bounded wait on phase `parity` of a local mbarrier with cluster-scope acquire (the
+// phase was completed by arrivals released from the other CTA of the pair).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
+  return ok != 0u;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          unsigned int* status, unsigned int code,
+                                                          uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(status, code);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Arrive (release, cluster scope) on the mbarrier at `local`'s offset in CTA `rank`.
+__device__ __forceinline__ void mbar_arrive_rank(uint64_t* local, uint32_t rank) {
+  uint32_t ra;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_after() {
@@ -160,59 +250,83 @@ __device__ __forceinline__ uint4 lds128p(uint32_t a) {
   return v;
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using L = Layout<kPair>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* full_t = bars;
-  uint64_t* empty_t = bars + kST;
-  uint64_t* full_a = bars + 2 * kST;
-  uint64_t* empty_a = bars + 2 * kST + kSA;
-  uint64_t* tfull = bars + 2 * kST + 2 * kSA;
+  uint64_t* empty_t = bars + L::ST;
+  uint64_t* full_a = bars + 2 * L::ST;
+  uint64_t* empty_a = bars + 2 * L::ST + L::SA;
+  uint64_t* tfull = bars + 2 * L::ST + 2 * L::SA;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + MISC_OFF);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + MISC_OFF + 4);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::MISC_OFF);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int KB = p.K / kBK;  // stages per tile
+  // Pair mode: the cluster's two CTAs share each tile; rank 0 (the leader) issues the MMAs.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0u;
+  const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstep = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  constexpr int kTileWords = kPair ? 2 * kBN / 8 : kBN / 8;  // packed words per tile
+  constexpr int kXR = kPair ? kBT / 2 : kBT;                 // activation rows this CTA loads
 #ifdef AWQ_PREFILL_DEBUG_DECL
   AWQ_PREFILL_DEBUG_DECL
 #endif
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kST; ++s) {
+    for (int s = 0; s < L::ST; ++s) {
       mbar_init(&full_t[s], 1);
       mbar_init(&empty_t[s], kDQ + 1);  // dequant warps + one MMA commit
     }
-    for (int s = 0; s < kSA; ++s) {
-      mbar_init(&full_a[s], kDQ);     // dequant warps
-      mbar_init(&empty_a[s], 1);      // MMA commit
+    for (int s = 0; s < L::SA; ++s) {
+      // own dequant warps (pair leader: one of them also expects the peer's signal bytes)
+      mbar_init(&full_a[s], kDQ);
+      mbar_init(&empty_a[s], 1);                     // MMA commit
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);        // MMA commit
-      mbar_init(&tempty[b], 4);       // four epilogue warps
+      mbar_init(&tfull[b], 1);                       // MMA commit
+      mbar_init(&tempty[b], kPair ? 8 : 4);          // epilogue warps (of both CTAs)
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
-                     smem_u32(const_cast<uint32_t*>(tmem_slot)))
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (kPair) {  // one warp of each CTA of the pair, collectively
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(const_cast<uint32_t*>(tmem_slot))), "n"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(const_cast<uint32_t*>(tmem_slot))), "n"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (*abort_flag) return false;
     if (mbar_wait_bounded(bar, parity, p.status, kStatusPrefillTimeout, kWaitLimitNs)) return true;
+    *abort_flag = 1u;
+    return false;
+  };
+  auto wait_cl = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait_cluster_bounded(bar, parity, p.status, kStatusPrefillTimeout, kWaitLimitNs)) return true;
     *abort_flag = 1u;
     return false;
   };
@@ -226,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       uint32_t ph = 0;
       int issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
-        const int m0 = (tile % p.tiles_t) * kBT;
-        const int cw0 = (tile / p.tiles_t) * (kBN / 8);
+      for (int tile = tile0; ok && tile < p.tiles; tile += tstep) {
+        const int m0 = (tile % p.tiles_t) * kBT + static_cast<int>(rank) * kXR;
+        const int cw0 = (tile / p.tiles_t) * kTileWords + static_cast<int>(rank) * (kBN / 8);
         for (int kb = 0; kb < KB; ++kb) {
 #ifdef AWQ_PREFILL_DEBUG_ROLE
           AWQ_PREFILL_DEBUG_ROLE(0, 0);
@@ -239,26 +353,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #endif
           const int k0 = kb * kBK;
           const int grp = k0 / p.G;
-          mbar_arrive_expect_tx(&full_t[s], STAGE_TX);
-          tma_load_2d(smem + X_OFF + s * X_BYTES, &p.tm_x, &full_t[s], k0, m0);
-          tma_load_2d(smem + W_OFF + s * W_BYTES, &p.tm_w, &full_t[s], cw0, k0);
-          tma_load_2d(smem + Z_OFF + s * 128, &p.tm_z, &full_t[s], cw0, grp);
-          tma_load_2d(smem + S_OFF + s * 256, &p.tm_s, &full_t[s], 8 * cw0, grp);
+          mbar_arrive_expect_tx(&full_t[s], stage_tx<kPair>());
+          tma_load_2d(smem + L::X_OFF + s * L::X_BYTES, &p.tm_x, &full_t[s], k0, m0);
+          tma_load_2d(smem + L::W_OFF + s * W_BYTES, &p.tm_w, &full_t[s], cw0, k0);
+          tma_load_2d(smem + L::Z_OFF + s * 128, &p.tm_z, &full_t[s], cw0, grp);
+          tma_load_2d(smem + L::S_OFF + s * 256, &p.tm_s, &full_t[s], 8 * cw0, grp);
           ++issued;
-          if (++s == kST) { s = 0; ph ^= 1u; }
+          if (++s == L::ST) { s = 0; ph ^= 1u; }
         }
       }
       if (!ok) {
         // drain: every issued stage's copies must land before the CTA can exit
-        for (int i = 0; i < kST && i < issued; ++i) {
-          if (--s < 0) { s = kST - 1; ph ^= 1u; }
+        for (int i = 0; i < L::ST && i < issued; ++i) {
+          if (--s < 0) { s = L::ST - 1; ph ^= 1u; }
           mbar_wait_bounded(&full_t[s], ph, p.status, kStatusPrefillTimeout, kWaitLimitNs);
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && kPair && !leader) {
+      // the leader's MMAs write this CTA's TMEM and read its shared memory: wait for the
+      // last of them before the CTA may free TMEM
+      if (tile0 < p.tiles) mbar_wait_bounded(drain, 0u, p.status, kStatusPrefillTimeout, kWaitLimitNs);
+    } else if (lane == 0) {
 #ifdef AWQ_PREFILL_DEBUG_WAIT
       unsigned long long dbg_t0 = 0;
 #endif
@@ -267,12 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       int li = 0;
       bool ok = true;
       bool any = false;
-      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x, ++li) {
-        const int b = li & 1;
+      for (int tile = tile0; ok && tile < p.tiles; tile += tstep, ++li) {
+        const int b = li % kAccBufs;
 #ifdef AWQ_PREFILL_DEBUG_WAIT
         AWQ_PREFILL_DEBUG_WAIT(0);
 #endif
-        if (!wait(&tempty[b], static_cast<uint32_t>(((li >> 1) & 1) ^ 1))) { ok = false; break; }
+        if (!wait(&tempty[b], static_cast<uint32_t>(((li / kAccBufs) & 1) ^ 1))) { ok = false; break; }
 #ifdef AWQ_PREFILL_DEBUG_WAIT
         AWQ_PREFILL_DEBUG_WAIT(1);
 #endif
@@ -285,28 +403,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #endif
           // full_a completes only after every dequant warp has seen full_t[s], so the
           // activation tile of stage s is in place as well (one wait per stage).
-          if (!wait(&full_a[sa], pha)) { ok = false; break; }
+          if (!(kPair ? wait_cl(&full_a[sa], pha) : wait(&full_a[sa], pha))) { ok = false; break; }
 #ifdef AWQ_PREFILL_DEBUG_WAIT
           AWQ_PREFILL_DEBUG_WAIT(4);
 #endif
           tc_fence_after();
-          const uint64_t adesc = sw128_desc(sbase + A_OFF + sa * A_BYTES, kA_LBO, kA_SBO);
-          const uint64_t bdesc = sw128_desc(sbase + X_OFF + s * X_BYTES, 16u, 1024u);
+          const uint64_t adesc = sw128_desc(sbase + L::A_OFF + sa * A_BYTES, kA_LBO, kA_SBO);
+          const uint64_t bdesc = sw128_desc(sbase + L::X_OFF + s * L::X_BYTES, 16u, 1024u);
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks)  // K += 16: A two atoms (2048 B), B 32 B
-            mma_f16(d, adesc + (2u * kA_SBO >> 4) * ks, bdesc + 2 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
+            mma_f16<kPair>(d, adesc + (2u * kA_SBO >> 4) * ks, bdesc + 2 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
           any = true;
-          mma_commit(&empty_t[s]);
-          mma_commit(&empty_a[sa]);
-          if (++s == kST) { s = 0; ph ^= 1u; }
-          if (++sa == kSA) { sa = 0; pha ^= 1u; }
+          mma_commit<kPair>(&empty_t[s]);
+          mma_commit<kPair>(&empty_a[sa]);
+          if (++s == L::ST) { s = 0; ph ^= 1u; }
+          if (++sa == L::SA) { sa = 0; pha ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(&tfull[b]);
+        mma_commit<kPair>(&tfull[b]);
       }
       if (any) {
         // all MMAs issued by this thread complete before TMEM is released
-        mma_commit(drain);
+        mma_commit<kPair>(drain);
         mbar_wait_bounded(drain, 0u, p.status, kStatusPrefillTimeout, kWaitLimitNs);
       }
     }
@@ -325,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     int s = 0, sa = 0;
     uint32_t ph = 0, pha = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+    for (int tile = tile0; ok && tile < p.tiles; tile += tstep) {
       for (int kb = 0; kb < KB; ++kb) {
 #ifdef AWQ_PREFILL_DEBUG_ROLE
         AWQ_PREFILL_DEBUG_ROLE(1, 0);
@@ -338,18 +456,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #ifdef AWQ_PREFILL_DEBUG_ROLE
         AWQ_PREFILL_DEBUG_ROLE(1, 2);
 #endif
-        const uint32_t wb = sbase + W_OFF + s * W_BYTES;
+        const uint32_t wb = sbase + L::W_OFF + s * W_BYTES;
         const uint2 r0 = lds64p(wb + rp * 64 + cg * 8);
         const uint2 r1 = lds64p(wb + (rp + 32) * 64 + cg * 8);
-        const uint2 z2 = lds64p(sbase + Z_OFF + s * 128 + cg * 8);
+        const uint2 z2 = lds64p(sbase + L::Z_OFF + s * 128 + cg * 8);
         const uint32_t w[2][2] = {{r0.x, r0.y}, {r1.x, r1.y}};
         const uint32_t zw[2] = {z2.x, z2.y};
-        const uint32_t ab = sbase + A_OFF + sa * A_BYTES;
+        const uint32_t ab = sbase + L::A_OFF + sa * A_BYTES;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int cc = c ^ csel;
           const int cw = 2 * cg + cc;
-          const uint4 s4 = lds128p(sbase + S_OFF + s * 256 + cw * 16);
+          const uint4 s4 = lds128p(sbase + L::S_OFF + s * 256 + cw * 16);
           const uint32_t sp[4] = {s4.x, s4.y, s4.z, s4.w};  // (s[2j], s[2j+1])
           uint32_t zp[4];                                    // (1024+z[2j], 1024+z[2j+1])
           const uint32_t zc = cc ? zw[1] : zw[0];
@@ -371,14 +489,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&full_a[sa]);
+          if constexpr (kPair) {
+            if (leader) {
+              // warp 2 also arms the bytes the peer's eight dequant warps will signal
+              if (warp == 2) mbar_arrive_expect_tx(&full_a[sa], kDQ * 4u);
+              else mbar_arrive(&full_a[sa]);
+            } else {
+              // A half in place (ordered before this async-proxy store by the fence above):
+              // signal the leader with a 4-byte store counted on its full_a[sa]
+              st_async_dsmem_f32(reinterpret_cast<float*>(smem + L::SIG_OFF + 4 * (warp - 2)),
+                                 &full_a[sa], 0u, 0.f);
+            }
+          } else {
+            mbar_arrive(&full_a[sa]);
+          }
           mbar_arrive(&empty_t[s]);
         }
 #ifdef AWQ_PREFILL_DEBUG_ROLE
         AWQ_PREFILL_DEBUG_ROLE(1, 3);
 #endif
-        if (++s == kST) { s = 0; ph ^= 1u; }
-        if (++sa == kSA) { sa = 0; pha ^= 1u; }
+        if (++s == L::ST) { s = 0; ph ^= 1u; }
+        if (++sa == L::SA) { sa = 0; pha ^= 1u; }
       }
     }
   } else {
@@ -386,12 +517,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
     const int nl = quad * 32 + lane;     // output column inside the tile
     int li = 0;
-    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++li) {
-      const int b = li & 1;
+    for (int tile = tile0; tile < p.tiles; tile += tstep, ++li) {
+      const int b = li % kAccBufs;
       const int m0 = (tile % p.tiles_t) * kBT;
-      const int n = (tile / p.tiles_t) * kBN + nl;
+      const int n = (tile / p.tiles_t) * (8 * kTileWords) + static_cast<int>(rank) * kBN + nl;
       const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
-      if (!wait(&tfull[b], static_cast<uint32_t>((li >> 1) & 1))) break;
+      if (!wait(&tfull[b], static_cast<uint32_t>((li / kAccBufs) & 1))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(b * kBT);
@@ -410,19 +541,57 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[b]);
+      if (lane == 0) {
+        if constexpr (kPair) mbar_arrive_rank(&tempty[b], 0u);  // the leader's barrier
+        else mbar_arrive(&tempty[b]);
+      }
     }
   }
 
   __syncthreads();
+  // Pair mode: neither CTA leaves while the other may still arrive on its barriers.
+  if constexpr (kPair) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
+    if constexpr (kPair)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols) : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols) : "memory");
   }
 }
 
-std::once_flag g_attr_once;
-cudaError_t g_attr_err = cudaSuccess;
+template <bool kPair>
+cudaError_t set_smem_attr() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(prefill_kernel<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Layout<kPair>::SMEM));
+  });
+  return err;
+}
+
+// Clusters of two that fit at once (one CTA per SM), from the occupancy API; cached.
+int pair_capacity() {
+  static std::once_flag once;
+  static int cap = 0;
+  std::call_once(once, [] {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Layout<true>::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&cap, prefill_kernel<true>, &cfg) != cudaSuccess) cap = 0;
+    (void)cudaGetLastError();
+  });
+  return cap;
+}
 
 }  // namespace
 
@@ -439,17 +608,27 @@ bool prefill_supported(const GemmProblem& p, const char** why) {
   return true;
 }
 
+// Pair mode (cta_group::2) is exact but measured slower than one CTA per tile on GB300
+// (1079 vs 1143 TFLOP/s at M = 2048, K = 4096, N = 11008): each stage's activation copy in
+// the peer waits on a commit from the other SM and the peer's readiness signal crosses
+// back, and the rings that fit in shared memory do not cover that loop.  Off by default.
+#ifndef AWQ_PREFILL_PAIR
+#define AWQ_PREFILL_PAIR 0
+#endif
+
 cudaError_t launch_prefill(const GemmProblem& p) {
-  std::call_once(g_attr_once, [] {
-    g_attr_err = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(SMEM));
-  });
-  if (g_attr_err != cudaSuccess) return g_attr_err;
+  cudaError_t e = set_smem_attr<false>();
+  if (e == cudaSuccess) e = set_smem_attr<true>();
+  if (e != cudaSuccess) return e;
+  // Pair mode (two CTAs per 256 x 256 tile) when enabled and pairs of SMs can be co-scheduled.
+  const int pairs = AWQ_PREFILL_PAIR ? pair_capacity() : 0;
+  const bool pair = pairs > 0;
   PrefillParams pp;
   const char* why = nullptr;
   const int C = p.N / 8;
   const int ngrp = p.K / p.G;
-  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kBK, kXRows,
+  const int x_rows = pair ? kBT / 2 : kBT;
+  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kBK, x_rows,
                     CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
       !make_tmap_2d(&pp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, 16, kBK,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
@@ -460,19 +639,38 @@ cudaError_t launch_prefill(const GemmProblem& p) {
     return cudaErrorInvalidValue;
   pp.bias = p.bias;
   pp.y = p.y;
-  cudaError_t e = status_word_ptr(&pp.status);
+  e = status_word_ptr(&pp.status);
   if (e != cudaSuccess) return e;
   pp.M = p.M; pp.K = p.K; pp.N = p.N; pp.C = C; pp.G = p.G;
   pp.tiles_t = (p.M + kBT - 1) / kBT;
-  const long long tiles = (long long)pp.tiles_t * ((p.N + kBN - 1) / kBN);
+  const int tile_n = pair ? 2 * kBN : kBN;
+  const long long tiles = (long long)pp.tiles_t * ((p.N + tile_n - 1) / tile_n);
   if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
   pp.tiles = static_cast<int>(tiles);
+  if (pair) {
+    const int clusters = pp.tiles < pairs ? pp.tiles : pairs;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Layout<true>::SMEM;
+    cfg.stream = p.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, prefill_kernel<true>, pp);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = pp.tiles < sms ? pp.tiles : sms;
-  prefill_kernel<<<grid, kThreads, SMEM, p.stream>>>(pp);
+  prefill_kernel<false><<<grid, kThreads, Layout<false>::SMEM, p.stream>>>(pp);
   return cudaGetLastError();
 }
 
