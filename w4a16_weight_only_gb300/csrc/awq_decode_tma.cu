@@ -552,7 +552,7 @@ constexpr int kRecvCap = 64 * 1024;  // bytes of the rank-0 receive region
 #define AWQ_DECODE_WAVE_FILL_PCT 90
 #endif
 #ifndef AWQ_DECODE_MAX_CTAS_PER_SM
-#define AWQ_DECODE_MAX_CTAS_PER_SM 2
+#define AWQ_DECODE_MAX_CTAS_PER_SM 3
 #endif
 constexpr int kMaxSlots = AWQ_DECODE_MAX_SLOTS;             // ring slots per warp
 constexpr int kWaveFillPct = AWQ_DECODE_WAVE_FILL_PCT;      // share of the slots one wave may fill
@@ -677,6 +677,10 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   long long best_grid = -1;
   for (int cs = 1; cs <= kMaxCluster; ++cs) {
     if (cs > 1 && cs * kNW > TS) break;
+    // Power-of-two clusters only: they still pack into SMs left partly free by the
+    // previous launch (programmatic dependent launch overlap); 3-, 5-, 6-CTA clusters
+    // were measured to split into a second wave there.
+    if ((cs & (cs - 1)) != 0) continue;
     if ((long long)cs * x_rows * 8 * GE::CW_W * 4 > kRecvCap) break;
     const long long grid = tiles * cs;
     long long per_sm = (grid + dl.sms - 1) / dl.sms;
