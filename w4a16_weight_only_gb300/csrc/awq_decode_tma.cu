@@ -73,6 +73,8 @@ struct __align__(64) TmaDecodeParams {
   int x_pitch;  // bytes per activation slot: 128 (one row, unswizzled) or 1024*TB
   // Byte offsets inside the 1024-aligned dynamic shared memory (activation rings at 0).
   int w_off, m_off, zl_off, bias_off, bar_off, recv_off;
+  int owners;  // CTAs of the cluster that finish a slice of the output tile (1 or cs)
+  int slice;   // floats of the packed partial each owner finishes (multiple of 4)
 };
 
 template <int TB, int CWL>
@@ -167,7 +169,9 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
     for (int s = 0; s < S; ++s) mbar_init(&my_bars[s], 1);
     if (warp == 0) {
       mbar_init(red_bar, 1);
-      if (rank == 0) mbar_arrive_expect_tx(red_bar, cs * static_cast<uint32_t>(pack_n) * 4u);
+      const int my_len = min(p.slice, max(0, pack_n - static_cast<int>(rank) * p.slice));
+      if (static_cast<int>(rank) < p.owners)
+        mbar_arrive_expect_tx(red_bar, cs * static_cast<uint32_t>(my_len) * 4u);
     }
     fence_mbar_init();
   }
@@ -455,10 +459,11 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
 #if AWQ_DECODE_LATE_TRIGGER
   launch_dependents();
 #endif
-  // Reduce: the warps of the CTA in a fixed order into a packed partial [token][column],
-  // pushed (st.async, counted on the rank-0 CTA's mbarrier) into the rank-0 CTA, which
-  // adds the cluster's partials in rank order, adds the bias and stores y.  Other CTAs
-  // exit right after their push.
+  // Reduce: the warps of the CTA in a fixed order into a packed partial [token][column];
+  // slice o of it is pushed (st.async, counted on the owner's mbarrier) into owner CTA o,
+  // which adds the cluster's partials of its slice in rank order, adds the bias and stores
+  // y.  One owner (rank 0) for small partials, every CTA a slice for large ones; CTAs that
+  // own nothing exit right after their push.
   __syncthreads();  // the ring is reused as the reduction buffer
   // Per-warp partials in fragment order (row X = (mi*TB + tb)*4 + e, 32 lanes), one float
   // of padding per 4 rows so the packed-order reads below spread over the banks.
@@ -500,10 +505,12 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
 #ifdef AWQ_DECODE_DEBUG_TIME
   AWQ_DECODE_DEBUG_TIME(7);
 #endif
-  for (int v = threadIdx.x; v < pack_n / 4; v += kNW * 32)
-    st_async_dsmem_v4(recv + rank * pack_n + 4 * v, red_bar, 0u,
-                      *reinterpret_cast<const float4*>(pack + 4 * v));
-  if (rank != 0) {
+  for (int v = threadIdx.x; v < pack_n / 4; v += kNW * 32) {
+    const int owner = (4 * v) / p.slice;
+    st_async_dsmem_v4(recv + rank * p.slice + (4 * v - owner * p.slice), red_bar,
+                      static_cast<uint32_t>(owner), *reinterpret_cast<const float4*>(pack + 4 * v));
+  }
+  if (static_cast<int>(rank) >= p.owners) {
 #ifdef AWQ_DECODE_DEBUG_TIME
     AWQ_DECODE_DEBUG_TIME(3);
 #endif
@@ -514,11 +521,13 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
   AWQ_DECODE_DEBUG_TIME(8);
 #endif
   const float* bias_s = reinterpret_cast<const float*>(smem + p.bias_off);
-  for (int i = threadIdx.x; got && i < pack_n; i += kNW * 32) {
+  const int lo = static_cast<int>(rank) * p.slice;
+  const int hi = min(pack_n, lo + p.slice);
+  for (int i = lo + threadIdx.x; got && i < hi; i += kNW * 32) {
     const int t = i / (8 * GE::CW_W), col = i - t * 8 * GE::CW_W;
     if (m0 + t >= p.M || 8 * cw0 + col >= p.N) continue;
     float sum = 0.f;
-    for (uint32_t r = 0; r < cs; ++r) sum += recv[r * pack_n + i];
+    for (uint32_t r = 0; r < cs; ++r) sum += recv[r * p.slice + (i - lo)];
     p.y[(long long)(m0 + t) * p.N + 8 * cw0 + col] = __float2half_rn(sum + bias_s[col]);
   }
 #ifdef AWQ_DECODE_DEBUG_TIME
@@ -531,13 +540,19 @@ struct Variant {
   bool sub;
 };
 
+#ifndef AWQ_DECODE_TB1_MAX_M
+#define AWQ_DECODE_TB1_MAX_M 8
+#endif
 Variant pick(const GemmProblem& p) {
-  if (p.M <= 8) return Variant{1, 2, true};
+  if (p.M <= AWQ_DECODE_TB1_MAX_M) return Variant{1, 2, true};
   if (p.M <= 16) return Variant{2, 1, true};
   return Variant{4, 1, false};
 }
 
-constexpr int kRecvCap = 64 * 1024;  // bytes of the rank-0 receive region
+constexpr int kRecvCap = 64 * 1024;  // bytes of a CTA's receive region
+// One owner sums cs partials of pack_n floats; from this many values on (and clusters of
+// at least 4) every CTA of the cluster finishes a slice instead.
+constexpr int kMultiOwnerMin = 4096;
 // Launch-plan limits (compile-time; overridable for tuning builds).
 #ifndef AWQ_DECODE_LATE_TRIGGER
 #define AWQ_DECODE_LATE_TRIGGER 0
@@ -562,6 +577,7 @@ constexpr int kMaxCtasPerSm = AWQ_DECODE_MAX_CTAS_PER_SM;   // CTAs of one launc
 struct Plan {
   int cs = 0, slots = 0, x_pitch = 0;
   int w_off = 0, m_off = 0, zl_off = 0, bias_off = 0, bar_off = 0, recv_off = 0, smem = 0;
+  int owners = 1, slice = 0;
 };
 
 template <int TB, int CWL>
@@ -577,7 +593,10 @@ Plan layout(int cs, int slots, int x_rows) {
   pl.bias_off = pl.zl_off + kNW * 128;
   pl.bar_off = pl.bias_off + 8 * GE::CW_W * 4;
   pl.recv_off = ((pl.bar_off + (kNW * slots + 1) * 8 + 15) / 16) * 16;
-  pl.smem = 1024 + pl.recv_off + cs * x_rows * 8 * GE::CW_W * 4;
+  const int pack_n = x_rows * 8 * GE::CW_W;
+  pl.owners = (pack_n * cs >= kMultiOwnerMin && cs >= 4) ? cs : 1;
+  pl.slice = pl.owners == 1 ? pack_n : ((pack_n + 4 * cs - 1) / (4 * cs)) * 4;
+  pl.smem = 1024 + pl.recv_off + cs * pl.slice * 4;
   return pl;
 }
 
@@ -681,7 +700,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
     // previous launch (programmatic dependent launch overlap); 3-, 5-, 6-CTA clusters
     // were measured to split into a second wave there.
     if ((cs & (cs - 1)) != 0) continue;
-    if ((long long)cs * x_rows * 8 * GE::CW_W * 4 > kRecvCap) break;
+    if (layout<TB, CWL>(cs, 1, x_rows).smem - layout<TB, CWL>(cs, 1, x_rows).recv_off - 1024 > kRecvCap) break;
     const long long grid = tiles * cs;
     long long per_sm = (grid + dl.sms - 1) / dl.sms;
     if (per_sm < 1) per_sm = 1;
@@ -746,6 +765,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   dp.x_pitch = pl.x_pitch;
   dp.w_off = pl.w_off; dp.m_off = pl.m_off; dp.zl_off = pl.zl_off;
   dp.bias_off = pl.bias_off; dp.bar_off = pl.bar_off; dp.recv_off = pl.recv_off;
+  dp.owners = pl.owners; dp.slice = pl.slice;
 
   const int nt = (C + GE::CW_W - 1) / GE::CW_W;
   const int mz = (p.M + 8 * TB - 1) / (8 * TB);
