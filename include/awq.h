@@ -146,6 +146,14 @@ awq_path_t awq_gemm_select_path(int64_t M, int64_t K, int64_t N, int64_t group_s
  * last check (its output is then unspecified), AWQ_OK otherwise. */
 awq_status_t awq_device_status(awq_stream_t stream);
 
+/* Failure-detection self test.  Launches one thread that waits on an mbarrier nothing
+ * ever completes, bounded by limit_ns of wall time (1e3 .. 1e9, else
+ * AWQ_ERR_INVALID_ARGUMENT): the wait gives up the same way a stalled stage of the GEMM
+ * kernels would -- it sets the device status word and the kernel returns, with no fault,
+ * trap or hang -- so a following awq_device_status returns AWQ_ERR_TIMEOUT (and clears
+ * the word).  Asynchronous on `stream`; one launch.  No counterpart on the pages. */
+awq_status_t awq_selftest_wait_timeout(uint64_t limit_ns, awq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

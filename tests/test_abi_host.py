@@ -123,6 +123,16 @@ def test_valid_call_without_sm103_device_is_refused(lib):
     assert lib.awq_last_error() != b""
 
 
+def test_selftest_argument_checks_are_host_side(lib):
+    # out-of-range limits are refused before any device access
+    assert lib.awq_selftest_wait_timeout(0, None) == 1
+    assert lib.awq_selftest_wait_timeout(2_000_000_000, None) == 1
+    # a valid limit without a CC 10.3 device is refused, nothing launched
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.awq_selftest_wait_timeout(1_000_000, None) == DEVICE
+
+
 def test_binding_raises_loudly_without_library(tmp_path):
     from w4a16_weight_only_gb300 import _binding
     with pytest.raises(RuntimeError, match="missing"):

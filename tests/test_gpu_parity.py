@@ -168,6 +168,19 @@ def test_device_status_clean(awq):
     awq.device_status()
 
 
+def test_bounded_wait_gives_up_and_reports(awq):
+    """A wait that nothing completes gives up after its limit, sets the status word and
+    returns (no fault, no hang); the context stays usable afterwards."""
+    awq.device_status()
+    awq.selftest_wait_timeout(2_000_000)
+    with pytest.raises(awq.AwqError, match="bounded wait"):
+        awq.device_status()
+    awq.device_status()  # cleared by the read
+    d = synth.awq_linear(9600, 1, 256, 64, group_size=128)
+    assert_close(run_gemm(awq, d), oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 128),
+                 "after timeout")
+
+
 # --------------------------------------------- every workload at full size ----
 
 def _sample(M, N, rng, n=2048):

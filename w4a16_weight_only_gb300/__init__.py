@@ -5,7 +5,7 @@ in ``csrc/``).  This package only builds it (``build.py``) and marshals argument
 (``_binding.py``); PyTorch supplies device memory and streams.
 """
 from ._binding import (AwqError, PATHS, awq_dequant, awq_gemm, device_status, last_error,
-                       load_library, runtime_available, select_path)
+                       load_library, runtime_available, select_path, selftest_wait_timeout)
 
 __all__ = ["AwqError", "PATHS", "awq_dequant", "awq_gemm", "device_status", "last_error",
-           "load_library", "runtime_available", "select_path"]
+           "load_library", "runtime_available", "select_path", "selftest_wait_timeout"]

@@ -31,6 +31,7 @@ SIGNATURES = {
     "awq_gemm_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp]),
     "awq_gemm_select_path": (_i32, [_i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "awq_device_status": (_i32, [_vp]),
+    "awq_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
 }
 
 _lib = None
@@ -168,3 +169,8 @@ def select_path(x, qweight, qzeros, scales, bias=None, group_size=128, out=None)
 
 def device_status(stream=None):
     _check(load_library().awq_device_status(_stream(stream)))
+
+
+def selftest_wait_timeout(limit_ns=2_000_000, stream=None):
+    """Launch the bounded-wait self test (awq.h); the next device_status() raises AwqError."""
+    _check(load_library().awq_selftest_wait_timeout(int(limit_ns), _stream(stream)))

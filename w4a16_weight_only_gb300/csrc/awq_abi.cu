@@ -238,4 +238,15 @@ awq_status_t awq_device_status(awq_stream_t stream) {
   return ok();
 }
 
+awq_status_t awq_selftest_wait_timeout(uint64_t limit_ns, awq_stream_t stream) {
+  if (limit_ns < 1000ull || limit_ns > 1000000000ull)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "limit_ns must be within [1e3, 1e9]");
+  awq_status_t st = check_device();
+  if (st != AWQ_OK) return st;
+  const cudaError_t e = awq::launch_selftest_wait(static_cast<unsigned long long>(limit_ns),
+                                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the wait self test");
+  return ok();
+}
+
 }  // extern "C"

@@ -54,6 +54,9 @@ cudaError_t status_word_ptr(unsigned int** ptr);
 bool prefill_supported(const GemmProblem& p, const char** why);
 cudaError_t launch_prefill(const GemmProblem& p);
 
+// Failure-detection self test: a bounded wait that nothing completes (see awq.h).
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
+
 // Loads the module (used by awq_runtime_available to prove the sm_103a image runs here).
 cudaError_t probe_kernel_image(cudaFuncAttributes* attr);
 
