@@ -44,18 +44,28 @@ namespace {
 using namespace ptx;
 
 constexpr int kBN = 128;   // output columns per tile (UMMA M)
-constexpr int kBT = 256;   // activation rows per tile (UMMA N)
+#ifndef AWQ_PREFILL_BT
+#define AWQ_PREFILL_BT 256
+#endif
+#ifndef AWQ_PREFILL_ST
+#define AWQ_PREFILL_ST 4
+#endif
+#ifndef AWQ_PREFILL_SA
+#define AWQ_PREFILL_SA 4
+#endif
+constexpr int kBT = AWQ_PREFILL_BT;   // activation rows per tile (UMMA N)
 constexpr int kBK = 64;    // K per stage
-constexpr int kST = 4;     // TMA ring depth
-constexpr int kSA = 4;     // dequantized-A ring depth
+constexpr int kST = AWQ_PREFILL_ST;  // TMA ring depth
+constexpr int kSA = AWQ_PREFILL_SA;  // dequantized-A ring depth
 constexpr int kDQ = 8;                        // dequant warps
 constexpr int kThreads = (2 + kDQ + 4) * 32;  // producer, MMA, dequant, epilogue
 #ifndef AWQ_PREFILL_ACC_BUFS
 #define AWQ_PREFILL_ACC_BUFS 2
 #endif
 constexpr int kAccBufs = AWQ_PREFILL_ACC_BUFS;      // TMEM accumulators (tile overlap)
-constexpr int kTmemCols = kAccBufs * kBT;           // 256 or 512 fp32 columns
-static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation size");
+// TMEM columns allocated (a power of two): the accumulators take kAccBufs * kBT of them.
+constexpr int kTmemCols = kAccBufs * kBT <= 256 ? 256 : 512;
+static_assert(kAccBufs * kBT <= 512 && kBT % 32 == 0 && kBT <= 256, "accumulators");
 constexpr uint32_t kMagic = 0x64006400u;
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
 constexpr unsigned int kStatusPrefillTimeout = 0x2u;
