@@ -121,7 +121,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 template <int TB>
 constexpr int kMinBlocks = TB == 1 ? AWQ_DECODE_MIN_BLOCKS_M8 : AWQ_DECODE_MIN_BLOCKS_WIDE;
 
-template <int TB, int CWL, bool kSub>
+// kOne: exactly one activation row (M = 1): the second token of each MMA column pair is
+// never folded or stored.
+template <int TB, int CWL, bool kSub, bool kOne>
 __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
     decode_tma_kernel(const __grid_constant__ TmaDecodeParams p) {
   using GE = Geo<TB, CWL>;
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
   int grp_of = j0 / spg;
   int grp_left = spg - (j0 - grp_of * spg);  // stages left in grp_of, counting j0
 
-  const bool one_row = p.x_rows == 1;
+  constexpr bool one_row = kOne;
   auto fold = [&]() {
     // acc += scale * (2^24 or 2^20 * sum x c - zero * sum x) for the group just finished.
     // Nibble nib of block hb is MMA mi = 4 (hb / 2) + nib, A rows g8 + 8 (hb % 2).
@@ -475,6 +477,7 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
     for (int tb = 0; tb < TB; ++tb)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
+        if (kOne && (e & 1)) continue;  // token 2q+1: never read back
         const int X = (mi * TB + tb) * 4 + e;
         mine[X * 32 + lane + (X >> 2)] = acc[mi][tb][e];
       }
@@ -630,9 +633,9 @@ cudaError_t dev_limits(DevLimits* out) {
 }
 
 // Co-resident clusters of size cs at `smem` bytes per CTA (occupancy API).
-template <int TB, int CWL, bool S>
+template <int TB, int CWL, bool S, bool O>
 int max_clusters(int cs, int smem) {
-  auto kern = decode_tma_kernel<TB, CWL, S>;
+  auto kern = decode_tma_kernel<TB, CWL, S, O>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, 1, 1);
   cfg.blockDim = dim3(kNW * 32, 1, 1);
@@ -657,7 +660,7 @@ int max_clusters(int cs, int smem) {
 // each warp keeping at least one 64-row stage; ties go to the smaller cluster.  Ring
 // depth: as many slots as the shared memory left per CTA allows, up to the warp's stage
 // count.  Cached per shape.
-template <int TB, int CWL, bool S>
+template <int TB, int CWL, bool S, bool O>
 cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   using GE = Geo<TB, CWL>;
   static std::mutex mu;
@@ -682,7 +685,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    auto kern = decode_tma_kernel<TB, CWL, S>;
+    auto kern = decode_tma_kernel<TB, CWL, S, O>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dl.smem_optin);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -715,7 +718,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
     // single wave with slack, checked against the occupancy API at this size
     bool fits = false;
     while (true) {
-      long long cap = (long long)max_clusters<TB, CWL, S>(cs, pl.smem) * cs;
+      long long cap = (long long)max_clusters<TB, CWL, S, O>(cs, pl.smem) * cs;
       if (cap > (long long)kMaxCtasPerSm * dl.sms) cap = (long long)kMaxCtasPerSm * dl.sms;
       if (grid * 100 <= cap * kWaveFillPct) { fits = true; break; }
       if (pl.slots <= red_slots || pl.slots <= 1) break;
@@ -734,11 +737,11 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   return cudaSuccess;
 }
 
-template <int TB, int CWL, bool S>
+template <int TB, int CWL, bool S, bool O>
 cudaError_t launch_v(const GemmProblem& p) {
   using GE = Geo<TB, CWL>;
   Plan pl;
-  cudaError_t e = plan_for<TB, CWL, S>(p, &pl);
+  cudaError_t e = plan_for<TB, CWL, S, O>(p, &pl);
   if (e != cudaSuccess) return e;
   const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
 
@@ -783,7 +786,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S>, dp);
+  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S, O>, dp);
 }
 
 }  // namespace
@@ -805,9 +808,9 @@ bool decode_tma_supported(const GemmProblem& p, const char** why) {
 
 cudaError_t launch_decode_tma(const GemmProblem& p) {
   const Variant v = pick(p);
-  if (v.TB == 1) return launch_v<1, 2, true>(p);
-  if (v.TB == 2) return launch_v<2, 1, true>(p);
-  return launch_v<4, 1, false>(p);
+  if (v.TB == 1) return p.M == 1 ? launch_v<1, 2, true, true>(p) : launch_v<1, 2, true, false>(p);
+  if (v.TB == 2) return launch_v<2, 1, true, false>(p);
+  return launch_v<4, 1, false, false>(p);
 }
 
 }  // namespace awq
