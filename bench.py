@@ -70,10 +70,10 @@ def step_bytes(lins):
 # `python bench.py --steps 60 --warmup 3 --no-cpu-baseline` summarised in
 # profiles/decode_tma_7b_m1_bench_launches.md; valid only for the kernel source it was
 # measured on (SHA-256 of the files below), else reported as null.
-TRAFFIC_BYTES_PER_LAUNCH = 18_587_300
+TRAFFIC_BYTES_PER_LAUNCH = 18_588_100
 TRAFFIC_SOURCES = {
     "w4a16_weight_only_gb300/csrc/awq_decode_tma.cu":
-        "06e02613c89bb3a6c06dab85e3f4f96234dae355fac3132b790db9917836d3f6",
+        "0d06859ef34b52f620bccd807e0e9c5a7bb3f58e0af9f9c4abe26a2d1b04249a",
     "w4a16_weight_only_gb300/csrc/awq_ptx.cuh":
         "594d27bfcdf987daf3de5b15bf561a524931a1ca3859ce6920e4c94921cfbf09",
 }
