@@ -106,6 +106,32 @@ def test_gemm_small_vs_oracle(awq, M, K, N, G, bias, path):
     assert_close(y, y_ref, f"{path} M={M} K={K} N={N} G={G}")
 
 
+# One token: the decode kernel gives each quantization group a warp spans its own MMA
+# token column (up to 8 groups per warp; beyond that the general small-batch variant runs),
+# with 8-warp CTAs where 4-warp ones would leave a warp 5 or more 64-row stages.  With 224
+# column tiles (N = 28672) the launch plan takes clusters of one CTA, so with G = 64 a warp
+# of an 8-warp CTA spans K / 512 groups: 3, 4 (first token column of each lane only), 4-5
+# (K = 2112: second column used by some warps), 8, and 16 for K = 8192 (general variant).
+# K = 4096, N = 11008 stays on 4-warp CTAs (4 stages a warp).
+ONE_TOKEN = [(1536, 28672, 64, True), (2048, 28672, 64, False), (2112, 28672, 64, True),
+             (4096, 28672, 64, False), (8192, 28672, 64, True), (4096, 4096, -1, True),
+             (11008, 4096, 64, False), (4096, 11008, 64, True), (28672, 8192, 128, False)]
+
+
+@pytest.mark.parametrize("K,N,G,bias", ONE_TOKEN)
+def test_one_token_group_spans(awq, K, N, G, bias):
+    d = synth.awq_linear(8500 + K + N + G, 1, K, N, group_size=G, bias=bias)
+    y = run_gemm(awq, d, "decode")
+    args = (d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    if K * N <= 32 * 1024 * 1024:
+        assert_close(y, oracle.gemm(*args), f"one token K={K} N={N} G={G}")
+    else:  # every column of a tile sees all of the tile's warps: sample columns
+        cols = np.concatenate([np.arange(512), np.arange(N - 512, N),
+                               np.random.default_rng(2).integers(0, N, 3072)])
+        rows = np.zeros_like(cols)
+        assert_close(y[rows, cols], oracle.gemm_sampled(*args, rows, cols), f"one token K={K} N={N} G={G}")
+
+
 @pytest.mark.parametrize("M", [1, 5, 8, 12, 16, 30, 32, 40, 300])
 @pytest.mark.parametrize("path", ["decode", "prefill", "generic"])
 def test_gemm_exact_case_bitwise(awq, M, path):

@@ -36,6 +36,7 @@
 // cluster's rank-0 CTA, which adds the partials in rank order, adds the bias and stores
 // y; the other CTAs exit right after their push.  No global workspace, no atomics:
 // repeated calls are bitwise identical.
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -51,12 +52,17 @@ using namespace ptx;
 #ifndef AWQ_DECODE_WARPS
 #define AWQ_DECODE_WARPS 4
 #endif
-constexpr int kNW = AWQ_DECODE_WARPS;  // warps per CTA
+constexpr int kNW = AWQ_DECODE_WARPS;  // warps per CTA (the one-token variant may take 8)
+#ifndef AWQ_DECODE_L2_PREFETCH
+#define AWQ_DECODE_L2_PREFETCH 0  // L2 prefetch of the stages past the ring, before the wait
+#endif
 constexpr int kRS = 64;      // rows of K per stage
 constexpr int kMaxCluster = 16;
 constexpr uint32_t kMagic = 0x64006400u;     // fp16 1024 in both halves
 constexpr uint32_t kOnes = 0x3C003C00u;      // fp16 1.0 in both halves
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 200 ms per wait
+// One-token variant: quantization groups a warp may span (one MMA token column each).
+constexpr int kOneGroups = 8;
 constexpr unsigned int kStatusDecodeTimeout = 0x1u;
 
 struct __align__(64) TmaDecodeParams {
@@ -70,6 +76,7 @@ struct __align__(64) TmaDecodeParams {
   int M, K, N, C, G;
   int x_rows;   // rows of the activation box: min(M, 8*TB)
   int slots;    // ring slots per warp
+  int meta_n;   // meta entries per warp: ring slots, or (one token) groups of the warp
   int x_pitch;  // bytes per activation slot: 128 (one row, unswizzled) or 1024*TB
   // Byte offsets inside the 1024-aligned dynamic shared memory (activation rings at 0).
   int w_off, m_off, zl_off, bias_off, bar_off, recv_off;
@@ -77,7 +84,7 @@ struct __align__(64) TmaDecodeParams {
   int slice;   // floats of the packed partial each owner finishes (multiple of 4)
 };
 
-template <int TB, int CWL>
+template <int TB, int CWL, int NW>
 struct Geo {
   static constexpr int CW_W = 8 * CWL;              // packed column-words per warp / CTA
   static constexpr int W_BYTES = kRS * CW_W * 4;    // packed weight tile per stage
@@ -89,7 +96,7 @@ struct Geo {
   static constexpr int E = NMMA * TB * 4 * 32;      // partial sums per warp
   static constexpr int PACK = 8 * TB * 8 * CW_W;    // packed partial: tokens x columns
   static constexpr int EP = E + E / 128;            // partials per warp, padded
-  static constexpr int RED_BYTES = (kNW * EP + PACK) * 4;  // reuses the activation+weight rings
+  static constexpr int RED_BYTES = (NW * EP + PACK) * 4;  // reuses the activation+weight rings
 };
 
 __device__ __forceinline__ uint2 lds64(uint32_t a) {
@@ -118,15 +125,23 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 #ifndef AWQ_DECODE_MIN_BLOCKS_WIDE
 #define AWQ_DECODE_MIN_BLOCKS_WIDE 3
 #endif
-template <int TB>
-constexpr int kMinBlocks = TB == 1 ? AWQ_DECODE_MIN_BLOCKS_M8 : AWQ_DECODE_MIN_BLOCKS_WIDE;
+// 8-warp CTAs: two per SM (up to 128 registers a thread).
+template <int TB, int NW>
+constexpr int kMinBlocks = NW == 8 ? 2 : (TB == 1 ? AWQ_DECODE_MIN_BLOCKS_M8 : AWQ_DECODE_MIN_BLOCKS_WIDE);
 
-// kOne: exactly one activation row (M = 1): the second token of each MMA column pair is
-// never folded or stored.
-template <int TB, int CWL, bool kSub, bool kOne>
-__global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
+// kOne: exactly one activation row (M = 1).  The MMA's 8 token columns would hold 7
+// zero columns, so they hold the warp's quantization groups instead: the activations of a
+// stage of group slot gs (groups counted from the warp's first one, at most kOneGroups)
+// go into token column 2 (gs % 4) + gs / 4, the other columns read zeros.  Each column
+// then accumulates sum x c (and, in the ones-MMA, sum x) of one group on its own, so no
+// accumulator is folded or cleared inside the loop; after it every lane folds the groups
+// of its own columns once (zero and scale rows kept in a per-warp stash indexed by group
+// slot) and the reduction also sums over the four lanes of each quad.
+template <int TB, int CWL, bool kSub, bool kOne, int NW>
+__global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     decode_tma_kernel(const __grid_constant__ TmaDecodeParams p) {
-  using GE = Geo<TB, CWL>;
+  static_assert(NW == 4 || NW == 8, "4 or 8 warps per CTA");
+  using GE = Geo<TB, CWL, NW>;
   constexpr int NMMA = GE::NMMA;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -145,14 +160,15 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
 
   // 32-bit arithmetic throughout: TS * P < 2^31 (checked on the host).
   const uint32_t TS = static_cast<uint32_t>(p.K / kRS);
-  const uint32_t P = cs * kNW;
-  const uint32_t wid = rank * kNW + static_cast<uint32_t>(warp);
+  const uint32_t P = cs * NW;
+  const uint32_t wid = rank * NW + static_cast<uint32_t>(warp);
   const int j0 = static_cast<int>(TS * wid / P);
   const int j1 = static_cast<int>(TS * (wid + 1) / P);
 
   unsigned char* x_ring = smem + (size_t)warp * S * p.x_pitch;
   unsigned char* w_ring = smem + p.w_off + (size_t)warp * S * GE::W_BYTES;
-  unsigned char* m_ring = smem + p.m_off + (size_t)warp * S * GE::META_SLOT;
+  // Meta rows: a ring of S slots, or (kOne) a stash with one entry per group of the warp.
+  unsigned char* m_ring = smem + p.m_off + (size_t)warp * p.meta_n * GE::META_SLOT;
   uint64_t* my_bars = bars + warp * S;
   const uint32_t x_ring_u32 = smem_u32(x_ring);
   const uint32_t w_ring_u32 = smem_u32(w_ring);
@@ -163,7 +179,7 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
 #endif
   // Reduction mbarrier (after all ring barriers): in the cluster's rank-0 CTA it counts
   // the bytes of the partial sums every CTA of the cluster pushes (its own included).
-  uint64_t* red_bar = bars + kNW * S;
+  uint64_t* red_bar = bars + NW * S;
   const int pack_n = p.x_rows * 8 * GE::CW_W;  // floats of one packed partial
   if (lane == 0) {
     prefetch_tmap(&p.tm_w);
@@ -187,7 +203,8 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
   const int spg = p.G / kRS;  // stages per quantization group
   const uint32_t x_tx = static_cast<uint32_t>(p.x_rows) * kRS * 2;
   // Issue-side stage/group counters (advanced by lane 0 only; no division per stage).
-  int iss_grp = j0 / spg;
+  const int g_first = j0 / spg;  // the warp's first group
+  int iss_grp = g_first;
   int iss_left = spg - (j0 - iss_grp * spg);  // stages left in iss_grp, counting the next
   auto issue_weights = [&](int slot, int j) {
     uint64_t* bar = &my_bars[slot];
@@ -195,8 +212,9 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
     mbar_arrive_expect_tx(bar, GE::W_BYTES + x_tx + (meta ? GE::META_TX : 0u));
     tma_load_2d(w_ring + slot * GE::W_BYTES, &p.tm_w, bar, cw0, j * kRS);
     if (meta) {
-      tma_load_2d(m_ring + slot * GE::META_SLOT, &p.tm_z, bar, cw0, iss_grp);
-      tma_load_2d(m_ring + slot * GE::META_SLOT + 128, &p.tm_s, bar, 8 * cw0, iss_grp);
+      unsigned char* md = m_ring + (kOne ? iss_grp - g_first : slot) * GE::META_SLOT;
+      tma_load_2d(md, &p.tm_z, bar, cw0, iss_grp);
+      tma_load_2d(md + 128, &p.tm_s, bar, 8 * cw0, iss_grp);
     }
     if (--iss_left == 0) {
       ++iss_grp;
@@ -211,7 +229,22 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
   // output stores at the end) are ordered after it.
   if (lane == 0)
     for (int s = 0; s < S && j0 + s < j1; ++s) issue_weights(s, j0 + s);
+#if AWQ_DECODE_L2_PREFETCH
+  // Stages past the ring: pull their packed weights (and any group rows they open) into
+  // L2 now, so the refills after the wait hit L2.  Whole tiles only (no partial boxes).
+  if (lane == 0 && cw0 + GE::CW_W <= p.C)
+    for (int j = j0 + S; j < j1; ++j) {
+      tma_prefetch_l2_2d(&p.tm_w, cw0, j * kRS);
+      if (j % spg == 0) {
+        tma_prefetch_l2_2d(&p.tm_z, cw0, j / spg);
+        tma_prefetch_l2_2d(&p.tm_s, 8 * cw0, j / spg);
+      }
+    }
+#endif
   grid_dependency_wait();
+#ifdef AWQ_DECODE_DEBUG_TIME
+  AWQ_DECODE_DEBUG_TIME(5);
+#endif
   if (lane == 0)
     for (int s = 0; s < S && j0 + s < j1; ++s) issue_x(s, j0 + s);
 #if !AWQ_DECODE_LATE_TRIGGER
@@ -251,7 +284,7 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
   // Bias of this CTA's columns, read now (off the critical path) for the epilogue.
   {
     float* bias_s = reinterpret_cast<float*>(smem + p.bias_off);
-    for (int i = threadIdx.x; i < 8 * GE::CW_W; i += kNW * 32) {
+    for (int i = threadIdx.x; i < 8 * GE::CW_W; i += NW * 32) {
       const int n = 8 * cw0 + i;
       bias_s[i] = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
     }
@@ -280,16 +313,34 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
       for (int e = 0; e < 4; ++e) acc[i][b][e] = 0.f;
   float accg[kSub ? NMMA : 1][TB][4];
   float xs[TB][4];
+  if constexpr (kOne) {  // accumulated over the whole range, cleared once
+#pragma unroll
+    for (int i = 0; i < NMMA; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) accg[i][0][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) xs[0][e] = 0.f;
+  }
   uint32_t zh[HB];         // the lane's zero half-word (4 nibbles) of every block
   uint32_t sv[HB][2];      // its scales: nibbles (0, 1) and (2, 3) as half2
   uint32_t zp[kSub ? 1 : HB][4];  // kExact: 1024 + zero, per nibble, both halves
   uint32_t sp[kSub ? 1 : HB][4];  // kExact: scale, per nibble, both halves
+  auto load_meta = [&](uint32_t mb) {
+#pragma unroll
+    for (int hb = 0; hb < HB; ++hb) {
+      const uint32_t wofs = 4u * static_cast<uint32_t>(4 * hb + wq);  // word offset, bytes
+      zh[hb] = lds32(mb + wofs) >> (16 * hh);
+      const uint4 v = lds128(mb + 128 + 4 * wofs);  // the word's 8 scales, column order
+      sv[hb][0] = prmt(v.x, v.y, sc_sel);
+      sv[hb][1] = prmt(v.z, v.w, sc_sel);
+    }
+  };
   int cur = -1;
+  bool x_on = x_real[0];  // kOne: this lane's ldmatrix row is the current group's column
   // Group of stage j is j / spg; tracked incrementally (one division per warp).
   int grp_of = j0 / spg;
   int grp_left = spg - (j0 - grp_of * spg);  // stages left in grp_of, counting j0
 
-  constexpr bool one_row = kOne;
   auto fold = [&]() {
     // acc += scale * (2^24 or 2^20 * sum x c - zero * sum x) for the group just finished.
     // Nibble nib of block hb is MMA mi = 4 (hb / 2) + nib, A rows g8 + 8 (hb % 2).
@@ -311,7 +362,6 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
           for (int tb = 0; tb < TB; ++tb)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              if (TB == 1 && e == 1 && one_row) continue;  // token 2q+1 does not exist
               const float a = __fmaf_rn(sz, xs[tb][e], acc[mi][tb][2 * rs + e]);
               acc[mi][tb][2 * rs + e] = __fmaf_rn(sa, accg[mi][tb][2 * rs + e], a);
             }
@@ -342,17 +392,14 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
     }
     --grp_left;
     const int grp = grp_of;
-    if (grp != cur) {
+    if (kOne && grp != cur) {
+      cur = grp;
+      const int gs = grp - g_first;
+      x_on = (lane & 7) == 2 * (gs & 3) + (gs >> 2);
+    } else if (!kOne && grp != cur) {
       if (kSub && cur >= 0) fold();
       cur = grp;
-#pragma unroll
-      for (int hb = 0; hb < HB; ++hb) {
-        const uint32_t wofs = 4u * static_cast<uint32_t>(4 * hb + wq);  // word offset, bytes
-        zh[hb] = lds32(mb + wofs) >> (16 * hh);
-        const uint4 v = lds128(mb + 128 + 4 * wofs);  // the word's 8 scales, column order
-        sv[hb][0] = prmt(v.x, v.y, sc_sel);
-        sv[hb][1] = prmt(v.z, v.w, sc_sel);
-      }
+      load_meta(mb);
       if (kSub) {
 #pragma unroll
         for (int i = 0; i < NMMA; ++i)
@@ -384,7 +431,7 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
       uint32_t xr[TB][4];
 #pragma unroll
       for (int tb = 0; tb < TB; ++tb)
-        ldmatrix_x4(xr[tb], (x_real[tb] ? xb : zero_line) + x_off[tb][pr]);
+        ldmatrix_x4(xr[tb], ((kOne ? x_on : x_real[tb]) ? xb : zero_line) + x_off[tb][pr]);
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int ks = 2 * pr + kk;
@@ -444,7 +491,39 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
       parity ^= 1u;
     }
   }
-  if (kSub && cur >= 0 && !failed) fold();
+  // kOne: the fold of every group, once; lane (g8, q) owns group slots q and q + 4
+  // (token columns 2q and 2q + 1).  out[mi][rs]: rows g8 + 8 rs of MMA mi.
+  float out[kOne ? NMMA : 1][2];
+  if constexpr (kOne) {
+#pragma unroll
+    for (int mi = 0; mi < NMMA; ++mi) out[mi][0] = out[mi][1] = 0.f;
+    const int ng = j1 > j0 ? (j1 - 1) / spg - g_first + 1 : 0;  // groups of this warp
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int gs = q + 4 * e;
+      if (e == 1 && ng <= 4) continue;  // warp-uniform
+      if (failed || gs >= ng) continue;
+      load_meta(m_ring_u32 + gs * GE::META_SLOT);
+#pragma unroll
+      for (int hb = 0; hb < HB; ++hb)
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&sv[hb][pp]));
+#pragma unroll
+          for (int n2 = 0; n2 < 2; ++n2) {
+            const int nib = 2 * pp + n2;
+            const float sc = n2 ? s2.y : s2.x;
+            const float z = __uint_as_float(((zh[hb] >> (4 * nib)) & 0xFu) | 0x4B000000u) - 8388608.f;
+            const float sa = sc * ((nib & 1) ? 1048576.f : 16777216.f);
+            const float sz = -sc * z;
+            const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
+            const float a = __fmaf_rn(sz, xs[0][e], out[mi][rs]);
+            out[mi][rs] = __fmaf_rn(sa, accg[mi][0][2 * rs + e], a);
+          }
+        }
+    }
+  }
+  if (kSub && !kOne && cur >= 0 && !failed) fold();
   if (failed) {
     // Let copies already issued land (bounded) before the slots are reused below.
     const int issued_end = min(j1, done + S);
@@ -477,17 +556,17 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
     for (int tb = 0; tb < TB; ++tb)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (kOne && (e & 1)) continue;  // token 2q+1: never read back
+        if (kOne && (e & 1)) continue;  // the token-0 slots carry the lane's fold
         const int X = (mi * TB + tb) * 4 + e;
-        mine[X * 32 + lane + (X >> 2)] = acc[mi][tb][e];
+        mine[X * 32 + lane + (X >> 2)] = kOne ? out[mi][e >> 1] : acc[mi][tb][e];
       }
   __syncthreads();
   // Packed partial: element (token t, column col) of the tile, summed over the warps.
   // Column col = 32 hb + 8 (g8 / 2) + 2 nib + g8 % 2 comes from lane group g8, nibble nib
   // of block hb, i.e. MMA mi = 4 (hb / 2) + nib, rows g8 + 8 (hb % 2); g8 varies fastest
   // across threads, the token slowest.
-  float* pack = red + kNW * GE::EP;
-  for (int i = threadIdx.x; i < pack_n; i += kNW * 32) {
+  float* pack = red + NW * GE::EP;
+  for (int i = threadIdx.x; i < pack_n; i += NW * 32) {
     const int g8i = i & 7, r = i >> 3;
     const int nib = r & 3, hb = (r >> 2) % HB, t = (r >> 2) / HB;
     const int col = 32 * hb + 8 * (g8i >> 1) + 2 * nib + (g8i & 1);
@@ -496,7 +575,14 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
     const int e = X * 32 + g8i * 4 + ((t & 7) >> 1) + (X >> 2);
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kNW; ++w) v += red[w * GE::EP + e];
+    for (int w = 0; w < NW; ++w) {
+      if constexpr (kOne) {  // the quad's four lanes hold different groups
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) v += red[w * GE::EP + e + qq];
+      } else {
+        v += red[w * GE::EP + e];
+      }
+    }
     pack[t * 8 * GE::CW_W + col] = v;
   }
   __syncthreads();
@@ -508,7 +594,7 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
 #ifdef AWQ_DECODE_DEBUG_TIME
   AWQ_DECODE_DEBUG_TIME(7);
 #endif
-  for (int v = threadIdx.x; v < pack_n / 4; v += kNW * 32) {
+  for (int v = threadIdx.x; v < pack_n / 4; v += NW * 32) {
     const int owner = (4 * v) / p.slice;
     st_async_dsmem_v4(recv + rank * p.slice + (4 * v - owner * p.slice), red_bar,
                       static_cast<uint32_t>(owner), *reinterpret_cast<const float4*>(pack + 4 * v));
@@ -526,7 +612,7 @@ __global__ void __launch_bounds__(kNW * 32, kMinBlocks<TB>)
   const float* bias_s = reinterpret_cast<const float*>(smem + p.bias_off);
   const int lo = static_cast<int>(rank) * p.slice;
   const int hi = min(pack_n, lo + p.slice);
-  for (int i = lo + threadIdx.x; got && i < hi; i += kNW * 32) {
+  for (int i = lo + threadIdx.x; got && i < hi; i += NW * 32) {
     const int t = i / (8 * GE::CW_W), col = i - t * 8 * GE::CW_W;
     if (m0 + t >= p.M || 8 * cw0 + col >= p.N) continue;
     float sum = 0.f;
@@ -563,6 +649,13 @@ constexpr int kMultiOwnerMin = 4096;
 #ifndef AWQ_DECODE_WIDE_X
 #define AWQ_DECODE_WIDE_X 0
 #endif
+#ifndef AWQ_DECODE_WIDE_STAGES
+#define AWQ_DECODE_WIDE_STAGES 5  // one-token variant: stages per warp that call for 8 warps
+#endif
+constexpr int kWideStages = AWQ_DECODE_WIDE_STAGES;
+#ifndef AWQ_DECODE_WIDE_SLOTS
+#define AWQ_DECODE_WIDE_SLOTS 2  // ring slots per warp of 8-warp CTAs
+#endif
 #ifndef AWQ_DECODE_MAX_SLOTS
 #define AWQ_DECODE_MAX_SLOTS 4
 #endif
@@ -570,7 +663,7 @@ constexpr int kMultiOwnerMin = 4096;
 #define AWQ_DECODE_WAVE_FILL_PCT 90
 #endif
 #ifndef AWQ_DECODE_MAX_CTAS_PER_SM
-#define AWQ_DECODE_MAX_CTAS_PER_SM 3
+#define AWQ_DECODE_MAX_CTAS_PER_SM 4
 #endif
 constexpr int kMaxSlots = AWQ_DECODE_MAX_SLOTS;             // ring slots per warp
 constexpr int kWaveFillPct = AWQ_DECODE_WAVE_FILL_PCT;      // share of the slots one wave may fill
@@ -578,24 +671,26 @@ constexpr int kMaxCtasPerSm = AWQ_DECODE_MAX_CTAS_PER_SM;   // CTAs of one launc
 
 // Cluster size, ring depth and shared memory layout of one launch.
 struct Plan {
-  int cs = 0, slots = 0, x_pitch = 0;
+  int cs = 0, slots = 0, x_pitch = 0, meta_n = 0;
   int w_off = 0, m_off = 0, zl_off = 0, bias_off = 0, bar_off = 0, recv_off = 0, smem = 0;
   int owners = 1, slice = 0;
 };
 
-template <int TB, int CWL>
-Plan layout(int cs, int slots, int x_rows) {
-  using GE = Geo<TB, CWL>;
+template <int TB, int CWL, bool O, int NW>
+Plan layout(int cs, int slots, int x_rows, int groups) {
+  using GE = Geo<TB, CWL, NW>;
+  const int meta_entries = O ? groups : slots;  // stash per group, or ring per slot
   Plan pl;
   pl.cs = cs;
   pl.slots = slots;
+  pl.meta_n = meta_entries;
   pl.x_pitch = (x_rows == 1 && !AWQ_DECODE_WIDE_X) ? 128 : 1024 * TB;
-  pl.w_off = kNW * slots * pl.x_pitch;
-  pl.m_off = pl.w_off + kNW * slots * GE::W_BYTES;
-  pl.zl_off = pl.m_off + kNW * slots * GE::META_SLOT;
-  pl.bias_off = pl.zl_off + kNW * 128;
+  pl.w_off = NW * slots * pl.x_pitch;
+  pl.m_off = pl.w_off + NW * slots * GE::W_BYTES;
+  pl.zl_off = pl.m_off + NW * meta_entries * GE::META_SLOT;
+  pl.bias_off = pl.zl_off + NW * 128;
   pl.bar_off = pl.bias_off + 8 * GE::CW_W * 4;
-  pl.recv_off = ((pl.bar_off + (kNW * slots + 1) * 8 + 15) / 16) * 16;
+  pl.recv_off = ((pl.bar_off + (NW * slots + 1) * 8 + 15) / 16) * 16;
   const int pack_n = x_rows * 8 * GE::CW_W;
   pl.owners = (pack_n * cs >= kMultiOwnerMin && cs >= 4) ? cs : 1;
   pl.slice = pl.owners == 1 ? pack_n : ((pack_n + 4 * cs - 1) / (4 * cs)) * 4;
@@ -632,13 +727,25 @@ cudaError_t dev_limits(DevLimits* out) {
   return cudaSuccess;
 }
 
+// Most quantization groups one warp's stage range touches: warp w of the P warps of a
+// column tile takes stages [TS w / P, TS (w + 1) / P), spg stages per group.
+int max_warp_groups(int TS, int P, int spg) {
+  int worst = 0;
+  for (int w = 0; w < P; ++w) {
+    const int j0 = static_cast<int>(static_cast<long long>(TS) * w / P);
+    const int j1 = static_cast<int>(static_cast<long long>(TS) * (w + 1) / P);
+    if (j1 > j0 && (j1 - 1) / spg - j0 / spg + 1 > worst) worst = (j1 - 1) / spg - j0 / spg + 1;
+  }
+  return worst;
+}
+
 // Co-resident clusters of size cs at `smem` bytes per CTA (occupancy API).
-template <int TB, int CWL, bool S, bool O>
+template <int TB, int CWL, bool S, bool O, int NW>
 int max_clusters(int cs, int smem) {
-  auto kern = decode_tma_kernel<TB, CWL, S, O>;
+  auto kern = decode_tma_kernel<TB, CWL, S, O, NW>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, 1, 1);
-  cfg.blockDim = dim3(kNW * 32, 1, 1);
+  cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -660,9 +767,9 @@ int max_clusters(int cs, int smem) {
 // each warp keeping at least one 64-row stage; ties go to the smaller cluster.  Ring
 // depth: as many slots as the shared memory left per CTA allows, up to the warp's stage
 // count.  Cached per shape.
-template <int TB, int CWL, bool S, bool O>
+template <int TB, int CWL, bool S, bool O, int NW>
 cudaError_t plan_for(const GemmProblem& p, Plan* out) {
-  using GE = Geo<TB, CWL>;
+  using GE = Geo<TB, CWL, NW>;
   static std::mutex mu;
   static std::map<std::tuple<int, int, int, int>, Plan> cache;
   int dev = 0;
@@ -685,7 +792,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    auto kern = decode_tma_kernel<TB, CWL, S, O>;
+    auto kern = decode_tma_kernel<TB, CWL, S, O, NW>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dl.smem_optin);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -694,35 +801,42 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   const long long tiles = (long long)nt * mz;
   const int TS = p.K / kRS;
   const int x_pitch = (x_rows == 1 && !AWQ_DECODE_WIDE_X) ? 128 : 1024 * TB;
-  const int red_slots = (GE::RED_BYTES + kNW * (x_pitch + GE::W_BYTES) - 1) / (kNW * (x_pitch + GE::W_BYTES));
+  const int red_slots = (GE::RED_BYTES + NW * (x_pitch + GE::W_BYTES) - 1) / (NW * (x_pitch + GE::W_BYTES));
   Plan best;
   long long best_grid = -1;
   for (int cs = 1; cs <= kMaxCluster; ++cs) {
-    if (cs > 1 && cs * kNW > TS) break;
+    if (cs > 1 && cs * NW > TS) break;
     // Power-of-two clusters only: they still pack into SMs left partly free by the
     // previous launch (programmatic dependent launch overlap); 3-, 5-, 6-CTA clusters
     // were measured to split into a second wave there.
     if ((cs & (cs - 1)) != 0) continue;
-    if (layout<TB, CWL>(cs, 1, x_rows).smem - layout<TB, CWL>(cs, 1, x_rows).recv_off - 1024 > kRecvCap) break;
+    // one-token variant, 4 warps: kOneGroups stash entries per warp whatever the warp's
+    // group span (sizing the stash to the span gave one shape a deeper ring, which measured
+    // slower); 8 warps: as many entries as the warp's groups.
+    const int groups = !O ? 0
+                       : NW == 4 ? kOneGroups
+                                 : std::min(kOneGroups, max_warp_groups(TS, cs * NW, p.G / kRS));
+    if (layout<TB, CWL, O, NW>(cs, 1, x_rows, groups).smem - layout<TB, CWL, O, NW>(cs, 1, x_rows, groups).recv_off - 1024 > kRecvCap) break;
     const long long grid = tiles * cs;
     long long per_sm = (grid + dl.sms - 1) / dl.sms;
     if (per_sm < 1) per_sm = 1;
     if (per_sm > kMaxCtasPerSm && cs > 1) continue;
     const int budget = static_cast<int>(dl.smem_per_sm / per_sm) - dl.reserved - 256;
-    const int spw = (TS + cs * kNW - 1) / (cs * kNW);  // stages of the busiest warp
-    int slots = spw < kMaxSlots ? spw : kMaxSlots;
-    while (slots > 1 && layout<TB, CWL>(cs, slots, x_rows).smem > budget) --slots;
+    const int spw = (TS + cs * NW - 1) / (cs * NW);  // stages of the busiest warp
+    const int max_slots = NW == 8 ? AWQ_DECODE_WIDE_SLOTS : kMaxSlots;
+    int slots = spw < max_slots ? spw : max_slots;
+    while (slots > 1 && layout<TB, CWL, O, NW>(cs, slots, x_rows, groups).smem > budget) --slots;
     if (slots < red_slots) slots = red_slots;
-    Plan pl = layout<TB, CWL>(cs, slots, x_rows);
+    Plan pl = layout<TB, CWL, O, NW>(cs, slots, x_rows, groups);
     if (pl.smem > dl.smem_optin) continue;
     // single wave with slack, checked against the occupancy API at this size
     bool fits = false;
     while (true) {
-      long long cap = (long long)max_clusters<TB, CWL, S, O>(cs, pl.smem) * cs;
+      long long cap = (long long)max_clusters<TB, CWL, S, O, NW>(cs, pl.smem) * cs;
       if (cap > (long long)kMaxCtasPerSm * dl.sms) cap = (long long)kMaxCtasPerSm * dl.sms;
       if (grid * 100 <= cap * kWaveFillPct) { fits = true; break; }
       if (pl.slots <= red_slots || pl.slots <= 1) break;
-      pl = layout<TB, CWL>(cs, pl.slots - 1, x_rows);
+      pl = layout<TB, CWL, O, NW>(cs, pl.slots - 1, x_rows, groups);
     }
     if (!fits && cs > 1) continue;
     const long long score = fits ? grid : 0;
@@ -737,11 +851,11 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   return cudaSuccess;
 }
 
-template <int TB, int CWL, bool S, bool O>
+template <int TB, int CWL, bool S, bool O, int NW>
 cudaError_t launch_v(const GemmProblem& p) {
-  using GE = Geo<TB, CWL>;
+  using GE = Geo<TB, CWL, NW>;
   Plan pl;
-  cudaError_t e = plan_for<TB, CWL, S, O>(p, &pl);
+  cudaError_t e = plan_for<TB, CWL, S, O, NW>(p, &pl);
   if (e != cudaSuccess) return e;
   const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
 
@@ -765,6 +879,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   dp.M = p.M; dp.K = p.K; dp.N = p.N; dp.C = C; dp.G = p.G;
   dp.x_rows = x_rows;
   dp.slots = pl.slots;
+  dp.meta_n = pl.meta_n;
   dp.x_pitch = pl.x_pitch;
   dp.w_off = pl.w_off; dp.m_off = pl.m_off; dp.zl_off = pl.zl_off;
   dp.bias_off = pl.bias_off; dp.bar_off = pl.bar_off; dp.recv_off = pl.recv_off;
@@ -774,7 +889,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   const int mz = (p.M + 8 * TB - 1) / (8 * TB);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nt * pl.cs), static_cast<unsigned>(mz), 1);
-  cfg.blockDim = dim3(kNW * 32, 1, 1);
+  cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
   cfg.stream = p.stream;
   cudaLaunchAttribute attr[2];
@@ -786,7 +901,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S, O>, dp);
+  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S, O, NW>, dp);
 }
 
 }  // namespace
@@ -802,15 +917,32 @@ bool decode_tma_supported(const GemmProblem& p, const char** why) {
     return false;
   }
   if ((p.M + 31) / 32 > 65535) { *why = "M too large for the decode grid"; return false; }
-  if ((long long)(p.K / kRS) * kMaxCluster * kNW >= (1LL << 31)) { *why = "K too large for the decode kernel"; return false; }
+  if ((long long)(p.K / kRS) * kMaxCluster * 8 >= (1LL << 31)) { *why = "K too large for the decode kernel"; return false; }
   return true;
 }
 
 cudaError_t launch_decode_tma(const GemmProblem& p) {
   const Variant v = pick(p);
-  if (v.TB == 1) return p.M == 1 ? launch_v<1, 2, true, true>(p) : launch_v<1, 2, true, false>(p);
-  if (v.TB == 2) return launch_v<2, 1, true, false>(p);
-  return launch_v<4, 1, false, false>(p);
+  if (v.TB == 1) {
+    if (p.M == 1) {
+      // One token: at most kOneGroups groups per warp.  8-warp CTAs where 4-warp ones
+      // would leave a warp kWideStages or more stages (long K: more warps share the work).
+      const int TS = p.K / kRS, spg = p.G / kRS;
+      Plan p4;
+      cudaError_t e = plan_for<1, 2, true, true, 4>(p, &p4);
+      if (e != cudaSuccess) return e;
+      if ((TS + 4 * p4.cs - 1) / (4 * p4.cs) >= kWideStages) {
+        Plan p8;
+        e = plan_for<1, 2, true, true, 8>(p, &p8);
+        if (e != cudaSuccess) return e;
+        if (max_warp_groups(TS, 8 * p8.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 8>(p);
+      }
+      if (max_warp_groups(TS, 4 * p4.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 4>(p);
+    }
+    return launch_v<1, 2, true, false, kNW>(p);
+  }
+  if (v.TB == 2) return launch_v<2, 1, true, false, kNW>(p);
+  return launch_v<4, 1, false, false, kNW>(p);
 }
 
 }  // namespace awq
