@@ -70,12 +70,12 @@ def step_bytes(lins):
 # `python bench.py --steps 60 --warmup 3 --no-cpu-baseline` summarised in
 # profiles/decode_tma_7b_m1_bench_launches.md; valid only for the kernel source it was
 # measured on (SHA-256 of the files below), else reported as null.
-TRAFFIC_BYTES_PER_LAUNCH = 18_588_100
+TRAFFIC_BYTES_PER_LAUNCH = 18_588_150
 TRAFFIC_SOURCES = {
     "w4a16_weight_only_gb300/csrc/awq_decode_tma.cu":
-        "0d06859ef34b52f620bccd807e0e9c5a7bb3f58e0af9f9c4abe26a2d1b04249a",
+        "40f606ca8535e28a9ab964ac7c520ea10c562294398eab11e23f6a8fc30a1777",
     "w4a16_weight_only_gb300/csrc/awq_ptx.cuh":
-        "594d27bfcdf987daf3de5b15bf561a524931a1ca3859ce6920e4c94921cfbf09",
+        "d6e2eb90c8015d39adb895095ee759e2fb2397c609be5e9c4fded03a2807c0e5",
 }
 
 
