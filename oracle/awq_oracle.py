@@ -28,12 +28,28 @@ What it computes, and where each step comes from:
   ``W`` the fp32 dequant widened exactly; bias broadcast over rows as in a
   linear layer (format page, "bias ... optional, shape [out_features]").
 
+* Round-to-nearest quantization (:func:`quantize_rtn`; GPTQModel wiki "AWQ",
+  "Group quantization and zero points", the table of the asymmetric and
+  symmetric modes): per output channel and group of ``G`` input features,
+  asymmetric ``scale = max(max - min, 1e-5) / 15``, ``zero = clamp(-round(min /
+  scale), 0, 15)``, ``code = clamp(round(w / scale) + zero, 0, 15)``;
+  symmetric ``scale = max(max|w|, 1e-5) / 7``, ``code = clamp(round(w /
+  scale), -8, 7) + 8`` with zero 8 (the page: packing shifts signed codes to
+  unsigned and supplies zero 2^(bits-1)).  Readings where the page is silent:
+  fp32 arithmetic on the fp16 weights (each operation correctly rounded), the
+  scale rounded to fp16 as a checkpoint stores it and the codes taken against
+  that stored scale, round half to even.
+
 Pins (tests/test_oracle.py, run without a GPU): ORDER and its inverse from
 the wiki's "Saved formats and packing" section, a hand-packed word, AWQ-004
 (sequential-nibble decode differs), AWQ-005 (zero equal to code gives an
 exact 0), group_size -1 equals group_size K, symmetric zero 8, exact
 rational dequant values, a pure-Python brute-force GEMM written separately,
-and an exact-arithmetic GEMM case.  Every function here has at least one pin.
+and an exact-arithmetic GEMM case; for the quantizer a hand-worked group
+(tests/golden/rtn_worked_example.txt), exact round trips of weights that lie on
+a grid spanning the whole code range, the half-step error bound, the clamped
+degenerate groups and group_size -1 equal to group_size K.  Every function
+here has at least one pin.
 """
 from __future__ import annotations
 
@@ -184,3 +200,41 @@ def within_tolerance(y, y_ref, rel: float = 1e-2):
     worst = float(np.max(ratio)) if (ratio.size and finite) else (0.0 if finite else float("inf"))
     ok = bool(finite and np.all(err <= bound))
     return ok, worst
+
+
+def quantize_rtn(w, group_size, sym=False):
+    """Round-to-nearest group quantization of a linear layer's fp16 weight into
+    the AWQ GEMM layout (GPTQModel wiki "AWQ", "Group quantization and zero
+    points").
+
+    ``w``: fp16 ``[N, K]`` (out_features x in_features: one row per output
+    channel; groups of ``G`` consecutive input features along each row).
+    Returns ``(qweight int32 [K, N/8], qzeros int32 [K/G, N/8], scales fp16
+    [K/G, N])``, packed with ORDER like a checkpoint.
+    """
+    w = np.asarray(w)
+    if w.dtype != np.float16:
+        raise ValueError("w must be fp16")
+    N, K = w.shape
+    G = resolve_group_size(K, group_size)
+    if N % 8 != 0:
+        raise ValueError("out_features must be a multiple of 8")
+    wf = w.astype(np.float32).reshape(N, K // G, G)  # exact widening
+    if not sym:
+        wmax = wf.max(axis=2)
+        wmin = wf.min(axis=2)
+        rng = np.maximum(wmax - wmin, np.float32(1e-5))           # fp32 subtraction
+        scale16 = (rng / np.float32(15)).astype(np.float16)        # fp32 division, RNE to fp16
+        s = scale16.astype(np.float32)
+        zero = np.clip(-np.rint(wmin / s), 0, 15)
+        code = np.clip(np.rint(wf / s[:, :, None]) + zero[:, :, None], 0, 15)
+    else:
+        amax = np.maximum(np.abs(wf).max(axis=2), np.float32(1e-5))
+        scale16 = (amax / np.float32(7)).astype(np.float16)
+        s = scale16.astype(np.float32)
+        zero = np.full(scale16.shape, 8.0, dtype=np.float32)
+        code = np.clip(np.rint(wf / s[:, :, None]), -8, 7) + 8
+    codes_kn = code.reshape(N, K).T.astype(np.int64)     # [K, N]
+    zeros_gn = zero.T.astype(np.int64)                   # [K/G, N]
+    return pack_codes(codes_kn), pack_codes(zeros_gn), np.ascontiguousarray(scale16.T)
+

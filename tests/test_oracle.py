@@ -264,3 +264,117 @@ def test_synth_is_seeded_and_shaped():
     codes = oracle.unpack_codes(awq_linear(6, 1, 512, 512)["qweight"])
     counts = np.bincount(codes.ravel(), minlength=16)
     assert counts.min() > 0.9 * codes.size / 16   # uniform codes 0..15
+
+
+# ------------------------------------------------ round-to-nearest quantizer ----
+# GPTQModel wiki "AWQ", "Group quantization and zero points": the asymmetric and symmetric
+# 4-bit modes.  The pins below rest on a group worked by hand, on exact round trips of
+# weights lying on a grid that spans the whole code range (the formulas then recover the
+# grid exactly), and on the half-step error bound of rounding.
+
+RTN_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "rtn_worked_example.txt")
+
+
+def _rtn_golden_rows():
+    rows = []
+    with open(RTN_GOLDEN) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            mode, w, scale_hex, zero, codes = line.split()
+            rows.append((mode, [float(v) for v in w.split(",")], int(scale_hex, 16), int(zero),
+                         [int(v) for v in codes.split(",")]))
+    return rows
+
+
+def _rtn_unpacked(w, G, sym):
+    qw, qz, sc = oracle.quantize_rtn(w, G, sym)
+    return oracle.unpack_codes(qw), oracle.unpack_codes(qz), sc
+
+
+@pytest.mark.parametrize("row", _rtn_golden_rows(), ids=lambda r: f"{r[0]}:{r[1]}")
+def test_rtn_worked_example(row):
+    mode, vals, scale_bits, zero, codes = row
+    # every output channel (row of the [N, K] weight) holds the worked group
+    w = np.tile(np.array(vals, dtype=np.float16), (8, 1))
+    c, z, sc = _rtn_unpacked(w, 4, mode == "sym")
+    assert c.shape == (4, 8) and z.shape == (1, 8) and sc.shape == (1, 8)
+    assert (c == np.array(codes)[:, None]).all()
+    assert (z == zero).all()
+    assert (sc.view(np.uint16) == scale_bits).all()
+
+
+def _grid_weight(rng, N, K, G, sym):
+    """W[n, k] = (code - zero) * s with s a power of two, every group spanning the full
+    code range (asymmetric: codes 0 and 15 present; symmetric: -7 or 7 as the largest
+    magnitude), so the page's formulas must give back codes, zeros and scales exactly."""
+    ng = K // G
+    p = rng.integers(4, 12, size=(N, ng))
+    s = np.ldexp(1.0, -p)                                     # exact in fp16
+    if sym:
+        code = rng.integers(-7, 8, size=(N, ng, G))
+        code[:, :, 0] = np.where(rng.random((N, ng)) < 0.5, -7, 7)
+        zero = np.full((N, ng), 8)
+        w = code * s[:, :, None]
+        code = code + 8
+    else:
+        code = rng.integers(0, 16, size=(N, ng, G))
+        code[:, :, 0] = 0
+        code[:, :, 1] = 15
+        zero = rng.integers(0, 16, size=(N, ng))
+        w = (code - zero[:, :, None]) * s[:, :, None]
+    w16 = w.reshape(N, K).astype(np.float16)
+    assert np.array_equal(w16.astype(np.float64), w.reshape(N, K))  # on the grid exactly
+    return w16, code.reshape(N, K), zero, s
+
+
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("N,K,G", [(8, 32, 16), (16, 64, 64), (24, 96, 32)])
+def test_rtn_recovers_grid_exactly(sym, N, K, G):
+    rng = np.random.default_rng(N * K + G + sym)
+    w16, code, zero, s = _grid_weight(rng, N, K, G, sym)
+    c, z, sc = _rtn_unpacked(w16, G, sym)
+    assert np.array_equal(c, code.T)
+    assert np.array_equal(z, zero.T)
+    assert np.array_equal(sc.astype(np.float64), s.T)
+
+
+def test_rtn_error_is_at_most_half_a_step():
+    rng = np.random.default_rng(7)
+    N, K, G = 32, 256, 64
+    w16 = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+    c, z, sc = _rtn_unpacked(w16, G, False)
+    s = sc.astype(np.float64)[np.arange(K) // G]             # [K, N]
+    rec = (c - z[np.arange(K) // G]) * s
+    err = np.abs(rec - w16.astype(np.float64).T)
+    # the range holds 15 steps, so no code or zero clamps for these groups
+    assert (err <= 0.5 * s * (1 + 1e-3)).all()
+
+
+def test_rtn_symmetric_zero_is_eight_and_zero_maps_to_eight():
+    rng = np.random.default_rng(8)
+    w16 = (rng.standard_normal((16, 128)) * 0.1).astype(np.float16)
+    w16[:, 5] = 0
+    c, z, _ = _rtn_unpacked(w16, 32, True)
+    assert (z == 8).all()
+    assert (c[5] == 8).all()
+
+
+def test_rtn_group_minus_one_equals_group_k():
+    rng = np.random.default_rng(9)
+    w16 = rng.standard_normal((8, 96)).astype(np.float16)
+    for sym in (False, True):
+        a = oracle.quantize_rtn(w16, -1, sym)
+        b = oracle.quantize_rtn(w16, 96, sym)
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
+
+
+def test_rtn_rejects_bad_shapes():
+    with pytest.raises(ValueError):
+        oracle.quantize_rtn(np.zeros((12, 64), np.float16), 32)
+    with pytest.raises(ValueError):
+        oracle.quantize_rtn(np.zeros((8, 64), np.float16), 24)
+    with pytest.raises(ValueError):
+        oracle.quantize_rtn(np.zeros((8, 64), np.float32), 32)
