@@ -500,6 +500,46 @@ def run_sweep(args, local):
         print(json.dumps(line), flush=True)
         del x, qw, qz, sc, bias, y
         torch.cuda.empty_cache()
+    if not args.case or "quantize" in args.case:
+        run_quantize_sweep(awq, timed, hbm, hbm_kind)
+
+
+def quantize_bytes(N, K, G):
+    """Bytes awq_quantize_rtn must move: the fp16 weight once, the packed outputs once."""
+    ng = K // G
+    return 2 * N * K + N * K // 2 + ng * N // 2 + 2 * ng * N
+
+
+def run_quantize_sweep(awq, timed, hbm, hbm_kind):
+    """awq_quantize_rtn on the 7B linears' fp16 weights [N, K], G = 128, both modes: HBM
+    GB/s over back-to-back calls on rotating weight copies (together > 3x L2)."""
+    import torch
+    for (N, K) in ((4096, 4096), (11008, 4096), (4096, 11008)):
+        G = 128
+        nbytes = quantize_bytes(N, K, G)
+        R = max(2, int(3 * L2_BYTES // (2 * N * K)) + 1)
+        g = torch.Generator(device="cuda").manual_seed(N + K)
+        ws = [(torch.randn((N, K), generator=g, device="cuda") * 0.02).half() for _ in range(R)]
+        for sym in (False, True):
+            outs = []
+            fn_i = [0]
+
+            def fn():
+                w = ws[fn_i[0] % R]
+                fn_i[0] += 1
+                outs.append(awq.awq_quantize_rtn(w, group_size=G, sym=sym))
+                if len(outs) > R:
+                    outs.pop(0)
+            timed(fn, R)
+            t = sorted(timed(fn, 2 * R) for _ in range(5))[2]
+            awq.device_status()
+            print(json.dumps({"workload": f"quantize_rtn_{'sym' if sym else 'asym'}_{N}x{K}_g{G}",
+                              "N": N, "K": K, "group_size": G, "sym": sym, "us": t,
+                              "GB_s": nbytes / t / 1e3, "frac_hbm": nbytes / t / 1e3 / hbm,
+                              "weight_copies": R, "hbm_peak_GB_s": hbm, "hbm_peak": hbm_kind}),
+                  flush=True)
+        del ws
+        torch.cuda.empty_cache()
 
 
 def main(argv=None):

@@ -94,6 +94,35 @@ awq_status_t awq_dequant(const int32_t* qweight, const int32_t* qzeros, const vo
                          void* w_out, awq_dtype_t out_dtype, awq_stream_t stream);
 
 /*
+ * awq_quantize_rtn -- round-to-nearest 4-bit group quantization of a linear layer's fp16
+ * weight into this layout (GPTQModel wiki "AWQ", "Group quantization and zero points":
+ * the asymmetric and symmetric modes of its table; packing with ORDER as the format
+ * page's "Reader" unpacks it).  Per output channel n and group g of G input features:
+ *
+ *   sym == 0:  scale = max(max - min, 1e-5) / 15
+ *              zero  = clamp(-round(min / scale), 0, 15)
+ *              code  = clamp(round(w / scale) + zero, 0, 15)
+ *   sym == 1:  scale = max(max |w|, 1e-5) / 7,  zero = 8
+ *              code  = clamp(round(w / scale), -8, 7) + 8
+ *
+ * Arithmetic is fp32 on the fp16 weights with every operation correctly rounded; the
+ * scale is rounded to fp16 (as stored) and the codes are taken against the stored scale;
+ * round is half to even.  Weights must be finite.
+ *
+ *   w_f16        fp16 [N, K] row-major: out_features x in_features (an nn.Linear weight)
+ *   qweight      int32 [K, N/8] out, qzeros int32 [K/G, N/8] out, scales_f16 fp16 [K/G, N] out
+ *
+ * Requirements: K > 0, N >= 0, N % 8 == 0, group_size == -1 or (> 0 and K % group_size
+ * == 0), the group size a multiple of 8 and K / group_size <= 65535; w 16-byte aligned,
+ * qweight/qzeros 4-byte aligned, scales 2-byte aligned; outputs must not overlap w.
+ * N == 0 returns AWQ_OK without a launch.  Argument errors are returned before any device
+ * access.  One kernel launch otherwise; asynchronous on `stream`.
+ */
+awq_status_t awq_quantize_rtn(const void* w_f16, int64_t N, int64_t K, int64_t group_size,
+                              int sym, int32_t* qweight, int32_t* qzeros, void* scales_f16,
+                              awq_stream_t stream);
+
+/*
  * awq_gemm -- fused W4A16 linear (the wiki's awq_gemm_forward in "Native GEMM" /
  * "Native AWQ runtime helpers"; fp32 accumulation always, as with its default
  * GPTQMODEL_FP32_ACCUM):

@@ -137,3 +137,21 @@ def test_binding_raises_loudly_without_library(tmp_path):
     from w4a16_weight_only_gb300 import _binding
     with pytest.raises(RuntimeError, match="missing"):
         _binding.load_library(str(tmp_path / "nope.so"))
+
+
+def test_quantize_argument_checks_are_host_side(lib):
+    q = lib.awq_quantize_rtn
+    W = P(0x300000)  # 16-byte aligned fake device address
+    assert q(W, 12, 64, 32, 0, A, A, B, None) == SHAPE       # N not a multiple of 8
+    assert q(W, 8, 48, 12, 0, A, A, B, None) == SHAPE        # group size not a multiple of 8
+    assert q(W, 8, 64, 24, 0, A, A, B, None) == SHAPE        # K % G != 0
+    assert q(W, 8, 524288, 8, 0, A, A, B, None) == SHAPE     # more than 65535 groups
+    assert q(W, 8, 64, 32, 2, A, A, B, None) == INVALID      # sym not 0/1
+    assert q(W, 8, 0, 32, 0, A, A, B, None) == INVALID       # K == 0
+    assert q(None, 8, 64, 32, 0, A, A, B, None) == INVALID
+    assert q(P(0x300008), 8, 64, 32, 0, A, A, B, None) == MISALIGNED
+    assert q(W, 0, 64, 32, 0, None, None, None, None) == 0   # N == 0: no launch
+    import torch
+    if not torch.cuda.is_available():
+        assert q(W, 8, 64, 32, 1, A, A, B, None) == DEVICE
+

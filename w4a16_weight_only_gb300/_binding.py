@@ -32,6 +32,7 @@ SIGNATURES = {
     "awq_gemm_select_path": (_i32, [_i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "awq_device_status": (_i32, [_vp]),
     "awq_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
+    "awq_quantize_rtn": (_i32, [_vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -156,6 +157,24 @@ def awq_dequant(qweight, qzeros, scales, group_size=128, out_dtype=torch.float16
                          DTYPE_F32 if out_dtype == torch.float32 else DTYPE_F16, _stream(stream))
     _check(st)
     return out
+
+
+def awq_quantize_rtn(w, group_size=128, sym=False, stream=None):
+    """Round-to-nearest 4-bit group quantization of an fp16 linear weight w [N, K]
+    (out_features x in_features) via the library's awq_quantize_rtn.  Returns
+    (qweight int32 [K, N/8], qzeros int32 [K/G, N/8], scales fp16 [K/G, N])."""
+    lib = load_library()
+    N, K = w.shape
+    dev = w.device
+    _need(w, "w", torch.float16, (N, K), dev)
+    ng = _groups(K, group_size)
+    qweight = torch.empty((K, N // 8), dtype=torch.int32, device=dev)
+    qzeros = torch.empty((ng, N // 8), dtype=torch.int32, device=dev)
+    scales = torch.empty((ng, N), dtype=torch.float16, device=dev)
+    st = lib.awq_quantize_rtn(_ptr(w), N, K, group_size, 1 if sym else 0, _ptr(qweight),
+                              _ptr(qzeros), _ptr(scales), _stream(stream))
+    _check(st)
+    return qweight, qzeros, scales
 
 
 def select_path(x, qweight, qzeros, scales, bias=None, group_size=128, out=None) -> str:

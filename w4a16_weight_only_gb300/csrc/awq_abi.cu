@@ -190,6 +190,32 @@ awq_status_t awq_dequant(const int32_t* qweight, const int32_t* qzeros, const vo
   return ok();
 }
 
+awq_status_t awq_quantize_rtn(const void* w_f16, int64_t N, int64_t K, int64_t group_size,
+                              int sym, int32_t* qweight, int32_t* qzeros, void* scales_f16,
+                              awq_stream_t stream) {
+  int G = 0;
+  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  if (st != AWQ_OK) return st;
+  if (sym != 0 && sym != 1) return fail(AWQ_ERR_INVALID_ARGUMENT, "sym must be 0 or 1 (got %d)", sym);
+  if (G % 8 != 0)
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "group size %d is not a multiple of 8 (16-byte group rows)", G);
+  if (K / G > 65535) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "K / group_size must be at most 65535");
+  if (N == 0) return ok();
+  if (!w_f16 || !qweight || !qzeros || !scales_f16)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "null pointer among w, qweight, qzeros, scales");
+  if (!al(w_f16, 16)) return fail(AWQ_ERR_MISALIGNED, "w must be 16-byte aligned");
+  if (!al(qweight, 4) || !al(qzeros, 4)) return fail(AWQ_ERR_MISALIGNED, "qweight/qzeros must be 4-byte aligned");
+  if (!al(scales_f16, 2)) return fail(AWQ_ERR_MISALIGNED, "scales must be 2-byte aligned");
+  st = check_device();
+  if (st != AWQ_OK) return st;
+  const cudaError_t e = awq::launch_quantize_rtn(
+      static_cast<const __half*>(w_f16), static_cast<int>(N), static_cast<int>(K), G, sym == 1,
+      reinterpret_cast<uint32_t*>(qweight), reinterpret_cast<uint32_t*>(qzeros),
+      static_cast<__half*>(scales_f16), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "awq_quantize_rtn launch");
+  return ok();
+}
+
 awq_status_t awq_gemm_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
                          const void* scales_f16, const void* bias_f16, int64_t M, int64_t K,
                          int64_t N, int64_t group_size, void* y_f16, awq_path_t path,

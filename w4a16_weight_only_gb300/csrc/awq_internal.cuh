@@ -28,6 +28,11 @@ enum Path { kAuto = 0, kDecode = 1, kPrefill = 2, kGeneric = 3 };
 cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
                            int G, void* out, bool out_f32, cudaStream_t stream);
 
+// Round-to-nearest group quantization (awq_quantize_rtn): w fp16 [N, K] -> qweight
+// [K, N/8], qzeros [K/G, N/8], scales [K/G, N].
+cudaError_t launch_quantize_rtn(const __half* w, int N, int K, int G, bool sym, uint32_t* qw,
+                                uint32_t* qz, __half* sc, cudaStream_t stream);
+
 // Any valid shape / alignment.
 cudaError_t launch_generic(const GemmProblem& p);
 
