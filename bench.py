@@ -512,33 +512,37 @@ def quantize_bytes(N, K, G):
 
 def run_quantize_sweep(awq, timed, hbm, hbm_kind):
     """awq_quantize_rtn on the 7B linears' fp16 weights [N, K], G = 128, both modes: HBM
-    GB/s over back-to-back calls on rotating weight copies (together > 3x L2)."""
+    GB/s over CUDA-graph replays of calls on rotating weight copies (together > 3x L2)."""
     import torch
+    stream = torch.cuda.Stream()
     for (N, K) in ((4096, 4096), (11008, 4096), (4096, 11008)):
         G = 128
         nbytes = quantize_bytes(N, K, G)
         R = max(2, int(3 * L2_BYTES // (2 * N * K)) + 1)
-        g = torch.Generator(device="cuda").manual_seed(N + K)
-        ws = [(torch.randn((N, K), generator=g, device="cuda") * 0.02).half() for _ in range(R)]
+        gen = torch.Generator(device="cuda").manual_seed(N + K)
+        ws = [(torch.randn((N, K), generator=gen, device="cuda") * 0.02).half() for _ in range(R)]
+        outs = [(torch.empty((K, N // 8), dtype=torch.int32, device="cuda"),
+                 torch.empty((K // G, N // 8), dtype=torch.int32, device="cuda"),
+                 torch.empty((K // G, N), dtype=torch.float16, device="cuda")) for _ in range(R)]
+        calls = max(R, (60 // R) * R)
         for sym in (False, True):
-            outs = []
-            fn_i = [0]
-
-            def fn():
-                w = ws[fn_i[0] % R]
-                fn_i[0] += 1
-                outs.append(awq.awq_quantize_rtn(w, group_size=G, sym=sym))
-                if len(outs) > R:
-                    outs.pop(0)
-            timed(fn, R)
-            t = sorted(timed(fn, 2 * R) for _ in range(5))[2]
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for i in range(2 * R):
+                    awq.awq_quantize_rtn(ws[i % R], G, sym, out=outs[i % R], stream=stream)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(calls):
+                        awq.awq_quantize_rtn(ws[i % R], G, sym, out=outs[i % R], stream=stream)
+            t = sorted(timed(g.replay, 1) / calls for _ in range(5))[2]
             awq.device_status()
             print(json.dumps({"workload": f"quantize_rtn_{'sym' if sym else 'asym'}_{N}x{K}_g{G}",
                               "N": N, "K": K, "group_size": G, "sym": sym, "us": t,
                               "GB_s": nbytes / t / 1e3, "frac_hbm": nbytes / t / 1e3 / hbm,
-                              "weight_copies": R, "hbm_peak_GB_s": hbm, "hbm_peak": hbm_kind}),
-                  flush=True)
-        del ws
+                              "weight_copies": R, "launches_per_graph": calls,
+                              "hbm_peak_GB_s": hbm, "hbm_peak": hbm_kind}), flush=True)
+            del g
+        del ws, outs
         torch.cuda.empty_cache()
 
 

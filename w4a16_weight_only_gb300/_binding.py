@@ -159,18 +159,25 @@ def awq_dequant(qweight, qzeros, scales, group_size=128, out_dtype=torch.float16
     return out
 
 
-def awq_quantize_rtn(w, group_size=128, sym=False, stream=None):
+def awq_quantize_rtn(w, group_size=128, sym=False, out=None, stream=None):
     """Round-to-nearest 4-bit group quantization of an fp16 linear weight w [N, K]
     (out_features x in_features) via the library's awq_quantize_rtn.  Returns
-    (qweight int32 [K, N/8], qzeros int32 [K/G, N/8], scales fp16 [K/G, N])."""
+    (qweight int32 [K, N/8], qzeros int32 [K/G, N/8], scales fp16 [K/G, N]), written into
+    `out` (a tuple of those three tensors) when given."""
     lib = load_library()
     N, K = w.shape
     dev = w.device
     _need(w, "w", torch.float16, (N, K), dev)
     ng = _groups(K, group_size)
-    qweight = torch.empty((K, N // 8), dtype=torch.int32, device=dev)
-    qzeros = torch.empty((ng, N // 8), dtype=torch.int32, device=dev)
-    scales = torch.empty((ng, N), dtype=torch.float16, device=dev)
+    if out is None:
+        qweight = torch.empty((K, N // 8), dtype=torch.int32, device=dev)
+        qzeros = torch.empty((ng, N // 8), dtype=torch.int32, device=dev)
+        scales = torch.empty((ng, N), dtype=torch.float16, device=dev)
+    else:
+        qweight, qzeros, scales = out
+        _need(qweight, "qweight", torch.int32, (K, N // 8), dev)
+        _need(qzeros, "qzeros", torch.int32, (ng, N // 8), dev)
+        _need(scales, "scales", torch.float16, (ng, N), dev)
     st = lib.awq_quantize_rtn(_ptr(w), N, K, group_size, 1 if sym else 0, _ptr(qweight),
                               _ptr(qzeros), _ptr(scales), _stream(stream))
     _check(st)
