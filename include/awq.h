@@ -53,7 +53,7 @@ typedef enum awq_status {
   AWQ_ERR_TIMEOUT = 6            /* a bounded device-side wait gave up (see awq_device_status) */
 } awq_status_t;
 
-typedef enum awq_dtype { AWQ_DTYPE_F16 = 0, AWQ_DTYPE_F32 = 1 } awq_dtype_t;
+typedef enum awq_dtype { AWQ_DTYPE_F16 = 0, AWQ_DTYPE_F32 = 1, AWQ_DTYPE_BF16 = 2 } awq_dtype_t;
 
 /* Kernel family used by awq_gemm_ex.  AUTO picks by M, K, N, G and alignment. */
 typedef enum awq_path {
@@ -92,6 +92,34 @@ const char* awq_status_string(awq_status_t status);
 awq_status_t awq_dequant(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
                          int64_t K, int64_t N, int64_t group_size,
                          void* w_out, awq_dtype_t out_dtype, awq_stream_t stream);
+
+/*
+ * bf16 activations and scales on the same weight layout (the native GEMM kernel's declared
+ * contract lists FP16/BF16: GPTQModel wiki "AWQ", "Selection and compatibility", its
+ * kernel table; vLLM accepts half and bfloat16: the vLLM article, section 4).  Same contract as awq_gemm_ex / awq_gemm / awq_dequant with
+ * bf16 in place of fp16 for x, scales, bias and y (and for w_out when out_dtype is
+ * AWQ_DTYPE_BF16):
+ *
+ *   y[m][n] = bf16_rne( sum_k x[m][k] * w[k][n]  (+ bias[n]) ),  w = (code - zero) * scale
+ *
+ * fp32 accumulation always.  The decode kernel carries each code into the MMA as the exact
+ * bf16 value 128 + c and folds (128 + zero) * sum x out per group; the prefill kernel rounds
+ * (c - zero) * scale once to bf16 for its tensor-core operand.  Paths: DECODE needs the
+ * TMA decode kernel's contract (K % 64, G % 64, N % 32, 16-byte aligned x, qweight,
+ * qzeros, scales); PREFILL as for fp16; GENERIC any valid shape.  AUTO chooses among them.
+ * awq_dequant_bf16 writes the exact fp32 value (AWQ_DTYPE_F32) or that value rounded once
+ * to bf16 (AWQ_DTYPE_BF16).
+ */
+awq_status_t awq_gemm_bf16_ex(const void* x_bf16, const int32_t* qweight, const int32_t* qzeros,
+                              const void* scales_bf16, const void* bias_bf16, int64_t M, int64_t K,
+                              int64_t N, int64_t group_size, void* y_bf16, awq_path_t path,
+                              awq_stream_t stream);
+awq_status_t awq_gemm_bf16(const void* x_bf16, const int32_t* qweight, const int32_t* qzeros,
+                           const void* scales_bf16, const void* bias_bf16, int64_t M, int64_t K,
+                           int64_t N, int64_t group_size, void* y_bf16, awq_stream_t stream);
+awq_status_t awq_dequant_bf16(const int32_t* qweight, const int32_t* qzeros, const void* scales_bf16,
+                              int64_t K, int64_t N, int64_t group_size, void* w_out,
+                              awq_dtype_t out_dtype, awq_stream_t stream);
 
 /*
  * awq_quantize_rtn -- round-to-nearest 4-bit group quantization of a linear layer's fp16

@@ -40,6 +40,12 @@ What it computes, and where each step comes from:
   scale rounded to fp16 as a checkpoint stores it and the codes taken against
   that stored scale, round half to even.
 
+* bf16 (the native GEMM's declared FP16/BF16 contract; GPTQModel wiki "AWQ",
+  "Selection and compatibility"): activations, scales and bias hold bf16
+  values; the GEMM definition is unchanged (fp64 of the exact values);
+  :func:`dequant_bf16` is the exact fp32 dequant rounded once to bf16
+  (:func:`round_to_bf16`, nearest even: bf16 is the upper half of an fp32).
+
 Pins (tests/test_oracle.py, run without a GPU): ORDER and its inverse from
 the wiki's "Saved formats and packing" section, a hand-packed word, AWQ-004
 (sequential-nibble decode differs), AWQ-005 (zero equal to code gives an
@@ -49,7 +55,8 @@ and an exact-arithmetic GEMM case; for the quantizer a hand-worked group
 (tests/golden/rtn_worked_example.txt), exact round trips of weights that lie on
 a grid spanning the whole code range, the half-step error bound, the clamped
 degenerate groups and group_size -1 equal to group_size K.  Every function
-here has at least one pin.
+here has at least one pin (bf16 rounding: hand-worked ties and torch's own
+bf16 conversion on random and edge values).
 """
 from __future__ import annotations
 
@@ -124,6 +131,22 @@ def dequant_f32(qweight, qzeros, scales, group_size) -> np.ndarray:
 def dequant_f16(qweight, qzeros, scales, group_size) -> np.ndarray:
     """fp16 [K, N]: round-to-nearest-even of :func:`dequant_f32`."""
     return dequant_f32(qweight, qzeros, scales, group_size).astype(np.float16)
+
+
+def round_to_bf16(values) -> np.ndarray:
+    """Round fp32 values to bf16 (nearest, ties to even), returned as fp32 arrays
+    holding the bf16 values.  bf16 keeps the upper 16 bits of an fp32 pattern, so
+    rounding adds 0x7FFF plus the kept part's lowest bit and clears the low half."""
+    u = np.ascontiguousarray(values, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
+    return r.astype(np.uint32).view(np.float32)
+
+
+def dequant_bf16(qweight, qzeros, scales, group_size) -> np.ndarray:
+    """bf16 dequant output: the exact fp32 value rounded once to bf16 (as fp32 values).
+    ``scales`` holds bf16 values (any float dtype that represents them exactly)."""
+    return round_to_bf16(dequant_f32(qweight, qzeros, scales, group_size))
 
 
 def dequant_page_layout(qweight, qzeros, scales, group_size) -> np.ndarray:

@@ -24,6 +24,8 @@ Workload recipe (per linear, draw order x, codes, zeros, scales, bias):
   * scales fp16 [K/G, N]   uniform [1e-3, 1e-2) drawn in fp32, rounded to fp16
   * bias   fp16 [N]        normal(0, 0.02) drawn in fp32, rounded to fp16
 G = K when group_size == -1.
+With dtype="bf16" the same draws are rounded to bf16 instead of fp16 (by torch's
+conversion) and returned as fp32 arrays holding the bf16 values.
 """
 from __future__ import annotations
 
@@ -51,7 +53,7 @@ def _groups(K: int, group_size: int) -> int:
 def awq_linear(seed: int, M: int, K: int, N: int, group_size: int = 128,
                bias: bool = False, sym: bool = False,
                x_kind: str = "normal", scale_kind: str = "uniform",
-               bias_kind: str = "normal") -> dict:
+               bias_kind: str = "normal", dtype: str = "f16") -> dict:
     """Draw one synthetic AWQ linear plus an activation batch.
 
     Returns a dict of numpy arrays: ``x`` fp16 [M,K], ``qweight`` int32
@@ -65,12 +67,15 @@ def awq_linear(seed: int, M: int, K: int, N: int, group_size: int = 128,
     """
     if N % 8 != 0:
         raise ValueError("N must be a multiple of 8 (eight codes per int32 word)")
+    if dtype not in ("f16", "bf16"):
+        raise ValueError(dtype)
+    half = np.float16 if dtype == "f16" else _to_bf16
     n_groups = _groups(K, group_size)
     rng = np.random.Generator(np.random.PCG64(seed))
     if x_kind == "normal":
-        x = rng.standard_normal((M, K), dtype=np.float32).astype(np.float16)
+        x = _as(rng.standard_normal((M, K), dtype=np.float32), half)
     elif x_kind == "smallint":
-        x = rng.integers(-4, 5, size=(M, K)).astype(np.float16)
+        x = _as(rng.integers(-4, 5, size=(M, K)).astype(np.float32), half)
     else:
         raise ValueError(x_kind)
     qweight = rng.integers(0, 1 << 32, size=(K, N // 8), dtype=np.uint64)
@@ -82,23 +87,33 @@ def awq_linear(seed: int, M: int, K: int, N: int, group_size: int = 128,
         qzeros = qzeros.astype(np.uint32).view(np.int32)
     if scale_kind == "uniform":
         scales = rng.uniform(1e-3, 1e-2, size=(n_groups, N)).astype(np.float32)
-        scales = scales.astype(np.float16)
+        scales = _as(scales, half)
     elif scale_kind == "pow2":
         p = rng.integers(4, 10, size=(n_groups, N))
-        scales = np.ldexp(np.ones((n_groups, N), np.float32), -p).astype(np.float16)
+        scales = _as(np.ldexp(np.ones((n_groups, N), np.float32), -p), half)
     else:
         raise ValueError(scale_kind)
     b = None
     if bias:
         if bias_kind == "normal":
-            b = rng.normal(0.0, 0.02, size=N).astype(np.float32).astype(np.float16)
+            b = _as(rng.normal(0.0, 0.02, size=N).astype(np.float32), half)
         elif bias_kind == "dyadic":
-            b = (rng.integers(-64, 65, size=N) / 64.0).astype(np.float16)
+            b = _as((rng.integers(-64, 65, size=N) / 64.0).astype(np.float32), half)
         else:
             raise ValueError(bias_kind)
     return {"x": np.ascontiguousarray(x), "qweight": np.ascontiguousarray(qweight),
             "qzeros": np.ascontiguousarray(qzeros), "scales": np.ascontiguousarray(scales),
-            "bias": b, "group_size": int(group_size), "M": M, "K": K, "N": N}
+            "bias": b, "group_size": int(group_size), "M": M, "K": K, "N": N, "dtype": dtype}
+
+
+def _to_bf16(a: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 by torch's conversion, back as fp32 arrays holding bf16 values."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def _as(a: np.ndarray, half) -> np.ndarray:
+    return a.astype(np.float16) if half is np.float16 else half(a)
 
 
 # Workloads shaped like the 7B / 70B linears the pages discuss.  Each entry:

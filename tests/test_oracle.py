@@ -378,3 +378,40 @@ def test_rtn_rejects_bad_shapes():
         oracle.quantize_rtn(np.zeros((8, 64), np.float16), 24)
     with pytest.raises(ValueError):
         oracle.quantize_rtn(np.zeros((8, 64), np.float32), 32)
+
+
+# ------------------------------------------------------------------ bf16 ----
+# bf16 = the upper 16 bits of an fp32 (7 stored significand bits); rounding to nearest, ties
+# to even.  Worked by hand around 1.0 (ulp 2^-7) and checked against torch's own conversion.
+
+def test_bf16_rounding_hand_worked():
+    one = 1.0
+    cases = [
+        (one + 2.0 ** -8, one),                         # exactly half an ulp: tie, to even (1.0)
+        (one + 3 * 2.0 ** -8, one + 2.0 ** -6),         # 1.5 ulp: tie between m=1 and m=2, to even
+        (one + 2.0 ** -8 + 2.0 ** -20, one + 2.0 ** -7),  # just above half: up
+        (one + 2.0 ** -8 - 2.0 ** -20, one),            # just below half: down
+        (-(one + 3 * 2.0 ** -8), -(one + 2.0 ** -6)),   # sign symmetric
+        (0.0, 0.0),
+        (3.0, 3.0),                                     # exact values unchanged
+    ]
+    got = oracle.round_to_bf16(np.array([c[0] for c in cases], dtype=np.float32))
+    assert np.array_equal(got, np.array([c[1] for c in cases], dtype=np.float32))
+
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    v = np.concatenate([rng.standard_normal(20000).astype(np.float32) * 10.0 ** rng.integers(-6, 6, 20000),
+                        np.array([1e-40, -3e-39, 65504.0, 3.3e38, 1.0 + 2 ** -8], dtype=np.float32)])
+    ref = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(oracle.round_to_bf16(v).view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_bf16_is_one_rounding_of_the_exact_value():
+    d = awq_linear(41, 1, 64, 16, group_size=32, dtype="bf16")
+    exact = oracle.dequant_f32(d["qweight"], d["qzeros"], d["scales"], 32)
+    got = oracle.dequant_bf16(d["qweight"], d["qzeros"], d["scales"], 32)
+    assert np.array_equal(got, oracle.round_to_bf16(exact))
+    # the bf16 value is within half a bf16 ulp of the exact one
+    assert (np.abs(got - exact) <= np.abs(exact) * 2.0 ** -8 + 1e-30).all()

@@ -18,7 +18,7 @@ STATUS_NAMES = {0: "AWQ_OK", 1: "AWQ_ERR_INVALID_ARGUMENT", 2: "AWQ_ERR_UNSUPPOR
                 6: "AWQ_ERR_TIMEOUT"}
 PATHS = {"auto": 0, "decode": 1, "prefill": 2, "generic": 3}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
-DTYPE_F16, DTYPE_F32 = 0, 1
+DTYPE_F16, DTYPE_F32, DTYPE_BF16 = 0, 1, 2
 
 # Every entry point of include/awq.h: name -> (restype, argtypes)
 _i64, _vp, _i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -33,6 +33,9 @@ SIGNATURES = {
     "awq_device_status": (_i32, [_vp]),
     "awq_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
     "awq_quantize_rtn": (_i32, [_vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
+    "awq_gemm_bf16": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "awq_gemm_bf16_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "awq_dequant_bf16": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp]),
 }
 
 _lib = None
@@ -107,10 +110,12 @@ def _groups(K, group_size):
 
 def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, path="auto",
              stream=None):
-    """y = x @ dequant(qweight, qzeros, scales) (+ bias) via the library's awq_gemm.
+    """y = x @ dequant(qweight, qzeros, scales) (+ bias) via the library's awq_gemm, or
+    awq_gemm_bf16 when x is bfloat16.
 
-    x fp16 [M, K] (leading dims are flattened), qweight int32 [K, N/8], qzeros int32
-    [K/G, N/8], scales fp16 [K/G, N], bias fp16 [N] or None.  Returns fp16 [..., N].
+    x fp16 or bf16 [M, K] (leading dims are flattened), qweight int32 [K, N/8], qzeros int32
+    [K/G, N/8], scales [K/G, N] and bias [N] (or None) of x's dtype.  Returns [..., N] of
+    x's dtype.
     """
     lib = load_library()
     lead = x.shape[:-1]
@@ -119,26 +124,29 @@ def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, pa
     M = x2.shape[0]
     N = qweight.shape[1] * 8
     dev = x.device
-    _need(x2, "x", torch.float16, (M, K), dev)
+    dt = x.dtype if x.dtype in (torch.float16, torch.bfloat16) else torch.float16
+    _need(x2, "x", dt, (M, K), dev)
     _need(qweight, "qweight", torch.int32, (K, N // 8), dev)
     ng = _groups(K, group_size)
     _need(qzeros, "qzeros", torch.int32, (ng, N // 8), dev)
-    _need(scales, "scales", torch.float16, (ng, N), dev)
+    _need(scales, "scales", dt, (ng, N), dev)
     if bias is not None:
-        _need(bias, "bias", torch.float16, (N,), dev)
+        _need(bias, "bias", dt, (N,), dev)
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+        out = torch.empty((M, N), dtype=dt, device=dev)
     else:
-        _need(out, "out", torch.float16, (M, N), dev)
-    st = lib.awq_gemm_ex(_ptr(x2), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
-                         M, K, N, group_size, _ptr(out), PATHS[path], _stream(stream))
+        _need(out, "out", dt, (M, N), dev)
+    fn = lib.awq_gemm_bf16_ex if dt == torch.bfloat16 else lib.awq_gemm_ex
+    st = fn(_ptr(x2), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
+            M, K, N, group_size, _ptr(out), PATHS[path], _stream(stream))
     _check(st)
     return out.reshape(*lead, N)
 
 
 def awq_dequant(qweight, qzeros, scales, group_size=128, out_dtype=torch.float16, out=None,
                 stream=None):
-    """Dense W [K, N] = (code - zero) * scale via the library's awq_dequant."""
+    """Dense W [K, N] = (code - zero) * scale via the library's awq_dequant (fp16 scales;
+    out fp16 or fp32) or awq_dequant_bf16 (bf16 scales; out bf16 or fp32)."""
     lib = load_library()
     K, C = qweight.shape
     N = 8 * C
@@ -146,15 +154,25 @@ def awq_dequant(qweight, qzeros, scales, group_size=128, out_dtype=torch.float16
     _need(qweight, "qweight", torch.int32, (K, C), dev)
     ng = _groups(K, group_size)
     _need(qzeros, "qzeros", torch.int32, (ng, C), dev)
-    _need(scales, "scales", torch.float16, (ng, N), dev)
-    if out_dtype not in (torch.float16, torch.float32):
-        raise TypeError("out_dtype must be torch.float16 or torch.float32")
+    bf = scales.dtype == torch.bfloat16
+    _need(scales, "scales", torch.bfloat16 if bf else torch.float16, (ng, N), dev)
+    half = torch.bfloat16 if bf else torch.float16
+    if out_dtype == torch.float16 and bf:
+        out_dtype = torch.bfloat16
+    if out_dtype not in (half, torch.float32):
+        raise TypeError(f"out_dtype must be {half} or torch.float32")
     if out is None:
         out = torch.empty((K, N), dtype=out_dtype, device=dev)
     else:
         _need(out, "out", out_dtype, (K, N), dev)
-    st = lib.awq_dequant(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size, _ptr(out),
-                         DTYPE_F32 if out_dtype == torch.float32 else DTYPE_F16, _stream(stream))
+    if bf:
+        st = lib.awq_dequant_bf16(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size,
+                                  _ptr(out), DTYPE_F32 if out_dtype == torch.float32 else DTYPE_BF16,
+                                  _stream(stream))
+    else:
+        st = lib.awq_dequant(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size,
+                             _ptr(out), DTYPE_F32 if out_dtype == torch.float32 else DTYPE_F16,
+                             _stream(stream))
     _check(st)
     return out
 

@@ -76,7 +76,7 @@ bool al(const void* p, uintptr_t a) { return awq::aligned(p, a); }
 awq_status_t build_problem(const void* x, const int32_t* qweight, const int32_t* qzeros,
                            const void* scales, const void* bias, int64_t M, int64_t K, int64_t N,
                            int64_t group_size, void* y, awq_stream_t stream, awq::GemmProblem* p,
-                           bool* empty) {
+                           bool* empty, bool bf16 = false) {
   if (M < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "M must be >= 0 (got %lld)", (long long)M);
   int G = 0;
   awq_status_t st = check_weight_shape(K, N, group_size, &G);
@@ -89,7 +89,7 @@ awq_status_t build_problem(const void* x, const int32_t* qweight, const int32_t*
   if (!x || !qweight || !qzeros || !scales || !y)
     return fail(AWQ_ERR_INVALID_ARGUMENT, "null pointer among x, qweight, qzeros, scales, y");
   if (!al(x, 2) || !al(scales, 2) || !al(y, 2) || (bias && !al(bias, 2)))
-    return fail(AWQ_ERR_MISALIGNED, "fp16 tensors must be 2-byte aligned");
+    return fail(AWQ_ERR_MISALIGNED, "16-bit tensors must be 2-byte aligned");
   if (!al(qweight, 4) || !al(qzeros, 4))
     return fail(AWQ_ERR_MISALIGNED, "qweight and qzeros must be 4-byte aligned");
   p->x = static_cast<const __half*>(x);
@@ -103,6 +103,7 @@ awq_status_t build_problem(const void* x, const int32_t* qweight, const int32_t*
   p->N = static_cast<int>(N);
   p->G = G;
   p->stream = reinterpret_cast<cudaStream_t>(stream);
+  p->bf16 = bf16;
   return AWQ_OK;
 }
 
@@ -216,22 +217,68 @@ awq_status_t awq_quantize_rtn(const void* w_f16, int64_t N, int64_t K, int64_t g
   return ok();
 }
 
-awq_status_t awq_gemm_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
-                         const void* scales_f16, const void* bias_f16, int64_t M, int64_t K,
-                         int64_t N, int64_t group_size, void* y_f16, awq_path_t path,
-                         awq_stream_t stream) {
+static awq_status_t gemm_any(const void* x, const int32_t* qweight, const int32_t* qzeros,
+                      const void* scales, const void* bias, int64_t M, int64_t K, int64_t N,
+                      int64_t group_size, void* y, awq_path_t path, awq_stream_t stream, bool bf16) {
   if (path < AWQ_PATH_AUTO || path > AWQ_PATH_GENERIC)
     return fail(AWQ_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
   awq::GemmProblem p{};
   bool empty = false;
-  awq_status_t st = build_problem(x_f16, qweight, qzeros, scales_f16, bias_f16, M, K, N,
-                                  group_size, y_f16, stream, &p, &empty);
+  awq_status_t st = build_problem(x, qweight, qzeros, scales, bias, M, K, N, group_size, y,
+                                  stream, &p, &empty, bf16);
   if (st != AWQ_OK) return st;
   if (empty) return ok();
   st = check_device();
   if (st != AWQ_OK) return st;
   const awq::Path use = path == AWQ_PATH_AUTO ? choose_path(p) : static_cast<awq::Path>(path);
   return run(p, use);
+}
+
+awq_status_t awq_gemm_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                         const void* scales_f16, const void* bias_f16, int64_t M, int64_t K,
+                         int64_t N, int64_t group_size, void* y_f16, awq_path_t path,
+                         awq_stream_t stream) {
+  return gemm_any(x_f16, qweight, qzeros, scales_f16, bias_f16, M, K, N, group_size, y_f16, path,
+                  stream, false);
+}
+
+awq_status_t awq_gemm_bf16_ex(const void* x_bf16, const int32_t* qweight, const int32_t* qzeros,
+                              const void* scales_bf16, const void* bias_bf16, int64_t M, int64_t K,
+                              int64_t N, int64_t group_size, void* y_bf16, awq_path_t path,
+                              awq_stream_t stream) {
+  return gemm_any(x_bf16, qweight, qzeros, scales_bf16, bias_bf16, M, K, N, group_size, y_bf16,
+                  path, stream, true);
+}
+
+awq_status_t awq_gemm_bf16(const void* x_bf16, const int32_t* qweight, const int32_t* qzeros,
+                           const void* scales_bf16, const void* bias_bf16, int64_t M, int64_t K,
+                           int64_t N, int64_t group_size, void* y_bf16, awq_stream_t stream) {
+  return gemm_any(x_bf16, qweight, qzeros, scales_bf16, bias_bf16, M, K, N, group_size, y_bf16,
+                  AWQ_PATH_AUTO, stream, true);
+}
+
+awq_status_t awq_dequant_bf16(const int32_t* qweight, const int32_t* qzeros, const void* scales_bf16,
+                              int64_t K, int64_t N, int64_t group_size, void* w_out,
+                              awq_dtype_t out_dtype, awq_stream_t stream) {
+  int G = 0;
+  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  if (st != AWQ_OK) return st;
+  if (out_dtype != AWQ_DTYPE_BF16 && out_dtype != AWQ_DTYPE_F32)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "out_dtype must be AWQ_DTYPE_BF16 or AWQ_DTYPE_F32");
+  if (N == 0) return ok();
+  if (!qweight || !qzeros || !scales_bf16 || !w_out)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "null pointer among qweight, qzeros, scales, w_out");
+  if (!al(qweight, 4) || !al(qzeros, 4)) return fail(AWQ_ERR_MISALIGNED, "qweight/qzeros must be 4-byte aligned");
+  if (!al(scales_bf16, 2)) return fail(AWQ_ERR_MISALIGNED, "scales must be 2-byte aligned");
+  if (!al(w_out, out_dtype == AWQ_DTYPE_F32 ? 4 : 2)) return fail(AWQ_ERR_MISALIGNED, "w_out misaligned for its dtype");
+  st = check_device();
+  if (st != AWQ_OK) return st;
+  const cudaError_t e = awq::launch_dequant(
+      reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
+      static_cast<const __half*>(scales_bf16), static_cast<int>(K), static_cast<int>(N), G, w_out,
+      out_dtype == AWQ_DTYPE_F32, reinterpret_cast<cudaStream_t>(stream), true);
+  if (e != cudaSuccess) return cuda_fail(e, "awq_dequant_bf16 launch");
+  return ok();
 }
 
 awq_status_t awq_gemm(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,

@@ -466,6 +466,7 @@ cudaError_t launch_decode_ldg(const GemmProblem& p) {
 }
 
 bool decode_supported(const GemmProblem& p, const char** why) {
+  if (p.bf16) return decode_tma_supported(p, why);  // the register-streaming kernel is fp16-only
   if (decode_tma_supported(p, nullptr)) return true;
   return decode_ldg_supported(p, why);
 }

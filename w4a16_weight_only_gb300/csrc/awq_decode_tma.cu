@@ -137,10 +137,17 @@ constexpr int kMinBlocks = NW == 8 ? 2 : (TB == 1 ? AWQ_DECODE_MIN_BLOCKS_M8 : A
 // accumulator is folded or cleared inside the loop; after it every lane folds the groups
 // of its own columns once (zero and scale rows kept in a per-warp stash indexed by group
 // slot) and the reduction also sums over the four lanes of each quad.
-template <int TB, int CWL, bool kSub, bool kOne, int NW>
+// kBF: bf16 activations, scales, bias and output.  A code c then enters the MMA as the
+// exact bf16 value 128 + c (0x4300 | c: the subnormal trick has no room for a 4-bit code
+// above bf16's 7-bit significand without leaving fp32's normal range in the products), so
+// the fold is acc += scale * (sum x (128 + c) - (128 + zero) * sum x).
+template <int TB, int CWL, bool kSub, bool kOne, int NW, bool kBF>
 __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     decode_tma_kernel(const __grid_constant__ TmaDecodeParams p) {
   static_assert(NW == 4 || NW == 8, "4 or 8 warps per CTA");
+  constexpr uint32_t kOne2 = kBF ? 0x3F803F80u : kOnes;     // 1.0 in both halves
+  constexpr uint32_t kMag = kBF ? 0x43004300u : kMagic;     // 128 (bf16) / 1024 (fp16)
+  constexpr float kBias = kBF ? 128.f : 0.f;                 // offset the operand carries
   using GE = Geo<TB, CWL, NW>;
   constexpr int NMMA = GE::NMMA;
   extern __shared__ unsigned char smem_raw[];
@@ -286,7 +293,9 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     float* bias_s = reinterpret_cast<float*>(smem + p.bias_off);
     for (int i = threadIdx.x; i < 8 * GE::CW_W; i += NW * 32) {
       const int n = 8 * cw0 + i;
-      bias_s[i] = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+      bias_s[i] = (p.bias != nullptr && n < p.N)
+                      ? elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[n])
+                      : 0.f;
     }
   }
   uint32_t x_off[TB][2];
@@ -348,15 +357,15 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     for (int hb = 0; hb < HB; ++hb)
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
-        const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&sv[hb][pp]));
+        const float2 s2 = pair_to_float2<kBF>(sv[hb][pp]);
 #pragma unroll
         for (int n2 = 0; n2 < 2; ++n2) {
           const int nib = 2 * pp + n2;
           const float sc = n2 ? s2.y : s2.x;
           // zero nibble as a float: 2^23 + z read as an fp32 bit pattern, minus 2^23
           const float z = __uint_as_float(((zh[hb] >> (4 * nib)) & 0xFu) | 0x4B000000u) - 8388608.f;
-          const float sa = sc * ((nib & 1) ? 1048576.f : 16777216.f);
-          const float sz = -sc * z;
+          const float sa = kBF ? sc : sc * ((nib & 1) ? 1048576.f : 16777216.f);
+          const float sz = -sc * (z + kBias);
           const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
 #pragma unroll
           for (int tb = 0; tb < TB; ++tb)
@@ -417,7 +426,7 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
           const uint32_t zd = prmt(zh[hb], zh[hb], 0x1010u);  // zero half-word in both halves
 #pragma unroll
           for (int nib = 0; nib < 4; ++nib) {
-            zp[kSub ? 0 : hb][nib] = and_or(zd >> (4 * nib), 0x000F000Fu, kMagic);
+            zp[kSub ? 0 : hb][nib] = and_or(zd >> (4 * nib), 0x000F000Fu, kMag);
             sp[kSub ? 0 : hb][nib] = prmt(sv[hb][nib >> 1], 0u, (nib & 1) ? 0x3232u : 0x1010u);
           }
         }
@@ -453,11 +462,16 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
         }
         auto operand = [&](int rb, int hb, int nib) -> uint32_t {
           const uint32_t s = wr[rb][hb];
-          if constexpr (kSub) {
+          if constexpr (kSub && kBF) {
+            return and_or(s >> (4 * nib), 0x000F000Fu, kMag);  // exact bf16 128 + c
+          } else if constexpr (kSub) {
             // exact fp16 subnormals c * 2^-24 (even nibble) or c * 2^-20 (odd nibble)
             return ((nib & 2) ? (s >> 8) : s) & ((nib & 1) ? 0x00F000F0u : 0x000F000Fu);
+          } else if constexpr (kBF) {
+            const uint32_t h = and_or(s >> (4 * nib), 0x000F000Fu, kMag);
+            return hmul2_bf16(hsub2_bf16(h, zp[kSub ? 0 : hb][nib]), sp[kSub ? 0 : hb][nib]);
           } else {
-            const uint32_t h = and_or(s >> (4 * nib), 0x000F000Fu, kMagic);
+            const uint32_t h = and_or(s >> (4 * nib), 0x000F000Fu, kMag);
             return hmul2(hsub2(h, zp[kSub ? 0 : hb][nib]), sp[kSub ? 0 : hb][nib]);
           }
         };
@@ -468,8 +482,12 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
           const uint32_t a2 = operand(1, hb0, nib), a3 = operand(1, hb0 + 1, nib);
 #pragma unroll
           for (int tb = 0; tb < TB; ++tb) {
-            if (kSub)
+            if constexpr (kSub && kBF)
+              mma16816_bf16(accg[mi][tb], a0, a1, a2, a3, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
+            else if constexpr (kSub)
               mma16816(accg[mi][tb], a0, a1, a2, a3, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
+            else if constexpr (kBF)
+              mma16816_bf16(acc[mi][tb], a0, a1, a2, a3, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
             else
               mma16816(acc[mi][tb], a0, a1, a2, a3, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
           }
@@ -477,7 +495,8 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
         if (kSub) {
 #pragma unroll
           for (int tb = 0; tb < TB; ++tb)
-            mma16816(xs[tb], kOnes, kOnes, kOnes, kOnes, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
+            if constexpr (kBF) mma16816_bf16(xs[tb], kOne2, kOne2, kOne2, kOne2, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
+            else mma16816(xs[tb], kOne2, kOne2, kOne2, kOne2, xr[tb][2 * kk], xr[tb][2 * kk + 1]);
         }
       }
     }
@@ -508,14 +527,14 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
       for (int hb = 0; hb < HB; ++hb)
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
-          const float2 s2 = __half22float2(*reinterpret_cast<const __half2*>(&sv[hb][pp]));
+          const float2 s2 = pair_to_float2<kBF>(sv[hb][pp]);
 #pragma unroll
           for (int n2 = 0; n2 < 2; ++n2) {
             const int nib = 2 * pp + n2;
             const float sc = n2 ? s2.y : s2.x;
             const float z = __uint_as_float(((zh[hb] >> (4 * nib)) & 0xFu) | 0x4B000000u) - 8388608.f;
-            const float sa = sc * ((nib & 1) ? 1048576.f : 16777216.f);
-            const float sz = -sc * z;
+            const float sa = kBF ? sc : sc * ((nib & 1) ? 1048576.f : 16777216.f);
+            const float sz = -sc * (z + kBias);
             const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
             const float a = __fmaf_rn(sz, xs[0][e], out[mi][rs]);
             out[mi][rs] = __fmaf_rn(sa, accg[mi][0][2 * rs + e], a);
@@ -617,7 +636,8 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     if (m0 + t >= p.M || 8 * cw0 + col >= p.N) continue;
     float sum = 0.f;
     for (uint32_t r = 0; r < cs; ++r) sum += recv[r * p.slice + (i - lo)];
-    p.y[(long long)(m0 + t) * p.N + 8 * cw0 + col] = __float2half_rn(sum + bias_s[col]);
+    reinterpret_cast<uint16_t*>(p.y)[(long long)(m0 + t) * p.N + 8 * cw0 + col] =
+        float_to_elem<kBF>(sum + bias_s[col]);
   }
 #ifdef AWQ_DECODE_DEBUG_TIME
   AWQ_DECODE_DEBUG_TIME(3);
@@ -740,9 +760,9 @@ int max_warp_groups(int TS, int P, int spg) {
 }
 
 // Co-resident clusters of size cs at `smem` bytes per CTA (occupancy API).
-template <int TB, int CWL, bool S, bool O, int NW>
+template <int TB, int CWL, bool S, bool O, int NW, bool B>
 int max_clusters(int cs, int smem) {
-  auto kern = decode_tma_kernel<TB, CWL, S, O, NW>;
+  auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, 1, 1);
   cfg.blockDim = dim3(NW * 32, 1, 1);
@@ -767,7 +787,7 @@ int max_clusters(int cs, int smem) {
 // each warp keeping at least one 64-row stage; ties go to the smaller cluster.  Ring
 // depth: as many slots as the shared memory left per CTA allows, up to the warp's stage
 // count.  Cached per shape.
-template <int TB, int CWL, bool S, bool O, int NW>
+template <int TB, int CWL, bool S, bool O, int NW, bool B>
 cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   using GE = Geo<TB, CWL, NW>;
   static std::mutex mu;
@@ -792,7 +812,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    auto kern = decode_tma_kernel<TB, CWL, S, O, NW>;
+    auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dl.smem_optin);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -832,7 +852,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
     // single wave with slack, checked against the occupancy API at this size
     bool fits = false;
     while (true) {
-      long long cap = (long long)max_clusters<TB, CWL, S, O, NW>(cs, pl.smem) * cs;
+      long long cap = (long long)max_clusters<TB, CWL, S, O, NW, B>(cs, pl.smem) * cs;
       if (cap > (long long)kMaxCtasPerSm * dl.sms) cap = (long long)kMaxCtasPerSm * dl.sms;
       if (grid * 100 <= cap * kWaveFillPct) { fits = true; break; }
       if (pl.slots <= red_slots || pl.slots <= 1) break;
@@ -851,11 +871,11 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   return cudaSuccess;
 }
 
-template <int TB, int CWL, bool S, bool O, int NW>
+template <int TB, int CWL, bool S, bool O, int NW, bool B>
 cudaError_t launch_v(const GemmProblem& p) {
   using GE = Geo<TB, CWL, NW>;
   Plan pl;
-  cudaError_t e = plan_for<TB, CWL, S, O, NW>(p, &pl);
+  cudaError_t e = plan_for<TB, CWL, S, O, NW, B>(p, &pl);
   if (e != cudaSuccess) return e;
   const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
 
@@ -865,11 +885,11 @@ cudaError_t launch_v(const GemmProblem& p) {
   const int ngrp = p.K / p.G;
   if (!make_tmap_2d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, GE::CW_W, kRS,
                     CWL == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B, &why) ||
-      !make_tmap_2d(&dp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kRS, x_rows,
+      !make_tmap_2d(&dp.tm_x, B ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kRS, x_rows,
                     (x_rows == 1 && !AWQ_DECODE_WIDE_X) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
       !make_tmap_2d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, GE::CW_W, 1,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
-      !make_tmap_2d(&dp.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.sc, p.N, ngrp, 8 * GE::CW_W, 1,
+      !make_tmap_2d(&dp.tm_s, B ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.sc, p.N, ngrp, 8 * GE::CW_W, 1,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why))
     return cudaErrorInvalidValue;
   dp.bias = p.bias;
@@ -901,7 +921,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S, O, NW>, dp);
+  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S, O, NW, B>, dp);
 }
 
 }  // namespace
@@ -921,7 +941,8 @@ bool decode_tma_supported(const GemmProblem& p, const char** why) {
   return true;
 }
 
-cudaError_t launch_decode_tma(const GemmProblem& p) {
+template <bool B>
+cudaError_t launch_decode_tma_t(const GemmProblem& p) {
   const Variant v = pick(p);
   if (v.TB == 1) {
     if (p.M == 1) {
@@ -929,20 +950,24 @@ cudaError_t launch_decode_tma(const GemmProblem& p) {
       // would leave a warp kWideStages or more stages (long K: more warps share the work).
       const int TS = p.K / kRS, spg = p.G / kRS;
       Plan p4;
-      cudaError_t e = plan_for<1, 2, true, true, 4>(p, &p4);
+      cudaError_t e = plan_for<1, 2, true, true, 4, B>(p, &p4);
       if (e != cudaSuccess) return e;
       if ((TS + 4 * p4.cs - 1) / (4 * p4.cs) >= kWideStages) {
         Plan p8;
-        e = plan_for<1, 2, true, true, 8>(p, &p8);
+        e = plan_for<1, 2, true, true, 8, B>(p, &p8);
         if (e != cudaSuccess) return e;
-        if (max_warp_groups(TS, 8 * p8.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 8>(p);
+        if (max_warp_groups(TS, 8 * p8.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 8, B>(p);
       }
-      if (max_warp_groups(TS, 4 * p4.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 4>(p);
+      if (max_warp_groups(TS, 4 * p4.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 4, B>(p);
     }
-    return launch_v<1, 2, true, false, kNW>(p);
+    return launch_v<1, 2, true, false, kNW, B>(p);
   }
-  if (v.TB == 2) return launch_v<2, 1, true, false, kNW>(p);
-  return launch_v<4, 1, false, false, kNW>(p);
+  if (v.TB == 2) return launch_v<2, 1, true, false, kNW, B>(p);
+  return launch_v<4, 1, false, false, kNW, B>(p);
+}
+
+cudaError_t launch_decode_tma(const GemmProblem& p) {
+  return p.bf16 ? launch_decode_tma_t<true>(p) : launch_decode_tma_t<false>(p);
 }
 
 }  // namespace awq

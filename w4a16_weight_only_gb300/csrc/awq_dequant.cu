@@ -12,7 +12,7 @@ namespace {
 // Each thread handles one packed word (8 output columns of one row) per iteration.
 // The fp32 value (code - zero) * scale is exact (a 5-bit integer times an 11-bit
 // significand); the fp16 output is that value rounded once to nearest even.
-template <bool kF32, bool kVec>
+template <bool kF32, bool kVec, bool kBF>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict__ qw,
                                                       const uint32_t* __restrict__ qz,
                                                       const __half* __restrict__ sc, int K, int C,
@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict
     for (int i = 0; i < 8; ++i) {
       const int code = (int)((q >> (4 * i)) & 0xFu);
       const int zero = (int)((z >> (4 * i)) & 0xFu);
-      v[nibble_column(i)] = __fmul_rn((float)(code - zero), __half2float(s[nibble_column(i)]));
+      v[nibble_column(i)] = __fmul_rn((float)(code - zero), elem_to_float<kBF>(__half_as_ushort(s[nibble_column(i)])));
     }
     const long long o = (long long)k * N + 8LL * cw;
     if (kF32) {
@@ -52,10 +52,10 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict
         for (int j = 0; j < 8; ++j) dst[j] = v[j];
       }
     } else {
-      __half* dst = static_cast<__half*>(out) + o;
-      __half h[8];
+      uint16_t* dst = static_cast<uint16_t*>(out) + o;
+      uint16_t h[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) h[j] = __float2half_rn(v[j]);
+      for (int j = 0; j < 8; ++j) h[j] = float_to_elem<kBF>(v[j]);
       if (kVec) {
         __stcs(reinterpret_cast<uint4*>(dst), *reinterpret_cast<uint4*>(h));
       } else {
@@ -73,7 +73,10 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict
 constexpr int kMT = 8;
 constexpr int kKT = 64;
 
+template <bool kBF>
 __global__ void __launch_bounds__(128) generic_gemm_kernel(GemmProblem p) {
+  const uint16_t* x16 = reinterpret_cast<const uint16_t*>(p.x);
+  const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.sc);
   __shared__ float xs[kMT][kKT];
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   const int C = p.N >> 3;
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(128) generic_gemm_kernel(GemmProblem p) {
     for (int e = threadIdx.x; e < kMT * kKT; e += blockDim.x) {
       const int m = e / kKT, kk = e % kKT;
       const int gm = m0 + m, gk = k0 + kk;
-      xs[m][kk] = (gm < p.M && gk < p.K) ? __half2float(p.x[(long long)gm * p.K + gk]) : 0.f;
+      xs[m][kk] = (gm < p.M && gk < p.K) ? elem_to_float<kBF>(x16[(long long)gm * p.K + gk]) : 0.f;
     }
     __syncthreads();
     if (active) {
@@ -102,27 +105,39 @@ __global__ void __launch_bounds__(128) generic_gemm_kernel(GemmProblem p) {
         const uint32_t z = p.qz[(long long)g * C + cw];
         const int code = (int)((q >> (4 * nib)) & 0xFu);
         const int zero = (int)((z >> (4 * nib)) & 0xFu);
-        const float w = __fmul_rn((float)(code - zero), __half2float(p.sc[(long long)g * p.N + n]));
+        const float w = __fmul_rn((float)(code - zero), elem_to_float<kBF>(sc16[(long long)g * p.N + n]));
 #pragma unroll
         for (int m = 0; m < kMT; ++m) acc[m] = __fmaf_rn(xs[m][kk], w, acc[m]);
       }
     }
   }
   if (active) {
-    const float b = p.bias ? __half2float(p.bias[n]) : 0.f;
+    const float b = p.bias ? elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[n]) : 0.f;
 #pragma unroll
     for (int m = 0; m < kMT; ++m) {
       const int gm = m0 + m;
-      if (gm < p.M) p.y[(long long)gm * p.N + n] = __float2half_rn(acc[m] + b);
+      if (gm < p.M) reinterpret_cast<uint16_t*>(p.y)[(long long)gm * p.N + n] = float_to_elem<kBF>(acc[m] + b);
     }
   }
   }  // m0
 }
 
+template <bool kBF>
+void launch_dequant_t(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int C, int G,
+                      void* out, bool out_f32, bool vec, int blocks, cudaStream_t stream) {
+  if (out_f32) {
+    if (vec) dequant_kernel<true, true, kBF><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+    else dequant_kernel<true, false, kBF><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+  } else {
+    if (vec) dequant_kernel<false, true, kBF><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+    else dequant_kernel<false, false, kBF><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
-                           int G, void* out, bool out_f32, cudaStream_t stream) {
+                           int G, void* out, bool out_f32, cudaStream_t stream, bool bf16) {
   const int C = N / 8;
   const long long total = (long long)K * C;
   if (total == 0) return cudaSuccess;
@@ -130,24 +145,20 @@ cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const __half*
   int blocks = (int)((total + 255) / 256);
   const int cap = 152 * 16;
   if (blocks > cap) blocks = cap;
-  if (out_f32) {
-    if (vec) dequant_kernel<true, true><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
-    else dequant_kernel<true, false><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
-  } else {
-    if (vec) dequant_kernel<false, true><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
-    else dequant_kernel<false, false><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
-  }
+  if (bf16) launch_dequant_t<true>(qw, qz, sc, K, C, G, out, out_f32, vec, blocks, stream);
+  else launch_dequant_t<false>(qw, qz, sc, K, C, G, out, out_f32, vec, blocks, stream);
   return cudaGetLastError();
 }
 
 cudaError_t probe_kernel_image(cudaFuncAttributes* attr) {
-  return cudaFuncGetAttributes(attr, dequant_kernel<false, true>);
+  return cudaFuncGetAttributes(attr, dequant_kernel<false, true, false>);
 }
 
 cudaError_t launch_generic(const GemmProblem& p) {
   const int mtiles = (p.M + kMT - 1) / kMT;
   dim3 grid((p.N + 127) / 128, mtiles < 65535 ? mtiles : 65535);
-  generic_gemm_kernel<<<grid, 128, 0, p.stream>>>(p);
+  if (p.bf16) generic_gemm_kernel<true><<<grid, 128, 0, p.stream>>>(p);
+  else generic_gemm_kernel<false><<<grid, 128, 0, p.stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -19,6 +20,7 @@ struct GemmProblem {
   __half* y;              // [M, N]
   int M, K, N, G;         // G already resolved (K when group_size == -1)
   cudaStream_t stream;
+  bool bf16 = false;      // x, scales, bias and y hold bf16 (same 16-bit storage)
 };
 
 // Kernel families; values equal awq_path_t.
@@ -26,7 +28,7 @@ enum Path { kAuto = 0, kDecode = 1, kPrefill = 2, kGeneric = 3 };
 
 // Dequant (awq_dequant).  out_f32 selects fp32 vs fp16 output.
 cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
-                           int G, void* out, bool out_f32, cudaStream_t stream);
+                           int G, void* out, bool out_f32, cudaStream_t stream, bool bf16 = false);
 
 // Round-to-nearest group quantization (awq_quantize_rtn): w fp16 [N, K] -> qweight
 // [K, N/8], qzeros [K/G, N/8], scales [K/G, N].
@@ -71,6 +73,19 @@ cudaError_t read_and_clear_status(cudaStream_t stream, unsigned int* value);
 // Column of a nibble: nibble i of a packed word holds column ORDER[i] of its eight,
 // ORDER = {0,2,4,6,1,3,5,7} (tensref.org/formats/awq, "Reader").
 __host__ __device__ constexpr int nibble_column(int i) { return ((i & 3) << 1) | (i >> 2); }
+
+// 16-bit activation / scale elements: fp16, or bf16 when kBF (same storage).
+template <bool kBF>
+__device__ __forceinline__ float elem_to_float(uint16_t u) {
+  if constexpr (kBF) return __uint_as_float(static_cast<uint32_t>(u) << 16);
+  else return __half2float(__ushort_as_half(u));
+}
+// One rounding (to nearest even) of fp32 to the element type, as its 16-bit pattern.
+template <bool kBF>
+__device__ __forceinline__ uint16_t float_to_elem(float f) {
+  if constexpr (kBF) return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  else return __half_as_ushort(__float2half_rn(f));
+}
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

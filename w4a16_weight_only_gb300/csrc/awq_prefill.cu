@@ -148,7 +148,10 @@ constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (1u << 15) | (0
 // the accumulator rows of its own A half.
 constexpr uint32_t kIdescPair = (kIdesc & ~(0x1Fu << 24)) | (static_cast<uint32_t>((2 * kBN) >> 4) << 24);
 
-template <bool kPair>
+// kind::f16 with bf16 A and B: formats 1 in the A and B format fields (bits 7-9, 10-12).
+constexpr uint32_t kIdescBF16 = (1u << 7) | (1u << 10);
+
+template <bool kPair, bool kBF = false>
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                         uint32_t accumulate) {
   if constexpr (kPair) {
@@ -156,14 +159,14 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdescPair), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(kIdescPair | (kBF ? kIdescBF16 : 0u)), "r"(accumulate)
         : "memory");
   } else {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(kIdesc | (kBF ? kIdescBF16 : 0u)), "r"(accumulate)
         : "memory");
   }
 }
@@ -260,8 +263,11 @@ __device__ __forceinline__ uint4 lds128p(uint32_t a) {
   return v;
 }
 
-template <bool kPair>
+// kBF: bf16 activations, scales, bias and output; the dequantized A tile is bf16
+// ((c - z) * s rounded once), the MMA kind::f16 with bf16 operands.
+template <bool kPair, bool kBF = false>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  constexpr uint32_t kMag = kBF ? 0x43004300u : kMagic;  // 128 (bf16) / 1024 (fp16), both halves
   using L = Layout<kPair>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -422,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const uint64_t bdesc = sw128_desc(sbase + L::X_OFF + s * L::X_BYTES, 16u, 1024u);
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks)  // K += 16: A two atoms (2048 B), B 32 B
-            mma_f16<kPair>(d, adesc + (2u * kA_SBO >> 4) * ks, bdesc + 2 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
+            mma_f16<kPair, kBF>(d, adesc + (2u * kA_SBO >> 4) * ks, bdesc + 2 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
           any = true;
           mma_commit<kPair>(&empty_t[s]);
           mma_commit<kPair>(&empty_a[sa]);
@@ -482,14 +488,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           uint32_t zp[4];                                    // (1024+z[2j], 1024+z[2j+1])
           const uint32_t zc = cc ? zw[1] : zw[0];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) zp[j] = and_or(zc >> (4 * j), 0x000F000Fu, kMagic);
+          for (int j = 0; j < 4; ++j) zp[j] = and_or(zc >> (4 * j), 0x000F000Fu, kMag);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             uint32_t v[4];
             const uint32_t wc = cc ? w[e][1] : w[e][0];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              v[j] = hmul2(hsub2(and_or(wc >> (4 * j), 0x000F000Fu, kMagic), zp[j]), sp[j]);
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t h = and_or(wc >> (4 * j), 0x000F000Fu, kMag);
+              v[j] = kBF ? hmul2_bf16(hsub2_bf16(h, zp[j]), sp[j]) : hmul2(hsub2(h, zp[j]), sp[j]);
+            }
             const int k = rp + 32 * e;
             const int off = ((cw >> 3) * 8 + (k >> 3)) * 1024 + (k & 7) * 128 +
                             (((cw & 7) ^ (k & 7)) << 4);
@@ -531,7 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int b = li % kAccBufs;
       const int m0 = (tile % p.tiles_t) * kBT;
       const int n = (tile / p.tiles_t) * (8 * kTileWords) + static_cast<int>(rank) * kBN + nl;
-      const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+      const float bias = (p.bias != nullptr && n < p.N)
+                             ? elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[n])
+                             : 0.f;
       if (!wait(&tfull[b], static_cast<uint32_t>((li / kAccBufs) & 1))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
@@ -545,7 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (t0 + j < p.M)
-              p.y[(long long)(t0 + j) * p.N + n] = __float2half_rn(__uint_as_float(v[j]) + bias);
+              reinterpret_cast<uint16_t*>(p.y)[(long long)(t0 + j) * p.N + n] =
+                  float_to_elem<kBF>(__uint_as_float(v[j]) + bias);
           }
         }
       }
@@ -570,12 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   }
 }
 
-template <bool kPair>
+template <bool kPair, bool kBF = false>
 cudaError_t set_smem_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(prefill_kernel<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(prefill_kernel<kPair, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(Layout<kPair>::SMEM));
   });
   return err;
@@ -627,24 +638,25 @@ bool prefill_supported(const GemmProblem& p, const char** why) {
 #endif
 
 cudaError_t launch_prefill(const GemmProblem& p) {
-  cudaError_t e = set_smem_attr<false>();
-  if (e == cudaSuccess) e = set_smem_attr<true>();
+  cudaError_t e = p.bf16 ? set_smem_attr<false, true>() : set_smem_attr<false>();
+  if (e == cudaSuccess && !p.bf16) e = set_smem_attr<true>();
   if (e != cudaSuccess) return e;
   // Pair mode (two CTAs per 256 x 256 tile) when enabled and pairs of SMs can be co-scheduled.
-  const int pairs = AWQ_PREFILL_PAIR ? pair_capacity() : 0;
+  const int pairs = (AWQ_PREFILL_PAIR && !p.bf16) ? pair_capacity() : 0;  // pair mode: fp16 only
   const bool pair = pairs > 0;
   PrefillParams pp;
   const char* why = nullptr;
   const int C = p.N / 8;
   const int ngrp = p.K / p.G;
   const int x_rows = pair ? kBT / 2 : kBT;
-  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kBK, x_rows,
+  const CUtensorMapDataType et = p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!make_tmap_2d(&pp.tm_x, et, 2, p.x, p.K, p.M, kBK, x_rows,
                     CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
       !make_tmap_2d(&pp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, 16, kBK,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
       !make_tmap_2d(&pp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, 16, 1,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
-      !make_tmap_2d(&pp.tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.sc, p.N, ngrp, 128, 1,
+      !make_tmap_2d(&pp.tm_s, et, 2, p.sc, p.N, ngrp, 128, 1,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why))
     return cudaErrorInvalidValue;
   pp.bias = p.bias;
@@ -680,7 +692,8 @@ cudaError_t launch_prefill(const GemmProblem& p) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = pp.tiles < sms ? pp.tiles : sms;
-  prefill_kernel<false><<<grid, kThreads, Layout<false>::SMEM, p.stream>>>(pp);
+  if (p.bf16) prefill_kernel<false, true><<<grid, kThreads, Layout<false>::SMEM, p.stream>>>(pp);
+  else prefill_kernel<false><<<grid, kThreads, Layout<false>::SMEM, p.stream>>>(pp);
   return cudaGetLastError();
 }
 
