@@ -431,9 +431,13 @@ def run_sweep(args, local):
         tf_kind = "measured bf16 burst (fp16 nominal rate equal)"
     except Exception:
         tflops, tf_kind = 1900.0, "fallback"
-    names = [w[2] for w in synth.WORKLOADS]
+    names = [(w[2], "f16") for w in synth.WORKLOADS]
+    # bf16 activations / scales on the decode bench linears, a small batch, prefill, 70B
+    names += [(n, "bf16") for n in ("7b_decode_m1_4096x4096_bias", "7b_decode_m1_4096x11008_bias",
+                                    "7b_decode_m1_11008x4096_bias", "7b_smallbatch_m16_4096x11008",
+                                    "7b_prefill_m2048_4096x11008", "70b_m1_8192x28672")]
     if args.case:
-        names = [n for n in names if args.case in n]
+        names = [(n, dt) for (n, dt) in names if args.case in (n if dt == "f16" else n + "_bf16")]
     stream = torch.cuda.Stream()
 
     def timed(fn, reps):
@@ -446,18 +450,22 @@ def run_sweep(args, local):
         b.synchronize()
         return a.elapsed_time(b) / reps * 1e3  # us
 
-    for name in names:
-        d = synth.workload_inputs(name)
+    for name, dt in names:
+        d = synth.workload_inputs(name, dt)
         M, K, N, G = d["M"], d["K"], d["N"], d["group_size"]
-        x = torch.from_numpy(d["x"]).cuda()
+        tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+        x = torch.from_numpy(d["x"]).to(tdt).cuda()
         qw = torch.from_numpy(d["qweight"]).cuda()
         qz = torch.from_numpy(d["qzeros"]).cuda()
-        sc = torch.from_numpy(d["scales"]).cuda()
-        bias = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
-        y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        sc = torch.from_numpy(d["scales"]).to(tdt).cuda()
+        bias = torch.from_numpy(d["bias"]).to(tdt).cuda() if d["bias"] is not None else None
+        y = torch.empty((M, N), dtype=tdt, device="cuda")
+        if dt == "bf16":
+            name = name + "_bf16"
         nbytes = algorithmic_bytes(M, K, N, G, bias is not None)
         flop = 2.0 * M * N * K
-        line = {"workload": name, "M": M, "K": K, "N": N, "group_size": G, "bias": bias is not None,
+        line = {"workload": name, "dtype": dt, "M": M, "K": K, "N": N, "group_size": G,
+                "bias": bias is not None,
                 "path": awq.select_path(x, qw, qz, sc, bias, G, y)}
         if M <= 32:
             R = max(2, min(16, int(3 * L2_BYTES // nbytes) + 1))

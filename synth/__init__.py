@@ -161,6 +161,6 @@ def workload(name: str):
     raise KeyError(name)
 
 
-def workload_inputs(name: str) -> dict:
+def workload_inputs(name: str, dtype: str = "f16") -> dict:
     cfg, si, _, M, K, N, G, b = workload(name)
-    return awq_linear(seed_for(cfg, si), M, K, N, group_size=G, bias=b)
+    return awq_linear(seed_for(cfg, si), M, K, N, group_size=G, bias=b, dtype=dtype)
