@@ -3,9 +3,10 @@ see awq_oracle.py)."""
 from .awq_oracle import (ORDER, REVERSE_ORDER, resolve_group_size, unpack_codes,
                          pack_codes, dequant_f32, dequant_f16, dequant_page_layout,
                          gemm, gemm_sampled, gemm_rows, dequant_columns_f32,
-                         within_tolerance, quantize_rtn, round_to_bf16, dequant_bf16)
+                         within_tolerance, quantize_rtn, round_to_bf16, dequant_bf16,
+                         gemm_grouped)
 
 __all__ = ["ORDER", "REVERSE_ORDER", "resolve_group_size", "unpack_codes", "pack_codes",
            "dequant_f32", "dequant_f16", "dequant_page_layout", "gemm", "gemm_sampled",
            "gemm_rows", "dequant_columns_f32", "within_tolerance", "quantize_rtn",
-           "round_to_bf16", "dequant_bf16"]
+           "round_to_bf16", "dequant_bf16", "gemm_grouped"]

@@ -46,6 +46,11 @@ What it computes, and where each step comes from:
   :func:`dequant_bf16` is the exact fp32 dequant rounded once to bf16
   (:func:`round_to_bf16`, nearest even: bf16 is the upper half of an fp32).
 
+* Grouped (mixture-of-experts) linear (:func:`gemm_grouped`; vLLM article,
+  section 5.4: routed expert layers with 4-bit AWQ weights): rows
+  ``offsets[e] .. offsets[e+1]-1`` of ``x`` (routed rows sorted by expert) go
+  through expert ``e``'s AWQ linear, each as :func:`gemm` defines it.
+
 Pins (tests/test_oracle.py, run without a GPU): ORDER and its inverse from
 the wiki's "Saved formats and packing" section, a hand-packed word, AWQ-004
 (sequential-nibble decode differs), AWQ-005 (zero equal to code gives an
@@ -260,4 +265,23 @@ def quantize_rtn(w, group_size, sym=False):
     codes_kn = code.reshape(N, K).T.astype(np.int64)     # [K, N]
     zeros_gn = zero.T.astype(np.int64)                   # [K/G, N]
     return pack_codes(codes_kn), pack_codes(zeros_gn), np.ascontiguousarray(scale16.T)
+
+
+def gemm_grouped(x, qweight, qzeros, scales, bias, group_size, offsets) -> np.ndarray:
+    """y [R, N]: rows offsets[e]..offsets[e+1]-1 of x [R, K] times expert e's weight
+    (qweight [E, K, N/8], qzeros [E, K/G, N/8], scales [E, K/G, N], bias [E, N] or
+    None), each block as :func:`gemm` (fp64)."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    E = len(offsets) - 1
+    R = np.asarray(x).shape[0]
+    N = np.asarray(qweight).shape[2] * 8
+    if offsets[0] != 0 or offsets[-1] != R or (np.diff(offsets) < 0).any():
+        raise ValueError("offsets must rise from 0 to the number of rows")
+    y = np.zeros((R, N), dtype=np.float64)
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            y[a:b] = gemm(np.asarray(x)[a:b], qweight[e], qzeros[e], scales[e],
+                          None if bias is None else bias[e], group_size)
+    return y
 

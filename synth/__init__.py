@@ -31,7 +31,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["awq_linear", "seed_for", "SYM_ZERO_WORD"]
+__all__ = ["awq_linear", "seed_for", "SYM_ZERO_WORD", "moe_inputs"]
 
 # Every nibble equal to 8.  A word with all nibbles equal is invariant under
 # any nibble permutation, so no ordering knowledge is needed to write it.
@@ -164,3 +164,31 @@ def workload(name: str):
 def workload_inputs(name: str, dtype: str = "f16") -> dict:
     cfg, si, _, M, K, N, G, b = workload(name)
     return awq_linear(seed_for(cfg, si), M, K, N, group_size=G, bias=b, dtype=dtype)
+
+
+def moe_inputs(seed: int, T: int, topk: int, E: int, K: int, N: int, group_size: int = 128,
+               bias: bool = False) -> dict:
+    """Synthetic mixture-of-experts layer: E experts' AWQ linears (each drawn as
+    awq_linear, seeds seed + 1 + e) and T tokens each routed to topk distinct experts
+    drawn uniformly; the routed rows (token copies) are sorted by expert (stable), so
+    expert e owns rows offsets[e] .. offsets[e+1]-1.  Returns x [T*topk, K] fp16,
+    qweight [E, K, N/8], qzeros [E, K/G, N/8], scales [E, K/G, N], bias [E, N] or None,
+    offsets int32 [E+1], token_of_row, plus the sizes."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    tokens = rng.standard_normal((T, K), dtype=np.float32).astype(np.float16)
+    choice = np.stack([rng.permutation(E)[:topk] for _ in range(T)])   # [T, topk]
+    expert_of_row = choice.reshape(-1)
+    token_of_row = np.repeat(np.arange(T), topk)
+    order = np.argsort(expert_of_row, kind="stable")
+    expert_of_row, token_of_row = expert_of_row[order], token_of_row[order]
+    counts = np.bincount(expert_of_row, minlength=E)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    ex = [awq_linear(seed + 1 + e, 1, K, N, group_size=group_size, bias=bias) for e in range(E)]
+    return {"x": np.ascontiguousarray(tokens[token_of_row]),
+            "qweight": np.ascontiguousarray(np.stack([d["qweight"] for d in ex])),
+            "qzeros": np.ascontiguousarray(np.stack([d["qzeros"] for d in ex])),
+            "scales": np.ascontiguousarray(np.stack([d["scales"] for d in ex])),
+            "bias": np.ascontiguousarray(np.stack([d["bias"] for d in ex])) if bias else None,
+            "offsets": offsets, "token_of_row": token_of_row, "group_size": int(group_size),
+            "R": int(T * topk), "E": E, "K": K, "N": N}
+

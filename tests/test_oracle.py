@@ -415,3 +415,53 @@ def test_dequant_bf16_is_one_rounding_of_the_exact_value():
     assert np.array_equal(got, oracle.round_to_bf16(exact))
     # the bf16 value is within half a bf16 ulp of the exact one
     assert (np.abs(got - exact) <= np.abs(exact) * 2.0 ** -8 + 1e-30).all()
+
+
+# ------------------------------------------------------- grouped (MoE) ----
+# vLLM article, section 5.4: routed expert layers with 4-bit AWQ weights.  The grouped oracle
+# must reduce to the pinned single-linear GEMM: identical experts give one GEMM over all
+# rows; empty experts own no rows; relabelling experts (and moving their row blocks) only
+# moves rows.
+
+def test_grouped_identical_experts_equal_one_gemm():
+    from synth import moe_inputs
+    d = moe_inputs(51, 12, 2, 4, 64, 16, group_size=32, bias=True)
+    qw = np.stack([d["qweight"][0]] * 4)
+    qz = np.stack([d["qzeros"][0]] * 4)
+    sc = np.stack([d["scales"][0]] * 4)
+    b = np.stack([d["bias"][0]] * 4)
+    y = oracle.gemm_grouped(d["x"], qw, qz, sc, b, 32, d["offsets"])
+    assert np.array_equal(y, oracle.gemm(d["x"], qw[0], qz[0], sc[0], b[0], 32))
+
+
+def test_grouped_blocks_and_empty_experts():
+    from synth import moe_inputs
+    d = moe_inputs(52, 5, 1, 8, 64, 16, group_size=-1)   # 5 rows over 8 experts: some empty
+    offs = d["offsets"]
+    assert (np.diff(offs) == 0).any()
+    y = oracle.gemm_grouped(d["x"], d["qweight"], d["qzeros"], d["scales"], None, -1, offs)
+    for e in range(8):
+        a, b = offs[e], offs[e + 1]
+        ref = oracle.gemm(d["x"][a:b], d["qweight"][e], d["qzeros"][e], d["scales"][e], None, -1)
+        assert np.array_equal(y[a:b], ref)
+
+
+def test_grouped_relabelling_moves_rows():
+    from synth import moe_inputs
+    d = moe_inputs(53, 9, 2, 3, 64, 16, group_size=32)
+    offs = d["offsets"]
+    y = oracle.gemm_grouped(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 32, offs)
+    perm = [2, 0, 1]  # new expert i is old expert perm[i]
+    blocks = [np.arange(offs[p], offs[p + 1]) for p in perm]
+    rows = np.concatenate(blocks)
+    new_offs = np.concatenate([[0], np.cumsum([len(b) for b in blocks])])
+    y2 = oracle.gemm_grouped(d["x"][rows], d["qweight"][perm], d["qzeros"][perm], d["scales"][perm],
+                             None, 32, new_offs)
+    assert np.array_equal(y2, y[rows])
+
+
+def test_grouped_rejects_bad_offsets():
+    from synth import moe_inputs
+    d = moe_inputs(54, 4, 1, 2, 64, 16, group_size=32)
+    with pytest.raises(ValueError):
+        oracle.gemm_grouped(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 32, [0, 3, 2])
