@@ -122,6 +122,32 @@ awq_status_t awq_dequant_bf16(const int32_t* qweight, const int32_t* qzeros, con
                               awq_dtype_t out_dtype, awq_stream_t stream);
 
 /*
+ * awq_gemm_grouped -- grouped (mixture-of-experts) W4A16 linear in one launch (routed expert
+ * layers with 4-bit AWQ weights: the vLLM article, section 5.4).  E experts' weights are
+ * stacked; the routed rows of x are sorted by expert:
+ *
+ *   y[r][n] = fp16_rne( sum_k x[r][k] * w_e[k][n] (+ bias[e][n]) )  for offsets[e] <= r < offsets[e+1]
+ *
+ *   x_f16           fp16 [R, K]            routed rows, sorted by expert
+ *   qweight         int32 [E, K, N/8], qzeros int32 [E, K/G, N/8], scales_f16 fp16 [E, K/G, N]
+ *   bias_f16        fp16 [E, N] or NULL
+ *   expert_offsets  DEVICE int32 [E + 1]: 0 = offsets[0] <= ... <= offsets[E] = R (may come
+ *                   from a routing kernel on the same stream; it is read on the device only,
+ *                   after the preceding kernel completes)
+ *   y_f16           fp16 [R, N]
+ *
+ * Requirements: those of the decode path's TMA kernel (K % 64 == 0, group size % 64 == 0,
+ * N % 32 == 0, x / qweight / qzeros / scales 16-byte aligned), 1 <= E <= 4096,
+ * R / 8 + E <= 65535, E*K*N < 2^40.  Offsets outside [0, R] or not rising give unspecified
+ * values in y but never an access outside x, y or the stacked weights.  R == 0 returns
+ * AWQ_OK without a launch.  One kernel launch; asynchronous on `stream`.
+ */
+awq_status_t awq_gemm_grouped(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                              const void* scales_f16, const void* bias_f16,
+                              const int32_t* expert_offsets, int64_t R, int64_t E, int64_t K,
+                              int64_t N, int64_t group_size, void* y_f16, awq_stream_t stream);
+
+/*
  * awq_quantize_rtn -- round-to-nearest 4-bit group quantization of a linear layer's fp16
  * weight into this layout (GPTQModel wiki "AWQ", "Group quantization and zero points":
  * the asymmetric and symmetric modes of its table; packing with ORDER as the format

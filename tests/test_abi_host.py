@@ -155,3 +155,16 @@ def test_quantize_argument_checks_are_host_side(lib):
     if not torch.cuda.is_available():
         assert q(W, 8, 64, 32, 1, A, A, B, None) == DEVICE
 
+
+def test_grouped_argument_checks_are_host_side(lib):
+    g = lib.awq_gemm_grouped
+    # (x, qweight, qzeros, scales, bias, offsets, R, E, K, N, G, y, stream)
+    assert g(A, A, A, A, None, A, 8, 0, 256, 256, 128, B, None) == INVALID       # E == 0
+    assert g(A, A, A, A, None, A, 8, 5000, 256, 256, 128, B, None) == INVALID    # E too large
+    assert g(A, A, A, A, None, A, 8, 2, 256, 12, 128, B, None) == SHAPE          # N % 8
+    assert g(A, A, A, A, None, A, 600000, 2, 256, 256, 128, B, None) == SHAPE    # R / 8 + E > 65535
+    assert g(A, A, A, A, None, None, 8, 2, 256, 256, 128, B, None) == INVALID    # null offsets
+    assert g(A, A, A, A, None, ODD, 8, 2, 256, 256, 128, B, None) == MISALIGNED
+    assert g(A, A, A, A, None, A, 8, 2, 96, 256, 32, B, None) == SHAPE           # outside the TMA contract
+    assert g(None, None, None, None, None, None, 0, 2, 256, 256, 128, None, None) == 0  # R == 0
+

@@ -36,6 +36,7 @@ SIGNATURES = {
     "awq_gemm_bf16": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "awq_gemm_bf16_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp]),
     "awq_dequant_bf16": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "awq_gemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp]),
 }
 
 _lib = None
@@ -141,6 +142,35 @@ def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, pa
             M, K, N, group_size, _ptr(out), PATHS[path], _stream(stream))
     _check(st)
     return out.reshape(*lead, N)
+
+
+def awq_gemm_grouped(x, qweight, qzeros, scales, offsets, bias=None, group_size=128, out=None,
+                     stream=None):
+    """Grouped (mixture-of-experts) linear via the library's awq_gemm_grouped: rows
+    offsets[e]..offsets[e+1]-1 of x fp16 [R, K] through expert e (qweight int32 [E, K, N/8],
+    qzeros int32 [E, K/G, N/8], scales fp16 [E, K/G, N], bias fp16 [E, N] or None);
+    offsets int32 [E+1] on the device.  Returns fp16 [R, N]."""
+    lib = load_library()
+    R, K = x.shape
+    E, _, C = qweight.shape
+    N = 8 * C
+    dev = x.device
+    _need(x, "x", torch.float16, (R, K), dev)
+    _need(qweight, "qweight", torch.int32, (E, K, C), dev)
+    ng = _groups(K, group_size)
+    _need(qzeros, "qzeros", torch.int32, (E, ng, C), dev)
+    _need(scales, "scales", torch.float16, (E, ng, N), dev)
+    _need(offsets, "offsets", torch.int32, (E + 1,), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.float16, (E, N), dev)
+    if out is None:
+        out = torch.empty((R, N), dtype=torch.float16, device=dev)
+    else:
+        _need(out, "out", torch.float16, (R, N), dev)
+    st = lib.awq_gemm_grouped(_ptr(x), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
+                              _ptr(offsets), R, E, K, N, group_size, _ptr(out), _stream(stream))
+    _check(st)
+    return out
 
 
 def awq_dequant(qweight, qzeros, scales, group_size=128, out_dtype=torch.float16, out=None,

@@ -250,6 +250,32 @@ awq_status_t awq_gemm_bf16_ex(const void* x_bf16, const int32_t* qweight, const 
                   path, stream, true);
 }
 
+awq_status_t awq_gemm_grouped(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                              const void* scales_f16, const void* bias_f16,
+                              const int32_t* expert_offsets, int64_t R, int64_t E, int64_t K,
+                              int64_t N, int64_t group_size, void* y_f16, awq_stream_t stream) {
+  if (E <= 0 || E > 4096) return fail(AWQ_ERR_INVALID_ARGUMENT, "E must be in 1..4096 (got %lld)", (long long)E);
+  awq::GemmProblem p{};
+  bool empty = false;
+  awq_status_t st = build_problem(x_f16, qweight, qzeros, scales_f16, bias_f16, R, K, N, group_size,
+                                  y_f16, stream, &p, &empty, false);
+  if (st != AWQ_OK) return st;
+  if (K * N * E >= kProdLimit) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "E*K*N must be below 2^40");
+  if ((R + 7) / 8 + E > 65535) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "R/8 + E must be at most 65535");
+  if (empty) return ok();
+  if (!expert_offsets) return fail(AWQ_ERR_INVALID_ARGUMENT, "null expert_offsets");
+  if (!al(expert_offsets, 4)) return fail(AWQ_ERR_MISALIGNED, "expert_offsets must be 4-byte aligned");
+  p.offsets = expert_offsets;
+  p.E = static_cast<int>(E);
+  const char* why = "";
+  if (!awq::decode_grouped_supported(p, &why)) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "grouped: %s", why);
+  st = check_device();
+  if (st != AWQ_OK) return st;
+  const cudaError_t e = awq::launch_decode_grouped(p);
+  if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_grouped launch");
+  return ok();
+}
+
 awq_status_t awq_gemm_bf16(const void* x_bf16, const int32_t* qweight, const int32_t* qzeros,
                            const void* scales_bf16, const void* bias_bf16, int64_t M, int64_t K,
                            int64_t N, int64_t group_size, void* y_bf16, awq_stream_t stream) {

@@ -81,6 +81,8 @@ struct __align__(64) TmaDecodeParams {
   // Byte offsets inside the 1024-aligned dynamic shared memory (activation rings at 0).
   int w_off, m_off, zl_off, bias_off, bar_off, recv_off;
   int owners;  // CTAs of the cluster that finish a slice of the output tile (1 or cs)
+  const int* offsets;  // grouped: expert row offsets (device, E + 1), else null
+  int E;               // grouped: experts
   int slice;   // floats of the packed partial each owner finishes (multiple of 4)
 };
 
@@ -141,9 +143,16 @@ constexpr int kMinBlocks = NW == 8 ? 2 : (TB == 1 ? AWQ_DECODE_MIN_BLOCKS_M8 : A
 // exact bf16 value 128 + c (0x4300 | c: the subnormal trick has no room for a 4-bit code
 // above bf16's 7-bit significand without leaving fp32's normal range in the products), so
 // the fold is acc += scale * (sum x (128 + c) - (128 + zero) * sum x).
-template <int TB, int CWL, bool kSub, bool kOne, int NW, bool kBF>
+// kGrp: grouped (mixture-of-experts) launch.  Weights, zeros, scales (and bias) are stacked
+// over E experts and read through 3D tensor maps; blockIdx.y counts 8-row tiles over the
+// experts in order, each CTA finding its expert and rows in the device offsets after the
+// grid-dependency wait (the offsets come from the routing); tiles past the last expert's
+// exit at once (whole clusters share blockIdx.y).  Rows of a tile that belong to the next
+// expert are computed and discarded.
+template <int TB, int CWL, bool kSub, bool kOne, int NW, bool kBF, bool kGrp = false>
 __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     decode_tma_kernel(const __grid_constant__ TmaDecodeParams p) {
+  static_assert(!kGrp || (TB == 1 && !kOne), "grouped launches use 8-row tiles");
   static_assert(NW == 4 || NW == 8, "4 or 8 warps per CTA");
   constexpr uint32_t kOne2 = kBF ? 0x3F803F80u : kOnes;     // 1.0 in both halves
   constexpr uint32_t kMag = kBF ? 0x43004300u : kMagic;     // 128 (bf16) / 1024 (fp16)
@@ -163,7 +172,27 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
   const uint32_t rank = cluster_ctarank();
   const uint32_t cs = cluster_nctarank();
   const int cw0 = static_cast<int>(blockIdx.x / cs) * GE::CW_W;
-  const int m0 = blockIdx.y * 8 * TB;
+  int m0 = blockIdx.y * 8 * TB;
+  int m_lim = p.M;  // rows of this tile are m0 .. min(m0 + 8 TB, m_lim) - 1
+  int ex = 0;       // expert (grouped)
+  if constexpr (kGrp) {
+    grid_dependency_wait();
+    int t = static_cast<int>(blockIdx.y);
+    bool found = false;
+    for (int e = 0; e < p.E && !found; ++e) {
+      const int a = p.offsets[e], b = p.offsets[e + 1];
+      const int n = b > a ? (b - a + 8 * TB - 1) / (8 * TB) : 0;
+      if (t < n) {
+        m0 = a + 8 * TB * t;
+        m_lim = min(b, p.M);
+        ex = e;
+        found = true;
+      } else {
+        t -= n;
+      }
+    }
+    if (!found) return;
+  }
 
   // 32-bit arithmetic throughout: TS * P < 2^31 (checked on the host).
   const uint32_t TS = static_cast<uint32_t>(p.K / kRS);
@@ -217,11 +246,17 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     uint64_t* bar = &my_bars[slot];
     const bool meta = (j == j0) || (iss_left == spg);
     mbar_arrive_expect_tx(bar, GE::W_BYTES + x_tx + (meta ? GE::META_TX : 0u));
-    tma_load_2d(w_ring + slot * GE::W_BYTES, &p.tm_w, bar, cw0, j * kRS);
+    if constexpr (kGrp) tma_load_3d(w_ring + slot * GE::W_BYTES, &p.tm_w, bar, cw0, j * kRS, ex);
+    else tma_load_2d(w_ring + slot * GE::W_BYTES, &p.tm_w, bar, cw0, j * kRS);
     if (meta) {
       unsigned char* md = m_ring + (kOne ? iss_grp - g_first : slot) * GE::META_SLOT;
-      tma_load_2d(md, &p.tm_z, bar, cw0, iss_grp);
-      tma_load_2d(md + 128, &p.tm_s, bar, 8 * cw0, iss_grp);
+      if constexpr (kGrp) {
+        tma_load_3d(md, &p.tm_z, bar, cw0, iss_grp, ex);
+        tma_load_3d(md + 128, &p.tm_s, bar, 8 * cw0, iss_grp, ex);
+      } else {
+        tma_load_2d(md, &p.tm_z, bar, cw0, iss_grp);
+        tma_load_2d(md + 128, &p.tm_s, bar, 8 * cw0, iss_grp);
+      }
     }
     if (--iss_left == 0) {
       ++iss_grp;
@@ -294,7 +329,7 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     for (int i = threadIdx.x; i < 8 * GE::CW_W; i += NW * 32) {
       const int n = 8 * cw0 + i;
       bias_s[i] = (p.bias != nullptr && n < p.N)
-                      ? elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[n])
+                      ? elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[(long long)ex * p.N + n])
                       : 0.f;
     }
   }
@@ -633,7 +668,7 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
   const int hi = min(pack_n, lo + p.slice);
   for (int i = lo + threadIdx.x; got && i < hi; i += NW * 32) {
     const int t = i / (8 * GE::CW_W), col = i - t * 8 * GE::CW_W;
-    if (m0 + t >= p.M || 8 * cw0 + col >= p.N) continue;
+    if (m0 + t >= m_lim || m0 + t < 0 || 8 * cw0 + col >= p.N) continue;
     float sum = 0.f;
     for (uint32_t r = 0; r < cs; ++r) sum += recv[r * p.slice + (i - lo)];
     reinterpret_cast<uint16_t*>(p.y)[(long long)(m0 + t) * p.N + 8 * cw0 + col] =
@@ -760,9 +795,9 @@ int max_warp_groups(int TS, int P, int spg) {
 }
 
 // Co-resident clusters of size cs at `smem` bytes per CTA (occupancy API).
-template <int TB, int CWL, bool S, bool O, int NW, bool B>
+template <int TB, int CWL, bool S, bool O, int NW, bool B, bool GR = false>
 int max_clusters(int cs, int smem) {
-  auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B>;
+  auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B, GR>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, 1, 1);
   cfg.blockDim = dim3(NW * 32, 1, 1);
@@ -787,7 +822,7 @@ int max_clusters(int cs, int smem) {
 // each warp keeping at least one 64-row stage; ties go to the smaller cluster.  Ring
 // depth: as many slots as the shared memory left per CTA allows, up to the warp's stage
 // count.  Cached per shape.
-template <int TB, int CWL, bool S, bool O, int NW, bool B>
+template <int TB, int CWL, bool S, bool O, int NW, bool B, bool GR = false>
 cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   using GE = Geo<TB, CWL, NW>;
   static std::mutex mu;
@@ -798,7 +833,8 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
   const int C = p.N / 8;
   const int nt = (C + GE::CW_W - 1) / GE::CW_W;
-  const long long mz = (p.M + 8 * TB - 1) / (8 * TB);
+  // grouped: an upper bound on the 8-row tiles over all experts
+  const long long mz = GR ? (p.M + 7) / 8 + p.E : (p.M + 8 * TB - 1) / (8 * TB);
   const auto key = std::make_tuple(dev, p.K, nt * (int)mz, x_rows);
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
@@ -812,7 +848,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B>;
+    auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B, GR>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dl.smem_optin);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -852,7 +888,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
     // single wave with slack, checked against the occupancy API at this size
     bool fits = false;
     while (true) {
-      long long cap = (long long)max_clusters<TB, CWL, S, O, NW, B>(cs, pl.smem) * cs;
+      long long cap = (long long)max_clusters<TB, CWL, S, O, NW, B, GR>(cs, pl.smem) * cs;
       if (cap > (long long)kMaxCtasPerSm * dl.sms) cap = (long long)kMaxCtasPerSm * dl.sms;
       if (grid * 100 <= cap * kWaveFillPct) { fits = true; break; }
       if (pl.slots <= red_slots || pl.slots <= 1) break;
@@ -871,11 +907,11 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   return cudaSuccess;
 }
 
-template <int TB, int CWL, bool S, bool O, int NW, bool B>
+template <int TB, int CWL, bool S, bool O, int NW, bool B, bool GR = false>
 cudaError_t launch_v(const GemmProblem& p) {
   using GE = Geo<TB, CWL, NW>;
   Plan pl;
-  cudaError_t e = plan_for<TB, CWL, S, O, NW, B>(p, &pl);
+  cudaError_t e = plan_for<TB, CWL, S, O, NW, B, GR>(p, &pl);
   if (e != cudaSuccess) return e;
   const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
 
@@ -883,14 +919,24 @@ cudaError_t launch_v(const GemmProblem& p) {
   const char* why = nullptr;
   const int C = p.N / 8;
   const int ngrp = p.K / p.G;
-  if (!make_tmap_2d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, GE::CW_W, kRS,
-                    CWL == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B, &why) ||
-      !make_tmap_2d(&dp.tm_x, B ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kRS, x_rows,
-                    (x_rows == 1 && !AWQ_DECODE_WIDE_X) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
-      !make_tmap_2d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, GE::CW_W, 1,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
-      !make_tmap_2d(&dp.tm_s, B ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.sc, p.N, ngrp, 8 * GE::CW_W, 1,
-                    CU_TENSOR_MAP_SWIZZLE_NONE, &why))
+  const CUtensorMapSwizzle wsw = CWL == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  const CUtensorMapDataType et = B ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  bool maps_ok = make_tmap_2d(&dp.tm_x, et, 2, p.x, p.K, p.M, kRS, x_rows,
+                              (x_rows == 1 && !AWQ_DECODE_WIDE_X) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, &why);
+  if (GR) {  // stacked experts: [E][K][C], [E][K/G][C], [E][K/G][N]
+    maps_ok = maps_ok &&
+              make_tmap_3d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, p.E, GE::CW_W, kRS, wsw, &why) &&
+              make_tmap_3d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, p.E, GE::CW_W, 1,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, &why) &&
+              make_tmap_3d(&dp.tm_s, et, 2, p.sc, p.N, ngrp, p.E, 8 * GE::CW_W, 1, CU_TENSOR_MAP_SWIZZLE_NONE, &why);
+  } else {
+    maps_ok = maps_ok &&
+              make_tmap_2d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, GE::CW_W, kRS, wsw, &why) &&
+              make_tmap_2d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, GE::CW_W, 1,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, &why) &&
+              make_tmap_2d(&dp.tm_s, et, 2, p.sc, p.N, ngrp, 8 * GE::CW_W, 1, CU_TENSOR_MAP_SWIZZLE_NONE, &why);
+  }
+  if (!maps_ok)
     return cudaErrorInvalidValue;
   dp.bias = p.bias;
   dp.y = p.y;
@@ -904,9 +950,11 @@ cudaError_t launch_v(const GemmProblem& p) {
   dp.w_off = pl.w_off; dp.m_off = pl.m_off; dp.zl_off = pl.zl_off;
   dp.bias_off = pl.bias_off; dp.bar_off = pl.bar_off; dp.recv_off = pl.recv_off;
   dp.owners = pl.owners; dp.slice = pl.slice;
+  dp.offsets = p.offsets;
+  dp.E = p.E;
 
   const int nt = (C + GE::CW_W - 1) / GE::CW_W;
-  const int mz = (p.M + 8 * TB - 1) / (8 * TB);
+  const int mz = GR ? (p.M + 7) / 8 + p.E : (p.M + 8 * TB - 1) / (8 * TB);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nt * pl.cs), static_cast<unsigned>(mz), 1);
   cfg.blockDim = dim3(NW * 32, 1, 1);
@@ -921,7 +969,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S, O, NW, B>, dp);
+  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S, O, NW, B, GR>, dp);
 }
 
 }  // namespace
@@ -964,6 +1012,18 @@ cudaError_t launch_decode_tma_t(const GemmProblem& p) {
   }
   if (v.TB == 2) return launch_v<2, 1, true, false, kNW, B>(p);
   return launch_v<4, 1, false, false, kNW, B>(p);
+}
+
+bool decode_grouped_supported(const GemmProblem& p, const char** why) {
+  static const char* dummy;
+  if (!why) why = &dummy;
+  if (p.bf16) { *why = "grouped launches take fp16"; return false; }
+  if (p.E <= 0 || p.offsets == nullptr) { *why = "grouped launch without experts"; return false; }
+  return decode_tma_supported(p, why);
+}
+
+cudaError_t launch_decode_grouped(const GemmProblem& p) {
+  return launch_v<1, 2, true, false, kNW, false, true>(p);
 }
 
 cudaError_t launch_decode_tma(const GemmProblem& p) {

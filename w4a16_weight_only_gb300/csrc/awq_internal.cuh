@@ -21,6 +21,11 @@ struct GemmProblem {
   int M, K, N, G;         // G already resolved (K when group_size == -1)
   cudaStream_t stream;
   bool bf16 = false;      // x, scales, bias and y hold bf16 (same 16-bit storage)
+  // Grouped (mixture-of-experts) problems: E experts' weights stacked ([E, K, N/8],
+  // [E, K/G, N/8], [E, K/G, N], bias [E, N]); rows offsets[e]..offsets[e+1]-1 of x / y
+  // belong to expert e (device array of E + 1 ints).  E == 0: a plain linear.
+  const int* offsets = nullptr;
+  int E = 0;
 };
 
 // Kernel families; values equal awq_path_t.
@@ -47,6 +52,15 @@ bool decode_ldg_supported(const GemmProblem& p, const char** why);
 cudaError_t launch_decode_ldg(const GemmProblem& p);
 bool decode_tma_supported(const GemmProblem& p, const char** why);
 cudaError_t launch_decode_tma(const GemmProblem& p);
+
+// Grouped decode (awq_gemm_grouped): the TMA decode kernel over stacked experts.
+bool decode_grouped_supported(const GemmProblem& p, const char** why);
+cudaError_t launch_decode_grouped(const GemmProblem& p);
+
+// Row-major 3D tensor map: dim0 contiguous elements, dim1 rows, dim2 planes (box depth 1).
+bool make_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                  const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2, uint32_t box0,
+                  uint32_t box1, CUtensorMapSwizzle swizzle, const char** why);
 
 // Row-major 2D tensor map: dim0 contiguous elements per row, dim1 rows.
 bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes,
