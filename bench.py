@@ -510,6 +510,51 @@ def run_sweep(args, local):
         torch.cuda.empty_cache()
     if not args.case or "quantize" in args.case:
         run_quantize_sweep(awq, timed, hbm, hbm_kind)
+    if not args.case or "moe" in args.case:
+        run_grouped_sweep(awq, timed, hbm, hbm_kind)
+
+
+def run_grouped_sweep(awq, timed, hbm, hbm_kind):
+    """awq_gemm_grouped on a mixture-of-experts layer shaped like the 7B MLP with E = 8
+    experts and top-2 routing (synthetic): HBM GB/s of the bytes the launch must move (the
+    experts that received rows, their metadata, x, y) over CUDA-graph replays of rotating
+    copies of the stacked weights (together > 3x L2)."""
+    import torch
+    stream = torch.cuda.Stream()
+    for (K, N) in ((4096, 14336), (14336, 4096)):
+        for T in (1, 16):
+            E, topk, G = 8, 2, 128
+            d = synth.moe_inputs(4000 + T + K, T, topk, E, K, N, group_size=G)
+            active = int((np.diff(d["offsets"]) > 0).sum())
+            R = d["R"]
+            nbytes = active * (K * N // 2 + (K // G) * N // 2 + 2 * (K // G) * N) + 2 * R * K + 2 * R * N
+            dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+            x, offs = dev(d["x"]), dev(d["offsets"])
+            w = (dev(d["qweight"]), dev(d["qzeros"]), dev(d["scales"]))
+            copies = max(2, int(3 * L2_BYTES // (active * K * N // 2)) + 1)
+            sets = [w] + [tuple(t.clone() for t in w) for _ in range(copies - 1)]
+            y = torch.empty((R, N), dtype=torch.float16, device="cuda")
+            calls = max(copies, (60 // copies) * copies)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for i in range(2 * copies):
+                    s = sets[i % copies]
+                    awq.awq_gemm_grouped(x, s[0], s[1], s[2], offs, None, G, out=y, stream=stream)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(calls):
+                        s = sets[i % copies]
+                        awq.awq_gemm_grouped(x, s[0], s[1], s[2], offs, None, G, out=y, stream=stream)
+            t = sorted(timed(g.replay, 1) / calls for _ in range(5))[2]
+            awq.device_status()
+            print(json.dumps({"workload": f"moe_e{E}_top{topk}_t{T}_{K}x{N}", "E": E, "topk": topk,
+                              "tokens": T, "rows": R, "active_experts": active, "K": K, "N": N,
+                              "group_size": G, "us": t, "GB_s": nbytes / t / 1e3,
+                              "frac_hbm": nbytes / t / 1e3 / hbm, "weight_copies": copies,
+                              "launches_per_graph": calls, "hbm_peak_GB_s": hbm,
+                              "hbm_peak": hbm_kind}), flush=True)
+            del sets, g, w, x, y
+            torch.cuda.empty_cache()
 
 
 def quantize_bytes(N, K, G):

@@ -833,8 +833,12 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
   const int C = p.N / 8;
   const int nt = (C + GE::CW_W - 1) / GE::CW_W;
-  // grouped: an upper bound on the 8-row tiles over all experts
-  const long long mz = GR ? (p.M + 7) / 8 + p.E : (p.M + 8 * TB - 1) / (8 * TB);
+  // grouped: the 8-row tiles that will hold rows, estimated (the offsets live on the device):
+  // R rows over E experts fill about max(R / 8, min(R, E)) tiles; the grid itself covers the
+  // upper bound R / 8 + E and the empty tiles exit at once
+  const long long mz = GR ? std::min<long long>((p.M + 7) / 8 + p.E,
+                                                std::max<long long>((p.M + 7) / 8, std::min(p.M, p.E)))
+                          : (p.M + 8 * TB - 1) / (8 * TB);
   const auto key = std::make_tuple(dev, p.K, nt * (int)mz, x_rows);
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(key);
