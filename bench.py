@@ -70,12 +70,12 @@ def step_bytes(lins):
 # `python bench.py --steps 60 --warmup 3 --no-cpu-baseline` summarised in
 # profiles/decode_tma_7b_m1_bench_launches.md; valid only for the kernel source it was
 # measured on (SHA-256 of the files below), else reported as null.
-TRAFFIC_BYTES_PER_LAUNCH = 18_588_150
+TRAFFIC_BYTES_PER_LAUNCH = 18_588_144
 TRAFFIC_SOURCES = {
     "w4a16_weight_only_gb300/csrc/awq_decode_tma.cu":
-        "40f606ca8535e28a9ab964ac7c520ea10c562294398eab11e23f6a8fc30a1777",
+        "5c3cce1c8f779c582aba04ffff707d7e7f033c7338278b8a252bf9eb2d79ec53",
     "w4a16_weight_only_gb300/csrc/awq_ptx.cuh":
-        "d6e2eb90c8015d39adb895095ee759e2fb2397c609be5e9c4fded03a2807c0e5",
+        "166c2c9cd2d4a880677df7bd3dc634de58dadf2fcdc9ba2bdcf045010269d495",
 }
 
 
@@ -338,20 +338,26 @@ def run_ours(args, rank, world, local):
     elapsed_max = reduce_max(elapsed, world)
     awq.device_status()
 
-    # end to end through the public API: pinned host x in, y read back, every step
-    host = []
-    for t in sets[0]:
-        host.append((t["x"].cpu().pin_memory(), torch.empty_like(t["y"], device="cpu").pin_memory()))
-    h2d = sum(h[0].numel() * 2 for h in host)
-    d2h = sum(h[1].numel() * 2 for h in host)
-    xs = [[torch.empty_like(t["x"]) for t in s] for s in sets]
+    # end to end through the public API: every step copies the step's activations (the three
+    # linears' x, staged in one pinned buffer) to the device in one copy, runs the three
+    # calls, and reads the three outputs back in one copy
+    xsz = [t["x"].numel() for t in sets[0]]
+    ysz = [t["y"].numel() for t in sets[0]]
+    hx_all = torch.cat([t["x"].reshape(-1).cpu() for t in sets[0]]).pin_memory()
+    hy_all = torch.empty(sum(ysz), dtype=torch.float16).pin_memory()
+    xd_all = torch.empty(sum(xsz), dtype=torch.float16, device="cuda")
+    yd_all = torch.empty(sum(ysz), dtype=torch.float16, device="cuda")
+    xd = [v.view(t["x"].shape) for v, t in zip(torch.split(xd_all, xsz), sets[0])]
+    yd = [v.view(t["y"].shape) for v, t in zip(torch.split(yd_all, ysz), sets[0])]
+    h2d = hx_all.numel() * 2
+    d2h = hy_all.numel() * 2
 
     def e2e_step(r):
-        for (hx, hy), t, xd in zip(host, sets[r], xs[r]):
-            xd.copy_(hx, non_blocking=True)
-            awq.awq_gemm(xd, t["qweight"], t["qzeros"], t["scales"], t["bias"],
-                         group_size=t["G"], out=t["y"])
-            hy.copy_(t["y"], non_blocking=True)
+        xd_all.copy_(hx_all, non_blocking=True)
+        for t, xv, yv in zip(sets[r], xd, yd):
+            awq.awq_gemm(xv, t["qweight"], t["qzeros"], t["scales"], t["bias"],
+                         group_size=t["G"], out=yv, stream=stream)
+        hy_all.copy_(yd_all, non_blocking=True)
         stream.synchronize()
 
     e2e_steps = min(args.steps, 2000)

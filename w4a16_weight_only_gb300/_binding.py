@@ -84,7 +84,7 @@ def _check(status: int):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
@@ -93,15 +93,25 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _cuda_index(t, name):
+    d = t.get_device()
+    if d < 0:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return d
+
+
 def _need(t, name, dtype, shape, device):
-    if t.dtype != dtype:
+    """Cheap per-call checks (this runs on every call): dtype, exact shape, row-major
+    layout, and the same CUDA device as the first operand (a host tensor's address must
+    never reach a kernel)."""
+    if t.dtype is not dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous (row-major)")
-    if t.numel() and t.device != device:
-        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.get_device() != device and t.numel():
+        raise ValueError(f"{name} is on {t.device}, expected device {device}")
 
 
 def _groups(K, group_size):
@@ -124,7 +134,7 @@ def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, pa
     x2 = x.reshape(-1, K)
     M = x2.shape[0]
     N = qweight.shape[1] * 8
-    dev = x.device
+    dev = _cuda_index(x, "x")
     dt = x.dtype if x.dtype in (torch.float16, torch.bfloat16) else torch.float16
     _need(x2, "x", dt, (M, K), dev)
     _need(qweight, "qweight", torch.int32, (K, N // 8), dev)
@@ -154,7 +164,7 @@ def awq_gemm_grouped(x, qweight, qzeros, scales, offsets, bias=None, group_size=
     R, K = x.shape
     E, _, C = qweight.shape
     N = 8 * C
-    dev = x.device
+    dev = _cuda_index(x, "x")
     _need(x, "x", torch.float16, (R, K), dev)
     _need(qweight, "qweight", torch.int32, (E, K, C), dev)
     ng = _groups(K, group_size)
@@ -180,7 +190,7 @@ def awq_dequant(qweight, qzeros, scales, group_size=128, out_dtype=torch.float16
     lib = load_library()
     K, C = qweight.shape
     N = 8 * C
-    dev = qweight.device
+    dev = _cuda_index(qweight, "qweight")
     _need(qweight, "qweight", torch.int32, (K, C), dev)
     ng = _groups(K, group_size)
     _need(qzeros, "qzeros", torch.int32, (ng, C), dev)
@@ -214,7 +224,7 @@ def awq_quantize_rtn(w, group_size=128, sym=False, out=None, stream=None):
     `out` (a tuple of those three tensors) when given."""
     lib = load_library()
     N, K = w.shape
-    dev = w.device
+    dev = _cuda_index(w, "w")
     _need(w, "w", torch.float16, (N, K), dev)
     ng = _groups(K, group_size)
     if out is None:
