@@ -51,6 +51,13 @@ What it computes, and where each step comes from:
   ``offsets[e] .. offsets[e+1]-1`` of ``x`` (routed rows sorted by expert) go
   through expert ``e``'s AWQ linear, each as :func:`gemm` defines it.
 
+* 8-bit weights (GPTQModel wiki "AWQ", "Saved formats and packing": widths
+  other than 4 pack as a continuous little-endian bit stream, and the INT4
+  order is not applied): column ``4*c + i`` of a row is byte ``i`` of word
+  ``c`` (:func:`unpack_codes8`); qweight ``[K, N/4]``, qzeros ``[K/G, N/4]``,
+  scales ``[K/G, N]``; ``w = (code - zero) * scale`` as for 4 bits
+  (:func:`dequant8_f32`, :func:`gemm8`).
+
 Pins (tests/test_oracle.py, run without a GPU): ORDER and its inverse from
 the wiki's "Saved formats and packing" section, a hand-packed word, AWQ-004
 (sequential-nibble decode differs), AWQ-005 (zero equal to code gives an
@@ -283,5 +290,52 @@ def gemm_grouped(x, qweight, qzeros, scales, bias, group_size, offsets) -> np.nd
         if b > a:
             y[a:b] = gemm(np.asarray(x)[a:b], qweight[e], qzeros[e], scales[e],
                           None if bias is None else bias[e], group_size)
+    return y
+
+
+def unpack_codes8(packed: np.ndarray) -> np.ndarray:
+    """[R, C] int32 words -> [R, 4C] 8-bit codes: column 4c + i is byte i of word c
+    (little-endian bit stream of 8-bit codes)."""
+    u = np.ascontiguousarray(packed).view(np.uint32).astype(np.uint64)
+    R, C = u.shape
+    out = np.empty((R, 4 * C), dtype=np.int64)
+    for i in range(4):
+        out[:, i::4] = ((u >> np.uint64(8 * i)) & np.uint64(0xFF)).astype(np.int64)
+    return out
+
+
+def pack_codes8(codes: np.ndarray) -> np.ndarray:
+    """Inverse of :func:`unpack_codes8`: [R, 4C] codes 0..255 -> [R, C] int32."""
+    codes = np.asarray(codes)
+    R, N = codes.shape
+    if N % 4 != 0:
+        raise ValueError("8-bit packing needs a width divisible by 4")
+    if codes.min(initial=0) < 0 or codes.max(initial=0) > 255:
+        raise ValueError("codes must lie in 0..255")
+    c = codes.astype(np.uint64)
+    word = np.zeros((R, N // 4), dtype=np.uint64)
+    for i in range(4):
+        word |= c[:, i::4] << np.uint64(8 * i)
+    return word.astype(np.uint32).view(np.int32)
+
+
+def dequant8_f32(qweight, qzeros, scales, group_size) -> np.ndarray:
+    """8-bit W[k, n] = (code[k, n] - zero[k // G, n]) * scale[k // G, n], fp32, [K, N]
+    (exact: a 9-bit integer times an 11-bit significand)."""
+    K = np.asarray(qweight).shape[0]
+    G = resolve_group_size(K, group_size)
+    codes = unpack_codes8(qweight).astype(np.float32)
+    zeros = unpack_codes8(qzeros).astype(np.float32)
+    sc = np.asarray(scales).astype(np.float32)
+    g_of_k = np.arange(K) // G
+    return ((codes - zeros[g_of_k]) * sc[g_of_k]).astype(np.float32)
+
+
+def gemm8(x, qweight, qzeros, scales, bias, group_size) -> np.ndarray:
+    """y = x @ W8 (+ bias) in fp64 with the 8-bit dequant."""
+    W = dequant8_f32(qweight, qzeros, scales, group_size).astype(np.float64)
+    y = np.asarray(x).astype(np.float64) @ W
+    if bias is not None:
+        y = y + np.asarray(bias).astype(np.float64)[None, :]
     return y
 

@@ -31,7 +31,7 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["awq_linear", "seed_for", "SYM_ZERO_WORD", "moe_inputs"]
+__all__ = ["awq_linear", "seed_for", "SYM_ZERO_WORD", "moe_inputs", "awq8_linear"]
 
 # Every nibble equal to 8.  A word with all nibbles equal is invariant under
 # any nibble permutation, so no ordering knowledge is needed to write it.
@@ -191,4 +191,31 @@ def moe_inputs(seed: int, T: int, topk: int, E: int, K: int, N: int, group_size:
             "bias": np.ascontiguousarray(np.stack([d["bias"] for d in ex])) if bias else None,
             "offsets": offsets, "token_of_row": token_of_row, "group_size": int(group_size),
             "R": int(T * topk), "E": E, "K": K, "N": N}
+
+
+def awq8_linear(seed: int, M: int, K: int, N: int, group_size: int = 128, bias: bool = False,
+                x_kind: str = "normal", scale_kind: str = "uniform") -> dict:
+    """8-bit variant of awq_linear: qweight int32 [K, N/4] and qzeros int32 [K/G, N/4] are
+    uniform 32-bit words (four independent uniform 8-bit codes each, whatever byte order
+    a reader applies); x, scales, bias drawn as for 4 bits (scales uniform [1e-4, 1e-3):
+    codes span 256 levels)."""
+    if N % 4 != 0:
+        raise ValueError("N must be a multiple of 4 (four codes per int32 word)")
+    n_groups = _groups(K, group_size)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if x_kind == "normal":
+        x = rng.standard_normal((M, K), dtype=np.float32).astype(np.float16)
+    else:
+        x = rng.integers(-4, 5, size=(M, K)).astype(np.float16)
+    qweight = rng.integers(0, 1 << 32, size=(K, N // 4), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    qzeros = rng.integers(0, 1 << 32, size=(n_groups, N // 4), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    if scale_kind == "uniform":
+        scales = rng.uniform(1e-4, 1e-3, size=(n_groups, N)).astype(np.float32).astype(np.float16)
+    else:
+        p = rng.integers(8, 14, size=(n_groups, N))
+        scales = np.ldexp(np.ones((n_groups, N), np.float32), -p).astype(np.float16)
+    b = rng.normal(0.0, 0.02, size=N).astype(np.float32).astype(np.float16) if bias else None
+    return {"x": np.ascontiguousarray(x), "qweight": np.ascontiguousarray(qweight),
+            "qzeros": np.ascontiguousarray(qzeros), "scales": np.ascontiguousarray(scales),
+            "bias": b, "group_size": int(group_size), "M": M, "K": K, "N": N, "bits": 8}
 

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
+import synth
 from synth import awq_linear, SYM_ZERO_WORD
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "awq_word_layout.txt")
@@ -465,3 +466,50 @@ def test_grouped_rejects_bad_offsets():
     d = moe_inputs(54, 4, 1, 2, 64, 16, group_size=32)
     with pytest.raises(ValueError):
         oracle.gemm_grouped(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 32, [0, 3, 2])
+
+
+# ---------------------------------------------------------------- 8-bit ----
+# GPTQModel wiki "AWQ", "Saved formats and packing": widths other than 4 pack as a continuous
+# little-endian bit stream (no INT4 order).  Worked by hand: columns 0..3 holding codes
+# 0x01, 0x02, 0x03, 0x04 make the word 0x04030201; column 3 = 0xFF makes the sign byte.
+
+def test_w8_hand_packed_words():
+    w = np.array([[0x04030201, 0xFF000000]], dtype=np.uint32).view(np.int32)
+    assert oracle.unpack_codes8(w).tolist() == [[1, 2, 3, 4, 0, 0, 0, 255]]
+    assert np.array_equal(oracle.pack_codes8(np.array([[1, 2, 3, 4, 0, 0, 0, 255]])), w)
+
+
+def test_w8_round_trip_and_rejects():
+    rng = np.random.default_rng(61)
+    words = rng.integers(0, 1 << 32, size=(5, 6), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    assert np.array_equal(oracle.pack_codes8(oracle.unpack_codes8(words)), words)
+    with pytest.raises(ValueError):
+        oracle.pack_codes8(np.zeros((1, 6), np.int64))
+    with pytest.raises(ValueError):
+        oracle.pack_codes8(np.full((1, 4), 256))
+
+
+def test_w8_dequant_exact_values_and_zero_point():
+    # code == zero gives exactly 0 (no +1, as for 4 bits); code 255 - zero 0 times scale
+    codes = np.array([[7, 255, 0, 128]] * 4)
+    zeros = np.array([[7, 0, 0, 200]])
+    scales = np.array([[0.5, 2.0 ** -10, 3.0, 0.25]], dtype=np.float16)
+    W = oracle.dequant8_f32(oracle.pack_codes8(codes), oracle.pack_codes8(zeros), scales, 4)
+    assert W[0].tolist() == [0.0, 255 * 2.0 ** -10, 0.0, (128 - 200) * 0.25]
+
+
+def test_w8_gemm_brute_force():
+    d = synth.awq8_linear(62, 3, 32, 8, group_size=16, bias=True)
+    y = oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 16)
+    K, N = 32, 8
+    for m in range(3):
+        for n in range(N):
+            terms = []
+            for k in range(K):
+                word = int(d["qweight"][k, n // 4]) & 0xFFFFFFFF
+                zword = int(d["qzeros"][k // 16, n // 4]) & 0xFFFFFFFF
+                code = (word >> (8 * (n % 4))) & 0xFF
+                zero = (zword >> (8 * (n % 4))) & 0xFF
+                terms.append(float(d["x"][m, k]) * ((code - zero) * float(d["scales"][k // 16, n])))
+            terms.append(float(d["bias"][n]))
+            assert abs(y[m, n] - math.fsum(terms)) <= 1e-12 * max(1.0, abs(y[m, n]))
