@@ -122,6 +122,29 @@ awq_status_t awq_dequant_bf16(const int32_t* qweight, const int32_t* qzeros, con
                               awq_dtype_t out_dtype, awq_stream_t stream);
 
 /*
+ * 8-bit weights in the GEMM layout (GPTQModel wiki "AWQ", "Saved formats and packing":
+ * widths other than 4 pack as a continuous little-endian bit stream, without the INT4
+ * order; Marlin-class kernels take 8 bits, "Selection and compatibility").  Column 4c + i of
+ * a row is byte i of word c:
+ *
+ *   qweight int32 [K, N/4], qzeros int32 [K/G, N/4], scales fp16 [K/G, N]
+ *   w[k][n] = (code[k][n] - zero[k/G][n]) * scale[k/G][n],  codes 0..255
+ *
+ * awq_gemm_w8 / awq_gemm_w8_ex: the awq_gemm contract with 8-bit weights (N % 4 == 0);
+ * awq_dequant_w8: the awq_dequant contract (exact fp32, or one rounding to fp16).
+ */
+awq_status_t awq_gemm_w8_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                            const void* scales_f16, const void* bias_f16, int64_t M, int64_t K,
+                            int64_t N, int64_t group_size, void* y_f16, awq_path_t path,
+                            awq_stream_t stream);
+awq_status_t awq_gemm_w8(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                         const void* scales_f16, const void* bias_f16, int64_t M, int64_t K,
+                         int64_t N, int64_t group_size, void* y_f16, awq_stream_t stream);
+awq_status_t awq_dequant_w8(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
+                            int64_t K, int64_t N, int64_t group_size, void* w_out,
+                            awq_dtype_t out_dtype, awq_stream_t stream);
+
+/*
  * awq_gemm_grouped -- grouped (mixture-of-experts) W4A16 linear in one launch (routed expert
  * layers with 4-bit AWQ weights: the vLLM article, section 5.4).  E experts' weights are
  * stacked; the routed rows of x are sorted by expert:

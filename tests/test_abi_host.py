@@ -168,3 +168,21 @@ def test_grouped_argument_checks_are_host_side(lib):
     assert g(A, A, A, A, None, A, 8, 2, 96, 256, 32, B, None) == SHAPE           # outside the TMA contract
     assert g(None, None, None, None, None, None, 0, 2, 256, 256, 128, None, None) == 0  # R == 0
 
+
+
+def test_w8_argument_checks_are_host_side(lib):
+    import torch
+    g = lib.awq_gemm_w8_ex
+    # (x, qweight, qzeros, scales, bias, M, K, N, G, y, path, stream)
+    assert g(A, A, A, A, None, 1, 256, 6, 128, B, 0, None) == SHAPE      # N % 4
+    assert g(A, A, A, A, None, 1, 256, 12, 96, B, 0, None) == SHAPE     # K % G
+    assert g(None, A, A, A, None, 1, 256, 12, 128, B, 0, None) == INVALID
+    assert g(A, A, A, A, None, 1, 256, 12, 128, B, 9, None) == INVALID  # bad path
+    assert g(A, A, A, A, None, 0, 256, 12, 128, B, 0, None) == 0        # M == 0: no launch
+    d = lib.awq_dequant_w8
+    assert d(A, A, A, 256, 6, 128, B, 0, None) == SHAPE
+    assert d(A, A, A, 256, 12, 128, B, 5, None) == INVALID               # bad dtype
+    assert d(A, A, A, 256, 0, 128, B, 0, None) == 0
+    if not torch.cuda.is_available():
+        assert g(A, A, A, A, None, 1, 256, 12, 128, B, 0, None) == DEVICE
+        assert d(A, A, A, 256, 12, 128, B, 0, None) == DEVICE

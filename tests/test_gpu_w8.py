@@ -1,0 +1,111 @@
+"""GPU parity of the 8-bit entry points (awq_dequant_w8, awq_gemm_w8; AutoAWQ's
+"w_bit" knob on the format page: 8-bit codes packed four to an int32 word) against the
+CPU oracle on the same seeded inputs.  Dequant must be bit-exact (fp32: the exact
+product; fp16: that product rounded once to nearest-even).  The GEMM is held to the fp16
+path's bar, |y - y_ref| <= 1e-2 * max(1, |y_ref|), and must be bit-exact where every
+product and partial sum is exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def awq():
+    from w4a16_weight_only_gb300 import build
+    build.build()
+    import w4a16_weight_only_gb300 as awq
+    assert awq.runtime_available(), awq.last_error()
+    return awq
+
+
+def to_dev(d):
+    t = {k: torch.from_numpy(np.ascontiguousarray(d[k])).cuda()
+         for k in ("x", "qweight", "qzeros", "scales")}
+    t["bias"] = None if d["bias"] is None else torch.from_numpy(d["bias"]).cuda()
+    return t
+
+
+def run(awq, d, path="auto"):
+    t = to_dev(d)
+    y = awq.awq_gemm_w8(t["x"], t["qweight"], t["qzeros"], t["scales"], t["bias"],
+                        group_size=d["group_size"], path=path)
+    torch.cuda.synchronize()
+    assert y.dtype == torch.float16
+    return y.cpu().numpy()
+
+
+def assert_close(y, y_ref, what):
+    err = np.abs(y.astype(np.float64) - y_ref)
+    tol = REL_TOL * np.maximum(1.0, np.abs(y_ref))
+    assert np.isfinite(y).all(), what
+    worst = float((err / tol).max()) if err.size else 0.0
+    assert worst <= 1.0, f"{what}: worst |err|/(1e-2*max(1,|ref|)) = {worst:.3f}"
+
+
+@pytest.mark.parametrize("K,N,G", [(256, 256, 128), (48, 12, 16), (4096, 4096, 128), (64, 4, -1),
+                                   (1000, 36, 8)])
+def test_dequant_w8_bit_exact(awq, K, N, G):
+    d = synth.awq8_linear(12000 + K + N, 1, K, N, group_size=G)
+    t = to_dev(d)
+    w16 = awq.awq_dequant_w8(t["qweight"], t["qzeros"], t["scales"], group_size=G)
+    w32 = awq.awq_dequant_w8(t["qweight"], t["qzeros"], t["scales"], group_size=G,
+                             out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref = oracle.dequant8_f32(d["qweight"], d["qzeros"], d["scales"], G)
+    assert np.array_equal(w32.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert np.array_equal(w16.cpu().numpy().view(np.uint16), ref.astype(np.float16).view(np.uint16))
+
+
+SMALL = [(1, 256, 256, 128, False), (3, 512, 192, 64, True), (8, 1024, 512, 128, True),
+         (17, 2048, 1024, 256, True), (32, 4096, 128, -1, False), (33, 256, 60, 16, True),
+         (100, 512, 132, 64, False), (300, 1024, 256, 128, True), (1, 64, 4, -1, False)]
+
+
+@pytest.mark.parametrize("M,K,N,G,bias", SMALL)
+@pytest.mark.parametrize("path", ["auto", "generic"])
+def test_gemm_w8_small_vs_oracle(awq, M, K, N, G, bias, path):
+    d = synth.awq8_linear(13000 + M + K + N, M, K, N, group_size=G, bias=bias)
+    y = run(awq, d, path)
+    y_ref = oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    assert_close(y, y_ref, f"w8 {path} M={M} K={K} N={N} G={G}")
+
+
+@pytest.mark.parametrize("M", [1, 16, 300])
+def test_gemm_w8_exact_case_bitwise(awq, M):
+    # x small integers, power-of-two scales, K = 256: |partial sums| <= 256 * 4 * 255 * 2^-8
+    # on a 2^-13 grid (23 bits), so fp32 accumulation is exact on any order and y must be
+    # the oracle's value rounded once to fp16
+    d = synth.awq8_linear(13500 + M, M, 256, 384, group_size=64, x_kind="smallint",
+                          scale_kind="pow2")
+    y = run(awq, d)
+    y_ref = oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 64)
+    assert np.array_equal(y.view(np.uint16), y_ref.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 11008), (64, 11008, 4096)])
+def test_gemm_w8_workload_shapes(awq, M, K, N):
+    d = synth.awq8_linear(13700 + M + K, M, K, N, group_size=128, bias=True)
+    y = run(awq, d)
+    assert_close(y, oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128),
+                 f"w8 M={M} K={K} N={N}")
+
+
+def test_gemm_w8_deterministic(awq):
+    d = synth.awq8_linear(13900, 24, 4096, 1024, group_size=128, bias=True)
+    a, b = run(awq, d), run(awq, d)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_gemm_w8_refuses_4bit_kernels(awq):
+    # the 4-bit tensor-core kernels decode nibbles; forcing them on 8-bit codes is an error
+    d = synth.awq8_linear(13950, 4, 256, 256, group_size=128)
+    for path in ("decode", "prefill"):
+        with pytest.raises(Exception):
+            run(awq, d, path)

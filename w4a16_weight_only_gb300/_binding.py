@@ -37,6 +37,9 @@ SIGNATURES = {
     "awq_gemm_bf16_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp]),
     "awq_dequant_bf16": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp]),
     "awq_gemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "awq_gemm_w8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "awq_gemm_w8_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "awq_dequant_w8": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp]),
 }
 
 _lib = None
@@ -152,6 +155,53 @@ def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, pa
             M, K, N, group_size, _ptr(out), PATHS[path], _stream(stream))
     _check(st)
     return out.reshape(*lead, N)
+
+
+def awq_gemm_w8(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, path="auto",
+                stream=None):
+    """y = x @ dequant8(qweight, qzeros, scales) (+ bias) via awq_gemm_w8: 8-bit codes,
+    qweight int32 [K, N/4], qzeros int32 [K/G, N/4], scales fp16 [K/G, N]; x fp16 [M, K]."""
+    lib = load_library()
+    lead = x.shape[:-1]
+    K = x.shape[-1]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    N = qweight.shape[1] * 4
+    dev = _cuda_index(x, "x")
+    _need(x2, "x", torch.float16, (M, K), dev)
+    _need(qweight, "qweight", torch.int32, (K, N // 4), dev)
+    ng = _groups(K, group_size)
+    _need(qzeros, "qzeros", torch.int32, (ng, N // 4), dev)
+    _need(scales, "scales", torch.float16, (ng, N), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.float16, (N,), dev)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    else:
+        _need(out, "out", torch.float16, (M, N), dev)
+    st = lib.awq_gemm_w8_ex(_ptr(x2), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
+                            M, K, N, group_size, _ptr(out), PATHS[path], _stream(stream))
+    _check(st)
+    return out.reshape(*lead, N)
+
+
+def awq_dequant_w8(qweight, qzeros, scales, group_size=128, out_dtype=torch.float16, stream=None):
+    """Dense W [K, N] from 8-bit codes via awq_dequant_w8 (fp16 or fp32)."""
+    lib = load_library()
+    K, C = qweight.shape
+    N = 4 * C
+    dev = _cuda_index(qweight, "qweight")
+    _need(qweight, "qweight", torch.int32, (K, C), dev)
+    ng = _groups(K, group_size)
+    _need(qzeros, "qzeros", torch.int32, (ng, C), dev)
+    _need(scales, "scales", torch.float16, (ng, N), dev)
+    if out_dtype not in (torch.float16, torch.float32):
+        raise TypeError("out_dtype must be torch.float16 or torch.float32")
+    out = torch.empty((K, N), dtype=out_dtype, device=dev)
+    st = lib.awq_dequant_w8(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size, _ptr(out),
+                            DTYPE_F32 if out_dtype == torch.float32 else DTYPE_F16, _stream(stream))
+    _check(st)
+    return out
 
 
 def awq_gemm_grouped(x, qweight, qzeros, scales, offsets, bias=None, group_size=128, out=None,

@@ -35,7 +35,8 @@ constexpr int64_t kDimLimit = (int64_t{1} << 31) - 1;
 constexpr int64_t kProdLimit = int64_t{1} << 40;
 
 // Shape rules shared by awq_dequant and awq_gemm.  Returns AWQ_OK and the resolved G.
-awq_status_t check_weight_shape(int64_t K, int64_t N, int64_t group_size, int* G_out) {
+awq_status_t check_weight_shape(int64_t K, int64_t N, int64_t group_size, int* G_out,
+                                int per_word = 8) {
   if (K <= 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "K must be positive (got %lld)", (long long)K);
   if (N < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "N must be >= 0 (got %lld)", (long long)N);
   if (group_size == 0 || group_size < -1)
@@ -44,9 +45,9 @@ awq_status_t check_weight_shape(int64_t K, int64_t N, int64_t group_size, int* G
   if (K > kDimLimit || N > kDimLimit)
     return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "K and N must be below 2^31");
   if (K * N >= kProdLimit) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "K*N must be below 2^40");
-  if (N % 8 != 0)
-    return fail(AWQ_ERR_UNSUPPORTED_SHAPE,
-                "N=%lld is not a multiple of 8 (eight 4-bit codes per int32 word)", (long long)N);
+  if (N % per_word != 0)
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "N=%lld is not a multiple of %d (codes per int32 word)",
+                (long long)N, per_word);
   const int64_t G = group_size == -1 ? K : group_size;
   if (K % G != 0)
     return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "K=%lld is not a multiple of group_size=%lld",
@@ -76,10 +77,10 @@ bool al(const void* p, uintptr_t a) { return awq::aligned(p, a); }
 awq_status_t build_problem(const void* x, const int32_t* qweight, const int32_t* qzeros,
                            const void* scales, const void* bias, int64_t M, int64_t K, int64_t N,
                            int64_t group_size, void* y, awq_stream_t stream, awq::GemmProblem* p,
-                           bool* empty, bool bf16 = false) {
+                           bool* empty, bool bf16 = false, int bits = 4) {
   if (M < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "M must be >= 0 (got %lld)", (long long)M);
   int G = 0;
-  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  awq_status_t st = check_weight_shape(K, N, group_size, &G, bits == 8 ? 4 : 8);
   if (st != AWQ_OK) return st;
   if (M > kDimLimit) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "M must be below 2^31");
   if (M * N >= kProdLimit || M * K >= kProdLimit)
@@ -104,6 +105,7 @@ awq_status_t build_problem(const void* x, const int32_t* qweight, const int32_t*
   p->G = G;
   p->stream = reinterpret_cast<cudaStream_t>(stream);
   p->bf16 = bf16;
+  p->bits = bits;
   return AWQ_OK;
 }
 
@@ -219,13 +221,14 @@ awq_status_t awq_quantize_rtn(const void* w_f16, int64_t N, int64_t K, int64_t g
 
 static awq_status_t gemm_any(const void* x, const int32_t* qweight, const int32_t* qzeros,
                       const void* scales, const void* bias, int64_t M, int64_t K, int64_t N,
-                      int64_t group_size, void* y, awq_path_t path, awq_stream_t stream, bool bf16) {
+                      int64_t group_size, void* y, awq_path_t path, awq_stream_t stream, bool bf16,
+                      int bits = 4) {
   if (path < AWQ_PATH_AUTO || path > AWQ_PATH_GENERIC)
     return fail(AWQ_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
   awq::GemmProblem p{};
   bool empty = false;
   awq_status_t st = build_problem(x, qweight, qzeros, scales, bias, M, K, N, group_size, y,
-                                  stream, &p, &empty, bf16);
+                                  stream, &p, &empty, bf16, bits);
   if (st != AWQ_OK) return st;
   if (empty) return ok();
   st = check_device();
@@ -273,6 +276,45 @@ awq_status_t awq_gemm_grouped(const void* x_f16, const int32_t* qweight, const i
   if (st != AWQ_OK) return st;
   const cudaError_t e = awq::launch_decode_grouped(p);
   if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_grouped launch");
+  return ok();
+}
+
+awq_status_t awq_gemm_w8_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                            const void* scales_f16, const void* bias_f16, int64_t M, int64_t K,
+                            int64_t N, int64_t group_size, void* y_f16, awq_path_t path,
+                            awq_stream_t stream) {
+  return gemm_any(x_f16, qweight, qzeros, scales_f16, bias_f16, M, K, N, group_size, y_f16, path,
+                  stream, false, 8);
+}
+
+awq_status_t awq_gemm_w8(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
+                         const void* scales_f16, const void* bias_f16, int64_t M, int64_t K,
+                         int64_t N, int64_t group_size, void* y_f16, awq_stream_t stream) {
+  return gemm_any(x_f16, qweight, qzeros, scales_f16, bias_f16, M, K, N, group_size, y_f16,
+                  AWQ_PATH_AUTO, stream, false, 8);
+}
+
+awq_status_t awq_dequant_w8(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
+                            int64_t K, int64_t N, int64_t group_size, void* w_out,
+                            awq_dtype_t out_dtype, awq_stream_t stream) {
+  int G = 0;
+  awq_status_t st = check_weight_shape(K, N, group_size, &G, 4);
+  if (st != AWQ_OK) return st;
+  if (out_dtype != AWQ_DTYPE_F16 && out_dtype != AWQ_DTYPE_F32)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "out_dtype must be AWQ_DTYPE_F16 or AWQ_DTYPE_F32");
+  if (N == 0) return ok();
+  if (!qweight || !qzeros || !scales_f16 || !w_out)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "null pointer among qweight, qzeros, scales, w_out");
+  if (!al(qweight, 4) || !al(qzeros, 4)) return fail(AWQ_ERR_MISALIGNED, "qweight/qzeros must be 4-byte aligned");
+  if (!al(scales_f16, 2)) return fail(AWQ_ERR_MISALIGNED, "scales must be 2-byte aligned");
+  if (!al(w_out, out_dtype == AWQ_DTYPE_F32 ? 4 : 2)) return fail(AWQ_ERR_MISALIGNED, "w_out misaligned for its dtype");
+  st = check_device();
+  if (st != AWQ_OK) return st;
+  const cudaError_t e = awq::launch_dequant8(
+      reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
+      static_cast<const __half*>(scales_f16), static_cast<int>(K), static_cast<int>(N), G, w_out,
+      out_dtype == AWQ_DTYPE_F32, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "awq_dequant_w8 launch");
   return ok();
 }
 

@@ -440,6 +440,7 @@ bool make_plan(const GemmProblem& p, Plan* plan, const char** why) {
 bool decode_ldg_supported(const GemmProblem& p, const char** why) {
   static const char* dummy;
   if (!why) why = &dummy;
+  if (p.bits != 4) { *why = "4-bit codes only"; return false; }
   if (p.K % 16 != 0) { *why = "decode needs K % 16 == 0"; return false; }
   if (p.G % 16 != 0) { *why = "decode needs group_size % 16 == 0"; return false; }
   const Variant v = pick_variant(p);

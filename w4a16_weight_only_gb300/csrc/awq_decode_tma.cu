@@ -981,6 +981,7 @@ cudaError_t launch_v(const GemmProblem& p) {
 bool decode_tma_supported(const GemmProblem& p, const char** why) {
   static const char* dummy;
   if (!why) why = &dummy;
+  if (p.bits != 4) { *why = "4-bit codes only"; return false; }
   if (p.K % kRS != 0) { *why = "TMA decode needs K % 64 == 0"; return false; }
   if (p.G % kRS != 0) { *why = "TMA decode needs group_size % 64 == 0"; return false; }
   if (p.N % 32 != 0) { *why = "TMA decode needs N % 32 == 0"; return false; }

@@ -66,6 +66,35 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict
   }
 }
 
+// 8-bit codes: one thread per packed word (4 output columns, byte i = column 4c + i); the
+// fp32 value (code - zero) * scale is exact (a 9-bit integer times an 11-bit significand).
+template <bool kF32>
+__global__ void __launch_bounds__(256) dequant8_kernel(const uint32_t* __restrict__ qw,
+                                                       const uint32_t* __restrict__ qz,
+                                                       const __half* __restrict__ sc, int K, int C,
+                                                       int G, void* __restrict__ out) {
+  const long long total = (long long)K * C;
+  const long long N = 4LL * C;
+  for (long long w = blockIdx.x * (long long)blockDim.x + threadIdx.x; w < total;
+       w += (long long)gridDim.x * blockDim.x) {
+    const int k = (int)(w / C);
+    const int cw = (int)(w - (long long)k * C);
+    const int g = k / G;
+    const uint32_t q = __ldcs(qw + w);
+    const uint32_t z = __ldg(qz + (long long)g * C + cw);
+    const __half* srow = sc + (long long)g * N + 4LL * cw;
+    const long long o = (long long)k * N + 4LL * cw;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int code = (int)((q >> (8 * i)) & 0xFFu);
+      const int zero = (int)((z >> (8 * i)) & 0xFFu);
+      const float v = __fmul_rn((float)(code - zero), __half2float(srow[i]));
+      if (kF32) static_cast<float*>(out)[o + i] = v;
+      else static_cast<__half*>(out)[o + i] = __float2half_rn(v);
+    }
+  }
+}
+
 // Generic fused GEMM: one thread per output column, kMT activation rows per block row,
 // activations staged through shared memory in kKT-wide slices.  fp32 accumulation in
 // increasing k order.  Used for shapes the fast kernels do not take (K or G not a
@@ -73,17 +102,19 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t* __restrict
 constexpr int kMT = 8;
 constexpr int kKT = 64;
 
-template <bool kBF>
+template <bool kBF, int kBits>
 __global__ void __launch_bounds__(128) generic_gemm_kernel(GemmProblem p) {
   const uint16_t* x16 = reinterpret_cast<const uint16_t*>(p.x);
   const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.sc);
   __shared__ float xs[kMT][kKT];
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  const int C = p.N >> 3;
+  const int C = kBits == 4 ? p.N >> 3 : p.N >> 2;
   const bool active = n < p.N;
-  const int cw = n >> 3;
+  const int cw = kBits == 4 ? n >> 3 : n >> 2;
   const int j = n & 7;
-  const int nib = ((j & 1) << 2) | (j >> 1);  // nibble holding column j (inverse of ORDER)
+  // bit offset of column n in its word: nibble holding column j (inverse of ORDER), or byte n % 4
+  const int shift = kBits == 4 ? 4 * (((j & 1) << 2) | (j >> 1)) : 8 * (n & 3);
+  const uint32_t mask = kBits == 4 ? 0xFu : 0xFFu;
   for (int m0 = blockIdx.y * kMT; m0 < p.M; m0 += gridDim.y * kMT) {
   float acc[kMT];
 #pragma unroll
@@ -103,8 +134,8 @@ __global__ void __launch_bounds__(128) generic_gemm_kernel(GemmProblem p) {
         const int g = k / p.G;
         const uint32_t q = p.qw[(long long)k * C + cw];
         const uint32_t z = p.qz[(long long)g * C + cw];
-        const int code = (int)((q >> (4 * nib)) & 0xFu);
-        const int zero = (int)((z >> (4 * nib)) & 0xFu);
+        const int code = (int)((q >> shift) & mask);
+        const int zero = (int)((z >> shift) & mask);
         const float w = __fmul_rn((float)(code - zero), elem_to_float<kBF>(sc16[(long long)g * p.N + n]));
 #pragma unroll
         for (int m = 0; m < kMT; ++m) acc[m] = __fmaf_rn(xs[m][kk], w, acc[m]);
@@ -150,6 +181,18 @@ cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const __half*
   return cudaGetLastError();
 }
 
+cudaError_t launch_dequant8(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
+                            int G, void* out, bool out_f32, cudaStream_t stream) {
+  const int C = N / 4;
+  const long long total = (long long)K * C;
+  if (total == 0) return cudaSuccess;
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (out_f32) dequant8_kernel<true><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+  else dequant8_kernel<false><<<blocks, 256, 0, stream>>>(qw, qz, sc, K, C, G, out);
+  return cudaGetLastError();
+}
+
 cudaError_t probe_kernel_image(cudaFuncAttributes* attr) {
   return cudaFuncGetAttributes(attr, dequant_kernel<false, true, false>);
 }
@@ -157,8 +200,9 @@ cudaError_t probe_kernel_image(cudaFuncAttributes* attr) {
 cudaError_t launch_generic(const GemmProblem& p) {
   const int mtiles = (p.M + kMT - 1) / kMT;
   dim3 grid((p.N + 127) / 128, mtiles < 65535 ? mtiles : 65535);
-  if (p.bf16) generic_gemm_kernel<true><<<grid, 128, 0, p.stream>>>(p);
-  else generic_gemm_kernel<false><<<grid, 128, 0, p.stream>>>(p);
+  if (p.bits == 8) generic_gemm_kernel<false, 8><<<grid, 128, 0, p.stream>>>(p);
+  else if (p.bf16) generic_gemm_kernel<true, 4><<<grid, 128, 0, p.stream>>>(p);
+  else generic_gemm_kernel<false, 4><<<grid, 128, 0, p.stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,9 @@ struct GemmProblem {
   // belong to expert e (device array of E + 1 ints).  E == 0: a plain linear.
   const int* offsets = nullptr;
   int E = 0;
+  // Code width: 4 (ORDER-interleaved nibbles, N/8 words a row) or 8 (little-endian bytes,
+  // N/4 words a row; GPTQModel wiki "AWQ", "Saved formats and packing").
+  int bits = 4;
 };
 
 // Kernel families; values equal awq_path_t.
@@ -34,6 +37,9 @@ enum Path { kAuto = 0, kDecode = 1, kPrefill = 2, kGeneric = 3 };
 // Dequant (awq_dequant).  out_f32 selects fp32 vs fp16 output.
 cudaError_t launch_dequant(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
                            int G, void* out, bool out_f32, cudaStream_t stream, bool bf16 = false);
+// 8-bit codes (awq_dequant_w8): qweight [K, N/4], qzeros [K/G, N/4], fp16 scales.
+cudaError_t launch_dequant8(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
+                            int G, void* out, bool out_f32, cudaStream_t stream);
 
 // Round-to-nearest group quantization (awq_quantize_rtn): w fp16 [N, K] -> qweight
 // [K, N/8], qzeros [K/G, N/8], scales [K/G, N].

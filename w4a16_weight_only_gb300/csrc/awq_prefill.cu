@@ -619,6 +619,7 @@ int pair_capacity() {
 bool prefill_supported(const GemmProblem& p, const char** why) {
   static const char* dummy;
   if (!why) why = &dummy;
+  if (p.bits != 4) { *why = "4-bit codes only"; return false; }
   if (p.K % kBK != 0) { *why = "prefill needs K % 64 == 0"; return false; }
   if (p.G % kBK != 0) { *why = "prefill needs group_size % 64 == 0"; return false; }
   if (p.N % 32 != 0) { *why = "prefill needs N % 32 == 0"; return false; }
