@@ -518,6 +518,56 @@ def run_sweep(args, local):
         run_quantize_sweep(awq, timed, hbm, hbm_kind)
     if not args.case or "moe" in args.case:
         run_grouped_sweep(awq, timed, hbm, hbm_kind)
+    if not args.case or "w8" in args.case:
+        run_w8_sweep(awq, timed, hbm, hbm_kind)
+
+
+def w8_bytes(M, K, N, G, bias):
+    """Bytes an 8-bit linear must move: one byte per code and per zero, fp16 scales, x, y, bias."""
+    ng = K // G
+    return K * N + ng * N + 2 * ng * N + 2 * M * K + 2 * M * N + (2 * N if bias else 0)
+
+
+def run_w8_sweep(awq, timed, hbm, hbm_kind):
+    """awq_gemm_w8 (8-bit codes) on the 7B decode linears, a 16-row batch and a 70B MLP
+    linear: HBM GB/s over CUDA-graph replays of rotating weight copies (together > 3x L2),
+    for the automatic path and for the plain generic kernel."""
+    import torch
+    stream = torch.cuda.Stream()
+    for (M, K, N) in ((1, 4096, 4096), (1, 4096, 11008), (1, 11008, 4096), (16, 4096, 11008),
+                      (1, 8192, 28672)):
+        G = 128
+        d = synth.awq8_linear(5000 + M + K + N, M, K, N, group_size=G, bias=True)
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        x, bias = dev(d["x"]), dev(d["bias"])
+        w = (dev(d["qweight"]), dev(d["qzeros"]), dev(d["scales"]))
+        nbytes = w8_bytes(M, K, N, G, True)
+        R = max(2, min(16, int(3 * L2_BYTES // nbytes) + 1))
+        sets = [w] + [tuple(t.clone() for t in w) for _ in range(R - 1)]
+        y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        line = {"workload": f"w8_m{M}_{K}x{N}", "bits": 8, "M": M, "K": K, "N": N, "group_size": G,
+                "bias": True, "weight_copies": R, "hbm_peak_GB_s": hbm, "hbm_peak": hbm_kind}
+        for path in ("auto", "generic"):
+            calls = max(R, ((240 if path == "auto" else 40) // R) * R)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for i in range(2 * R):
+                    s = sets[i % R]
+                    awq.awq_gemm_w8(x, s[0], s[1], s[2], bias, G, out=y, path=path, stream=stream)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(calls):
+                        s = sets[i % R]
+                        awq.awq_gemm_w8(x, s[0], s[1], s[2], bias, G, out=y, path=path, stream=stream)
+            t = sorted(timed(g.replay, 1) / calls for _ in range(5))[2]
+            awq.device_status()
+            key = "" if path == "auto" else "generic_"
+            line.update({key + "us": t, key + "GB_s": nbytes / t / 1e3,
+                         key + "frac_hbm": nbytes / t / 1e3 / hbm})
+            del g
+        print(json.dumps(line), flush=True)
+        del sets, w, x, y
+        torch.cuda.empty_cache()
 
 
 def run_grouped_sweep(awq, timed, hbm, hbm_kind):

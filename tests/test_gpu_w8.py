@@ -68,44 +68,70 @@ SMALL = [(1, 256, 256, 128, False), (3, 512, 192, 64, True), (8, 1024, 512, 128,
          (100, 512, 132, 64, False), (300, 1024, 256, 128, True), (1, 64, 4, -1, False)]
 
 
+def decode_ok(K, N, G):
+    G = K if G == -1 else G
+    return K % 64 == 0 and G % 64 == 0 and N % 16 == 0
+
+
 @pytest.mark.parametrize("M,K,N,G,bias", SMALL)
-@pytest.mark.parametrize("path", ["auto", "generic"])
+@pytest.mark.parametrize("path", ["auto", "decode", "generic"])
 def test_gemm_w8_small_vs_oracle(awq, M, K, N, G, bias, path):
+    if path == "decode" and not decode_ok(K, N, G):
+        pytest.skip("shape outside the tensor-core kernel's contract")
     d = synth.awq8_linear(13000 + M + K + N, M, K, N, group_size=G, bias=bias)
     y = run(awq, d, path)
     y_ref = oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
     assert_close(y, y_ref, f"w8 {path} M={M} K={K} N={N} G={G}")
 
 
-@pytest.mark.parametrize("M", [1, 16, 300])
-def test_gemm_w8_exact_case_bitwise(awq, M):
+@pytest.mark.parametrize("M", [1, 5, 16, 32, 300])
+@pytest.mark.parametrize("path", ["decode", "generic"])
+def test_gemm_w8_exact_case_bitwise(awq, M, path):
     # x small integers, power-of-two scales, K = 256: |partial sums| <= 256 * 4 * 255 * 2^-8
     # on a 2^-13 grid (23 bits), so fp32 accumulation is exact on any order and y must be
     # the oracle's value rounded once to fp16
     d = synth.awq8_linear(13500 + M, M, 256, 384, group_size=64, x_kind="smallint",
                           scale_kind="pow2")
-    y = run(awq, d)
+    y = run(awq, d, path)
     y_ref = oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 64)
     assert np.array_equal(y.view(np.uint16), y_ref.astype(np.float16).view(np.uint16))
 
 
-@pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 11008), (64, 11008, 4096)])
-def test_gemm_w8_workload_shapes(awq, M, K, N):
-    d = synth.awq8_linear(13700 + M + K, M, K, N, group_size=128, bias=True)
+# the decode kernel's variants at 8 bits: one token with 4- and 8-warp CTAs (long K), one
+# group per row (G = K), 8-row tiles, 16-row tiles, the exact-operand 32-row tiles, a
+# ragged column tile (N = 48: 12 of a tile's 16 words), M past 32 (several row tiles)
+WORK = [(1, 4096, 4096, 128), (1, 11008, 4096, 128), (1, 28672, 1024, 128), (1, 4096, 1024, -1),
+        (4, 4096, 11008, 128), (16, 4096, 11008, 128), (24, 4096, 4096, 128), (32, 11008, 4096, 128),
+        (7, 1024, 48, 64), (1, 1024, 16, 128), (64, 11008, 4096, 128)]
+
+
+@pytest.mark.parametrize("M,K,N,G", WORK)
+def test_gemm_w8_workload_shapes(awq, M, K, N, G):
+    d = synth.awq8_linear(13700 + M + K + N, M, K, N, group_size=G, bias=True)
     y = run(awq, d)
-    assert_close(y, oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128),
-                 f"w8 M={M} K={K} N={N}")
+    assert_close(y, oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G),
+                 f"w8 M={M} K={K} N={N} G={G}")
 
 
-def test_gemm_w8_deterministic(awq):
-    d = synth.awq8_linear(13900, 24, 4096, 1024, group_size=128, bias=True)
+@pytest.mark.parametrize("M", [1, 24])
+def test_gemm_w8_deterministic(awq, M):
+    d = synth.awq8_linear(13900 + M, M, 4096, 1024, group_size=128, bias=True)
     a, b = run(awq, d), run(awq, d)
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
 
 
-def test_gemm_w8_refuses_4bit_kernels(awq):
-    # the 4-bit tensor-core kernels decode nibbles; forcing them on 8-bit codes is an error
+def test_gemm_w8_auto_matches_decode(awq):
+    # small M takes the decode kernel: same bits as forcing it
+    d = synth.awq8_linear(13960, 3, 4096, 4096, group_size=128, bias=True)
+    assert np.array_equal(run(awq, d).view(np.uint16), run(awq, d, "decode").view(np.uint16))
+
+
+def test_gemm_w8_refuses_nibble_kernels(awq):
+    # the tcgen05 prefill kernel decodes nibbles; forcing it on 8-bit codes is an error, and
+    # the decode kernel refuses N % 16 != 0 at 8 bits
     d = synth.awq8_linear(13950, 4, 256, 256, group_size=128)
-    for path in ("decode", "prefill"):
-        with pytest.raises(Exception):
-            run(awq, d, path)
+    with pytest.raises(Exception):
+        run(awq, d, "prefill")
+    d = synth.awq8_linear(13951, 4, 256, 40, group_size=128)
+    with pytest.raises(Exception):
+        run(awq, d, "decode")

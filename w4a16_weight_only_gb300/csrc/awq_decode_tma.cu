@@ -86,17 +86,20 @@ struct __align__(64) TmaDecodeParams {
   int slice;   // floats of the packed partial each owner finishes (multiple of 4)
 };
 
-template <int TB, int CWL, int NW>
+template <int TB, int CWL, int NW, int BITS = 4>
 struct Geo {
+  static_assert(BITS == 4 || BITS == 8, "4- or 8-bit codes");
+  static constexpr int CPW = 32 / BITS;             // columns per packed word
   static constexpr int CW_W = 8 * CWL;              // packed column-words per warp / CTA
+  static constexpr int NCOL = CPW * CW_W;           // output columns per CTA
   static constexpr int W_BYTES = kRS * CW_W * 4;    // packed weight tile per stage
   static constexpr int Z_BYTES = CW_W * 4;
-  static constexpr int S_BYTES = 8 * CW_W * 2;
+  static constexpr int S_BYTES = NCOL * 2;
   static constexpr int META_SLOT = ((128 + S_BYTES + 127) / 128) * 128;  // zeros at 0, scales at 128
   static constexpr uint32_t META_TX = Z_BYTES + S_BYTES;
-  static constexpr int NMMA = 4 * CWL;
+  static constexpr int NMMA = (CPW / 2) * CWL;      // 16-column MMAs per k16-step
   static constexpr int E = NMMA * TB * 4 * 32;      // partial sums per warp
-  static constexpr int PACK = 8 * TB * 8 * CW_W;    // packed partial: tokens x columns
+  static constexpr int PACK = 8 * TB * NCOL;        // packed partial: tokens x columns
   static constexpr int EP = E + E / 128;            // partials per warp, padded
   static constexpr int RED_BYTES = (NW * EP + PACK) * 4;  // reuses the activation+weight rings
 };
@@ -149,16 +152,24 @@ constexpr int kMinBlocks = NW == 8 ? 2 : (TB == 1 ? AWQ_DECODE_MIN_BLOCKS_M8 : A
 // grid-dependency wait (the offsets come from the routing); tiles past the last expert's
 // exit at once (whole clusters share blockIdx.y).  Rows of a tile that belong to the next
 // expert are computed and discarded.
-template <int TB, int CWL, bool kSub, bool kOne, int NW, bool kBF, bool kGrp = false>
+// BITS = 8: four 8-bit codes per word, byte i of word c is column 4c + i (no interleave).
+// A lane's half-word then holds two columns of one K row; the codes enter the MMA as the
+// exact fp16 subnormals c * 2^-24 (both bytes: an 8-bit code fits the 10-bit subnormal
+// significand), or as 1024 + c in the exact-operand variant.  Same tiles, ring, cluster
+// reduction and launch plan as 4 bits, half the output columns per CTA.  fp16 only
+// (128 + c leaves bf16's 8 significant bits for c > 127).
+template <int TB, int CWL, bool kSub, bool kOne, int NW, bool kBF, bool kGrp = false, int BITS = 4>
 __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     decode_tma_kernel(const __grid_constant__ TmaDecodeParams p) {
   static_assert(!kGrp || (TB == 1 && !kOne), "grouped launches use 8-row tiles");
+  static_assert(BITS == 4 || (!kBF && !kGrp), "8-bit codes: fp16, plain launches");
   static_assert(NW == 4 || NW == 8, "4 or 8 warps per CTA");
   constexpr uint32_t kOne2 = kBF ? 0x3F803F80u : kOnes;     // 1.0 in both halves
   constexpr uint32_t kMag = kBF ? 0x43004300u : kMagic;     // 128 (bf16) / 1024 (fp16)
   constexpr float kBias = kBF ? 128.f : 0.f;                 // offset the operand carries
-  using GE = Geo<TB, CWL, NW>;
+  using GE = Geo<TB, CWL, NW, BITS>;
   constexpr int NMMA = GE::NMMA;
+  constexpr int CPW = GE::CPW, NCOL = GE::NCOL;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -216,7 +227,7 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
   // Reduction mbarrier (after all ring barriers): in the cluster's rank-0 CTA it counts
   // the bytes of the partial sums every CTA of the cluster pushes (its own included).
   uint64_t* red_bar = bars + NW * S;
-  const int pack_n = p.x_rows * 8 * GE::CW_W;  // floats of one packed partial
+  const int pack_n = p.x_rows * NCOL;  // floats of one packed partial
   if (lane == 0) {
     prefetch_tmap(&p.tm_w);
     prefetch_tmap(&p.tm_x);
@@ -252,10 +263,10 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
       unsigned char* md = m_ring + (kOne ? iss_grp - g_first : slot) * GE::META_SLOT;
       if constexpr (kGrp) {
         tma_load_3d(md, &p.tm_z, bar, cw0, iss_grp, ex);
-        tma_load_3d(md + 128, &p.tm_s, bar, 8 * cw0, iss_grp, ex);
+        tma_load_3d(md + 128, &p.tm_s, bar, CPW * cw0, iss_grp, ex);
       } else {
         tma_load_2d(md, &p.tm_z, bar, cw0, iss_grp);
-        tma_load_2d(md + 128, &p.tm_s, bar, 8 * cw0, iss_grp);
+        tma_load_2d(md + 128, &p.tm_s, bar, CPW * cw0, iss_grp);
       }
     }
     if (--iss_left == 0) {
@@ -279,7 +290,7 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
       tma_prefetch_l2_2d(&p.tm_w, cw0, j * kRS);
       if (j % spg == 0) {
         tma_prefetch_l2_2d(&p.tm_z, cw0, j / spg);
-        tma_prefetch_l2_2d(&p.tm_s, 8 * cw0, j / spg);
+        tma_prefetch_l2_2d(&p.tm_s, CPW * cw0, j / spg);
       }
     }
 #endif
@@ -326,8 +337,8 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
   // Bias of this CTA's columns, read now (off the critical path) for the epilogue.
   {
     float* bias_s = reinterpret_cast<float*>(smem + p.bias_off);
-    for (int i = threadIdx.x; i < 8 * GE::CW_W; i += NW * 32) {
-      const int n = 8 * cw0 + i;
+    for (int i = threadIdx.x; i < NCOL; i += NW * 32) {
+      const int n = CPW * cw0 + i;
       bias_s[i] = (p.bias != nullptr && n < p.N)
                       ? elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[(long long)ex * p.N + n])
                       : 0.f;
@@ -374,10 +385,24 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     for (int hb = 0; hb < HB; ++hb) {
       const uint32_t wofs = 4u * static_cast<uint32_t>(4 * hb + wq);  // word offset, bytes
       zh[hb] = lds32(mb + wofs) >> (16 * hh);
-      const uint4 v = lds128(mb + 128 + 4 * wofs);  // the word's 8 scales, column order
-      sv[hb][0] = prmt(v.x, v.y, sc_sel);
-      sv[hb][1] = prmt(v.z, v.w, sc_sel);
+      if constexpr (BITS == 8) {  // the half-word's two columns 4w + 2hh, +1: adjacent scales
+        sv[hb][0] = lds32(mb + 128 + 2 * wofs + 4 * hh);
+        sv[hb][1] = 0u;
+      } else {
+        const uint4 v = lds128(mb + 128 + 4 * wofs);  // the word's 8 scales, column order
+        sv[hb][0] = prmt(v.x, v.y, sc_sel);
+        sv[hb][1] = prmt(v.z, v.w, sc_sel);
+      }
     }
+  };
+  // Fold terms of code u (nibble 0-3 / byte 0-1) of the lane's half-word in block hb:
+  // its MMA mi (rows g8 + 8 (hb % 2)), the factor on sum x c, and -scale * (zero + offset).
+  auto fold8 = [&](int hb, int u, float& sa, float& sz) {
+    const float2 s2 = pair_to_float2<false>(sv[hb][0]);
+    const float sc = u ? s2.y : s2.x;
+    const float z = __uint_as_float(((zh[hb] >> (8 * u)) & 0xFFu) | 0x4B000000u) - 8388608.f;
+    sa = sc * 16777216.f;
+    sz = -sc * z;
   };
   int cur = -1;
   bool x_on = x_real[0];  // kOne: this lane's ldmatrix row is the current group's column
@@ -387,21 +412,16 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
 
   auto fold = [&]() {
     // acc += scale * (2^24 or 2^20 * sum x c - zero * sum x) for the group just finished.
-    // Nibble nib of block hb is MMA mi = 4 (hb / 2) + nib, A rows g8 + 8 (hb % 2).
+    // Nibble nib of block hb is MMA mi = 4 (hb / 2) + nib, A rows g8 + 8 (hb % 2); byte u
+    // (8 bits) is MMA 2 (hb / 2) + u.
+    if constexpr (BITS == 8) {
 #pragma unroll
-    for (int hb = 0; hb < HB; ++hb)
+      for (int hb = 0; hb < HB; ++hb)
 #pragma unroll
-      for (int pp = 0; pp < 2; ++pp) {
-        const float2 s2 = pair_to_float2<kBF>(sv[hb][pp]);
-#pragma unroll
-        for (int n2 = 0; n2 < 2; ++n2) {
-          const int nib = 2 * pp + n2;
-          const float sc = n2 ? s2.y : s2.x;
-          // zero nibble as a float: 2^23 + z read as an fp32 bit pattern, minus 2^23
-          const float z = __uint_as_float(((zh[hb] >> (4 * nib)) & 0xFu) | 0x4B000000u) - 8388608.f;
-          const float sa = kBF ? sc : sc * ((nib & 1) ? 1048576.f : 16777216.f);
-          const float sz = -sc * (z + kBias);
-          const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
+        for (int u = 0; u < 2; ++u) {
+          float sa, sz;
+          fold8(hb, u, sa, sz);
+          const int mi = 2 * (hb >> 1) + u, rs = hb & 1;
 #pragma unroll
           for (int tb = 0; tb < TB; ++tb)
 #pragma unroll
@@ -410,7 +430,31 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
               acc[mi][tb][2 * rs + e] = __fmaf_rn(sa, accg[mi][tb][2 * rs + e], a);
             }
         }
-      }
+    } else {
+#pragma unroll
+      for (int hb = 0; hb < HB; ++hb)
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          const float2 s2 = pair_to_float2<kBF>(sv[hb][pp]);
+#pragma unroll
+          for (int n2 = 0; n2 < 2; ++n2) {
+            const int nib = 2 * pp + n2;
+            const float sc = n2 ? s2.y : s2.x;
+            // zero nibble as a float: 2^23 + z read as an fp32 bit pattern, minus 2^23
+            const float z = __uint_as_float(((zh[hb] >> (4 * nib)) & 0xFu) | 0x4B000000u) - 8388608.f;
+            const float sa = kBF ? sc : sc * ((nib & 1) ? 1048576.f : 16777216.f);
+            const float sz = -sc * (z + kBias);
+            const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
+#pragma unroll
+            for (int tb = 0; tb < TB; ++tb)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float a = __fmaf_rn(sz, xs[tb][e], acc[mi][tb][2 * rs + e]);
+                acc[mi][tb][2 * rs + e] = __fmaf_rn(sa, accg[mi][tb][2 * rs + e], a);
+              }
+          }
+        }
+    }
   };
 
   int done = j0;  // first stage not yet waited for
@@ -459,10 +503,18 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
 #pragma unroll
         for (int hb = 0; hb < HB; ++hb) {
           const uint32_t zd = prmt(zh[hb], zh[hb], 0x1010u);  // zero half-word in both halves
+          if constexpr (BITS == 8) {
 #pragma unroll
-          for (int nib = 0; nib < 4; ++nib) {
-            zp[kSub ? 0 : hb][nib] = and_or(zd >> (4 * nib), 0x000F000Fu, kMag);
-            sp[kSub ? 0 : hb][nib] = prmt(sv[hb][nib >> 1], 0u, (nib & 1) ? 0x3232u : 0x1010u);
+            for (int u = 0; u < 2; ++u) {
+              zp[kSub ? 0 : hb][u] = and_or(zd >> (8 * u), 0x00FF00FFu, kMag);
+              sp[kSub ? 0 : hb][u] = prmt(sv[hb][0], 0u, u ? 0x3232u : 0x1010u);
+            }
+          } else {
+#pragma unroll
+            for (int nib = 0; nib < 4; ++nib) {
+              zp[kSub ? 0 : hb][nib] = and_or(zd >> (4 * nib), 0x000F000Fu, kMag);
+              sp[kSub ? 0 : hb][nib] = prmt(sv[hb][nib >> 1], 0u, (nib & 1) ? 0x3232u : 0x1010u);
+            }
           }
         }
       }
@@ -497,7 +549,13 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
         }
         auto operand = [&](int rb, int hb, int nib) -> uint32_t {
           const uint32_t s = wr[rb][hb];
-          if constexpr (kSub && kBF) {
+          if constexpr (BITS == 8 && kSub) {
+            // byte nib of both half-words as the exact fp16 subnormal c * 2^-24
+            return (nib ? (s >> 8) : s) & 0x00FF00FFu;
+          } else if constexpr (BITS == 8) {
+            const uint32_t h = and_or(s >> (8 * nib), 0x00FF00FFu, kMag);  // 1024 + c
+            return hmul2(hsub2(h, zp[kSub ? 0 : hb][nib]), sp[kSub ? 0 : hb][nib]);
+          } else if constexpr (kSub && kBF) {
             return and_or(s >> (4 * nib), 0x000F000Fu, kMag);  // exact bf16 128 + c
           } else if constexpr (kSub) {
             // exact fp16 subnormals c * 2^-24 (even nibble) or c * 2^-20 (odd nibble)
@@ -512,7 +570,9 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
         };
 #pragma unroll
         for (int mi = 0; mi < NMMA; ++mi) {
-          const int hb0 = 2 * (mi >> 2), nib = mi & 3;
+          // 4 bits: MMA mi = nibble mi % 4 of blocks 2 (mi / 4), +1; 8 bits: byte mi % 2 of
+          // blocks 2 (mi / 2), +1
+          const int hb0 = BITS == 8 ? 2 * (mi >> 1) : 2 * (mi >> 2), nib = BITS == 8 ? (mi & 1) : (mi & 3);
           const uint32_t a0 = operand(0, hb0, nib), a1 = operand(0, hb0 + 1, nib);
           const uint32_t a2 = operand(1, hb0, nib), a3 = operand(1, hb0 + 1, nib);
 #pragma unroll
@@ -558,23 +618,36 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
       if (e == 1 && ng <= 4) continue;  // warp-uniform
       if (failed || gs >= ng) continue;
       load_meta(m_ring_u32 + gs * GE::META_SLOT);
+      if constexpr (BITS == 8) {
 #pragma unroll
-      for (int hb = 0; hb < HB; ++hb)
+        for (int hb = 0; hb < HB; ++hb)
 #pragma unroll
-        for (int pp = 0; pp < 2; ++pp) {
-          const float2 s2 = pair_to_float2<kBF>(sv[hb][pp]);
-#pragma unroll
-          for (int n2 = 0; n2 < 2; ++n2) {
-            const int nib = 2 * pp + n2;
-            const float sc = n2 ? s2.y : s2.x;
-            const float z = __uint_as_float(((zh[hb] >> (4 * nib)) & 0xFu) | 0x4B000000u) - 8388608.f;
-            const float sa = kBF ? sc : sc * ((nib & 1) ? 1048576.f : 16777216.f);
-            const float sz = -sc * (z + kBias);
-            const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
+          for (int u = 0; u < 2; ++u) {
+            float sa, sz;
+            fold8(hb, u, sa, sz);
+            const int mi = 2 * (hb >> 1) + u, rs = hb & 1;
             const float a = __fmaf_rn(sz, xs[0][e], out[mi][rs]);
             out[mi][rs] = __fmaf_rn(sa, accg[mi][0][2 * rs + e], a);
           }
-        }
+      } else {
+#pragma unroll
+        for (int hb = 0; hb < HB; ++hb)
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp) {
+            const float2 s2 = pair_to_float2<kBF>(sv[hb][pp]);
+#pragma unroll
+            for (int n2 = 0; n2 < 2; ++n2) {
+              const int nib = 2 * pp + n2;
+              const float sc = n2 ? s2.y : s2.x;
+              const float z = __uint_as_float(((zh[hb] >> (4 * nib)) & 0xFu) | 0x4B000000u) - 8388608.f;
+              const float sa = kBF ? sc : sc * ((nib & 1) ? 1048576.f : 16777216.f);
+              const float sz = -sc * (z + kBias);
+              const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
+              const float a = __fmaf_rn(sz, xs[0][e], out[mi][rs]);
+              out[mi][rs] = __fmaf_rn(sa, accg[mi][0][2 * rs + e], a);
+            }
+          }
+      }
     }
   }
   if (kSub && !kOne && cur >= 0 && !failed) fold();
@@ -620,11 +693,15 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
   // of block hb, i.e. MMA mi = 4 (hb / 2) + nib, rows g8 + 8 (hb % 2); g8 varies fastest
   // across threads, the token slowest.
   float* pack = red + NW * GE::EP;
+  // 8 bits: column col = 16 hb + 4 (g8 / 2) + 2 (g8 % 2) + u from byte u of block hb, MMA
+  // mi = 2 (hb / 2) + u.
   for (int i = threadIdx.x; i < pack_n; i += NW * 32) {
     const int g8i = i & 7, r = i >> 3;
-    const int nib = r & 3, hb = (r >> 2) % HB, t = (r >> 2) / HB;
-    const int col = 32 * hb + 8 * (g8i >> 1) + 2 * nib + (g8i & 1);
-    const int mi = 4 * (hb >> 1) + nib, rs = hb & 1;
+    constexpr int U = CPW / 2, LU = BITS == 8 ? 1 : 2;  // codes per half-word, log2
+    const int nib = r & (U - 1), hb = (r >> LU) % HB, t = (r >> LU) / HB;
+    const int col = BITS == 8 ? 16 * hb + 4 * (g8i >> 1) + 2 * (g8i & 1) + nib
+                              : 32 * hb + 8 * (g8i >> 1) + 2 * nib + (g8i & 1);
+    const int mi = U * (hb >> 1) + nib, rs = hb & 1;
     const int X = (mi * TB + (t >> 3)) * 4 + 2 * rs + (t & 1);
     const int e = X * 32 + g8i * 4 + ((t & 7) >> 1) + (X >> 2);
     float v = 0.f;
@@ -637,7 +714,7 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
         v += red[w * GE::EP + e];
       }
     }
-    pack[t * 8 * GE::CW_W + col] = v;
+    pack[t * NCOL + col] = v;
   }
   __syncthreads();
 #ifdef AWQ_DECODE_DEBUG_TIME
@@ -667,11 +744,11 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
   const int lo = static_cast<int>(rank) * p.slice;
   const int hi = min(pack_n, lo + p.slice);
   for (int i = lo + threadIdx.x; got && i < hi; i += NW * 32) {
-    const int t = i / (8 * GE::CW_W), col = i - t * 8 * GE::CW_W;
-    if (m0 + t >= m_lim || m0 + t < 0 || 8 * cw0 + col >= p.N) continue;
+    const int t = i / NCOL, col = i - t * NCOL;
+    if (m0 + t >= m_lim || m0 + t < 0 || CPW * cw0 + col >= p.N) continue;
     float sum = 0.f;
     for (uint32_t r = 0; r < cs; ++r) sum += recv[r * p.slice + (i - lo)];
-    reinterpret_cast<uint16_t*>(p.y)[(long long)(m0 + t) * p.N + 8 * cw0 + col] =
+    reinterpret_cast<uint16_t*>(p.y)[(long long)(m0 + t) * p.N + CPW * cw0 + col] =
         float_to_elem<kBF>(sum + bias_s[col]);
   }
 #ifdef AWQ_DECODE_DEBUG_TIME
@@ -731,9 +808,9 @@ struct Plan {
   int owners = 1, slice = 0;
 };
 
-template <int TB, int CWL, bool O, int NW>
+template <int TB, int CWL, bool O, int NW, int BITS = 4>
 Plan layout(int cs, int slots, int x_rows, int groups) {
-  using GE = Geo<TB, CWL, NW>;
+  using GE = Geo<TB, CWL, NW, BITS>;
   const int meta_entries = O ? groups : slots;  // stash per group, or ring per slot
   Plan pl;
   pl.cs = cs;
@@ -744,9 +821,9 @@ Plan layout(int cs, int slots, int x_rows, int groups) {
   pl.m_off = pl.w_off + NW * slots * GE::W_BYTES;
   pl.zl_off = pl.m_off + NW * meta_entries * GE::META_SLOT;
   pl.bias_off = pl.zl_off + NW * 128;
-  pl.bar_off = pl.bias_off + 8 * GE::CW_W * 4;
+  pl.bar_off = pl.bias_off + GE::NCOL * 4;
   pl.recv_off = ((pl.bar_off + (NW * slots + 1) * 8 + 15) / 16) * 16;
-  const int pack_n = x_rows * 8 * GE::CW_W;
+  const int pack_n = x_rows * GE::NCOL;
   pl.owners = (pack_n * cs >= kMultiOwnerMin && cs >= 4) ? cs : 1;
   pl.slice = pl.owners == 1 ? pack_n : ((pack_n + 4 * cs - 1) / (4 * cs)) * 4;
   pl.smem = 1024 + pl.recv_off + cs * pl.slice * 4;
@@ -795,9 +872,9 @@ int max_warp_groups(int TS, int P, int spg) {
 }
 
 // Co-resident clusters of size cs at `smem` bytes per CTA (occupancy API).
-template <int TB, int CWL, bool S, bool O, int NW, bool B, bool GR = false>
+template <int TB, int CWL, bool S, bool O, int NW, bool B, bool GR = false, int BITS = 4>
 int max_clusters(int cs, int smem) {
-  auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B, GR>;
+  auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B, GR, BITS>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, 1, 1);
   cfg.blockDim = dim3(NW * 32, 1, 1);
@@ -822,16 +899,16 @@ int max_clusters(int cs, int smem) {
 // each warp keeping at least one 64-row stage; ties go to the smaller cluster.  Ring
 // depth: as many slots as the shared memory left per CTA allows, up to the warp's stage
 // count.  Cached per shape.
-template <int TB, int CWL, bool S, bool O, int NW, bool B, bool GR = false>
+template <int TB, int CWL, bool S, bool O, int NW, bool B, bool GR = false, int BITS = 4>
 cudaError_t plan_for(const GemmProblem& p, Plan* out) {
-  using GE = Geo<TB, CWL, NW>;
+  using GE = Geo<TB, CWL, NW, BITS>;
   static std::mutex mu;
   static std::map<std::tuple<int, int, int, int>, Plan> cache;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
-  const int C = p.N / 8;
+  const int C = p.N / GE::CPW;
   const int nt = (C + GE::CW_W - 1) / GE::CW_W;
   // grouped: the 8-row tiles that will hold rows, estimated (the offsets live on the device):
   // R rows over E experts fill about max(R / 8, min(R, E)) tiles; the grid itself covers the
@@ -852,7 +929,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B, GR>;
+    auto kern = decode_tma_kernel<TB, CWL, S, O, NW, B, GR, BITS>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dl.smem_optin);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -876,7 +953,7 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
     const int groups = !O ? 0
                        : NW == 4 ? kOneGroups
                                  : std::min(kOneGroups, max_warp_groups(TS, cs * NW, p.G / kRS));
-    if (layout<TB, CWL, O, NW>(cs, 1, x_rows, groups).smem - layout<TB, CWL, O, NW>(cs, 1, x_rows, groups).recv_off - 1024 > kRecvCap) break;
+    if (layout<TB, CWL, O, NW, BITS>(cs, 1, x_rows, groups).smem - layout<TB, CWL, O, NW, BITS>(cs, 1, x_rows, groups).recv_off - 1024 > kRecvCap) break;
     const long long grid = tiles * cs;
     long long per_sm = (grid + dl.sms - 1) / dl.sms;
     if (per_sm < 1) per_sm = 1;
@@ -885,18 +962,18 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
     const int spw = (TS + cs * NW - 1) / (cs * NW);  // stages of the busiest warp
     const int max_slots = NW == 8 ? AWQ_DECODE_WIDE_SLOTS : kMaxSlots;
     int slots = spw < max_slots ? spw : max_slots;
-    while (slots > 1 && layout<TB, CWL, O, NW>(cs, slots, x_rows, groups).smem > budget) --slots;
+    while (slots > 1 && layout<TB, CWL, O, NW, BITS>(cs, slots, x_rows, groups).smem > budget) --slots;
     if (slots < red_slots) slots = red_slots;
-    Plan pl = layout<TB, CWL, O, NW>(cs, slots, x_rows, groups);
+    Plan pl = layout<TB, CWL, O, NW, BITS>(cs, slots, x_rows, groups);
     if (pl.smem > dl.smem_optin) continue;
     // single wave with slack, checked against the occupancy API at this size
     bool fits = false;
     while (true) {
-      long long cap = (long long)max_clusters<TB, CWL, S, O, NW, B, GR>(cs, pl.smem) * cs;
+      long long cap = (long long)max_clusters<TB, CWL, S, O, NW, B, GR, BITS>(cs, pl.smem) * cs;
       if (cap > (long long)kMaxCtasPerSm * dl.sms) cap = (long long)kMaxCtasPerSm * dl.sms;
       if (grid * 100 <= cap * kWaveFillPct) { fits = true; break; }
       if (pl.slots <= red_slots || pl.slots <= 1) break;
-      pl = layout<TB, CWL, O, NW>(cs, pl.slots - 1, x_rows, groups);
+      pl = layout<TB, CWL, O, NW, BITS>(cs, pl.slots - 1, x_rows, groups);
     }
     if (!fits && cs > 1) continue;
     const long long score = fits ? grid : 0;
@@ -911,17 +988,17 @@ cudaError_t plan_for(const GemmProblem& p, Plan* out) {
   return cudaSuccess;
 }
 
-template <int TB, int CWL, bool S, bool O, int NW, bool B, bool GR = false>
+template <int TB, int CWL, bool S, bool O, int NW, bool B, bool GR = false, int BITS = 4>
 cudaError_t launch_v(const GemmProblem& p) {
-  using GE = Geo<TB, CWL, NW>;
+  using GE = Geo<TB, CWL, NW, BITS>;
   Plan pl;
-  cudaError_t e = plan_for<TB, CWL, S, O, NW, B, GR>(p, &pl);
+  cudaError_t e = plan_for<TB, CWL, S, O, NW, B, GR, BITS>(p, &pl);
   if (e != cudaSuccess) return e;
   const int x_rows = p.M < 8 * TB ? p.M : 8 * TB;
 
   TmaDecodeParams dp;
   const char* why = nullptr;
-  const int C = p.N / 8;
+  const int C = p.N / GE::CPW;
   const int ngrp = p.K / p.G;
   const CUtensorMapSwizzle wsw = CWL == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
   const CUtensorMapDataType et = B ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -932,13 +1009,13 @@ cudaError_t launch_v(const GemmProblem& p) {
               make_tmap_3d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, p.E, GE::CW_W, kRS, wsw, &why) &&
               make_tmap_3d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, p.E, GE::CW_W, 1,
                            CU_TENSOR_MAP_SWIZZLE_NONE, &why) &&
-              make_tmap_3d(&dp.tm_s, et, 2, p.sc, p.N, ngrp, p.E, 8 * GE::CW_W, 1, CU_TENSOR_MAP_SWIZZLE_NONE, &why);
+              make_tmap_3d(&dp.tm_s, et, 2, p.sc, p.N, ngrp, p.E, GE::NCOL, 1, CU_TENSOR_MAP_SWIZZLE_NONE, &why);
   } else {
     maps_ok = maps_ok &&
               make_tmap_2d(&dp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, GE::CW_W, kRS, wsw, &why) &&
               make_tmap_2d(&dp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, GE::CW_W, 1,
                            CU_TENSOR_MAP_SWIZZLE_NONE, &why) &&
-              make_tmap_2d(&dp.tm_s, et, 2, p.sc, p.N, ngrp, 8 * GE::CW_W, 1, CU_TENSOR_MAP_SWIZZLE_NONE, &why);
+              make_tmap_2d(&dp.tm_s, et, 2, p.sc, p.N, ngrp, GE::NCOL, 1, CU_TENSOR_MAP_SWIZZLE_NONE, &why);
   }
   if (!maps_ok)
     return cudaErrorInvalidValue;
@@ -973,7 +1050,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S, O, NW, B, GR>, dp);
+  return cudaLaunchKernelEx(&cfg, decode_tma_kernel<TB, CWL, S, O, NW, B, GR, BITS>, dp);
 }
 
 }  // namespace
@@ -981,10 +1058,12 @@ cudaError_t launch_v(const GemmProblem& p) {
 bool decode_tma_supported(const GemmProblem& p, const char** why) {
   static const char* dummy;
   if (!why) why = &dummy;
-  if (p.bits != 4) { *why = "4-bit codes only"; return false; }
+  if (p.bits != 4 && p.bits != 8) { *why = "4- or 8-bit codes only"; return false; }
+  if (p.bits == 8 && (p.bf16 || p.offsets != nullptr)) { *why = "8-bit codes: fp16 plain launches only"; return false; }
   if (p.K % kRS != 0) { *why = "TMA decode needs K % 64 == 0"; return false; }
   if (p.G % kRS != 0) { *why = "TMA decode needs group_size % 64 == 0"; return false; }
-  if (p.N % 32 != 0) { *why = "TMA decode needs N % 32 == 0"; return false; }
+  // packed rows a multiple of 16 bytes (tensor-map strides): N % 32 (4 bits), N % 16 (8)
+  if (p.N % (p.bits == 8 ? 16 : 32) != 0) { *why = "TMA decode needs N % 32 == 0 (N % 16 for 8 bits)"; return false; }
   if (!aligned(p.x, 16) || !aligned(p.qw, 16) || !aligned(p.qz, 16) || !aligned(p.sc, 16)) {
     *why = "TMA decode needs 16-byte aligned x, qweight, qzeros, scales";
     return false;
@@ -994,7 +1073,7 @@ bool decode_tma_supported(const GemmProblem& p, const char** why) {
   return true;
 }
 
-template <bool B>
+template <bool B, int BITS = 4>
 cudaError_t launch_decode_tma_t(const GemmProblem& p) {
   const Variant v = pick(p);
   if (v.TB == 1) {
@@ -1003,26 +1082,27 @@ cudaError_t launch_decode_tma_t(const GemmProblem& p) {
       // would leave a warp kWideStages or more stages (long K: more warps share the work).
       const int TS = p.K / kRS, spg = p.G / kRS;
       Plan p4;
-      cudaError_t e = plan_for<1, 2, true, true, 4, B>(p, &p4);
+      cudaError_t e = plan_for<1, 2, true, true, 4, B, false, BITS>(p, &p4);
       if (e != cudaSuccess) return e;
       if ((TS + 4 * p4.cs - 1) / (4 * p4.cs) >= kWideStages) {
         Plan p8;
-        e = plan_for<1, 2, true, true, 8, B>(p, &p8);
+        e = plan_for<1, 2, true, true, 8, B, false, BITS>(p, &p8);
         if (e != cudaSuccess) return e;
-        if (max_warp_groups(TS, 8 * p8.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 8, B>(p);
+        if (max_warp_groups(TS, 8 * p8.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 8, B, false, BITS>(p);
       }
-      if (max_warp_groups(TS, 4 * p4.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 4, B>(p);
+      if (max_warp_groups(TS, 4 * p4.cs, spg) <= kOneGroups) return launch_v<1, 2, true, true, 4, B, false, BITS>(p);
     }
-    return launch_v<1, 2, true, false, kNW, B>(p);
+    return launch_v<1, 2, true, false, kNW, B, false, BITS>(p);
   }
-  if (v.TB == 2) return launch_v<2, 1, true, false, kNW, B>(p);
-  return launch_v<4, 1, false, false, kNW, B>(p);
+  if (v.TB == 2) return launch_v<2, 1, true, false, kNW, B, false, BITS>(p);
+  return launch_v<4, 1, false, false, kNW, B, false, BITS>(p);
 }
 
 bool decode_grouped_supported(const GemmProblem& p, const char** why) {
   static const char* dummy;
   if (!why) why = &dummy;
   if (p.bf16) { *why = "grouped launches take fp16"; return false; }
+  if (p.bits != 4) { *why = "grouped launches take 4-bit codes"; return false; }
   if (p.E <= 0 || p.offsets == nullptr) { *why = "grouped launch without experts"; return false; }
   return decode_tma_supported(p, why);
 }
@@ -1032,6 +1112,7 @@ cudaError_t launch_decode_grouped(const GemmProblem& p) {
 }
 
 cudaError_t launch_decode_tma(const GemmProblem& p) {
+  if (p.bits == 8) return launch_decode_tma_t<false, 8>(p);
   return p.bf16 ? launch_decode_tma_t<true>(p) : launch_decode_tma_t<false>(p);
 }
 
