@@ -186,3 +186,15 @@ def test_w8_argument_checks_are_host_side(lib):
     if not torch.cuda.is_available():
         assert g(A, A, A, A, None, 1, 256, 12, 128, B, 0, None) == DEVICE
         assert d(A, A, A, 256, 12, 128, B, 0, None) == DEVICE
+
+
+def test_linear_layer_refuses_host_tensors_and_bad_widths(lib):
+    import torch
+    from w4a16_weight_only_gb300 import AwqLinear
+    qw = torch.zeros((256, 32), dtype=torch.int32)
+    qz = torch.zeros((2, 32), dtype=torch.int32)
+    sc = torch.zeros((2, 256), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        AwqLinear(qw, qz, sc, None, group_size=128)          # host tensors never reach a kernel
+    with pytest.raises(ValueError):
+        AwqLinear(qw, qz, sc, None, group_size=128, bits=5)

@@ -4,13 +4,13 @@ The computation lives in ``libawq_gb300.so`` (C ABI in ``include/awq.h``, CUDA s
 in ``csrc/``).  This package only builds it (``build.py``) and marshals arguments
 (``_binding.py``); PyTorch supplies device memory and streams.
 """
-from ._binding import (AwqError, PATHS, awq_dequant, awq_dequant_w8, awq_gemm, awq_gemm_grouped,
+from ._binding import (AwqError, AwqLinear, PATHS, awq_dequant, awq_dequant_w8, awq_gemm, awq_gemm_grouped,
                        awq_gemm_w8, awq_quantize_rtn,
                        device_status,
                        last_error, load_library, runtime_available, select_path,
                        selftest_wait_timeout)
 
-__all__ = ["AwqError", "PATHS", "awq_dequant", "awq_dequant_w8", "awq_gemm", "awq_gemm_grouped",
+__all__ = ["AwqError", "AwqLinear", "PATHS", "awq_dequant", "awq_dequant_w8", "awq_gemm", "awq_gemm_grouped",
            "awq_gemm_w8", "awq_quantize_rtn",
            "device_status",
            "last_error",

@@ -157,6 +157,73 @@ def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, pa
     return out.reshape(*lead, N)
 
 
+class AwqLinear:
+    """An AWQ linear layer whose weights are validated once: ``layer(x)`` runs
+    ``awq_gemm_ex`` (fp16), ``awq_gemm_bf16_ex`` (bf16 scales) or ``awq_gemm_w8_ex``
+    (``bits=8``) with only x and out checked per call.
+
+    qweight int32 [K, N/8] (4 bits) or [K, N/4] (8 bits), qzeros int32 [K/G, N/8 or N/4],
+    scales fp16 or bf16 [K/G, N] (it sets the activation dtype; 8 bits: fp16), bias [N] of
+    the same dtype or None, all contiguous on one CUDA device.  The layer keeps references
+    to the tensors; it reads them in place on every call (in-place updates are seen)."""
+
+    __slots__ = ("K", "N", "group_size", "bits", "dtype", "device", "_fn", "_w", "_path",
+                 "_tensors")
+
+    def __init__(self, qweight, qzeros, scales, bias=None, group_size=128, bits=4, path="auto"):
+        lib = load_library()
+        if bits not in (4, 8):
+            raise ValueError("bits must be 4 or 8")
+        if qweight.dim() != 2 or qweight.shape[0] == 0:
+            raise ValueError("qweight must be a non-empty [K, N / (32 / bits)] int32 matrix")
+        per = 32 // bits
+        K, C = qweight.shape
+        N = C * per
+        dev = _cuda_index(qweight, "qweight")
+        dt = scales.dtype
+        if dt not in (torch.float16, torch.bfloat16) or (bits == 8 and dt is not torch.float16):
+            raise TypeError("scales must be float16 (or bfloat16 with 4-bit codes)")
+        _need(qweight, "qweight", torch.int32, (K, C), dev)
+        ng = _groups(K, group_size)
+        _need(qzeros, "qzeros", torch.int32, (ng, C), dev)
+        _need(scales, "scales", dt, (ng, N), dev)
+        if bias is not None:
+            _need(bias, "bias", dt, (N,), dev)
+        self.K, self.N, self.group_size, self.bits = K, N, group_size, bits
+        self.dtype, self.device = dt, dev
+        self._fn = (lib.awq_gemm_w8_ex if bits == 8
+                    else lib.awq_gemm_bf16_ex if dt is torch.bfloat16 else lib.awq_gemm_ex)
+        self._w = (qweight.data_ptr(), qzeros.data_ptr(), scales.data_ptr(), _ptr(bias))
+        self._path = PATHS[path]
+        self._tensors = (qweight, qzeros, scales, bias)
+
+    def __call__(self, x, out=None, stream=None):
+        """y [..., N] = x [..., K] @ W (+ bias) on ``stream`` (default: the current stream)."""
+        K, N, dt = self.K, self.N, self.dtype
+        if x.dtype is not dt:
+            raise TypeError(f"x must be {dt}, got {x.dtype}")
+        if x.get_device() != self.device:
+            raise ValueError(f"x is on {x.device}, expected CUDA device {self.device}")
+        shape = x.shape
+        if shape[-1] != K or not x.is_contiguous():
+            raise ValueError(f"x must be a contiguous [..., {K}] tensor, got {tuple(shape)}")
+        M = x.numel() // K
+        if out is None:
+            out = torch.empty(shape[:-1] + (N,), dtype=dt, device=x.device)
+        elif (out.dtype is not dt or out.get_device() != self.device or out.shape[-1] != N
+              or out.numel() != M * N or not out.is_contiguous()):
+            raise ValueError(f"out must be a contiguous {dt} [..., {N}] tensor of {M} rows "
+                             f"on device {self.device}")
+        w = self._w
+        st = self._fn(x.data_ptr(), w[0], w[1], w[2], w[3], M, K, N, self.group_size,
+                      out.data_ptr(), self._path,
+                      (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None
+                      else torch.cuda.current_stream().cuda_stream)
+        if st != AWQ_OK:
+            raise AwqError(st, last_error())
+        return out
+
+
 def awq_gemm_w8(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, path="auto",
                 stream=None):
     """y = x @ dequant8(qweight, qzeros, scales) (+ bias) via awq_gemm_w8: 8-bit codes,
