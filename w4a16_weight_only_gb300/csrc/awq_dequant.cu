@@ -95,62 +95,135 @@ __global__ void __launch_bounds__(256) dequant8_kernel(const uint32_t* __restric
   }
 }
 
-// Generic fused GEMM: one thread per output column, kMT activation rows per block row,
-// activations staged through shared memory in kKT-wide slices.  fp32 accumulation in
-// increasing k order.  Used for shapes the fast kernels do not take (K or G not a
-// multiple of 16, N not a multiple of the decode tile, unaligned pointers).
-constexpr int kMT = 8;
-constexpr int kKT = 64;
+// Generic fused GEMM, for the shapes the tensor-core kernels do not take (any K, any group
+// size dividing K, any N the packing allows, 4-byte aligned words and 2-byte aligned
+// elements).  A CTA of kGW warps owns TW consecutive packed words of every row (the
+// TW * 32 / kBits columns they hold) and MT activation rows; K is cut into kGW contiguous
+// chunks, one per warp.  Inside a warp lane (kr, w) takes word w of rows kr, kr + LK,
+// kr + 2 LK, ... of the chunk (LK = 32 / TW), so one load instruction reads LK whole row
+// segments of the tile.  Per group a lane accumulates sum x * code for each of its
+// columns and sum x (fp32), and folds them once at the group's end:
+// acc += scale * (sum x code - zero * sum x).  The LK lanes of a word are then added by
+// butterfly shuffles, the warps in warp order through shared memory, the bias last, and
+// y is rounded once.  Every order is fixed: repeated calls give the same bits.
+constexpr int kGW = 16;
 
-template <bool kBF, int kBits>
-__global__ void __launch_bounds__(128) generic_gemm_kernel(GemmProblem p) {
+template <bool kBF, int kBits, int TW, int MT>
+__global__ void __launch_bounds__(kGW * 32, 1) generic_gemm_kernel(GemmProblem p) {
+  constexpr int CPW = 32 / kBits;  // columns per packed word
+  constexpr int LK = 32 / TW;      // rows of K a warp step covers
+  constexpr int NC = TW * CPW;     // columns of the tile
+  constexpr uint32_t kMask = kBits == 4 ? 0xFu : 0xFFu;
+  __shared__ float part[kGW][MT][NC];
   const uint16_t* x16 = reinterpret_cast<const uint16_t*>(p.x);
   const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.sc);
-  __shared__ float xs[kMT][kKT];
-  const int n = blockIdx.x * blockDim.x + threadIdx.x;
-  const int C = kBits == 4 ? p.N >> 3 : p.N >> 2;
-  const bool active = n < p.N;
-  const int cw = kBits == 4 ? n >> 3 : n >> 2;
-  const int j = n & 7;
-  // bit offset of column n in its word: nibble holding column j (inverse of ORDER), or byte n % 4
-  const int shift = kBits == 4 ? 4 * (((j & 1) << 2) | (j >> 1)) : 8 * (n & 3);
-  const uint32_t mask = kBits == 4 ? 0xFu : 0xFFu;
-  for (int m0 = blockIdx.y * kMT; m0 < p.M; m0 += gridDim.y * kMT) {
-  float acc[kMT];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int kr = lane / TW, wi = lane % TW;
+  const int C = p.N / CPW;
+  const int cw = blockIdx.x * TW + wi;
+  const bool col_ok = cw < C;
+  const int chunk = ((p.K + kGW - 1) / kGW + LK - 1) / LK * LK;
+  const int klo = min(p.K, warp * chunk), khi = min(p.K, klo + chunk);
+  // bit offset of column j of a word: the nibble holding it (inverse of ORDER), or byte j
+  auto shift_of = [](int j) { return kBits == 4 ? 4 * (((j & 1) << 2) | (j >> 1)) : 8 * j; };
+  for (int m0 = blockIdx.y * MT; m0 < p.M; m0 += gridDim.y * MT) {
+    float acc[MT][CPW];
 #pragma unroll
-  for (int m = 0; m < kMT; ++m) acc[m] = 0.f;
-  for (int k0 = 0; k0 < p.K; k0 += kKT) {
-    __syncthreads();
-    for (int e = threadIdx.x; e < kMT * kKT; e += blockDim.x) {
-      const int m = e / kKT, kk = e % kKT;
-      const int gm = m0 + m, gk = k0 + kk;
-      xs[m][kk] = (gm < p.M && gk < p.K) ? elem_to_float<kBF>(x16[(long long)gm * p.K + gk]) : 0.f;
-    }
-    __syncthreads();
-    if (active) {
-      const int kend = min(kKT, p.K - k0);
-      for (int kk = 0; kk < kend; ++kk) {
-        const int k = k0 + kk;
-        const int g = k / p.G;
-        const uint32_t q = p.qw[(long long)k * C + cw];
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int j = 0; j < CPW; ++j) acc[m][j] = 0.f;
+    int k = klo + kr;
+    if (col_ok && k < khi) {
+      float a[MT][CPW], sx[MT], zf[CPW], sf[CPW];
+      int g = k / p.G, gend = (g + 1) * p.G;
+      auto open_group = [&]() {
         const uint32_t z = p.qz[(long long)g * C + cw];
-        const int code = (int)((q >> shift) & mask);
-        const int zero = (int)((z >> shift) & mask);
-        const float w = __fmul_rn((float)(code - zero), elem_to_float<kBF>(sc16[(long long)g * p.N + n]));
 #pragma unroll
-        for (int m = 0; m < kMT; ++m) acc[m] = __fmaf_rn(xs[m][kk], w, acc[m]);
+        for (int j = 0; j < CPW; ++j) {
+          zf[j] = static_cast<float>((z >> shift_of(j)) & kMask);
+          sf[j] = elem_to_float<kBF>(sc16[(long long)g * p.N + CPW * cw + j]);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          sx[m] = 0.f;
+#pragma unroll
+          for (int j = 0; j < CPW; ++j) a[m][j] = 0.f;
+        }
+      };
+      auto fold = [&]() {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int j = 0; j < CPW; ++j)
+            acc[m][j] = __fmaf_rn(sf[j], __fmaf_rn(-zf[j], sx[m], a[m][j]), acc[m][j]);
+      };
+      open_group();
+      for (; k < khi; k += LK) {
+        if (k >= gend) {
+          fold();
+          g = k / p.G;
+          gend = (g + 1) * p.G;
+          open_group();
+        }
+        const uint32_t q = p.qw[(long long)k * C + cw];
+        float xv[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          xv[m] = (m0 + m < p.M) ? elem_to_float<kBF>(x16[(long long)(m0 + m) * p.K + k]) : 0.f;
+#pragma unroll
+        for (int j = 0; j < CPW; ++j) {
+          const float c = static_cast<float>((q >> shift_of(j)) & kMask);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) a[m][j] = __fmaf_rn(xv[m], c, a[m][j]);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) sx[m] += xv[m];
       }
+      fold();
     }
-  }
-  if (active) {
-    const float b = p.bias ? elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[n]) : 0.f;
 #pragma unroll
-    for (int m = 0; m < kMT; ++m) {
-      const int gm = m0 + m;
-      if (gm < p.M) reinterpret_cast<uint16_t*>(p.y)[(long long)gm * p.N + n] = float_to_elem<kBF>(acc[m] + b);
+    for (int off = TW; off < 32; off <<= 1)
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int j = 0; j < CPW; ++j) acc[m][j] += __shfl_xor_sync(0xffffffffu, acc[m][j], off);
+    if (kr == 0)
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int j = 0; j < CPW; ++j) part[warp][m][wi * CPW + j] = acc[m][j];
+    __syncthreads();
+    for (int e = threadIdx.x; e < MT * NC; e += blockDim.x) {
+      const int m = e / NC, c = e - m * NC;
+      const int n = blockIdx.x * NC + c, gm = m0 + m;
+      if (gm >= p.M || n >= p.N) continue;
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGW; ++w) sum += part[w][m][c];
+      if (p.bias) sum += elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[n]);
+      reinterpret_cast<uint16_t*>(p.y)[(long long)gm * p.N + n] = float_to_elem<kBF>(sum);
     }
+    __syncthreads();
   }
-  }  // m0
+}
+
+template <bool kBF, int kBits, int TW>
+void launch_generic_t(const GemmProblem& p, int C) {
+  const int tiles = (C + TW - 1) / TW;
+  const int mt = p.M == 1 ? 1 : 4;
+  const int mtiles = (p.M + mt - 1) / mt;
+  dim3 grid(tiles, mtiles < 65535 ? mtiles : 65535);
+  if (mt == 1) generic_gemm_kernel<kBF, kBits, TW, 1><<<grid, kGW * 32, 0, p.stream>>>(p);
+  else generic_gemm_kernel<kBF, kBits, TW, 4><<<grid, kGW * 32, 0, p.stream>>>(p);
+}
+
+template <bool kBF, int kBits>
+void launch_generic_b(const GemmProblem& p) {
+  const int C = p.N / (32 / kBits);
+  const int mtiles = p.M == 1 ? 1 : (p.M + 3) / 4;
+  // 8-word tiles (32-byte row segments) when they give at least two CTAs per SM, else 4
+  if ((long long)((C + 7) / 8) * mtiles >= 2 * 152) launch_generic_t<kBF, kBits, 8>(p, C);
+  else launch_generic_t<kBF, kBits, 4>(p, C);
 }
 
 template <bool kBF>
@@ -198,11 +271,9 @@ cudaError_t probe_kernel_image(cudaFuncAttributes* attr) {
 }
 
 cudaError_t launch_generic(const GemmProblem& p) {
-  const int mtiles = (p.M + kMT - 1) / kMT;
-  dim3 grid((p.N + 127) / 128, mtiles < 65535 ? mtiles : 65535);
-  if (p.bits == 8) generic_gemm_kernel<false, 8><<<grid, 128, 0, p.stream>>>(p);
-  else if (p.bf16) generic_gemm_kernel<true, 4><<<grid, 128, 0, p.stream>>>(p);
-  else generic_gemm_kernel<false, 4><<<grid, 128, 0, p.stream>>>(p);
+  if (p.bits == 8) launch_generic_b<false, 8>(p);
+  else if (p.bf16) launch_generic_b<true, 4>(p);
+  else launch_generic_b<false, 4>(p);
   return cudaGetLastError();
 }
 
