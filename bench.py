@@ -70,10 +70,10 @@ def step_bytes(lins):
 # `python bench.py --steps 60 --warmup 3 --no-cpu-baseline` summarised in
 # profiles/decode_tma_7b_m1_bench_launches.md; valid only for the kernel source it was
 # measured on (SHA-256 of the files below), else reported as null.
-TRAFFIC_BYTES_PER_LAUNCH = 18_588_144
+TRAFFIC_BYTES_PER_LAUNCH = 18_588_014
 TRAFFIC_SOURCES = {
     "w4a16_weight_only_gb300/csrc/awq_decode_tma.cu":
-        "5c3cce1c8f779c582aba04ffff707d7e7f033c7338278b8a252bf9eb2d79ec53",
+        "e0bf1b4352904e9b6879cf2735e6ab931c5e5ea67ff9e2f48bb1a89323b2e3f5",
     "w4a16_weight_only_gb300/csrc/awq_ptx.cuh":
         "166c2c9cd2d4a880677df7bd3dc634de58dadf2fcdc9ba2bdcf045010269d495",
 }
@@ -572,6 +572,41 @@ def run_w8_sweep(awq, timed, hbm, hbm_kind):
             del g
         print(json.dumps(line), flush=True)
         del sets, w, x, y
+        torch.cuda.empty_cache()
+    # large M: TFLOP/s of back-to-back launches, beside dequant + cuBLAS fp16
+    tflops = 1900.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tflops = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        pass
+    for (M, K, N) in ((512, 4096, 11008), (2048, 4096, 11008), (2048, 11008, 4096), (4096, 8192, 28672)):
+        G = 128
+        d = synth.awq8_linear(5100 + M + K + N, M, K, N, group_size=G, bias=True)
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        x, bias = dev(d["x"]), dev(d["bias"])
+        qw, qz, sc = dev(d["qweight"]), dev(d["qzeros"]), dev(d["scales"])
+        y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        flop = 2.0 * M * N * K
+        # eager launches on the current stream (the one `timed` records its events on)
+        fn = lambda: awq.awq_gemm_w8(x, qw, qz, sc, bias, G, out=y)
+        timed(fn, 3)
+        t = timed(fn, 10)
+        wd = awq.awq_dequant_w8(qw, qz, sc, G)
+        torch.cuda.synchronize()
+        mm = lambda: torch.matmul(x, wd, out=y)
+        timed(mm, 3)
+        t_mm = timed(mm, 10)
+        dq = lambda: awq.awq_dequant_w8(qw, qz, sc, G)
+        timed(dq, 3)
+        t_dq = timed(dq, 10)
+        awq.device_status()
+        print(json.dumps({"workload": f"w8_m{M}_{K}x{N}", "bits": 8, "M": M, "K": K, "N": N,
+                          "group_size": G, "bias": True, "us": t, "TFLOP_s": flop / t / 1e6,
+                          "frac_tensor": flop / t / 1e6 / tflops, "cublas_fp16_dense_us": t_mm,
+                          "dequant_plus_cublas_us": t_dq + t_mm, "tensor_peak_TFLOP_s": tflops}),
+              flush=True)
+        del x, qw, qz, sc, y, wd
         torch.cuda.empty_cache()
 
 

@@ -74,9 +74,9 @@ def decode_ok(K, N, G):
 
 
 @pytest.mark.parametrize("M,K,N,G,bias", SMALL)
-@pytest.mark.parametrize("path", ["auto", "decode", "generic"])
+@pytest.mark.parametrize("path", ["auto", "decode", "prefill", "generic"])
 def test_gemm_w8_small_vs_oracle(awq, M, K, N, G, bias, path):
-    if path == "decode" and not decode_ok(K, N, G):
+    if path in ("decode", "prefill") and not decode_ok(K, N, G):
         pytest.skip("shape outside the tensor-core kernel's contract")
     d = synth.awq8_linear(13000 + M + K + N, M, K, N, group_size=G, bias=bias)
     y = run(awq, d, path)
@@ -85,7 +85,7 @@ def test_gemm_w8_small_vs_oracle(awq, M, K, N, G, bias, path):
 
 
 @pytest.mark.parametrize("M", [1, 5, 16, 32, 300])
-@pytest.mark.parametrize("path", ["decode", "generic"])
+@pytest.mark.parametrize("path", ["decode", "prefill", "generic"])
 def test_gemm_w8_exact_case_bitwise(awq, M, path):
     # x small integers, power-of-two scales, K = 256: |partial sums| <= 256 * 4 * 255 * 2^-8
     # on a 2^-13 grid (23 bits), so fp32 accumulation is exact on any order and y must be
@@ -113,7 +113,19 @@ def test_gemm_w8_workload_shapes(awq, M, K, N, G):
                  f"w8 M={M} K={K} N={N} G={G}")
 
 
-@pytest.mark.parametrize("M", [1, 24])
+@pytest.mark.parametrize("M,K,N", [(300, 4096, 1024), (512, 4096, 11008), (2048, 11008, 4096),
+                                   (257, 1024, 4112)])
+def test_gemm_w8_prefill_shapes(awq, M, K, N):
+    # the tcgen05 kernel: several row and column tiles, a ragged row tile (M = 257), a ragged
+    # column tile (N = 4112: 16 of the last tile's 128 columns); the oracle on sampled rows
+    d = synth.awq8_linear(14100 + M + K, M, K, N, group_size=128, bias=True)
+    y = run(awq, d)
+    rows = np.unique(np.concatenate([np.random.default_rng(M).integers(0, M, 24), [0, M - 1]]))
+    ref = oracle.gemm8(d["x"][rows], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128)
+    assert_close(y[rows], ref, f"w8 prefill M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("M", [1, 24, 600])
 def test_gemm_w8_deterministic(awq, M):
     d = synth.awq8_linear(13900 + M, M, 4096, 1024, group_size=128, bias=True)
     a, b = run(awq, d), run(awq, d)
@@ -126,12 +138,12 @@ def test_gemm_w8_auto_matches_decode(awq):
     assert np.array_equal(run(awq, d).view(np.uint16), run(awq, d, "decode").view(np.uint16))
 
 
-def test_gemm_w8_refuses_nibble_kernels(awq):
-    # the tcgen05 prefill kernel decodes nibbles; forcing it on 8-bit codes is an error, and
-    # the decode kernel refuses N % 16 != 0 at 8 bits
-    d = synth.awq8_linear(13950, 4, 256, 256, group_size=128)
-    with pytest.raises(Exception):
-        run(awq, d, "prefill")
-    d = synth.awq8_linear(13951, 4, 256, 40, group_size=128)
-    with pytest.raises(Exception):
-        run(awq, d, "decode")
+def test_gemm_w8_tensor_core_contract(awq):
+    # both tensor-core kernels refuse N % 16 != 0 at 8 bits (packed rows must be whole
+    # 16-byte units for the tensor maps); the automatic path then takes the generic kernel
+    d = synth.awq8_linear(13951, 40, 256, 40, group_size=128)
+    for path in ("decode", "prefill"):
+        with pytest.raises(Exception):
+            run(awq, d, path)
+    y = run(awq, d)
+    assert_close(y, oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 128), "w8 N=40")

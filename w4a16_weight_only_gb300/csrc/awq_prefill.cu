@@ -30,6 +30,12 @@
 // columns; N = 256: each CTA loads its own 128 activation rows, no TMA multicast); the
 // even CTA issues the MMAs and commits to both CTAs' barriers, the odd CTA's dequant warps
 // signal readiness with a counted st.async into the even CTA's barrier.
+//
+// 8-bit variant (kBits = 8, fp16, one CTA per tile): the same 128-column tile is 32 packed
+// words a row (byte i of word c = column 4c + i), so the stage's packed tile is 64 rows x
+// 32 words and its zero row 32 words; a dequant thread reads four words of each of its
+// rows, and one byte permute per column pair puts two codes under the 0x6400 exponent
+// (1024 + c, exact) before the same HSUB2 / HMUL2 and the same A-tile chunks.
 #include <mutex>
 
 #include "awq_internal.cuh"
@@ -80,17 +86,17 @@ constexpr unsigned int kStatusPrefillTimeout = 0x2u;
 #define AWQ_PREFILL_PAIR_SA 5
 #endif
 constexpr int A_BYTES = kBN * kBK * 2;       // 16 KB
-constexpr int W_BYTES = kBK * 16 * 4;        // 4 KB
 constexpr int kXRows = kBT;
-template <bool kPair>
+template <bool kPair, int kBits = 4>
 struct Layout {
+  static constexpr int W_BYTES = kBK * (kBN * kBits / 32) * 4;  // packed tile: 4 or 8 KB
   static constexpr int ST = kPair ? AWQ_PREFILL_PAIR_ST : kST;  // TMA ring depth
   static constexpr int SA = kPair ? AWQ_PREFILL_PAIR_SA : kSA;  // dequantized-A ring depth
   static constexpr int X_BYTES = (kPair ? kBT / 2 : kBT) * kBK * 2;  // 16 or 32 KB
   static constexpr int X_OFF = 0;
   static constexpr int A_OFF = X_OFF + ST * X_BYTES;
   static constexpr int W_OFF = A_OFF + SA * A_BYTES;
-  static constexpr int Z_OFF = W_OFF + ST * W_BYTES;  // 128 B per stage
+  static constexpr int Z_OFF = W_OFF + ST * W_BYTES;  // 128 B per stage (16 or 32 words)
   static constexpr int S_OFF = Z_OFF + ST * 128;      // 256 B per stage
   static constexpr int BAR_OFF = S_OFF + ST * 256;
   // barriers: full_t[ST], empty_t[ST], full_a[SA], empty_a[SA], tfull[2], tempty[2], drain
@@ -102,13 +108,15 @@ struct Layout {
 };
 
 // Bytes one CTA's stage copies land: its activation rows, packed tile, zero and scale rows.
-template <bool kPair>
-constexpr uint32_t stage_tx() { return (kPair ? kXRows / 2 : kXRows) * kBK * 2 + W_BYTES + 16 * 4 + 128 * 2; }
+template <bool kPair, int kBits = 4>
+__host__ __device__ constexpr uint32_t stage_tx() {
+  return (kPair ? kXRows / 2 : kXRows) * kBK * 2 + Layout<kPair, kBits>::W_BYTES + (kBN * kBits / 32) * 4 + 128 * 2;
+}
 
 struct __align__(64) PrefillParams {
   CUtensorMap tm_x;  // x [M][K] f16, box {64, 256}, 128B swizzle
-  CUtensorMap tm_w;  // qweight [K][C] u32, box {16, 64}
-  CUtensorMap tm_z;  // qzeros [K/G][C] u32, box {16, 1}
+  CUtensorMap tm_w;  // qweight [K][C] u32, box {16, 64} (8 bits: {32, 64})
+  CUtensorMap tm_z;  // qzeros [K/G][C] u32, box {16, 1} (8 bits: {32, 1})
   CUtensorMap tm_s;  // scales [K/G][N] f16, box {128, 1}
   const __half* bias;
   __half* y;
@@ -265,10 +273,13 @@ __device__ __forceinline__ uint4 lds128p(uint32_t a) {
 
 // kBF: bf16 activations, scales, bias and output; the dequantized A tile is bf16
 // ((c - z) * s rounded once), the MMA kind::f16 with bf16 operands.
-template <bool kPair, bool kBF = false>
+template <bool kPair, bool kBF = false, int kBits = 4>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  static_assert(kBits == 4 || (kBits == 8 && !kBF && !kPair), "8-bit codes: fp16, one CTA per tile");
   constexpr uint32_t kMag = kBF ? 0x43004300u : kMagic;  // 128 (bf16) / 1024 (fp16), both halves
-  using L = Layout<kPair>;
+  constexpr int CPW = 32 / kBits;                        // columns per packed word
+  using L = Layout<kPair, kBits>;
+  constexpr int W_BYTES = L::W_BYTES;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -292,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const bool leader = rank == 0u;
   const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int tstep = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  constexpr int kTileWords = kPair ? 2 * kBN / 8 : kBN / 8;  // packed words per tile
+  constexpr int kTileWords = (kPair ? 2 * kBN : kBN) / CPW;  // packed words per tile
   constexpr int kXR = kPair ? kBT / 2 : kBT;                 // activation rows this CTA loads
 #ifdef AWQ_PREFILL_DEBUG_DECL
   AWQ_PREFILL_DEBUG_DECL
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       bool ok = true;
       for (int tile = tile0; ok && tile < p.tiles; tile += tstep) {
         const int m0 = (tile % p.tiles_t) * kBT + static_cast<int>(rank) * kXR;
-        const int cw0 = (tile / p.tiles_t) * kTileWords + static_cast<int>(rank) * (kBN / 8);
+        const int cw0 = (tile / p.tiles_t) * kTileWords + static_cast<int>(rank) * (kBN / CPW);
         for (int kb = 0; kb < KB; ++kb) {
 #ifdef AWQ_PREFILL_DEBUG_ROLE
           AWQ_PREFILL_DEBUG_ROLE(0, 0);
@@ -369,11 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #endif
           const int k0 = kb * kBK;
           const int grp = k0 / p.G;
-          mbar_arrive_expect_tx(&full_t[s], stage_tx<kPair>());
+          mbar_arrive_expect_tx(&full_t[s], stage_tx<kPair, kBits>());
           tma_load_2d(smem + L::X_OFF + s * L::X_BYTES, &p.tm_x, &full_t[s], k0, m0);
           tma_load_2d(smem + L::W_OFF + s * W_BYTES, &p.tm_w, &full_t[s], cw0, k0);
           tma_load_2d(smem + L::Z_OFF + s * 128, &p.tm_z, &full_t[s], cw0, grp);
-          tma_load_2d(smem + L::S_OFF + s * 256, &p.tm_s, &full_t[s], 8 * cw0, grp);
+          tma_load_2d(smem + L::S_OFF + s * 256, &p.tm_s, &full_t[s], CPW * cw0, grp);
           ++issued;
           if (++s == L::ST) { s = 0; ph ^= 1u; }
         }
@@ -473,12 +484,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         AWQ_PREFILL_DEBUG_ROLE(1, 2);
 #endif
         const uint32_t wb = sbase + L::W_OFF + s * W_BYTES;
+        const uint32_t ab = sbase + L::A_OFF + sa * A_BYTES;
+        if constexpr (kBits == 8) {
+          // words 4cg .. 4cg+3 of rows rp, rp + 32 (128-byte rows: a quarter-warp reads one
+          // whole row), the matching zero words; chunk cw = 2cg + cc is words 2cc, 2cc + 1
+          const uint4 r0 = lds128p(wb + rp * 128 + cg * 16);
+          const uint4 r1 = lds128p(wb + (rp + 32) * 128 + cg * 16);
+          const uint4 z4 = lds128p(sbase + L::Z_OFF + s * 128 + cg * 16);
+          const uint32_t w8[2][4] = {{r0.x, r0.y, r0.z, r0.w}, {r1.x, r1.y, r1.z, r1.w}};
+          const uint32_t zw8[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int cc = c ^ csel;
+            const int cw = 2 * cg + cc;
+            const uint4 s4 = lds128p(sbase + L::S_OFF + s * 256 + cw * 16);
+            const uint32_t sp[4] = {s4.x, s4.y, s4.z, s4.w};  // (s[2j], s[2j+1])
+            // column pair j = bytes (2 (j % 2), +1) of word 2cc + j / 2, as 1024 + code
+            const uint32_t za = cc ? zw8[2] : zw8[0], zb = cc ? zw8[3] : zw8[1];
+            uint32_t zp[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) zp[j] = prmt(j < 2 ? za : zb, kMag, (j & 1) ? 0x7352u : 0x7150u);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const uint32_t wa = cc ? w8[e][2] : w8[e][0], wb2 = cc ? w8[e][3] : w8[e][1];
+              uint32_t v[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t h = prmt(j < 2 ? wa : wb2, kMag, (j & 1) ? 0x7352u : 0x7150u);
+                v[j] = hmul2(hsub2(h, zp[j]), sp[j]);
+              }
+              const int k = rp + 32 * e;
+              const int off = ((cw >> 3) * 8 + (k >> 3)) * 1024 + (k & 7) * 128 +
+                              (((cw & 7) ^ (k & 7)) << 4);
+              sts128(ab + off, v[0], v[1], v[2], v[3]);
+            }
+          }
+        } else {
         const uint2 r0 = lds64p(wb + rp * 64 + cg * 8);
         const uint2 r1 = lds64p(wb + (rp + 32) * 64 + cg * 8);
         const uint2 z2 = lds64p(sbase + L::Z_OFF + s * 128 + cg * 8);
         const uint32_t w[2][2] = {{r0.x, r0.y}, {r1.x, r1.y}};
         const uint32_t zw[2] = {z2.x, z2.y};
-        const uint32_t ab = sbase + L::A_OFF + sa * A_BYTES;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int cc = c ^ csel;
@@ -504,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             sts128(ab + off, v[0], v[1], v[2], v[3]);
           }
         }
+        }  // kBits
         fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) {
@@ -538,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int tile = tile0; tile < p.tiles; tile += tstep, ++li) {
       const int b = li % kAccBufs;
       const int m0 = (tile % p.tiles_t) * kBT;
-      const int n = (tile / p.tiles_t) * (8 * kTileWords) + static_cast<int>(rank) * kBN + nl;
+      const int n = (tile / p.tiles_t) * (CPW * kTileWords) + static_cast<int>(rank) * kBN + nl;
       const float bias = (p.bias != nullptr && n < p.N)
                              ? elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[n])
                              : 0.f;
@@ -581,13 +628,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   }
 }
 
-template <bool kPair, bool kBF = false>
+template <bool kPair, bool kBF = false, int kBits = 4>
 cudaError_t set_smem_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(prefill_kernel<kPair, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(Layout<kPair>::SMEM));
+    err = cudaFuncSetAttribute(prefill_kernel<kPair, kBF, kBits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Layout<kPair, kBits>::SMEM));
   });
   return err;
 }
@@ -619,10 +666,12 @@ int pair_capacity() {
 bool prefill_supported(const GemmProblem& p, const char** why) {
   static const char* dummy;
   if (!why) why = &dummy;
-  if (p.bits != 4) { *why = "4-bit codes only"; return false; }
+  if (p.bits != 4 && p.bits != 8) { *why = "4- or 8-bit codes only"; return false; }
+  if (p.bits == 8 && p.bf16) { *why = "8-bit codes: fp16 only"; return false; }
   if (p.K % kBK != 0) { *why = "prefill needs K % 64 == 0"; return false; }
   if (p.G % kBK != 0) { *why = "prefill needs group_size % 64 == 0"; return false; }
-  if (p.N % 32 != 0) { *why = "prefill needs N % 32 == 0"; return false; }
+  // packed rows a multiple of 16 bytes (tensor-map strides): N % 32 (4 bits), N % 16 (8)
+  if (p.N % (p.bits == 8 ? 16 : 32) != 0) { *why = "prefill needs N % 32 == 0 (N % 16 for 8 bits)"; return false; }
   if (!aligned(p.x, 16) || !aligned(p.qw, 16) || !aligned(p.qz, 16) || !aligned(p.sc, 16)) {
     *why = "prefill needs 16-byte aligned x, qweight, qzeros, scales";
     return false;
@@ -639,23 +688,25 @@ bool prefill_supported(const GemmProblem& p, const char** why) {
 #endif
 
 cudaError_t launch_prefill(const GemmProblem& p) {
-  cudaError_t e = p.bf16 ? set_smem_attr<false, true>() : set_smem_attr<false>();
-  if (e == cudaSuccess && !p.bf16) e = set_smem_attr<true>();
+  const bool w8 = p.bits == 8;
+  cudaError_t e = w8 ? set_smem_attr<false, false, 8>() : p.bf16 ? set_smem_attr<false, true>() : set_smem_attr<false>();
+  if (e == cudaSuccess && !p.bf16 && !w8 && AWQ_PREFILL_PAIR) e = set_smem_attr<true>();
   if (e != cudaSuccess) return e;
   // Pair mode (two CTAs per 256 x 256 tile) when enabled and pairs of SMs can be co-scheduled.
-  const int pairs = (AWQ_PREFILL_PAIR && !p.bf16) ? pair_capacity() : 0;  // pair mode: fp16 only
+  const int pairs = (AWQ_PREFILL_PAIR && !p.bf16 && !w8) ? pair_capacity() : 0;  // pair mode: fp16, 4 bits
   const bool pair = pairs > 0;
   PrefillParams pp;
   const char* why = nullptr;
-  const int C = p.N / 8;
+  const int C = p.N / (w8 ? 4 : 8);
+  const int box_w = kBN / (w8 ? 4 : 8);  // packed words of a tile row
   const int ngrp = p.K / p.G;
   const int x_rows = pair ? kBT / 2 : kBT;
   const CUtensorMapDataType et = p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (!make_tmap_2d(&pp.tm_x, et, 2, p.x, p.K, p.M, kBK, x_rows,
                     CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
-      !make_tmap_2d(&pp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, 16, kBK,
+      !make_tmap_2d(&pp.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qw, C, p.K, box_w, kBK,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
-      !make_tmap_2d(&pp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, 16, 1,
+      !make_tmap_2d(&pp.tm_z, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.qz, C, ngrp, box_w, 1,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why) ||
       !make_tmap_2d(&pp.tm_s, et, 2, p.sc, p.N, ngrp, 128, 1,
                     CU_TENSOR_MAP_SWIZZLE_NONE, &why))
@@ -693,7 +744,8 @@ cudaError_t launch_prefill(const GemmProblem& p) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int grid = pp.tiles < sms ? pp.tiles : sms;
-  if (p.bf16) prefill_kernel<false, true><<<grid, kThreads, Layout<false>::SMEM, p.stream>>>(pp);
+  if (w8) prefill_kernel<false, false, 8><<<grid, kThreads, Layout<false, 8>::SMEM, p.stream>>>(pp);
+  else if (p.bf16) prefill_kernel<false, true><<<grid, kThreads, Layout<false>::SMEM, p.stream>>>(pp);
   else prefill_kernel<false><<<grid, kThreads, Layout<false>::SMEM, p.stream>>>(pp);
   return cudaGetLastError();
 }
