@@ -413,13 +413,21 @@ def run_case(args, local):
     _build.build()
     import w4a16_weight_only_gb300 as awq
     torch.cuda.set_device(local)
-    d = synth.workload_inputs(args.case)
+    import re
+    m8 = re.fullmatch(r"w8_m(\d+)_(\d+)x(\d+)", args.case)
+    if m8:  # 8-bit codes: w8_m<M>_<K>x<N>, G = 128, bias
+        M, K, N = (int(v) for v in m8.groups())
+        d = synth.awq8_linear(5000 + M + K + N, M, K, N, group_size=128, bias=True)
+        gemm = awq.awq_gemm_w8
+    else:
+        d = synth.workload_inputs(args.case)
+        gemm = awq.awq_gemm
     t = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "qweight", "qzeros", "scales")}
     b = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
     y = torch.empty((d["M"], d["N"]), dtype=torch.float16, device="cuda")
     for i in range(args.warmup + args.steps):
-        awq.awq_gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], b, group_size=d["group_size"],
-                     out=y, path=args.path)
+        gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], b, group_size=d["group_size"],
+             out=y, path=args.path)
     torch.cuda.synchronize()
     awq.device_status()
     print(json.dumps({"case": args.case, "path": args.path, "launches": args.warmup + args.steps}))
@@ -703,7 +711,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="profiling mode: run only this workload linear (see synth.WORKLOADS)")
+                    help="profiling mode: run only this workload linear (see synth.WORKLOADS, or "
+                         "w8_m<M>_<K>x<N> for 8-bit codes)")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "prefill", "generic"])
     ap.add_argument("--sweep", action="store_true",
                     help="per-workload table (one JSON line per workload), not the bench line")
