@@ -130,7 +130,12 @@ awq_status_t awq_dequant_bf16(const int32_t* qweight, const int32_t* qzeros, con
  *   qweight int32 [K, N/4], qzeros int32 [K/G, N/4], scales fp16 [K/G, N]
  *   w[k][n] = (code[k][n] - zero[k/G][n]) * scale[k/G][n],  codes 0..255
  *
- * awq_gemm_w8 / awq_gemm_w8_ex: the awq_gemm contract with 8-bit weights (N % 4 == 0);
+ * awq_gemm_w8 / awq_gemm_w8_ex: the awq_gemm contract with 8-bit weights (N % 4 == 0).
+ * The tensor-core families take 8-bit codes when K % 64 == 0, group_size % 64 == 0,
+ * N % 16 == 0 and x, qweight, qzeros, scales are 16-byte aligned (AWQ_PATH_DECODE for any
+ * M, chosen for M <= 32; AWQ_PATH_PREFILL, chosen above); everything else runs
+ * AWQ_PATH_GENERIC.  Forcing a family whose contract the shape breaks returns
+ * AWQ_ERR_UNSUPPORTED_SHAPE.  (awq_gemm_select_path describes 4-bit calls only.)
  * awq_dequant_w8: the awq_dequant contract (exact fp32, or one rounding to fp16).
  */
 awq_status_t awq_gemm_w8_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
