@@ -703,6 +703,47 @@ def run_quantize_sweep(awq, timed, hbm, hbm_kind):
         torch.cuda.empty_cache()
 
 
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def run_cpu_oracle(args):
+    """CPU oracle table (no GPU): the C oracle's dequant and fp64 linear on every workload
+    shape (synth.WORKLOADS; --configs selects), timed in full, one JSON line per shape.
+    Threads: OpenMP's default (all host cores) unless OMP_NUM_THREADS says otherwise; the
+    dequant is single-threaded by construction."""
+    from oracle import c_oracle
+    c_oracle.build()
+    cfgs = {int(c) for c in args.configs.split(",")} if args.configs else None
+    threads = int(os.environ.get("OMP_NUM_THREADS", "0")) or os.cpu_count()
+    model = cpu_model()
+    for (cfg, idx, name, M, K, N, G, bias) in synth.WORKLOADS:
+        if cfgs is not None and cfg not in cfgs:
+            continue
+        d = synth.workload_inputs(name)
+        args_ = (d["qweight"], d["qzeros"], d["scales"], G)
+        t0 = time.perf_counter()
+        c_oracle.dequant_f32(*args_)
+        t_dq = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        c_oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+        t_gemm = time.perf_counter() - t0
+        print(json.dumps({"workload": name, "config": cfg, "M": M, "K": K, "N": N, "group_size": G,
+                          "kind": "C oracle", "dequant_s": t_dq,
+                          "linear_s": t_gemm, "linear_includes_dequant": True,
+                          "GB_s": step_bytes([d]) / t_gemm / 1e9,
+                          "GFLOP_s": 2.0 * M * N * K / t_gemm / 1e9,
+                          "threads": threads, "cores": os.cpu_count(), "cpu": model}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -716,7 +757,13 @@ def main(argv=None):
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "prefill", "generic"])
     ap.add_argument("--sweep", action="store_true",
                     help="per-workload table (one JSON line per workload), not the bench line")
+    ap.add_argument("--cpu-oracle", action="store_true",
+                    help="time the C oracle (dequant, fp64 linear) on every workload shape; no GPU")
+    ap.add_argument("--configs", default=None, help="--cpu-oracle: comma-separated config indices")
     args = ap.parse_args(argv)
+    if args.cpu_oracle:
+        run_cpu_oracle(args)
+        return
     rank, world, local = dist_setup(args)
     if args.sweep:
         run_sweep(args, local)
