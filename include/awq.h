@@ -55,7 +55,10 @@ typedef enum awq_status {
 
 typedef enum awq_dtype { AWQ_DTYPE_F16 = 0, AWQ_DTYPE_F32 = 1, AWQ_DTYPE_BF16 = 2 } awq_dtype_t;
 
-/* Kernel family used by awq_gemm_ex.  AUTO picks by M, K, N, G and alignment. */
+/* Kernel family used by awq_gemm_ex.  AUTO picks by M, K, N, G and alignment: decode for
+ * M <= 32; above that, when both tensor-core families take the shape, whichever a cost
+ * model fitted to GB300 timings predicts faster (decode's 32-row tiles win up to M = 64 ..
+ * 192 depending on N and K); else the family whose contract holds, else generic. */
 typedef enum awq_path {
   AWQ_PATH_AUTO = 0,
   AWQ_PATH_DECODE = 1,   /* split-K streaming kernel for small M (tensor-core m16n8k16) */
@@ -132,8 +135,8 @@ awq_status_t awq_dequant_bf16(const int32_t* qweight, const int32_t* qzeros, con
  *
  * awq_gemm_w8 / awq_gemm_w8_ex: the awq_gemm contract with 8-bit weights (N % 4 == 0).
  * The tensor-core families take 8-bit codes when K % 64 == 0, group_size % 64 == 0,
- * N % 16 == 0 and x, qweight, qzeros, scales are 16-byte aligned (AWQ_PATH_DECODE for any
- * M, chosen for M <= 32; AWQ_PATH_PREFILL, chosen above); everything else runs
+ * N % 16 == 0 and x, qweight, qzeros, scales are 16-byte aligned (AWQ_PATH_DECODE and
+ * AWQ_PATH_PREFILL for any M, chosen as for 4-bit codes); everything else runs
  * AWQ_PATH_GENERIC.  Forcing a family whose contract the shape breaks returns
  * AWQ_ERR_UNSUPPORTED_SHAPE.  (awq_gemm_select_path describes 4-bit calls only.)
  * awq_dequant_w8: the awq_dequant contract (exact fp32, or one rounding to fp16).
@@ -245,8 +248,9 @@ awq_status_t awq_gemm_ex(const void* x_f16, const int32_t* qweight, const int32_
                          int64_t M, int64_t K, int64_t N, int64_t group_size,
                          void* y_f16, awq_path_t path, awq_stream_t stream);
 
-/* The family awq_gemm would pick for this shape and these pointers (no launch, no
- * device access).  Returns AWQ_PATH_AUTO (0) on an invalid shape. */
+/* The family awq_gemm would pick for this shape and these pointers (no launch; above
+ * 32 rows it reads the current device's SM count, 152 if there is none).  Returns
+ * AWQ_PATH_AUTO (0) on an invalid shape. */
 awq_path_t awq_gemm_select_path(int64_t M, int64_t K, int64_t N, int64_t group_size,
                                 const void* x_f16, const int32_t* qweight,
                                 const int32_t* qzeros, const void* scales_f16,

@@ -228,3 +228,28 @@ def test_workload_parity(awq, name):
         rows, cols = _sample(M, N, rng)
         assert_close(y[rows, cols], oracle.gemm_sampled(*args, rows, cols), name)
     assert np.all(np.isfinite(y.astype(np.float32)))
+
+
+@pytest.mark.parametrize("M", [33, 64, 100, 192, 256])
+@pytest.mark.parametrize("path", ["auto", "decode", "prefill"])
+def test_medium_batch_both_families(awq, M, path):
+    # 33..256 rows: both tensor-core kernels take the shape (decode in several 32-row tiles,
+    # prefill in one row tile); the automatic choice between them is a cost model
+    d = synth.awq_linear(15000 + M, M, 4096, 1024, group_size=128, bias=True)
+    y = run_gemm(awq, d, path)
+    assert_close(y, oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128),
+                 f"M={M} {path}")
+
+
+@pytest.mark.parametrize("M,K,N,want", [(64, 4096, 4096, "decode"), (192, 4096, 4096, "decode"),
+                                        (512, 4096, 4096, "prefill"), (64, 4096, 11008, "decode"),
+                                        (128, 4096, 11008, "prefill"), (192, 11008, 4096, "decode"),
+                                        (512, 11008, 4096, "prefill"), (2048, 4096, 11008, "prefill")])
+def test_automatic_family_choice(awq, M, K, N, want):
+    # the measured crossovers the cost model was fitted to (152 SMs)
+    x = torch.empty((M, K), dtype=torch.float16, device="cuda")
+    qw = torch.empty((K, N // 8), dtype=torch.int32, device="cuda")
+    qz = torch.empty((K // 128, N // 8), dtype=torch.int32, device="cuda")
+    sc = torch.empty((K // 128, N), dtype=torch.float16, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    assert awq.select_path(x, qw, qz, sc, None, 128, y) == want

@@ -109,10 +109,40 @@ awq_status_t build_problem(const void* x, const int32_t* qweight, const int32_t*
   return AWQ_OK;
 }
 
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    (void)cudaGetLastError();
+    return 152;
+  }
+  return sms;
+}
+
+// Above 32 rows both tensor-core families can run; the estimates below (microseconds,
+// fitted to GB300 timings of both kernels on the 7B and 70B linears at M = 33 .. 512)
+// pick the faster.  Decode: the first 32-row tile streams the weights (about 3 TB/s plus
+// 8 us of launch chain), each further 32-row tile costs 0.25 ns per code (its unpack and
+// MMAs; the weights come from L2).  Prefill: waves of 128 x 256 tiles over the SMs, about
+// 0.5 us per 64-deep K stage.
+bool prefill_faster(const awq::GemmProblem& p) {
+  const double kn = static_cast<double>(p.K) * static_cast<double>(p.N);
+  const double weight_bytes = kn * p.bits / 8.0 + 3.0 * static_cast<double>(p.K / p.G) * p.N;
+  const double row_tiles = static_cast<double>((p.M + 31) / 32);
+  const double decode_us = weight_bytes / 3.0e6 + 8.0 + (row_tiles - 1.0) * kn * 2.5e-7;
+  const long long sms = sm_count();
+  const long long tiles = ((p.N + 127) / 128) * ((p.M + 255) / 256);
+  const double prefill_us = static_cast<double>((tiles + sms - 1) / sms) * (p.K / 64) * 0.5 + 2.0;
+  return prefill_us < decode_us;
+}
+
 awq::Path choose_path(const awq::GemmProblem& p) {
-  if (p.M <= 32 && awq::decode_supported(p, nullptr)) return awq::kDecode;
-  if (awq::prefill_supported(p, nullptr)) return awq::kPrefill;
-  if (awq::decode_supported(p, nullptr)) return awq::kDecode;
+  const bool dec = awq::decode_supported(p, nullptr);
+  if (p.M <= 32 && dec) return awq::kDecode;
+  const bool pre = awq::prefill_supported(p, nullptr);
+  if (pre && dec) return prefill_faster(p) ? awq::kPrefill : awq::kDecode;
+  if (pre) return awq::kPrefill;
+  if (dec) return awq::kDecode;
   return awq::kGeneric;
 }
 
