@@ -253,3 +253,27 @@ def test_automatic_family_choice(awq, M, K, N, want):
     sc = torch.empty((K // 128, N), dtype=torch.float16, device="cuda")
     y = torch.empty((M, N), dtype=torch.float16, device="cuda")
     assert awq.select_path(x, qw, qz, sc, None, 128, y) == want
+
+
+# narrow-tile prefill (32/64/128-row token tiles; K split over clusters of 4, 2 or 1 CTAs by
+# tile count): 4096 x 4096 at 32 and 64 rows (4-way split), 11008 x 4096 at 128 rows (2-way),
+# K = 4160 (65 stages: an uneven 4-way split), 4096 x 11008 (no split), one row
+@pytest.mark.parametrize("M,K,N", [(32, 4096, 4096), (64, 4096, 4096), (128, 11008, 4096),
+                                   (17, 4160, 1024), (100, 4096, 11008), (1, 1024, 512)])
+def test_prefill_narrow_tiles(awq, M, K, N):
+    d = synth.awq_linear(16000 + M + K, M, K, N, group_size=64, bias=True)
+    y = run_gemm(awq, d, "prefill")
+    assert_close(y, oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 64),
+                 f"narrow prefill M={M} K={K} N={N}")
+    assert np.array_equal(run_gemm(awq, d, "prefill").view(np.uint16), y.view(np.uint16))
+
+
+@pytest.mark.parametrize("M", [32, 64, 128])
+def test_prefill_narrow_tiles_exact_bitwise(awq, M):
+    # exact-arithmetic inputs: the split partial sums are exact in fp32, so y is the oracle's
+    # value rounded once to fp16 whatever the split
+    d = synth.awq_linear(16500 + M, M, 4096, 1024, group_size=128, bias=True, x_kind="smallint",
+                         scale_kind="pow2", bias_kind="dyadic")
+    y = run_gemm(awq, d, "prefill")
+    want = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), want.view(np.uint16))

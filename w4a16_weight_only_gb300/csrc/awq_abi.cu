@@ -119,21 +119,17 @@ int sm_count() {
   return sms;
 }
 
-// Above 32 rows both tensor-core families can run; the estimates below (microseconds,
-// fitted to GB300 timings of both kernels on the 7B and 70B linears at M = 33 .. 512)
-// pick the faster.  Decode: the first 32-row tile streams the weights (about 3 TB/s plus
-// 8 us of launch chain), each further 32-row tile costs 0.25 ns per code (its unpack and
-// MMAs; the weights come from L2).  Prefill: waves of 128 x 256 tiles over the SMs, about
-// 0.5 us per 64-deep K stage.
+// Above 32 rows both tensor-core families can run; estimates fitted to GB300 timings of
+// both kernels on the 7B and 70B linears at M = 8 .. 512 pick the faster.  Decode: the
+// first 32-row tile streams the weights (about 3 TB/s plus 8 us of launch chain), each
+// further 32-row tile costs 0.25 ns per code (its unpack and MMAs; the weights come from
+// L2).  Prefill: the estimate of the plan it would launch (awq_prefill.cu).
 bool prefill_faster(const awq::GemmProblem& p) {
   const double kn = static_cast<double>(p.K) * static_cast<double>(p.N);
   const double weight_bytes = kn * p.bits / 8.0 + 3.0 * static_cast<double>(p.K / p.G) * p.N;
   const double row_tiles = static_cast<double>((p.M + 31) / 32);
   const double decode_us = weight_bytes / 3.0e6 + 8.0 + (row_tiles - 1.0) * kn * 2.5e-7;
-  const long long sms = sm_count();
-  const long long tiles = ((p.N + 127) / 128) * ((p.M + 255) / 256);
-  const double prefill_us = static_cast<double>((tiles + sms - 1) / sms) * (p.K / 64) * 0.5 + 2.0;
-  return prefill_us < decode_us;
+  return awq::prefill_estimate_us(p, sm_count()) < decode_us;
 }
 
 awq::Path choose_path(const awq::GemmProblem& p) {

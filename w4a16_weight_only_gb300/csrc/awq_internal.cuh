@@ -79,6 +79,8 @@ cudaError_t status_word_ptr(unsigned int** ptr);
 
 // tcgen05/TMEM kernel for large M.
 bool prefill_supported(const GemmProblem& p, const char** why);
+// Estimated duration (us) of launch_prefill for p on a device with `sms` SMs.
+double prefill_estimate_us(const GemmProblem& p, int sms);
 cudaError_t launch_prefill(const GemmProblem& p);
 
 // Failure-detection self test: a bounded wait that nothing completes (see awq.h).

@@ -36,6 +36,7 @@
 // 32 words and its zero row 32 words; a dequant thread reads four words of each of its
 // rows, and one byte permute per column pair puts two codes under the 0x6400 exponent
 // (1024 + c, exact) before the same HSUB2 / HMUL2 and the same A-tile chunks.
+#include <algorithm>
 #include <mutex>
 
 #include "awq_internal.cuh"
@@ -63,6 +64,14 @@ constexpr int kBT = AWQ_PREFILL_BT;   // activation rows per tile (UMMA N)
 constexpr int kBK = 64;    // K per stage
 constexpr int kST = AWQ_PREFILL_ST;  // TMA ring depth
 constexpr int kSA = AWQ_PREFILL_SA;  // dequantized-A ring depth
+#ifndef AWQ_PREFILL_SMALL_ST
+#define AWQ_PREFILL_SMALL_ST 8
+#endif
+constexpr int kSTsmall = AWQ_PREFILL_SMALL_ST;  // TMA ring depth of the narrow token tiles
+#ifndef AWQ_PREFILL_SMALL_SA
+#define AWQ_PREFILL_SMALL_SA 8
+#endif
+constexpr int kSAsmall = AWQ_PREFILL_SMALL_SA;  // dequantized-A ring depth of the narrow tiles
 constexpr int kDQ = 8;                        // dequant warps
 constexpr int kThreads = (2 + kDQ + 4) * 32;  // producer, MMA, dequant, epilogue
 #ifndef AWQ_PREFILL_ACC_BUFS
@@ -86,31 +95,46 @@ constexpr unsigned int kStatusPrefillTimeout = 0x2u;
 #define AWQ_PREFILL_PAIR_SA 5
 #endif
 constexpr int A_BYTES = kBN * kBK * 2;       // 16 KB
-constexpr int kXRows = kBT;
-template <bool kPair, int kBits = 4>
+// Narrow token tiles (BT < 256) keep one dequantized-A slot fewer, so that two CTAs fit on
+// an SM; split-K launches (SPLIT > 1) add the receive area of the cluster's partial sums.
+template <bool kPair, int kBits = 4, int BT = kBT, int SPLIT = 1>
 struct Layout {
   static constexpr int W_BYTES = kBK * (kBN * kBits / 32) * 4;  // packed tile: 4 or 8 KB
-  static constexpr int ST = kPair ? AWQ_PREFILL_PAIR_ST : kST;  // TMA ring depth
-  static constexpr int SA = kPair ? AWQ_PREFILL_PAIR_SA : kSA;  // dequantized-A ring depth
-  static constexpr int X_BYTES = (kPair ? kBT / 2 : kBT) * kBK * 2;  // 16 or 32 KB
+  static constexpr int X_BYTES = (kPair ? BT / 2 : BT) * kBK * 2;  // 4 .. 32 KB
+  // narrow tiles: the receive area first, then as deep a dequantized-A ring as fits beside
+  // a 4-stage TMA ring (at most kSAsmall), then as deep a TMA ring as fits (at most kSTsmall)
+  static constexpr int kBudget = 227 * 1024 - 2048 - (SPLIT - 1) * kBN * (BT + 4) * 4;
+  static constexpr int SA_FIT = (kBudget - 4 * (X_BYTES + W_BYTES + 384)) / (kBN * kBK * 2);
+  static constexpr int SA = kPair ? AWQ_PREFILL_PAIR_SA
+                                  : (BT < kBT ? (SA_FIT < kSAsmall ? SA_FIT : kSAsmall) : kSA);  // dequantized-A ring depth
+  static_assert(SA >= 2, "dequantized-A ring");
+  static constexpr int ST_FIT = (kBudget - SA * kBN * kBK * 2) / (X_BYTES + W_BYTES + 384);
+  static constexpr int ST = kPair ? AWQ_PREFILL_PAIR_ST
+                                  : (BT < kBT ? (ST_FIT < kSTsmall ? ST_FIT : kSTsmall) : kST);  // TMA ring depth
+  static_assert(ST >= 2, "TMA ring");
   static constexpr int X_OFF = 0;
   static constexpr int A_OFF = X_OFF + ST * X_BYTES;
   static constexpr int W_OFF = A_OFF + SA * A_BYTES;
   static constexpr int Z_OFF = W_OFF + ST * W_BYTES;  // 128 B per stage (16 or 32 words)
   static constexpr int S_OFF = Z_OFF + ST * 128;      // 256 B per stage
   static constexpr int BAR_OFF = S_OFF + ST * 256;
-  // barriers: full_t[ST], empty_t[ST], full_a[SA], empty_a[SA], tfull[2], tempty[2], drain
-  static constexpr int NBARS = 2 * ST + 2 * SA + 4 + 1;
+  // barriers: full_t[ST], empty_t[ST], full_a[SA], empty_a[SA], tfull[2], tempty[2], drain, recv
+  static constexpr int NBARS = 2 * ST + 2 * SA + 4 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base (u32), abort flag (u32)
   static constexpr int SIG_OFF = MISC_OFF + 16;         // pair: targets of the peer's signals
-  static constexpr size_t SMEM = 1024 + SIG_OFF + 64;
+  // split-K: rank 0 receives ranks 1 .. SPLIT-1's fp32 partials, [rank - 1][column][token],
+  // rows padded by 4 floats (odd multiples of 16 bytes: conflict-free 128-bit reads)
+  static constexpr int RECV_PITCH = BT + 4;
+  static constexpr int RECV_OFF = ((SIG_OFF + 64 + 15) / 16) * 16;
+  static constexpr int RECV_BYTES = (SPLIT - 1) * kBN * RECV_PITCH * 4;
+  static constexpr size_t SMEM = 1024 + RECV_OFF + RECV_BYTES;
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 // Bytes one CTA's stage copies land: its activation rows, packed tile, zero and scale rows.
-template <bool kPair, int kBits = 4>
+template <bool kPair, int kBits = 4, int BT = kBT>
 __host__ __device__ constexpr uint32_t stage_tx() {
-  return (kPair ? kXRows / 2 : kXRows) * kBK * 2 + Layout<kPair, kBits>::W_BYTES + (kBN * kBits / 32) * 4 + 128 * 2;
+  return (kPair ? BT / 2 : BT) * kBK * 2 + Layout<kPair, kBits>::W_BYTES + (kBN * kBits / 32) * 4 + 128 * 2;
 }
 
 struct __align__(64) PrefillParams {
@@ -147,9 +171,12 @@ constexpr uint32_t kA_SBO = 1024;      // between 8-row K groups
 
 // Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B, A MN-major, B K-major,
 // N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (1u << 15) | (0u << 16) |
-                            (static_cast<uint32_t>(kBT >> 3) << 17) |
-                            (static_cast<uint32_t>(kBN >> 4) << 24);
+template <int BT>
+__host__ __device__ constexpr uint32_t idesc_n() {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (1u << 15) | (0u << 16) |
+         (static_cast<uint32_t>(BT >> 3) << 17) | (static_cast<uint32_t>(kBN >> 4) << 24);
+}
+constexpr uint32_t kIdesc = idesc_n<kBT>();
 
 // Pair mode (cta_group::2): the MMA spans the two CTAs of a cluster, M = 256 (128 A rows
 // from each CTA's shared memory), N = 256 (128 B rows from each); every CTA's TMEM holds
@@ -159,7 +186,7 @@ constexpr uint32_t kIdescPair = (kIdesc & ~(0x1Fu << 24)) | (static_cast<uint32_
 // kind::f16 with bf16 A and B: formats 1 in the A and B format fields (bits 7-9, 10-12).
 constexpr uint32_t kIdescBF16 = (1u << 7) | (1u << 10);
 
-template <bool kPair, bool kBF = false>
+template <bool kPair, bool kBF = false, int BT = kBT>
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                         uint32_t accumulate) {
   if constexpr (kPair) {
@@ -174,7 +201,7 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc | (kBF ? kIdescBF16 : 0u)), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(idesc_n<BT>() | (kBF ? kIdescBF16 : 0u)), "r"(accumulate)
         : "memory");
   }
 }
@@ -231,6 +258,20 @@ __device__ __forceinline__ void mbar_arrive_rank(uint64_t* local, uint32_t rank)
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
 }
 
+// Cluster-window address of `local`'s offset in CTA `rank`, and an asynchronous 16-byte
+// store to such an address whose bytes complete on the (cluster-window) mbarrier `rbar`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  return ra;
+}
+__device__ __forceinline__ void st_async_v4_at(uint32_t raddr, uint32_t rbar, uint32_t a, uint32_t b,
+                                               uint32_t c, uint32_t d) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
+               : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
@@ -273,12 +314,22 @@ __device__ __forceinline__ uint4 lds128p(uint32_t a) {
 
 // kBF: bf16 activations, scales, bias and output; the dequantized A tile is bf16
 // ((c - z) * s rounded once), the MMA kind::f16 with bf16 operands.
-template <bool kPair, bool kBF = false, int kBits = 4>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+// BT: activation rows per tile (UMMA N = BT).  SPLIT > 1: a cluster of SPLIT CTAs shares
+// one tile, CTA r taking K stages [r KB / SPLIT, (r + 1) KB / SPLIT); ranks 1 .. SPLIT-1
+// push their fp32 accumulators into rank 0's receive area (st.async, counted on rank 0's
+// recv barrier), and rank 0 adds them in rank order, adds the bias and stores y.  Split
+// launches give every cluster exactly one tile.
+template <bool kPair, bool kBF = false, int kBits = 4, int BT = kBT, int SPLIT = 1>
+__global__ void __launch_bounds__(kThreads, BT < kBT ? 2 : 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   static_assert(kBits == 4 || (kBits == 8 && !kBF && !kPair), "8-bit codes: fp16, one CTA per tile");
+  static_assert(SPLIT == 1 || !kPair, "split-K launches use one CTA per tile share");
+  static_assert(BT % 32 == 0 && BT >= 32 && BT <= 256 && (kPair ? BT == kBT : true), "token tile");
+  // TMEM columns allocated (a power of two, at least 32): kAccBufs accumulators of BT
+  constexpr int kCols = kAccBufs * BT <= 32 ? 32 : kAccBufs * BT <= 64 ? 64 : kAccBufs * BT <= 128 ? 128
+                                            : kAccBufs * BT <= 256 ? 256 : 512;
   constexpr uint32_t kMag = kBF ? 0x43004300u : kMagic;  // 128 (bf16) / 1024 (fp16), both halves
   constexpr int CPW = 32 / kBits;                        // columns per packed word
-  using L = Layout<kPair, kBits>;
+  using L = Layout<kPair, kBits, BT, SPLIT>;
   constexpr int W_BYTES = L::W_BYTES;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -292,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* tfull = bars + 2 * L::ST + 2 * L::SA;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
+  uint64_t* recv_bar = drain + 1;  // split-K: rank 0's partials received
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::MISC_OFF);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::MISC_OFF + 4);
 
@@ -301,10 +353,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   // Pair mode: the cluster's two CTAs share each tile; rank 0 (the leader) issues the MMAs.
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0u;
-  const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int tstep = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // Split-K: this CTA's share of the tile's K stages.
+  const uint32_t krank = SPLIT > 1 ? cluster_ctarank() : 0u;
+  const int kb0 = static_cast<int>(static_cast<long long>(KB) * krank / SPLIT);
+  const int kb1 = static_cast<int>(static_cast<long long>(KB) * (krank + 1) / SPLIT);
+  const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1)
+                          : static_cast<int>(blockIdx.x) / SPLIT;
+  const int tstep = kPair ? static_cast<int>(gridDim.x >> 1)
+                          : static_cast<int>(gridDim.x) / SPLIT;
   constexpr int kTileWords = (kPair ? 2 * kBN : kBN) / CPW;  // packed words per tile
-  constexpr int kXR = kPair ? kBT / 2 : kBT;                 // activation rows this CTA loads
+  constexpr int kXR = kPair ? BT / 2 : BT;                   // activation rows this CTA loads
 #ifdef AWQ_PREFILL_DEBUG_DECL
   AWQ_PREFILL_DEBUG_DECL
 #endif
@@ -324,24 +382,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(&tempty[b], kPair ? 8 : 4);          // epilogue warps (of both CTAs)
     }
     mbar_init(drain, 1);
+    mbar_init(recv_bar, 1);
+    if (SPLIT > 1 && krank == 0u)  // the partials of ranks 1 .. SPLIT-1, one phase
+      mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((SPLIT - 1) * kBN * BT * 4));
     *abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
     if constexpr (kPair) {  // one warp of each CTA of the pair, collectively
       asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                       smem_u32(const_cast<uint32_t*>(tmem_slot))), "n"(kTmemCols)
+                       smem_u32(const_cast<uint32_t*>(tmem_slot))), "n"(kCols)
                    : "memory");
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     } else {
       asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                       smem_u32(const_cast<uint32_t*>(tmem_slot))), "n"(kTmemCols)
+                       smem_u32(const_cast<uint32_t*>(tmem_slot))), "n"(kCols)
                    : "memory");
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
   }
   __syncthreads();
-  if constexpr (kPair) cluster_sync_all();  // both CTAs' barriers exist before any remote use
+  if constexpr (kPair || SPLIT > 1) cluster_sync_all();  // the cluster's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -368,9 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       int issued = 0;
       bool ok = true;
       for (int tile = tile0; ok && tile < p.tiles; tile += tstep) {
-        const int m0 = (tile % p.tiles_t) * kBT + static_cast<int>(rank) * kXR;
+        const int m0 = (tile % p.tiles_t) * BT + static_cast<int>(rank) * kXR;
         const int cw0 = (tile / p.tiles_t) * kTileWords + static_cast<int>(rank) * (kBN / CPW);
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
 #ifdef AWQ_PREFILL_DEBUG_ROLE
           AWQ_PREFILL_DEBUG_ROLE(0, 0);
 #endif
@@ -380,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #endif
           const int k0 = kb * kBK;
           const int grp = k0 / p.G;
-          mbar_arrive_expect_tx(&full_t[s], stage_tx<kPair, kBits>());
+          mbar_arrive_expect_tx(&full_t[s], stage_tx<kPair, kBits, BT>());
           tma_load_2d(smem + L::X_OFF + s * L::X_BYTES, &p.tm_x, &full_t[s], k0, m0);
           tma_load_2d(smem + L::W_OFF + s * W_BYTES, &p.tm_w, &full_t[s], cw0, k0);
           tma_load_2d(smem + L::Z_OFF + s * 128, &p.tm_z, &full_t[s], cw0, grp);
@@ -422,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         AWQ_PREFILL_DEBUG_WAIT(1);
 #endif
         tc_fence_after();
-        const uint32_t d = tmem_base + static_cast<uint32_t>(b * kBT);
-        for (int kb = 0; kb < KB; ++kb) {
+        const uint32_t d = tmem_base + static_cast<uint32_t>(b * BT);
+        for (int kb = kb0; kb < kb1; ++kb) {
 #ifdef AWQ_PREFILL_DEBUG_WAIT
           AWQ_PREFILL_DEBUG_WAIT(2);
           AWQ_PREFILL_DEBUG_WAIT(3);
@@ -439,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const uint64_t bdesc = sw128_desc(sbase + L::X_OFF + s * L::X_BYTES, 16u, 1024u);
 #pragma unroll
           for (int ks = 0; ks < kBK / 16; ++ks)  // K += 16: A two atoms (2048 B), B 32 B
-            mma_f16<kPair, kBF>(d, adesc + (2u * kA_SBO >> 4) * ks, bdesc + 2 * ks, (kb > 0 || ks > 0) ? 1u : 0u);
+            mma_f16<kPair, kBF, BT>(d, adesc + (2u * kA_SBO >> 4) * ks, bdesc + 2 * ks, (kb > kb0 || ks > 0) ? 1u : 0u);
           any = true;
           mma_commit<kPair>(&empty_t[s]);
           mma_commit<kPair>(&empty_a[sa]);
@@ -471,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint32_t ph = 0, pha = 0;
     bool ok = true;
     for (int tile = tile0; ok && tile < p.tiles; tile += tstep) {
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
 #ifdef AWQ_PREFILL_DEBUG_ROLE
         AWQ_PREFILL_DEBUG_ROLE(1, 0);
 #endif
@@ -584,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     int li = 0;
     for (int tile = tile0; tile < p.tiles; tile += tstep, ++li) {
       const int b = li % kAccBufs;
-      const int m0 = (tile % p.tiles_t) * kBT;
+      const int m0 = (tile % p.tiles_t) * BT;
       const int n = (tile / p.tiles_t) * (CPW * kTileWords) + static_cast<int>(rank) * kBN + nl;
       const float bias = (p.bias != nullptr && n < p.N)
                              ? elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(p.bias)[n])
@@ -592,9 +653,53 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       if (!wait(&tfull[b], static_cast<uint32_t>((li / kAccBufs) & 1))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                             static_cast<uint32_t>(b * kBT);
+                             static_cast<uint32_t>(b * BT);
+      if constexpr (SPLIT > 1) {
+        float* recv = reinterpret_cast<float*>(smem + L::RECV_OFF);
+        if (krank != 0u) {
+          // this share's partial sums of column nl, all BT tokens, into rank 0
+          const uint32_t rbar = cluster_addr(recv_bar, 0u);
+          const uint32_t rdst = cluster_addr(recv + (static_cast<int>(krank - 1) * kBN + nl) * L::RECV_PITCH, 0u);
 #pragma unroll 1
-      for (int c = 0; c < kBT / 32; ++c) {
+          for (int c = 0; c < BT / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              st_async_v4_at(rdst + static_cast<uint32_t>((c * 32 + j) * 4), rbar, v[j], v[j + 1], v[j + 2], v[j + 3]);
+          }
+        } else {
+          if (!wait_cl(recv_bar, 0u)) break;
+#pragma unroll 1
+          for (int c = 0; c < BT / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+            for (int r = 1; r < SPLIT; ++r) {  // rank order, summed in place
+              const float* src = recv + ((r - 1) * kBN + nl) * L::RECV_PITCH + c * 32;
+#pragma unroll
+              for (int j = 0; j < 32; j += 4) {
+                const float4 q4 = *reinterpret_cast<const float4*>(src + j);
+                v[j] = __float_as_uint(__uint_as_float(v[j]) + q4.x);
+                v[j + 1] = __float_as_uint(__uint_as_float(v[j + 1]) + q4.y);
+                v[j + 2] = __float_as_uint(__uint_as_float(v[j + 2]) + q4.z);
+                v[j + 3] = __float_as_uint(__uint_as_float(v[j + 3]) + q4.w);
+              }
+            }
+            const int t0 = m0 + c * 32;
+            if (n < p.N) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (t0 + j < p.M)
+                  reinterpret_cast<uint16_t*>(p.y)[(long long)(t0 + j) * p.N + n] =
+                      float_to_elem<kBF>(__uint_as_float(v[j]) + bias);
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+      for (int c = 0; c < BT / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(taddr + c * 32, v);
         const int t0 = m0 + c * 32;
@@ -607,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           }
         }
       }
+      }  // SPLIT
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -616,25 +722,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
   }
 
+  // Split-K: rank 0 leaves only once the other ranks' pushes have landed (bounded: after a
+  // give-up elsewhere they may never come).
+  if (SPLIT > 1 && krank == 0u && threadIdx.x == 0)
+    (void)mbar_wait_cluster_bounded(recv_bar, 0u, p.status, kStatusPrefillTimeout, kWaitLimitNs);
   __syncthreads();
-  // Pair mode: neither CTA leaves while the other may still arrive on its barriers.
-  if constexpr (kPair) cluster_sync_all();
+  // Pair mode: neither CTA leaves while the other may still arrive on its barriers; split
+  // mode: nor while its pushes into rank 0 may be in flight.
+  if constexpr (kPair || SPLIT > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     if constexpr (kPair)
-      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols) : "memory");
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kCols) : "memory");
     else
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols) : "memory");
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kCols) : "memory");
   }
 }
 
-template <bool kPair, bool kBF = false, int kBits = 4>
+template <bool kPair, bool kBF = false, int kBits = 4, int BT = kBT, int SPLIT = 1>
 cudaError_t set_smem_attr() {
   static std::once_flag once;
   static cudaError_t err = cudaSuccess;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(prefill_kernel<kPair, kBF, kBits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(Layout<kPair, kBits>::SMEM));
+    err = cudaFuncSetAttribute(prefill_kernel<kPair, kBF, kBits, BT, SPLIT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(Layout<kPair, kBits, BT, SPLIT>::SMEM));
+    if (err == cudaSuccess && SPLIT > 1)
+      err = cudaFuncSetAttribute(prefill_kernel<kPair, kBF, kBits, BT, SPLIT>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   return err;
 }
@@ -687,8 +802,143 @@ bool prefill_supported(const GemmProblem& p, const char** why) {
 #define AWQ_PREFILL_PAIR 0
 #endif
 
+namespace {
+
+// CTAs of a narrow-tile launch that are resident on the device at once (occupancy API;
+// whole clusters for split launches); cached.  At most two CTAs of this kernel share an SM
+// (registers), so the TMEM they allocate (at most 256 columns each for BT <= 128) never
+// exceeds the SM's 512 columns and tcgen05.alloc never waits on another CTA.
+template <int BT, int SPLIT>
+int small_capacity() {
+  static std::once_flag once;
+  static int cap = 0;
+  std::call_once(once, [] {
+    if (set_smem_attr<false, false, 4, BT, SPLIT>() != cudaSuccess) { (void)cudaGetLastError(); return; }
+    auto kern = prefill_kernel<false, false, 4, BT, SPLIT>;
+    const size_t smem = Layout<false, 4, BT, SPLIT>::SMEM;
+    if (SPLIT == 1) {
+      int dev = 0, sms = 0, per_sm = 0;
+      if (cudaGetDevice(&dev) == cudaSuccess &&
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) == cudaSuccess)
+        cap = per_sm * sms;
+    } else {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(SPLIT, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = SPLIT;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess) cap = clusters * SPLIT;
+    }
+    (void)cudaGetLastError();
+  });
+  return cap;
+}
+
+template <int BT, int SPLIT>
+cudaError_t launch_small_t(const GemmProblem& p, PrefillParams& pp) {
+  cudaError_t e = set_smem_attr<false, false, 4, BT, SPLIT>();
+  if (e != cudaSuccess) return e;
+  pp.tiles_t = (p.M + BT - 1) / BT;
+  const long long tiles = (long long)pp.tiles_t * ((p.N + kBN - 1) / kBN);
+  if (tiles * SPLIT > 0x7fffffffLL) return cudaErrorInvalidValue;
+  pp.tiles = static_cast<int>(tiles);
+  auto kern = prefill_kernel<false, false, 4, BT, SPLIT>;
+  const size_t smem = Layout<false, 4, BT, SPLIT>::SMEM;
+  if (SPLIT == 1) {  // persistent over the tiles
+    const int cap = small_capacity<BT, 1>();
+    const int grid = pp.tiles < cap ? pp.tiles : (cap > 0 ? cap : 1);
+    kern<<<grid, kThreads, smem, p.stream>>>(pp);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pp.tiles * SPLIT), 1, 1);  // one tile per cluster
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = p.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = SPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, pp);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Narrow-tile variant for fp16 activations and 4-bit codes with M <= 128: the narrowest
+// token tile holding M rows, and K split over a cluster of 2 or 4 CTAs when that keeps more
+// CTAs busy in one wave (at least four stages each).  bt = 0: the 256-row kernel.
+struct SmallPlan {
+  int bt = 0, split = 1;
+};
+long long small_cap(int bt, int split);
+SmallPlan plan_small(const GemmProblem& p) {
+  SmallPlan sp;
+#ifdef AWQ_PREFILL_NO_SMALL
+  return sp;
+#endif
+  if (p.bf16 || p.bits != 4 || p.M > 128) return sp;
+  sp.bt = p.M <= 32 ? 32 : p.M <= 64 ? 64 : 128;
+  const long long tiles = (long long)((p.N + kBN - 1) / kBN) * ((p.M + sp.bt - 1) / sp.bt);
+  const int KB = p.K / kBK;
+  auto cap = [&](int split) -> long long { return small_cap(sp.bt, split); };
+  long long best = std::min(tiles, cap(1));
+  for (int split : {2, 4}) {
+    if (KB < 4 * split) continue;
+    const long long c = cap(split);
+    if (tiles * split <= c && tiles * split > best) {
+      best = tiles * split;
+      sp.split = split;
+    }
+  }
+  return sp;
+}
+
+long long small_cap(int bt, int split) {
+  if (bt == 32) return split == 1 ? small_capacity<32, 1>() : split == 2 ? small_capacity<32, 2>() : small_capacity<32, 4>();
+  if (bt == 64) return split == 1 ? small_capacity<64, 1>() : split == 2 ? small_capacity<64, 2>() : small_capacity<64, 4>();
+  return split == 1 ? small_capacity<128, 1>() : split == 2 ? small_capacity<128, 2>() : 0;
+}
+
+cudaError_t launch_small(const GemmProblem& p, PrefillParams& pp, const SmallPlan& sp) {
+  if (sp.bt == 32) return sp.split == 4 ? launch_small_t<32, 4>(p, pp) : sp.split == 2 ? launch_small_t<32, 2>(p, pp) : launch_small_t<32, 1>(p, pp);
+  if (sp.bt == 64) return sp.split == 4 ? launch_small_t<64, 4>(p, pp) : sp.split == 2 ? launch_small_t<64, 2>(p, pp) : launch_small_t<64, 1>(p, pp);
+  return sp.split == 2 ? launch_small_t<128, 2>(p, pp) : launch_small_t<128, 1>(p, pp);
+}
+
+}  // namespace
+
+// Estimated duration of launch_prefill for p, in microseconds, from the plan it would take
+// (fitted to GB300 timings of the 7B and 70B linears at M = 8 .. 512, within about 10 %):
+// waves of CTAs over what is resident at once, each CTA about 0.45-0.5 us per 64-deep K
+// stage of its share plus a fixed part (split launches: the partial-sum exchange, growing
+// with the token tile).
+double prefill_estimate_us(const GemmProblem& p, int sms) {
+  const SmallPlan sp = plan_small(p);
+  if (sp.bt) {
+    const long long tiles = (long long)((p.N + kBN - 1) / kBN) * ((p.M + sp.bt - 1) / sp.bt);
+    long long cap = small_cap(sp.bt, sp.split);
+    if (cap <= 0) cap = sms;
+    const double waves = static_cast<double>((tiles * sp.split + cap - 1) / cap);
+    return waves * ((p.K / kBK) / static_cast<double>(sp.split) * 0.45 + 2.0 + 0.04 * sp.bt * (sp.split - 1));
+  }
+  const long long tiles = (long long)((p.N + kBN - 1) / kBN) * ((p.M + kBT - 1) / kBT);
+  return static_cast<double>((tiles + sms - 1) / sms) * (p.K / kBK) * 0.5 + 2.0;
+}
+
 cudaError_t launch_prefill(const GemmProblem& p) {
   const bool w8 = p.bits == 8;
+  const SmallPlan sp = plan_small(p);
   cudaError_t e = w8 ? set_smem_attr<false, false, 8>() : p.bf16 ? set_smem_attr<false, true>() : set_smem_attr<false>();
   if (e == cudaSuccess && !p.bf16 && !w8 && AWQ_PREFILL_PAIR) e = set_smem_attr<true>();
   if (e != cudaSuccess) return e;
@@ -700,7 +950,7 @@ cudaError_t launch_prefill(const GemmProblem& p) {
   const int C = p.N / (w8 ? 4 : 8);
   const int box_w = kBN / (w8 ? 4 : 8);  // packed words of a tile row
   const int ngrp = p.K / p.G;
-  const int x_rows = pair ? kBT / 2 : kBT;
+  const int x_rows = sp.bt ? sp.bt : (pair ? kBT / 2 : kBT);
   const CUtensorMapDataType et = p.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (!make_tmap_2d(&pp.tm_x, et, 2, p.x, p.K, p.M, kBK, x_rows,
                     CU_TENSOR_MAP_SWIZZLE_128B, &why) ||
@@ -716,6 +966,7 @@ cudaError_t launch_prefill(const GemmProblem& p) {
   e = status_word_ptr(&pp.status);
   if (e != cudaSuccess) return e;
   pp.M = p.M; pp.K = p.K; pp.N = p.N; pp.C = C; pp.G = p.G;
+  if (sp.bt) return launch_small(p, pp, sp);
   pp.tiles_t = (p.M + kBT - 1) / kBT;
   const int tile_n = pair ? 2 * kBN : kBN;
   const long long tiles = (long long)pp.tiles_t * ((p.N + tile_n - 1) / tile_n);
