@@ -129,6 +129,10 @@ struct Layout {
   static constexpr int RECV_BYTES = (SPLIT - 1) * kBN * RECV_PITCH * 4;
   static constexpr size_t SMEM = 1024 + RECV_OFF + RECV_BYTES;
   static_assert(SMEM <= 227 * 1024, "shared memory");
+  // TMEM: whatever the register count, shared memory alone keeps at most two CTAs of this
+  // kernel on an SM, and each allocates at most 256 columns below 256-row tiles (512 at
+  // 256 rows, where one CTA fills the SM): tcgen05.alloc never waits for another CTA.
+  static_assert(BT == kBT || SMEM > 228 * 1024 / 3, "at most two narrow-tile CTAs per SM");
 };
 
 // Bytes one CTA's stage copies land: its activation rows, packed tile, zero and scale rows.
@@ -806,8 +810,8 @@ namespace {
 
 // CTAs of a narrow-tile launch that are resident on the device at once (occupancy API;
 // whole clusters for split launches); cached.  At most two CTAs of this kernel share an SM
-// (registers), so the TMEM they allocate (at most 256 columns each for BT <= 128) never
-// exceeds the SM's 512 columns and tcgen05.alloc never waits on another CTA.
+// (shared memory, checked in Layout), so the TMEM they allocate (at most 256 columns each
+// for BT <= 128) never exceeds the SM's 512 columns and tcgen05.alloc never waits.
 template <int BT, int SPLIT>
 int small_capacity() {
   static std::once_flag once;
