@@ -114,12 +114,13 @@ def test_gemm_w8_workload_shapes(awq, M, K, N, G):
 
 
 @pytest.mark.parametrize("M,K,N", [(300, 4096, 1024), (512, 4096, 11008), (2048, 11008, 4096),
-                                   (257, 1024, 4112)])
+                                   (257, 1024, 4112), (64, 4096, 1024), (32, 4096, 4096),
+                                   (100, 11008, 4096)])
 def test_gemm_w8_prefill_shapes(awq, M, K, N):
     # the tcgen05 kernel: several row and column tiles, a ragged row tile (M = 257), a ragged
     # column tile (N = 4112: 16 of the last tile's 128 columns); the oracle on sampled rows
     d = synth.awq8_linear(14100 + M + K, M, K, N, group_size=128, bias=True)
-    y = run(awq, d)
+    y = run(awq, d, "prefill")
     rows = np.unique(np.concatenate([np.random.default_rng(M).integers(0, M, 24), [0, M - 1]]))
     ref = oracle.gemm8(d["x"][rows], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128)
     assert_close(y[rows], ref, f"w8 prefill M={M} K={K} N={N}")

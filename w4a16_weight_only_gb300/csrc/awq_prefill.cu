@@ -812,14 +812,14 @@ namespace {
 // whole clusters for split launches); cached.  At most two CTAs of this kernel share an SM
 // (shared memory, checked in Layout), so the TMEM they allocate (at most 256 columns each
 // for BT <= 128) never exceeds the SM's 512 columns and tcgen05.alloc never waits.
-template <int BT, int SPLIT>
+template <bool BF, int BITS, int BT, int SPLIT>
 int small_capacity() {
   static std::once_flag once;
   static int cap = 0;
   std::call_once(once, [] {
-    if (set_smem_attr<false, false, 4, BT, SPLIT>() != cudaSuccess) { (void)cudaGetLastError(); return; }
-    auto kern = prefill_kernel<false, false, 4, BT, SPLIT>;
-    const size_t smem = Layout<false, 4, BT, SPLIT>::SMEM;
+    if (set_smem_attr<false, BF, BITS, BT, SPLIT>() != cudaSuccess) { (void)cudaGetLastError(); return; }
+    auto kern = prefill_kernel<false, BF, BITS, BT, SPLIT>;
+    const size_t smem = Layout<false, BITS, BT, SPLIT>::SMEM;
     if (SPLIT == 1) {
       int dev = 0, sms = 0, per_sm = 0;
       if (cudaGetDevice(&dev) == cudaSuccess &&
@@ -846,18 +846,18 @@ int small_capacity() {
   return cap;
 }
 
-template <int BT, int SPLIT>
+template <bool BF, int BITS, int BT, int SPLIT>
 cudaError_t launch_small_t(const GemmProblem& p, PrefillParams& pp) {
-  cudaError_t e = set_smem_attr<false, false, 4, BT, SPLIT>();
+  cudaError_t e = set_smem_attr<false, BF, BITS, BT, SPLIT>();
   if (e != cudaSuccess) return e;
   pp.tiles_t = (p.M + BT - 1) / BT;
   const long long tiles = (long long)pp.tiles_t * ((p.N + kBN - 1) / kBN);
   if (tiles * SPLIT > 0x7fffffffLL) return cudaErrorInvalidValue;
   pp.tiles = static_cast<int>(tiles);
-  auto kern = prefill_kernel<false, false, 4, BT, SPLIT>;
-  const size_t smem = Layout<false, 4, BT, SPLIT>::SMEM;
+  auto kern = prefill_kernel<false, BF, BITS, BT, SPLIT>;
+  const size_t smem = Layout<false, BITS, BT, SPLIT>::SMEM;
   if (SPLIT == 1) {  // persistent over the tiles
-    const int cap = small_capacity<BT, 1>();
+    const int cap = small_capacity<BF, BITS, BT, 1>();
     const int grid = pp.tiles < cap ? pp.tiles : (cap > 0 ? cap : 1);
     kern<<<grid, kThreads, smem, p.stream>>>(pp);
     return cudaGetLastError();
@@ -879,23 +879,23 @@ cudaError_t launch_small_t(const GemmProblem& p, PrefillParams& pp) {
   return cudaGetLastError();
 }
 
-// Narrow-tile variant for fp16 activations and 4-bit codes with M <= 128: the narrowest
-// token tile holding M rows, and K split over a cluster of 2 or 4 CTAs when that keeps more
-// CTAs busy in one wave (at least four stages each).  bt = 0: the 256-row kernel.
+// Narrow-tile variant for M <= 128 (fp16 or bf16, 4- or 8-bit codes): the narrowest token
+// tile holding M rows, and K split over a cluster of 2 or 4 CTAs when that keeps more CTAs
+// busy in one wave (at least four stages each).  bt = 0: the 256-row kernel.
 struct SmallPlan {
   int bt = 0, split = 1;
 };
-long long small_cap(int bt, int split);
+long long small_cap(const GemmProblem& p, int bt, int split);
 SmallPlan plan_small(const GemmProblem& p) {
   SmallPlan sp;
 #ifdef AWQ_PREFILL_NO_SMALL
   return sp;
 #endif
-  if (p.bf16 || p.bits != 4 || p.M > 128) return sp;
+  if (p.M > 128) return sp;
   sp.bt = p.M <= 32 ? 32 : p.M <= 64 ? 64 : 128;
   const long long tiles = (long long)((p.N + kBN - 1) / kBN) * ((p.M + sp.bt - 1) / sp.bt);
   const int KB = p.K / kBK;
-  auto cap = [&](int split) -> long long { return small_cap(sp.bt, split); };
+  auto cap = [&](int split) -> long long { return small_cap(p, sp.bt, split); };
   long long best = std::min(tiles, cap(1));
   for (int split : {2, 4}) {
     if (KB < 4 * split) continue;
@@ -908,16 +908,34 @@ SmallPlan plan_small(const GemmProblem& p) {
   return sp;
 }
 
-long long small_cap(int bt, int split) {
-  if (bt == 32) return split == 1 ? small_capacity<32, 1>() : split == 2 ? small_capacity<32, 2>() : small_capacity<32, 4>();
-  if (bt == 64) return split == 1 ? small_capacity<64, 1>() : split == 2 ? small_capacity<64, 2>() : small_capacity<64, 4>();
-  return split == 1 ? small_capacity<128, 1>() : split == 2 ? small_capacity<128, 2>() : 0;
+template <bool BF, int BITS>
+long long small_cap_t(int bt, int split) {
+  if (bt == 32)
+    return split == 1 ? small_capacity<BF, BITS, 32, 1>() : split == 2 ? small_capacity<BF, BITS, 32, 2>()
+                                                                       : small_capacity<BF, BITS, 32, 4>();
+  if (bt == 64)
+    return split == 1 ? small_capacity<BF, BITS, 64, 1>() : split == 2 ? small_capacity<BF, BITS, 64, 2>()
+                                                                       : small_capacity<BF, BITS, 64, 4>();
+  return split == 1 ? small_capacity<BF, BITS, 128, 1>() : split == 2 ? small_capacity<BF, BITS, 128, 2>() : 0;
+}
+long long small_cap(const GemmProblem& p, int bt, int split) {
+  if (p.bits == 8) return small_cap_t<false, 8>(bt, split);
+  return p.bf16 ? small_cap_t<true, 4>(bt, split) : small_cap_t<false, 4>(bt, split);
 }
 
+template <bool BF, int BITS>
+cudaError_t launch_small_b(const GemmProblem& p, PrefillParams& pp, const SmallPlan& sp) {
+  if (sp.bt == 32)
+    return sp.split == 4 ? launch_small_t<BF, BITS, 32, 4>(p, pp)
+                         : sp.split == 2 ? launch_small_t<BF, BITS, 32, 2>(p, pp) : launch_small_t<BF, BITS, 32, 1>(p, pp);
+  if (sp.bt == 64)
+    return sp.split == 4 ? launch_small_t<BF, BITS, 64, 4>(p, pp)
+                         : sp.split == 2 ? launch_small_t<BF, BITS, 64, 2>(p, pp) : launch_small_t<BF, BITS, 64, 1>(p, pp);
+  return sp.split == 2 ? launch_small_t<BF, BITS, 128, 2>(p, pp) : launch_small_t<BF, BITS, 128, 1>(p, pp);
+}
 cudaError_t launch_small(const GemmProblem& p, PrefillParams& pp, const SmallPlan& sp) {
-  if (sp.bt == 32) return sp.split == 4 ? launch_small_t<32, 4>(p, pp) : sp.split == 2 ? launch_small_t<32, 2>(p, pp) : launch_small_t<32, 1>(p, pp);
-  if (sp.bt == 64) return sp.split == 4 ? launch_small_t<64, 4>(p, pp) : sp.split == 2 ? launch_small_t<64, 2>(p, pp) : launch_small_t<64, 1>(p, pp);
-  return sp.split == 2 ? launch_small_t<128, 2>(p, pp) : launch_small_t<128, 1>(p, pp);
+  if (p.bits == 8) return launch_small_b<false, 8>(p, pp, sp);
+  return p.bf16 ? launch_small_b<true, 4>(p, pp, sp) : launch_small_b<false, 4>(p, pp, sp);
 }
 
 }  // namespace
@@ -931,7 +949,7 @@ double prefill_estimate_us(const GemmProblem& p, int sms) {
   const SmallPlan sp = plan_small(p);
   if (sp.bt) {
     const long long tiles = (long long)((p.N + kBN - 1) / kBN) * ((p.M + sp.bt - 1) / sp.bt);
-    long long cap = small_cap(sp.bt, sp.split);
+    long long cap = small_cap(p, sp.bt, sp.split);
     if (cap <= 0) cap = sms;
     const double waves = static_cast<double>((tiles * sp.split + cap - 1) / cap);
     return waves * ((p.K / kBK) / static_cast<double>(sp.split) * 0.45 + 2.0 + 0.04 * sp.bt * (sp.split - 1));
