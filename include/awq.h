@@ -138,7 +138,7 @@ awq_status_t awq_dequant_bf16(const int32_t* qweight, const int32_t* qzeros, con
  * N % 16 == 0 and x, qweight, qzeros, scales are 16-byte aligned (AWQ_PATH_DECODE and
  * AWQ_PATH_PREFILL for any M, chosen as for 4-bit codes); everything else runs
  * AWQ_PATH_GENERIC.  Forcing a family whose contract the shape breaks returns
- * AWQ_ERR_UNSUPPORTED_SHAPE.  (awq_gemm_select_path describes 4-bit calls only.)
+ * AWQ_ERR_UNSUPPORTED_SHAPE.  (awq_gemm_select_path_ex describes 8-bit calls.)
  * awq_dequant_w8: the awq_dequant contract (exact fp32, or one rounding to fp16).
  */
 awq_status_t awq_gemm_w8_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
@@ -255,6 +255,14 @@ awq_path_t awq_gemm_select_path(int64_t M, int64_t K, int64_t N, int64_t group_s
                                 const void* x_f16, const int32_t* qweight,
                                 const int32_t* qzeros, const void* scales_f16,
                                 const void* bias_f16, const void* y_f16);
+
+/* The same for any entry point: dtype AWQ_DTYPE_F16 or AWQ_DTYPE_BF16 (activations, scales,
+ * bias, output), bits 4 (qweight [K, N/8]) or 8 (qweight [K, N/4], fp16 only).  Returns
+ * AWQ_PATH_AUTO (0) on an invalid shape or combination. */
+awq_path_t awq_gemm_select_path_ex(int64_t M, int64_t K, int64_t N, int64_t group_size,
+                                   const void* x, const int32_t* qweight, const int32_t* qzeros,
+                                   const void* scales, const void* bias, const void* y,
+                                   awq_dtype_t dtype, int32_t bits);
 
 /* Synchronizes `stream`, then reads and clears the library's device status word on the
  * current device.  Returns AWQ_ERR_TIMEOUT if a kernel gave up a bounded wait since the

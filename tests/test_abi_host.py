@@ -198,3 +198,15 @@ def test_linear_layer_refuses_host_tensors_and_bad_widths(lib):
         AwqLinear(qw, qz, sc, None, group_size=128)          # host tensors never reach a kernel
     with pytest.raises(ValueError):
         AwqLinear(qw, qz, sc, None, group_size=128, bits=5)
+
+
+def test_select_path_ex_is_host_only(lib):
+    sel = lib.awq_gemm_select_path_ex
+    F16, BF16 = 0, 2
+    assert sel(1, 4096, 4096, 128, A, A, A, A, None, B, F16, 4) == 1       # decode
+    assert sel(1, 4096, 4096, 128, A, A, A, A, None, B, BF16, 4) == 1      # bf16 decode
+    assert sel(1, 4096, 4096, 128, A, A, A, A, None, B, F16, 8) == 1       # 8-bit decode
+    assert sel(1, 256, 40, 128, A, A, A, A, None, B, F16, 8) == 3          # N % 16 != 0: generic
+    assert sel(1, 4096, 4096, 128, A, A, A, A, None, B, BF16, 8) == 0      # 8-bit bf16: invalid
+    assert sel(1, 4096, 4096, 128, A, A, A, A, None, B, 1, 4) == 0         # f32 activations: invalid
+    assert sel(1, 256, 12, 128, A, A, A, A, None, B, F16, 4) == 0          # N % 8 at 4 bits

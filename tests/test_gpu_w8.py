@@ -133,6 +133,13 @@ def test_gemm_w8_deterministic(awq, M):
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
 
 
+def test_gemm_w8_selected_families(awq):
+    for (M, want) in ((1, "decode"), (16, "decode"), (2048, "prefill")):
+        d = synth.awq8_linear(13970 + M, M, 4096, 1024, group_size=128)
+        t = to_dev(d)
+        assert awq.select_path(t["x"], t["qweight"], t["qzeros"], t["scales"], bits=8) == want
+
+
 def test_gemm_w8_auto_matches_decode(awq):
     # small M takes the decode kernel: same bits as forcing it
     d = synth.awq8_linear(13960, 3, 4096, 4096, group_size=128, bias=True)

@@ -30,6 +30,7 @@ SIGNATURES = {
     "awq_gemm": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "awq_gemm_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp]),
     "awq_gemm_select_path": (_i32, [_i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "awq_gemm_select_path_ex": (_i32, [_i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32]),
     "awq_device_status": (_i32, [_vp]),
     "awq_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
     "awq_quantize_rtn": (_i32, [_vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
@@ -359,12 +360,16 @@ def awq_quantize_rtn(w, group_size=128, sym=False, out=None, stream=None):
     return qweight, qzeros, scales
 
 
-def select_path(x, qweight, qzeros, scales, bias=None, group_size=128, out=None) -> str:
+def select_path(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, bits=4) -> str:
+    """The kernel family awq_gemm (bits=4; bf16 when x is bfloat16) or awq_gemm_w8 (bits=8)
+    would run for these tensors: "decode", "prefill", "generic", or "auto" if invalid."""
     lib = load_library()
     M, K = x.reshape(-1, x.shape[-1]).shape
-    N = qweight.shape[1] * 8
-    r = lib.awq_gemm_select_path(M, K, N, group_size, _ptr(x), _ptr(qweight), _ptr(qzeros),
-                                 _ptr(scales), _ptr(bias), _ptr(out) if out is not None else _ptr(x))
+    N = qweight.shape[1] * (32 // bits)
+    dt = DTYPE_BF16 if x.dtype == torch.bfloat16 else DTYPE_F16
+    r = lib.awq_gemm_select_path_ex(M, K, N, group_size, _ptr(x), _ptr(qweight), _ptr(qzeros),
+                                    _ptr(scales), _ptr(bias), _ptr(out) if out is not None else _ptr(x),
+                                    dt, bits)
     return PATH_NAMES.get(r, "auto")
 
 

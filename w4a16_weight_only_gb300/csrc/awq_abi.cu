@@ -395,6 +395,22 @@ awq_path_t awq_gemm_select_path(int64_t M, int64_t K, int64_t N, int64_t group_s
   return static_cast<awq_path_t>(choose_path(p));
 }
 
+awq_path_t awq_gemm_select_path_ex(int64_t M, int64_t K, int64_t N, int64_t group_size,
+                                   const void* x, const int32_t* qweight, const int32_t* qzeros,
+                                   const void* scales, const void* bias, const void* y,
+                                   awq_dtype_t dtype, int32_t bits) {
+  if ((dtype != AWQ_DTYPE_F16 && dtype != AWQ_DTYPE_BF16) || (bits != 4 && bits != 8) ||
+      (bits == 8 && dtype != AWQ_DTYPE_F16))
+    return AWQ_PATH_AUTO;
+  awq::GemmProblem p{};
+  bool empty = false;
+  if (build_problem(x, qweight, qzeros, scales, bias, M, K, N, group_size, const_cast<void*>(y),
+                    nullptr, &p, &empty, dtype == AWQ_DTYPE_BF16, bits) != AWQ_OK || empty)
+    return AWQ_PATH_AUTO;
+  ok();
+  return static_cast<awq_path_t>(choose_path(p));
+}
+
 awq_status_t awq_device_status(awq_stream_t stream) {
   awq_status_t st = check_device();
   if (st != AWQ_OK) return st;
