@@ -70,10 +70,10 @@ def step_bytes(lins):
 # `python bench.py --steps 60 --warmup 3 --no-cpu-baseline` summarised in
 # profiles/decode_tma_7b_m1_bench_launches.md; valid only for the kernel source it was
 # measured on (SHA-256 of the files below), else reported as null.
-TRAFFIC_BYTES_PER_LAUNCH = 18_588_014
+TRAFFIC_BYTES_PER_LAUNCH = 18_587_960
 TRAFFIC_SOURCES = {
     "w4a16_weight_only_gb300/csrc/awq_decode_tma.cu":
-        "e0bf1b4352904e9b6879cf2735e6ab931c5e5ea67ff9e2f48bb1a89323b2e3f5",
+        "80fa11a21ccd77af8cde8307dc1a850d280a7d85979ca6036cb2d3c6bcd5b877",
     "w4a16_weight_only_gb300/csrc/awq_ptx.cuh":
         "166c2c9cd2d4a880677df7bd3dc634de58dadf2fcdc9ba2bdcf045010269d495",
 }
