@@ -65,7 +65,8 @@ def test_dequant_w8_bit_exact(awq, K, N, G):
 
 SMALL = [(1, 256, 256, 128, False), (3, 512, 192, 64, True), (8, 1024, 512, 128, True),
          (17, 2048, 1024, 256, True), (32, 4096, 128, -1, False), (33, 256, 60, 16, True),
-         (100, 512, 132, 64, False), (300, 1024, 256, 128, True), (1, 64, 4, -1, False)]
+         (100, 512, 132, 64, False), (300, 1024, 256, 128, True), (1, 64, 4, -1, False),
+         (12, 1024, 1024, 128, True)]
 
 
 def decode_ok(K, N, G):
@@ -101,6 +102,7 @@ def test_gemm_w8_exact_case_bitwise(awq, M, path):
 # group per row (G = K), 8-row tiles, 16-row tiles, the exact-operand 32-row tiles, a
 # ragged column tile (N = 48: 12 of a tile's 16 words), M past 32 (several row tiles)
 WORK = [(1, 4096, 4096, 128), (1, 11008, 4096, 128), (1, 28672, 1024, 128), (1, 4096, 1024, -1),
+        (16, 4096, 4096, 128),
         (4, 4096, 11008, 128), (16, 4096, 11008, 128), (24, 4096, 4096, 128), (32, 11008, 4096, 128),
         (7, 1024, 48, 64), (1, 1024, 16, 128), (64, 11008, 4096, 128)]
 
