@@ -78,3 +78,18 @@ def test_traffic_reported_only_for_measured_source(monkeypatch):
     bad = {k: "0" * 64 for k in bench.TRAFFIC_SOURCES}
     monkeypatch.setattr(bench, "TRAFFIC_SOURCES", bad)
     assert bench.measured_traffic() is None
+
+
+def test_cpu_oracle_mode_prints_one_line_per_shape():
+    # the C oracle timed on the tiny config (no GPU involved), one JSON line per workload
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-oracle", "--configs", "0"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT,
+                       env=dict(os.environ, OMP_NUM_THREADS="2"))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    assert [d["workload"] for d in lines] == ["tiny_m1_256x256"]
+    d = lines[0]
+    assert d["kind"] == "C oracle" and d["threads"] == 2 and d["linear_s"] > 0 and d["dequant_s"] > 0
+    assert d["GB_s"] > 0 and d["M"] == 1 and d["K"] == 256 and d["N"] == 256
