@@ -1,12 +1,21 @@
 #!/usr/bin/env python
-"""Benchmark: AWQ W4A16 awq_gemm on the 7B-shaped decode workload (M = 1, the three
-linears 4096x4096, 4096x11008, 11008x4096, group size 128, fp16 bias).
+"""Benchmark: AWQ W4A16 awq_gemm on one GB300.
 
-A step is one pass of the hot path over one batch: three awq_gemm calls, one per
-linear (one kernel launch each).  Inputs are seeded synthetic tensors resident in HBM.
-Weights rotate over R independent sets whose total (R * 55.7 MB) exceeds the 129 MB L2,
-so every step streams its weights from HBM.  Steps are replayed from CUDA graphs and
-timed with CUDA events on the replay stream, after W warm-up steps.
+Headline (the JSON line's `value`): decode GB/s on the 70B-shaped linears at M = 1 --
+one step is the three linears 8192x8192, 8192x28672, 28672x8192 (group size 128, fp16
+bias), one awq_gemm call (one kernel launch) each, through prepared AwqLinear layers.
+Weights rotate over R independent sets whose total exceeds 3x the 129 MB L2, so every
+step streams its weights from HBM.  Steps are replayed from CUDA graphs and timed with
+CUDA events on the replay stream: W warm-up steps, then repetitions of exactly K timed
+steps until the repetitions cover at least 0.5 s; the reported step time is the median
+repetition.  nvidia-smi clocks are sampled during every timed region.
+
+Extra blocks on the same line: `prefill` -- TFLOP/s of the 70B linears at M = 4096 (the
+three linears per step, eager launches, inputs larger than L2), beside awq_dequant +
+cuBLAS on the same step; `decode_7b` -- the 7B decode step (M = 1: 4096x4096, 4096x11008,
+11008x4096, bias); `e2e` -- the headline step end to end through the public call with
+pinned host buffers (one host-to-device copy of the step's activations, three calls, one
+device-to-host copy of the outputs, a synchronize per step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -36,12 +45,20 @@ import synth  # noqa: E402
 METRIC = ("awq_gemm GB/s (decode, % HBM roofline) and TFLOP/s (prefill, % fp16 peak) "
           "on 1 GB300")
 UNIT = "GB/s"
-LINEARS = ["7b_decode_m1_4096x4096_bias", "7b_decode_m1_4096x11008_bias",
-           "7b_decode_m1_11008x4096_bias"]
-WORKLOAD_NAME = ("7B decode GEMV M=1: linears 4096x4096, 4096x11008, 11008x4096; "
+LINEARS = ["70b_m1_8192x8192", "70b_m1_8192x28672", "70b_m1_28672x8192"]
+WORKLOAD_NAME = ("70B decode M=1: linears 8192x8192, 8192x28672, 28672x8192; "
                  "group_size 128; fp16 bias")
+LINEARS_7B = ["7b_decode_m1_4096x4096_bias", "7b_decode_m1_4096x11008_bias",
+              "7b_decode_m1_11008x4096_bias"]
+WORKLOAD_7B = ("7B decode M=1: linears 4096x4096, 4096x11008, 11008x4096; group_size 128; "
+               "fp16 bias")
+PREFILL = ["70b_m4096_8192x8192", "70b_m4096_8192x28672", "70b_m4096_28672x8192"]
+WORKLOAD_PREFILL = ("70B prefill M=4096: linears 8192x8192, 8192x28672, 28672x8192; "
+                    "group_size 128; fp16 bias")
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_TFLOPS = 1900.0
+MIN_TIMED_S = 0.5  # every timed region repeats its K-step repetitions until it covers this
 
 
 def algorithmic_bytes(M, K, N, G, bias):
@@ -51,9 +68,9 @@ def algorithmic_bytes(M, K, N, G, bias):
     return K * N // 2 + ng * N // 2 + 2 * ng * N + 2 * M * K + 2 * M * N + (2 * N if bias else 0)
 
 
-def workload_linears(set_index: int):
+def workload_linears(set_index: int, names=None):
     out = []
-    for name in LINEARS:
+    for name in (names or LINEARS):
         cfg, si, _, M, K, N, G, b = synth.workload(name)
         seed = synth.seed_for(cfg, si) + 100000 * set_index
         out.append(synth.awq_linear(seed, M, K, N, group_size=G, bias=b))
@@ -65,15 +82,23 @@ def step_bytes(lins):
                for d in lins)
 
 
+def step_flop(names):
+    tot = 0.0
+    for name in names:
+        _, _, _, M, K, N, _, _ = synth.workload(name)
+        tot += 2.0 * M * N * K
+    return tot
+
+
 # DRAM traffic of the decode kernel per launch (dram__bytes_read.sum + dram__bytes_write.sum),
-# averaged over the three linears of one step, from the ncu launch list of
-# `python bench.py --steps 60 --warmup 3 --no-cpu-baseline` summarised in
-# profiles/decode_tma_7b_m1_bench_launches.md; valid only for the kernel source it was
+# averaged over the three linears of one headline step, from the ncu launch list of
+# `python bench.py --steps 20 --warmup 3 --no-cpu-baseline --decode-only` summarised in
+# profiles/decode_tma_70b_m1_bench_launches.md; valid only for the kernel source it was
 # measured on (SHA-256 of the files below), else reported as null.
-TRAFFIC_BYTES_PER_LAUNCH = 18_587_960
+TRAFFIC_BYTES_PER_LAUNCH = 93_162_129
 TRAFFIC_SOURCES = {
     "w4a16_weight_only_gb300/csrc/awq_decode_tma.cu":
-        "80fa11a21ccd77af8cde8307dc1a850d280a7d85979ca6036cb2d3c6bcd5b877",
+        "0170e47375a8599b14fee3621e4126f3f3c04d86018a35633b14a3a4bea01665",
     "w4a16_weight_only_gb300/csrc/awq_ptx.cuh":
         "166c2c9cd2d4a880677df7bd3dc634de58dadf2fcdc9ba2bdcf045010269d495",
 }
@@ -91,14 +116,31 @@ def measured_traffic():
     return TRAFFIC_BYTES_PER_LAUNCH
 
 
-def peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _peaks_file():
     try:
-        with open(path) as f:
-            p = json.load(f)
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except Exception:
+        return None
+
+
+def peaks():
+    p = _peaks_file()
+    try:
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak(sustained: bool):
+    """Dense fp16 tensor peak: the measured bf16 cuBLAS figure (fp16 runs at the same nominal
+    rate), sustained for a kernel timed inside a long loop, burst for one timed alone."""
+    p = _peaks_file()
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        return float(p[key]), f"measured ({key}; fp16 nominal rate equal to bf16)"
+    except Exception:
+        return FALLBACK_TFLOPS, "fallback"
 
 
 class ClockSampler:
@@ -116,6 +158,7 @@ class ClockSampler:
                 stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+        self.rows = None
 
     def start(self):
         self.t0 = time.time()
@@ -123,10 +166,9 @@ class ClockSampler:
     def end(self):
         self.t1 = time.time()
 
-    def finish(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "nvidia-smi unavailable"}
+    def _collect(self):
+        if self.rows is not None or self.proc is None:
+            return
         time.sleep(0.05)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
@@ -138,19 +180,38 @@ class ClockSampler:
             try:
                 ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
                 ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
-                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:], parts[3]))
             except Exception:
                 continue
-        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.02 <= r[0] <= self.t1 + 0.02]
+        self.rows = rows
+
+    def window(self, t0, t1):
+        """Summary of the samples taken inside [t0, t1] (wall clock, seconds)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self._collect()
+        rows = self.rows
+        inside = [r for r in rows if t0 - 0.02 <= r[0] <= t1 + 0.02]
         used = inside
         if not used and rows:
-            mid = 0.5 * (self.t0 + self.t1)
+            mid = 0.5 * (t0 + t1)
             used = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in used for i, v in enumerate(r[3]) if v == "Active"})
+        power = []
+        for r in used:
+            try:
+                power.append(float(r[4]))
+            except ValueError:
+                pass
         return {"sm_mhz": statistics.median([r[1] for r in used]) if used else None,
                 "sm_max_mhz": max(r[2] for r in used) if used else None,
+                "power_w_median": statistics.median(power) if power else None,
                 "reasons": reasons, "samples": len(inside)}
+
+    def finish(self):
+        return self.window(self.t0, self.t1)
 
 
 def dist_setup(args):
@@ -214,7 +275,7 @@ def oracle_step(sub):
 
 
 def cpu_baseline(seconds: float = 12.0):
-    width = 1024
+    width = 512
     sub, nbytes = oracle_sample(width)
     oracle_step(sub)
     n, t0 = 0, time.perf_counter()
@@ -225,7 +286,7 @@ def cpu_baseline(seconds: float = 12.0):
         if el >= seconds:
             break
     return {"value": nbytes * n / el / 1e9, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"first {width} output columns of each of the three linears (M=1), "
+            "sample": f"first {width} output columns of each of the three 70B linears (M=1), "
                       f"{n} passes in {el:.1f} s; numpy fp64 matmul (BLAS threads), "
                       "unpack/dequant single-threaded"}
 
@@ -234,12 +295,12 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     # size each step so that warm-up + timed steps end within about two minutes
-    probe_sub, _ = oracle_sample(512)
+    probe_sub, _ = oracle_sample(256)
     t0 = time.perf_counter()
     oracle_step(probe_sub)
-    per512 = max(time.perf_counter() - t0, 1e-4)
+    per256 = max(time.perf_counter() - t0, 1e-4)
     budget = 120.0 / max(1, args.steps + args.warmup)
-    width = int(max(8, min(28672, 512 * budget / per512)) // 8 * 8)
+    width = int(max(8, min(28672, 256 * budget / per256)) // 8 * 8)
     sub, nbytes = oracle_sample(width)
     for _ in range(args.warmup):
         oracle_step(sub)
@@ -249,8 +310,8 @@ def run_reference(args, rank, world):
     el = time.perf_counter() - t0
     value = nbytes * args.steps / el / 1e9
     widths = ", ".join(f"{d['K']}x{d['N']}" for d in sub)
-    desc = (f"first min({width}, N) output columns of each of the three linears (M=1) per step "
-            f"(K x columns: {widths}); numpy fp64 matmul (BLAS threads), unpack/dequant "
+    desc = (f"first min({width}, N) output columns of each of the three 70B linears (M=1) per "
+            f"step (K x columns: {widths}); numpy fp64 matmul (BLAS threads), unpack/dequant "
             "single-threaded")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
@@ -264,6 +325,235 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------- GPU path ----
 
+def timed_repetitions(run_k, k, stream, min_s=MIN_TIMED_S, max_reps=100000):
+    """Repetitions of exactly k steps (run_k(k) enqueues them on `stream`), each bracketed by
+    CUDA events recorded on that stream, until the repetitions cover min_s.  Returns the
+    per-repetition times (s) and the wall-clock window of the region."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True)]
+    w0 = time.time()
+    evs[0].record(stream)
+    total, reps = 0.0, 0
+    while reps < max_reps:
+        # enqueue a batch of repetitions, then measure what they took
+        batch = 1 if reps == 0 else max(1, min(256, int(reps * (min_s - total) / max(total, 1e-9)) + 1))
+        for _ in range(batch):
+            run_k(k)
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            evs.append(e)
+            reps += 1
+        evs[-1].synchronize()
+        total = evs[0].elapsed_time(evs[-1]) / 1e3
+        if total >= min_s:
+            break
+    w1 = time.time()
+    times = [evs[i].elapsed_time(evs[i + 1]) / 1e3 for i in range(len(evs) - 1)]
+    return times, (w0, w1)
+
+
+def _device_sets(names, R, torch, awq):
+    """R independent weight sets (set 0 from the workload seeds) with their activations,
+    outputs and prepared AwqLinear layers (static weights, as at model load)."""
+    lins0 = workload_linears(0, names)
+    sets = []
+    for r in range(R):
+        lins = lins0 if r == 0 else workload_linears(r, names)
+        dev = []
+        for d in lins:
+            t = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "qweight", "qzeros", "scales")}
+            t["bias"] = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
+            t["y"] = torch.empty((d["M"], d["N"]), dtype=torch.float16, device="cuda")
+            t["G"] = d["group_size"]
+            t["layer"] = awq.AwqLinear(t["qweight"], t["qzeros"], t["scales"], t["bias"], t["G"])
+            dev.append(t)
+        sets.append(dev)
+    return lins0, sets
+
+
+def _decode_region(names, args, world, torch, awq, stream, clocks):
+    """The decode step over rotating weight sets, replayed from CUDA graphs; returns the
+    median step time, the timing details and the sets (for the end-to-end runs)."""
+    lins0 = workload_linears(0, names)
+    per_set = sum(d["qweight"].nbytes + d["qzeros"].nbytes + d["scales"].nbytes for d in lins0)
+    R = max(2, int(np.ceil(3.0 * L2_BYTES / per_set)))
+    _, sets = _device_sets(names, R, torch, awq)
+    sp = stream.cuda_stream
+
+    def step(r):
+        for t in sets[r]:
+            t["layer"](t["x"], out=t["y"], stream=sp)
+
+    with torch.cuda.stream(stream):
+        for r in range(R):  # eager warm-up (first calls set kernel attributes)
+            step(r)
+        stream.synchronize()
+        cycle = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cycle, stream=stream):
+            for r in range(R):
+                step(r)
+        singles = []
+        for r in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(r)
+            singles.append(g)
+
+    def run_steps(k):
+        full, rem = divmod(k, R)
+        for _ in range(full):
+            cycle.replay()
+        for r in range(rem):
+            singles[r].replay()
+
+    with torch.cuda.stream(stream):
+        run_steps(max(args.warmup, 3))
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        times, (w0, w1) = timed_repetitions(run_steps, args.steps, stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    awq.device_status()
+    t_step = statistics.median(times) / args.steps
+    return {"t_step": t_step, "reps": len(times), "timed_s": sum(times), "R": R,
+            "per_set": per_set, "win": (w0, w1), "sets": sets,
+            "nbytes": step_bytes(lins0), "launches": len(names) * args.steps * len(times)}
+
+
+def _prefill_region(args, world, torch, awq, stream, clocks):
+    """The 70B prefill step (three linears at M = 4096), eager launches through prepared
+    layers, inputs larger than L2; beside it awq_dequant + cuBLAS on the same step."""
+    lins = workload_linears(0, PREFILL)
+    dev = []
+    for d in lins:
+        t = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "qweight", "qzeros", "scales")}
+        t["bias"] = torch.from_numpy(d["bias"]).cuda()
+        t["y"] = torch.empty((d["M"], d["N"]), dtype=torch.float16, device="cuda")
+        t["layer"] = awq.AwqLinear(t["qweight"], t["qzeros"], t["scales"], t["bias"], d["group_size"])
+        t["G"] = d["group_size"]
+        dev.append(t)
+    del lins
+    sp = stream.cuda_stream
+    path = awq.select_path(dev[0]["x"], dev[0]["qweight"], dev[0]["qzeros"], dev[0]["scales"],
+                           dev[0]["bias"], dev[0]["G"], dev[0]["y"])
+
+    def run_steps(k):
+        for _ in range(k):
+            for t in dev:
+                t["layer"](t["x"], out=t["y"], stream=sp)
+
+    with torch.cuda.stream(stream):
+        run_steps(max(args.warmup, 3))
+        torch.cuda.synchronize()
+        barrier(world)
+        times, (w0, w1) = timed_repetitions(run_steps, args.steps, stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    awq.device_status()
+    t_step = statistics.median(times) / args.steps
+
+    # comparator: the pages' large-batch strategy (dequantize to a dense fp16 weight, then a
+    # library GEMM), timed the same way on the same step
+    for t in dev:
+        t["wd"] = torch.empty((t["qweight"].shape[0], t["y"].shape[1]), dtype=torch.float16,
+                              device="cuda")
+
+    def run_ref(k):
+        for _ in range(k):
+            for t in dev:
+                awq.awq_dequant(t["qweight"], t["qzeros"], t["scales"], t["G"], out=t["wd"],
+                                stream=stream)
+                torch.addmm(t["bias"], t["x"], t["wd"], out=t["y"])
+
+    with torch.cuda.stream(stream):
+        run_ref(max(args.warmup, 3))
+        torch.cuda.synchronize()
+        ref_times, (r0, r1) = timed_repetitions(run_ref, args.steps, stream)
+        torch.cuda.synchronize()
+    t_ref = statistics.median(ref_times) / args.steps
+    del dev
+    torch.cuda.empty_cache()
+    return {"t_step": t_step, "reps": len(times), "timed_s": sum(times), "win": (w0, w1),
+            "t_ref": t_ref, "ref_win": (r0, r1), "path": path,
+            "launches": len(PREFILL) * args.steps * len(times)}
+
+
+def _e2e(reg, args, world, torch, stream):
+    """The headline step end to end through the public call: per step one pinned
+    host-to-device copy of the step's activations, the three calls, one device-to-host copy
+    of the outputs and a synchronize; eagerly and replayed from CUDA graphs.  Each loop
+    covers at least MIN_TIMED_S."""
+    sets, R = reg["sets"], reg["R"]
+    xsz = [t["x"].numel() for t in sets[0]]
+    ysz = [t["y"].numel() for t in sets[0]]
+    hx_all = torch.cat([t["x"].reshape(-1).cpu() for t in sets[0]]).pin_memory()
+    hy_all = torch.empty(sum(ysz), dtype=torch.float16).pin_memory()
+    xd_all = torch.empty(sum(xsz), dtype=torch.float16, device="cuda")
+    yd_all = torch.empty(sum(ysz), dtype=torch.float16, device="cuda")
+    xd = [v.view(t["x"].shape) for v, t in zip(torch.split(xd_all, xsz), sets[0])]
+    yd = [v.view(t["y"].shape) for v, t in zip(torch.split(yd_all, ysz), sets[0])]
+    h2d, d2h = hx_all.numel() * 2, hy_all.numel() * 2
+    sp = stream.cuda_stream
+
+    def e2e_step(r):
+        with torch.cuda.stream(stream):
+            xd_all.copy_(hx_all, non_blocking=True)
+            for t, xv, yv in zip(sets[r], xd, yd):
+                t["layer"](xv, out=yv, stream=sp)
+            hy_all.copy_(yd_all, non_blocking=True)
+        stream.synchronize()
+
+    def loop(fn):
+        for i in range(max(args.warmup, 3)):
+            fn(i % R)
+        barrier(world)
+        w0 = time.time()
+        n, t0 = 0, time.perf_counter()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        while True:
+            for _ in range(args.steps):
+                fn(n % R)
+                n += 1
+            if time.perf_counter() - t0 >= MIN_TIMED_S:
+                break
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record(stream)
+        e1.synchronize()
+        wins.append((w0, time.time()))
+        return n, reduce_max(e0.elapsed_time(e1) / 1e3, world)
+
+    wins = []
+    n_e, el_e = loop(e2e_step)
+    graphs = []
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    for r in range(R):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap):
+            xd_all.copy_(hx_all, non_blocking=True)
+            for t, xv, yv in zip(sets[r], xd, yd):
+                t["layer"](xv, out=yv, stream=cap.cuda_stream)
+            hy_all.copy_(yd_all, non_blocking=True)
+        graphs.append(gr)
+    stream.wait_stream(cap)
+
+    def graph_step(r):
+        with torch.cuda.stream(stream):
+            graphs[r].replay()
+        stream.synchronize()
+
+    n_g, el_g = loop(graph_step)
+    nbytes = reg["nbytes"]
+    return ({"value": world * nbytes * n_e / el_e / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+             "d2h_bytes_per_step": d2h, "steps": n_e, "timed_s": el_e, "win": wins[0]},
+            {"value": world * nbytes * n_g / el_g / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+             "d2h_bytes_per_step": d2h, "steps": n_g, "timed_s": el_g, "win": wins[1],
+             "note": "input copy, three calls, output copy per step, replayed from CUDA graphs; "
+                     "a synchronize per step"})
+
+
 def run_ours(args, rank, world, local):
     import torch
     from w4a16_weight_only_gb300 import build as _build
@@ -273,166 +563,91 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     if not awq.runtime_available():
         raise RuntimeError("awq runtime unavailable: " + awq.last_error())
-    lins0 = workload_linears(0)
-    per_set = sum(d["qweight"].nbytes + d["qzeros"].nbytes + d["scales"].nbytes for d in lins0)
-    R = max(2, int(np.ceil(2.5 * L2_BYTES / per_set)))
-    sets = []
-    for r in range(R):
-        lins = lins0 if r == 0 else workload_linears(r)
-        dev = []
-        for d in lins:
-            t = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "qweight", "qzeros", "scales")}
-            t["bias"] = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
-            t["y"] = torch.empty((d["M"], d["N"]), dtype=torch.float16, device="cuda")
-            t["G"] = d["group_size"]
-            dev.append(t)
-        sets.append(dev)
-    nbytes = step_bytes(lins0)
-    launches_per_step = len(LINEARS)
-
-    def step(r):
-        for t in sets[r]:
-            awq.awq_gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], t["bias"],
-                         group_size=t["G"], out=t["y"])
-
-    # eager warm-up (first calls set kernel attributes), then capture
-    for r in range(R):
-        step(r)
-    torch.cuda.synchronize()
-    cycle = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(cycle):
-        for r in range(R):
-            step(r)
-    singles = []
-    for r in range(R):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            step(r)
-        singles.append(g)
-
-    def run_steps(k):
-        full, rem = divmod(k, R)
-        for _ in range(full):
-            cycle.replay()
-        for r in range(rem):
-            singles[r].replay()
-
+    stream = torch.cuda.Stream()
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    run_steps(max(args.warmup, 3))
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks.start()
-    ev0.record(stream)
-    run_steps(args.steps)
-    ev1.record(stream)
-    ev1.synchronize()
-    clocks.end()
-    torch.cuda.synchronize()
-    barrier(world)
-    elapsed = ev0.elapsed_time(ev1) / 1e3
-    clk = clocks.finish()
-    elapsed_max = reduce_max(elapsed, world)
-    awq.device_status()
+    hbm, hbm_kind = peaks()
 
-    # end to end through the public API: every step copies the step's activations (the three
-    # linears' x, staged in one pinned buffer) to the device in one copy, runs the three
-    # calls, and reads the three outputs back in one copy
-    xsz = [t["x"].numel() for t in sets[0]]
-    ysz = [t["y"].numel() for t in sets[0]]
-    hx_all = torch.cat([t["x"].reshape(-1).cpu() for t in sets[0]]).pin_memory()
-    hy_all = torch.empty(sum(ysz), dtype=torch.float16).pin_memory()
-    xd_all = torch.empty(sum(xsz), dtype=torch.float16, device="cuda")
-    yd_all = torch.empty(sum(ysz), dtype=torch.float16, device="cuda")
-    xd = [v.view(t["x"].shape) for v, t in zip(torch.split(xd_all, xsz), sets[0])]
-    yd = [v.view(t["y"].shape) for v, t in zip(torch.split(yd_all, ysz), sets[0])]
-    h2d = hx_all.numel() * 2
-    d2h = hy_all.numel() * 2
+    # headline: 70B decode
+    reg = _decode_region(LINEARS, args, world, torch, awq, stream, clocks)
+    t_max = reduce_max(reg["t_step"], world)
+    nbytes = reg["nbytes"]
+    value = world * nbytes / t_max / 1e9
+    achieved = nbytes / reg["t_step"] / 1e9
+    e2e, e2e_graph = _e2e(reg, args, world, torch, stream)
+    del reg["sets"]
+    torch.cuda.empty_cache()
 
-    # the layers are built once (weights validated once, as at model load); each call checks
-    # only its activations and output
-    layers = [[awq.AwqLinear(t["qweight"], t["qzeros"], t["scales"], t["bias"], t["G"]) for t in ts]
-              for ts in sets]
-    sp = stream.cuda_stream
-
-    def e2e_step(r):
-        xd_all.copy_(hx_all, non_blocking=True)
-        for lin, xv, yv in zip(layers[r], xd, yd):
-            lin(xv, out=yv, stream=sp)
-        hy_all.copy_(yd_all, non_blocking=True)
-        stream.synchronize()
-
-    e2e_steps = min(args.steps, 2000)
-    for i in range(max(args.warmup, 3)):
-        e2e_step(i % R)
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
-        e2e_step(i % R)
-    e1.record(stream)
-    e1.synchronize()
-    e2e_el = reduce_max(e0.elapsed_time(e1) / 1e3, world)
-
-    # the same steps replayed from CUDA graphs (one per weight set, each holding the input
-    # copy, the three calls and the output copy), a synchronize per step: what a serving
-    # loop that captures its decode step pays, without the per-call host overhead
-    graphs = []
-    cap_stream = torch.cuda.Stream()  # graphs are captured on a side stream
-    cap_stream.wait_stream(stream)
-    for r in range(R):
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=cap_stream):
-            xd_all.copy_(hx_all, non_blocking=True)
-            for lin, xv, yv in zip(layers[r], xd, yd):
-                lin(xv, out=yv, stream=cap_stream.cuda_stream)
-            hy_all.copy_(yd_all, non_blocking=True)
-        graphs.append(gr)
-    stream.wait_stream(cap_stream)
-    for i in range(max(args.warmup, 3)):
-        graphs[i % R].replay()
-        stream.synchronize()
-    barrier(world)
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    for i in range(e2e_steps):
-        graphs[i % R].replay()
-        stream.synchronize()
-    g1.record(stream)
-    g1.synchronize()
-    e2e_graph_el = reduce_max(g0.elapsed_time(g1) / 1e3, world)
-    del graphs
-
-    peak, peak_kind = peaks()
-    achieved = nbytes * args.steps / elapsed / 1e9
-    value = job_gbs(nbytes, args.steps, world, elapsed_max)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps * 1e3,
+        "warmup": args.warmup, "ms_per_step": t_max * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_NAME, "M": 1, "group_size": 128, "bias": True,
                    "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {R} rotating weight sets, "
-                         f"{R * per_set / 1e6:.0f} MB > 129 MB",
-                   "bytes_per_step": nbytes, "launch": "CUDA graph replays"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": peak_kind,
-                     "kernel": "decode_kernel (awq_gemm decode path)",
+                   "l2": f"inputs larger than L2: {reg['R']} rotating weight sets, "
+                         f"{reg['R'] * reg['per_set'] / 1e6:.0f} MB > 3 x 129 MB",
+                   "bytes_per_step": nbytes, "launch": "CUDA graph replays of AwqLinear calls",
+                   "timing": f"{reg['reps']} repetitions of {args.steps} steps "
+                             f"({reg['timed_s']:.3f} s timed); median repetition"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "peak_source": hbm_kind + " (hbm_gbs, STREAM copy)",
+                     "kernel": "decode_tma_kernel (awq_gemm decode path)",
                      "traffic": measured_traffic(),
-                     "traffic_unit": "bytes per launch (mean of the three linears)"},
-        "e2e": {"value": world * nbytes * e2e_steps / e2e_el / 1e9, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "e2e_graph": {"value": world * nbytes * e2e_steps / e2e_graph_el / 1e9, "unit": UNIT,
-                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                      "note": "input copy, three calls, output copy per step, replayed from "
-                              "CUDA graphs; a synchronize per step"},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
+                     "traffic_unit": "bytes per launch (mean of the three linears)",
+                     "algorithmic_bytes_per_launch": nbytes / len(LINEARS)},
+        "e2e": e2e,
+        "e2e_graph": e2e_graph,
+        "gpu_launches": reg["launches"],
     }
+    windows = {"": reg["win"], "e2e": e2e.pop("win"), "e2e_graph": e2e_graph.pop("win")}
+    if not args.decode_only:
+        r7 = _decode_region(LINEARS_7B, args, world, torch, awq, stream, clocks)
+        del r7["sets"]
+        torch.cuda.empty_cache()
+        t7 = reduce_max(r7["t_step"], world)
+        line["decode_7b"] = {
+            "workload": WORKLOAD_7B, "value": world * r7["nbytes"] / t7 / 1e9, "unit": UNIT,
+            "ms_per_step": t7 * 1e3, "bytes_per_step": r7["nbytes"],
+            "roofline": {"bound": "hbm", "achieved": r7["nbytes"] / r7["t_step"] / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": r7["nbytes"] / r7["t_step"] / 1e9 / hbm,
+                         "peak_source": hbm_kind},
+            "timing": f"{r7['reps']} repetitions of {args.steps} steps ({r7['timed_s']:.3f} s); "
+                      f"{r7['R']} rotating weight sets; CUDA graph replays",
+            "gpu_launches": r7["launches"]}
+        windows["decode_7b"] = r7["win"]
+        pf = _prefill_region(args, world, torch, awq, stream, clocks)
+        flop = step_flop(PREFILL)
+        tp = reduce_max(pf["t_step"], world)
+        peak_s, src_s = tensor_peak(sustained=True)
+        peak_b, _ = tensor_peak(sustained=False)
+        ach = flop / pf["t_step"] / 1e12
+        line["prefill"] = {
+            "workload": WORKLOAD_PREFILL, "metric": "TFLOP/s", "value": world * flop / tp / 1e12,
+            "unit": "TFLOP/s", "ms_per_step": tp * 1e3, "flop_per_step": flop, "path": pf["path"],
+            "roofline": {"bound": "tensor", "achieved": ach, "peak": peak_s, "unit": "TFLOP/s",
+                         "frac": ach / peak_s, "peak_source": src_s + ": the step loop runs for "
+                         "seconds under the power cap", "frac_of_burst_peak": ach / peak_b,
+                         "kernel": "prefill_kernel (tcgen05/TMEM)", "traffic": None},
+            "timing": f"{pf['reps']} repetitions of {args.steps} steps ({pf['timed_s']:.3f} s); "
+                      "eager launches; inputs larger than L2 (x 67-235 MB per linear)",
+            "dequant_plus_cublas": {"ms_per_step": pf["t_ref"] * 1e3,
+                                    "TFLOP_s": flop / pf["t_ref"] / 1e12,
+                                    "note": "awq_dequant to a dense fp16 weight, then torch.addmm "
+                                            "(cuBLAS), per linear: comparator, not the product"},
+            "gpu_launches": pf["launches"]}
+        windows["prefill"] = pf["win"]
+        windows["prefill.dequant_plus_cublas"] = pf["ref_win"]
+    # clock samples of every timed region (the sampler ran throughout)
+    for key, (w0, w1) in windows.items():
+        clk = clocks.window(w0, w1)
+        if key == "":
+            line["clocks"] = clk
+        elif "." in key:
+            a, b = key.split(".")
+            line[a][b]["clocks"] = clk
+        else:
+            line[key]["clocks"] = clk
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     return line if rank == 0 else None
@@ -780,10 +995,12 @@ def run_cpu_oracle(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="headline decode step (and its end-to-end runs) only, no extra blocks")
     ap.add_argument("--case", default=None,
                     help="profiling mode: run only this workload linear (see synth.WORKLOADS, or "
                          "w8_m<M>_<K>x<N> for 8-bit codes)")

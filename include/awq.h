@@ -229,12 +229,11 @@ awq_status_t awq_quantize_rtn(const void* w_f16, int64_t N, int64_t K, int64_t g
  * without launching").  Exactly one kernel launch otherwise.
  * Accuracy: |y - y_exact| <= 1e-2 * max(1, |y_exact|) elementwise, y_exact being the
  * same sum in exact arithmetic.
- * Stream ordering: the small-M kernel is launched as a programmatic dependent launch and
- * starts reading qweight, qzeros, scales and bias before the kernel issued just before
- * it on `stream` has finished; x is read and y written only after that kernel's results
- * are visible.  So those four weight tensors must be complete before the preceding
- * kernel launch on the same stream (not written by that kernel); any earlier work, copy
- * or event dependency is ordered as usual.
+ * Stream ordering: plain stream order.  The small-M kernel is a programmatic dependent
+ * launch (its set-up overlaps the tail of the preceding kernel on `stream`), but it reads
+ * no input and writes no output before that kernel's results are visible, so a kernel
+ * that writes x or the weights (awq_quantize_rtn, a copy kernel, ...) may come directly
+ * before it.  awq_gemm_any with AWQ_GEMM_STATIC_WEIGHTS relaxes this for the weights.
  */
 awq_status_t awq_gemm(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,
                       const void* scales_f16, const void* bias_f16,
@@ -247,6 +246,30 @@ awq_status_t awq_gemm_ex(const void* x_f16, const int32_t* qweight, const int32_
                          const void* scales_f16, const void* bias_f16,
                          int64_t M, int64_t K, int64_t N, int64_t group_size,
                          void* y_f16, awq_path_t path, awq_stream_t stream);
+
+/* Flags of awq_gemm_any. */
+typedef enum awq_gemm_flags {
+  AWQ_GEMM_DEFAULT = 0,
+  /* The caller promises that qweight, qzeros, scales and bias are complete before the kernel
+   * launched immediately before this call on `stream` is launched (weights loaded once, as
+   * at model load): the small-M kernel then starts streaming them before that kernel has
+   * finished, under its tail.  x is still read, and y written, only after that kernel's
+   * results are visible.  Breaking the promise (e.g. the preceding kernel writes the
+   * weights) gives unspecified y. */
+  AWQ_GEMM_STATIC_WEIGHTS = 1
+} awq_gemm_flags_t;
+
+/*
+ * awq_gemm_any -- one entry point for every activation type and code width, with flags:
+ * dtype AWQ_DTYPE_F16 (the awq_gemm_ex contract) or AWQ_DTYPE_BF16 (awq_gemm_bf16_ex),
+ * bits 4 (qweight [K, N/8]) or 8 (awq_gemm_w8_ex: qweight [K, N/4], fp16 only); flags a
+ * combination of awq_gemm_flags_t (unknown bits: AWQ_ERR_INVALID_ARGUMENT).  With
+ * AWQ_GEMM_DEFAULT it behaves exactly as the matching entry point above.
+ */
+awq_status_t awq_gemm_any(const void* x, const int32_t* qweight, const int32_t* qzeros,
+                          const void* scales, const void* bias, int64_t M, int64_t K, int64_t N,
+                          int64_t group_size, void* y, awq_dtype_t dtype, int32_t bits,
+                          awq_path_t path, uint32_t flags, awq_stream_t stream);
 
 /* The family awq_gemm would pick for this shape and these pointers (no launch; above
  * 32 rows it reads the current device's SM count, 152 if there is none).  Returns

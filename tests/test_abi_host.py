@@ -210,3 +210,20 @@ def test_select_path_ex_is_host_only(lib):
     assert sel(1, 4096, 4096, 128, A, A, A, A, None, B, BF16, 8) == 0      # 8-bit bf16: invalid
     assert sel(1, 4096, 4096, 128, A, A, A, A, None, B, 1, 4) == 0         # f32 activations: invalid
     assert sel(1, 256, 12, 128, A, A, A, A, None, B, F16, 4) == 0          # N % 8 at 4 bits
+
+
+def test_gemm_any_argument_checks_are_host_side(lib):
+    import torch
+    g = lib.awq_gemm_any
+    F16, F32, BF16, AUTO = 0, 1, 2, 0
+    # (x, qweight, qzeros, scales, bias, M, K, N, G, y, dtype, bits, path, flags, stream)
+    assert g(A, A, A, A, None, 1, 256, 64, 128, B, F16, 4, AUTO, 2, None) == INVALID   # unknown flag
+    assert g(A, A, A, A, None, 1, 256, 64, 128, B, F32, 4, AUTO, 0, None) == INVALID   # f32 activations
+    assert g(A, A, A, A, None, 1, 256, 64, 128, B, F16, 6, AUTO, 0, None) == INVALID   # 6-bit codes
+    assert g(A, A, A, A, None, 1, 256, 64, 128, B, BF16, 8, AUTO, 0, None) == INVALID  # 8-bit bf16
+    assert g(A, A, A, A, None, 1, 256, 64, 128, B, F16, 4, 7, 1, None) == INVALID      # bad path
+    assert g(A, A, A, A, None, 1, 256, 12, 128, B, F16, 4, AUTO, 1, None) == SHAPE     # N % 8 (4 bits)
+    assert g(A, A, A, A, None, 1, 256, 12, 128, B, F16, 8, AUTO, 1, None) != SHAPE     # N % 4 (8 bits)
+    assert g(A, A, A, A, None, 0, 256, 64, 128, B, BF16, 4, AUTO, 1, None) == 0        # M == 0
+    if not torch.cuda.is_available():
+        assert g(A, A, A, A, None, 1, 256, 64, 128, B, F16, 4, AUTO, 1, None) == DEVICE

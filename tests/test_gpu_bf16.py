@@ -1,12 +1,19 @@
 """GPU parity of the bf16 entry points (awq_gemm_bf16, awq_dequant_bf16; the native GEMM's
 declared FP16/BF16 contract, GPTQModel wiki "AWQ", "Selection and compatibility") against
 the CPU oracle on the same seeded inputs (synth draws rounded to bf16).  Dequant must be
-bit-exact.  The GEMM is held to a bound derived from its arithmetic (no page fixes a bf16
-tolerance): a kernel may round each dequantized weight once to bf16 (relative error at
-most 2^-8: 8 significant bits), accumulates in fp32 and rounds y once to bf16, so
-    |y - y_ref| <= (2^-8 + K 2^-24) * sum_k |x_k| |w_k| + 2^-8 |y_ref| + 1e-6
-elementwise; and the GEMM must be bit-exact (after the oracle's own bf16 rounding) where
-every product and partial sum is exact."""
+bit-exact.  The GEMM is held to the fp16 path's criterion, |y - y_ref| <= 1e-2 *
+max(1, |y_ref|) elementwise, against the reference its arithmetic defines:
+
+* kernels that carry exact weights into an fp32 accumulation (the decode kernel up to 16
+  rows: codes as the exact bf16 values 128 + c with zero and scale folded per group; the
+  generic kernel) against the oracle's fp64 GEMM of the exact weights;
+* kernels that round each dequantized weight once to bf16 for the tensor core (prefill,
+  and decode's 17..32-row tiles) against the fp64 GEMM of the oracle's bf16-rounded
+  dequant (``oracle.dequant_bf16``): weight rounding alone (2^-9 relative, random signs)
+  moves y by about 2^-9 sqrt(K) rms(x w), which reaches the 1e-2 criterion at K >= 2048.
+
+and the GEMM must be bit-exact (after the oracle's own bf16 rounding) where every product
+and partial sum is exact."""
 import numpy as np
 import pytest
 import torch
@@ -36,33 +43,44 @@ def to_dev(d):
 
 
 def run(awq, d, path="auto"):
+    """y (as fp32) and the kernel family that ran."""
     t = to_dev(d)
+    used = path if path != "auto" else awq.select_path(t["x"], t["qweight"], t["qzeros"],
+                                                        t["scales"], t["bias"], d["group_size"])
     y = awq.awq_gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], t["bias"],
                      group_size=d["group_size"], path=path)
     torch.cuda.synchronize()
     assert y.dtype == torch.bfloat16
-    return y.float().cpu().numpy()
+    return y.float().cpu().numpy(), used
 
 
-def abs_product(d, rows=None, cols=None):
-    """sum_k |x[m, k]| |w[k, n]| for all (m, n), or for the sampled pairs."""
+def rounds_weights(used, M):
+    """The kernel rounds each dequantized weight once to bf16 (its tensor-core operand)."""
+    return used == "prefill" or (used == "decode" and M > 16)
+
+
+def reference(d, rounded, rows=None, cols=None):
+    """fp64 y of the exact weights (the oracle's GEMM), or of the weights rounded once to
+    bf16 (the oracle's dequant_bf16); all (m, n), or the sampled pairs."""
     G = d["group_size"]
+    args = (d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    if not rounded:
+        return oracle.gemm(*args) if rows is None else oracle.gemm_sampled(*args, rows, cols)
+    b = 0.0 if d["bias"] is None else d["bias"].astype(np.float64)
     if rows is None:
-        W = oracle.dequant_f32(d["qweight"], d["qzeros"], d["scales"], G).astype(np.float64)
-        return np.abs(d["x"].astype(np.float64)) @ np.abs(W)
+        W = oracle.dequant_bf16(d["qweight"], d["qzeros"], d["scales"], G).astype(np.float64)
+        return d["x"].astype(np.float64) @ W + b
     ucols, inv = np.unique(cols, return_inverse=True)
-    Wc = oracle.dequant_columns_f32(d["qweight"], d["qzeros"], d["scales"], G, ucols)
-    xa = np.abs(d["x"][rows].astype(np.float64))
-    return np.einsum("sk,sk->s", xa, np.abs(Wc[:, inv].T.astype(np.float64)))
+    Wc = oracle.round_to_bf16(oracle.dequant_columns_f32(d["qweight"], d["qzeros"], d["scales"],
+                                                        G, ucols)).astype(np.float64)
+    out = np.einsum("sk,sk->s", d["x"][rows].astype(np.float64), Wc[:, inv].T)
+    return out + (0.0 if d["bias"] is None else d["bias"][cols].astype(np.float64))
 
 
-def assert_close(y, y_ref, what, d, rows=None, cols=None):
-    K = d["K"]
-    bound = (2.0 ** -8 + K * 2.0 ** -24) * abs_product(d, rows, cols) + 2.0 ** -8 * np.abs(y_ref) + 1e-6
-    err = np.abs(y.astype(np.float64) - y_ref)
+def assert_close(y, y_ref, what):
     assert np.isfinite(y).all(), what
-    worst = float((err / bound).max())
-    assert worst <= 1.0, f"{what}: worst |err| / bound = {worst:.3f}"
+    ok, worst = oracle.within_tolerance(y.astype(np.float64), y_ref, 1e-2)
+    assert ok, f"{what}: worst |err|/(1e-2*max(1,|ref|)) = {worst:.3f}"
 
 
 def decode_ok(K, N, G):
@@ -95,9 +113,8 @@ def test_gemm_bf16_small_vs_oracle(awq, M, K, N, G, bias, path):
     if path in ("decode", "prefill") and not decode_ok(K, N, G):
         pytest.skip("shape outside the tensor-core kernels' contract")
     d = synth.awq_linear(8800 + M + K + N, M, K, N, group_size=G, bias=bias, dtype="bf16")
-    y = run(awq, d, path)
-    y_ref = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
-    assert_close(y, y_ref, f"bf16 {path} M={M} K={K} N={N} G={G}", d)
+    y, used = run(awq, d, path)
+    assert_close(y, reference(d, rounds_weights(used, M)), f"bf16 {path}->{used} M={M} K={K} N={N} G={G}")
 
 
 @pytest.mark.parametrize("M", [1, 5, 8, 16, 32, 300])
@@ -107,7 +124,7 @@ def test_gemm_bf16_exact_case_bitwise(awq, M, path):
     # exact in fp32 on every path, so y must be the oracle's value rounded once to bf16
     d = synth.awq_linear(9700 + M, M, 2048, 384, group_size=128, bias=True, x_kind="smallint",
                          scale_kind="pow2", bias_kind="dyadic", dtype="bf16")
-    y = run(awq, d, path)
+    y, _ = run(awq, d, path)
     y_ref = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128)
     want = oracle.round_to_bf16(y_ref.astype(np.float32))
     assert np.array_equal(y.view(np.uint32), want.view(np.uint32))
@@ -122,22 +139,21 @@ WORK = [(1, 4096, 11008, 128), (1, 11008, 4096, 128), (8, 4096, 4096, 128), (16,
 @pytest.mark.parametrize("M,K,N,G", WORK)
 def test_gemm_bf16_workload_shapes(awq, M, K, N, G):
     d = synth.awq_linear(9900 + M + K, M, K, N, group_size=G, bias=True, dtype="bf16")
-    y = run(awq, d)
-    args = (d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    y, used = run(awq, d)
+    rounded = rounds_weights(used, M)
     if M * K * N <= 32 * 4096 * 11008 and K * N <= 64 * 1024 * 1024:
-        assert_close(y, oracle.gemm(*args), f"bf16 M={M} K={K} N={N}", d)
+        assert_close(y, reference(d, rounded), f"bf16 {used} M={M} K={K} N={N}")
     else:
         rng = np.random.default_rng(3)
         rows = np.concatenate([rng.integers(0, M, 2048), [0, M - 1]])
         cols = np.concatenate([rng.integers(0, N, 2048), [0, N - 1]])
-        assert_close(y[rows, cols], oracle.gemm_sampled(*args, rows, cols), f"bf16 M={M} K={K} N={N}",
-                     d, rows, cols)
+        assert_close(y[rows, cols], reference(d, rounded, rows, cols), f"bf16 {used} M={M} K={K} N={N}")
 
 
 @pytest.mark.parametrize("M", [1, 16, 600])
 def test_gemm_bf16_deterministic(awq, M):
     d = synth.awq_linear(9950 + M, M, 4096, 1024, group_size=128, bias=True, dtype="bf16")
-    a, b = run(awq, d), run(awq, d)
+    a, b = run(awq, d)[0], run(awq, d)[0]
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 

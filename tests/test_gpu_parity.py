@@ -230,6 +230,17 @@ def test_workload_parity(awq, name):
     assert np.all(np.isfinite(y.astype(np.float32)))
 
 
+def test_workload_70b_prefill_full_matrix(awq):
+    # every element of one 70B prefill linear (M = 4096, 8192 x 8192, bias) against the plain
+    # C oracle (fp64, OpenMP over rows on the host cores), not a sample
+    from oracle import c_oracle
+    d = synth.workload_inputs("70b_m4096_8192x8192")
+    y = run_gemm(awq, d)
+    y_ref = c_oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], d["group_size"])
+    assert y.shape == y_ref.shape == (4096, 8192)
+    assert_close(y, y_ref, "70b_m4096_8192x8192 (full matrix)")
+
+
 @pytest.mark.parametrize("M", [33, 64, 100, 192, 256])
 @pytest.mark.parametrize("path", ["auto", "decode", "prefill"])
 def test_medium_batch_both_families(awq, M, path):

@@ -102,6 +102,32 @@ def test_quantize_then_gemm(awq):
     assert ok, worst
 
 
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_quantize_then_gemm_back_to_back(awq, M):
+    # the quantizer rewrites the weight buffers and awq_gemm runs directly after it on the
+    # same stream, no copy or synchronize between: the GEMM must see the new weights (its
+    # programmatic launch may overlap the quantizer's tail, its reads may not)
+    N, K, G = 11008, 4096, 128
+    wa, wb = _weights(31, N, K), _weights(32, N, K)
+    x = synth.awq_linear(33 + M, M, K, 8, group_size=G)["x"]
+    xd = torch.from_numpy(x).cuda()
+    wad, wbd = torch.from_numpy(wa).cuda(), torch.from_numpy(wb).cuda()
+    out = (torch.empty((K, N // 8), dtype=torch.int32, device="cuda"),
+           torch.empty((K // G, N // 8), dtype=torch.int32, device="cuda"),
+           torch.empty((K // G, N), dtype=torch.float16, device="cuda"))
+    y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    torch.cuda.synchronize()
+    awq.awq_quantize_rtn(wad, group_size=G, out=out)
+    awq.awq_gemm(xd, *out, None, group_size=G, out=y)
+    awq.awq_quantize_rtn(wbd, group_size=G, out=out)
+    awq.awq_gemm(xd, *out, None, group_size=G, out=y)
+    got = y.cpu().numpy()
+    rqw, rqz, rsc = oracle.quantize_rtn(wb, G)
+    y_ref = oracle.gemm(x, rqw, rqz, rsc, None, G)
+    ok, worst = oracle.within_tolerance(got.astype(np.float64), y_ref, 1e-2)
+    assert ok, worst
+
+
 def test_quantize_empty_and_errors(awq):
     w = torch.zeros((0, 64), dtype=torch.float16, device="cuda")
     qw, qz, sc = awq.awq_quantize_rtn(w, group_size=32)

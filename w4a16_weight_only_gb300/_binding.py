@@ -41,7 +41,10 @@ SIGNATURES = {
     "awq_gemm_w8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "awq_gemm_w8_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp]),
     "awq_dequant_w8": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp]),
+    "awq_gemm_any": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _i32, _i32,
+                            ctypes.c_uint32, _vp]),
 }
+GEMM_STATIC_WEIGHTS = 1
 
 _lib = None
 _lock = threading.Lock()
@@ -124,13 +127,14 @@ def _groups(K, group_size):
 
 
 def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, path="auto",
-             stream=None):
-    """y = x @ dequant(qweight, qzeros, scales) (+ bias) via the library's awq_gemm, or
-    awq_gemm_bf16 when x is bfloat16.
+             stream=None, static_weights=False):
+    """y = x @ dequant(qweight, qzeros, scales) (+ bias) via the library's awq_gemm_any
+    (fp16 or bf16 activations, 4-bit codes).
 
     x fp16 or bf16 [M, K] (leading dims are flattened), qweight int32 [K, N/8], qzeros int32
     [K/G, N/8], scales [K/G, N] and bias [N] (or None) of x's dtype.  Returns [..., N] of
-    x's dtype.
+    x's dtype.  static_weights=True passes AWQ_GEMM_STATIC_WEIGHTS: the weights must then
+    be complete before the kernel launched just before this call on the stream.
     """
     lib = load_library()
     lead = x.shape[:-1]
@@ -151,27 +155,36 @@ def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, pa
         out = torch.empty((M, N), dtype=dt, device=dev)
     else:
         _need(out, "out", dt, (M, N), dev)
-    fn = lib.awq_gemm_bf16_ex if dt == torch.bfloat16 else lib.awq_gemm_ex
-    st = fn(_ptr(x2), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
-            M, K, N, group_size, _ptr(out), PATHS[path], _stream(stream))
+    st = lib.awq_gemm_any(_ptr(x2), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
+                          M, K, N, group_size, _ptr(out),
+                          DTYPE_BF16 if dt == torch.bfloat16 else DTYPE_F16, 4, PATHS[path],
+                          GEMM_STATIC_WEIGHTS if static_weights else 0, _stream(stream))
     _check(st)
     return out.reshape(*lead, N)
 
 
 class AwqLinear:
     """An AWQ linear layer whose weights are validated once: ``layer(x)`` runs
-    ``awq_gemm_ex`` (fp16), ``awq_gemm_bf16_ex`` (bf16 scales) or ``awq_gemm_w8_ex``
-    (``bits=8``) with only x and out checked per call.
+    ``awq_gemm_any`` (fp16 or bf16 activations, 4- or 8-bit codes) with only x and out
+    checked per call.
 
     qweight int32 [K, N/8] (4 bits) or [K, N/4] (8 bits), qzeros int32 [K/G, N/8 or N/4],
     scales fp16 or bf16 [K/G, N] (it sets the activation dtype; 8 bits: fp16), bias [N] of
     the same dtype or None, all contiguous on one CUDA device.  The layer keeps references
-    to the tensors; it reads them in place on every call (in-place updates are seen)."""
+    to the tensors and reads them in place on every call.
 
-    __slots__ = ("K", "N", "group_size", "bits", "dtype", "device", "_fn", "_w", "_path",
-                 "_tensors")
+    static_weights=True (the default: weights loaded once, as at model load) passes
+    AWQ_GEMM_STATIC_WEIGHTS, so a small-M call starts streaming the weights under the tail
+    of the kernel launched just before it.  The weights must then be complete before that
+    kernel is launched: a kernel that updates them in place must not be the one launched
+    immediately before a call on the same stream (use static_weights=False for such
+    layers)."""
 
-    def __init__(self, qweight, qzeros, scales, bias=None, group_size=128, bits=4, path="auto"):
+    __slots__ = ("K", "N", "group_size", "bits", "dtype", "device", "_w", "_path",
+                 "_tensors", "_dt", "_flags")
+
+    def __init__(self, qweight, qzeros, scales, bias=None, group_size=128, bits=4, path="auto",
+                 static_weights=True):
         lib = load_library()
         if bits not in (4, 8):
             raise ValueError("bits must be 4 or 8")
@@ -192,8 +205,8 @@ class AwqLinear:
             _need(bias, "bias", dt, (N,), dev)
         self.K, self.N, self.group_size, self.bits = K, N, group_size, bits
         self.dtype, self.device = dt, dev
-        self._fn = (lib.awq_gemm_w8_ex if bits == 8
-                    else lib.awq_gemm_bf16_ex if dt is torch.bfloat16 else lib.awq_gemm_ex)
+        self._dt = DTYPE_BF16 if dt is torch.bfloat16 else DTYPE_F16
+        self._flags = GEMM_STATIC_WEIGHTS if static_weights else 0
         self._w = (qweight.data_ptr(), qzeros.data_ptr(), scales.data_ptr(), _ptr(bias))
         self._path = PATHS[path]
         self._tensors = (qweight, qzeros, scales, bias)
@@ -216,17 +229,17 @@ class AwqLinear:
             raise ValueError(f"out must be a contiguous {dt} [..., {N}] tensor of {M} rows "
                              f"on device {self.device}")
         w = self._w
-        st = self._fn(x.data_ptr(), w[0], w[1], w[2], w[3], M, K, N, self.group_size,
-                      out.data_ptr(), self._path,
-                      (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None
-                      else torch.cuda.current_stream().cuda_stream)
+        st = _lib.awq_gemm_any(x.data_ptr(), w[0], w[1], w[2], w[3], M, K, N, self.group_size,
+                               out.data_ptr(), self._dt, self.bits, self._path, self._flags,
+                               (stream if isinstance(stream, int) else stream.cuda_stream)
+                               if stream is not None else torch.cuda.current_stream().cuda_stream)
         if st != AWQ_OK:
             raise AwqError(st, last_error())
         return out
 
 
 def awq_gemm_w8(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, path="auto",
-                stream=None):
+                stream=None, static_weights=False):
     """y = x @ dequant8(qweight, qzeros, scales) (+ bias) via awq_gemm_w8: 8-bit codes,
     qweight int32 [K, N/4], qzeros int32 [K/G, N/4], scales fp16 [K/G, N]; x fp16 [M, K]."""
     lib = load_library()
@@ -247,8 +260,9 @@ def awq_gemm_w8(x, qweight, qzeros, scales, bias=None, group_size=128, out=None,
         out = torch.empty((M, N), dtype=torch.float16, device=dev)
     else:
         _need(out, "out", torch.float16, (M, N), dev)
-    st = lib.awq_gemm_w8_ex(_ptr(x2), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
-                            M, K, N, group_size, _ptr(out), PATHS[path], _stream(stream))
+    st = lib.awq_gemm_any(_ptr(x2), _ptr(qweight), _ptr(qzeros), _ptr(scales), _ptr(bias),
+                          M, K, N, group_size, _ptr(out), DTYPE_F16, 8, PATHS[path],
+                          GEMM_STATIC_WEIGHTS if static_weights else 0, _stream(stream))
     _check(st)
     return out.reshape(*lead, N)
 

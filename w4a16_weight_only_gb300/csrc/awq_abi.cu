@@ -248,19 +248,35 @@ awq_status_t awq_quantize_rtn(const void* w_f16, int64_t N, int64_t K, int64_t g
 static awq_status_t gemm_any(const void* x, const int32_t* qweight, const int32_t* qzeros,
                       const void* scales, const void* bias, int64_t M, int64_t K, int64_t N,
                       int64_t group_size, void* y, awq_path_t path, awq_stream_t stream, bool bf16,
-                      int bits = 4) {
+                      int bits = 4, uint32_t flags = 0u) {
   if (path < AWQ_PATH_AUTO || path > AWQ_PATH_GENERIC)
     return fail(AWQ_ERR_INVALID_ARGUMENT, "unknown path %d", static_cast<int>(path));
+  if ((flags & ~static_cast<uint32_t>(AWQ_GEMM_STATIC_WEIGHTS)) != 0u)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", flags);
   awq::GemmProblem p{};
   bool empty = false;
   awq_status_t st = build_problem(x, qweight, qzeros, scales, bias, M, K, N, group_size, y,
                                   stream, &p, &empty, bf16, bits);
   if (st != AWQ_OK) return st;
   if (empty) return ok();
+  p.static_weights = (flags & AWQ_GEMM_STATIC_WEIGHTS) != 0u;
   st = check_device();
   if (st != AWQ_OK) return st;
   const awq::Path use = path == AWQ_PATH_AUTO ? choose_path(p) : static_cast<awq::Path>(path);
   return run(p, use);
+}
+
+awq_status_t awq_gemm_any(const void* x, const int32_t* qweight, const int32_t* qzeros,
+                          const void* scales, const void* bias, int64_t M, int64_t K, int64_t N,
+                          int64_t group_size, void* y, awq_dtype_t dtype, int32_t bits,
+                          awq_path_t path, uint32_t flags, awq_stream_t stream) {
+  if (dtype != AWQ_DTYPE_F16 && dtype != AWQ_DTYPE_BF16)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "dtype must be AWQ_DTYPE_F16 or AWQ_DTYPE_BF16");
+  if (bits != 4 && bits != 8) return fail(AWQ_ERR_INVALID_ARGUMENT, "bits must be 4 or 8 (got %d)", bits);
+  if (bits == 8 && dtype != AWQ_DTYPE_F16)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "8-bit codes take fp16 activations and scales");
+  return gemm_any(x, qweight, qzeros, scales, bias, M, K, N, group_size, y, path, stream,
+                  dtype == AWQ_DTYPE_BF16, bits, flags);
 }
 
 awq_status_t awq_gemm_ex(const void* x_f16, const int32_t* qweight, const int32_t* qzeros,

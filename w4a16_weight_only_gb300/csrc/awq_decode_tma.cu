@@ -84,6 +84,7 @@ struct __align__(64) TmaDecodeParams {
   const int* offsets;  // grouped: expert row offsets (device, E + 1), else null
   int E;               // grouped: experts
   int slice;   // floats of the packed partial each owner finishes (multiple of 4)
+  int early;   // 1: the caller declared the weights static; stream them before the grid wait
 };
 
 template <int TB, int CWL, int NW, int BITS = 4>
@@ -278,9 +279,11 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     tma_load_2d(x_ring + slot * p.x_pitch, &p.tm_x, &my_bars[slot], j * kRS, m0);
   };
 
-  // Weights do not depend on the preceding grid: stream them first.  Activations (and the
-  // output stores at the end) are ordered after it.
-  if (lane == 0)
+  // Static weights (declared by the caller: complete before the preceding kernel launch)
+  // do not depend on the preceding grid: stream them first, under its tail.  By default
+  // every read waits for the preceding grid.  Activations and the output stores are always
+  // ordered after it.
+  if (lane == 0 && p.early)
     for (int s = 0; s < S && j0 + s < j1; ++s) issue_weights(s, j0 + s);
 #if AWQ_DECODE_L2_PREFETCH
   // Stages past the ring: pull their packed weights (and any group rows they open) into
@@ -298,8 +301,11 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
 #ifdef AWQ_DECODE_DEBUG_TIME
   AWQ_DECODE_DEBUG_TIME(5);
 #endif
-  if (lane == 0)
+  if (lane == 0) {
+    if (!p.early)
+      for (int s = 0; s < S && j0 + s < j1; ++s) issue_weights(s, j0 + s);
     for (int s = 0; s < S && j0 + s < j1; ++s) issue_x(s, j0 + s);
+  }
 #if !AWQ_DECODE_LATE_TRIGGER
   launch_dependents();
 #endif
@@ -1036,6 +1042,7 @@ cudaError_t launch_v(const GemmProblem& p) {
   dp.owners = pl.owners; dp.slice = pl.slice;
   dp.offsets = p.offsets;
   dp.E = p.E;
+  dp.early = (p.static_weights && !GR) ? 1 : 0;
 
   const int nt = (C + GE::CW_W - 1) / GE::CW_W;
   const int mz = GR ? (p.M + 7) / 8 + p.E : (p.M + 8 * TB - 1) / (8 * TB);

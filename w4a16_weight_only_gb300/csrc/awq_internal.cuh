@@ -29,6 +29,10 @@ struct GemmProblem {
   // Code width: 4 (ORDER-interleaved nibbles, N/8 words a row) or 8 (little-endian bytes,
   // N/4 words a row; GPTQModel wiki "AWQ", "Saved formats and packing").
   int bits = 4;
+  // The caller declares qweight, qzeros, scales and bias complete before the kernel launched
+  // just before this one on the stream (AWQ_GEMM_STATIC_WEIGHTS): the small-M kernel may then
+  // stream them before its programmatic-launch wait.
+  bool static_weights = false;
 };
 
 // Kernel families; values equal awq_path_t.

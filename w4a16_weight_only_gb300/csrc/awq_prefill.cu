@@ -1023,19 +1023,12 @@ cudaError_t launch_prefill(const GemmProblem& p) {
   return cudaGetLastError();
 }
 
+// Looked up on every call (no cache): the address belongs to the current context, which a
+// device reset or a new context replaces.
 cudaError_t status_word_ptr(unsigned int** ptr) {
-  static unsigned int* cache[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && cache[dev]) {
-    *ptr = cache[dev];
-    return cudaSuccess;
-  }
   void* a = nullptr;
-  e = cudaGetSymbolAddress(&a, g_status_word);
+  const cudaError_t e = cudaGetSymbolAddress(&a, g_status_word);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64) cache[dev] = static_cast<unsigned int*>(a);
   *ptr = static_cast<unsigned int*>(a);
   return cudaSuccess;
 }
