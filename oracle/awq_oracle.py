@@ -58,6 +58,18 @@ What it computes, and where each step comes from:
   scales ``[K/G, N]``; ``w = (code - zero) * scale`` as for 4 bits
   (:func:`dequant8_f32`, :func:`gemm8`).
 
+* Tile-packed layout (:func:`repack`, :func:`unpack_repacked`): the optional one-off
+  conversion into a kernel-native layout (no page prints one; repacking the AWQ order
+  away for a kernel is the prior art of the vLLM article, section 5.1, and of the
+  GPTQModel wiki, "Marlin and Machete").  It is lossless on codes, zeros and scales and
+  needs K % 64 == 0 and G % 64 == 0.  For output-column tile t (columns 128t .. 128t+127)
+  and K stage s (rows 64s .. 64s+63) one block of 4608 bytes sits at byte (t*K/64 + s) *
+  4608: two halves h (rows 64s + 32h ..), each 128 columns x 4 words, word (h, c, j) at
+  index 512h + 4c + j holding the codes of column 128t + c for rows 64s + 32h + 8j + 0..7,
+  row offset ORDER[p] in nibble p (the checkpoint's column interleave, applied along K);
+  then 128 meta words, word c = scale bits (fp16) | zero << 16 of column 128t + c for the
+  group of row 64s.  Columns past N hold code 0, zero 0, scale 0.
+
 Pins (tests/test_oracle.py, run without a GPU): ORDER and its inverse from
 the wiki's "Saved formats and packing" section, a hand-packed word, AWQ-004
 (sequential-nibble decode differs), AWQ-005 (zero equal to code gives an
@@ -339,3 +351,98 @@ def gemm8(x, qweight, qzeros, scales, bias, group_size) -> np.ndarray:
         y = y + np.asarray(bias).astype(np.float64)[None, :]
     return y
 
+
+
+# ------------------------------------------------------------ tile-packed layout ----
+# The optional one-off repack into this library's kernel-native layout (see the module
+# docstring): blocks of PACK_TN columns x PACK_TK K rows.
+PACK_TN = 128
+PACK_TK = 64
+PACK_BLOCK_WORDS = PACK_TN * PACK_TK // 8 + PACK_TN  # 1024 code words + 128 meta words
+PACK_BLOCK_BYTES = 4 * PACK_BLOCK_WORDS              # 4608
+
+
+def repack_size(K: int, N: int, group_size: int) -> int:
+    """Bytes of the tile-packed layout: one block per (column tile, K stage)."""
+    G = resolve_group_size(K, group_size)
+    if K % PACK_TK != 0 or G % PACK_TK != 0 or N % 8 != 0:
+        raise ValueError("the tile-packed layout needs K % 64 == 0, G % 64 == 0, N % 8 == 0")
+    return -(-N // PACK_TN) * (K // PACK_TK) * PACK_BLOCK_BYTES
+
+
+def repack(qweight, qzeros, scales, group_size) -> np.ndarray:
+    """Checkpoint layout -> tile-packed layout, as uint32 words (see the module docstring).
+    Steps: unpack codes and zeros with the page's reader, pad the columns to whole tiles,
+    then write every block word by word."""
+    K, C = qweight.shape
+    N = 8 * C
+    G = resolve_group_size(K, group_size)
+    nbytes = repack_size(K, N, group_size)
+    codes = unpack_codes(qweight)                  # [K, N]
+    zeros = unpack_codes(qzeros)                   # [K/G, N]
+    sbits = np.ascontiguousarray(scales, dtype=np.float16).view(np.uint16).astype(np.uint64)
+    NT, KS = -(-N // PACK_TN), K // PACK_TK
+    Np = NT * PACK_TN
+    cp = np.zeros((K, Np), dtype=np.uint64)
+    cp[:, :N] = codes
+    zp = np.zeros((K // G, Np), dtype=np.uint64)
+    zp[:, :N] = zeros
+    sp = np.zeros((K // G, Np), dtype=np.uint64)
+    sp[:, :N] = sbits
+    out = np.zeros(nbytes // 4, dtype=np.uint64)
+    for t in range(NT):
+        cols = slice(PACK_TN * t, PACK_TN * (t + 1))
+        for s in range(KS):
+            base = (t * KS + s) * PACK_BLOCK_WORDS
+            blk = cp[PACK_TK * s:PACK_TK * (s + 1), cols]     # [64 rows, 128 columns]
+            for h in range(2):
+                for j in range(4):
+                    word = np.zeros(PACK_TN, dtype=np.uint64)
+                    for p in range(8):
+                        row = 32 * h + 8 * j + ORDER[p]
+                        word |= blk[row] << np.uint64(4 * p)
+                    out[base + 512 * h + 4 * np.arange(PACK_TN) + j] = word
+            g = (PACK_TK * s) // G
+            out[base + 1024:base + 1024 + PACK_TN] = sp[g, cols] | (zp[g, cols] << np.uint64(16))
+    return out.astype(np.uint32)
+
+
+def unpack_repacked(packed, K: int, N: int, group_size: int):
+    """Tile-packed words -> (codes [K, N], zeros [K/G, N], scales fp16 [K/G, N]), reading
+    every block back; the zero and scale of a group are taken from its first stage."""
+    G = resolve_group_size(K, group_size)
+    words = np.asarray(packed, dtype=np.uint32).astype(np.uint64)
+    assert words.size * 4 == repack_size(K, N, group_size)
+    NT, KS = -(-N // PACK_TN), K // PACK_TK
+    codes = np.zeros((K, NT * PACK_TN), dtype=np.int64)
+    zeros = np.zeros((K // G, NT * PACK_TN), dtype=np.int64)
+    sbits = np.zeros((K // G, NT * PACK_TN), dtype=np.uint16)
+    for t in range(NT):
+        for s in range(KS):
+            base = (t * KS + s) * PACK_BLOCK_WORDS
+            for h in range(2):
+                for j in range(4):
+                    word = words[base + 512 * h + 4 * np.arange(PACK_TN) + j]
+                    for p in range(8):
+                        row = PACK_TK * s + 32 * h + 8 * j + ORDER[p]
+                        codes[row, PACK_TN * t:PACK_TN * (t + 1)] = (word >> np.uint64(4 * p)) & np.uint64(0xF)
+            if (PACK_TK * s) % G == 0:
+                meta = words[base + 1024:base + 1024 + PACK_TN]
+                g = (PACK_TK * s) // G
+                sbits[g, PACK_TN * t:PACK_TN * (t + 1)] = (meta & np.uint64(0xFFFF)).astype(np.uint16)
+                zeros[g, PACK_TN * t:PACK_TN * (t + 1)] = (meta >> np.uint64(16)) & np.uint64(0xF)
+    return codes[:, :N], zeros[:, :N], sbits[:, :N].view(np.float16)
+
+
+def gemm_packed(x, packed, bias, K: int, N: int, group_size: int) -> np.ndarray:
+    """y = x @ W (+ bias) in fp64 with W read back from the tile-packed layout:
+    W[k, n] = (code[k, n] - zero[k // G, n]) * scale[k // G, n] in fp32, as :func:`gemm`."""
+    G = resolve_group_size(K, group_size)
+    codes, zeros, sc = unpack_repacked(packed, K, N, group_size)
+    g_of_k = np.arange(K) // G
+    W = ((codes.astype(np.float32) - zeros[g_of_k].astype(np.float32))
+         * sc[g_of_k].astype(np.float32)).astype(np.float64)
+    y = np.asarray(x).astype(np.float64) @ W
+    if bias is not None:
+        y = y + np.asarray(bias).astype(np.float64)[None, :]
+    return y

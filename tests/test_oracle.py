@@ -513,3 +513,90 @@ def test_w8_gemm_brute_force():
                 terms.append(float(d["x"][m, k]) * ((code - zero) * float(d["scales"][k // 16, n])))
             terms.append(float(d["bias"][n]))
             assert abs(y[m, n] - math.fsum(terms)) <= 1e-12 * max(1.0, abs(y[m, n]))
+
+
+# ------------------------------------------------------------ tile-packed layout ----
+
+def _packed_case(name):
+    """The two hand-worked inputs of tests/golden/packed_layout.txt."""
+    if name == "A":
+        K, N, G = 64, 8, 64
+    else:
+        K, N, G = 128, 136, 64
+    k = np.arange(K)[:, None]
+    n = np.arange(N)[None, :]
+    codes = (k + n) % 16
+    g = np.arange(K // G)[:, None]
+    if name == "A":
+        zeros = np.broadcast_to(n % 16, (1, N))
+        scales = (1.0 + n / 8.0).astype(np.float16)
+    else:
+        zeros = (n + 3 * g) % 16
+        scales = np.broadcast_to(2.0 ** -(g + 1.0), (K // G, N)).astype(np.float16)
+    return (oracle.pack_codes(codes), oracle.pack_codes(np.ascontiguousarray(zeros)),
+            np.ascontiguousarray(scales), K, N, G)
+
+
+def _golden_packed():
+    path = os.path.join(os.path.dirname(__file__), "golden", "packed_layout.txt")
+    sizes, words = {}, []
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        f = line.split()
+        if f[0] == "size":
+            sizes[f[1]] = int(f[2])
+        else:
+            words.append((f[0], int(f[1]), int(f[2], 16)))
+    return sizes, words
+
+
+def test_packed_layout_golden_words():
+    sizes, words = _golden_packed()
+    packed = {}
+    for name in ("A", "B"):
+        qw, qz, sc, K, N, G = _packed_case(name)
+        packed[name] = oracle.repack(qw, qz, sc, G)
+        assert packed[name].size == sizes[name]
+        assert oracle.repack_size(K, N, G) == 4 * sizes[name]
+    for name, idx, want in words:
+        assert int(packed[name][idx]) == want, (name, idx, hex(int(packed[name][idx])))
+
+
+@pytest.mark.parametrize("K,N,G", [(64, 8, 64), (128, 136, 64), (256, 384, 128), (512, 264, -1),
+                                   (192, 1032, 64), (1024, 128, 256)])
+def test_packed_round_trip_is_lossless(K, N, G):
+    # repack -> read back == the checkpoint reader's codes, zeros and scales (pinned to the
+    # pages above); the layout is only a permutation plus padding
+    d = awq_linear(300 + K + N, 1, K, N, group_size=G)
+    pk = oracle.repack(d["qweight"], d["qzeros"], d["scales"], G)
+    codes, zeros, sc = oracle.unpack_repacked(pk, K, N, G)
+    assert np.array_equal(codes, oracle.unpack_codes(d["qweight"]))
+    assert np.array_equal(zeros, oracle.unpack_codes(d["qzeros"]))
+    assert np.array_equal(sc.view(np.uint16), d["scales"].view(np.uint16))
+
+
+def test_packed_padding_and_group_copies():
+    # columns past N are all-zero words; every stage of a group carries the same meta row
+    K, N, G = 256, 136, 128
+    d = awq_linear(310, 1, K, N, group_size=G)
+    pk = oracle.repack(d["qweight"], d["qzeros"], d["scales"], G).reshape(2, K // 64, 1152)
+    assert not pk[1, :, 8 * 4:512].any() and not pk[1, :, 512 + 8 * 4:1024].any()
+    assert not pk[1, :, 1024 + 8:].any()
+    assert np.array_equal(pk[:, 0, 1024:], pk[:, 1, 1024:])
+    assert np.array_equal(pk[:, 2, 1024:], pk[:, 3, 1024:])
+    assert not np.array_equal(pk[:, 1, 1024:], pk[:, 2, 1024:])
+
+
+def test_packed_gemm_equals_checkpoint_gemm():
+    d = awq_linear(320, 3, 256, 264, group_size=64, bias=True)
+    pk = oracle.repack(d["qweight"], d["qzeros"], d["scales"], 64)
+    y = oracle.gemm_packed(d["x"], pk, d["bias"], 256, 264, 64)
+    assert np.array_equal(y, oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 64))
+
+
+def test_packed_rejects_unsupported_shapes():
+    for K, N, G in [(96, 64, 32), (128, 64, 32), (64, 12, 64)]:
+        with pytest.raises(ValueError):
+            oracle.repack_size(K, N, G)
