@@ -673,12 +673,18 @@ def run_case(args, local):
     t = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "qweight", "qzeros", "scales")}
     b = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
     y = torch.empty((d["M"], d["N"]), dtype=torch.float16, device="cuda")
-    for i in range(args.warmup + args.steps):
-        gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], b, group_size=d["group_size"],
-             out=y, path=args.path)
+    if args.packed:  # the tile-packed layout: one repack, then awq_gemm_packed calls
+        pk = awq.awq_repack(t["qweight"], t["qzeros"], t["scales"], d["group_size"])
+        for i in range(args.warmup + args.steps):
+            awq.awq_gemm_packed(t["x"], pk, b, d["K"], d["N"], d["group_size"], out=y)
+    else:
+        for i in range(args.warmup + args.steps):
+            gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], b, group_size=d["group_size"],
+                 out=y, path=args.path)
     torch.cuda.synchronize()
     awq.device_status()
-    print(json.dumps({"case": args.case, "path": args.path, "launches": args.warmup + args.steps}))
+    print(json.dumps({"case": args.case, "path": "packed" if args.packed else args.path,
+                      "launches": args.warmup + args.steps}))
 
 
 def run_sweep(args, local):
@@ -1005,6 +1011,8 @@ def main(argv=None):
                     help="profiling mode: run only this workload linear (see synth.WORKLOADS, or "
                          "w8_m<M>_<K>x<N> for 8-bit codes)")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "prefill", "generic"])
+    ap.add_argument("--packed", action="store_true",
+                    help="profiling mode: repack once, then call awq_gemm_packed")
     ap.add_argument("--sweep", action="store_true",
                     help="per-workload table (one JSON line per workload), not the bench line")
     ap.add_argument("--cpu-oracle", action="store_true",

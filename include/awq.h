@@ -287,6 +287,41 @@ awq_path_t awq_gemm_select_path_ex(int64_t M, int64_t K, int64_t N, int64_t grou
                                    const void* scales, const void* bias, const void* y,
                                    awq_dtype_t dtype, int32_t bits);
 
+/*
+ * Tile-packed layout: an optional one-off conversion of the checkpoint layout into this
+ * library's kernel-native order, and the linear that reads it.  (No page prints such a
+ * layout; converting the AWQ order away for a kernel is the prior art of the vLLM article,
+ * section 5.1, and of the GPTQModel wiki, "Marlin and Machete".)  Lossless on codes, zeros
+ * and scales.  For output-column tile t (128 columns) and K stage s (64 rows) one block of
+ * 1152 uint32 words at word (t * K/64 + s) * 1152:
+ *   word 512 h + 4 c + j (h < 2, c < 128, j < 4): 4-bit codes of column 128 t + c for rows
+ *     64 s + 32 h + 8 j + 0..7, row offset ORDER[p] in nibble p (ORDER = {0,2,4,6,1,3,5,7});
+ *   word 1024 + c: fp16 scale bits | zero << 16 of column 128 t + c, group of row 64 s;
+ *   columns past N: zero.
+ * Requirements: those of awq_dequant plus K % 64 == 0 and group size % 64 == 0 (or -1).
+ *
+ * awq_repack_size: bytes of the packed weights, ceil(N / 128) * (K / 64) * 4608 (host only,
+ *   no device access).
+ * awq_repack: writes them to packed_out (DEVICE, caller-owned, 16-byte aligned,
+ *   awq_repack_size bytes); reads qweight/qzeros/scales as awq_dequant does; K / 64 <=
+ *   65535.  One kernel launch, asynchronous on `stream`.  N == 0: AWQ_OK, no launch.
+ * awq_gemm_packed: y = fp16_rne(x W (+ bias)) as awq_gemm, W read from the packed layout
+ *   (x fp16 [M, K] 16-byte aligned, packed 16-byte aligned, bias fp16 [N] or NULL, y fp16
+ *   [M, N]; fp32 accumulation, a fixed summation order: repeated calls are bitwise
+ *   identical; |y - y_exact| <= 1e-2 * max(1, |y_exact|)).  A tcgen05 kernel whose
+ *   dequantized weights stay in tensor memory; built for prefill-sized M (any M >= 1 runs;
+ *   small M is faster through awq_gemm on the checkpoint layout).  M == 0 or N == 0:
+ *   AWQ_OK, no launch.  One kernel launch otherwise, asynchronous on `stream`, plain stream
+ *   order.
+ */
+awq_status_t awq_repack_size(int64_t K, int64_t N, int64_t group_size, size_t* bytes);
+awq_status_t awq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
+                        int64_t K, int64_t N, int64_t group_size, void* packed_out,
+                        awq_stream_t stream);
+awq_status_t awq_gemm_packed(const void* x_f16, const void* packed, const void* bias_f16,
+                             int64_t M, int64_t K, int64_t N, int64_t group_size, void* y_f16,
+                             awq_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the library's device status word on the
  * current device.  Returns AWQ_ERR_TIMEOUT if a kernel gave up a bounded wait since the
  * last check (its output is then unspecified), AWQ_OK otherwise. */

@@ -227,3 +227,33 @@ def test_gemm_any_argument_checks_are_host_side(lib):
     assert g(A, A, A, A, None, 0, 256, 64, 128, B, BF16, 4, AUTO, 1, None) == 0        # M == 0
     if not torch.cuda.is_available():
         assert g(A, A, A, A, None, 1, 256, 64, 128, B, F16, 4, AUTO, 1, None) == DEVICE
+
+
+def test_packed_layout_argument_checks_are_host_side(lib):
+    import ctypes
+    import torch
+    n = ctypes.c_size_t(0)
+    assert lib.awq_repack_size(8192, 28672, 128, ctypes.byref(n)) == 0
+    assert n.value == 224 * 128 * 4608
+    assert lib.awq_repack_size(128, 136, -1, ctypes.byref(n)) == 0 and n.value == 2 * 2 * 4608
+    assert lib.awq_repack_size(96, 64, 32, ctypes.byref(n)) == SHAPE     # K % 64
+    assert lib.awq_repack_size(256, 64, 32, ctypes.byref(n)) == SHAPE    # G % 64
+    assert lib.awq_repack_size(256, 12, 128, ctypes.byref(n)) == SHAPE   # N % 8
+    assert lib.awq_repack_size(256, 64, 128, None) == INVALID
+    r = lib.awq_repack
+    # (qweight, qzeros, scales, K, N, G, packed, stream)
+    assert r(A, A, A, 256, 64, 128, None, None) == INVALID
+    assert r(A, A, A, 256, 64, 32, B, None) == SHAPE
+    assert r(A, A, A, 256, 0, 128, B, None) == 0                         # N == 0: no launch
+    assert r(A, A, A, 256, 64, 128, P(0x200008), None) == MISALIGNED            # packed 16-byte aligned
+    g = lib.awq_gemm_packed
+    # (x, packed, bias, M, K, N, G, y, stream)
+    assert g(A, B, None, 4, 256, 64, 128, B, None) != SHAPE
+    assert g(A, B, None, 4, 96, 64, 32, B, None) == SHAPE
+    assert g(None, B, None, 4, 256, 64, 128, B, None) == INVALID
+    assert g(P(0x100002), B, None, 4, 256, 64, 128, B, None) == MISALIGNED      # x 16-byte aligned
+    assert g(A, B, None, 0, 256, 64, 128, B, None) == 0                  # M == 0: no launch
+    assert g(A, B, None, -1, 256, 64, 128, B, None) == INVALID
+    if not torch.cuda.is_available():
+        assert g(A, B, None, 4, 256, 64, 128, B, None) == DEVICE
+        assert r(A, A, A, 256, 64, 128, B, None) == DEVICE

@@ -1,0 +1,117 @@
+"""GPU parity of the tile-packed layout (awq_repack, awq_gemm_packed) against the CPU oracle
+on the same seeded inputs: the repacked words must equal the oracle's bit for bit (the
+layout is a lossless permutation plus padding); the linear on the packed weights must
+satisfy |y - y_ref| <= 1e-2 * max(1, |y_ref|) elementwise (fp16 output, fp32
+accumulation, y_ref fp64) and be bit-exact where every partial sum is exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def awq():
+    from w4a16_weight_only_gb300 import build
+    build.build()
+    import w4a16_weight_only_gb300 as awq
+    assert awq.runtime_available(), awq.last_error()
+    return awq
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def packed_of(awq, d):
+    return awq.awq_repack(dev(d["qweight"]), dev(d["qzeros"]), dev(d["scales"]), d["group_size"])
+
+
+def run(awq, d, pk=None):
+    pk = packed_of(awq, d) if pk is None else pk
+    b = None if d["bias"] is None else dev(d["bias"])
+    y = awq.awq_gemm_packed(dev(d["x"]), pk, b, d["K"], d["N"], d["group_size"])
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def assert_close(y, y_ref, what):
+    ok, worst = oracle.within_tolerance(y.astype(np.float64), y_ref, 1e-2)
+    assert ok, f"{what}: worst |err|/(1e-2*max(1,|ref|)) = {worst:.3f}"
+
+
+@pytest.mark.parametrize("K,N,G", [(64, 8, 64), (128, 136, 64), (256, 384, 128), (512, 264, -1),
+                                   (4096, 4096, 128), (11008, 4096, 128), (4096, 11008, -1),
+                                   (1024, 1032, 256)])
+def test_repack_bit_exact(awq, K, N, G):
+    d = synth.awq_linear(21000 + K + N, 1, K, N, group_size=G)
+    got = packed_of(awq, d)
+    torch.cuda.synchronize()
+    assert got.numel() * 4 == awq.awq_repack_size(K, N, G) == oracle.repack_size(K, N, G)
+    want = oracle.repack(d["qweight"], d["qzeros"], d["scales"], G)
+    assert np.array_equal(got.cpu().numpy().view(np.uint32), want)
+
+
+# token tiles of 64 (M <= 64), 128 (M <= 128) and 256 rows, ragged rows and column tiles,
+# one group per K (G = -1), several tiles per CTA
+SMALL = [(1, 256, 256, 128, False), (17, 512, 136, 64, True), (64, 1024, 264, 128, True),
+         (65, 256, 128, -1, False), (128, 2048, 512, 256, True), (129, 512, 392, 64, True),
+         (256, 1024, 256, 128, False), (300, 768, 1032, 64, True), (600, 512, 520, 128, True),
+         (1000, 256, 128, 64, False)]
+
+
+@pytest.mark.parametrize("M,K,N,G,bias", SMALL)
+def test_gemm_packed_vs_oracle(awq, M, K, N, G, bias):
+    d = synth.awq_linear(22000 + M + K + N, M, K, N, group_size=G, bias=bias)
+    y = run(awq, d)
+    y_ref = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    assert_close(y, y_ref, f"packed M={M} K={K} N={N} G={G}")
+
+
+@pytest.mark.parametrize("M", [1, 40, 100, 256, 300])
+def test_gemm_packed_exact_case_bitwise(awq, M):
+    # small-integer x, power-of-two scales, dyadic bias: every product and partial sum is
+    # exact in fp32, so y is the oracle's value rounded once to fp16
+    d = synth.awq_linear(23000 + M, M, 2048, 392, group_size=128, bias=True, x_kind="smallint",
+                         scale_kind="pow2", bias_kind="dyadic")
+    y = run(awq, d)
+    want = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
+
+
+def test_gemm_packed_deterministic(awq):
+    d = synth.awq_linear(23500, 700, 4096, 1024, group_size=128, bias=True)
+    pk = packed_of(awq, d)
+    a, b = run(awq, d, pk), run(awq, d, pk)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+@pytest.mark.parametrize("name", ["7b_prefill_m512_4096x11008", "7b_prefill_m2048_11008x4096",
+                                  "70b_m4096_8192x28672", "70b_m16_8192x8192", "7b_decode_m1_4096x4096_bias"])
+def test_gemm_packed_workloads(awq, name):
+    d = synth.workload_inputs(name)
+    M, K, N, G = d["M"], d["K"], d["N"], d["group_size"]
+    y = run(awq, d)
+    args = (d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    if M * K * N <= 32 * 4096 * 11008 and K * N <= 64 * 1024 * 1024:
+        assert_close(y, oracle.gemm(*args), name)
+    else:
+        rng = np.random.default_rng(5)
+        rows = np.concatenate([rng.integers(0, M, 2048), np.zeros(256, np.int64), np.full(256, M - 1)])
+        cols = np.concatenate([rng.integers(0, N, 2048), rng.integers(0, N, 512)])
+        assert_close(y[rows, cols], oracle.gemm_sampled(*args, rows, cols), name)
+    assert np.all(np.isfinite(y.astype(np.float32)))
+
+
+def test_gemm_packed_empty_and_errors(awq):
+    d = synth.awq_linear(23900, 0, 256, 128, group_size=128)
+    pk = packed_of(awq, d)
+    y = awq.awq_gemm_packed(dev(d["x"]), pk, None, 256, 128, 128)
+    assert tuple(y.shape) == (0, 128)
+    with pytest.raises(awq.AwqError):  # K % 64
+        awq.awq_repack_size(96, 64, 32)
+    with pytest.raises(awq.AwqError):  # group size % 64
+        awq.awq_repack_size(256, 64, 32)

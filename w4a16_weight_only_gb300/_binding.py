@@ -43,6 +43,9 @@ SIGNATURES = {
     "awq_dequant_w8": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp]),
     "awq_gemm_any": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _i32, _i32,
                             ctypes.c_uint32, _vp]),
+    "awq_repack_size": (_i32, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
+    "awq_repack": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
+    "awq_gemm_packed": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
 }
 GEMM_STATIC_WEIGHTS = 1
 
@@ -394,3 +397,56 @@ def device_status(stream=None):
 def selftest_wait_timeout(limit_ns=2_000_000, stream=None):
     """Launch the bounded-wait self test (awq.h); the next device_status() raises AwqError."""
     _check(load_library().awq_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def awq_repack_size(K, N, group_size=128) -> int:
+    """Bytes of the tile-packed layout of a [K, N] linear (host only)."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().awq_repack_size(K, N, group_size, ctypes.byref(n)))
+    return int(n.value)
+
+
+def awq_repack(qweight, qzeros, scales, group_size=128, out=None, stream=None):
+    """One-off conversion of checkpoint-layout weights into the tile-packed layout via the
+    library's awq_repack.  Returns (or fills) an int32 device tensor of
+    awq_repack_size(K, N, group_size) / 4 words."""
+    lib = load_library()
+    K, C = qweight.shape
+    N = 8 * C
+    dev = _cuda_index(qweight, "qweight")
+    _need(qweight, "qweight", torch.int32, (K, C), dev)
+    ng = _groups(K, group_size)
+    _need(qzeros, "qzeros", torch.int32, (ng, C), dev)
+    _need(scales, "scales", torch.float16, (ng, N), dev)
+    words = awq_repack_size(K, N, group_size) // 4
+    if out is None:
+        out = torch.empty((words,), dtype=torch.int32, device=dev)
+    else:
+        _need(out, "out", torch.int32, (words,), dev)
+    _check(lib.awq_repack(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size, _ptr(out),
+                          _stream(stream)))
+    return out
+
+
+def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None):
+    """y = x @ W (+ bias) with W in the tile-packed layout (awq_repack's output) via the
+    library's awq_gemm_packed; x fp16 [..., K] (leading dims flattened), bias fp16 [N] or
+    None.  Returns fp16 [..., N]."""
+    lib = load_library()
+    lead = x.shape[:-1]
+    if x.shape[-1] != K:
+        raise ValueError(f"x must be [..., {K}], got {tuple(x.shape)}")
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    dev = _cuda_index(x, "x")
+    _need(x2, "x", torch.float16, (M, K), dev)
+    _need(packed, "packed", torch.int32, (awq_repack_size(K, N, group_size) // 4,), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.float16, (N,), dev)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    else:
+        _need(out, "out", torch.float16, (M, N), dev)
+    _check(lib.awq_gemm_packed(_ptr(x2), _ptr(packed), _ptr(bias), M, K, N, group_size, _ptr(out),
+                               _stream(stream)))
+    return out.reshape(*lead, N)

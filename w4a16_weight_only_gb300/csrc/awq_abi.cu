@@ -427,6 +427,76 @@ awq_path_t awq_gemm_select_path_ex(int64_t M, int64_t K, int64_t N, int64_t grou
   return static_cast<awq_path_t>(choose_path(p));
 }
 
+awq_status_t awq_repack_size(int64_t K, int64_t N, int64_t group_size, size_t* bytes) {
+  int G = 0;
+  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  if (st != AWQ_OK) return st;
+  if (!bytes) return fail(AWQ_ERR_INVALID_ARGUMENT, "null bytes pointer");
+  const char* why = "";
+  if (!awq::packed_supported(K, N, G, &why)) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "%s", why);
+  *bytes = awq::packed_bytes(K, N);
+  return ok();
+}
+
+awq_status_t awq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
+                        int64_t K, int64_t N, int64_t group_size, void* packed_out,
+                        awq_stream_t stream) {
+  int G = 0;
+  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  if (st != AWQ_OK) return st;
+  const char* why = "";
+  if (!awq::packed_supported(K, N, G, &why)) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "%s", why);
+  if (N == 0) return ok();
+  if (!qweight || !qzeros || !scales_f16 || !packed_out)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "null pointer among qweight, qzeros, scales, packed_out");
+  if (!al(qweight, 4) || !al(qzeros, 4)) return fail(AWQ_ERR_MISALIGNED, "qweight/qzeros must be 4-byte aligned");
+  if (!al(scales_f16, 2)) return fail(AWQ_ERR_MISALIGNED, "scales must be 2-byte aligned");
+  if (!al(packed_out, 16)) return fail(AWQ_ERR_MISALIGNED, "packed_out must be 16-byte aligned");
+  if (K / 64 > 65535) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "K / 64 must be at most 65535");
+  st = check_device();
+  if (st != AWQ_OK) return st;
+  const cudaError_t e = awq::launch_repack(
+      reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
+      static_cast<const __half*>(scales_f16), static_cast<int>(K), static_cast<int>(N), G, packed_out,
+      reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "awq_repack launch");
+  return ok();
+}
+
+awq_status_t awq_gemm_packed(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
+                             int64_t K, int64_t N, int64_t group_size, void* y_f16,
+                             awq_stream_t stream) {
+  if (M < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "M must be >= 0 (got %lld)", (long long)M);
+  int G = 0;
+  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  if (st != AWQ_OK) return st;
+  const char* why = "";
+  if (!awq::packed_supported(K, N, G, &why)) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "%s", why);
+  if (M > kDimLimit) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "M must be below 2^31");
+  if (M * N >= kProdLimit || M * K >= kProdLimit)
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "M*N and M*K must be below 2^40");
+  if (M == 0 || N == 0) return ok();
+  if (!x_f16 || !packed || !y_f16) return fail(AWQ_ERR_INVALID_ARGUMENT, "null pointer among x, packed, y");
+  if (!al(x_f16, 16)) return fail(AWQ_ERR_MISALIGNED, "x must be 16-byte aligned");
+  if (!al(packed, 16)) return fail(AWQ_ERR_MISALIGNED, "packed must be 16-byte aligned");
+  if (!al(y_f16, 2) || (bias_f16 && !al(bias_f16, 2)))
+    return fail(AWQ_ERR_MISALIGNED, "y and bias must be 2-byte aligned");
+  st = check_device();
+  if (st != AWQ_OK) return st;
+  awq::GemmProblem p{};
+  p.x = static_cast<const __half*>(x_f16);
+  p.bias = static_cast<const __half*>(bias_f16);
+  p.y = static_cast<__half*>(y_f16);
+  p.M = static_cast<int>(M);
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.G = G;
+  p.stream = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = awq::launch_packed(p, packed);
+  if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_packed launch");
+  return ok();
+}
+
 awq_status_t awq_device_status(awq_stream_t stream) {
   awq_status_t st = check_device();
   if (st != AWQ_OK) return st;

@@ -87,6 +87,14 @@ bool prefill_supported(const GemmProblem& p, const char** why);
 double prefill_estimate_us(const GemmProblem& p, int sms);
 cudaError_t launch_prefill(const GemmProblem& p);
 
+// Tile-packed layout (awq_repack / awq_gemm_packed): shape rule, size in bytes, the
+// one-off conversion, and the linear that reads it (x, bias, y, M, K, N, G, stream of p).
+bool packed_supported(int64_t K, int64_t N, int64_t G, const char** why);
+size_t packed_bytes(int64_t K, int64_t N);
+cudaError_t launch_repack(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
+                          int G, void* out, cudaStream_t stream);
+cudaError_t launch_packed(const GemmProblem& p, const void* packed);
+
 // Failure-detection self test: a bounded wait that nothing completes (see awq.h).
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 

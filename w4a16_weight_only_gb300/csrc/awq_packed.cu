@@ -1,0 +1,507 @@
+// Tile-packed layout: the one-off repack (awq_repack) and the tensor-core linear that reads
+// it (awq_gemm_packed).
+//
+// Layout (this library's kernel-native order; repacking the AWQ order away for a kernel is
+// the prior art of the vLLM article, section 5.1, and of the GPTQModel wiki, "Marlin and
+// Machete").  For output-column tile t (128 columns) and K stage s (64 rows) one block of
+// 1152 words sits at word (t * K/64 + s) * 1152:
+//   words 512 h + 4 c + j (h < 2, c < 128, j < 4): the 4-bit codes of column 128 t + c for
+//     rows 64 s + 32 h + 8 j + 0..7, row offset ORDER[p] in nibble p (ORDER = {0,2,4,6,1,3,
+//     5,7}: the checkpoint's column interleave applied along K, so (word >> 4 i) & 0x000F000F
+//     holds rows (2 i, 2 i + 1) of the run in its two halves);
+//   words 1024 + c: scale bits (fp16) | zero << 16 of column 128 t + c, for the group of
+//     row 64 s (every stage of a group carries a copy);
+//   columns past N: all zero.
+// A CTA's K loop over one column tile reads consecutive blocks: one bulk copy per stage.
+//
+// The linear (y = x W + bias, w = (code - zero) * scale; tensref.org/formats/awq,
+// "Reader"; GPTQModel wiki "AWQ", "Native GEMM": fused dequant-GEMM, fp32 accumulation):
+// persistent tcgen05 kernel, one CTA per SM, tiles of 128 output columns (the MMA's M side)
+// by BT activation rows (its N side).  The dequantized weights never touch shared memory:
+// each dequant thread owns one output column (one TMEM lane), turns the 32 codes of its
+// half-stage into 16 fp16 pairs ((c - z) * s exactly: 0x6400 exponent trick, HSUB2,
+// HMUL2) and stores them with tcgen05.st into a TMEM ring that the MMA reads as its A
+// operand.  Shared memory carries only the activation tiles (TMA, 128-byte swizzle) and the
+// packed blocks, which keeps its traffic per stage well below the checkpoint-layout kernel's
+// (no A tile written and read back).
+//
+// Warp roles (448 threads): warp 0 producer (one TMA copy of the activation tile and one
+// bulk copy of the packed block per stage), warp 1 TMEM allocation and the MMA-issuing
+// thread, warps 2-9 dequant (warp w: TMEM lanes 32 (w % 4) .., K half (w - 2) / 4), warps
+// 10-13 epilogue (tcgen05.ld, + bias, fp16 stores).  Every wait is bounded in wall time;
+// on give-up the kernel sets the device status word, every role leaves its loop, issued
+// copies and MMAs are drained (bounded) and TMEM is freed.
+#include <mutex>
+
+#include "awq_internal.cuh"
+#include "awq_ptx.cuh"
+
+namespace awq {
+namespace {
+
+using namespace ptx;
+
+constexpr int kTN = 128;                    // output columns per tile / block
+constexpr int kTK = 64;                     // K rows per stage / block
+constexpr int kBlockWords = 1024 + kTN;     // codes + meta
+constexpr int kBlockBytes = 4 * kBlockWords;  // 4608
+constexpr int kDQ = 8;                      // dequant warps
+constexpr int kThreads = (2 + kDQ + 4) * 32;
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
+constexpr unsigned int kStatusPackedTimeout = 0x4u;
+constexpr uint32_t kMagic = 0x64006400u;    // fp16 1024 in both halves
+constexpr int kSmemCap = 227 * 1024;
+constexpr int kSmemMin = 120 * 1024;        // one CTA per SM: it allocates all 512 TMEM columns
+
+// ------------------------------------------------------------------- repack ----
+
+// One CTA per block (column tile t = blockIdx.y, stage s = blockIdx.x).  Thread (h, j, cw):
+// rows 64 s + 32 h + 8 j + 0..7 of checkpoint word 16 t + cw hold 8 columns x 8 rows of
+// codes; it writes the 8 columns' code words.  Thread c also writes meta word c.  The
+// block is assembled in shared memory and stored with 16-byte writes.
+__global__ void __launch_bounds__(128) repack_kernel(const uint32_t* __restrict__ qw,
+                                                     const uint32_t* __restrict__ qz,
+                                                     const uint16_t* __restrict__ sc,
+                                                     uint32_t* __restrict__ out, int K, int N, int G) {
+  __shared__ __align__(16) uint32_t blk[kBlockWords];
+  const int s = blockIdx.x, t = blockIdx.y, KS = K / kTK;
+  const int C = N / 8;
+  const int tid = threadIdx.x;
+  {
+    const int h = tid >> 6, j = (tid >> 4) & 3, cw = tid & 15;
+    const int word = 16 * t + cw;
+    const int r0 = kTK * s + 32 * h + 8 * j;
+    uint32_t in[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) in[r] = word < C ? __ldg(qw + static_cast<size_t>(r0 + r) * C + word) : 0u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {  // column 8 cw + q: nibble of position q in ORDER
+      int nib = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nib = nibble_column(i) == q ? i : nib;
+      uint32_t v = 0u;
+#pragma unroll
+      for (int p = 0; p < 8; ++p) v |= ((in[nibble_column(p)] >> (4 * nib)) & 0xFu) << (4 * p);
+      blk[512 * h + 4 * (8 * cw + q) + j] = v;
+    }
+  }
+  {
+    const int n = kTN * t + tid;
+    const int g = (kTK * s) / G;
+    uint32_t m = 0u;
+    if (n < N) {
+      int nib = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nib = nibble_column(i) == (n & 7) ? i : nib;
+      const uint32_t z = (__ldg(qz + static_cast<size_t>(g) * C + n / 8) >> (4 * nib)) & 0xFu;
+      m = static_cast<uint32_t>(__ldg(sc + static_cast<size_t>(g) * N + n)) | (z << 16);
+    }
+    blk[1024 + tid] = m;
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(t * KS + s) * kBlockWords);
+  const uint4* src = reinterpret_cast<const uint4*>(blk);
+  for (int i = tid; i < kBlockWords / 4; i += 128) dst[i] = src[i];
+}
+
+// ------------------------------------------------------------ packed linear ----
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// D (TMEM) += A (TMEM, 128 lanes x 16 fp16) * B (shared memory descriptor).
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// tcgen05.ld of 32 columns without the wait (tmem_wait_ld completes every load issued
+// before it).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Waits for every tcgen05.ld issued before it; the 32 registers pass through the asm so
+// that no use of them can be scheduled above the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]),
+                 "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]),
+                 "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]),
+                 "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]),
+                 "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
+}
+
+// Shared-memory descriptor of a K-major operand with 128-byte swizzle: rows of 128 B (64
+// fp16 along K), 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;            // leading byte offset (unused), 16 B
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;    // stride byte offset: 8-row groups
+  d |= static_cast<uint64_t>(1u) << 46;            // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;            // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, fp16 A and B, both K-major (A comes
+// from TMEM), N = BT, M = 128.
+template <int BT>
+constexpr uint32_t idesc_ts() {
+  return (1u << 4) | (static_cast<uint32_t>(BT >> 3) << 17) | (static_cast<uint32_t>(kTN >> 4) << 24);
+}
+
+// Per-BT resources: TMEM holds NACC accumulators of BT columns and one A slot of 32 columns
+// (64 K rows of fp16 pairs) per pipeline slot; shared memory holds, per slot, the activation
+// tile and the packed block.  One ring: slot s carries stage j's activations, packed block
+// and dequantized A operand, for j = s mod ST.
+template <int BT>
+struct Cfg {
+  static constexpr int NACC = BT >= 256 ? 1 : 2;
+  static constexpr int SA_FIT = (512 - NACC * BT) / 32;
+  static constexpr int X_BYTES = BT * kTK * 2;
+  static constexpr int STAGE = X_BYTES + kBlockBytes;
+  static constexpr int ST_FIT = (kSmemCap - 2048) / STAGE;
+  static constexpr int ST0 = ST_FIT < SA_FIT ? ST_FIT : SA_FIT;
+  static constexpr int ST = ST0 < 8 ? ST0 : 8;
+  static constexpr int X_OFF = 0;
+  static constexpr int B_OFF = ST * X_BYTES;
+  static constexpr int BAR_OFF = B_OFF + ST * kBlockBytes;
+  // full_t[ST], empty[ST], full_a[ST], acc_full[2], acc_empty[2], drain
+  static constexpr int NBARS = 3 * ST + 5;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int USED = 1024 + MISC_OFF + 16;
+  static constexpr int SMEM = USED < kSmemMin ? kSmemMin : USED;
+  static constexpr uint32_t A_COL0 = NACC * BT;
+  static_assert(ST >= 3 && SMEM <= kSmemCap, "resources");
+  static_assert(NACC * BT + ST * 32 <= 512, "TMEM columns");
+};
+
+struct __align__(128) PackedParams {
+  CUtensorMap tm_x;          // x [M][K] f16, box {64, BT}, 128B swizzle
+  const uint32_t* packed;    // tile-packed weights
+  const __half* bias;
+  __half* y;
+  unsigned int* status;
+  int M, K, N;
+  int tiles_t, tiles;        // activation-row tiles, total tiles
+};
+
+template <int BT>
+__global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_constant__ PackedParams p) {
+  using CF = Cfg<BT>;
+  constexpr int ST = CF::ST, NACC = CF::NACC;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::BAR_OFF);
+  uint64_t* full_t = bars;            // activation tile + packed block of the slot landed
+  uint64_t* empty = bars + ST;        // slot free: block read by the dequant warps, MMAs done
+  uint64_t* full_a = bars + 2 * ST;   // dequantized A operand of the slot in TMEM
+  uint64_t* acc_full = bars + 3 * ST;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KS = p.K / kTK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full_t[s], 1);
+      mbar_init(&empty[s], kDQ + 1);  // dequant warps (block read) + the MMA commit
+      mbar_init(&full_a[s], kDQ);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot)))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Bounded wait; on give-up every role learns it through the abort flag (read only then,
+  // and before each blocking wait of the roles that poll it).
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(bar, parity, p.status, kStatusPackedTimeout, kWaitLimitNs)) return true;
+    *abort_flag = 1u;
+    return false;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_x);
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+        const int m0 = (tile % p.tiles_t) * BT;
+        const int t = tile / p.tiles_t;
+        const uint32_t* src = p.packed + static_cast<size_t>(t) * KS * kBlockWords;
+        for (int kb = 0; kb < KS; ++kb) {
+          if (!wait(&empty[s], ph ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + kBlockBytes));
+          tma_load_2d(smem + CF::X_OFF + s * CF::X_BYTES, &p.tm_x, &full_t[s], kb * kTK, m0);
+          bulk_load(smem + CF::B_OFF + s * kBlockBytes, src + static_cast<size_t>(kb) * kBlockWords,
+                    kBlockBytes, &full_t[s]);
+          ++issued;
+          if (++s == ST) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {  // every issued stage's copies land before the CTA may exit
+        for (int i = 0; i < ST && i < issued; ++i) {
+          if (--s < 0) { s = ST - 1; ph ^= 1u; }
+          mbar_wait_bounded(&full_t[s], ph, p.status, kStatusPackedTimeout, kWaitLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    // Stages go in pairs: one wait on the later stage's full_a covers both (every dequant
+    // warp arrives on its slots in stage order, and each arrival releases the warp's TMEM
+    // stores of all earlier stages); the activation tiles are in place once full_a is (the
+    // dequant warps waited for them).  One commit per stage frees its slot.
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_ts<BT>();
+      int s = 0, li = 0;
+      uint32_t ph = 0;
+      bool ok = true, any = false;
+      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x, ++li) {
+        const int b = li % NACC;
+        if (!wait(&acc_empty[b], static_cast<uint32_t>(((li / NACC) & 1) ^ 1))) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(b * BT);
+        for (int kb = 0; kb < KS; kb += 2) {
+          const int n2 = KS - kb < 2 ? KS - kb : 2;
+          const int sl = s + n2 - 1 < ST ? s + n2 - 1 : s + n2 - 1 - ST;
+          const uint32_t phl = s + n2 - 1 < ST ? ph : ph ^ 1u;
+          if (!wait(&full_a[sl], phl)) { ok = false; break; }
+          tc_fence_after();
+          for (int i = 0; i < n2; ++i) {
+            const uint32_t a = tmem_base + CF::A_COL0 + static_cast<uint32_t>(s * 32);
+            const uint64_t bdesc = sw128_kmajor_desc(sbase + CF::X_OFF + s * CF::X_BYTES);
+#pragma unroll
+            for (int ks = 0; ks < kTK / 16; ++ks)  // K += 16: A 8 TMEM columns, B 32 bytes
+              mma_ts(d, a + 8u * ks, bdesc + 2u * ks, idesc, (kb + i > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&empty[s]);
+            if (++s == ST) { s = 0; ph ^= 1u; }
+          }
+          any = true;
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[b]);
+      }
+      if (any) {  // every MMA completes before TMEM is released
+        mma_commit(drain);
+        mbar_wait_bounded(drain, 0u, p.status, kStatusPackedTimeout, kWaitLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 2 + kDQ) {
+    // ------------------------------------------------------------------ dequant
+    // Thread = output column c of the tile (TMEM lane), K half h of every stage: the four
+    // code words of its half-run (one 16-byte load, lanes contiguous) and its meta word;
+    // pair i of the result holds rows 32 h + 2 i, +1 (nibbles i % 4 and i % 4 + 4 of word
+    // i / 4), stored to TMEM columns 16 h + i of the slot's A operand.  The slot's A operand
+    // is free once its activations have landed: the producer refilled the slot only after
+    // the previous round's MMAs completed.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int c = 32 * q + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+      for (int kb = 0; kb < KS; ++kb) {
+        if (!wait(&full_t[s], ph)) { ok = false; break; }
+        tc_fence_after();  // the TMEM stores below come after the previous round's MMAs
+        const unsigned char* blk = smem + CF::B_OFF + s * kBlockBytes;
+        const uint4 w4 = *reinterpret_cast<const uint4*>(blk + 16 * (128 * h + c));
+        const uint32_t meta = *reinterpret_cast<const uint32_t*>(blk + 4 * (1024 + c));
+        const uint32_t zz = kMagic | ((meta >> 16) * 0x00010001u);  // (1024 + z) in both halves
+        const uint32_t ss = prmt(meta, 0u, 0x1010u);                  // scale in both halves
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        uint32_t v[16];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii)
+            v[4 * jj + ii] = hmul2(hsub2(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMagic), zz), ss);
+        tmem_st16(tmem_base + lane_addr + CF::A_COL0 + static_cast<uint32_t>(s * 32 + 16 * h), v);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&full_a[s]);
+          mbar_arrive(&empty[s]);
+        }
+        if (++s == ST) { s = 0; ph ^= 1u; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    // The next 32-column chunk is loaded from TMEM while the current one is stored.
+    const int q = warp & 3;              // TMEM lanes 32 q .. 32 q + 31
+    const int nl = 32 * q + lane;        // output column inside the tile
+    int li = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++li) {
+      const int b = li % NACC;
+      const int m0 = (tile % p.tiles_t) * BT;
+      const int n = (tile / p.tiles_t) * kTN + nl;
+      const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+      if (!wait(&acc_full[b], static_cast<uint32_t>((li / NACC) & 1))) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT);
+      uint32_t va[32], vb[32];
+      tmem_ld32_nowait(taddr, va);
+      tmem_wait_ld(va);
+#pragma unroll
+      for (int cc = 0; cc < BT / 32; ++cc) {
+        uint32_t (&cur)[32] = (cc & 1) ? vb : va;
+        uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
+        if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
+        const int t0 = m0 + 32 * cc;
+        if (n < p.N) {
+          __half* yp = p.y + static_cast<size_t>(t0) * p.N + n;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __float2half_rn(__uint_as_float(cur[j]) + bias);
+        }
+        if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
+  }
+}
+
+template <int BT>
+cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
+  using CF = Cfg<BT>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(packed_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  PackedParams pp = base;
+  const char* why = nullptr;
+  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, BT,
+                    CU_TENSOR_MAP_SWIZZLE_128B, &why))
+    return cudaErrorInvalidValue;
+  pp.tiles_t = (p.M + BT - 1) / BT;
+  const long long tiles = static_cast<long long>(pp.tiles_t) * ((p.N + kTN - 1) / kTN);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  pp.tiles = static_cast<int>(tiles);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = pp.tiles < sms ? pp.tiles : sms;
+  packed_kernel<BT><<<grid, kThreads, CF::SMEM, p.stream>>>(pp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool packed_supported(int64_t K, int64_t N, int64_t G, const char** why) {
+  static const char* dummy;
+  if (!why) why = &dummy;
+  if (K % kTK != 0) { *why = "the tile-packed layout needs K % 64 == 0"; return false; }
+  if (G % kTK != 0) { *why = "the tile-packed layout needs group_size % 64 == 0 (or -1)"; return false; }
+  if (N % 8 != 0) { *why = "N must be a multiple of 8"; return false; }
+  return true;
+}
+
+size_t packed_bytes(int64_t K, int64_t N) {
+  return static_cast<size_t>((N + kTN - 1) / kTN) * static_cast<size_t>(K / kTK) * kBlockBytes;
+}
+
+cudaError_t launch_repack(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
+                          int G, void* out, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(K / kTK), static_cast<unsigned>((N + kTN - 1) / kTN));
+  repack_kernel<<<grid, 128, 0, stream>>>(qw, qz, reinterpret_cast<const uint16_t*>(sc),
+                                          static_cast<uint32_t*>(out), K, N, G);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_packed(const GemmProblem& p, const void* packed) {
+  PackedParams pp{};
+  pp.packed = static_cast<const uint32_t*>(packed);
+  pp.bias = p.bias;
+  pp.y = p.y;
+  cudaError_t e = status_word_ptr(&pp.status);
+  if (e != cudaSuccess) return e;
+  pp.M = p.M; pp.K = p.K; pp.N = p.N;
+  if (p.M <= 64) return launch_bt<64>(pp, p);
+  if (p.M <= 128) return launch_bt<128>(pp, p);
+  return launch_bt<256>(pp, p);
+}
+
+}  // namespace awq
