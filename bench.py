@@ -11,8 +11,10 @@ steps until the repetitions cover at least 0.5 s; the reported step time is the 
 repetition.  nvidia-smi clocks are sampled during every timed region.
 
 Extra blocks on the same line: `prefill` -- TFLOP/s of the 70B linears at M = 4096 (the
-three linears per step, eager launches, inputs larger than L2), beside awq_dequant +
-cuBLAS on the same step; `decode_7b` -- the 7B decode step (M = 1: 4096x4096, 4096x11008,
+three linears per step, eager launches, inputs larger than L2) through prepared layers with
+the tile-packed weights (awq_gemm_packed; the one-off awq_repack timed separately), beside
+awq_gemm on the checkpoint layout and awq_dequant + cuBLAS on the same step; `prefill_7b` --
+the same for the 7B linears at M = 2048; `decode_7b` -- the 7B decode step (M = 1: 4096x4096, 4096x11008,
 11008x4096, bias); `e2e` -- the headline step end to end through the public call with
 pinned host buffers (one host-to-device copy of the step's activations, three calls, one
 device-to-host copy of the outputs, a synchronize per step).
@@ -55,6 +57,8 @@ WORKLOAD_7B = ("7B decode M=1: linears 4096x4096, 4096x11008, 11008x4096; group_
 PREFILL = ["70b_m4096_8192x8192", "70b_m4096_8192x28672", "70b_m4096_28672x8192"]
 WORKLOAD_PREFILL = ("70B prefill M=4096: linears 8192x8192, 8192x28672, 28672x8192; "
                     "group_size 128; fp16 bias")
+PREFILL_7B = ["7b_prefill_m2048_4096x11008", "7b_prefill_m2048_11008x4096"]
+WORKLOAD_PREFILL_7B = "7B prefill M=2048: linears 4096x11008, 11008x4096; group_size 128; no bias"
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_TFLOPS = 1900.0
@@ -421,40 +425,61 @@ def _decode_region(names, args, world, torch, awq, stream, clocks):
             "nbytes": step_bytes(lins0), "launches": len(names) * args.steps * len(times)}
 
 
-def _prefill_region(args, world, torch, awq, stream, clocks):
-    """The 70B prefill step (three linears at M = 4096), eager launches through prepared
-    layers, inputs larger than L2; beside it awq_dequant + cuBLAS on the same step."""
-    lins = workload_linears(0, PREFILL)
+def _prefill_region(names, args, world, torch, awq, stream):
+    """A prefill step (the linears `names`, one call each), eager launches, inputs larger
+    than L2, timed three ways: prepared layers with the tile-packed copy (awq_gemm_packed;
+    the one-off repack timed separately), prepared layers on the checkpoint layout
+    (awq_gemm), and the pages' large-batch strategy (awq_dequant to a dense fp16 weight,
+    then a library GEMM) as a comparator."""
+    lins = workload_linears(0, names)
     dev = []
     for d in lins:
         t = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "qweight", "qzeros", "scales")}
-        t["bias"] = torch.from_numpy(d["bias"]).cuda()
+        t["bias"] = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
         t["y"] = torch.empty((d["M"], d["N"]), dtype=torch.float16, device="cuda")
-        t["layer"] = awq.AwqLinear(t["qweight"], t["qzeros"], t["scales"], t["bias"], d["group_size"])
         t["G"] = d["group_size"]
+        t["plain"] = awq.AwqLinear(t["qweight"], t["qzeros"], t["scales"], t["bias"], t["G"])
         dev.append(t)
     del lins
     sp = stream.cuda_stream
-    path = awq.select_path(dev[0]["x"], dev[0]["qweight"], dev[0]["qzeros"], dev[0]["scales"],
-                           dev[0]["bias"], dev[0]["G"], dev[0]["y"])
+    # the one-off conversion, timed on its own (median of 5 passes over the step's linears)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for t in dev:
+            t["layer"] = awq.AwqLinear(t["qweight"], t["qzeros"], t["scales"], t["bias"], t["G"],
+                                       packed=True)
+        rp = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for t in dev:
+                awq.awq_repack(t["qweight"], t["qzeros"], t["scales"], t["G"], out=t["layer"].packed,
+                               stream=stream)
+            b.record(stream)
+            b.synchronize()
+            rp.append(a.elapsed_time(b) / 1e3)
+    t_repack = statistics.median(rp)
 
-    def run_steps(k):
+    def timed_step(run_k):
+        with torch.cuda.stream(stream):
+            run_k(max(args.warmup, 3))
+            torch.cuda.synchronize()
+            barrier(world)
+            times, win = timed_repetitions(run_k, args.steps, stream)
+            torch.cuda.synchronize()
+            barrier(world)
+        return statistics.median(times) / args.steps, len(times), sum(times), win
+
+    def run_packed(k):
         for _ in range(k):
             for t in dev:
                 t["layer"](t["x"], out=t["y"], stream=sp)
 
-    with torch.cuda.stream(stream):
-        run_steps(max(args.warmup, 3))
-        torch.cuda.synchronize()
-        barrier(world)
-        times, (w0, w1) = timed_repetitions(run_steps, args.steps, stream)
-        torch.cuda.synchronize()
-        barrier(world)
-    awq.device_status()
-    t_step = statistics.median(times) / args.steps
+    def run_plain(k):
+        for _ in range(k):
+            for t in dev:
+                t["plain"](t["x"], out=t["y"], stream=sp)
 
-    # comparator: the pages' large-batch strategy (dequantize to a dense fp16 weight, then a
-    # library GEMM), timed the same way on the same step
     for t in dev:
         t["wd"] = torch.empty((t["qweight"].shape[0], t["y"].shape[1]), dtype=torch.float16,
                               device="cuda")
@@ -464,19 +489,52 @@ def _prefill_region(args, world, torch, awq, stream, clocks):
             for t in dev:
                 awq.awq_dequant(t["qweight"], t["qzeros"], t["scales"], t["G"], out=t["wd"],
                                 stream=stream)
-                torch.addmm(t["bias"], t["x"], t["wd"], out=t["y"])
+                if t["bias"] is not None:
+                    torch.addmm(t["bias"], t["x"], t["wd"], out=t["y"])
+                else:
+                    torch.matmul(t["x"], t["wd"], out=t["y"])
 
-    with torch.cuda.stream(stream):
-        run_ref(max(args.warmup, 3))
-        torch.cuda.synchronize()
-        ref_times, (r0, r1) = timed_repetitions(run_ref, args.steps, stream)
-        torch.cuda.synchronize()
-    t_ref = statistics.median(ref_times) / args.steps
+    out = {"packed": timed_step(run_packed), "checkpoint": timed_step(run_plain),
+           "ref": timed_step(run_ref), "t_repack": t_repack}
+    awq.device_status()
     del dev
     torch.cuda.empty_cache()
-    return {"t_step": t_step, "reps": len(times), "timed_s": sum(times), "win": (w0, w1),
-            "t_ref": t_ref, "ref_win": (r0, r1), "path": path,
-            "launches": len(PREFILL) * args.steps * len(times)}
+    return out
+
+
+def _prefill_block(names, workload, args, world, torch, awq, stream, windows, key):
+    pf = _prefill_region(names, args, world, torch, awq, stream)
+    flop = step_flop(names)
+    t_p, reps, timed_s, win = pf["packed"]
+    tp = reduce_max(t_p, world)
+    peak_s, src_s = tensor_peak(sustained=True)
+    peak_b, _ = tensor_peak(sustained=False)
+    ach = flop / t_p / 1e12
+    t_c, reps_c, timed_c, win_c = pf["checkpoint"]
+    t_r, reps_r, timed_r, win_r = pf["ref"]
+    windows[key] = win
+    windows[key + ".checkpoint_layout"] = win_c
+    windows[key + ".dequant_plus_cublas"] = win_r
+    return {
+        "workload": workload, "metric": "TFLOP/s", "value": world * flop / tp / 1e12,
+        "unit": "TFLOP/s", "ms_per_step": tp * 1e3, "flop_per_step": flop,
+        "path": "awq_gemm_packed (tile-packed weights, AwqLinear(packed=True))",
+        "roofline": {"bound": "tensor", "achieved": ach, "peak": peak_s, "unit": "TFLOP/s",
+                     "frac": ach / peak_s, "peak_source": src_s + ": the step loop runs for "
+                     "seconds under the power cap", "frac_of_burst_peak": ach / peak_b,
+                     "kernel": "packed_kernel (tcgen05, A operand in TMEM)", "traffic": None},
+        "timing": f"{reps} repetitions of {args.steps} steps ({timed_s:.3f} s); eager launches; "
+                  "inputs larger than L2",
+        "repack_ms_one_off": pf["t_repack"] * 1e3,
+        "checkpoint_layout": {"ms_per_step": t_c * 1e3, "TFLOP_s": flop / t_c / 1e12,
+                              "note": "awq_gemm on the checkpoint layout (prefill_kernel, "
+                                      "dequantized tile in shared memory)",
+                              "timing": f"{reps_c} repetitions ({timed_c:.3f} s)"},
+        "dequant_plus_cublas": {"ms_per_step": t_r * 1e3, "TFLOP_s": flop / t_r / 1e12,
+                                "timing": f"{reps_r} repetitions ({timed_r:.3f} s)",
+                                "note": "awq_dequant to a dense fp16 weight, then torch.addmm "
+                                        "(cuBLAS), per linear: comparator, not the product"},
+        "gpu_launches": len(names) * args.steps * reps}
 
 
 def _e2e(reg, args, world, torch, stream):
@@ -616,28 +674,10 @@ def run_ours(args, rank, world, local):
                       f"{r7['R']} rotating weight sets; CUDA graph replays",
             "gpu_launches": r7["launches"]}
         windows["decode_7b"] = r7["win"]
-        pf = _prefill_region(args, world, torch, awq, stream, clocks)
-        flop = step_flop(PREFILL)
-        tp = reduce_max(pf["t_step"], world)
-        peak_s, src_s = tensor_peak(sustained=True)
-        peak_b, _ = tensor_peak(sustained=False)
-        ach = flop / pf["t_step"] / 1e12
-        line["prefill"] = {
-            "workload": WORKLOAD_PREFILL, "metric": "TFLOP/s", "value": world * flop / tp / 1e12,
-            "unit": "TFLOP/s", "ms_per_step": tp * 1e3, "flop_per_step": flop, "path": pf["path"],
-            "roofline": {"bound": "tensor", "achieved": ach, "peak": peak_s, "unit": "TFLOP/s",
-                         "frac": ach / peak_s, "peak_source": src_s + ": the step loop runs for "
-                         "seconds under the power cap", "frac_of_burst_peak": ach / peak_b,
-                         "kernel": "prefill_kernel (tcgen05/TMEM)", "traffic": None},
-            "timing": f"{pf['reps']} repetitions of {args.steps} steps ({pf['timed_s']:.3f} s); "
-                      "eager launches; inputs larger than L2 (x 67-235 MB per linear)",
-            "dequant_plus_cublas": {"ms_per_step": pf["t_ref"] * 1e3,
-                                    "TFLOP_s": flop / pf["t_ref"] / 1e12,
-                                    "note": "awq_dequant to a dense fp16 weight, then torch.addmm "
-                                            "(cuBLAS), per linear: comparator, not the product"},
-            "gpu_launches": pf["launches"]}
-        windows["prefill"] = pf["win"]
-        windows["prefill.dequant_plus_cublas"] = pf["ref_win"]
+        line["prefill"] = _prefill_block(PREFILL, WORKLOAD_PREFILL, args, world, torch, awq, stream,
+                                         windows, "prefill")
+        line["prefill_7b"] = _prefill_block(PREFILL_7B, WORKLOAD_PREFILL_7B, args, world, torch, awq,
+                                            stream, windows, "prefill_7b")
     # clock samples of every timed region (the sampler ran throughout)
     for key, (w0, w1) in windows.items():
         clk = clocks.window(w0, w1)

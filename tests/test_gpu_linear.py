@@ -92,3 +92,39 @@ def test_linear_refuses_bad_activations(awq):
         awq.AwqLinear(qw, qz, sc.float(), None, group_size=128)
     with pytest.raises(ValueError):
         awq.AwqLinear(qw, qz[:1, :8], sc, None, group_size=64)
+
+
+@pytest.mark.parametrize("M", [1, 40, 255, 256, 700])
+def test_linear_packed_switches_layout_by_rows(awq, M):
+    # packed=True keeps a tile-packed copy: calls of >= packed_min_rows rows run
+    # awq_gemm_packed on it (bit for bit the functional call), smaller ones the checkpoint
+    # layout (bit for bit awq_gemm); both within the oracle's tolerance
+    K, N, G = 1024, 392, 128
+    d = synth.awq_linear(20400 + M, M, K, N, group_size=G, bias=True)
+    x, qw, qz, sc, b = (dev(d[k]) for k in ("x", "qweight", "qzeros", "scales", "bias"))
+    lin = awq.AwqLinear(qw, qz, sc, b, group_size=G, packed=True)
+    y = lin(x)
+    if M >= lin.packed_min_rows:
+        y_ref = awq.awq_gemm_packed(x, awq.awq_repack(qw, qz, sc, G), b, K, N, G)
+    else:
+        y_ref = awq.awq_gemm(x, qw, qz, sc, b, group_size=G)
+    torch.cuda.synchronize()
+    assert same(y, y_ref)
+    ref = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+    assert (err <= 1e-2 * np.maximum(1.0, np.abs(ref))).all()
+
+
+def test_linear_packed_refuses_other_formats(awq):
+    d = synth.awq_linear(20500, 2, 256, 128, group_size=128, dtype="bf16")
+    qw, qz = dev(d["qweight"]), dev(d["qzeros"])
+    with pytest.raises(ValueError):
+        awq.AwqLinear(qw, qz, dev(d["scales"], torch.bfloat16), None, group_size=128, packed=True)
+    d8 = synth.awq8_linear(20501, 2, 256, 128, group_size=128)
+    with pytest.raises(ValueError):
+        awq.AwqLinear(dev(d8["qweight"]), dev(d8["qzeros"]), dev(d8["scales"]), None, group_size=128,
+                      bits=8, packed=True)
+    d2 = synth.awq_linear(20502, 2, 96, 64, group_size=32)
+    with pytest.raises(awq.AwqError):  # K % 64: no tile-packed layout
+        awq.AwqLinear(dev(d2["qweight"]), dev(d2["qzeros"]), dev(d2["scales"]), None, group_size=32,
+                      packed=True)

@@ -166,10 +166,22 @@ def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, pa
     return out.reshape(*lead, N)
 
 
+# Rows from which a layer built with packed=True runs awq_gemm_packed (its tile-packed copy)
+# rather than awq_gemm on the checkpoint layout: the packed kernel's 256-row tiles start to
+# pay there (GB300: 53 against 71 us at 512 x 4096 x 11008).
+PACKED_MIN_ROWS = 256
+
+
 class AwqLinear:
     """An AWQ linear layer whose weights are validated once: ``layer(x)`` runs
     ``awq_gemm_any`` (fp16 or bf16 activations, 4- or 8-bit codes) with only x and out
     checked per call.
+
+    packed=True (fp16, 4-bit codes, K % 64 == 0, group size % 64 == 0) also keeps a
+    tile-packed copy of the weights, written once by awq_repack at construction (a device
+    allocation of awq_repack_size bytes, about the size of the packed weights), and runs
+    calls of at least ``packed_min_rows`` rows through awq_gemm_packed; smaller calls keep
+    the checkpoint layout.
 
     qweight int32 [K, N/8] (4 bits) or [K, N/4] (8 bits), qzeros int32 [K/G, N/8 or N/4],
     scales fp16 or bf16 [K/G, N] (it sets the activation dtype; 8 bits: fp16), bias [N] of
@@ -184,10 +196,10 @@ class AwqLinear:
     layers)."""
 
     __slots__ = ("K", "N", "group_size", "bits", "dtype", "device", "_w", "_path",
-                 "_tensors", "_dt", "_flags")
+                 "_tensors", "_dt", "_flags", "packed", "packed_min_rows")
 
     def __init__(self, qweight, qzeros, scales, bias=None, group_size=128, bits=4, path="auto",
-                 static_weights=True):
+                 static_weights=True, packed=False, packed_min_rows=PACKED_MIN_ROWS):
         lib = load_library()
         if bits not in (4, 8):
             raise ValueError("bits must be 4 or 8")
@@ -211,6 +223,12 @@ class AwqLinear:
         self._dt = DTYPE_BF16 if dt is torch.bfloat16 else DTYPE_F16
         self._flags = GEMM_STATIC_WEIGHTS if static_weights else 0
         self._w = (qweight.data_ptr(), qzeros.data_ptr(), scales.data_ptr(), _ptr(bias))
+        self.packed = None
+        self.packed_min_rows = int(packed_min_rows)
+        if packed:
+            if bits != 4 or dt is not torch.float16:
+                raise ValueError("the tile-packed layout takes fp16 scales and 4-bit codes")
+            self.packed = awq_repack(qweight, qzeros, scales, group_size)
         self._path = PATHS[path]
         self._tensors = (qweight, qzeros, scales, bias)
 
@@ -232,6 +250,14 @@ class AwqLinear:
             raise ValueError(f"out must be a contiguous {dt} [..., {N}] tensor of {M} rows "
                              f"on device {self.device}")
         w = self._w
+        if self.packed is not None and M >= self.packed_min_rows:
+            st = _lib.awq_gemm_packed(x.data_ptr(), self.packed.data_ptr(), w[3], M, K, N,
+                                      self.group_size, out.data_ptr(),
+                                      (stream if isinstance(stream, int) else stream.cuda_stream)
+                                      if stream is not None else torch.cuda.current_stream().cuda_stream)
+            if st != AWQ_OK:
+                raise AwqError(st, last_error())
+            return out
         st = _lib.awq_gemm_any(x.data_ptr(), w[0], w[1], w[2], w[3], M, K, N, self.group_size,
                                out.data_ptr(), self._dt, self.bits, self._path, self._flags,
                                (stream if isinstance(stream, int) else stream.cuda_stream)
