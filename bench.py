@@ -388,14 +388,17 @@ def _decode_region(names, args, world, torch, awq, stream, clocks):
         for t in sets[r]:
             t["layer"](t["x"], out=t["y"], stream=sp)
 
+    # one graph of exactly K steps (weight sets in rotation) when K is moderate, so that a timed
+    # repetition is one replay; for large K a graph of R steps replayed, plus single steps
+    kg = args.steps if args.steps <= 512 else R
     with torch.cuda.stream(stream):
         for r in range(R):  # eager warm-up (first calls set kernel attributes)
             step(r)
         stream.synchronize()
         cycle = torch.cuda.CUDAGraph()
         with torch.cuda.graph(cycle, stream=stream):
-            for r in range(R):
-                step(r)
+            for i in range(kg):
+                step(i % R)
         singles = []
         for r in range(R):
             g = torch.cuda.CUDAGraph()
@@ -404,11 +407,11 @@ def _decode_region(names, args, world, torch, awq, stream, clocks):
             singles.append(g)
 
     def run_steps(k):
-        full, rem = divmod(k, R)
+        full, rem = divmod(k, kg)
         for _ in range(full):
             cycle.replay()
         for r in range(rem):
-            singles[r].replay()
+            singles[r % R].replay()
 
     with torch.cuda.stream(stream):
         run_steps(max(args.warmup, 3))

@@ -248,6 +248,9 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
 
   // Stage j of this warp: packed weights always, the group's zero and scale rows only when
   // stage j opens a group (or is the warp's first stage), activations separately.
+  // Weights and their metadata are streamed once: evict them from L2 first; the activations
+  // (read by every column tile, and the next call's input may be this call's output) last.
+  const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
   const int spg = p.G / kRS;  // stages per quantization group
   const uint32_t x_tx = static_cast<uint32_t>(p.x_rows) * kRS * 2;
   // Issue-side stage/group counters (advanced by lane 0 only; no division per stage).
@@ -259,15 +262,15 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     const bool meta = (j == j0) || (iss_left == spg);
     mbar_arrive_expect_tx(bar, GE::W_BYTES + x_tx + (meta ? GE::META_TX : 0u));
     if constexpr (kGrp) tma_load_3d(w_ring + slot * GE::W_BYTES, &p.tm_w, bar, cw0, j * kRS, ex);
-    else tma_load_2d(w_ring + slot * GE::W_BYTES, &p.tm_w, bar, cw0, j * kRS);
+    else tma_load_2d_hint(w_ring + slot * GE::W_BYTES, &p.tm_w, bar, cw0, j * kRS, pol_w);
     if (meta) {
       unsigned char* md = m_ring + (kOne ? iss_grp - g_first : slot) * GE::META_SLOT;
       if constexpr (kGrp) {
         tma_load_3d(md, &p.tm_z, bar, cw0, iss_grp, ex);
         tma_load_3d(md + 128, &p.tm_s, bar, CPW * cw0, iss_grp, ex);
       } else {
-        tma_load_2d(md, &p.tm_z, bar, cw0, iss_grp);
-        tma_load_2d(md + 128, &p.tm_s, bar, CPW * cw0, iss_grp);
+        tma_load_2d_hint(md, &p.tm_z, bar, cw0, iss_grp, pol_w);
+        tma_load_2d_hint(md + 128, &p.tm_s, bar, CPW * cw0, iss_grp, pol_w);
       }
     }
     if (--iss_left == 0) {
@@ -276,7 +279,7 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
     }
   };
   auto issue_x = [&](int slot, int j) {
-    tma_load_2d(x_ring + slot * p.x_pitch, &p.tm_x, &my_bars[slot], j * kRS, m0);
+    tma_load_2d_hint(x_ring + slot * p.x_pitch, &p.tm_x, &my_bars[slot], j * kRS, m0, pol_x);
   };
 
   // Static weights (declared by the caller: complete before the preceding kernel launch)

@@ -106,11 +106,12 @@ __global__ void __launch_bounds__(128) repack_kernel(const uint32_t* __restrict_
 
 // ------------------------------------------------------------ packed linear ----
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
           smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
@@ -289,6 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&p.tm_x);
+      // packed blocks are read by the token tiles of one column tile, close together in time:
+      // evict them first; activation tiles are re-read by every column tile: evict them last
+      const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
       int s = 0, issued = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -299,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
         for (int kb = 0; kb < KS; ++kb) {
           if (!wait(&empty[s], ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + kBlockBytes));
-          tma_load_2d(smem + CF::X_OFF + s * CF::X_BYTES, &p.tm_x, &full_t[s], kb * kTK, m0);
+          tma_load_2d_hint(smem + CF::X_OFF + s * CF::X_BYTES, &p.tm_x, &full_t[s], kb * kTK, m0, pol_x);
           bulk_load(smem + CF::B_OFF + s * kBlockBytes, src + static_cast<size_t>(kb) * kBlockWords,
-                    kBlockBytes, &full_t[s]);
+                    kBlockBytes, &full_t[s], pol_w);
           ++issued;
           if (++s == ST) { s = 0; ph ^= 1u; }
         }
