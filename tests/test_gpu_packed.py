@@ -82,6 +82,36 @@ def test_gemm_packed_exact_case_bitwise(awq, M):
     assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
 
 
+@pytest.mark.parametrize("M,K,N", [(300, 8192, 512), (256, 8192, 256), (512, 8192, 384), (260, 4096, 512)])
+def test_gemm_packed_long_k_pairs(awq, M, K, N):
+    # K >= 8192 with an even number of 128-column tiles runs the two-CTA (cta_group::2) kernel,
+    # an odd number (N = 384) and K = 4096 the single-CTA one; exact-arithmetic inputs make
+    # both bitwise checkable, random ones check the tolerance
+    d = synth.awq_linear(23200 + M + N, M, K, N, group_size=128, bias=True, x_kind="smallint",
+                         scale_kind="pow2", bias_kind="dyadic")
+    y = run(awq, d)
+    want = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
+    d = synth.awq_linear(23300 + M + N, M, K, N, group_size=128, bias=True)
+    assert_close(run(awq, d), oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128),
+                 f"packed M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("M,K,N", [(300, 8192, 512), (256, 8192, 256), (512, 8192, 384), (260, 4096, 512)])
+def test_gemm_packed_long_k_pairs(awq, M, K, N):
+    # K >= 8192 with an even number of 128-column tiles runs the two-CTA (cta_group::2) kernel,
+    # an odd number (N = 384) and K = 4096 the single-CTA one; exact-arithmetic inputs make
+    # both bitwise checkable, random ones check the tolerance
+    d = synth.awq_linear(23200 + M + N, M, K, N, group_size=128, bias=True, x_kind="smallint",
+                         scale_kind="pow2", bias_kind="dyadic")
+    y = run(awq, d)
+    want = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
+    d = synth.awq_linear(23300 + M + N, M, K, N, group_size=128, bias=True)
+    assert_close(run(awq, d), oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128),
+                 f"packed M={M} K={K} N={N}")
+
+
 def test_gemm_packed_deterministic(awq):
     d = synth.awq_linear(23500, 700, 4096, 1024, group_size=128, bias=True)
     pk = packed_of(awq, d)

@@ -52,6 +52,7 @@ constexpr unsigned int kStatusPackedTimeout = 0x4u;
 constexpr uint32_t kMagic = 0x64006400u;    // fp16 1024 in both halves
 constexpr int kSmemCap = 227 * 1024;
 constexpr int kSmemMin = 120 * 1024;        // one CTA per SM: it allocates all 512 TMEM columns
+constexpr int kPairMinK = 8192;             // K from which M > 128 runs the two-CTA kernel
 
 // ------------------------------------------------------------------- repack ----
 
@@ -173,6 +174,54 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
                  "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
                :
                : "memory");
+}
+
+// Pair mode (tcgen05 cta_group::2): the MMA spans the two CTAs of a cluster.
+__device__ __forceinline__ void mma_ts_pair(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive, once the MMAs issued so far complete, on the barrier at `bar`'s offset in both CTAs.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(static_cast<unsigned short>(0x3))
+      : "memory");
+}
+// Arrive (release, cluster scope) on the barrier at `local`'s offset in CTA `rank`.
+__device__ __forceinline__ void mbar_arrive_at(uint64_t* local, uint32_t rank) {
+  uint32_t ra;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+// Asynchronous 4-byte store into CTA `rank`'s shared memory at `local`'s offset, counted (4
+// bytes) on that CTA's barrier at `bar`'s offset.  It does not block the issuing thread; the
+// barrier's completion releases the thread's earlier operations at cluster scope.
+__device__ __forceinline__ void st_async_signal(const void* local, uint64_t* bar, uint32_t rank) {
+  uint32_t ra, rb;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+               "r"(0u), "r"(rb)
+               : "memory");
+}
+// try_wait with cluster-scope acquire (the phase completes through arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0u;
 }
 
 // Shared-memory descriptor of a K-major operand with 128-byte swizzle: rows of 128 B (64
@@ -445,6 +494,319 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
   }
 }
 
+// ------------------------------------------------------------------ pair mode ----
+// Large M: a cluster of two CTAs shares one tile of 256 output columns (M = 256 of
+// tcgen05.mma.cta_group::2: each CTA dequantizes its own 128 columns, its own column tile of
+// the packed layout, into its own TMEM) by 256 activation rows (N = 256: each CTA loads its
+// own 128 rows, so each SM's shared memory carries half the activations per MMA of the
+// single-CTA kernel).  CTA 0 issues the MMAs and commits to the barriers of both CTAs; the
+// dequant and epilogue warps of CTA 1 arrive on CTA 0's barriers.  Each CTA's TMEM holds the
+// accumulator rows of its own columns.
+struct PairCfg {
+  static constexpr int BT = 256;
+  static constexpr int XH_BYTES = (BT / 2) * kTK * 2;  // this CTA's half of the activation tile
+  static constexpr int STAGE = XH_BYTES + kBlockBytes;
+  static constexpr int SA_FIT = (512 - BT) / 32;
+  static constexpr int ST_FIT = (kSmemCap - 2048) / STAGE;
+  static constexpr int ST0 = ST_FIT < SA_FIT ? ST_FIT : SA_FIT;
+  static constexpr int ST = ST0 < 8 ? ST0 : 8;
+  static constexpr int X_OFF = 0;
+  static constexpr int B_OFF = ST * XH_BYTES;
+  static constexpr int BAR_OFF = B_OFF + ST * kBlockBytes;
+  // full_t[ST], empty[ST], full_a[ST], acc_full, acc_empty, drain
+  static constexpr int NBARS = 3 * ST + 3;
+  static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int SIG_OFF = MISC_OFF + 16;         // CTA 0: targets of CTA 1's signals
+  static constexpr int USED = 1024 + SIG_OFF + 4 * kDQ;
+  static constexpr int SMEM = USED < kSmemMin ? kSmemMin : USED;
+  static constexpr uint32_t A_COL0 = BT;
+  static_assert(ST >= 3 && SMEM <= kSmemCap, "resources");
+  static_assert(BT + ST * 32 <= 512, "TMEM columns");
+};
+// kind::f16, fp32 accumulate, fp16 A (TMEM) and B (K-major), N = 256, M = 256.
+constexpr uint32_t kIdescPair = (1u << 4) | (static_cast<uint32_t>(256 >> 3) << 17) |
+                                (static_cast<uint32_t>(256 >> 4) << 24);
+
+__global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_constant__ PackedParams p) {
+  using CF = PairCfg;
+  constexpr int ST = CF::ST, BT = CF::BT;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CF::BAR_OFF);
+  uint64_t* full_t = bars;            // this CTA's activation half + packed block landed
+  uint64_t* empty = bars + ST;        // slot free: block read here, the pair's MMAs done
+  uint64_t* full_a = bars + 2 * ST;   // CTA 0 only: both CTAs' A operands of the slot in TMEM
+  uint64_t* acc_full = bars + 3 * ST;
+  uint64_t* acc_empty = acc_full + 1; // CTA 0 only: both CTAs' epilogues read the accumulator
+  uint64_t* drain = acc_empty + 1;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KS = p.K / kTK;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = static_cast<int>(blockIdx.x >> 1), npairs = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full_t[s], 1);
+      mbar_init(&empty[s], kDQ + 1);   // this CTA's dequant warps + CTA 0's commit
+      // CTA 0's dequant warps (one of them also expects the 4-byte signals of CTA 1's eight)
+      mbar_init(&full_a[s], kDQ);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 8);           // the epilogue warps of both CTAs
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {  // one warp of each CTA of the pair, collectively
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot)))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(bar, parity, p.status, kStatusPackedTimeout, kWaitLimitNs)) return true;
+    *abort_flag = 1u;
+    return false;
+  };
+  auto wait_cl = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if (*abort_flag) return false;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_cl(bar, parity)) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(p.status, kStatusPackedTimeout);
+        *abort_flag = 1u;
+        return false;
+      }
+    }
+    return true;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_x);
+      const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < p.tiles; tile += npairs) {
+        const int m0 = (tile % p.tiles_t) * BT + static_cast<int>(rank) * (BT / 2);
+        const int t = (tile / p.tiles_t) * 2 + static_cast<int>(rank);
+        const uint32_t* src = p.packed + static_cast<size_t>(t) * KS * kBlockWords;
+        for (int kb = 0; kb < KS; ++kb) {
+          if (!wait(&empty[s], ph ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::XH_BYTES + kBlockBytes));
+          tma_load_2d_hint(smem + CF::X_OFF + s * CF::XH_BYTES, &p.tm_x, &full_t[s], kb * kTK, m0, pol_x);
+          bulk_load(smem + CF::B_OFF + s * kBlockBytes, src + static_cast<size_t>(kb) * kBlockWords,
+                    kBlockBytes, &full_t[s], pol_w);
+          ++issued;
+          if (++s == ST) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        for (int i = 0; i < ST && i < issued; ++i) {
+          if (--s < 0) { s = ST - 1; ph ^= 1u; }
+          mbar_wait_bounded(&full_t[s], ph, p.status, kStatusPackedTimeout, kWaitLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (CTA 0)
+    if (lane == 0 && rank == 0) {
+      int s = 0, li = 0;
+      uint32_t ph = 0;
+      bool ok = true, any = false;
+      for (int tile = pair; ok && tile < p.tiles; tile += npairs, ++li) {
+        if (!wait_cl(acc_empty, static_cast<uint32_t>((li & 1) ^ 1))) { ok = false; break; }
+        tc_fence_after();
+        for (int kb = 0; kb < KS; kb += 2) {
+          // Both CTAs' A operands of a pair of stages (their dequant warps waited for their
+          // activation halves first): one wait on the later stage's full_a covers both (the
+          // warps of CTA 0 arrive in stage order, CTA 1 signals once per pair, after its
+          // stores of both stages).
+          const int n2 = KS - kb < 2 ? KS - kb : 2;
+          const int sl = s + n2 - 1 < ST ? s + n2 - 1 : s + n2 - 1 - ST;
+          const uint32_t phl = s + n2 - 1 < ST ? ph : ph ^ 1u;
+          if (!wait_cl(&full_a[sl], phl)) { ok = false; break; }
+          tc_fence_after();
+          for (int i = 0; i < n2; ++i) {
+            const uint32_t a = tmem_base + CF::A_COL0 + static_cast<uint32_t>(s * 32);
+            const uint64_t bdesc = sw128_kmajor_desc(sbase + CF::X_OFF + s * CF::XH_BYTES);
+#pragma unroll
+            for (int ks = 0; ks < kTK / 16; ++ks)
+              mma_ts_pair(tmem_base, a + 8u * ks, bdesc + 2u * ks, kIdescPair,
+                          (kb + i > 0 || ks > 0) ? 1u : 0u);
+            mma_commit_pair(&empty[s]);
+            if (++s == ST) { s = 0; ph ^= 1u; }
+          }
+          any = true;
+        }
+        if (!ok) break;
+        mma_commit_pair(acc_full);
+      }
+      if (any) {  // every MMA completes (in both CTAs) before TMEM is released
+        mma_commit_pair(drain);
+        mbar_wait_bounded(drain, 0u, p.status, kStatusPackedTimeout, kWaitLimitNs);
+      }
+    } else if (lane == 0 && pair < p.tiles) {
+      // CTA 1: CTA 0's MMAs read this CTA's shared memory and TMEM until the last commit
+      mbar_wait_bounded(drain, 0u, p.status, kStatusPackedTimeout, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else if (warp < 2 + kDQ) {
+    // ------------------------------------------------------------------ dequant
+    // As in the single-CTA kernel (thread = output column of this CTA's tile, K half h).
+    // Readiness goes to CTA 0's full_a: an arrival from CTA 0's warps, a counted asynchronous
+    // store from CTA 1's (a remote arrive would stall the warp for over a thousand cycles).
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int c = 32 * q + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int tile = pair; ok && tile < p.tiles; tile += npairs) {
+      for (int kb = 0; kb < KS; ++kb) {
+        if (!wait(&full_t[s], ph)) { ok = false; break; }
+        tc_fence_after();
+        const unsigned char* blk = smem + CF::B_OFF + s * kBlockBytes;
+        const uint4 w4 = *reinterpret_cast<const uint4*>(blk + 16 * (128 * h + c));
+        const uint32_t meta = *reinterpret_cast<const uint32_t*>(blk + 4 * (1024 + c));
+        const uint32_t zz = kMagic | ((meta >> 16) * 0x00010001u);
+        const uint32_t ss = prmt(meta, 0u, 0x1010u);
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        uint32_t v[16];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int ii = 0; ii < 4; ++ii)
+            v[4 * jj + ii] = hmul2(hsub2(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMagic), zz), ss);
+        tmem_st16(tmem_base + lane_addr + CF::A_COL0 + static_cast<uint32_t>(s * 32 + 16 * h), v);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          // the MMA waits on the second stage of each pair (or a tile's last, unpaired stage)
+          const bool sig = (kb & 1) || kb + 1 == KS;
+          if (rank == 0) {
+            if (warp == 2 && sig) mbar_arrive_expect_tx(&full_a[s], 4u * kDQ);
+            else mbar_arrive(&full_a[s]);
+          } else if (sig) {
+            st_async_signal(smem + CF::SIG_OFF + 4 * (warp - 2), &full_a[s], 0u);
+          }
+          mbar_arrive(&empty[s]);
+        }
+        if (++s == ST) { s = 0; ph ^= 1u; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int nl = 32 * q + lane;
+    int li = 0;
+    for (int tile = pair; tile < p.tiles; tile += npairs, ++li) {
+      const int m0 = (tile % p.tiles_t) * BT;
+      const int n = ((tile / p.tiles_t) * 2 + static_cast<int>(rank)) * kTN + nl;
+      const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+      if (!wait(acc_full, static_cast<uint32_t>(li & 1))) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+      uint32_t va[32], vb[32];
+      tmem_ld32_nowait(taddr, va);
+      tmem_wait_ld(va);
+#pragma unroll
+      for (int cc = 0; cc < BT / 32; ++cc) {
+        uint32_t (&cur)[32] = (cc & 1) ? vb : va;
+        uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
+        if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
+        const int t0 = m0 + 32 * cc;
+        if (n < p.N) {
+          __half* yp = p.y + static_cast<size_t>(t0) * p.N + n;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __float2half_rn(__uint_as_float(cur[j]) + bias);
+        }
+        if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_at(acc_empty, 0u);
+    }
+  }
+
+  __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while the other may still arrive on its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
+  }
+}
+
+cudaError_t launch_pair(const PackedParams& base, const GemmProblem& p) {
+  using CF = PairCfg;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int cap = 0;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(packed_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = CF::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&cap, packed_pair_kernel, &cfg) != cudaSuccess) cap = 0;
+    (void)cudaGetLastError();
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  if (cap <= 0) return cudaErrorInvalidConfiguration;
+  PackedParams pp = base;
+  const char* why = nullptr;
+  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, CF::BT / 2,
+                    CU_TENSOR_MAP_SWIZZLE_128B, &why))
+    return cudaErrorInvalidValue;
+  pp.tiles_t = (p.M + CF::BT - 1) / CF::BT;
+  const long long tiles = static_cast<long long>(pp.tiles_t) * ((p.N + 2 * kTN - 1) / (2 * kTN));
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  pp.tiles = static_cast<int>(tiles);
+  const int clusters = pp.tiles < cap ? pp.tiles : cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = CF::SMEM;
+  cfg.stream = p.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_pair_kernel, pp);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int BT>
 cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
   using CF = Cfg<BT>;
@@ -505,6 +867,11 @@ cudaError_t launch_packed(const GemmProblem& p, const void* packed) {
   pp.M = p.M; pp.K = p.K; pp.N = p.N;
   if (p.M <= 64) return launch_bt<64>(pp, p);
   if (p.M <= 128) return launch_bt<128>(pp, p);
+  // Pairs of column tiles (the packed layout holds ceil(N / 128) of them) for long K: sustained
+  // under the power cap the pair kernel ran 1508 against 1460 TFLOP/s on the 70B linears at
+  // M = 4096 (it moves half the activations per SM, so it clocks higher at the same power);
+  // at K = 4096 the single-CTA kernel was ahead (1374 against 1343 on the 7B linears).
+  if (p.K >= kPairMinK && ((p.N + kTN - 1) / kTN) % 2 == 0) return launch_pair(pp, p);
   return launch_bt<256>(pp, p);
 }
 
