@@ -112,6 +112,39 @@ def test_gemm_packed_long_k_pairs(awq, M, K, N):
                  f"packed M={M} K={K} N={N}")
 
 
+# narrow token tiles (32 / 64 / 128 rows) with K split over clusters of 2 or 4 CTAs, chosen by
+# tile count: 8 tiles of 32 rows (4-way), 4 of 64 (2-way), 8 of 128 (2-way), an uneven split
+# (K = 4160: 65 stages), a persistent unsplit launch (N = 28672: 224 tiles)
+NARROW = [(16, 4096, 1024), (32, 4096, 1024), (48, 2048, 512), (100, 4096, 1024), (9, 4160, 512),
+          (1, 4096, 4096), (24, 8192, 28672), (128, 11008, 4096)]
+
+
+@pytest.mark.parametrize("M,K,N", NARROW)
+def test_gemm_packed_narrow_split(awq, M, K, N):
+    d = synth.awq_linear(23400 + M + K, M, K, N, group_size=64, bias=True)
+    y = run(awq, d)
+    args = (d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 64)
+    if K * N <= 64 * 1024 * 1024:
+        assert_close(y, oracle.gemm(*args), f"packed narrow M={M} K={K} N={N}")
+    else:
+        rng = np.random.default_rng(6)
+        rows = np.concatenate([rng.integers(0, M, 2048), [0, M - 1]])
+        cols = np.concatenate([rng.integers(0, N, 2048), [0, N - 1]])
+        assert_close(y[rows, cols], oracle.gemm_sampled(*args, rows, cols), f"packed narrow M={M} K={K} N={N}")
+    assert np.array_equal(run(awq, d).view(np.uint16), y.view(np.uint16))  # fixed reduction order
+
+
+@pytest.mark.parametrize("M", [8, 32, 64, 128])
+def test_gemm_packed_narrow_split_exact_bitwise(awq, M):
+    # exact-arithmetic inputs: the split partial sums are exact in fp32, so y is the oracle's
+    # value rounded once to fp16 whatever the split
+    d = synth.awq_linear(23600 + M, M, 4096, 1024, group_size=128, bias=True, x_kind="smallint",
+                         scale_kind="pow2", bias_kind="dyadic")
+    y = run(awq, d)
+    want = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
+
+
 def test_gemm_packed_deterministic(awq):
     d = synth.awq_linear(23500, 700, 4096, 1024, group_size=128, bias=True)
     pk = packed_of(awq, d)

@@ -167,9 +167,10 @@ def awq_gemm(x, qweight, qzeros, scales, bias=None, group_size=128, out=None, pa
 
 
 # Rows from which a layer built with packed=True runs awq_gemm_packed (its tile-packed copy)
-# rather than awq_gemm on the checkpoint layout: the packed kernel's 256-row tiles start to
-# pay there (GB300: 53 against 71 us at 512 x 4096 x 11008).
-PACKED_MIN_ROWS = 256
+# rather than awq_gemm on the checkpoint layout: on GB300 the packed kernels were faster from
+# 128 rows on every 7B / 70B linear (e.g. 25.0 against 34.4 us at 128 x 4096 x 11008, 80.5
+# against 115 us at 128 x 8192 x 28672), mixed at 64 rows, slower at 32 and below.
+PACKED_MIN_ROWS = 128
 
 
 class AwqLinear:

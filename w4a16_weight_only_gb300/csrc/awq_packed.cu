@@ -200,6 +200,21 @@ __device__ __forceinline__ void mbar_arrive_at(uint64_t* local, uint32_t rank) {
   asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
 }
+// Cluster-window address of `local`'s offset in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+  return ra;
+}
+// Asynchronous 16-byte store to a cluster-window address, counted on the (cluster-window)
+// barrier `rbar`.
+__device__ __forceinline__ void st_async_v4_at(uint32_t raddr, uint32_t rbar, uint32_t a, uint32_t b,
+                                               uint32_t c, uint32_t d) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
+               : "memory");
+}
+
 // Asynchronous 4-byte store into CTA `rank`'s shared memory at `local`'s offset, counted (4
 // bytes) on that CTA's barrier at `bar`'s offset.  It does not block the issuing thread; the
 // barrier's completion releases the thread's earlier operations at cluster scope.
@@ -243,30 +258,42 @@ constexpr uint32_t idesc_ts() {
   return (1u << 4) | (static_cast<uint32_t>(BT >> 3) << 17) | (static_cast<uint32_t>(kTN >> 4) << 24);
 }
 
-// Per-BT resources: TMEM holds NACC accumulators of BT columns and one A slot of 32 columns
-// (64 K rows of fp16 pairs) per pipeline slot; shared memory holds, per slot, the activation
-// tile and the packed block.  One ring: slot s carries stage j's activations, packed block
-// and dequantized A operand, for j = s mod ST.
-template <int BT>
+// Resources of a (token tile BT, K split SPLIT) configuration.  TMEM holds NACC accumulators
+// of BT columns and one A slot of 32 columns (64 K rows of fp16 pairs) per pipeline slot;
+// shared memory holds, per slot, the activation tile and the packed block (one ring: slot s
+// carries stage j's activations, packed block and A operand, j = s mod ST), plus, in rank 0 of
+// a split, the other ranks' partial sums.  Narrow tiles (BT <= 64) allocate 256 TMEM columns
+// and at most half an SM's shared memory, so two CTAs share an SM.
+template <int BT, int SPLIT>
 struct Cfg {
   static constexpr int NACC = BT >= 256 ? 1 : 2;
-  static constexpr int SA_FIT = (512 - NACC * BT) / 32;
+  static constexpr bool kNarrow = BT <= 64;
+  static constexpr int COLS = kNarrow ? 256 : 512;           // TMEM columns allocated
+  static constexpr int SA_FIT = (COLS - NACC * BT) / 32;
   static constexpr int X_BYTES = BT * kTK * 2;
   static constexpr int STAGE = X_BYTES + kBlockBytes;
-  static constexpr int ST_FIT = (kSmemCap - 2048) / STAGE;
+  static constexpr int RECV_PITCH = BT + 4;                  // floats per received column
+  static constexpr int RECV_BYTES = (SPLIT - 1) * kTN * RECV_PITCH * 4;
+  static constexpr int CAP = kNarrow ? 112 * 1024 : kSmemCap;
+  static constexpr int ST_FIT = (CAP - 2048 - RECV_BYTES) / STAGE;
   static constexpr int ST0 = ST_FIT < SA_FIT ? ST_FIT : SA_FIT;
   static constexpr int ST = ST0 < 8 ? ST0 : 8;
   static constexpr int X_OFF = 0;
   static constexpr int B_OFF = ST * X_BYTES;
   static constexpr int BAR_OFF = B_OFF + ST * kBlockBytes;
-  // full_t[ST], empty[ST], full_a[ST], acc_full[2], acc_empty[2], drain
-  static constexpr int NBARS = 3 * ST + 5;
+  // full_t[ST], empty[ST], full_a[ST], acc_full[2], acc_empty[2], drain, recv
+  static constexpr int NBARS = 3 * ST + 6;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-  static constexpr int USED = 1024 + MISC_OFF + 16;
-  static constexpr int SMEM = USED < kSmemMin ? kSmemMin : USED;
+  static constexpr int RECV_OFF = ((MISC_OFF + 16 + 15) / 16) * 16;
+  static constexpr int USED = 1024 + RECV_OFF + RECV_BYTES;
+  // at most one CTA per SM with 512 columns, at most two with 256: tcgen05.alloc never waits
+  static constexpr int SMEM_MIN = kNarrow ? 80 * 1024 : kSmemMin;
+  static constexpr int SMEM = USED < SMEM_MIN ? SMEM_MIN : USED;
   static constexpr uint32_t A_COL0 = NACC * BT;
-  static_assert(ST >= 3 && SMEM <= kSmemCap, "resources");
-  static_assert(NACC * BT + ST * 32 <= 512, "TMEM columns");
+  // narrow tiles: two stages per dequant iteration (the dequant latency bounds them)
+  static constexpr bool kDqPairs = kNarrow;
+  static_assert(ST >= 3 && SMEM <= CAP, "resources");
+  static_assert(NACC * BT + ST * 32 <= COLS, "TMEM columns");
 };
 
 struct __align__(128) PackedParams {
@@ -279,9 +306,28 @@ struct __align__(128) PackedParams {
   int tiles_t, tiles;        // activation-row tiles, total tiles
 };
 
-template <int BT>
-__global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_constant__ PackedParams p) {
-  using CF = Cfg<BT>;
+// The tiles a CTA takes (tile0, tile0 + tstep, ...) and its K stages [kb0, kb1): without a
+// split, tiles blockIdx.x + k gridDim.x and all stages; with one, the cluster's tile and rank
+// r's share of the stages.  Each role of the kernel builds its own copy where it loops: one
+// copy built before the roles diverge made the 256-row kernel 11% slower.
+template <int SPLIT>
+struct Span {
+  int tile0, tstep, kb0, kb1;
+  __device__ __forceinline__ Span(int tiles, int KS, uint32_t krank)
+      : tile0(SPLIT > 1 ? static_cast<int>(blockIdx.x) / SPLIT : static_cast<int>(blockIdx.x)),
+        tstep(SPLIT > 1 ? tiles : static_cast<int>(gridDim.x)),
+        kb0(SPLIT > 1 ? static_cast<int>(static_cast<long long>(KS) * krank / SPLIT) : 0),
+        kb1(SPLIT > 1 ? static_cast<int>(static_cast<long long>(KS) * (krank + 1) / SPLIT) : KS) {}
+};
+
+// SPLIT > 1: a cluster of SPLIT CTAs shares one tile, CTA r taking K stages
+// [r KS / SPLIT, (r + 1) KS / SPLIT); ranks 1 .. SPLIT-1 push their fp32 accumulators into
+// rank 0's shared memory (st.async, counted on rank 0's recv barrier), and rank 0 adds them
+// in rank order, adds the bias and stores y.  Split launches give every cluster one tile.
+template <int BT, int SPLIT>
+__global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
+    packed_kernel(const __grid_constant__ PackedParams p) {
+  using CF = Cfg<BT, SPLIT>;
   constexpr int ST = CF::ST, NACC = CF::NACC;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -294,12 +340,14 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
   uint64_t* acc_full = bars + 3 * ST;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
+  uint64_t* recv_bar = drain + 1;     // split rank 0: the other ranks' partials landed
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int KS = p.K / kTK;
+  const uint32_t krank = SPLIT > 1 ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -312,16 +360,20 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
       mbar_init(&acc_empty[b], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(recv_bar, 1);
+    if (SPLIT > 1 && krank == 0u)  // the partials of ranks 1 .. SPLIT-1, one phase
+      mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((SPLIT - 1) * kTN * BT * 4));
     *abort_flag = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
-                     smem_u32(const_cast<uint32_t*>(tmem_slot)))
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot))), "n"(CF::COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   __syncthreads();
+  if constexpr (SPLIT > 1) cluster_sync_all();  // rank 0's recv barrier exists before any push
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -334,9 +386,25 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
     *abort_flag = 1u;
     return false;
   };
+  // the same with cluster-scope acquire (phases completed by other CTAs' pushes)
+  auto wait_cluster = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if (*abort_flag) return false;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_cl(bar, parity)) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(p.status, kStatusPackedTimeout);
+        *abort_flag = 1u;
+        return false;
+      }
+    }
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
+    const Span<SPLIT> sp(p.tiles, KS, krank);
+    const int tile0 = sp.tile0, tstep = sp.tstep, kb0 = sp.kb0, kb1 = sp.kb1;
     if (lane == 0) {
       prefetch_tmap(&p.tm_x);
       // packed blocks are read by the token tiles of one column tile, close together in time:
@@ -345,11 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
       int s = 0, issued = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < p.tiles; tile += tstep) {
         const int m0 = (tile % p.tiles_t) * BT;
         const int t = tile / p.tiles_t;
         const uint32_t* src = p.packed + static_cast<size_t>(t) * KS * kBlockWords;
-        for (int kb = 0; kb < KS; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait(&empty[s], ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + kBlockBytes));
           tma_load_2d_hint(smem + CF::X_OFF + s * CF::X_BYTES, &p.tm_x, &full_t[s], kb * kTK, m0, pol_x);
@@ -368,6 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    const Span<SPLIT> sp(p.tiles, KS, krank);
+    const int tile0 = sp.tile0, tstep = sp.tstep, kb0 = sp.kb0, kb1 = sp.kb1;
     // Stages go in pairs: one wait on the later stage's full_a covers both (every dequant
     // warp arrives on its slots in stage order, and each arrival releases the warp's TMEM
     // stores of all earlier stages); the activation tiles are in place once full_a is (the
@@ -377,13 +447,13 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
       int s = 0, li = 0;
       uint32_t ph = 0;
       bool ok = true, any = false;
-      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x, ++li) {
+      for (int tile = tile0; ok && tile < p.tiles; tile += tstep, ++li) {
         const int b = li % NACC;
         if (!wait(&acc_empty[b], static_cast<uint32_t>(((li / NACC) & 1) ^ 1))) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(b * BT);
-        for (int kb = 0; kb < KS; kb += 2) {
-          const int n2 = KS - kb < 2 ? KS - kb : 2;
+        for (int kb = kb0; kb < kb1; kb += 2) {
+          const int n2 = kb1 - kb < 2 ? kb1 - kb : 2;
           const int sl = s + n2 - 1 < ST ? s + n2 - 1 : s + n2 - 1 - ST;
           const uint32_t phl = s + n2 - 1 < ST ? ph : ph ^ 1u;
           if (!wait(&full_a[sl], phl)) { ok = false; break; }
@@ -393,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
             const uint64_t bdesc = sw128_kmajor_desc(sbase + CF::X_OFF + s * CF::X_BYTES);
 #pragma unroll
             for (int ks = 0; ks < kTK / 16; ++ks)  // K += 16: A 8 TMEM columns, B 32 bytes
-              mma_ts(d, a + 8u * ks, bdesc + 2u * ks, idesc, (kb + i > 0 || ks > 0) ? 1u : 0u);
+              mma_ts(d, a + 8u * ks, bdesc + 2u * ks, idesc, (kb + i > kb0 || ks > 0) ? 1u : 0u);
             mma_commit(&empty[s]);
             if (++s == ST) { s = 0; ph ^= 1u; }
           }
@@ -410,53 +480,88 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
     __syncwarp();
   } else if (warp < 2 + kDQ) {
     // ------------------------------------------------------------------ dequant
+    const Span<SPLIT> sp(p.tiles, KS, krank);
+    const int tile0 = sp.tile0, tstep = sp.tstep, kb0 = sp.kb0, kb1 = sp.kb1;
     // Thread = output column c of the tile (TMEM lane), K half h of every stage: the four
     // code words of its half-run (one 16-byte load, lanes contiguous) and its meta word;
     // pair i of the result holds rows 32 h + 2 i, +1 (nibbles i % 4 and i % 4 + 4 of word
     // i / 4), stored to TMEM columns 16 h + i of the slot's A operand.  The slot's A operand
     // is free once its activations have landed: the producer refilled the slot only after
-    // the previous round's MMAs completed.
+    // the previous round's MMAs completed.  Narrow tiles take two consecutive stages per
+    // iteration (the CTA's stages of all its tiles form one sequence), overlapping the
+    // pair's waits, loads and TMEM stores.
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     const int c = 32 * q + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    const int my_tiles = tile0 < p.tiles ? (p.tiles - 1 - tile0) / tstep + 1 : 0;
+    const long long total = static_cast<long long>(my_tiles) * (kb1 - kb0);  // the CTA's stages
+    constexpr int kStep = CF::kDqPairs ? 2 : 1;
+    auto convert = [&](const uint4& w4, uint32_t meta, uint32_t (&v)[16]) {
+      const uint32_t zz = kMagic | ((meta >> 16) * 0x00010001u);  // (1024 + z) in both halves
+      const uint32_t ss = prmt(meta, 0u, 0x1010u);                  // scale in both halves
+      const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii)
+          v[4 * jj + ii] = hmul2(hsub2(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMagic), zz), ss);
+    };
     int s = 0;
     uint32_t ph = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
-      for (int kb = 0; kb < KS; ++kb) {
-        if (!wait(&full_t[s], ph)) { ok = false; break; }
-        tc_fence_after();  // the TMEM stores below come after the previous round's MMAs
-        const unsigned char* blk = smem + CF::B_OFF + s * kBlockBytes;
-        const uint4 w4 = *reinterpret_cast<const uint4*>(blk + 16 * (128 * h + c));
-        const uint32_t meta = *reinterpret_cast<const uint32_t*>(blk + 4 * (1024 + c));
-        const uint32_t zz = kMagic | ((meta >> 16) * 0x00010001u);  // (1024 + z) in both halves
-        const uint32_t ss = prmt(meta, 0u, 0x1010u);                  // scale in both halves
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-        uint32_t v[16];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-          for (int ii = 0; ii < 4; ++ii)
-            v[4 * jj + ii] = hmul2(hsub2(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMagic), zz), ss);
-        tmem_st16(tmem_base + lane_addr + CF::A_COL0 + static_cast<uint32_t>(s * 32 + 16 * h), v);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&full_a[s]);
-          mbar_arrive(&empty[s]);
+    for (long long g = 0; g < total; g += kStep) {
+      const bool two = kStep == 2 && g + 1 < total;
+      const int s1 = s + 1 == ST ? 0 : s + 1;
+      const uint32_t ph1 = s + 1 == ST ? ph ^ 1u : ph;
+      if (!wait(&full_t[s], ph)) break;
+      const unsigned char* b0 = smem + CF::B_OFF + s * kBlockBytes;
+      const uint4 w0 = *reinterpret_cast<const uint4*>(b0 + 16 * (128 * h + c));
+      const uint32_t m0 = *reinterpret_cast<const uint32_t*>(b0 + 4 * (1024 + c));
+      uint4 w1 = make_uint4(0u, 0u, 0u, 0u);
+      uint32_t m1 = 0u;
+      if (two) {
+        if (!wait(&full_t[s1], ph1)) break;
+        const unsigned char* b1 = smem + CF::B_OFF + s1 * kBlockBytes;
+        w1 = *reinterpret_cast<const uint4*>(b1 + 16 * (128 * h + c));
+        m1 = *reinterpret_cast<const uint32_t*>(b1 + 4 * (1024 + c));
+      }
+      tc_fence_after();  // the TMEM stores below come after the previous round's MMAs
+      uint32_t v[16];
+      convert(w0, m0, v);
+      tmem_st16(tmem_base + lane_addr + CF::A_COL0 + static_cast<uint32_t>(s * 32 + 16 * h), v);
+      if (two) {
+        convert(w1, m1, v);
+        tmem_st16(tmem_base + lane_addr + CF::A_COL0 + static_cast<uint32_t>(s1 * 32 + 16 * h), v);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&full_a[s]);
+        mbar_arrive(&empty[s]);
+        if (two) {
+          mbar_arrive(&full_a[s1]);
+          mbar_arrive(&empty[s1]);
         }
-        if (++s == ST) { s = 0; ph ^= 1u; }
+      }
+      if (two) {
+        s = s1 + 1 == ST ? 0 : s1 + 1;
+        ph = s1 + 1 == ST ? ph1 ^ 1u : ph1;
+      } else {
+        s = s1;
+        ph = ph1;
       }
     }
   } else {
     // ------------------------------------------------------------------ epilogue
+    const Span<SPLIT> sp(p.tiles, KS, krank);
+    const int tile0 = sp.tile0, tstep = sp.tstep;
     // The next 32-column chunk is loaded from TMEM while the current one is stored.
     const int q = warp & 3;              // TMEM lanes 32 q .. 32 q + 31
     const int nl = 32 * q + lane;        // output column inside the tile
+    float* recv = reinterpret_cast<float*>(smem + CF::RECV_OFF);
     int li = 0;
-    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++li) {
+    for (int tile = tile0; tile < p.tiles; tile += tstep, ++li) {
       const int b = li % NACC;
       const int m0 = (tile % p.tiles_t) * BT;
       const int n = (tile / p.tiles_t) * kTN + nl;
@@ -464,22 +569,65 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
       if (!wait(&acc_full[b], static_cast<uint32_t>((li / NACC) & 1))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT);
-      uint32_t va[32], vb[32];
-      tmem_ld32_nowait(taddr, va);
-      tmem_wait_ld(va);
+      if (SPLIT > 1 && krank != 0u) {
+        // this rank's partial sums of column nl, all BT rows, into rank 0
+        const uint32_t rbar = cluster_addr(recv_bar, 0u);
+        const uint32_t rdst = cluster_addr(recv + (static_cast<int>(krank - 1) * kTN + nl) * CF::RECV_PITCH, 0u);
+#pragma unroll 1
+        for (int cc = 0; cc < BT / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32_nowait(taddr + 32 * cc, v);
+          tmem_wait_ld(v);
 #pragma unroll
-      for (int cc = 0; cc < BT / 32; ++cc) {
-        uint32_t (&cur)[32] = (cc & 1) ? vb : va;
-        uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
-        if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
-        const int t0 = m0 + 32 * cc;
-        if (n < p.N) {
-          __half* yp = p.y + static_cast<size_t>(t0) * p.N + n;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __float2half_rn(__uint_as_float(cur[j]) + bias);
+          for (int j = 0; j < 32; j += 4)
+            st_async_v4_at(rdst + static_cast<uint32_t>((32 * cc + j) * 4), rbar, v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
-        if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
+      } else {
+        if (SPLIT > 1 && !wait_cluster(recv_bar, 0u)) break;
+        // chunk cc of the accumulator (in cur), plus the other ranks' partials in rank order,
+        // plus the bias, rounded once and stored
+        auto finish = [&](int cc, uint32_t (&cur)[32]) {
+#pragma unroll
+          for (int r = 1; r < SPLIT; ++r) {
+            const float* src = recv + ((r - 1) * kTN + nl) * CF::RECV_PITCH + 32 * cc;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 q4 = *reinterpret_cast<const float4*>(src + j);
+              cur[j] = __float_as_uint(__uint_as_float(cur[j]) + q4.x);
+              cur[j + 1] = __float_as_uint(__uint_as_float(cur[j + 1]) + q4.y);
+              cur[j + 2] = __float_as_uint(__uint_as_float(cur[j + 2]) + q4.z);
+              cur[j + 3] = __float_as_uint(__uint_as_float(cur[j + 3]) + q4.w);
+            }
+          }
+          const int t0 = m0 + 32 * cc;
+          if (n < p.N) {
+            __half* yp = p.y + static_cast<size_t>(t0) * p.N + n;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __float2half_rn(__uint_as_float(cur[j]) + bias);
+          }
+        };
+        if constexpr (CF::kNarrow) {  // one or two chunks: no prefetch (register budget)
+#pragma unroll 1
+          for (int cc = 0; cc < BT / 32; ++cc) {
+            uint32_t v[32];
+            tmem_ld32_nowait(taddr + 32 * cc, v);
+            tmem_wait_ld(v);
+            finish(cc, v);
+          }
+        } else {
+          uint32_t va[32], vb[32];
+          tmem_ld32_nowait(taddr, va);
+          tmem_wait_ld(va);
+#pragma unroll
+          for (int cc = 0; cc < BT / 32; ++cc) {
+            uint32_t (&cur)[32] = (cc & 1) ? vb : va;
+            uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
+            if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
+            finish(cc, cur);
+            if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -487,10 +635,15 @@ __global__ void __launch_bounds__(kThreads, 1) packed_kernel(const __grid_consta
     }
   }
 
+  // split: rank 0 leaves only once the other ranks' pushes have landed (bounded: after a
+  // give-up elsewhere some may never come), and no rank leaves before the others are done
+  if (SPLIT > 1 && krank == 0u && threadIdx.x == 0) (void)wait_cluster(recv_bar, 0u);
   __syncthreads();
+  if constexpr (SPLIT > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(CF::COLS)
+                 : "memory");
   }
 }
 
@@ -807,13 +960,13 @@ cudaError_t launch_pair(const PackedParams& base, const GemmProblem& p) {
   return cudaGetLastError();
 }
 
-template <int BT>
+template <int BT, int SPLIT>
 cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
-  using CF = Cfg<BT>;
+  using CF = Cfg<BT, SPLIT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(packed_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    attr_err = cudaFuncSetAttribute(packed_kernel<BT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   PackedParams pp = base;
@@ -823,15 +976,55 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
     return cudaErrorInvalidValue;
   pp.tiles_t = (p.M + BT - 1) / BT;
   const long long tiles = static_cast<long long>(pp.tiles_t) * ((p.N + kTN - 1) / kTN);
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (tiles * SPLIT > 0x7fffffffLL) return cudaErrorInvalidValue;
   pp.tiles = static_cast<int>(tiles);
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (SPLIT == 1) {  // persistent over the tiles, as many CTAs as are resident at once
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int cap = (CF::kNarrow ? 2 : 1) * sms;
+    const int grid = pp.tiles < cap ? pp.tiles : cap;
+    packed_kernel<BT, SPLIT><<<grid, kThreads, CF::SMEM, p.stream>>>(pp);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pp.tiles * SPLIT), 1, 1);  // one tile per cluster
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = CF::SMEM;
+  cfg.stream = p.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = SPLIT;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_kernel<BT, SPLIT>, pp);
   if (e != cudaSuccess) return e;
-  const int grid = pp.tiles < sms ? pp.tiles : sms;
-  packed_kernel<BT><<<grid, kThreads, CF::SMEM, p.stream>>>(pp);
   return cudaGetLastError();
+}
+
+// Token tile and K split of a launch with M <= 128 rows: the narrowest tile holding M rows
+// (32, 64 or 128), and the largest split (2 or 4 for 32 rows, 2 for 64 and 128) that keeps
+// every CTA resident in one wave (two CTAs per SM below 128-row tiles) with at least four
+// stages each.
+struct PackedPlan {
+  int bt = 256, split = 1;
+};
+PackedPlan packed_plan(int M, int K, int N, int sms) {
+  PackedPlan pl;
+  if (M > 128) return pl;
+  pl.bt = M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  const long long tiles = static_cast<long long>((M + pl.bt - 1) / pl.bt) * ((N + kTN - 1) / kTN);
+  const long long cap = static_cast<long long>(pl.bt <= 64 ? 2 : 1) * sms;
+  const int KS = K / kTK;
+  for (int split : {2, 4}) {
+    if (split == 4 && pl.bt != 32) continue;
+    if (KS / split < 4 || tiles * split > cap) continue;
+    pl.split = split;
+  }
+  return pl;
 }
 
 }  // namespace
@@ -865,14 +1058,21 @@ cudaError_t launch_packed(const GemmProblem& p, const void* packed) {
   cudaError_t e = status_word_ptr(&pp.status);
   if (e != cudaSuccess) return e;
   pp.M = p.M; pp.K = p.K; pp.N = p.N;
-  if (p.M <= 64) return launch_bt<64>(pp, p);
-  if (p.M <= 128) return launch_bt<128>(pp, p);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const PackedPlan pl = packed_plan(p.M, p.K, p.N, sms);
+  if (pl.bt == 32)
+    return pl.split == 4 ? launch_bt<32, 4>(pp, p) : pl.split == 2 ? launch_bt<32, 2>(pp, p) : launch_bt<32, 1>(pp, p);
+  if (pl.bt == 64) return pl.split == 2 ? launch_bt<64, 2>(pp, p) : launch_bt<64, 1>(pp, p);
+  if (pl.bt == 128) return pl.split == 2 ? launch_bt<128, 2>(pp, p) : launch_bt<128, 1>(pp, p);
   // Pairs of column tiles (the packed layout holds ceil(N / 128) of them) for long K: sustained
   // under the power cap the pair kernel ran 1508 against 1460 TFLOP/s on the 70B linears at
   // M = 4096 (it moves half the activations per SM, so it clocks higher at the same power);
   // at K = 4096 the single-CTA kernel was ahead (1374 against 1343 on the 7B linears).
   if (p.K >= kPairMinK && ((p.N + kTN - 1) / kTN) % 2 == 0) return launch_pair(pp, p);
-  return launch_bt<256>(pp, p);
+  return launch_bt<256, 1>(pp, p);
 }
 
 }  // namespace awq
