@@ -818,6 +818,20 @@ def run_sweep(args, local):
                          "cublas_fp16_dense_us": t_mm, "cublas_fp16_dense_TFLOP_s": flop / t_mm / 1e6,
                          "dequant_plus_cublas_us": t_dq + t_mm})
             del wd
+            if dt == "f16" and K % 64 == 0 and (G == -1 or G % 64 == 0):
+                # the tile-packed layout: the one-off repack, then awq_gemm_packed with the
+                # stream's workspace (stream-K where the plan takes it)
+                pk = awq.awq_repack(qw, qz, sc, G, stream=stream)
+                rp = lambda: awq.awq_repack(qw, qz, sc, G, out=pk, stream=stream)
+                timed(rp, 2)
+                t_rp = timed(rp, 5)
+                ws = torch.zeros((awq.awq_gemm_packed_workspace_size(),), dtype=torch.uint8, device="cuda")
+                fp = lambda: awq.awq_gemm_packed(x, pk, bias, K, N, G, out=y, stream=stream, workspace=ws)
+                timed(fp, 3)
+                t_p = timed(fp, 10)
+                line.update({"packed_us": t_p, "packed_TFLOP_s": flop / t_p / 1e6,
+                             "packed_frac_tensor": flop / t_p / 1e6 / tflops, "repack_us": t_rp})
+                del pk, ws
         awq.device_status()
         line.update({"hbm_peak_GB_s": hbm, "hbm_peak": hbm_kind, "tensor_peak_TFLOP_s": tflops,
                      "tensor_peak": tf_kind})

@@ -322,6 +322,31 @@ awq_status_t awq_gemm_packed(const void* x_f16, const void* packed, const void* 
                              int64_t M, int64_t K, int64_t N, int64_t group_size, void* y_f16,
                              awq_stream_t stream);
 
+/*
+ * The packed linear with a workspace, for prefill shapes whose 256-row x 128-column tiles
+ * leave SMs idle in the last round (e.g. 512 x 4096 x 11008: 172 tiles on 152 SMs).  Such
+ * calls run a stream-K kernel: the tiles' 64-row K stages form one sequence split evenly over
+ * one CTA per SM; a tile cut between CTAs is finished by the CTA holding its first stages,
+ * which adds the other CTAs' fp32 partial sums (written to the workspace) in CTA order.  Other
+ * shapes run exactly as awq_gemm_packed.  (No page prints a work split; stream-K is the
+ * published decomposition of Osama et al., "Stream-K", PPoPP 2023.)
+ *
+ * awq_gemm_packed_workspace_size: bytes the current device needs (256-byte flag area sized by
+ *   the SM count, then 128 KB per SM).
+ * awq_gemm_packed_ws: arguments as awq_gemm_packed, plus workspace (DEVICE, caller-owned,
+ *   256-byte aligned, workspace_bytes >= awq_gemm_packed_workspace_size, its first
+ *   256-byte-rounded 4 * SM-count bytes ZERO before the first call; each call leaves them
+ *   zero).  A workspace smaller than required (or NULL) gives awq_gemm_packed's plan.
+ *   Results: awq_gemm_packed's criterion, and bitwise repeatable for a given shape and
+ *   device; they may differ from awq_gemm_packed's in the last bits (another summation
+ *   order).  Calls that share a workspace must not overlap in time (order them on one
+ *   stream).  After awq_device_status reports a timeout, zero the flag area again.
+ */
+awq_status_t awq_gemm_packed_workspace_size(size_t* bytes);
+awq_status_t awq_gemm_packed_ws(const void* x_f16, const void* packed, const void* bias_f16,
+                                int64_t M, int64_t K, int64_t N, int64_t group_size, void* y_f16,
+                                void* workspace, size_t workspace_bytes, awq_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the library's device status word on the
  * current device.  Returns AWQ_ERR_TIMEOUT if a kernel gave up a bounded wait since the
  * last check (its output is then unspecified), AWQ_OK otherwise. */

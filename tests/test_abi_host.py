@@ -254,6 +254,16 @@ def test_packed_layout_argument_checks_are_host_side(lib):
     assert g(P(0x100002), B, None, 4, 256, 64, 128, B, None) == MISALIGNED      # x 16-byte aligned
     assert g(A, B, None, 0, 256, 64, 128, B, None) == 0                  # M == 0: no launch
     assert g(A, B, None, -1, 256, 64, 128, B, None) == INVALID
+    w = lib.awq_gemm_packed_ws
+    # (x, packed, bias, M, K, N, G, y, workspace, workspace_bytes, stream)
+    assert w(A, B, None, 4, 96, 64, 32, B, A, 1 << 20, None) == SHAPE
+    assert w(A, B, None, 4, 256, 64, 128, B, P(0x100010), 1 << 20, None) == MISALIGNED  # 256-byte aligned
+    assert w(A, B, None, 0, 256, 64, 128, B, A, 1 << 20, None) == 0         # M == 0: no launch
+    assert w(None, B, None, 4, 256, 64, 128, B, A, 1 << 20, None) == INVALID
+    assert lib.awq_gemm_packed_workspace_size(None) == INVALID
     if not torch.cuda.is_available():
         assert g(A, B, None, 4, 256, 64, 128, B, None) == DEVICE
         assert r(A, A, A, 256, 64, 128, B, None) == DEVICE
+        assert w(A, B, None, 4, 256, 64, 128, B, A, 1 << 20, None) == DEVICE
+        assert w(A, B, None, 4, 256, 64, 128, B, None, 0, None) == DEVICE    # no workspace: plain plan
+        assert lib.awq_gemm_packed_workspace_size(ctypes.byref(n)) == DEVICE

@@ -97,17 +97,34 @@ def test_linear_refuses_bad_activations(awq):
 @pytest.mark.parametrize("M", [1, 40, 127, 128, 700])
 def test_linear_packed_switches_layout_by_rows(awq, M):
     # packed=True keeps a tile-packed copy: calls of >= packed_min_rows rows run
-    # awq_gemm_packed on it (bit for bit the functional call), smaller ones the checkpoint
-    # layout (bit for bit awq_gemm); both within the oracle's tolerance
+    # awq_gemm_packed_ws on it (bit for bit the functional call with the stream's workspace),
+    # smaller ones the checkpoint layout (bit for bit awq_gemm); both within the oracle's
+    # tolerance
     K, N, G = 1024, 392, 128
     d = synth.awq_linear(20400 + M, M, K, N, group_size=G, bias=True)
     x, qw, qz, sc, b = (dev(d[k]) for k in ("x", "qweight", "qzeros", "scales", "bias"))
     lin = awq.AwqLinear(qw, qz, sc, b, group_size=G, packed=True)
     y = lin(x)
     if M >= lin.packed_min_rows:
-        y_ref = awq.awq_gemm_packed(x, awq.awq_repack(qw, qz, sc, G), b, K, N, G)
+        y_ref = awq.awq_gemm_packed(x, awq.awq_repack(qw, qz, sc, G), b, K, N, G, workspace="auto")
     else:
         y_ref = awq.awq_gemm(x, qw, qz, sc, b, group_size=G)
+    torch.cuda.synchronize()
+    assert same(y, y_ref)
+    ref = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+    assert (err <= 1e-2 * np.maximum(1.0, np.abs(ref))).all()
+
+
+def test_linear_packed_stream_k_shape(awq):
+    # 2 x 16 tiles of 256 x 128 on one CTA per SM: the layer's call runs the stream-K kernel
+    # through the stream's workspace, bit for bit the functional call with that workspace
+    M, K, N, G = 257, 4096, 2048, 128
+    d = synth.awq_linear(20450, M, K, N, group_size=G, bias=True)
+    x, qw, qz, sc, b = (dev(d[k]) for k in ("x", "qweight", "qzeros", "scales", "bias"))
+    lin = awq.AwqLinear(qw, qz, sc, b, group_size=G, packed=True)
+    y = lin(x)
+    y_ref = awq.awq_gemm_packed(x, awq.awq_repack(qw, qz, sc, G), b, K, N, G, workspace="auto")
     torch.cuda.synchronize()
     assert same(y, y_ref)
     ref = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)

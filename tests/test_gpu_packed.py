@@ -145,6 +145,83 @@ def test_gemm_packed_narrow_split_exact_bitwise(awq, M):
     assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
 
 
+# Stream-K (awq_gemm_packed_ws): shapes whose 256-row tiles fill the SMs poorly, with K
+# stages cut between CTAs (a tile spread over several CTAs at 257 x 4096 x 2048), ragged rows
+# and columns, G = 64 / 128 / -1, and a long-K shape the pair kernel would otherwise take
+# (up to three contributors per finished tile at 512 x 11008 x 4096)
+SK = [(257, 4096, 2048, 128, True), (384, 4096, 2048, -1, True), (700, 8192, 1032, 64, True),
+      (512, 4096, 11008, 128, False), (512, 11008, 4096, 128, True)]
+
+
+def sk_flag_bytes():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return (sms * 4 + 255) // 256 * 256
+
+
+def run_ws(awq, d, ws, pk=None):
+    pk = packed_of(awq, d) if pk is None else pk
+    b = None if d["bias"] is None else dev(d["bias"])
+    y = awq.awq_gemm_packed(dev(d["x"]), pk, b, d["K"], d["N"], d["group_size"], workspace=ws)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,K,N,G,bias", SK)
+def test_gemm_packed_stream_k(awq, M, K, N, G, bias):
+    d = synth.awq_linear(24000 + M + K, M, K, N, group_size=G, bias=bias)
+    ws = torch.zeros(awq.awq_gemm_packed_workspace_size(), dtype=torch.uint8, device="cuda")
+    pk = packed_of(awq, d)
+    y = run_ws(awq, d, ws, pk)
+    fb = sk_flag_bytes()
+    assert not ws[:fb].any().item()      # every flag lowered again
+    assert ws[fb:].any().item()          # partial sums were written: the stream-K kernel ran
+    args = (d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    if K * N <= 64 * 1024 * 1024:
+        assert_close(y, oracle.gemm(*args), f"stream-K M={M} K={K} N={N} G={G}")
+    else:
+        rng = np.random.default_rng(8)
+        rows = np.concatenate([rng.integers(0, M, 4096), [0, M - 1]])
+        cols = np.concatenate([rng.integers(0, N, 4096), [0, N - 1]])
+        assert_close(y[rows, cols], oracle.gemm_sampled(*args, rows, cols), f"stream-K M={M} K={K} N={N}")
+    assert np.array_equal(run_ws(awq, d, ws, pk).view(np.uint16), y.view(np.uint16))  # fixed order
+
+
+def test_gemm_packed_stream_k_exact_bitwise(awq):
+    # exact-arithmetic inputs: every partial sum is exact in fp32, so the CTA-cut tiles give the
+    # oracle's value rounded once to fp16
+    d = synth.awq_linear(24500, 257, 4096, 2048, group_size=128, bias=True, x_kind="smallint",
+                         scale_kind="pow2", bias_kind="dyadic")
+    ws = torch.zeros(awq.awq_gemm_packed_workspace_size(), dtype=torch.uint8, device="cuda")
+    y = run_ws(awq, d, ws)
+    assert ws[sk_flag_bytes():].any().item()
+    want = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
+
+
+def test_gemm_packed_stream_k_workspace_reuse(awq):
+    # one workspace across stream-K shapes of different grids and a shape that does not take
+    # stream-K, in rotation: each result bit for bit its first value
+    cases = [synth.awq_linear(24600 + i, M, K, N, group_size=128, bias=True)
+             for i, (M, K, N) in enumerate([(257, 4096, 2048), (1000, 512, 256), (384, 4096, 2048)])]
+    ws = torch.zeros(awq.awq_gemm_packed_workspace_size(), dtype=torch.uint8, device="cuda")
+    pks = [packed_of(awq, d) for d in cases]
+    first = [run_ws(awq, d, ws, pk) for d, pk in zip(cases, pks)]
+    for _ in range(3):
+        for d, pk, y0 in zip(cases, pks, first):
+            assert np.array_equal(run_ws(awq, d, ws, pk).view(np.uint16), y0.view(np.uint16))
+    assert not ws[:sk_flag_bytes()].any().item()
+
+
+def test_gemm_packed_ws_small_workspace_is_the_plain_plan(awq):
+    # a workspace below the required size gives awq_gemm_packed's own launch, bit for bit
+    d = synth.awq_linear(24700, 257, 4096, 2048, group_size=128, bias=True)
+    pk = packed_of(awq, d)
+    small = torch.zeros(awq.awq_gemm_packed_workspace_size() - 256, dtype=torch.uint8, device="cuda")
+    y = run_ws(awq, d, small, pk)
+    assert not small.any().item()
+    assert np.array_equal(y.view(np.uint16), run(awq, d, pk).view(np.uint16))
+
+
 def test_gemm_packed_deterministic(awq):
     d = synth.awq_linear(23500, 700, 4096, 1024, group_size=128, bias=True)
     pk = packed_of(awq, d)

@@ -46,6 +46,8 @@ SIGNATURES = {
     "awq_repack_size": (_i32, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
     "awq_repack": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "awq_gemm_packed": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "awq_gemm_packed_workspace_size": (_i32, [ctypes.POINTER(ctypes.c_size_t)]),
+    "awq_gemm_packed_ws": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, ctypes.c_size_t, _vp]),
 }
 GEMM_STATIC_WEIGHTS = 1
 
@@ -252,10 +254,11 @@ class AwqLinear:
                              f"on device {self.device}")
         w = self._w
         if self.packed is not None and M >= self.packed_min_rows:
-            st = _lib.awq_gemm_packed(x.data_ptr(), self.packed.data_ptr(), w[3], M, K, N,
-                                      self.group_size, out.data_ptr(),
-                                      (stream if isinstance(stream, int) else stream.cuda_stream)
-                                      if stream is not None else torch.cuda.current_stream().cuda_stream)
+            sh = ((stream if isinstance(stream, int) else stream.cuda_stream)
+                  if stream is not None else torch.cuda.current_stream().cuda_stream)
+            ws = packed_workspace(self.device, sh)
+            st = _lib.awq_gemm_packed_ws(x.data_ptr(), self.packed.data_ptr(), w[3], M, K, N,
+                                         self.group_size, out.data_ptr(), ws.data_ptr(), ws.numel(), sh)
             if st != AWQ_OK:
                 raise AwqError(st, last_error())
             return out
@@ -455,10 +458,35 @@ def awq_repack(qweight, qzeros, scales, group_size=128, out=None, stream=None):
     return out
 
 
-def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None):
+def awq_gemm_packed_workspace_size() -> int:
+    """Bytes of workspace awq_gemm_packed_ws needs on the current device."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().awq_gemm_packed_workspace_size(ctypes.byref(n)))
+    return int(n.value)
+
+
+_workspaces = {}
+
+
+def packed_workspace(device, stream_handle):
+    """The zero-filled uint8 workspace that packed calls on (device, stream) share (calls on
+    one stream never overlap).  Allocated by PyTorch on first use: make the first packed call
+    on a stream outside CUDA graph capture."""
+    key = (int(device), int(stream_handle))
+    ws = _workspaces.get(key)
+    if ws is None:
+        with torch.cuda.device(int(device)):
+            ws = torch.zeros((awq_gemm_packed_workspace_size(),), dtype=torch.uint8, device=int(device))
+        _workspaces[key] = ws
+    return ws
+
+
+def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None, workspace=None):
     """y = x @ W (+ bias) with W in the tile-packed layout (awq_repack's output) via the
     library's awq_gemm_packed; x fp16 [..., K] (leading dims flattened), bias fp16 [N] or
-    None.  Returns fp16 [..., N]."""
+    None.  Returns fp16 [..., N].  workspace: a zero-filled uint8 device tensor of at least
+    awq_gemm_packed_workspace_size() bytes, or "auto" for the (device, stream) one: the call
+    then goes through awq_gemm_packed_ws (stream-K on shapes that fill the SMs poorly)."""
     lib = load_library()
     lead = x.shape[:-1]
     if x.shape[-1] != K:
@@ -474,6 +502,14 @@ def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None
         out = torch.empty((M, N), dtype=torch.float16, device=dev)
     else:
         _need(out, "out", torch.float16, (M, N), dev)
-    _check(lib.awq_gemm_packed(_ptr(x2), _ptr(packed), _ptr(bias), M, K, N, group_size, _ptr(out),
-                               _stream(stream)))
+    sh = _stream(stream)
+    if workspace is None:
+        _check(lib.awq_gemm_packed(_ptr(x2), _ptr(packed), _ptr(bias), M, K, N, group_size, _ptr(out), sh))
+    else:
+        if isinstance(workspace, str) and workspace == "auto":
+            workspace = packed_workspace(dev, sh.value or 0)
+        if workspace.dtype is not torch.uint8 or workspace.get_device() != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous uint8 tensor on x's device")
+        _check(lib.awq_gemm_packed_ws(_ptr(x2), _ptr(packed), _ptr(bias), M, K, N, group_size, _ptr(out),
+                                      workspace.data_ptr(), workspace.numel(), sh))
     return out.reshape(*lead, N)

@@ -463,9 +463,9 @@ awq_status_t awq_repack(const int32_t* qweight, const int32_t* qzeros, const voi
   return ok();
 }
 
-awq_status_t awq_gemm_packed(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
-                             int64_t K, int64_t N, int64_t group_size, void* y_f16,
-                             awq_stream_t stream) {
+static awq_status_t gemm_packed(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
+                                int64_t K, int64_t N, int64_t group_size, void* y_f16, void* workspace,
+                                size_t workspace_bytes, awq_stream_t stream) {
   if (M < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "M must be >= 0 (got %lld)", (long long)M);
   int G = 0;
   awq_status_t st = check_weight_shape(K, N, group_size, &G);
@@ -492,9 +492,34 @@ awq_status_t awq_gemm_packed(const void* x_f16, const void* packed, const void* 
   p.N = static_cast<int>(N);
   p.G = G;
   p.stream = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = awq::launch_packed(p, packed);
+  const cudaError_t e = awq::launch_packed(p, packed, workspace, workspace_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_packed launch");
   return ok();
+}
+
+awq_status_t awq_gemm_packed(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
+                             int64_t K, int64_t N, int64_t group_size, void* y_f16,
+                             awq_stream_t stream) {
+  return gemm_packed(x_f16, packed, bias_f16, M, K, N, group_size, y_f16, nullptr, 0, stream);
+}
+
+awq_status_t awq_gemm_packed_workspace_size(size_t* bytes) {
+  if (!bytes) return fail(AWQ_ERR_INVALID_ARGUMENT, "null bytes pointer");
+  awq_status_t st = check_device();
+  if (st != AWQ_OK) return st;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the SM count");
+  *bytes = awq::packed_workspace_bytes(sms);
+  return ok();
+}
+
+awq_status_t awq_gemm_packed_ws(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
+                                int64_t K, int64_t N, int64_t group_size, void* y_f16, void* workspace,
+                                size_t workspace_bytes, awq_stream_t stream) {
+  if (workspace && !al(workspace, 256)) return fail(AWQ_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  return gemm_packed(x_f16, packed, bias_f16, M, K, N, group_size, y_f16, workspace, workspace_bytes, stream);
 }
 
 awq_status_t awq_device_status(awq_stream_t stream) {

@@ -93,7 +93,11 @@ bool packed_supported(int64_t K, int64_t N, int64_t G, const char** why);
 size_t packed_bytes(int64_t K, int64_t N);
 cudaError_t launch_repack(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
                           int G, void* out, cudaStream_t stream);
-cudaError_t launch_packed(const GemmProblem& p, const void* packed);
+// With a workspace of at least packed_workspace_bytes(SM count) bytes (flags zero), launches
+// with M > 128 whose tiles fill the SMs poorly run the stream-K kernel.
+size_t packed_workspace_bytes(int sms);
+cudaError_t launch_packed(const GemmProblem& p, const void* packed, void* workspace = nullptr,
+                          size_t workspace_bytes = 0);
 
 // Failure-detection self test: a bounded wait that nothing completes (see awq.h).
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);

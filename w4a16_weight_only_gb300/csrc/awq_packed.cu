@@ -275,7 +275,10 @@ struct Cfg {
   static constexpr int RECV_PITCH = BT + 4;                  // floats per received column
   static constexpr int RECV_BYTES = (SPLIT - 1) * kTN * RECV_PITCH * 4;
   static constexpr int CAP = kNarrow ? 112 * 1024 : kSmemCap;
-  static constexpr int ST_FIT = (CAP - 2048 - RECV_BYTES) / STAGE;
+  // one accumulator (the MMA waits for the epilogue): y leaves through a 1 KB staging tile
+  // per epilogue warp (16 rows x 32 columns) as 16-byte stores
+  static constexpr int YST_BYTES = NACC == 1 ? 4 * 1024 : 0;
+  static constexpr int ST_FIT = (CAP - 2048 - RECV_BYTES - YST_BYTES) / STAGE;
   static constexpr int ST0 = ST_FIT < SA_FIT ? ST_FIT : SA_FIT;
   static constexpr int ST = ST0 < 8 ? ST0 : 8;
   static constexpr int X_OFF = 0;
@@ -285,7 +288,8 @@ struct Cfg {
   static constexpr int NBARS = 3 * ST + 6;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr int RECV_OFF = ((MISC_OFF + 16 + 15) / 16) * 16;
-  static constexpr int USED = 1024 + RECV_OFF + RECV_BYTES;
+  static constexpr int YST_OFF = RECV_OFF + RECV_BYTES;
+  static constexpr int USED = 1024 + YST_OFF + YST_BYTES;
   // at most one CTA per SM with 512 columns, at most two with 256: tcgen05.alloc never waits
   static constexpr int SMEM_MIN = kNarrow ? 80 * 1024 : kSmemMin;
   static constexpr int SMEM = USED < SMEM_MIN ? SMEM_MIN : USED;
@@ -304,6 +308,11 @@ struct __align__(128) PackedParams {
   unsigned int* status;
   int M, K, N;
   int tiles_t, tiles;        // activation-row tiles, total tiles
+  int y_vec;                 // y 16-byte aligned (N % 8 == 0 always): 16-byte stores allowed
+  // stream-K only: work units (tiles x stages), ready flags and partial-sum slots
+  long long units;
+  unsigned int* flags;       // [grid], zero between calls
+  float* partial;            // [grid][kSkRows][kTN] fp32
 };
 
 // The tiles a CTA takes (tile0, tile0 + tstep, ...) and its K stages [kb0, kb1): without a
@@ -320,14 +329,78 @@ struct Span {
         kb1(SPLIT > 1 ? static_cast<int>(static_cast<long long>(KS) * (krank + 1) / SPLIT) : KS) {}
 };
 
+// Rows t0 .. t0 + 31 of the warp's 32 output columns c0 + lane (lane's values in v), plus the
+// bias, rounded once to fp16.  With a staging tile (16 rows x 32 columns of the warp's own
+// shared memory) the rows leave as 16-byte stores, 16 at a time; without, one 2-byte store
+// per value.
+__device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, const uint32_t (&v)[32],
+                                          float bias, int t0, int c0, int lane) {
+  if (stage != nullptr) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      __syncwarp();  // the previous round's reads of the tile are done
+#pragma unroll
+      for (int i = 0; i < 16; ++i) stage[i * 32 + lane] = __float2half_rn(__uint_as_float(v[16 * k + i]) + bias);
+      __syncwarp();
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int piece = lane + 32 * r;  // 16 rows x 4 pieces of 8 columns
+        const int row = piece >> 2, col = (piece & 3) * 8;
+        const int t = t0 + 16 * k + row;
+        if (t < p.M && c0 + col < p.N)  // N % 8 == 0: a piece is wholly inside or outside
+          *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(t) * p.N + c0 + col) =
+              *reinterpret_cast<const uint4*>(stage + row * 32 + col);
+      }
+    }
+    return;
+  }
+  const int n = c0 + lane;
+  if (n < p.N) {
+    __half* yp = p.y + static_cast<size_t>(t0) * p.N + n;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __float2half_rn(__uint_as_float(v[j]) + bias);
+  }
+}
+
+// Stream-K (256-row tiles, one CTA per SM): the tiles' K stages form one sequence of units
+// (unit u: stage u % KS of tile u / KS) and CTA i takes units [U i / G, U (i + 1) / G) of the U
+// units, so every CTA does the same work whatever the tile count.  A tile cut between CTAs is
+// finished by the CTA holding its first stage, which reaches that piece last (it ends its
+// range); the CTAs holding later stages of it start their ranges there, write their fp32
+// partial sums to their own slot of a global workspace and raise their flag.  Only a range's
+// first piece can start inside a tile, so a CTA writes at most one partial.  The finisher adds
+// the partials in CTA order (bitwise repeatable), adds the bias, stores y and lowers the flags.
+constexpr int kSkRows = 256;                  // token rows of a stream-K tile
+constexpr size_t kSkSlotBytes = static_cast<size_t>(kSkRows) * kTN * 4;
+constexpr int kSkMinUnits = 8;                // stages per CTA below which stream-K is not used
+constexpr int kSkMaxStaged = 3;               // contributors whose rows fit the idle ring twice
+__device__ __forceinline__ long long sk_bound(long long units, long long i, long long grid) {
+  return units * i / grid;
+}
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* ptr) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_release_gpu(unsigned int* ptr, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
 // SPLIT > 1: a cluster of SPLIT CTAs shares one tile, CTA r taking K stages
 // [r KS / SPLIT, (r + 1) KS / SPLIT); ranks 1 .. SPLIT-1 push their fp32 accumulators into
 // rank 0's shared memory (st.async, counted on rank 0's recv barrier), and rank 0 adds them
 // in rank order, adds the bias and stores y.  Split launches give every cluster one tile.
-template <int BT, int SPLIT>
+template <int BT, int SPLIT, bool SK = false>
 __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
     packed_kernel(const __grid_constant__ PackedParams p) {
   using CF = Cfg<BT, SPLIT>;
+  static_assert(!SK || (BT == kSkRows && SPLIT == 1), "stream-K: 256-row tiles, no cluster split");
   constexpr int ST = CF::ST, NACC = CF::NACC;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -341,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint64_t* recv_bar = drain + 1;     // split rank 0: the other ranks' partials landed
+  uint64_t* epi_sync = drain + 1;     // stream-K: the four epilogue warps meet (same slot)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF + 4);
 
@@ -360,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
       mbar_init(&acc_empty[b], 4);
     }
     mbar_init(drain, 1);
-    mbar_init(recv_bar, 1);
+    mbar_init(recv_bar, SK ? 4 : 1);
     if (SPLIT > 1 && krank == 0u)  // the partials of ranks 1 .. SPLIT-1, one phase
       mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((SPLIT - 1) * kTN * BT * 4));
     *abort_flag = 0u;
@@ -413,6 +487,23 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
       int s = 0, issued = 0;
       uint32_t ph = 0;
       bool ok = true;
+      if constexpr (SK) {
+        const long long u0 = sk_bound(p.units, blockIdx.x, gridDim.x);
+        const long long u1 = sk_bound(p.units, blockIdx.x + 1, gridDim.x);
+        int tile = static_cast<int>(u0 / KS), kb = static_cast<int>(u0 - static_cast<long long>(tile) * KS);
+        for (long long u = u0; u < u1; ++u) {
+          const int m0 = (tile % p.tiles_t) * BT;
+          const uint32_t* src = p.packed + static_cast<size_t>(tile / p.tiles_t) * KS * kBlockWords;
+          if (!wait(&empty[s], ph ^ 1u)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + kBlockBytes));
+          tma_load_2d_hint(smem + CF::X_OFF + s * CF::X_BYTES, &p.tm_x, &full_t[s], kb * kTK, m0, pol_x);
+          bulk_load(smem + CF::B_OFF + s * kBlockBytes, src + static_cast<size_t>(kb) * kBlockWords,
+                    kBlockBytes, &full_t[s], pol_w);
+          ++issued;
+          if (++s == ST) { s = 0; ph ^= 1u; }
+          if (++kb == KS) { kb = 0; ++tile; }
+        }
+      } else
       for (int tile = tile0; ok && tile < p.tiles; tile += tstep) {
         const int m0 = (tile % p.tiles_t) * BT;
         const int t = tile / p.tiles_t;
@@ -447,6 +538,39 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
       int s = 0, li = 0;
       uint32_t ph = 0;
       bool ok = true, any = false;
+      if constexpr (SK) {  // one accumulator round per piece of a tile in the CTA's range
+        const long long u0 = sk_bound(p.units, blockIdx.x, gridDim.x);
+        const long long u1 = sk_bound(p.units, blockIdx.x + 1, gridDim.x);
+        for (long long u = u0; ok && u < u1; ++li) {
+          const int tile = static_cast<int>(u / KS);
+          const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * KS);
+          const int kb1 = u1 - u < KS - kb0 ? kb0 + static_cast<int>(u1 - u) : KS;
+          u += kb1 - kb0;
+          const int b = li % NACC;
+          if (!wait(&acc_empty[b], static_cast<uint32_t>(((li / NACC) & 1) ^ 1))) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(b * BT);
+          for (int kb = kb0; kb < kb1; kb += 2) {
+            const int n2 = kb1 - kb < 2 ? kb1 - kb : 2;
+            const int sl = s + n2 - 1 < ST ? s + n2 - 1 : s + n2 - 1 - ST;
+            const uint32_t phl = s + n2 - 1 < ST ? ph : ph ^ 1u;
+            if (!wait(&full_a[sl], phl)) { ok = false; break; }
+            tc_fence_after();
+            for (int i = 0; i < n2; ++i) {
+              const uint32_t a = tmem_base + CF::A_COL0 + static_cast<uint32_t>(s * 32);
+              const uint64_t bdesc = sw128_kmajor_desc(sbase + CF::X_OFF + s * CF::X_BYTES);
+#pragma unroll
+              for (int ks = 0; ks < kTK / 16; ++ks)  // K += 16: A 8 TMEM columns, B 32 bytes
+                mma_ts(d, a + 8u * ks, bdesc + 2u * ks, idesc, (kb + i > kb0 || ks > 0) ? 1u : 0u);
+              mma_commit(&empty[s]);
+              if (++s == ST) { s = 0; ph ^= 1u; }
+            }
+            any = true;
+          }
+          if (!ok) break;
+          mma_commit(&acc_full[b]);
+        }
+      } else
       for (int tile = tile0; ok && tile < p.tiles; tile += tstep, ++li) {
         const int b = li % NACC;
         if (!wait(&acc_empty[b], static_cast<uint32_t>(((li / NACC) & 1) ^ 1))) { ok = false; break; }
@@ -495,7 +619,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
     const int c = 32 * q + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
     const int my_tiles = tile0 < p.tiles ? (p.tiles - 1 - tile0) / tstep + 1 : 0;
-    const long long total = static_cast<long long>(my_tiles) * (kb1 - kb0);  // the CTA's stages
+    const long long total =  // the CTA's stages
+        SK ? sk_bound(p.units, blockIdx.x + 1, gridDim.x) - sk_bound(p.units, blockIdx.x, gridDim.x)
+           : static_cast<long long>(my_tiles) * (kb1 - kb0);
     constexpr int kStep = CF::kDqPairs ? 2 : 1;
     auto convert = [&](const uint4& w4, uint32_t meta, uint32_t (&v)[16]) {
       const uint32_t zz = kMagic | ((meta >> 16) * 0x00010001u);  // (1024 + z) in both halves
@@ -560,7 +686,144 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
     const int q = warp & 3;              // TMEM lanes 32 q .. 32 q + 31
     const int nl = 32 * q + lane;        // output column inside the tile
     float* recv = reinterpret_cast<float*>(smem + CF::RECV_OFF);
+    __half* ystage = (CF::YST_BYTES > 0 && p.y_vec != 0)
+                         ? reinterpret_cast<__half*>(smem + CF::YST_OFF) + q * 512 : nullptr;
     int li = 0;
+    if constexpr (SK) {
+      const int bid = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+      const long long u0 = sk_bound(p.units, bid, G), u1 = sk_bound(p.units, bid + 1, G);
+      volatile uint32_t* sk_ok = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF + 8);
+      const bool leader = warp == 2 + kDQ && lane == 0;
+      uint32_t mph = 0;
+      // the four epilogue warps meet (bounded; arrival releases each warp's earlier stores)
+      auto meet = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_sync);
+        const bool met = wait(epi_sync, mph);
+        mph ^= 1u;
+        return met;
+      };
+      for (long long u = u0; u < u1; ++li) {
+        const int tile = static_cast<int>(u / KS);
+        const int kb0 = static_cast<int>(u - static_cast<long long>(tile) * KS);
+        const int kb1 = u1 - u < KS - kb0 ? kb0 + static_cast<int>(u1 - u) : KS;
+        u += kb1 - kb0;
+        const int b = li % NACC;
+        const int m0 = (tile % p.tiles_t) * BT;
+        const int n = (tile / p.tiles_t) * kTN + nl;
+        if (!wait(&acc_full[b], static_cast<uint32_t>((li / NACC) & 1))) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT);
+        if (kb0 != 0) {
+          // a later piece of the tile (the range's first): partial sums to this CTA's slot,
+          // [row][column] so that each warp store covers 128 contiguous bytes, then the flag
+          float* slot = p.partial + static_cast<size_t>(bid) * (kSkRows * kTN);
+#pragma unroll 1
+          for (int cc = 0; cc < BT / 32; ++cc) {
+            uint32_t v[32];
+            tmem_ld32_nowait(taddr + 32 * cc, v);
+            tmem_wait_ld(v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) __stcg(slot + static_cast<size_t>(32 * cc + j) * kTN + nl, __uint_as_float(v[j]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[b]);
+          const bool met = meet();
+          if (met && leader) {
+            __threadfence();
+            st_release_gpu(p.flags + bid, 1u);
+          }
+          if (!met) break;
+          continue;
+        }
+        // the tile's first piece: add the partials of the CTAs whose ranges start inside it
+        const long long tile_end = static_cast<long long>(tile + 1) * KS;
+        int c1 = bid + 1;
+        while (c1 < G && sk_bound(p.units, c1, G) < tile_end) ++c1;
+        if (leader) {
+          uint32_t ok = 1u;
+          for (int c = bid + 1; ok != 0u && c < c1; ++c) {
+            if (ld_acquire_gpu(p.flags + c) != 0u) continue;
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(p.flags + c) == 0u) {
+              if (*abort_flag != 0u || globaltimer_ns() - t0 > kWaitLimitNs) {
+                atomicOr(p.status, kStatusPackedTimeout);
+                *abort_flag = 1u;
+                ok = 0u;
+                break;
+              }
+            }
+          }
+          *sk_ok = ok;
+        }
+        if (!meet()) break;
+        const bool have = *sk_ok != 0u;
+        const int nc = c1 - bid - 1;  // contributors
+        // This piece ends the CTA's range: its MMAs are complete, so the ring's shared memory
+        // is idle.  The contributors' rows of each 32-row chunk (nc x 16 KB, [row][column])
+        // come in there by cp.async, double-buffered a chunk ahead, and are added from
+        // shared memory, so no y store waits behind a global load.
+        const bool staged = have && nc <= kSkMaxStaged;
+        const int et = threadIdx.x - (2 + kDQ) * 32;  // 0 .. 127
+        auto fetch = [&](int cc) {
+          float* buf = reinterpret_cast<float*>(smem) + (cc & 1) * (kSkMaxStaged * 32 * kTN);
+          for (int c = 0; c < nc; ++c) {
+            const float* src = p.partial + static_cast<size_t>(bid + 1 + c) * (kSkRows * kTN) +
+                               static_cast<size_t>(32 * cc) * kTN;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {  // 16 KB: 1024 pieces of 16 bytes over 128 threads
+              const int i = et + 128 * k;
+              cp_async16(buf + c * (32 * kTN) + 4 * i, src + 4 * i);
+            }
+          }
+          cp_async_commit();
+        };
+        if (staged) fetch(0);
+        const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+        uint32_t va[32], vb[32];
+        tmem_ld32_nowait(taddr, va);
+        tmem_wait_ld(va);
+        bool chunks_met = true;
+#pragma unroll
+        for (int cc = 0; cc < BT / 32; ++cc) {
+          uint32_t (&cur)[32] = (cc & 1) ? vb : va;
+          uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
+          if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
+          if (staged) {
+            cp_async_wait_all();        // this thread's pieces of chunk cc landed
+            if (chunks_met) chunks_met = meet();  // all pieces of chunk cc landed; chunk cc - 1 read
+            if (cc + 1 < BT / 32) fetch(cc + 1);
+            const float* buf = reinterpret_cast<const float*>(smem) + (cc & 1) * (kSkMaxStaged * 32 * kTN);
+#pragma unroll 1
+            for (int c = 0; c < nc; ++c) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                cur[j] = __float_as_uint(__uint_as_float(cur[j]) + buf[c * (32 * kTN) + j * kTN + nl]);
+            }
+          } else if (have) {
+#pragma unroll 1
+            for (int c = bid + 1; c < c1; ++c) {
+              const float* slot = p.partial + static_cast<size_t>(c) * (kSkRows * kTN);
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                cur[j] = __float_as_uint(__uint_as_float(cur[j]) +
+                                         __ldcg(slot + static_cast<size_t>(32 * cc + j) * kTN + nl));
+            }
+          }
+          store_y32(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
+          if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
+        }
+        if (!chunks_met) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[b]);
+        const bool met = meet();  // every epilogue thread has read the partials: lower the flags
+        if (met && have && leader)
+          for (int c = bid + 1; c < c1; ++c) p.flags[c] = 0u;
+        if (!met) break;
+      }
+    } else
     for (int tile = tile0; tile < p.tiles; tile += tstep, ++li) {
       const int b = li % NACC;
       const int m0 = (tile % p.tiles_t) * BT;
@@ -599,13 +862,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
               cur[j + 3] = __float_as_uint(__uint_as_float(cur[j + 3]) + q4.w);
             }
           }
-          const int t0 = m0 + 32 * cc;
-          if (n < p.N) {
-            __half* yp = p.y + static_cast<size_t>(t0) * p.N + n;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __float2half_rn(__uint_as_float(cur[j]) + bias);
-          }
+          store_y32(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
         };
         if constexpr (CF::kNarrow) {  // one or two chunks: no prefetch (register budget)
 #pragma unroll 1
@@ -1005,6 +1262,57 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
   return cudaGetLastError();
 }
 
+// Stream-K launch (256-row tiles): one CTA per SM, at least kSkMinUnits stages each.
+size_t sk_flag_bytes(int sms) { return (static_cast<size_t>(sms) * 4 + 255) / 256 * 256; }
+
+cudaError_t launch_sk(const PackedParams& base, const GemmProblem& p, void* workspace, int sms) {
+  using CF = Cfg<kSkRows, 1>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(packed_kernel<kSkRows, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    CF::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  PackedParams pp = base;
+  const char* why = nullptr;
+  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, kSkRows,
+                    CU_TENSOR_MAP_SWIZZLE_128B, &why))
+    return cudaErrorInvalidValue;
+  pp.tiles_t = (p.M + kSkRows - 1) / kSkRows;
+  const long long tiles = static_cast<long long>(pp.tiles_t) * ((p.N + kTN - 1) / kTN);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  pp.tiles = static_cast<int>(tiles);
+  pp.units = tiles * (p.K / kTK);
+  long long grid = pp.units / kSkMinUnits;
+  if (grid > sms) grid = sms;
+  if (grid < 1) grid = 1;
+  pp.flags = static_cast<unsigned int*>(workspace);
+  pp.partial = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + sk_flag_bytes(sms));
+  packed_kernel<kSkRows, 1, true><<<static_cast<unsigned>(grid), kThreads, CF::SMEM, p.stream>>>(pp);
+  return cudaGetLastError();
+}
+
+// Whether a launch with M > 128 rows takes the stream-K kernel, by estimated time in stage
+// periods: the persistent launch needs rounds x K/64 of them (x 0.85 for the pair kernel, its
+// measured time per stage against the single-CTA kernel's on the 7B linears at M = 2048);
+// stream-K needs ceil(units / SMs) plus kSkOverheadStages (partial sums, the finishers' tails:
+// about 16 us, 37 stage periods, on GB300 at 512 x 4096 x 11008, where it ran 47.7 against
+// 50.2 us; 45.5 against 64.0 at 512 x 11008 x 4096; slower at M = 2048 on both 7B shapes).
+constexpr int kSkOverheadStages = 40;
+bool use_stream_k(int M, int K, int N, int sms, bool pair) {
+  const long long KS = K / kTK;
+  const long long NT = (N + kTN - 1) / kTN;
+  const long long tiles = static_cast<long long>((M + kSkRows - 1) / kSkRows) * NT;
+  const long long units = tiles * KS;
+  if (units < static_cast<long long>(sms) * kSkMinUnits) return false;
+  const long long work = pair ? tiles / 2 : tiles;   // pair tiles span two column tiles
+  const long long slots = pair ? sms / 2 : sms;
+  const double persistent = static_cast<double>((work + slots - 1) / slots * KS) * (pair ? 0.85 : 1.0);
+  const double stream_k = static_cast<double>((units + sms - 1) / sms + kSkOverheadStages);
+  return stream_k < persistent;
+}
+
 // Token tile and K split of a launch with M <= 128 rows: the narrowest tile holding M rows
 // (32, 64 or 128), and the largest split (2 or 4 for 32 rows, 2 for 64 and 128) that keeps
 // every CTA resident in one wave (two CTAs per SM below 128-row tiles) with at least four
@@ -1050,7 +1358,11 @@ cudaError_t launch_repack(const uint32_t* qw, const uint32_t* qz, const __half* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_packed(const GemmProblem& p, const void* packed) {
+size_t packed_workspace_bytes(int sms) {
+  return sk_flag_bytes(sms) + static_cast<size_t>(sms) * kSkSlotBytes;
+}
+
+cudaError_t launch_packed(const GemmProblem& p, const void* packed, void* workspace, size_t workspace_bytes) {
   PackedParams pp{};
   pp.packed = static_cast<const uint32_t*>(packed);
   pp.bias = p.bias;
@@ -1058,6 +1370,7 @@ cudaError_t launch_packed(const GemmProblem& p, const void* packed) {
   cudaError_t e = status_word_ptr(&pp.status);
   if (e != cudaSuccess) return e;
   pp.M = p.M; pp.K = p.K; pp.N = p.N;
+  pp.y_vec = aligned(p.y, 16) ? 1 : 0;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1071,7 +1384,11 @@ cudaError_t launch_packed(const GemmProblem& p, const void* packed) {
   // under the power cap the pair kernel ran 1508 against 1460 TFLOP/s on the 70B linears at
   // M = 4096 (it moves half the activations per SM, so it clocks higher at the same power);
   // at K = 4096 the single-CTA kernel was ahead (1374 against 1343 on the 7B linears).
-  if (p.K >= kPairMinK && ((p.N + kTN - 1) / kTN) % 2 == 0) return launch_pair(pp, p);
+  const bool pair = p.K >= kPairMinK && ((p.N + kTN - 1) / kTN) % 2 == 0;
+  if (workspace != nullptr && workspace_bytes >= packed_workspace_bytes(sms) &&
+      use_stream_k(p.M, p.K, p.N, sms, pair))
+    return launch_sk(pp, p, workspace, sms);
+  if (pair) return launch_pair(pp, p);
   return launch_bt<256, 1>(pp, p);
 }
 
