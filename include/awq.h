@@ -347,6 +347,31 @@ awq_status_t awq_gemm_packed_ws(const void* x_f16, const void* packed, const voi
                                 int64_t M, int64_t K, int64_t N, int64_t group_size, void* y_f16,
                                 void* workspace, size_t workspace_bytes, awq_stream_t stream);
 
+/*
+ * awq_gemm_packed_noalloc: awq_gemm_packed_ws without a caller workspace.  No page has a
+ * counterpart: it is a convenience of this library.  It works in scratch memory the library
+ * reserves on each device when it is loaded, one fixed 20 MiB array (the workspace of a device
+ * with up to 159 SMs; GB300 has 152).  On a device that would need more it returns
+ * AWQ_ERR_UNSUPPORTED_DEVICE and launches nothing.
+ *
+ * It is meant for callers that cannot give the library device memory at the call site: a
+ * host application whose device memory is all handed to its own pool before the first call,
+ * or code behind an interface that passes only the layer's tensors, so that neither an
+ * allocation inside the library nor an extra buffer argument is possible.
+ *
+ * It allocates nothing.  The first call on a device looks up the array's address (once per
+ * device, with that device current); make that first call before any stream capture that is
+ * to contain it.  Every call then clears the array's flag area with one asynchronous memset
+ * on `stream` and launches what awq_gemm_packed_ws would launch with a workspace of its own,
+ * with the same results.  All calls on one device share the array: calls that overlap in time
+ * (on different streams, or from host threads without ordering between them) race on it and
+ * may produce wrong results; order them on one stream.  Arguments, requirements and errors
+ * otherwise as awq_gemm_packed.
+ */
+awq_status_t awq_gemm_packed_noalloc(const void* x_f16, const void* packed, const void* bias_f16,
+                                     int64_t M, int64_t K, int64_t N, int64_t group_size,
+                                     void* y_f16, awq_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the library's device status word on the
  * current device.  Returns AWQ_ERR_TIMEOUT if a kernel gave up a bounded wait since the
  * last check (its output is then unspecified), AWQ_OK otherwise. */

@@ -261,9 +261,15 @@ def test_packed_layout_argument_checks_are_host_side(lib):
     assert w(A, B, None, 0, 256, 64, 128, B, A, 1 << 20, None) == 0         # M == 0: no launch
     assert w(None, B, None, 4, 256, 64, 128, B, A, 1 << 20, None) == INVALID
     assert lib.awq_gemm_packed_workspace_size(None) == INVALID
+    z = lib.awq_gemm_packed_noalloc
+    # (x, packed, bias, M, K, N, G, y, stream): the packed linear's checks, before any scratch use
+    assert z(A, B, None, 4, 96, 64, 32, B, None) == SHAPE
+    assert z(P(0x100002), B, None, 4, 256, 64, 128, B, None) == MISALIGNED
+    assert z(A, B, None, 0, 256, 64, 128, B, None) == 0                   # M == 0: nothing to do
     if not torch.cuda.is_available():
         assert g(A, B, None, 4, 256, 64, 128, B, None) == DEVICE
         assert r(A, A, A, 256, 64, 128, B, None) == DEVICE
         assert w(A, B, None, 4, 256, 64, 128, B, A, 1 << 20, None) == DEVICE
         assert w(A, B, None, 4, 256, 64, 128, B, None, 0, None) == DEVICE    # no workspace: plain plan
         assert lib.awq_gemm_packed_workspace_size(ctypes.byref(n)) == DEVICE
+        assert z(A, B, None, 4, 256, 64, 128, B, None) == DEVICE

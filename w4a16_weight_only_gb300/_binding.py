@@ -48,6 +48,7 @@ SIGNATURES = {
     "awq_gemm_packed": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "awq_gemm_packed_workspace_size": (_i32, [ctypes.POINTER(ctypes.c_size_t)]),
     "awq_gemm_packed_ws": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, ctypes.c_size_t, _vp]),
+    "awq_gemm_packed_noalloc": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
 }
 GEMM_STATIC_WEIGHTS = 1
 
@@ -512,4 +513,28 @@ def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None
             raise ValueError("workspace must be a contiguous uint8 tensor on x's device")
         _check(lib.awq_gemm_packed_ws(_ptr(x2), _ptr(packed), _ptr(bias), M, K, N, group_size, _ptr(out),
                                       workspace.data_ptr(), workspace.numel(), sh))
+    return out.reshape(*lead, N)
+
+
+def awq_gemm_packed_noalloc(x, packed, bias, K, N, group_size=128, out=None, stream=None):
+    """awq_gemm_packed through the library's awq_gemm_packed_noalloc: the stream-K workspace is
+    the library's fixed device scratch, so the C call allocates nothing (pass ``out`` to keep
+    this wrapper from allocating y).  Calls that overlap in time share that scratch and race."""
+    lib = load_library()
+    lead = x.shape[:-1]
+    if x.shape[-1] != K:
+        raise ValueError(f"x must be [..., {K}], got {tuple(x.shape)}")
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    dev = _cuda_index(x, "x")
+    _need(x2, "x", torch.float16, (M, K), dev)
+    _need(packed, "packed", torch.int32, (awq_repack_size(K, N, group_size) // 4,), dev)
+    if bias is not None:
+        _need(bias, "bias", torch.float16, (N,), dev)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    else:
+        _need(out, "out", torch.float16, (M, N), dev)
+    _check(lib.awq_gemm_packed_noalloc(_ptr(x2), _ptr(packed), _ptr(bias), M, K, N, group_size, _ptr(out),
+                                       _stream(stream)))
     return out.reshape(*lead, N)

@@ -463,9 +463,12 @@ awq_status_t awq_repack(const int32_t* qweight, const int32_t* qzeros, const voi
   return ok();
 }
 
-static awq_status_t gemm_packed(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
-                                int64_t K, int64_t N, int64_t group_size, void* y_f16, void* workspace,
-                                size_t workspace_bytes, awq_stream_t stream) {
+// Checks of the packed linear's arguments; fills *p, and *launch = false when there is nothing
+// to compute (M == 0 or N == 0).
+static awq_status_t packed_problem(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
+                                   int64_t K, int64_t N, int64_t group_size, void* y_f16,
+                                   awq_stream_t stream, awq::GemmProblem* p, bool* launch) {
+  *launch = false;
   if (M < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "M must be >= 0 (got %lld)", (long long)M);
   int G = 0;
   awq_status_t st = check_weight_shape(K, N, group_size, &G);
@@ -483,15 +486,25 @@ static awq_status_t gemm_packed(const void* x_f16, const void* packed, const voi
     return fail(AWQ_ERR_MISALIGNED, "y and bias must be 2-byte aligned");
   st = check_device();
   if (st != AWQ_OK) return st;
+  p->x = static_cast<const __half*>(x_f16);
+  p->bias = static_cast<const __half*>(bias_f16);
+  p->y = static_cast<__half*>(y_f16);
+  p->M = static_cast<int>(M);
+  p->K = static_cast<int>(K);
+  p->N = static_cast<int>(N);
+  p->G = G;
+  p->stream = reinterpret_cast<cudaStream_t>(stream);
+  *launch = true;
+  return ok();
+}
+
+static awq_status_t gemm_packed(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
+                                int64_t K, int64_t N, int64_t group_size, void* y_f16, void* workspace,
+                                size_t workspace_bytes, awq_stream_t stream) {
   awq::GemmProblem p{};
-  p.x = static_cast<const __half*>(x_f16);
-  p.bias = static_cast<const __half*>(bias_f16);
-  p.y = static_cast<__half*>(y_f16);
-  p.M = static_cast<int>(M);
-  p.K = static_cast<int>(K);
-  p.N = static_cast<int>(N);
-  p.G = G;
-  p.stream = reinterpret_cast<cudaStream_t>(stream);
+  bool launch = false;
+  const awq_status_t st = packed_problem(x_f16, packed, bias_f16, M, K, N, group_size, y_f16, stream, &p, &launch);
+  if (st != AWQ_OK || !launch) return st;
   const cudaError_t e = awq::launch_packed(p, packed, workspace, workspace_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_packed launch");
   return ok();
@@ -512,6 +525,33 @@ awq_status_t awq_gemm_packed_workspace_size(size_t* bytes) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "reading the SM count");
   *bytes = awq::packed_workspace_bytes(sms);
+  return ok();
+}
+
+awq_status_t awq_gemm_packed_noalloc(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
+                                     int64_t K, int64_t N, int64_t group_size, void* y_f16,
+                                     awq_stream_t stream) {
+  awq::GemmProblem p{};
+  bool launch = false;
+  awq_status_t st = packed_problem(x_f16, packed, bias_f16, M, K, N, group_size, y_f16, stream, &p, &launch);
+  if (st != AWQ_OK || !launch) return st;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the SM count");
+  const size_t need = awq::packed_workspace_bytes(sms);
+  if (need > awq::packed_static_scratch_bytes())
+    return fail(AWQ_ERR_UNSUPPORTED_DEVICE,
+                "this device's %d SMs need %zu bytes of scratch, more than the %zu-byte static array", sms,
+                need, awq::packed_static_scratch_bytes());
+  void* scratch = nullptr;
+  e = awq::packed_static_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "locating the static scratch");
+  // the ready flags start every call lowered (a call that gave up a wait may leave some raised)
+  e = cudaMemsetAsync(scratch, 0, awq::packed_workspace_flag_bytes(sms), p.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch flags");
+  e = awq::launch_packed(p, packed, scratch, need);
+  if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_packed_noalloc launch");
   return ok();
 }
 

@@ -96,6 +96,11 @@ cudaError_t launch_repack(const uint32_t* qw, const uint32_t* qz, const __half* 
 // With a workspace of at least packed_workspace_bytes(SM count) bytes (flags zero), launches
 // with M > 128 whose tiles fill the SMs poorly run the stream-K kernel.
 size_t packed_workspace_bytes(int sms);
+size_t packed_workspace_flag_bytes(int sms);  // the leading flag area of that workspace
+// The library's fixed device scratch (awq_gemm_packed_noalloc): its size, and its address on
+// the current device (looked up once per device).
+size_t packed_static_scratch_bytes();
+cudaError_t packed_static_scratch(void** ptr);
 cudaError_t launch_packed(const GemmProblem& p, const void* packed, void* workspace = nullptr,
                           size_t workspace_bytes = 0);
 

@@ -1358,8 +1358,38 @@ cudaError_t launch_repack(const uint32_t* qw, const uint32_t* qz, const __half* 
   return cudaGetLastError();
 }
 
+size_t packed_workspace_flag_bytes(int sms) { return sk_flag_bytes(sms); }
+
 size_t packed_workspace_bytes(int sms) {
   return sk_flag_bytes(sms) + static_cast<size_t>(sms) * kSkSlotBytes;
+}
+
+// Fixed device scratch for awq_gemm_packed_noalloc: the stream-K workspace of a device with up
+// to 159 SMs (768 bytes of flags + 159 x 128 KB), reserved with the module, so that entry point
+// needs no allocation.  One array per device context, shared by every call on that device.
+namespace {
+constexpr size_t kStaticScratchBytes = 20u << 20;
+static __device__ __align__(256) unsigned char g_packed_scratch[kStaticScratchBytes];
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices];
+cudaError_t g_scratch_err[kMaxDevices];
+std::once_flag g_scratch_once[kMaxDevices];
+}  // namespace
+
+size_t packed_static_scratch_bytes() { return kStaticScratchBytes; }
+
+cudaError_t packed_static_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  // the symbol's address on this device, looked up once with the device current
+  std::call_once(g_scratch_once[dev], [dev] {
+    g_scratch_err[dev] = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_packed_scratch);
+  });
+  if (g_scratch_err[dev] != cudaSuccess) return g_scratch_err[dev];
+  *ptr = g_scratch_ptr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_packed(const GemmProblem& p, const void* packed, void* workspace, size_t workspace_bytes) {
