@@ -99,12 +99,12 @@ def step_flop(names):
 # `python bench.py --steps 20 --warmup 3 --no-cpu-baseline --decode-only` summarised in
 # profiles/decode_tma_70b_m1_bench_launches.md; valid only for the kernel source it was
 # measured on (SHA-256 of the files below), else reported as null.
-TRAFFIC_BYTES_PER_LAUNCH = 93_162_129
+TRAFFIC_BYTES_PER_LAUNCH = 93_193_924
 TRAFFIC_SOURCES = {
     "w4a16_weight_only_gb300/csrc/awq_decode_tma.cu":
-        "0170e47375a8599b14fee3621e4126f3f3c04d86018a35633b14a3a4bea01665",
+        "b01453c4e416019eed09b63b331e35f7da7f3a4ec5ddc4950faa12ed7a5b4818",
     "w4a16_weight_only_gb300/csrc/awq_ptx.cuh":
-        "166c2c9cd2d4a880677df7bd3dc634de58dadf2fcdc9ba2bdcf045010269d495",
+        "7488ac9d3e1525b7a303d4e435be38b50cdcbf4b04c725918e9c8ee96f8b2e02",
 }
 
 
@@ -716,10 +716,10 @@ def run_case(args, local):
     t = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "qweight", "qzeros", "scales")}
     b = torch.from_numpy(d["bias"]).cuda() if d["bias"] is not None else None
     y = torch.empty((d["M"], d["N"]), dtype=torch.float16, device="cuda")
-    if args.packed:  # the tile-packed layout: one repack, then awq_gemm_packed calls
+    if args.packed:  # the tile-packed layout: one repack, then the calls AwqLinear(packed=True) makes
         pk = awq.awq_repack(t["qweight"], t["qzeros"], t["scales"], d["group_size"])
         for i in range(args.warmup + args.steps):
-            awq.awq_gemm_packed(t["x"], pk, b, d["K"], d["N"], d["group_size"], out=y)
+            awq.awq_gemm_packed(t["x"], pk, b, d["K"], d["N"], d["group_size"], out=y, workspace="auto")
     else:
         for i in range(args.warmup + args.steps):
             gemm(t["x"], t["qweight"], t["qzeros"], t["scales"], b, group_size=d["group_size"],
@@ -1069,7 +1069,7 @@ def main(argv=None):
                          "w8_m<M>_<K>x<N> for 8-bit codes)")
     ap.add_argument("--path", default="auto", choices=["auto", "decode", "prefill", "generic"])
     ap.add_argument("--packed", action="store_true",
-                    help="profiling mode: repack once, then call awq_gemm_packed")
+                    help="profiling mode: repack once, then call awq_gemm_packed with the stream's workspace")
     ap.add_argument("--sweep", action="store_true",
                     help="per-workload table (one JSON line per workload), not the bench line")
     ap.add_argument("--cpu-oracle", action="store_true",
