@@ -927,7 +927,8 @@ struct PairCfg {
   static constexpr int NBARS = 3 * ST + 3;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr int SIG_OFF = MISC_OFF + 16;         // CTA 0: targets of CTA 1's signals
-  static constexpr int USED = 1024 + SIG_OFF + 4 * kDQ;
+  static constexpr int YST_OFF = ((SIG_OFF + 4 * kDQ + 15) / 16) * 16;  // y staging, 1 KB a warp
+  static constexpr int USED = 1024 + YST_OFF + 4 * 1024;
   static constexpr int SMEM = USED < kSmemMin ? kSmemMin : USED;
   static constexpr uint32_t A_COL0 = BT;
   static_assert(ST >= 3 && SMEM <= kSmemCap, "resources");
@@ -1127,6 +1128,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
     // ------------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int nl = 32 * q + lane;
+    __half* ystage = p.y_vec != 0 ? reinterpret_cast<__half*>(smem + CF::YST_OFF) + q * 512 : nullptr;
     int li = 0;
     for (int tile = pair; tile < p.tiles; tile += npairs, ++li) {
       const int m0 = (tile % p.tiles_t) * BT;
@@ -1143,13 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
         uint32_t (&cur)[32] = (cc & 1) ? vb : va;
         uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
         if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
-        const int t0 = m0 + 32 * cc;
-        if (n < p.N) {
-          __half* yp = p.y + static_cast<size_t>(t0) * p.N + n;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __float2half_rn(__uint_as_float(cur[j]) + bias);
-        }
+        store_y32(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
         if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
       }
       tc_fence_before();
