@@ -360,7 +360,8 @@ awq_status_t awq_gemm_packed_ws(const void* x_f16, const void* packed, const voi
  * allocation inside the library nor an extra buffer argument is possible.
  *
  * It allocates nothing.  The first call on a device looks up the array's address (once per
- * device, with that device current); make that first call before any stream capture that is
+ * device, with that device current, kept for the life of the process: do not use this entry
+ * point after resetting the device); make that first call before any stream capture that is
  * to contain it.  Every call then clears the array's flag area with one asynchronous memset
  * on `stream` and launches what awq_gemm_packed_ws would launch with a workspace of its own,
  * with the same results.  All calls on one device share the array: calls that overlap in time
