@@ -176,6 +176,35 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[32]) {
                : "memory");
 }
 
+// tcgen05.ld of 16 TMEM lanes x 32 columns without the wait, in the MMA-fragment layout:
+// thread t gets, for each 8-column group k, registers 4k .. 4k + 3 = (lane t/4, column
+// 2(t%4)), (lane t/4, 2(t%4) + 1), (lane t/4 + 8, 2(t%4)), (lane t/4 + 8, 2(t%4) + 1).
+__device__ __forceinline__ void tmem_ld16x256_nowait(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+// Four 8x8 b16 matrices into shared memory, transposed: register m of every thread holds its
+// fragment of matrix m (thread t: row t/4, elements 2(t%4), +1); lanes 8m .. 8m + 7 give the
+// addresses of the rows of the stored (transposed) matrix m.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, const uint32_t (&m)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr),
+               "r"(m[0]), "r"(m[1]), "r"(m[2]), "r"(m[3])
+               : "memory");
+}
+__device__ __forceinline__ uint4 lds128_u(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Pair mode (tcgen05 cta_group::2): the MMA spans the two CTAs of a cluster.
 __device__ __forceinline__ void mma_ts_pair(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
@@ -360,6 +389,48 @@ __device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, 
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __float2half_rn(__uint_as_float(v[j]) + bias);
+  }
+}
+
+// Rows t_base .. t_base + 31 of the warp's 32 output columns c0 .. c0 + 31 from two 16x256b
+// fragment loads (f[0..15]: the quadrant's lanes 0-15, f[16..31]: lanes 16-31), plus the bias
+// (ba[h]: column c0 + 16 h + t/4, bb[h]: that + 8), rounded once to fp16.  Sixteen rows at a
+// time go into the warp's staging tile (16 rows x 64 bytes) transposed by stmatrix, each
+// 16-byte chunk of a row XOR-swizzled by (row / 2) % 4 so the eight rows of a matrix fall in
+// distinct banks, and leave as 16-byte stores.
+__device__ __forceinline__ void store_y32_frag(const PackedParams& p, __half* stage, const uint32_t (&f)[32],
+                                               const float (&ba)[2], const float (&bb)[2], int t_base,
+                                               int c0, int lane) {
+  const uint32_t sbase = smem_u32(stage);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {  // tokens 16 r .. 16 r + 15: 8-token groups 2 r, 2 r + 1
+    __syncwarp();                // the previous round's reads of the tile are done
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t m[4];
+#pragma unroll
+      for (int gg = 0; gg < 2; ++gg) {
+        const int g = 2 * r + gg;
+        m[2 * gg] = pack_half2(__uint_as_float(f[16 * h + 4 * g]) + ba[h], __uint_as_float(f[16 * h + 4 * g + 1]) + ba[h]);
+        m[2 * gg + 1] = pack_half2(__uint_as_float(f[16 * h + 4 * g + 2]) + bb[h], __uint_as_float(f[16 * h + 4 * g + 3]) + bb[h]);
+      }
+      // matrix mm = (token group gg = mm / 2, column block mm % 2); lane 8 mm + i: its row i
+      const int mm = lane >> 3, i = lane & 7;
+      const int row = 8 * (mm >> 1) + i;
+      const int chunk = 2 * h + (mm & 1);  // columns 8 chunk .. 8 chunk + 7 of the warp's 32
+      stmatrix_x4_trans(sbase + static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) * 16)), m);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int piece = lane + 32 * k;  // 16 rows x 4 chunks
+      const int row = piece >> 2, chunk = piece & 3;
+      const int t = t_base + 16 * r + row;
+      const int col = c0 + 8 * chunk;
+      if (t < p.M && col < p.N)  // N % 8 == 0: a chunk is wholly inside or outside
+        *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(t) * p.N + col) =
+            lds128_u(sbase + static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) * 16)));
+    }
   }
 }
 
@@ -872,6 +943,32 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
             tmem_wait_ld(v);
             finish(cc, v);
           }
+        } else if (SPLIT == 1 && ystage != nullptr) {
+          // one accumulator: MMA-fragment loads, stmatrix into the staging tile, 16-byte stores
+          const int c0 = n - lane;
+          float ba[2], bb[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int na = c0 + 16 * h + (lane >> 2), nb = na + 8;
+            ba[h] = (p.bias != nullptr && na < p.N) ? __half2float(p.bias[na]) : 0.f;
+            bb[h] = (p.bias != nullptr && nb < p.N) ? __half2float(p.bias[nb]) : 0.f;
+          }
+          const uint32_t fbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT);
+          uint32_t va[32], vb[32];
+          tmem_ld16x256_nowait(fbase, va);
+          tmem_ld16x256_nowait(fbase + (16u << 16), va + 16);
+          tmem_wait_ld(va);
+#pragma unroll
+          for (int cc = 0; cc < BT / 32; ++cc) {
+            uint32_t (&cur)[32] = (cc & 1) ? vb : va;
+            uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
+            if (cc + 1 < BT / 32) {
+              tmem_ld16x256_nowait(fbase + 32 * (cc + 1), nxt);
+              tmem_ld16x256_nowait(fbase + (16u << 16) + 32 * (cc + 1), nxt + 16);
+            }
+            store_y32_frag(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane);
+            if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
+          }
         } else {
           uint32_t va[32], vb[32];
           tmem_ld32_nowait(taddr, va);
@@ -1138,15 +1235,40 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
       uint32_t va[32], vb[32];
-      tmem_ld32_nowait(taddr, va);
-      tmem_wait_ld(va);
+      if (ystage != nullptr) {  // MMA-fragment loads, stmatrix into the staging tile, 16-byte stores
+        const int c0 = n - lane;
+        float ba[2], bb[2];
 #pragma unroll
-      for (int cc = 0; cc < BT / 32; ++cc) {
-        uint32_t (&cur)[32] = (cc & 1) ? vb : va;
-        uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
-        if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
-        store_y32(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
-        if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
+        for (int h = 0; h < 2; ++h) {
+          const int na = c0 + 16 * h + (lane >> 2), nb = na + 8;
+          ba[h] = (p.bias != nullptr && na < p.N) ? __half2float(p.bias[na]) : 0.f;
+          bb[h] = (p.bias != nullptr && nb < p.N) ? __half2float(p.bias[nb]) : 0.f;
+        }
+        tmem_ld16x256_nowait(taddr, va);
+        tmem_ld16x256_nowait(taddr + (16u << 16), va + 16);
+        tmem_wait_ld(va);
+#pragma unroll
+        for (int cc = 0; cc < BT / 32; ++cc) {
+          uint32_t (&cur)[32] = (cc & 1) ? vb : va;
+          uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
+          if (cc + 1 < BT / 32) {
+            tmem_ld16x256_nowait(taddr + 32 * (cc + 1), nxt);
+            tmem_ld16x256_nowait(taddr + (16u << 16) + 32 * (cc + 1), nxt + 16);
+          }
+          store_y32_frag(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane);
+          if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
+        }
+      } else {
+        tmem_ld32_nowait(taddr, va);
+        tmem_wait_ld(va);
+#pragma unroll
+        for (int cc = 0; cc < BT / 32; ++cc) {
+          uint32_t (&cur)[32] = (cc & 1) ? vb : va;
+          uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
+          if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
+          store_y32(p, nullptr, cur, bias, m0 + 32 * cc, n - lane, lane);
+          if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
+        }
       }
       tc_fence_before();
       __syncwarp();
