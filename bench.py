@@ -831,7 +831,7 @@ def run_sweep(args, local):
                          "cublas_fp16_dense_us": t_mm, "cublas_fp16_dense_TFLOP_s": flop / t_mm / 1e6,
                          "dequant_plus_cublas_us": t_dq + t_mm})
             del wd
-            if dt == "f16" and K % 64 == 0 and (G == -1 or G % 64 == 0):
+            if K % 64 == 0 and (G == -1 or G % 64 == 0):
                 # the tile-packed layout: the one-off repack, then awq_gemm_packed with the
                 # stream's workspace (stream-K where the plan takes it)
                 pk = awq.awq_repack(qw, qz, sc, G, stream=stream)

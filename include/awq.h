@@ -296,7 +296,7 @@ awq_path_t awq_gemm_select_path_ex(int64_t M, int64_t K, int64_t N, int64_t grou
  * 1152 uint32 words at word (t * K/64 + s) * 1152:
  *   word 512 h + 4 c + j (h < 2, c < 128, j < 4): 4-bit codes of column 128 t + c for rows
  *     64 s + 32 h + 8 j + 0..7, row offset ORDER[p] in nibble p (ORDER = {0,2,4,6,1,3,5,7});
- *   word 1024 + c: fp16 scale bits | zero << 16 of column 128 t + c, group of row 64 s;
+ *   word 1024 + c: scale bits (fp16 or bf16) | zero << 16 of column 128 t + c, group of row 64 s;
  *   columns past N: zero.
  * Requirements: those of awq_dequant plus K % 64 == 0 and group size % 64 == 0 (or -1).
  *
@@ -304,7 +304,9 @@ awq_path_t awq_gemm_select_path_ex(int64_t M, int64_t K, int64_t N, int64_t grou
  *   no device access).
  * awq_repack: writes them to packed_out (DEVICE, caller-owned, 16-byte aligned,
  *   awq_repack_size bytes); reads qweight/qzeros/scales as awq_dequant does; K / 64 <=
- *   65535.  One kernel launch, asynchronous on `stream`.  N == 0: AWQ_OK, no launch.
+ *   65535.  The scale words are copied bit for bit, so bf16 scales give the packed weights
+ *   of awq_gemm_packed_ex with AWQ_DTYPE_BF16.  One kernel launch, asynchronous on `stream`.
+ *   N == 0: AWQ_OK, no launch.
  * awq_gemm_packed: y = fp16_rne(x W (+ bias)) as awq_gemm, W read from the packed layout
  *   (x fp16 [M, K] 16-byte aligned, packed 16-byte aligned, bias fp16 [N] or NULL, y fp16
  *   [M, N]; fp32 accumulation, a fixed summation order: repeated calls are bitwise
@@ -372,6 +374,22 @@ awq_status_t awq_gemm_packed_ws(const void* x_f16, const void* packed, const voi
 awq_status_t awq_gemm_packed_noalloc(const void* x_f16, const void* packed, const void* bias_f16,
                                      int64_t M, int64_t K, int64_t N, int64_t group_size,
                                      void* y_f16, awq_stream_t stream);
+
+/*
+ * awq_gemm_packed_ex: the packed linear for either activation type.  dtype AWQ_DTYPE_F16 (x,
+ * bias, y fp16; the packed weights written from fp16 scales) or AWQ_DTYPE_BF16 (x, bias, y
+ * bf16; the packed weights written by awq_repack from bf16 scales: it copies the 16-bit scale
+ * words as they are).  bf16 dequantizes exactly as awq_dequant_bf16 does (c - z exact, one
+ * rounding of (c - z) * s to bf16; GPTQModel wiki "AWQ", "Selection and compatibility": FP16
+ * and BF16 activations) and accumulates in fp32; y is rounded once to bf16.  workspace /
+ * workspace_bytes as awq_gemm_packed_ws (NULL / 0: awq_gemm_packed's plan).  Other arguments,
+ * requirements, results and errors as awq_gemm_packed_ws; AWQ_ERR_INVALID_ARGUMENT for
+ * another dtype.
+ */
+awq_status_t awq_gemm_packed_ex(const void* x, const void* packed, const void* bias, int64_t M,
+                                int64_t K, int64_t N, int64_t group_size, void* y,
+                                awq_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                                awq_stream_t stream);
 
 /* Synchronizes `stream`, then reads and clears the library's device status word on the
  * current device.  Returns AWQ_ERR_TIMEOUT if a kernel gave up a bounded wait since the

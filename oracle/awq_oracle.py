@@ -373,14 +373,18 @@ def repack_size(K: int, N: int, group_size: int) -> int:
 def repack(qweight, qzeros, scales, group_size) -> np.ndarray:
     """Checkpoint layout -> tile-packed layout, as uint32 words (see the module docstring).
     Steps: unpack codes and zeros with the page's reader, pad the columns to whole tiles,
-    then write every block word by word."""
+    then write every block word by word.  scales: fp16 values, or their 16-bit words as a
+    uint16 array (bf16 scales: the layout carries the scale word unchanged, whatever its
+    format)."""
     K, C = qweight.shape
     N = 8 * C
     G = resolve_group_size(K, group_size)
     nbytes = repack_size(K, N, group_size)
     codes = unpack_codes(qweight)                  # [K, N]
     zeros = unpack_codes(qzeros)                   # [K/G, N]
-    sbits = np.ascontiguousarray(scales, dtype=np.float16).view(np.uint16).astype(np.uint64)
+    sc = np.asarray(scales)
+    sbits = (sc if sc.dtype == np.uint16 else np.ascontiguousarray(sc, dtype=np.float16).view(np.uint16))
+    sbits = sbits.astype(np.uint64)
     NT, KS = -(-N // PACK_TN), K // PACK_TK
     Np = NT * PACK_TN
     cp = np.zeros((K, Np), dtype=np.uint64)

@@ -162,3 +162,76 @@ def test_bf16_rejects_mixed_dtypes(awq):
     t = to_dev(d)
     with pytest.raises(TypeError):
         awq.awq_gemm(t["x"], t["qweight"], t["qzeros"], t["scales"].half(), None, group_size=128)
+
+
+# Tile-packed layout with bf16 (awq_repack copies the bf16 scale words; awq_gemm_packed_ex with
+# AWQ_DTYPE_BF16): the kernels round each dequantized weight once to bf16, so the reference is
+# the fp64 GEMM of the oracle's bf16-rounded dequant.  Shapes: narrow split tiles, the 256-row
+# kernel with ragged rows and columns, stream-K (through a workspace), the pair kernel (K = 8192).
+PACKED_BF = [(40, 1024, 512, 128, True, None), (300, 1024, 264, 64, True, None),
+             (257, 4096, 2048, 128, True, "ws"), (300, 8192, 512, 128, False, None),
+             (700, 512, 1032, -1, True, None)]
+
+
+def bf_words(a):
+    return (np.ascontiguousarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def packed_bf(awq, t, G):
+    return awq.awq_repack(t["qweight"], t["qzeros"], t["scales"], G)
+
+
+@pytest.mark.parametrize("K,N,G", [(256, 264, 64), (4096, 11008, 128), (512, 1032, -1)])
+def test_repack_bf16_scale_words(awq, K, N, G):
+    d = synth.awq_linear(9800 + K + N, 1, K, N, group_size=G, dtype="bf16")
+    pk = packed_bf(awq, to_dev(d), G)
+    torch.cuda.synchronize()
+    want = oracle.repack(d["qweight"], d["qzeros"], bf_words(d["scales"]), G)
+    assert np.array_equal(pk.cpu().numpy().view(np.uint32), want)
+
+
+@pytest.mark.parametrize("M,K,N,G,bias,ws", PACKED_BF)
+def test_gemm_packed_bf16_vs_oracle(awq, M, K, N, G, bias, ws):
+    d = synth.awq_linear(9850 + M + K, M, K, N, group_size=G, bias=bias, dtype="bf16")
+    t = to_dev(d)
+    pk = packed_bf(awq, t, G)
+    w = None
+    if ws:
+        w = torch.zeros((awq.awq_gemm_packed_workspace_size(),), dtype=torch.uint8, device="cuda")
+    y = awq.awq_gemm_packed(t["x"], pk, t["bias"], K, N, G, workspace=w)
+    torch.cuda.synchronize()
+    assert y.dtype == torch.bfloat16
+    if ws:
+        assert w[(torch.cuda.get_device_properties(0).multi_processor_count * 4 + 255) // 256 * 256:].any().item()
+    assert_close(y.float().cpu().numpy(), reference(d, True), f"packed bf16 M={M} K={K} N={N} G={G}")
+    y2 = awq.awq_gemm_packed(t["x"], pk, t["bias"], K, N, G, workspace=w)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+
+
+@pytest.mark.parametrize("M,K,N,ws", [(300, 2048, 384, None), (257, 4096, 2048, "ws"), (64, 2048, 384, None)])
+def test_gemm_packed_bf16_exact_case_bitwise(awq, M, K, N, ws):
+    # exact-arithmetic inputs: every weight (c - z) * 2^k and every partial sum is exact, so y
+    # is the oracle's value rounded once to bf16 whatever the kernel's summation order
+    d = synth.awq_linear(9900 + M + K, M, K, N, group_size=128, bias=True, x_kind="smallint",
+                         scale_kind="pow2", bias_kind="dyadic", dtype="bf16")
+    t = to_dev(d)
+    pk = packed_bf(awq, t, 128)
+    w = None if not ws else torch.zeros((awq.awq_gemm_packed_workspace_size(),), dtype=torch.uint8, device="cuda")
+    y = awq.awq_gemm_packed(t["x"], pk, t["bias"], K, N, 128, workspace=w).float().cpu().numpy()
+    want = oracle.round_to_bf16(oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128).astype(np.float32))
+    assert np.array_equal(y.view(np.uint32), want.view(np.uint32))
+
+
+def test_linear_packed_bf16(awq):
+    # AwqLinear(packed=True) with bf16 scales: calls of >= 128 rows on the packed copy, bit for
+    # bit the functional call with the stream's workspace
+    M, K, N, G = 257, 4096, 2048, 128
+    d = synth.awq_linear(9960, M, K, N, group_size=G, bias=True, dtype="bf16")
+    t = to_dev(d)
+    lin = awq.AwqLinear(t["qweight"], t["qzeros"], t["scales"], t["bias"], group_size=G, packed=True)
+    y = lin(t["x"])
+    y_ref = awq.awq_gemm_packed(t["x"], packed_bf(awq, t, G), t["bias"], K, N, G, workspace="auto")
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_ref)
+    assert_close(y.float().cpu().numpy(), reference(d, True), "AwqLinear packed bf16")

@@ -577,6 +577,23 @@ def test_packed_round_trip_is_lossless(K, N, G):
     assert np.array_equal(sc.view(np.uint16), d["scales"].view(np.uint16))
 
 
+def test_packed_scale_words_pass_through():
+    # the layout stores each scale's 16-bit word unchanged: fp16 words give the fp16 layout, and
+    # bf16 words (bf16 scales) read back bit for bit
+    K, N, G = 256, 264, 64
+    d = awq_linear(305, 1, K, N, group_size=G)
+    pk = oracle.repack(d["qweight"], d["qzeros"], d["scales"], G)
+    assert np.array_equal(oracle.repack(d["qweight"], d["qzeros"], d["scales"].view(np.uint16), G), pk)
+    db = awq_linear(306, 1, K, N, group_size=G, dtype="bf16")
+    words = (np.ascontiguousarray(db["scales"], dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((words.astype(np.uint32) << 16).view(np.float32), db["scales"].astype(np.float32))
+    pkb = oracle.repack(db["qweight"], db["qzeros"], words, G)
+    codes, zeros, sc = oracle.unpack_repacked(pkb, K, N, G)
+    assert np.array_equal(sc.view(np.uint16), words)
+    assert np.array_equal(codes, oracle.unpack_codes(db["qweight"]))
+    assert np.array_equal(zeros, oracle.unpack_codes(db["qzeros"]))
+
+
 def test_packed_padding_and_group_copies():
     # columns past N are all-zero words; every stage of a group carries the same meta row
     K, N, G = 256, 136, 128

@@ -49,6 +49,7 @@ SIGNATURES = {
     "awq_gemm_packed_workspace_size": (_i32, [ctypes.POINTER(ctypes.c_size_t)]),
     "awq_gemm_packed_ws": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, ctypes.c_size_t, _vp]),
     "awq_gemm_packed_noalloc": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "awq_gemm_packed_ex": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp, ctypes.c_size_t, _vp]),
 }
 GEMM_STATIC_WEIGHTS = 1
 
@@ -181,11 +182,11 @@ class AwqLinear:
     ``awq_gemm_any`` (fp16 or bf16 activations, 4- or 8-bit codes) with only x and out
     checked per call.
 
-    packed=True (fp16, 4-bit codes, K % 64 == 0, group size % 64 == 0) also keeps a
+    packed=True (fp16 or bf16, 4-bit codes, K % 64 == 0, group size % 64 == 0) also keeps a
     tile-packed copy of the weights, written once by awq_repack at construction (a device
     allocation of awq_repack_size bytes, about the size of the packed weights), and runs
-    calls of at least ``packed_min_rows`` rows through awq_gemm_packed; smaller calls keep
-    the checkpoint layout.
+    calls of at least ``packed_min_rows`` rows through awq_gemm_packed_ex with the stream's
+    workspace; smaller calls keep the checkpoint layout.
 
     qweight int32 [K, N/8] (4 bits) or [K, N/4] (8 bits), qzeros int32 [K/G, N/8 or N/4],
     scales fp16 or bf16 [K/G, N] (it sets the activation dtype; 8 bits: fp16), bias [N] of
@@ -230,8 +231,8 @@ class AwqLinear:
         self.packed = None
         self.packed_min_rows = int(packed_min_rows)
         if packed:
-            if bits != 4 or dt is not torch.float16:
-                raise ValueError("the tile-packed layout takes fp16 scales and 4-bit codes")
+            if bits != 4:
+                raise ValueError("the tile-packed layout takes 4-bit codes")
             self.packed = awq_repack(qweight, qzeros, scales, group_size)
         self._path = PATHS[path]
         self._tensors = (qweight, qzeros, scales, bias)
@@ -258,8 +259,9 @@ class AwqLinear:
             sh = ((stream if isinstance(stream, int) else stream.cuda_stream)
                   if stream is not None else torch.cuda.current_stream().cuda_stream)
             ws = packed_workspace(self.device, sh)
-            st = _lib.awq_gemm_packed_ws(x.data_ptr(), self.packed.data_ptr(), w[3], M, K, N,
-                                         self.group_size, out.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+            st = _lib.awq_gemm_packed_ex(x.data_ptr(), self.packed.data_ptr(), w[3], M, K, N,
+                                         self.group_size, out.data_ptr(), self._dt, ws.data_ptr(),
+                                         ws.numel(), sh)
             if st != AWQ_OK:
                 raise AwqError(st, last_error())
             return out
@@ -448,7 +450,9 @@ def awq_repack(qweight, qzeros, scales, group_size=128, out=None, stream=None):
     _need(qweight, "qweight", torch.int32, (K, C), dev)
     ng = _groups(K, group_size)
     _need(qzeros, "qzeros", torch.int32, (ng, C), dev)
-    _need(scales, "scales", torch.float16, (ng, N), dev)
+    if scales.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("scales must be float16 or bfloat16 (their 16-bit words are copied)")
+    _need(scales, "scales", scales.dtype, (ng, N), dev)
     words = awq_repack_size(K, N, group_size) // 4
     if out is None:
         out = torch.empty((words,), dtype=torch.int32, device=dev)
@@ -485,9 +489,10 @@ def packed_workspace(device, stream_handle):
 def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None, workspace=None):
     """y = x @ W (+ bias) with W in the tile-packed layout (awq_repack's output) via the
     library's awq_gemm_packed; x fp16 [..., K] (leading dims flattened), bias fp16 [N] or
-    None.  Returns fp16 [..., N].  workspace: a zero-filled uint8 device tensor of at least
-    awq_gemm_packed_workspace_size() bytes, or "auto" for the (device, stream) one: the call
-    then goes through awq_gemm_packed_ws (stream-K on shapes that fill the SMs poorly)."""
+    None.  Returns [..., N] in x's dtype.  workspace: a zero-filled uint8 device tensor of at
+    least awq_gemm_packed_workspace_size() bytes, or "auto" for the (device, stream) one: the
+    call then goes through awq_gemm_packed_ws (stream-K on shapes that fill the SMs poorly).
+    bfloat16 x (packed weights written from bfloat16 scales) goes through awq_gemm_packed_ex."""
     lib = load_library()
     lead = x.shape[:-1]
     if x.shape[-1] != K:
@@ -495,16 +500,25 @@ def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None
     x2 = x.reshape(-1, K)
     M = x2.shape[0]
     dev = _cuda_index(x, "x")
-    _need(x2, "x", torch.float16, (M, K), dev)
+    dt = x.dtype
+    if dt not in (torch.float16, torch.bfloat16):
+        raise TypeError("x must be float16 or bfloat16")
+    _need(x2, "x", dt, (M, K), dev)
     _need(packed, "packed", torch.int32, (awq_repack_size(K, N, group_size) // 4,), dev)
     if bias is not None:
-        _need(bias, "bias", torch.float16, (N,), dev)
+        _need(bias, "bias", dt, (N,), dev)
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=dev)
+        out = torch.empty((M, N), dtype=dt, device=dev)
     else:
-        _need(out, "out", torch.float16, (M, N), dev)
+        _need(out, "out", dt, (M, N), dev)
     sh = _stream(stream)
-    if workspace is None:
+    if dt is torch.bfloat16:  # awq_gemm_packed_ex (its workspace, if any, as below)
+        if isinstance(workspace, str) and workspace == "auto":
+            workspace = packed_workspace(dev, sh.value or 0)
+        ws, wsb = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel())
+        _check(lib.awq_gemm_packed_ex(_ptr(x2), _ptr(packed), _ptr(bias), M, K, N, group_size, _ptr(out),
+                                      DTYPE_BF16, ws, wsb, sh))
+    elif workspace is None:
         _check(lib.awq_gemm_packed(_ptr(x2), _ptr(packed), _ptr(bias), M, K, N, group_size, _ptr(out), sh))
     else:
         if isinstance(workspace, str) and workspace == "auto":

@@ -467,7 +467,7 @@ awq_status_t awq_repack(const int32_t* qweight, const int32_t* qzeros, const voi
 // to compute (M == 0 or N == 0).
 static awq_status_t packed_problem(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
                                    int64_t K, int64_t N, int64_t group_size, void* y_f16,
-                                   awq_stream_t stream, awq::GemmProblem* p, bool* launch) {
+                                   awq_stream_t stream, awq::GemmProblem* p, bool* launch, bool bf16 = false) {
   *launch = false;
   if (M < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "M must be >= 0 (got %lld)", (long long)M);
   int G = 0;
@@ -494,6 +494,7 @@ static awq_status_t packed_problem(const void* x_f16, const void* packed, const 
   p->N = static_cast<int>(N);
   p->G = G;
   p->stream = reinterpret_cast<cudaStream_t>(stream);
+  p->bf16 = bf16;
   *launch = true;
   return ok();
 }
@@ -552,6 +553,22 @@ awq_status_t awq_gemm_packed_noalloc(const void* x_f16, const void* packed, cons
   if (e != cudaSuccess) return cuda_fail(e, "clearing the scratch flags");
   e = awq::launch_packed(p, packed, scratch, need);
   if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_packed_noalloc launch");
+  return ok();
+}
+
+awq_status_t awq_gemm_packed_ex(const void* x, const void* packed, const void* bias, int64_t M, int64_t K,
+                                int64_t N, int64_t group_size, void* y, awq_dtype_t dtype, void* workspace,
+                                size_t workspace_bytes, awq_stream_t stream) {
+  if (dtype != AWQ_DTYPE_F16 && dtype != AWQ_DTYPE_BF16)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "dtype must be AWQ_DTYPE_F16 or AWQ_DTYPE_BF16");
+  if (workspace && !al(workspace, 256)) return fail(AWQ_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  awq::GemmProblem p{};
+  bool launch = false;
+  const awq_status_t st = packed_problem(x, packed, bias, M, K, N, group_size, y, stream, &p, &launch,
+                                         dtype == AWQ_DTYPE_BF16);
+  if (st != AWQ_OK || !launch) return st;
+  const cudaError_t e = awq::launch_packed(p, packed, workspace, workspace_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_packed_ex launch");
   return ok();
 }
 

@@ -50,6 +50,8 @@ constexpr int kThreads = (2 + kDQ + 4) * 32;
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
 constexpr unsigned int kStatusPackedTimeout = 0x4u;
 constexpr uint32_t kMagic = 0x64006400u;    // fp16 1024 in both halves
+constexpr uint32_t kMagicBF = 0x43004300u;  // bf16 128 in both halves
+constexpr uint32_t kIdescBF = (1u << 7) | (1u << 10);  // instruction descriptor: A and B bf16
 constexpr int kSmemCap = 227 * 1024;
 constexpr int kSmemMin = 120 * 1024;        // one CTA per SM: it allocates all 512 TMEM columns
 constexpr int kPairMinK = 8192;             // K from which M > 128 runs the two-CTA kernel
@@ -200,9 +202,31 @@ __device__ __forceinline__ uint4 lds128_u(uint32_t a) {
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
   return v;
 }
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
+// Two values rounded once to the element type (fp16, or bf16 when kBF), lo in the low half.
+template <bool kBF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kBF) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+template <bool kBF>
+__device__ __forceinline__ float load_bias(const __half* bias, int n) {
+  return elem_to_float<kBF>(reinterpret_cast<const uint16_t*>(bias)[n]);
+}
+// (c - z) * s on element pairs: the subtraction is exact, the product rounds once.
+template <bool kBF>
+__device__ __forceinline__ uint32_t dq_sub(uint32_t a, uint32_t b) {
+  if constexpr (kBF) return hsub2_bf16(a, b);
+  else return hsub2(a, b);
+}
+template <bool kBF>
+__device__ __forceinline__ uint32_t dq_mul(uint32_t a, uint32_t b) {
+  if constexpr (kBF) return hmul2_bf16(a, b);
+  else return hmul2(a, b);
 }
 
 // Pair mode (tcgen05 cta_group::2): the MMA spans the two CTAs of a cluster.
@@ -362,6 +386,7 @@ struct Span {
 // bias, rounded once to fp16.  With a staging tile (16 rows x 32 columns of the warp's own
 // shared memory) the rows leave as 16-byte stores, 16 at a time; without, one 2-byte store
 // per value.
+template <bool kBF>
 __device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, const uint32_t (&v)[32],
                                           float bias, int t0, int c0, int lane) {
   if (stage != nullptr) {
@@ -369,7 +394,8 @@ __device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, 
     for (int k = 0; k < 2; ++k) {
       __syncwarp();  // the previous round's reads of the tile are done
 #pragma unroll
-      for (int i = 0; i < 16; ++i) stage[i * 32 + lane] = __float2half_rn(__uint_as_float(v[16 * k + i]) + bias);
+      for (int i = 0; i < 16; ++i)
+        stage[i * 32 + lane] = __ushort_as_half(float_to_elem<kBF>(__uint_as_float(v[16 * k + i]) + bias));
       __syncwarp();
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
@@ -388,7 +414,7 @@ __device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, 
     __half* yp = p.y + static_cast<size_t>(t0) * p.N + n;
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __float2half_rn(__uint_as_float(v[j]) + bias);
+      if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __ushort_as_half(float_to_elem<kBF>(__uint_as_float(v[j]) + bias));
   }
 }
 
@@ -398,6 +424,7 @@ __device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, 
 // time go into the warp's staging tile (16 rows x 64 bytes) transposed by stmatrix, each
 // 16-byte chunk of a row XOR-swizzled by (row / 2) % 4 so the eight rows of a matrix fall in
 // distinct banks, and leave as 16-byte stores.
+template <bool kBF>
 __device__ __forceinline__ void store_y32_frag(const PackedParams& p, __half* stage, const uint32_t (&f)[32],
                                                const float (&ba)[2], const float (&bb)[2], int t_base,
                                                int c0, int lane) {
@@ -411,8 +438,8 @@ __device__ __forceinline__ void store_y32_frag(const PackedParams& p, __half* st
 #pragma unroll
       for (int gg = 0; gg < 2; ++gg) {
         const int g = 2 * r + gg;
-        m[2 * gg] = pack_half2(__uint_as_float(f[16 * h + 4 * g]) + ba[h], __uint_as_float(f[16 * h + 4 * g + 1]) + ba[h]);
-        m[2 * gg + 1] = pack_half2(__uint_as_float(f[16 * h + 4 * g + 2]) + bb[h], __uint_as_float(f[16 * h + 4 * g + 3]) + bb[h]);
+        m[2 * gg] = pack2<kBF>(__uint_as_float(f[16 * h + 4 * g]) + ba[h], __uint_as_float(f[16 * h + 4 * g + 1]) + ba[h]);
+        m[2 * gg + 1] = pack2<kBF>(__uint_as_float(f[16 * h + 4 * g + 2]) + bb[h], __uint_as_float(f[16 * h + 4 * g + 3]) + bb[h]);
       }
       // matrix mm = (token group gg = mm / 2, column block mm % 2); lane 8 mm + i: its row i
       const int mm = lane >> 3, i = lane & 7;
@@ -467,7 +494,7 @@ __device__ __forceinline__ void st_release_gpu(unsigned int* ptr, unsigned int v
 // [r KS / SPLIT, (r + 1) KS / SPLIT); ranks 1 .. SPLIT-1 push their fp32 accumulators into
 // rank 0's shared memory (st.async, counted on rank 0's recv barrier), and rank 0 adds them
 // in rank order, adds the bias and stores y.  Split launches give every cluster one tile.
-template <int BT, int SPLIT, bool SK = false>
+template <int BT, int SPLIT, bool SK = false, bool kBF = false>
 __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
     packed_kernel(const __grid_constant__ PackedParams p) {
   using CF = Cfg<BT, SPLIT>;
@@ -605,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
     // stores of all earlier stages); the activation tiles are in place once full_a is (the
     // dequant warps waited for them).  One commit per stage frees its slot.
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_ts<BT>();
+      constexpr uint32_t idesc = idesc_ts<BT>() | (kBF ? kIdescBF : 0u);
       int s = 0, li = 0;
       uint32_t ph = 0;
       bool ok = true, any = false;
@@ -695,14 +722,15 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
            : static_cast<long long>(my_tiles) * (kb1 - kb0);
     constexpr int kStep = CF::kDqPairs ? 2 : 1;
     auto convert = [&](const uint4& w4, uint32_t meta, uint32_t (&v)[16]) {
-      const uint32_t zz = kMagic | ((meta >> 16) * 0x00010001u);  // (1024 + z) in both halves
+      constexpr uint32_t kMag = kBF ? kMagicBF : kMagic;
+      const uint32_t zz = kMag | ((meta >> 16) * 0x00010001u);  // (1024 + z), bf16: (128 + z)
       const uint32_t ss = prmt(meta, 0u, 0x1010u);                  // scale in both halves
       const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
         for (int ii = 0; ii < 4; ++ii)
-          v[4 * jj + ii] = hmul2(hsub2(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMagic), zz), ss);
+          v[4 * jj + ii] = dq_mul<kBF>(dq_sub<kBF>(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMag), zz), ss);
     };
     int s = 0;
     uint32_t ph = 0;
@@ -851,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
           cp_async_commit();
         };
         if (staged) fetch(0);
-        const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+        const float bias = (p.bias != nullptr && n < p.N) ? load_bias<kBF>(p.bias, n) : 0.f;
         uint32_t va[32], vb[32];
         tmem_ld32_nowait(taddr, va);
         tmem_wait_ld(va);
@@ -882,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
                                          __ldcg(slot + static_cast<size_t>(32 * cc + j) * kTN + nl));
             }
           }
-          store_y32(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
+          store_y32<kBF>(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
           if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
         }
         if (!chunks_met) break;
@@ -899,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
       const int b = li % NACC;
       const int m0 = (tile % p.tiles_t) * BT;
       const int n = (tile / p.tiles_t) * kTN + nl;
-      const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+      const float bias = (p.bias != nullptr && n < p.N) ? load_bias<kBF>(p.bias, n) : 0.f;
       if (!wait(&acc_full[b], static_cast<uint32_t>((li / NACC) & 1))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT);
@@ -933,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
               cur[j + 3] = __float_as_uint(__uint_as_float(cur[j + 3]) + q4.w);
             }
           }
-          store_y32(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
+          store_y32<kBF>(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
         };
         if constexpr (CF::kNarrow) {  // one or two chunks: no prefetch (register budget)
 #pragma unroll 1
@@ -950,8 +978,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int na = c0 + 16 * h + (lane >> 2), nb = na + 8;
-            ba[h] = (p.bias != nullptr && na < p.N) ? __half2float(p.bias[na]) : 0.f;
-            bb[h] = (p.bias != nullptr && nb < p.N) ? __half2float(p.bias[nb]) : 0.f;
+            ba[h] = (p.bias != nullptr && na < p.N) ? load_bias<kBF>(p.bias, na) : 0.f;
+            bb[h] = (p.bias != nullptr && nb < p.N) ? load_bias<kBF>(p.bias, nb) : 0.f;
           }
           const uint32_t fbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT);
           uint32_t va[32], vb[32];
@@ -966,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
               tmem_ld16x256_nowait(fbase + 32 * (cc + 1), nxt);
               tmem_ld16x256_nowait(fbase + (16u << 16) + 32 * (cc + 1), nxt + 16);
             }
-            store_y32_frag(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane);
+            store_y32_frag<kBF>(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane);
             if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
           }
         } else {
@@ -1035,6 +1063,7 @@ struct PairCfg {
 constexpr uint32_t kIdescPair = (1u << 4) | (static_cast<uint32_t>(256 >> 3) << 17) |
                                 (static_cast<uint32_t>(256 >> 4) << 24);
 
+template <bool kBF>
 __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_constant__ PackedParams p) {
   using CF = PairCfg;
   constexpr int ST = CF::ST, BT = CF::BT;
@@ -1156,7 +1185,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
             const uint64_t bdesc = sw128_kmajor_desc(sbase + CF::X_OFF + s * CF::XH_BYTES);
 #pragma unroll
             for (int ks = 0; ks < kTK / 16; ++ks)
-              mma_ts_pair(tmem_base, a + 8u * ks, bdesc + 2u * ks, kIdescPair,
+              mma_ts_pair(tmem_base, a + 8u * ks, bdesc + 2u * ks, kIdescPair | (kBF ? kIdescBF : 0u),
                           (kb + i > 0 || ks > 0) ? 1u : 0u);
             mma_commit_pair(&empty[s]);
             if (++s == ST) { s = 0; ph ^= 1u; }
@@ -1194,7 +1223,8 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
         const unsigned char* blk = smem + CF::B_OFF + s * kBlockBytes;
         const uint4 w4 = *reinterpret_cast<const uint4*>(blk + 16 * (128 * h + c));
         const uint32_t meta = *reinterpret_cast<const uint32_t*>(blk + 4 * (1024 + c));
-        const uint32_t zz = kMagic | ((meta >> 16) * 0x00010001u);
+        constexpr uint32_t kMag = kBF ? kMagicBF : kMagic;
+        const uint32_t zz = kMag | ((meta >> 16) * 0x00010001u);
         const uint32_t ss = prmt(meta, 0u, 0x1010u);
         const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
         uint32_t v[16];
@@ -1202,7 +1232,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
         for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
           for (int ii = 0; ii < 4; ++ii)
-            v[4 * jj + ii] = hmul2(hsub2(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMagic), zz), ss);
+            v[4 * jj + ii] = dq_mul<kBF>(dq_sub<kBF>(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMag), zz), ss);
         tmem_st16(tmem_base + lane_addr + CF::A_COL0 + static_cast<uint32_t>(s * 32 + 16 * h), v);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
@@ -1230,7 +1260,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
     for (int tile = pair; tile < p.tiles; tile += npairs, ++li) {
       const int m0 = (tile % p.tiles_t) * BT;
       const int n = ((tile / p.tiles_t) * 2 + static_cast<int>(rank)) * kTN + nl;
-      const float bias = (p.bias != nullptr && n < p.N) ? __half2float(p.bias[n]) : 0.f;
+      const float bias = (p.bias != nullptr && n < p.N) ? load_bias<kBF>(p.bias, n) : 0.f;
       if (!wait(acc_full, static_cast<uint32_t>(li & 1))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
@@ -1241,8 +1271,8 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int na = c0 + 16 * h + (lane >> 2), nb = na + 8;
-          ba[h] = (p.bias != nullptr && na < p.N) ? __half2float(p.bias[na]) : 0.f;
-          bb[h] = (p.bias != nullptr && nb < p.N) ? __half2float(p.bias[nb]) : 0.f;
+          ba[h] = (p.bias != nullptr && na < p.N) ? load_bias<kBF>(p.bias, na) : 0.f;
+          bb[h] = (p.bias != nullptr && nb < p.N) ? load_bias<kBF>(p.bias, nb) : 0.f;
         }
         tmem_ld16x256_nowait(taddr, va);
         tmem_ld16x256_nowait(taddr + (16u << 16), va + 16);
@@ -1255,7 +1285,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
             tmem_ld16x256_nowait(taddr + 32 * (cc + 1), nxt);
             tmem_ld16x256_nowait(taddr + (16u << 16) + 32 * (cc + 1), nxt + 16);
           }
-          store_y32_frag(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane);
+          store_y32_frag<kBF>(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane);
           if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
         }
       } else {
@@ -1266,7 +1296,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
           uint32_t (&cur)[32] = (cc & 1) ? vb : va;
           uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
           if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
-          store_y32(p, nullptr, cur, bias, m0 + 32 * cc, n - lane, lane);
+          store_y32<kBF>(p, nullptr, cur, bias, m0 + 32 * cc, n - lane, lane);
           if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
         }
       }
@@ -1284,13 +1314,14 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
   }
 }
 
+template <bool kBF>
 cudaError_t launch_pair(const PackedParams& base, const GemmProblem& p) {
   using CF = PairCfg;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int cap = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(packed_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    attr_err = cudaFuncSetAttribute(packed_pair_kernel<kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
     if (attr_err != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
@@ -1303,14 +1334,14 @@ cudaError_t launch_pair(const PackedParams& base, const GemmProblem& p) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&cap, packed_pair_kernel, &cfg) != cudaSuccess) cap = 0;
+    if (cudaOccupancyMaxActiveClusters(&cap, packed_pair_kernel<kBF>, &cfg) != cudaSuccess) cap = 0;
     (void)cudaGetLastError();
   });
   if (attr_err != cudaSuccess) return attr_err;
   if (cap <= 0) return cudaErrorInvalidConfiguration;
   PackedParams pp = base;
   const char* why = nullptr;
-  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, CF::BT / 2,
+  if (!make_tmap_2d(&pp.tm_x, kBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, CF::BT / 2,
                     CU_TENSOR_MAP_SWIZZLE_128B, &why))
     return cudaErrorInvalidValue;
   pp.tiles_t = (p.M + CF::BT - 1) / CF::BT;
@@ -1330,23 +1361,23 @@ cudaError_t launch_pair(const PackedParams& base, const GemmProblem& p) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_pair_kernel, pp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_pair_kernel<kBF>, pp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int BT, int SPLIT>
+template <int BT, int SPLIT, bool kBF>
 cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
   using CF = Cfg<BT, SPLIT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(packed_kernel<BT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    attr_err = cudaFuncSetAttribute(packed_kernel<BT, SPLIT, false, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   PackedParams pp = base;
   const char* why = nullptr;
-  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, BT,
+  if (!make_tmap_2d(&pp.tm_x, kBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, BT,
                     CU_TENSOR_MAP_SWIZZLE_128B, &why))
     return cudaErrorInvalidValue;
   pp.tiles_t = (p.M + BT - 1) / BT;
@@ -1360,7 +1391,7 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
     if (e != cudaSuccess) return e;
     const int cap = (CF::kNarrow ? 2 : 1) * sms;
     const int grid = pp.tiles < cap ? pp.tiles : cap;
-    packed_kernel<BT, SPLIT><<<grid, kThreads, CF::SMEM, p.stream>>>(pp);
+    packed_kernel<BT, SPLIT, false, kBF><<<grid, kThreads, CF::SMEM, p.stream>>>(pp);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -1375,7 +1406,7 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_kernel<BT, SPLIT>, pp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_kernel<BT, SPLIT, false, kBF>, pp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1383,18 +1414,19 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
 // Stream-K launch (256-row tiles): one CTA per SM, at least kSkMinUnits stages each.
 size_t sk_flag_bytes(int sms) { return (static_cast<size_t>(sms) * 4 + 255) / 256 * 256; }
 
+template <bool kBF>
 cudaError_t launch_sk(const PackedParams& base, const GemmProblem& p, void* workspace, int sms) {
   using CF = Cfg<kSkRows, 1>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(packed_kernel<kSkRows, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(packed_kernel<kSkRows, 1, true, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     CF::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   PackedParams pp = base;
   const char* why = nullptr;
-  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, kSkRows,
+  if (!make_tmap_2d(&pp.tm_x, kBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, kSkRows,
                     CU_TENSOR_MAP_SWIZZLE_128B, &why))
     return cudaErrorInvalidValue;
   pp.tiles_t = (p.M + kSkRows - 1) / kSkRows;
@@ -1407,7 +1439,7 @@ cudaError_t launch_sk(const PackedParams& base, const GemmProblem& p, void* work
   if (grid < 1) grid = 1;
   pp.flags = static_cast<unsigned int*>(workspace);
   pp.partial = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + sk_flag_bytes(sms));
-  packed_kernel<kSkRows, 1, true><<<static_cast<unsigned>(grid), kThreads, CF::SMEM, p.stream>>>(pp);
+  packed_kernel<kSkRows, 1, true, kBF><<<static_cast<unsigned>(grid), kThreads, CF::SMEM, p.stream>>>(pp);
   return cudaGetLastError();
 }
 
@@ -1451,6 +1483,27 @@ PackedPlan packed_plan(int M, int K, int N, int sms) {
     pl.split = split;
   }
   return pl;
+}
+
+// The plan of one launch (token tile, K split, stream-K or the pair kernel) and the launch.
+template <bool kBF>
+cudaError_t launch_planned(const PackedParams& pp, const GemmProblem& p, void* workspace, size_t workspace_bytes,
+                           int sms) {
+  const PackedPlan pl = packed_plan(p.M, p.K, p.N, sms);
+  if (pl.bt == 32)
+    return pl.split == 4 ? launch_bt<32, 4, kBF>(pp, p) : pl.split == 2 ? launch_bt<32, 2, kBF>(pp, p) : launch_bt<32, 1, kBF>(pp, p);
+  if (pl.bt == 64) return pl.split == 2 ? launch_bt<64, 2, kBF>(pp, p) : launch_bt<64, 1, kBF>(pp, p);
+  if (pl.bt == 128) return pl.split == 2 ? launch_bt<128, 2, kBF>(pp, p) : launch_bt<128, 1, kBF>(pp, p);
+  // Pairs of column tiles (the packed layout holds ceil(N / 128) of them) for long K: sustained
+  // under the power cap the pair kernel ran 1508 against 1460 TFLOP/s on the 70B linears at
+  // M = 4096 (it moves half the activations per SM, so it clocks higher at the same power);
+  // at K = 4096 the single-CTA kernel was ahead (1374 against 1343 on the 7B linears).
+  const bool pair = p.K >= kPairMinK && ((p.N + kTN - 1) / kTN) % 2 == 0;
+  if (workspace != nullptr && workspace_bytes >= packed_workspace_bytes(sms) &&
+      use_stream_k(p.M, p.K, p.N, sms, pair))
+    return launch_sk<kBF>(pp, p, workspace, sms);
+  if (pair) return launch_pair<kBF>(pp, p);
+  return launch_bt<256, 1, kBF>(pp, p);
 }
 
 }  // namespace
@@ -1523,21 +1576,8 @@ cudaError_t launch_packed(const GemmProblem& p, const void* packed, void* worksp
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const PackedPlan pl = packed_plan(p.M, p.K, p.N, sms);
-  if (pl.bt == 32)
-    return pl.split == 4 ? launch_bt<32, 4>(pp, p) : pl.split == 2 ? launch_bt<32, 2>(pp, p) : launch_bt<32, 1>(pp, p);
-  if (pl.bt == 64) return pl.split == 2 ? launch_bt<64, 2>(pp, p) : launch_bt<64, 1>(pp, p);
-  if (pl.bt == 128) return pl.split == 2 ? launch_bt<128, 2>(pp, p) : launch_bt<128, 1>(pp, p);
-  // Pairs of column tiles (the packed layout holds ceil(N / 128) of them) for long K: sustained
-  // under the power cap the pair kernel ran 1508 against 1460 TFLOP/s on the 70B linears at
-  // M = 4096 (it moves half the activations per SM, so it clocks higher at the same power);
-  // at K = 4096 the single-CTA kernel was ahead (1374 against 1343 on the 7B linears).
-  const bool pair = p.K >= kPairMinK && ((p.N + kTN - 1) / kTN) % 2 == 0;
-  if (workspace != nullptr && workspace_bytes >= packed_workspace_bytes(sms) &&
-      use_stream_k(p.M, p.K, p.N, sms, pair))
-    return launch_sk(pp, p, workspace, sms);
-  if (pair) return launch_pair(pp, p);
-  return launch_bt<256, 1>(pp, p);
+  return p.bf16 ? launch_planned<true>(pp, p, workspace, workspace_bytes, sms)
+                : launch_planned<false>(pp, p, workspace, workspace_bytes, sms);
 }
 
 }  // namespace awq
