@@ -69,6 +69,11 @@ What it computes, and where each step comes from:
   row offset ORDER[p] in nibble p (the checkpoint's column interleave, applied along K);
   then 128 meta words, word c = scale bits (fp16) | zero << 16 of column 128t + c for the
   group of row 64s.  Columns past N hold code 0, zero 0, scale 0.
+* Tile-packed layout of 8-bit codes (:func:`repack8`, :func:`unpack_repacked8`): the same
+  tiles and stages, one block of 8704 bytes each: two halves h, two 16-row quarters k of
+  each, 128 columns x 4 words, word (h, k, c, j) at index 1024h + 512k + 4c + j holding the
+  codes of column 128t + c for rows 64s + 32h + 16k + 4j + 0..3, row offset b in byte b;
+  then the 128 meta words as above (8-bit zeros fit the upper half).  Needs N % 4 == 0.
 
 Pins (tests/test_oracle.py, run without a GPU): ORDER and its inverse from
 the wiki's "Saved formats and packing" section, a hand-packed word, AWQ-004
@@ -449,4 +454,95 @@ def gemm_packed(x, packed, bias, K: int, N: int, group_size: int) -> np.ndarray:
     y = np.asarray(x).astype(np.float64) @ W
     if bias is not None:
         y = y + np.asarray(bias).astype(np.float64)[None, :]
+    return y
+
+
+PACK8_BLOCK_WORDS = PACK_TN * PACK_TK // 4 + PACK_TN  # 2048 code words + 128 meta words
+PACK8_BLOCK_BYTES = 4 * PACK8_BLOCK_WORDS              # 8704
+
+
+def repack8_size(K: int, N: int, group_size: int) -> int:
+    """Bytes of the 8-bit tile-packed layout: one block per (column tile, K stage)."""
+    G = resolve_group_size(K, group_size)
+    if K % PACK_TK != 0 or G % PACK_TK != 0 or N % 4 != 0:
+        raise ValueError("the 8-bit tile-packed layout needs K % 64 == 0, G % 64 == 0, N % 4 == 0")
+    return -(-N // PACK_TN) * (K // PACK_TK) * PACK8_BLOCK_BYTES
+
+
+def repack8(qweight, qzeros, scales, group_size) -> np.ndarray:
+    """8-bit checkpoint layout -> 8-bit tile-packed layout, as uint32 words (module docstring).
+    Steps: unpack codes and zeros with the 8-bit reader, pad the columns to whole tiles, then
+    write every block word by word."""
+    K, C = qweight.shape
+    N = 4 * C
+    G = resolve_group_size(K, group_size)
+    nbytes = repack8_size(K, N, group_size)
+    codes = unpack_codes8(qweight)
+    zeros = unpack_codes8(qzeros)
+    sbits = np.ascontiguousarray(scales, dtype=np.float16).view(np.uint16).astype(np.uint64)
+    NT, KS = -(-N // PACK_TN), K // PACK_TK
+    Np = NT * PACK_TN
+    cp = np.zeros((K, Np), dtype=np.uint64)
+    cp[:, :N] = codes
+    zp = np.zeros((K // G, Np), dtype=np.uint64)
+    zp[:, :N] = zeros
+    sp = np.zeros((K // G, Np), dtype=np.uint64)
+    sp[:, :N] = sbits
+    out = np.zeros(nbytes // 4, dtype=np.uint64)
+    for t in range(NT):
+        cols = slice(PACK_TN * t, PACK_TN * (t + 1))
+        for s in range(KS):
+            base = (t * KS + s) * PACK8_BLOCK_WORDS
+            for h in range(2):
+                for k in range(2):
+                    for j in range(4):
+                        word = np.zeros(PACK_TN, dtype=np.uint64)
+                        for b in range(4):
+                            row = PACK_TK * s + 32 * h + 16 * k + 4 * j + b
+                            word |= cp[row, cols] << np.uint64(8 * b)
+                        out[base + 1024 * h + 512 * k + 4 * np.arange(PACK_TN) + j] = word
+            g = (PACK_TK * s) // G
+            out[base + 2048:base + 2048 + PACK_TN] = sp[g, cols] | (zp[g, cols] << np.uint64(16))
+    return out.astype(np.uint32)
+
+
+def unpack_repacked8(packed, K: int, N: int, group_size: int):
+    """8-bit tile-packed words -> (codes [K, N], zeros [K/G, N], scales fp16 [K/G, N]), reading
+    every block back; the zero and scale of a group are taken from its first stage."""
+    G = resolve_group_size(K, group_size)
+    words = np.asarray(packed, dtype=np.uint32).astype(np.uint64)
+    assert words.size * 4 == repack8_size(K, N, group_size)
+    NT, KS = -(-N // PACK_TN), K // PACK_TK
+    codes = np.zeros((K, NT * PACK_TN), dtype=np.int64)
+    zeros = np.zeros((K // G, NT * PACK_TN), dtype=np.int64)
+    sbits = np.zeros((K // G, NT * PACK_TN), dtype=np.uint16)
+    for t in range(NT):
+        for s in range(KS):
+            base = (t * KS + s) * PACK8_BLOCK_WORDS
+            for h in range(2):
+                for k in range(2):
+                    for j in range(4):
+                        word = words[base + 1024 * h + 512 * k + 4 * np.arange(PACK_TN) + j]
+                        for b in range(4):
+                            row = PACK_TK * s + 32 * h + 16 * k + 4 * j + b
+                            codes[row, PACK_TN * t:PACK_TN * (t + 1)] = (word >> np.uint64(8 * b)) & np.uint64(0xFF)
+            if (PACK_TK * s) % G == 0:
+                meta = words[base + 2048:base + 2048 + PACK_TN]
+                g = (PACK_TK * s) // G
+                sbits[g, PACK_TN * t:PACK_TN * (t + 1)] = (meta & np.uint64(0xFFFF)).astype(np.uint16)
+                zeros[g, PACK_TN * t:PACK_TN * (t + 1)] = (meta >> np.uint64(16)) & np.uint64(0xFF)
+    return codes[:, :N], zeros[:, :N], sbits[:, :N].view(np.float16)
+
+
+def gemm_packed8(x, packed, bias, K: int, N: int, group_size: int) -> np.ndarray:
+    """y = x @ W (+ bias) in fp64 with W read back from the 8-bit tile-packed layout:
+    W[k, n] = (code[k, n] - zero[k // G, n]) * scale[k // G, n] in fp32, as :func:`gemm8`."""
+    G = resolve_group_size(K, group_size)
+    codes, zeros, sc = unpack_repacked8(packed, K, N, group_size)
+    g_of_k = np.arange(K) // G
+    W = ((codes.astype(np.float32) - zeros[g_of_k].astype(np.float32))
+         * sc[g_of_k].astype(np.float32)).astype(np.float64)
+    y = np.asarray(x).astype(np.float64) @ W
+    if bias is not None:
+        y = y + np.asarray(bias).astype(np.float64)
     return y

@@ -594,6 +594,54 @@ def test_packed_scale_words_pass_through():
     assert np.array_equal(zeros, oracle.unpack_codes(db["qzeros"]))
 
 
+def oracle_w8_case(seed, K, N, G, M=1, bias=False):
+    return synth.awq8_linear(seed, M, K, N, group_size=G, bias=bias)
+
+
+def test_packed8_hand_derived_words():
+    # K = 64, N = 4 (one 8-bit word per row), code[k][n] = k + 64 n, zero 0x2A in column 1,
+    # scale 1.0 (0x3C00): words written out by hand from the layout's definition
+    K, N, G = 64, 4, 64
+    codes = np.array([[k + 64 * n for n in range(N)] for k in range(K)])
+    zeros = np.zeros((1, N), dtype=np.int64)
+    zeros[0, 1] = 0x2A
+    qw, qz = oracle.pack_codes8(codes), oracle.pack_codes8(zeros)
+    sc = np.full((1, N), 1.0, dtype=np.float16)
+    pk = oracle.repack8(qw, qz, sc, G)
+    assert pk.size * 4 == oracle.repack8_size(K, N, G) == 8704
+    assert int(pk[0]) == 0x03020100                 # h 0, k 0, column 0, j 0: rows 0..3
+    assert int(pk[1]) == 0x07060504                 # j 1: rows 4..7
+    assert int(pk[4]) == 0x43424140                 # column 1 (codes 64 + row): rows 0..3
+    assert int(pk[512 + 4 * 2 + 3]) == 0x9F9E9D9C   # k 1, column 2, j 3: rows 28..31 -> 156..159
+    assert int(pk[1024 + 512 + 4 * 3 + 3]) == 0xFFFEFDFC  # h 1, k 1, column 3, j 3: rows 60..63
+    assert int(pk[2048 + 1]) == (0x2A << 16) | 0x3C00     # meta of column 1
+    assert int(pk[2048 + 0]) == 0x3C00
+    assert not pk[4 * 4:512].any() and not pk[2048 + 4:].any()   # columns 4..127: padding
+
+
+@pytest.mark.parametrize("K,N,G", [(64, 4, 64), (128, 136, 64), (256, 384, 128), (512, 260, -1)])
+def test_packed8_round_trip_is_lossless(K, N, G):
+    d = oracle_w8_case(330 + K + N, K, N, G)
+    pk = oracle.repack8(d["qweight"], d["qzeros"], d["scales"], G)
+    codes, zeros, sc = oracle.unpack_repacked8(pk, K, N, G)
+    assert np.array_equal(codes, oracle.unpack_codes8(d["qweight"]))
+    assert np.array_equal(zeros, oracle.unpack_codes8(d["qzeros"]))
+    assert np.array_equal(sc.view(np.uint16), d["scales"].view(np.uint16))
+
+
+def test_packed8_gemm_equals_checkpoint_gemm():
+    d = oracle_w8_case(340, 256, 264, 64, M=3, bias=True)
+    pk = oracle.repack8(d["qweight"], d["qzeros"], d["scales"], 64)
+    y = oracle.gemm_packed8(d["x"], pk, d["bias"], 256, 264, 64)
+    assert np.array_equal(y, oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 64))
+
+
+def test_packed8_rejects_unsupported_shapes():
+    for K, N, G in [(96, 64, 32), (128, 64, 32), (64, 6, 64)]:
+        with pytest.raises(ValueError):
+            oracle.repack8_size(K, N, G)
+
+
 def test_packed_padding_and_group_copies():
     # columns past N are all-zero words; every stage of a group carries the same meta row
     K, N, G = 256, 136, 128
