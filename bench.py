@@ -932,13 +932,24 @@ def run_w8_sweep(awq, timed, hbm, hbm_kind):
         dq = lambda: awq.awq_dequant_w8(qw, qz, sc, G)
         timed(dq, 3)
         t_dq = timed(dq, 10)
+        # the 8-bit tile-packed layout: one-off repack, then awq_gemm_packed_w8 with a workspace
+        pk = awq.awq_repack(qw, qz, sc, G, bits=8)
+        rp = lambda: awq.awq_repack(qw, qz, sc, G, out=pk, bits=8)
+        timed(rp, 2)
+        t_rp = timed(rp, 5)
+        ws = torch.zeros((awq.awq_gemm_packed_workspace_size(),), dtype=torch.uint8, device="cuda")
+        fp = lambda: awq.awq_gemm_packed(x, pk, bias, K, N, G, out=y, workspace=ws, bits=8)
+        timed(fp, 3)
+        t_p = timed(fp, 10)
         awq.device_status()
         print(json.dumps({"workload": f"w8_m{M}_{K}x{N}", "bits": 8, "M": M, "K": K, "N": N,
                           "group_size": G, "bias": True, "us": t, "TFLOP_s": flop / t / 1e6,
                           "frac_tensor": flop / t / 1e6 / tflops, "cublas_fp16_dense_us": t_mm,
-                          "dequant_plus_cublas_us": t_dq + t_mm, "tensor_peak_TFLOP_s": tflops}),
+                          "dequant_plus_cublas_us": t_dq + t_mm, "packed_us": t_p,
+                          "packed_TFLOP_s": flop / t_p / 1e6, "packed_frac_tensor": flop / t_p / 1e6 / tflops,
+                          "repack_us": t_rp, "tensor_peak_TFLOP_s": tflops}),
               flush=True)
-        del x, qw, qz, sc, y, wd
+        del x, qw, qz, sc, y, wd, pk, ws
         torch.cuda.empty_cache()
 
 

@@ -391,6 +391,31 @@ awq_status_t awq_gemm_packed_ex(const void* x, const void* packed, const void* b
                                 awq_dtype_t dtype, void* workspace, size_t workspace_bytes,
                                 awq_stream_t stream);
 
+/*
+ * Tile-packed layout of 8-bit codes (GPTQModel wiki "AWQ", "Saved formats and packing": the
+ * 8-bit GEMM layout, byte i of word c = column 4c + i; qweight [K, N/4], qzeros [K/G, N/4],
+ * fp16 scales).  Same tiles and meta words as the 4-bit layout; for tile t, stage s one block
+ * of 2176 uint32 words at word (t * K/64 + s) * 2176:
+ *   word 1024 h + 512 k + 4 c + j (h, k < 2, c < 128, j < 4): the 8-bit codes of column
+ *     128 t + c for rows 64 s + 32 h + 16 k + 4 j + 0..3, row offset b in byte b;
+ *   word 2048 + c: fp16 scale bits | zero << 16 (8-bit zero) of column 128 t + c;
+ *   columns past N: zero.
+ * Requirements: those of awq_dequant_w8 plus K % 64 == 0 and group size % 64 == 0 (or -1).
+ * awq_repack_w8_size: ceil(N / 128) * (K / 64) * 8704 bytes (host only).
+ * awq_repack_w8: as awq_repack, from 8-bit checkpoint tensors.
+ * awq_gemm_packed_w8: y = fp16_rne(x W (+ bias)) from the 8-bit packed layout (fp16 x, bias,
+ *   y; (c - z) * s formed exactly and rounded once to fp16, fp32 accumulation), with an
+ *   optional workspace as awq_gemm_packed_ws (NULL / 0: no stream-K).  Arguments, results and
+ *   errors otherwise as awq_gemm_packed_ws.
+ */
+awq_status_t awq_repack_w8_size(int64_t K, int64_t N, int64_t group_size, size_t* bytes);
+awq_status_t awq_repack_w8(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
+                           int64_t K, int64_t N, int64_t group_size, void* packed_out,
+                           awq_stream_t stream);
+awq_status_t awq_gemm_packed_w8(const void* x_f16, const void* packed, const void* bias_f16,
+                                int64_t M, int64_t K, int64_t N, int64_t group_size, void* y_f16,
+                                void* workspace, size_t workspace_bytes, awq_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the library's device status word on the
  * current device.  Returns AWQ_ERR_TIMEOUT if a kernel gave up a bounded wait since the
  * last check (its output is then unspecified), AWQ_OK otherwise. */

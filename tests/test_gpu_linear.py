@@ -133,12 +133,12 @@ def test_linear_packed_stream_k_shape(awq):
 
 
 def test_linear_packed_refuses_other_formats(awq):
-    # 8-bit codes and shapes outside the layout have no tile-packed form (bf16 scales do: see
-    # tests/test_gpu_bf16.py)
+    # shapes outside the layout have no tile-packed form (bf16 scales and 8-bit codes do: see
+    # tests/test_gpu_bf16.py and tests/test_gpu_w8.py); 8-bit codes with bf16 scales are refused
     d8 = synth.awq8_linear(20501, 2, 256, 128, group_size=128)
-    with pytest.raises(ValueError):
-        awq.AwqLinear(dev(d8["qweight"]), dev(d8["qzeros"]), dev(d8["scales"]), None, group_size=128,
-                      bits=8, packed=True)
+    with pytest.raises(TypeError):
+        awq.AwqLinear(dev(d8["qweight"]), dev(d8["qzeros"]), dev(d8["scales"]).to(torch.bfloat16), None,
+                      group_size=128, bits=8, packed=True)
     d2 = synth.awq_linear(20502, 2, 96, 64, group_size=32)
     with pytest.raises(awq.AwqError):  # K % 64: no tile-packed layout
         awq.AwqLinear(dev(d2["qweight"]), dev(d2["qzeros"]), dev(d2["scales"]), None, group_size=32,

@@ -157,3 +157,71 @@ def test_gemm_w8_tensor_core_contract(awq):
             run(awq, d, path)
     y = run(awq, d)
     assert_close(y, oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 128), "w8 N=40")
+
+
+# Tile-packed layout of 8-bit codes (awq_repack_w8, awq_gemm_packed_w8): the repack is a
+# byte permutation plus padding (bit-exact against the oracle); the linear forms (c - z) * s
+# exactly and rounds it once to fp16, like the fp16 4-bit packed path.  Shapes: narrow split
+# tiles, the 256-row kernel with ragged rows and columns (N % 128 != 0), stream-K (through a
+# workspace), the pair kernel (K = 8192, even column-tile count).
+@pytest.mark.parametrize("K,N,G", [(64, 4, 64), (256, 260, 64), (4096, 11008, 128), (512, 1028, -1)])
+def test_repack_w8_bit_exact(awq, K, N, G):
+    d = synth.awq8_linear(12500 + K + N, 1, K, N, group_size=G)
+    t = to_dev(d)
+    pk = awq.awq_repack(t["qweight"], t["qzeros"], t["scales"], G, bits=8)
+    torch.cuda.synchronize()
+    assert pk.numel() * 4 == awq.awq_repack_size(K, N, G, bits=8) == oracle.repack8_size(K, N, G)
+    want = oracle.repack8(d["qweight"], d["qzeros"], d["scales"], G)
+    assert np.array_equal(pk.cpu().numpy().view(np.uint32), want)
+
+
+PACKED8 = [(40, 1024, 512, 128, True, None), (300, 1024, 260, 64, True, None),
+           (257, 4096, 2048, 128, True, "ws"), (300, 8192, 512, 128, False, None),
+           (700, 512, 1028, -1, True, None)]
+
+
+@pytest.mark.parametrize("M,K,N,G,bias,ws", PACKED8)
+def test_gemm_packed_w8_vs_oracle(awq, M, K, N, G, bias, ws):
+    d = synth.awq8_linear(12600 + M + K, M, K, N, group_size=G, bias=bias)
+    t = to_dev(d)
+    pk = awq.awq_repack(t["qweight"], t["qzeros"], t["scales"], G, bits=8)
+    w = None
+    if ws:
+        w = torch.zeros((awq.awq_gemm_packed_workspace_size(),), dtype=torch.uint8, device="cuda")
+    y = awq.awq_gemm_packed(t["x"], pk, t["bias"], K, N, G, workspace=w, bits=8)
+    torch.cuda.synchronize()
+    if ws:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert w[(sms * 4 + 255) // 256 * 256:].any().item()  # the stream-K kernel ran
+    y_ref = oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G)
+    assert_close(y.cpu().numpy(), y_ref, f"packed w8 M={M} K={K} N={N} G={G}")
+    y2 = awq.awq_gemm_packed(t["x"], pk, t["bias"], K, N, G, workspace=w, bits=8)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+
+
+@pytest.mark.parametrize("M,K,N,ws", [(300, 2048, 384, None), (257, 4096, 2048, "ws"), (64, 2048, 384, None)])
+def test_gemm_packed_w8_exact_case_bitwise(awq, M, K, N, ws):
+    # small-integer activations, power-of-two scales: every product and partial sum is exact,
+    # so y is the oracle's value rounded once to fp16 whatever the summation order
+    d = synth.awq8_linear(12700 + M + K, M, K, N, group_size=128, x_kind="smallint", scale_kind="pow2")
+    t = to_dev(d)
+    pk = awq.awq_repack(t["qweight"], t["qzeros"], t["scales"], 128, bits=8)
+    w = None if not ws else torch.zeros((awq.awq_gemm_packed_workspace_size(),), dtype=torch.uint8, device="cuda")
+    y = awq.awq_gemm_packed(t["x"], pk, None, K, N, 128, workspace=w, bits=8).cpu().numpy()
+    want = oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], None, 128).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
+
+
+def test_linear_packed_w8(awq):
+    M, K, N, G = 300, 4096, 2048, 128
+    d = synth.awq8_linear(12800, M, K, N, group_size=G, bias=True)
+    t = to_dev(d)
+    lin = awq.AwqLinear(t["qweight"], t["qzeros"], t["scales"], t["bias"], group_size=G, bits=8, packed=True)
+    y = lin(t["x"])
+    pk = awq.awq_repack(t["qweight"], t["qzeros"], t["scales"], G, bits=8)
+    y_ref = awq.awq_gemm_packed(t["x"], pk, t["bias"], K, N, G, workspace="auto", bits=8)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_ref)
+    assert_close(y.cpu().numpy(), oracle.gemm8(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G),
+                 "AwqLinear packed w8")

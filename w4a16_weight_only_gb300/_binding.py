@@ -50,6 +50,9 @@ SIGNATURES = {
     "awq_gemm_packed_ws": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, ctypes.c_size_t, _vp]),
     "awq_gemm_packed_noalloc": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "awq_gemm_packed_ex": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp, ctypes.c_size_t, _vp]),
+    "awq_repack_w8_size": (_i32, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
+    "awq_repack_w8": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
+    "awq_gemm_packed_w8": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, ctypes.c_size_t, _vp]),
 }
 GEMM_STATIC_WEIGHTS = 1
 
@@ -182,11 +185,12 @@ class AwqLinear:
     ``awq_gemm_any`` (fp16 or bf16 activations, 4- or 8-bit codes) with only x and out
     checked per call.
 
-    packed=True (fp16 or bf16, 4-bit codes, K % 64 == 0, group size % 64 == 0) also keeps a
-    tile-packed copy of the weights, written once by awq_repack at construction (a device
-    allocation of awq_repack_size bytes, about the size of the packed weights), and runs
-    calls of at least ``packed_min_rows`` rows through awq_gemm_packed_ex with the stream's
-    workspace; smaller calls keep the checkpoint layout.
+    packed=True (4-bit codes with fp16 or bf16, or 8-bit codes with fp16; K % 64 == 0, group
+    size % 64 == 0) also keeps a tile-packed copy of the weights, written once by awq_repack at
+    construction (a device allocation of awq_repack_size bytes, about the size of the packed
+    weights), and runs calls of at least ``packed_min_rows`` rows through awq_gemm_packed_ex
+    (8 bits: awq_gemm_packed_w8) with the stream's workspace; smaller calls keep the
+    checkpoint layout.
 
     qweight int32 [K, N/8] (4 bits) or [K, N/4] (8 bits), qzeros int32 [K/G, N/8 or N/4],
     scales fp16 or bf16 [K/G, N] (it sets the activation dtype; 8 bits: fp16), bias [N] of
@@ -231,9 +235,7 @@ class AwqLinear:
         self.packed = None
         self.packed_min_rows = int(packed_min_rows)
         if packed:
-            if bits != 4:
-                raise ValueError("the tile-packed layout takes 4-bit codes")
-            self.packed = awq_repack(qweight, qzeros, scales, group_size)
+            self.packed = awq_repack(qweight, qzeros, scales, group_size, bits=bits)
         self._path = PATHS[path]
         self._tensors = (qweight, qzeros, scales, bias)
 
@@ -259,9 +261,13 @@ class AwqLinear:
             sh = ((stream if isinstance(stream, int) else stream.cuda_stream)
                   if stream is not None else torch.cuda.current_stream().cuda_stream)
             ws = packed_workspace(self.device, sh)
-            st = _lib.awq_gemm_packed_ex(x.data_ptr(), self.packed.data_ptr(), w[3], M, K, N,
-                                         self.group_size, out.data_ptr(), self._dt, ws.data_ptr(),
-                                         ws.numel(), sh)
+            if self.bits == 8:
+                st = _lib.awq_gemm_packed_w8(x.data_ptr(), self.packed.data_ptr(), w[3], M, K, N,
+                                             self.group_size, out.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+            else:
+                st = _lib.awq_gemm_packed_ex(x.data_ptr(), self.packed.data_ptr(), w[3], M, K, N,
+                                             self.group_size, out.data_ptr(), self._dt, ws.data_ptr(),
+                                             ws.numel(), sh)
             if st != AWQ_OK:
                 raise AwqError(st, last_error())
             return out
@@ -432,34 +438,38 @@ def selftest_wait_timeout(limit_ns=2_000_000, stream=None):
     _check(load_library().awq_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
-def awq_repack_size(K, N, group_size=128) -> int:
-    """Bytes of the tile-packed layout of a [K, N] linear (host only)."""
+def awq_repack_size(K, N, group_size=128, bits=4) -> int:
+    """Bytes of the tile-packed layout of a [K, N] linear of 4- or 8-bit codes (host only)."""
     n = ctypes.c_size_t(0)
-    _check(load_library().awq_repack_size(K, N, group_size, ctypes.byref(n)))
+    lib = load_library()
+    f = lib.awq_repack_w8_size if bits == 8 else lib.awq_repack_size
+    _check(f(K, N, group_size, ctypes.byref(n)))
     return int(n.value)
 
 
-def awq_repack(qweight, qzeros, scales, group_size=128, out=None, stream=None):
+def awq_repack(qweight, qzeros, scales, group_size=128, out=None, stream=None, bits=4):
     """One-off conversion of checkpoint-layout weights into the tile-packed layout via the
-    library's awq_repack.  Returns (or fills) an int32 device tensor of
-    awq_repack_size(K, N, group_size) / 4 words."""
+    library's awq_repack (bits=8: awq_repack_w8, fp16 scales).  Returns (or fills) an int32
+    device tensor of awq_repack_size(K, N, group_size, bits) / 4 words."""
     lib = load_library()
+    if bits not in (4, 8):
+        raise ValueError("bits must be 4 or 8")
     K, C = qweight.shape
-    N = 8 * C
+    N = (32 // bits) * C
     dev = _cuda_index(qweight, "qweight")
     _need(qweight, "qweight", torch.int32, (K, C), dev)
     ng = _groups(K, group_size)
     _need(qzeros, "qzeros", torch.int32, (ng, C), dev)
-    if scales.dtype not in (torch.float16, torch.bfloat16):
-        raise TypeError("scales must be float16 or bfloat16 (their 16-bit words are copied)")
+    if scales.dtype not in (torch.float16, torch.bfloat16) or (bits == 8 and scales.dtype is not torch.float16):
+        raise TypeError("scales must be float16 or bfloat16 (their 16-bit words are copied; 8 bits: float16)")
     _need(scales, "scales", scales.dtype, (ng, N), dev)
-    words = awq_repack_size(K, N, group_size) // 4
+    words = awq_repack_size(K, N, group_size, bits) // 4
     if out is None:
         out = torch.empty((words,), dtype=torch.int32, device=dev)
     else:
         _need(out, "out", torch.int32, (words,), dev)
-    _check(lib.awq_repack(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size, _ptr(out),
-                          _stream(stream)))
+    f = lib.awq_repack_w8 if bits == 8 else lib.awq_repack
+    _check(f(_ptr(qweight), _ptr(qzeros), _ptr(scales), K, N, group_size, _ptr(out), _stream(stream)))
     return out
 
 
@@ -486,13 +496,14 @@ def packed_workspace(device, stream_handle):
     return ws
 
 
-def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None, workspace=None):
+def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None, workspace=None, bits=4):
     """y = x @ W (+ bias) with W in the tile-packed layout (awq_repack's output) via the
     library's awq_gemm_packed; x fp16 [..., K] (leading dims flattened), bias fp16 [N] or
     None.  Returns [..., N] in x's dtype.  workspace: a zero-filled uint8 device tensor of at
     least awq_gemm_packed_workspace_size() bytes, or "auto" for the (device, stream) one: the
     call then goes through awq_gemm_packed_ws (stream-K on shapes that fill the SMs poorly).
-    bfloat16 x (packed weights written from bfloat16 scales) goes through awq_gemm_packed_ex."""
+    bfloat16 x (packed weights written from bfloat16 scales) goes through awq_gemm_packed_ex;
+    bits=8 (packed weights from awq_repack(..., bits=8), float16 x) through awq_gemm_packed_w8."""
     lib = load_library()
     lead = x.shape[:-1]
     if x.shape[-1] != K:
@@ -504,7 +515,9 @@ def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None
     if dt not in (torch.float16, torch.bfloat16):
         raise TypeError("x must be float16 or bfloat16")
     _need(x2, "x", dt, (M, K), dev)
-    _need(packed, "packed", torch.int32, (awq_repack_size(K, N, group_size) // 4,), dev)
+    if bits == 8 and dt is not torch.float16:
+        raise TypeError("8-bit codes take float16 activations")
+    _need(packed, "packed", torch.int32, (awq_repack_size(K, N, group_size, bits) // 4,), dev)
     if bias is not None:
         _need(bias, "bias", dt, (N,), dev)
     if out is None:
@@ -512,7 +525,13 @@ def awq_gemm_packed(x, packed, bias, K, N, group_size=128, out=None, stream=None
     else:
         _need(out, "out", dt, (M, N), dev)
     sh = _stream(stream)
-    if dt is torch.bfloat16:  # awq_gemm_packed_ex (its workspace, if any, as below)
+    if bits == 8:
+        if isinstance(workspace, str) and workspace == "auto":
+            workspace = packed_workspace(dev, sh.value or 0)
+        ws, wsb = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel())
+        _check(lib.awq_gemm_packed_w8(_ptr(x2), _ptr(packed), _ptr(bias), M, K, N, group_size, _ptr(out),
+                                      ws, wsb, sh))
+    elif dt is torch.bfloat16:  # awq_gemm_packed_ex (its workspace, if any, as below)
         if isinstance(workspace, str) and workspace == "auto":
             workspace = packed_workspace(dev, sh.value or 0)
         ws, wsb = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel())

@@ -427,54 +427,79 @@ awq_path_t awq_gemm_select_path_ex(int64_t M, int64_t K, int64_t N, int64_t grou
   return static_cast<awq_path_t>(choose_path(p));
 }
 
-awq_status_t awq_repack_size(int64_t K, int64_t N, int64_t group_size, size_t* bytes) {
+// Tile-packed layout of 4- or 8-bit codes: size and the one-off conversion.
+static awq_status_t repack_size_bits(int64_t K, int64_t N, int64_t group_size, size_t* bytes, int bits) {
   int G = 0;
-  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  awq_status_t st = check_weight_shape(K, N, group_size, &G, bits == 8 ? 4 : 8);
   if (st != AWQ_OK) return st;
   if (!bytes) return fail(AWQ_ERR_INVALID_ARGUMENT, "null bytes pointer");
   const char* why = "";
-  if (!awq::packed_supported(K, N, G, &why)) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "%s", why);
-  *bytes = awq::packed_bytes(K, N);
+  if (!(bits == 8 ? awq::packed8_supported(K, N, G, &why) : awq::packed_supported(K, N, G, &why)))
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "%s", why);
+  *bytes = bits == 8 ? awq::packed8_bytes(K, N) : awq::packed_bytes(K, N);
   return ok();
 }
 
-awq_status_t awq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
-                        int64_t K, int64_t N, int64_t group_size, void* packed_out,
-                        awq_stream_t stream) {
+static awq_status_t repack_bits(const int32_t* qweight, const int32_t* qzeros, const void* scales,
+                                int64_t K, int64_t N, int64_t group_size, void* packed_out,
+                                awq_stream_t stream, int bits) {
   int G = 0;
-  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  awq_status_t st = check_weight_shape(K, N, group_size, &G, bits == 8 ? 4 : 8);
   if (st != AWQ_OK) return st;
   const char* why = "";
-  if (!awq::packed_supported(K, N, G, &why)) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "%s", why);
+  if (!(bits == 8 ? awq::packed8_supported(K, N, G, &why) : awq::packed_supported(K, N, G, &why)))
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "%s", why);
   if (N == 0) return ok();
-  if (!qweight || !qzeros || !scales_f16 || !packed_out)
+  if (!qweight || !qzeros || !scales || !packed_out)
     return fail(AWQ_ERR_INVALID_ARGUMENT, "null pointer among qweight, qzeros, scales, packed_out");
   if (!al(qweight, 4) || !al(qzeros, 4)) return fail(AWQ_ERR_MISALIGNED, "qweight/qzeros must be 4-byte aligned");
-  if (!al(scales_f16, 2)) return fail(AWQ_ERR_MISALIGNED, "scales must be 2-byte aligned");
+  if (!al(scales, 2)) return fail(AWQ_ERR_MISALIGNED, "scales must be 2-byte aligned");
   if (!al(packed_out, 16)) return fail(AWQ_ERR_MISALIGNED, "packed_out must be 16-byte aligned");
   if (K / 64 > 65535) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "K / 64 must be at most 65535");
   st = check_device();
   if (st != AWQ_OK) return st;
-  const cudaError_t e = awq::launch_repack(
-      reinterpret_cast<const uint32_t*>(qweight), reinterpret_cast<const uint32_t*>(qzeros),
-      static_cast<const __half*>(scales_f16), static_cast<int>(K), static_cast<int>(N), G, packed_out,
-      reinterpret_cast<cudaStream_t>(stream));
+  const auto* qw = reinterpret_cast<const uint32_t*>(qweight);
+  const auto* qz = reinterpret_cast<const uint32_t*>(qzeros);
+  const auto* sc = static_cast<const __half*>(scales);
+  const auto strm = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e =
+      bits == 8 ? awq::launch_repack8(qw, qz, sc, static_cast<int>(K), static_cast<int>(N), G, packed_out, strm)
+                : awq::launch_repack(qw, qz, sc, static_cast<int>(K), static_cast<int>(N), G, packed_out, strm);
   if (e != cudaSuccess) return cuda_fail(e, "awq_repack launch");
   return ok();
+}
+
+awq_status_t awq_repack_size(int64_t K, int64_t N, int64_t group_size, size_t* bytes) {
+  return repack_size_bits(K, N, group_size, bytes, 4);
+}
+awq_status_t awq_repack(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
+                        int64_t K, int64_t N, int64_t group_size, void* packed_out,
+                        awq_stream_t stream) {
+  return repack_bits(qweight, qzeros, scales_f16, K, N, group_size, packed_out, stream, 4);
+}
+awq_status_t awq_repack_w8_size(int64_t K, int64_t N, int64_t group_size, size_t* bytes) {
+  return repack_size_bits(K, N, group_size, bytes, 8);
+}
+awq_status_t awq_repack_w8(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,
+                           int64_t K, int64_t N, int64_t group_size, void* packed_out,
+                           awq_stream_t stream) {
+  return repack_bits(qweight, qzeros, scales_f16, K, N, group_size, packed_out, stream, 8);
 }
 
 // Checks of the packed linear's arguments; fills *p, and *launch = false when there is nothing
 // to compute (M == 0 or N == 0).
 static awq_status_t packed_problem(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
                                    int64_t K, int64_t N, int64_t group_size, void* y_f16,
-                                   awq_stream_t stream, awq::GemmProblem* p, bool* launch, bool bf16 = false) {
+                                   awq_stream_t stream, awq::GemmProblem* p, bool* launch, bool bf16 = false,
+                                   int bits = 4) {
   *launch = false;
   if (M < 0) return fail(AWQ_ERR_INVALID_ARGUMENT, "M must be >= 0 (got %lld)", (long long)M);
   int G = 0;
-  awq_status_t st = check_weight_shape(K, N, group_size, &G);
+  awq_status_t st = check_weight_shape(K, N, group_size, &G, bits == 8 ? 4 : 8);
   if (st != AWQ_OK) return st;
   const char* why = "";
-  if (!awq::packed_supported(K, N, G, &why)) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "%s", why);
+  if (!(bits == 8 ? awq::packed8_supported(K, N, G, &why) : awq::packed_supported(K, N, G, &why)))
+    return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "%s", why);
   if (M > kDimLimit) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "M must be below 2^31");
   if (M * N >= kProdLimit || M * K >= kProdLimit)
     return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "M*N and M*K must be below 2^40");
@@ -495,6 +520,7 @@ static awq_status_t packed_problem(const void* x_f16, const void* packed, const 
   p->G = G;
   p->stream = reinterpret_cast<cudaStream_t>(stream);
   p->bf16 = bf16;
+  p->bits = bits;
   *launch = true;
   return ok();
 }
@@ -569,6 +595,20 @@ awq_status_t awq_gemm_packed_ex(const void* x, const void* packed, const void* b
   if (st != AWQ_OK || !launch) return st;
   const cudaError_t e = awq::launch_packed(p, packed, workspace, workspace_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_packed_ex launch");
+  return ok();
+}
+
+awq_status_t awq_gemm_packed_w8(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
+                                int64_t K, int64_t N, int64_t group_size, void* y_f16, void* workspace,
+                                size_t workspace_bytes, awq_stream_t stream) {
+  if (workspace && !al(workspace, 256)) return fail(AWQ_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+  awq::GemmProblem p{};
+  bool launch = false;
+  const awq_status_t st = packed_problem(x_f16, packed, bias_f16, M, K, N, group_size, y_f16, stream, &p,
+                                         &launch, false, 8);
+  if (st != AWQ_OK || !launch) return st;
+  const cudaError_t e = awq::launch_packed(p, packed, workspace, workspace_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_packed_w8 launch");
   return ok();
 }
 

@@ -93,6 +93,12 @@ bool packed_supported(int64_t K, int64_t N, int64_t G, const char** why);
 size_t packed_bytes(int64_t K, int64_t N);
 cudaError_t launch_repack(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
                           int G, void* out, cudaStream_t stream);
+// The same for 8-bit codes (qweight [K, N/4]): shape rule, size, conversion.  launch_packed
+// reads this layout when p.bits == 8 (fp16 only).
+bool packed8_supported(int64_t K, int64_t N, int64_t G, const char** why);
+size_t packed8_bytes(int64_t K, int64_t N);
+cudaError_t launch_repack8(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N,
+                           int G, void* out, cudaStream_t stream);
 // With a workspace of at least packed_workspace_bytes(SM count) bytes (flags zero), launches
 // with M > 128 whose tiles fill the SMs poorly run the stream-K kernel.
 size_t packed_workspace_bytes(int sms);

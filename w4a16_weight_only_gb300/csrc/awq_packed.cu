@@ -43,8 +43,17 @@ using namespace ptx;
 
 constexpr int kTN = 128;                    // output columns per tile / block
 constexpr int kTK = 64;                     // K rows per stage / block
-constexpr int kBlockWords = 1024 + kTN;     // codes + meta
+constexpr int kBlockWords = 1024 + kTN;     // codes + meta (4-bit codes)
 constexpr int kBlockBytes = 4 * kBlockWords;  // 4608
+// Block of one (column tile, K stage) for BITS-bit codes: code words, then kTN meta words at
+// word META.  8-bit codes: word (h, k, c, j) at 1024 h + 512 k + 4 c + j holds column c's
+// codes for rows 32 h + 16 k + 4 j + 0..3 (row offset b in byte b).
+template <int BITS>
+struct Blk {
+  static constexpr int META = BITS == 8 ? 2048 : 1024;
+  static constexpr int WORDS = META + kTN;
+  static constexpr int BYTES = 4 * WORDS;  // 4608 / 8704
+};
 constexpr int kDQ = 8;                      // dequant warps
 constexpr int kThreads = (2 + kDQ + 4) * 32;
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
@@ -105,6 +114,48 @@ __global__ void __launch_bounds__(128) repack_kernel(const uint32_t* __restrict_
   uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(t * KS + s) * kBlockWords);
   const uint4* src = reinterpret_cast<const uint4*>(blk);
   for (int i = tid; i < kBlockWords / 4; i += 128) dst[i] = src[i];
+}
+
+// 8-bit codes: one CTA per block; task (q, cw) (q: rows 4 q .. 4 q + 3 of the stage, cw: one of
+// the tile's 32 checkpoint words of 4 columns) transposes a 4 x 4 byte square into the four
+// columns' code words.  Thread c also writes meta word c.
+__global__ void __launch_bounds__(128) repack8_kernel(const uint32_t* __restrict__ qw,
+                                                      const uint32_t* __restrict__ qz,
+                                                      const uint16_t* __restrict__ sc,
+                                                      uint32_t* __restrict__ out, int K, int N, int G) {
+  constexpr int W8 = Blk<8>::WORDS;
+  __shared__ __align__(16) uint32_t blk[W8];
+  const int s = blockIdx.x, t = blockIdx.y, KS = K / kTK;
+  const int C = N / 4;
+  const int tid = threadIdx.x;
+  for (int task = tid; task < 16 * 32; task += 128) {
+    const int cw = task & 31, q = task >> 5;
+    const int word = 32 * t + cw;
+    const int r0 = kTK * s + 4 * q;
+    uint32_t in[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) in[r] = word < C ? __ldg(qw + static_cast<size_t>(r0 + r) * C + word) : 0u;
+    const int h = q >> 3, k = (q >> 2) & 1, j = q & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // column 4 cw + i: byte i of rows r0 .. r0 + 3
+      const uint32_t sel = static_cast<uint32_t>((4 + i) << 4 | i);
+      blk[1024 * h + 512 * k + 4 * (4 * cw + i) + j] = prmt(prmt(in[0], in[1], sel), prmt(in[2], in[3], sel), 0x5410u);
+    }
+  }
+  {
+    const int n = kTN * t + tid;
+    const int g = (kTK * s) / G;
+    uint32_t m = 0u;
+    if (n < N) {
+      const uint32_t z = (__ldg(qz + static_cast<size_t>(g) * C + n / 4) >> (8 * (n & 3))) & 0xFFu;
+      m = static_cast<uint32_t>(__ldg(sc + static_cast<size_t>(g) * N + n)) | (z << 16);
+    }
+    blk[Blk<8>::META + tid] = m;
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(t * KS + s) * W8);
+  const uint4* src = reinterpret_cast<const uint4*>(blk);
+  for (int i = tid; i < W8 / 4; i += 128) dst[i] = src[i];
 }
 
 // ------------------------------------------------------------ packed linear ----
@@ -317,14 +368,15 @@ constexpr uint32_t idesc_ts() {
 // carries stage j's activations, packed block and A operand, j = s mod ST), plus, in rank 0 of
 // a split, the other ranks' partial sums.  Narrow tiles (BT <= 64) allocate 256 TMEM columns
 // and at most half an SM's shared memory, so two CTAs share an SM.
-template <int BT, int SPLIT>
+template <int BT, int SPLIT, int BITS = 4>
 struct Cfg {
   static constexpr int NACC = BT >= 256 ? 1 : 2;
   static constexpr bool kNarrow = BT <= 64;
   static constexpr int COLS = kNarrow ? 256 : 512;           // TMEM columns allocated
   static constexpr int SA_FIT = (COLS - NACC * BT) / 32;
   static constexpr int X_BYTES = BT * kTK * 2;
-  static constexpr int STAGE = X_BYTES + kBlockBytes;
+  static constexpr int BLK = Blk<BITS>::BYTES;
+  static constexpr int STAGE = X_BYTES + BLK;
   static constexpr int RECV_PITCH = BT + 4;                  // floats per received column
   static constexpr int RECV_BYTES = (SPLIT - 1) * kTN * RECV_PITCH * 4;
   static constexpr int CAP = kNarrow ? 112 * 1024 : kSmemCap;
@@ -336,7 +388,7 @@ struct Cfg {
   static constexpr int ST = ST0 < 8 ? ST0 : 8;
   static constexpr int X_OFF = 0;
   static constexpr int B_OFF = ST * X_BYTES;
-  static constexpr int BAR_OFF = B_OFF + ST * kBlockBytes;
+  static constexpr int BAR_OFF = B_OFF + ST * BLK;
   // full_t[ST], empty[ST], full_a[ST], acc_full[2], acc_empty[2], drain, recv
   static constexpr int NBARS = 3 * ST + 6;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
@@ -361,12 +413,55 @@ struct __align__(128) PackedParams {
   unsigned int* status;
   int M, K, N;
   int tiles_t, tiles;        // activation-row tiles, total tiles
-  int y_vec;                 // y 16-byte aligned (N % 8 == 0 always): 16-byte stores allowed
+  int y_vec;                 // y 16-byte aligned and N % 8 == 0: 16-byte stores of y allowed
   // stream-K only: work units (tiles x stages), ready flags and partial-sum slots
   long long units;
   unsigned int* flags;       // [grid], zero between calls
   float* partial;            // [grid][kSkRows][kTN] fp32
 };
+
+// A dequant thread's share of one stage's block (thread = output column c, K half h): its codes
+// (4-bit: one 16-byte load; 8-bit: two) and its column's meta word.
+template <int BITS>
+struct StageCodes {
+  uint4 a, b;
+  uint32_t meta;
+};
+template <int BITS>
+__device__ __forceinline__ void load_codes(const unsigned char* blk, int h, int c, StageCodes<BITS>& r) {
+  if constexpr (BITS == 8) {
+    r.a = *reinterpret_cast<const uint4*>(blk + 4096 * h + 16 * c);
+    r.b = *reinterpret_cast<const uint4*>(blk + 4096 * h + 2048 + 16 * c);
+  } else {
+    r.a = *reinterpret_cast<const uint4*>(blk + 16 * (128 * h + c));
+  }
+  r.meta = *reinterpret_cast<const uint32_t*>(blk + 4 * (Blk<BITS>::META + c));
+}
+// The 16 element pairs (rows 32 h + 2 i, + 1) of the A operand: (c - z) * s, exact subtraction
+// and one rounding.  4-bit: (word >> 4 i') & 0x000F000F holds rows (2 i', 2 i' + 1) of the
+// word's eight (ORDER interleave along K), or'ed into 1024 + c (bf16: 128 + c).  8-bit: word q
+// holds rows 4 q .. 4 q + 3 one byte each; a byte permute places two of them as 1024 + c.
+template <int BITS, bool kBF>
+__device__ __forceinline__ void convert_codes(const StageCodes<BITS>& cd, uint32_t (&v)[16]) {
+  constexpr uint32_t kMag = kBF ? kMagicBF : kMagic;
+  const uint32_t zz = kMag | ((cd.meta >> 16) * 0x00010001u);  // (1024 + z), bf16: (128 + z)
+  const uint32_t ss = prmt(cd.meta, 0u, 0x1010u);                // scale in both halves
+  if constexpr (BITS == 8) {
+    const uint32_t w[8] = {cd.a.x, cd.a.y, cd.a.z, cd.a.w, cd.b.x, cd.b.y, cd.b.z, cd.b.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {  // bytes (0, 1) and (2, 3) under kMag's exponent bytes
+      v[2 * q] = dq_mul<kBF>(dq_sub<kBF>(prmt(w[q], kMag, 0x7150u), zz), ss);
+      v[2 * q + 1] = dq_mul<kBF>(dq_sub<kBF>(prmt(w[q], kMag, 0x7352u), zz), ss);
+    }
+  } else {
+    const uint32_t w[4] = {cd.a.x, cd.a.y, cd.a.z, cd.a.w};
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+        v[4 * jj + ii] = dq_mul<kBF>(dq_sub<kBF>(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMag), zz), ss);
+  }
+}
 
 // The tiles a CTA takes (tile0, tile0 + tstep, ...) and its K stages [kb0, kb1): without a
 // split, tiles blockIdx.x + k gridDim.x and all stages; with one, the cluster's tile and rank
@@ -494,10 +589,12 @@ __device__ __forceinline__ void st_release_gpu(unsigned int* ptr, unsigned int v
 // [r KS / SPLIT, (r + 1) KS / SPLIT); ranks 1 .. SPLIT-1 push their fp32 accumulators into
 // rank 0's shared memory (st.async, counted on rank 0's recv barrier), and rank 0 adds them
 // in rank order, adds the bias and stores y.  Split launches give every cluster one tile.
-template <int BT, int SPLIT, bool SK = false, bool kBF = false>
-__global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
+template <int BT, int SPLIT, bool SK = false, bool kBF = false, int BITS = 4>
+__global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 1)
     packed_kernel(const __grid_constant__ PackedParams p) {
-  using CF = Cfg<BT, SPLIT>;
+  using CF = Cfg<BT, SPLIT, BITS>;
+  using BK = Blk<BITS>;
+  static_assert(BITS == 4 || (BITS == 8 && !kBF), "8-bit codes: fp16 only");
   static_assert(!SK || (BT == kSkRows && SPLIT == 1), "stream-K: 256-row tiles, no cluster split");
   constexpr int ST = CF::ST, NACC = CF::NACC;
   extern __shared__ unsigned char smem_raw[];
@@ -591,12 +688,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
         int tile = static_cast<int>(u0 / KS), kb = static_cast<int>(u0 - static_cast<long long>(tile) * KS);
         for (long long u = u0; u < u1; ++u) {
           const int m0 = (tile % p.tiles_t) * BT;
-          const uint32_t* src = p.packed + static_cast<size_t>(tile / p.tiles_t) * KS * kBlockWords;
+          const uint32_t* src = p.packed + static_cast<size_t>(tile / p.tiles_t) * KS * BK::WORDS;
           if (!wait(&empty[s], ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + kBlockBytes));
+          mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + BK::BYTES));
           tma_load_2d_hint(smem + CF::X_OFF + s * CF::X_BYTES, &p.tm_x, &full_t[s], kb * kTK, m0, pol_x);
-          bulk_load(smem + CF::B_OFF + s * kBlockBytes, src + static_cast<size_t>(kb) * kBlockWords,
-                    kBlockBytes, &full_t[s], pol_w);
+          bulk_load(smem + CF::B_OFF + s * BK::BYTES, src + static_cast<size_t>(kb) * BK::WORDS,
+                    BK::BYTES, &full_t[s], pol_w);
           ++issued;
           if (++s == ST) { s = 0; ph ^= 1u; }
           if (++kb == KS) { kb = 0; ++tile; }
@@ -605,13 +702,13 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
       for (int tile = tile0; ok && tile < p.tiles; tile += tstep) {
         const int m0 = (tile % p.tiles_t) * BT;
         const int t = tile / p.tiles_t;
-        const uint32_t* src = p.packed + static_cast<size_t>(t) * KS * kBlockWords;
+        const uint32_t* src = p.packed + static_cast<size_t>(t) * KS * BK::WORDS;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait(&empty[s], ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + kBlockBytes));
+          mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + BK::BYTES));
           tma_load_2d_hint(smem + CF::X_OFF + s * CF::X_BYTES, &p.tm_x, &full_t[s], kb * kTK, m0, pol_x);
-          bulk_load(smem + CF::B_OFF + s * kBlockBytes, src + static_cast<size_t>(kb) * kBlockWords,
-                    kBlockBytes, &full_t[s], pol_w);
+          bulk_load(smem + CF::B_OFF + s * BK::BYTES, src + static_cast<size_t>(kb) * BK::WORDS,
+                    BK::BYTES, &full_t[s], pol_w);
           ++issued;
           if (++s == ST) { s = 0; ph ^= 1u; }
         }
@@ -721,17 +818,6 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
         SK ? sk_bound(p.units, blockIdx.x + 1, gridDim.x) - sk_bound(p.units, blockIdx.x, gridDim.x)
            : static_cast<long long>(my_tiles) * (kb1 - kb0);
     constexpr int kStep = CF::kDqPairs ? 2 : 1;
-    auto convert = [&](const uint4& w4, uint32_t meta, uint32_t (&v)[16]) {
-      constexpr uint32_t kMag = kBF ? kMagicBF : kMagic;
-      const uint32_t zz = kMag | ((meta >> 16) * 0x00010001u);  // (1024 + z), bf16: (128 + z)
-      const uint32_t ss = prmt(meta, 0u, 0x1010u);                  // scale in both halves
-      const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-        for (int ii = 0; ii < 4; ++ii)
-          v[4 * jj + ii] = dq_mul<kBF>(dq_sub<kBF>(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMag), zz), ss);
-    };
     int s = 0;
     uint32_t ph = 0;
     for (long long g = 0; g < total; g += kStep) {
@@ -739,23 +825,18 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
       const int s1 = s + 1 == ST ? 0 : s + 1;
       const uint32_t ph1 = s + 1 == ST ? ph ^ 1u : ph;
       if (!wait(&full_t[s], ph)) break;
-      const unsigned char* b0 = smem + CF::B_OFF + s * kBlockBytes;
-      const uint4 w0 = *reinterpret_cast<const uint4*>(b0 + 16 * (128 * h + c));
-      const uint32_t m0 = *reinterpret_cast<const uint32_t*>(b0 + 4 * (1024 + c));
-      uint4 w1 = make_uint4(0u, 0u, 0u, 0u);
-      uint32_t m1 = 0u;
+      StageCodes<BITS> c0, c1;
+      load_codes<BITS>(smem + CF::B_OFF + s * BK::BYTES, h, c, c0);
       if (two) {
         if (!wait(&full_t[s1], ph1)) break;
-        const unsigned char* b1 = smem + CF::B_OFF + s1 * kBlockBytes;
-        w1 = *reinterpret_cast<const uint4*>(b1 + 16 * (128 * h + c));
-        m1 = *reinterpret_cast<const uint32_t*>(b1 + 4 * (1024 + c));
+        load_codes<BITS>(smem + CF::B_OFF + s1 * BK::BYTES, h, c, c1);
       }
       tc_fence_after();  // the TMEM stores below come after the previous round's MMAs
       uint32_t v[16];
-      convert(w0, m0, v);
+      convert_codes<BITS, kBF>(c0, v);
       tmem_st16(tmem_base + lane_addr + CF::A_COL0 + static_cast<uint32_t>(s * 32 + 16 * h), v);
       if (two) {
-        convert(w1, m1, v);
+        convert_codes<BITS, kBF>(c1, v);
         tmem_st16(tmem_base + lane_addr + CF::A_COL0 + static_cast<uint32_t>(s1 * 32 + 16 * h), v);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -1037,17 +1118,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT>::kNarrow ? 2 : 1)
 // single-CTA kernel).  CTA 0 issues the MMAs and commits to the barriers of both CTAs; the
 // dequant and epilogue warps of CTA 1 arrive on CTA 0's barriers.  Each CTA's TMEM holds the
 // accumulator rows of its own columns.
+template <int BITS = 4>
 struct PairCfg {
   static constexpr int BT = 256;
   static constexpr int XH_BYTES = (BT / 2) * kTK * 2;  // this CTA's half of the activation tile
-  static constexpr int STAGE = XH_BYTES + kBlockBytes;
+  static constexpr int BLK = Blk<BITS>::BYTES;
+  static constexpr int STAGE = XH_BYTES + BLK;
   static constexpr int SA_FIT = (512 - BT) / 32;
   static constexpr int ST_FIT = (kSmemCap - 2048) / STAGE;
   static constexpr int ST0 = ST_FIT < SA_FIT ? ST_FIT : SA_FIT;
   static constexpr int ST = ST0 < 8 ? ST0 : 8;
   static constexpr int X_OFF = 0;
   static constexpr int B_OFF = ST * XH_BYTES;
-  static constexpr int BAR_OFF = B_OFF + ST * kBlockBytes;
+  static constexpr int BAR_OFF = B_OFF + ST * BLK;
   // full_t[ST], empty[ST], full_a[ST], acc_full, acc_empty, drain
   static constexpr int NBARS = 3 * ST + 3;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
@@ -1063,9 +1146,11 @@ struct PairCfg {
 constexpr uint32_t kIdescPair = (1u << 4) | (static_cast<uint32_t>(256 >> 3) << 17) |
                                 (static_cast<uint32_t>(256 >> 4) << 24);
 
-template <bool kBF>
+template <bool kBF, int BITS = 4>
 __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_constant__ PackedParams p) {
-  using CF = PairCfg;
+  using CF = PairCfg<BITS>;
+  using BK = Blk<BITS>;
+  static_assert(BITS == 4 || (BITS == 8 && !kBF), "8-bit codes: fp16 only");
   constexpr int ST = CF::ST, BT = CF::BT;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -1143,13 +1228,13 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
       for (int tile = pair; ok && tile < p.tiles; tile += npairs) {
         const int m0 = (tile % p.tiles_t) * BT + static_cast<int>(rank) * (BT / 2);
         const int t = (tile / p.tiles_t) * 2 + static_cast<int>(rank);
-        const uint32_t* src = p.packed + static_cast<size_t>(t) * KS * kBlockWords;
+        const uint32_t* src = p.packed + static_cast<size_t>(t) * KS * BK::WORDS;
         for (int kb = 0; kb < KS; ++kb) {
           if (!wait(&empty[s], ph ^ 1u)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::XH_BYTES + kBlockBytes));
+          mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::XH_BYTES + BK::BYTES));
           tma_load_2d_hint(smem + CF::X_OFF + s * CF::XH_BYTES, &p.tm_x, &full_t[s], kb * kTK, m0, pol_x);
-          bulk_load(smem + CF::B_OFF + s * kBlockBytes, src + static_cast<size_t>(kb) * kBlockWords,
-                    kBlockBytes, &full_t[s], pol_w);
+          bulk_load(smem + CF::B_OFF + s * BK::BYTES, src + static_cast<size_t>(kb) * BK::WORDS,
+                    BK::BYTES, &full_t[s], pol_w);
           ++issued;
           if (++s == ST) { s = 0; ph ^= 1u; }
         }
@@ -1220,19 +1305,10 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
       for (int kb = 0; kb < KS; ++kb) {
         if (!wait(&full_t[s], ph)) { ok = false; break; }
         tc_fence_after();
-        const unsigned char* blk = smem + CF::B_OFF + s * kBlockBytes;
-        const uint4 w4 = *reinterpret_cast<const uint4*>(blk + 16 * (128 * h + c));
-        const uint32_t meta = *reinterpret_cast<const uint32_t*>(blk + 4 * (1024 + c));
-        constexpr uint32_t kMag = kBF ? kMagicBF : kMagic;
-        const uint32_t zz = kMag | ((meta >> 16) * 0x00010001u);
-        const uint32_t ss = prmt(meta, 0u, 0x1010u);
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        StageCodes<BITS> cd;
+        load_codes<BITS>(smem + CF::B_OFF + s * BK::BYTES, h, c, cd);
         uint32_t v[16];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-          for (int ii = 0; ii < 4; ++ii)
-            v[4 * jj + ii] = dq_mul<kBF>(dq_sub<kBF>(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMag), zz), ss);
+        convert_codes<BITS, kBF>(cd, v);
         tmem_st16(tmem_base + lane_addr + CF::A_COL0 + static_cast<uint32_t>(s * 32 + 16 * h), v);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
@@ -1314,14 +1390,14 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
   }
 }
 
-template <bool kBF>
+template <bool kBF, int BITS>
 cudaError_t launch_pair(const PackedParams& base, const GemmProblem& p) {
-  using CF = PairCfg;
+  using CF = PairCfg<BITS>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int cap = 0;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(packed_pair_kernel<kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    attr_err = cudaFuncSetAttribute(packed_pair_kernel<kBF, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
     if (attr_err != cudaSuccess) return;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
@@ -1334,7 +1410,7 @@ cudaError_t launch_pair(const PackedParams& base, const GemmProblem& p) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&cap, packed_pair_kernel<kBF>, &cfg) != cudaSuccess) cap = 0;
+    if (cudaOccupancyMaxActiveClusters(&cap, packed_pair_kernel<kBF, BITS>, &cfg) != cudaSuccess) cap = 0;
     (void)cudaGetLastError();
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -1361,18 +1437,18 @@ cudaError_t launch_pair(const PackedParams& base, const GemmProblem& p) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_pair_kernel<kBF>, pp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_pair_kernel<kBF, BITS>, pp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int BT, int SPLIT, bool kBF>
+template <int BT, int SPLIT, bool kBF, int BITS>
 cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
-  using CF = Cfg<BT, SPLIT>;
+  using CF = Cfg<BT, SPLIT, BITS>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(packed_kernel<BT, SPLIT, false, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    attr_err = cudaFuncSetAttribute(packed_kernel<BT, SPLIT, false, kBF, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   PackedParams pp = base;
@@ -1391,7 +1467,7 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
     if (e != cudaSuccess) return e;
     const int cap = (CF::kNarrow ? 2 : 1) * sms;
     const int grid = pp.tiles < cap ? pp.tiles : cap;
-    packed_kernel<BT, SPLIT, false, kBF><<<grid, kThreads, CF::SMEM, p.stream>>>(pp);
+    packed_kernel<BT, SPLIT, false, kBF, BITS><<<grid, kThreads, CF::SMEM, p.stream>>>(pp);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -1406,7 +1482,7 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_kernel<BT, SPLIT, false, kBF>, pp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_kernel<BT, SPLIT, false, kBF, BITS>, pp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1414,13 +1490,13 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
 // Stream-K launch (256-row tiles): one CTA per SM, at least kSkMinUnits stages each.
 size_t sk_flag_bytes(int sms) { return (static_cast<size_t>(sms) * 4 + 255) / 256 * 256; }
 
-template <bool kBF>
+template <bool kBF, int BITS>
 cudaError_t launch_sk(const PackedParams& base, const GemmProblem& p, void* workspace, int sms) {
-  using CF = Cfg<kSkRows, 1>;
+  using CF = Cfg<kSkRows, 1, BITS>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(packed_kernel<kSkRows, 1, true, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(packed_kernel<kSkRows, 1, true, kBF, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     CF::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -1439,7 +1515,7 @@ cudaError_t launch_sk(const PackedParams& base, const GemmProblem& p, void* work
   if (grid < 1) grid = 1;
   pp.flags = static_cast<unsigned int*>(workspace);
   pp.partial = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + sk_flag_bytes(sms));
-  packed_kernel<kSkRows, 1, true, kBF><<<static_cast<unsigned>(grid), kThreads, CF::SMEM, p.stream>>>(pp);
+  packed_kernel<kSkRows, 1, true, kBF, BITS><<<static_cast<unsigned>(grid), kThreads, CF::SMEM, p.stream>>>(pp);
   return cudaGetLastError();
 }
 
@@ -1486,14 +1562,14 @@ PackedPlan packed_plan(int M, int K, int N, int sms) {
 }
 
 // The plan of one launch (token tile, K split, stream-K or the pair kernel) and the launch.
-template <bool kBF>
+template <bool kBF, int BITS>
 cudaError_t launch_planned(const PackedParams& pp, const GemmProblem& p, void* workspace, size_t workspace_bytes,
                            int sms) {
   const PackedPlan pl = packed_plan(p.M, p.K, p.N, sms);
   if (pl.bt == 32)
-    return pl.split == 4 ? launch_bt<32, 4, kBF>(pp, p) : pl.split == 2 ? launch_bt<32, 2, kBF>(pp, p) : launch_bt<32, 1, kBF>(pp, p);
-  if (pl.bt == 64) return pl.split == 2 ? launch_bt<64, 2, kBF>(pp, p) : launch_bt<64, 1, kBF>(pp, p);
-  if (pl.bt == 128) return pl.split == 2 ? launch_bt<128, 2, kBF>(pp, p) : launch_bt<128, 1, kBF>(pp, p);
+    return pl.split == 4 ? launch_bt<32, 4, kBF, BITS>(pp, p) : pl.split == 2 ? launch_bt<32, 2, kBF, BITS>(pp, p) : launch_bt<32, 1, kBF, BITS>(pp, p);
+  if (pl.bt == 64) return pl.split == 2 ? launch_bt<64, 2, kBF, BITS>(pp, p) : launch_bt<64, 1, kBF, BITS>(pp, p);
+  if (pl.bt == 128) return pl.split == 2 ? launch_bt<128, 2, kBF, BITS>(pp, p) : launch_bt<128, 1, kBF, BITS>(pp, p);
   // Pairs of column tiles (the packed layout holds ceil(N / 128) of them) for long K: sustained
   // under the power cap the pair kernel ran 1508 against 1460 TFLOP/s on the 70B linears at
   // M = 4096 (it moves half the activations per SM, so it clocks higher at the same power);
@@ -1501,12 +1577,33 @@ cudaError_t launch_planned(const PackedParams& pp, const GemmProblem& p, void* w
   const bool pair = p.K >= kPairMinK && ((p.N + kTN - 1) / kTN) % 2 == 0;
   if (workspace != nullptr && workspace_bytes >= packed_workspace_bytes(sms) &&
       use_stream_k(p.M, p.K, p.N, sms, pair))
-    return launch_sk<kBF>(pp, p, workspace, sms);
-  if (pair) return launch_pair<kBF>(pp, p);
-  return launch_bt<256, 1, kBF>(pp, p);
+    return launch_sk<kBF, BITS>(pp, p, workspace, sms);
+  if (pair) return launch_pair<kBF, BITS>(pp, p);
+  return launch_bt<256, 1, kBF, BITS>(pp, p);
 }
 
 }  // namespace
+
+bool packed8_supported(int64_t K, int64_t N, int64_t G, const char** why) {
+  static const char* dummy;
+  if (!why) why = &dummy;
+  if (K % kTK != 0) { *why = "the tile-packed layout needs K % 64 == 0"; return false; }
+  if (G % kTK != 0) { *why = "the tile-packed layout needs group_size % 64 == 0 (or -1)"; return false; }
+  if (N % 4 != 0) { *why = "N must be a multiple of 4"; return false; }
+  return true;
+}
+
+size_t packed8_bytes(int64_t K, int64_t N) {
+  return static_cast<size_t>((N + kTN - 1) / kTN) * static_cast<size_t>(K / kTK) * Blk<8>::BYTES;
+}
+
+cudaError_t launch_repack8(const uint32_t* qw, const uint32_t* qz, const __half* sc, int K, int N, int G,
+                           void* out, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(K / kTK), static_cast<unsigned>((N + kTN - 1) / kTN));
+  repack8_kernel<<<grid, 128, 0, stream>>>(qw, qz, reinterpret_cast<const uint16_t*>(sc),
+                                           static_cast<uint32_t*>(out), K, N, G);
+  return cudaGetLastError();
+}
 
 bool packed_supported(int64_t K, int64_t N, int64_t G, const char** why) {
   static const char* dummy;
@@ -1571,13 +1668,16 @@ cudaError_t launch_packed(const GemmProblem& p, const void* packed, void* worksp
   cudaError_t e = status_word_ptr(&pp.status);
   if (e != cudaSuccess) return e;
   pp.M = p.M; pp.K = p.K; pp.N = p.N;
-  pp.y_vec = aligned(p.y, 16) ? 1 : 0;
+  // 16-byte stores of y need a 16-byte aligned base and rows of whole 16-byte pieces (N % 8
+  // == 0: always for 4-bit codes; 8-bit codes allow N % 4 == 0, whose y takes 2-byte stores)
+  pp.y_vec = (aligned(p.y, 16) && p.N % 8 == 0) ? 1 : 0;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  return p.bf16 ? launch_planned<true>(pp, p, workspace, workspace_bytes, sms)
-                : launch_planned<false>(pp, p, workspace, workspace_bytes, sms);
+  if (p.bits == 8) return launch_planned<false, 8>(pp, p, workspace, workspace_bytes, sms);
+  return p.bf16 ? launch_planned<true, 4>(pp, p, workspace, workspace_bytes, sms)
+                : launch_planned<false, 4>(pp, p, workspace, workspace_bytes, sms);
 }
 
 }  // namespace awq
