@@ -261,6 +261,22 @@ def test_packed_layout_argument_checks_are_host_side(lib):
     assert w(A, B, None, 0, 256, 64, 128, B, A, 1 << 20, None) == 0         # M == 0: no launch
     assert w(None, B, None, 4, 256, 64, 128, B, A, 1 << 20, None) == INVALID
     assert lib.awq_gemm_packed_workspace_size(None) == INVALID
+    # 8-bit tile-packed layout: 8704-byte blocks, N % 4
+    assert lib.awq_repack_w8_size(8192, 28672, 128, ctypes.byref(n)) == 0 and n.value == 224 * 128 * 8704
+    assert lib.awq_repack_w8_size(128, 260, -1, ctypes.byref(n)) == 0 and n.value == 3 * 2 * 8704
+    assert lib.awq_repack_w8_size(256, 6, 128, ctypes.byref(n)) == SHAPE    # N % 4
+    assert lib.awq_repack_w8_size(96, 64, 32, ctypes.byref(n)) == SHAPE     # K % 64
+    r8 = lib.awq_repack_w8
+    assert r8(A, A, A, 256, 64, 128, None, None) == INVALID
+    assert r8(A, A, A, 256, 64, 128, P(0x200008), None) == MISALIGNED
+    assert r8(A, A, A, 256, 0, 128, B, None) == 0
+    g8 = lib.awq_gemm_packed_w8
+    # (x, packed, bias, M, K, N, G, y, workspace, workspace_bytes, stream)
+    assert g8(A, B, None, 4, 256, 6, 128, B, None, 0, None) == SHAPE
+    assert g8(P(0x100002), B, None, 4, 256, 260, 128, B, None, 0, None) == MISALIGNED
+    assert g8(A, B, None, 0, 256, 260, 128, B, None, 0, None) == 0
+    e = lib.awq_gemm_packed_ex
+    assert e(A, B, None, 4, 256, 64, 128, B, 1, None, 0, None) == INVALID   # fp32 activations
     z = lib.awq_gemm_packed_noalloc
     # (x, packed, bias, M, K, N, G, y, stream): the packed linear's checks, before any scratch use
     assert z(A, B, None, 4, 96, 64, 32, B, None) == SHAPE
@@ -273,3 +289,6 @@ def test_packed_layout_argument_checks_are_host_side(lib):
         assert w(A, B, None, 4, 256, 64, 128, B, None, 0, None) == DEVICE    # no workspace: plain plan
         assert lib.awq_gemm_packed_workspace_size(ctypes.byref(n)) == DEVICE
         assert z(A, B, None, 4, 256, 64, 128, B, None) == DEVICE
+        assert g8(A, B, None, 4, 256, 260, 128, B, None, 0, None) == DEVICE
+        assert r8(A, A, A, 256, 64, 128, B, None) == DEVICE
+        assert e(A, B, None, 4, 256, 64, 128, B, 2, None, 0, None) == DEVICE
