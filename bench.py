@@ -994,6 +994,42 @@ def run_grouped_sweep(awq, timed, hbm, hbm_kind):
                               "hbm_peak": hbm_kind}), flush=True)
             del sets, g, w, x, y
             torch.cuda.empty_cache()
+    # prefill-sized routed batches (T = 4096 tokens, top-2 of 8 experts): TFLOP/s of the routed
+    # rows, the grouped decode kernel beside the grouped tile-packed kernel (one-off repack of
+    # the experts timed separately)
+    tflops = 1900.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tflops = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        pass
+    for (K, N) in ((4096, 14336), (14336, 4096)):
+        E, topk, G, T = 8, 2, 128, 4096
+        d = synth.moe_inputs(4100 + K, T, topk, E, K, N, group_size=G)
+        R = d["R"]
+        flop = 2.0 * R * K * N
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        x, offs = dev(d["x"]), dev(d["offsets"])
+        qw, qz, sc = dev(d["qweight"]), dev(d["qzeros"]), dev(d["scales"])
+        y = torch.empty((R, N), dtype=torch.float16, device="cuda")
+        # launches on the current stream: the one `timed` makes current and records on
+        fd = lambda: awq.awq_gemm_grouped(x, qw, qz, sc, offs, None, G, out=y)
+        timed(fd, 1)
+        t_dec = timed(fd, 3)
+        pk = awq.awq_repack_experts(qw, qz, sc, G)
+        t_rp = timed(lambda: awq.awq_repack_experts(qw, qz, sc, G), 2)
+        fp = lambda: awq.awq_gemm_packed_grouped(x, pk, offs, K, N, None, G, out=y)
+        timed(fp, 3)
+        t_p = timed(fp, 10)
+        awq.device_status()
+        print(json.dumps({"workload": f"moe_prefill_e{E}_top{topk}_t{T}_{K}x{N}", "E": E, "topk": topk,
+                          "tokens": T, "rows": R, "K": K, "N": N, "group_size": G,
+                          "grouped_decode_us": t_dec, "grouped_decode_TFLOP_s": flop / t_dec / 1e6,
+                          "packed_us": t_p, "packed_TFLOP_s": flop / t_p / 1e6,
+                          "packed_frac_tensor": flop / t_p / 1e6 / tflops, "repack_experts_us": t_rp,
+                          "tensor_peak_TFLOP_s": tflops}), flush=True)
+        del x, qw, qz, sc, y, pk
+        torch.cuda.empty_cache()
 
 
 def quantize_bytes(N, K, G):

@@ -60,3 +60,48 @@ def test_grouped_rejects_outside_contract(awq):
     d = synth.moe_inputs(701, 4, 1, 2, 96, 64, group_size=32)  # K % 64 != 0
     with pytest.raises(awq.AwqError):
         run(awq, d)
+
+
+# Grouped linear on stacked tile-packed experts (awq_repack_experts, awq_gemm_packed_grouped):
+# prefill-sized routed batches.  Cases: uneven experts with some empty, one expert holding all
+# rows, expert boundaries inside and at the edges of 256-row tiles, ragged column tiles.
+def run_packed(awq, d):
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    pk = awq.awq_repack_experts(dev(d["qweight"]), dev(d["qzeros"]), dev(d["scales"]), d["group_size"])
+    y = awq.awq_gemm_packed_grouped(dev(d["x"]), pk, dev(d["offsets"]), d["K"], d["N"],
+                                    None if d["bias"] is None else dev(d["bias"]), group_size=d["group_size"])
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,topk,E,K,N,G,bias", [(600, 2, 8, 1024, 520, 128, True), (300, 1, 1, 512, 256, 64, False),
+                                                 (700, 2, 16, 512, 384, -1, True), (2048, 2, 8, 2048, 1024, 128, True)])
+def test_grouped_packed_vs_oracle(awq, T, topk, E, K, N, G, bias):
+    d = synth.moe_inputs(31000 + T + E, T, topk, E, K, N, group_size=G, bias=bias)
+    y = run_packed(awq, d)
+    check(y, d)
+    assert np.array_equal(run_packed(awq, d).view(np.uint16), y.view(np.uint16))
+
+
+def test_grouped_packed_tile_edges(awq):
+    # hand-set offsets: empty first expert, an expert of exactly 256 rows, one of 257, one of 1,
+    # an empty one in the middle, the rest in the last
+    d = synth.moe_inputs(31500, 800, 1, 6, 512, 264, group_size=128, bias=True)
+    d["offsets"] = np.array([0, 0, 256, 513, 514, 514, 800], dtype=np.int32)
+    y = run_packed(awq, d)
+    check(y, d)
+
+
+def test_grouped_packed_exact_case_bitwise(awq):
+    # small-integer activations, power-of-two scales: every product and sum is exact, so y is
+    # the oracle's value rounded once to fp16
+    E, K, N, G, R = 4, 1024, 384, 128, 700
+    ex = [synth.awq_linear(31600 + e, 1, K, N, group_size=G, x_kind="smallint", scale_kind="pow2")
+          for e in range(E)]
+    x = synth.awq_linear(31650, R, K, N, group_size=G, x_kind="smallint", scale_kind="pow2")["x"]
+    d = {"x": x, "qweight": np.stack([a["qweight"] for a in ex]), "qzeros": np.stack([a["qzeros"] for a in ex]),
+         "scales": np.stack([a["scales"] for a in ex]), "bias": None, "group_size": G, "K": K, "N": N,
+         "offsets": np.array([0, 100, 400, 401, R], dtype=np.int32)}
+    y = run_packed(awq, d)
+    want = oracle.gemm_grouped(d["x"], d["qweight"], d["qzeros"], d["scales"], None, G, d["offsets"])
+    assert np.array_equal(y.view(np.uint16), want.astype(np.float16).view(np.uint16))

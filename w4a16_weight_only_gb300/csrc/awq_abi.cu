@@ -612,6 +612,25 @@ awq_status_t awq_gemm_packed_w8(const void* x_f16, const void* packed, const voi
   return ok();
 }
 
+awq_status_t awq_gemm_packed_grouped(const void* x_f16, const void* packed, const void* bias_f16,
+                                     const int32_t* expert_offsets, int64_t R, int64_t E, int64_t K,
+                                     int64_t N, int64_t group_size, void* y_f16, awq_stream_t stream) {
+  if (E <= 0 || E > awq::kPackedGroupedMaxE)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "E must be in 1..%d (got %lld)", awq::kPackedGroupedMaxE, (long long)E);
+  awq::GemmProblem p{};
+  bool launch = false;
+  awq_status_t st = packed_problem(x_f16, packed, bias_f16, R, K, N, group_size, y_f16, stream, &p, &launch);
+  if (st != AWQ_OK || !launch) return st;
+  if (K * N * E >= kProdLimit) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "E*K*N must be below 2^40");
+  if (!expert_offsets) return fail(AWQ_ERR_INVALID_ARGUMENT, "null expert_offsets");
+  if (!al(expert_offsets, 4)) return fail(AWQ_ERR_MISALIGNED, "expert_offsets must be 4-byte aligned");
+  p.offsets = expert_offsets;
+  p.E = static_cast<int>(E);
+  const cudaError_t e = awq::launch_packed_grouped(p, packed);
+  if (e != cudaSuccess) return cuda_fail(e, "awq_gemm_packed_grouped launch");
+  return ok();
+}
+
 awq_status_t awq_gemm_packed_ws(const void* x_f16, const void* packed, const void* bias_f16, int64_t M,
                                 int64_t K, int64_t N, int64_t group_size, void* y_f16, void* workspace,
                                 size_t workspace_bytes, awq_stream_t stream) {

@@ -414,11 +414,75 @@ struct __align__(128) PackedParams {
   int M, K, N;
   int tiles_t, tiles;        // activation-row tiles, total tiles
   int y_vec;                 // y 16-byte aligned and N % 8 == 0: 16-byte stores of y allowed
+  // grouped (experts) only: device row offsets [E + 1], column tiles per expert, words per
+  // expert's packed layout
+  const int* offsets;
+  int E, grp_nt;
+  size_t expert_words;
   // stream-K only: work units (tiles x stages), ready flags and partial-sum slots
   long long units;
   unsigned int* flags;       // [grid], zero between calls
   float* partial;            // [grid][kSkRows][kTN] fp32
 };
+
+// Grouped (mixture-of-experts) launches: rows offsets[e] .. offsets[e + 1] - 1 of x and y belong
+// to expert e, whose packed layout is the e-th of E stacked ones.  Tiles run over (expert,
+// 256-row tile of its rows, column tile), row tiles fastest; the CTAs find the tile starts
+// of the experts in a table built at the start (E <= kGrpMaxE).  Offsets are clamped into
+// [0, R] and made non-decreasing, so bad offsets give wrong rows, never a bad access.
+constexpr int kGrpMaxE = kPackedGroupedMaxE;
+constexpr int kGrpBytes = 4 * (kGrpMaxE + 4);
+__device__ __forceinline__ void grp_rows(const PackedParams& p, int e, int& a, int& b) {
+  a = min(max(__ldg(p.offsets + e), 0), p.M);
+  b = min(max(__ldg(p.offsets + e + 1), a), p.M);
+}
+__device__ __forceinline__ int grp_count(const PackedParams& p, int e) {
+  int a, b;
+  grp_rows(p, e, a, b);
+  return (b - a + 255) / 256 * p.grp_nt;
+}
+// One warp: ts[e] = tiles of experts 0 .. e - 1, ts[E] = all tiles.
+__device__ __forceinline__ void grp_build_table(const PackedParams& p, int* ts, int lane) {
+  const int per = (p.E + 31) / 32;
+  const int e0 = min(p.E, lane * per), e1 = min(p.E, e0 + per);
+  int mine = 0;
+  for (int e = e0; e < e1; ++e) mine += grp_count(p, e);
+  int incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  int run = incl - mine;
+  for (int e = e0; e < e1; ++e) {
+    ts[e] = run;
+    run += grp_count(p, e);
+  }
+  if (lane == 31) ts[p.E] = incl;
+}
+struct GrpTile {
+  int e, row0, rowb, nt;
+};
+// Tile -> its expert (the last e with ts[e] <= tile: the tile lies in e's non-empty range),
+// first row, end of the expert's rows, column tile.
+__device__ __forceinline__ GrpTile grp_tile(const PackedParams& p, const int* ts, int tile) {
+  int lo = 0, hi = p.E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (ts[mid] <= tile) lo = mid;
+    else hi = mid;
+  }
+  int a, b;
+  grp_rows(p, lo, a, b);
+  const int mt = (b - a + 255) / 256;
+  const int local = tile - ts[lo];
+  GrpTile g;
+  g.e = lo;
+  g.row0 = a + 256 * (local % mt);
+  g.rowb = b;
+  g.nt = local / mt;
+  return g;
+}
 
 // A dequant thread's share of one stage's block (thread = output column c, K half h): its codes
 // (4-bit: one 16-byte load; 8-bit: two) and its column's meta word.
@@ -483,7 +547,7 @@ struct Span {
 // per value.
 template <bool kBF>
 __device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, const uint32_t (&v)[32],
-                                          float bias, int t0, int c0, int lane) {
+                                          float bias, int t0, int c0, int lane, int mlim) {
   if (stage != nullptr) {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -497,7 +561,7 @@ __device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, 
         const int piece = lane + 32 * r;  // 16 rows x 4 pieces of 8 columns
         const int row = piece >> 2, col = (piece & 3) * 8;
         const int t = t0 + 16 * k + row;
-        if (t < p.M && c0 + col < p.N)  // N % 8 == 0: a piece is wholly inside or outside
+        if (t < mlim && c0 + col < p.N)  // N % 8 == 0: a piece is wholly inside or outside
           *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(t) * p.N + c0 + col) =
               *reinterpret_cast<const uint4*>(stage + row * 32 + col);
       }
@@ -509,7 +573,7 @@ __device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, 
     __half* yp = p.y + static_cast<size_t>(t0) * p.N + n;
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (t0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = __ushort_as_half(float_to_elem<kBF>(__uint_as_float(v[j]) + bias));
+      if (t0 + j < mlim) yp[static_cast<size_t>(j) * p.N] = __ushort_as_half(float_to_elem<kBF>(__uint_as_float(v[j]) + bias));
   }
 }
 
@@ -522,7 +586,7 @@ __device__ __forceinline__ void store_y32(const PackedParams& p, __half* stage, 
 template <bool kBF>
 __device__ __forceinline__ void store_y32_frag(const PackedParams& p, __half* stage, const uint32_t (&f)[32],
                                                const float (&ba)[2], const float (&bb)[2], int t_base,
-                                               int c0, int lane) {
+                                               int c0, int lane, int mlim) {
   const uint32_t sbase = smem_u32(stage);
 #pragma unroll
   for (int r = 0; r < 2; ++r) {  // tokens 16 r .. 16 r + 15: 8-token groups 2 r, 2 r + 1
@@ -549,7 +613,7 @@ __device__ __forceinline__ void store_y32_frag(const PackedParams& p, __half* st
       const int row = piece >> 2, chunk = piece & 3;
       const int t = t_base + 16 * r + row;
       const int col = c0 + 8 * chunk;
-      if (t < p.M && col < p.N)  // N % 8 == 0: a chunk is wholly inside or outside
+      if (t < mlim && col < p.N)  // N % 8 == 0: a chunk is wholly inside or outside
         *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(t) * p.N + col) =
             lds128_u(sbase + static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) * 16)));
     }
@@ -589,12 +653,13 @@ __device__ __forceinline__ void st_release_gpu(unsigned int* ptr, unsigned int v
 // [r KS / SPLIT, (r + 1) KS / SPLIT); ranks 1 .. SPLIT-1 push their fp32 accumulators into
 // rank 0's shared memory (st.async, counted on rank 0's recv barrier), and rank 0 adds them
 // in rank order, adds the bias and stores y.  Split launches give every cluster one tile.
-template <int BT, int SPLIT, bool SK = false, bool kBF = false, int BITS = 4>
+template <int BT, int SPLIT, bool SK = false, bool kBF = false, int BITS = 4, bool GRP = false>
 __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 1)
     packed_kernel(const __grid_constant__ PackedParams p) {
   using CF = Cfg<BT, SPLIT, BITS>;
   using BK = Blk<BITS>;
   static_assert(BITS == 4 || (BITS == 8 && !kBF), "8-bit codes: fp16 only");
+  static_assert(!GRP || (BT == 256 && SPLIT == 1 && !SK), "grouped: the persistent 256-row kernel");
   static_assert(!SK || (BT == kSkRows && SPLIT == 1), "stream-K: 256-row tiles, no cluster split");
   constexpr int ST = CF::ST, NACC = CF::NACC;
   extern __shared__ unsigned char smem_raw[];
@@ -641,10 +706,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // grouped: the experts' tile starts, after the ring (the host adds kGrpBytes to the launch)
+  int* grp_ts = reinterpret_cast<int*>(smem + CF::YST_OFF + CF::YST_BYTES);
+  if constexpr (GRP) {
+    if (warp == 2 + kDQ) grp_build_table(p, grp_ts, lane);
+  }
   __syncthreads();
   if constexpr (SPLIT > 1) cluster_sync_all();  // rank 0's recv barrier exists before any push
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = GRP ? grp_ts[p.E] : p.tiles;
 
   // Bounded wait; on give-up every role learns it through the abort flag (read only then,
   // and before each blocking wait of the roles that poll it).
@@ -699,10 +770,19 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
           if (++kb == KS) { kb = 0; ++tile; }
         }
       } else
-      for (int tile = tile0; ok && tile < p.tiles; tile += tstep) {
-        const int m0 = (tile % p.tiles_t) * BT;
-        const int t = tile / p.tiles_t;
-        const uint32_t* src = p.packed + static_cast<size_t>(t) * KS * BK::WORDS;
+      for (int tile = tile0; ok && tile < ntiles; tile += tstep) {
+        int m0, t;
+        const uint32_t* src = p.packed;
+        if constexpr (GRP) {
+          const GrpTile g = grp_tile(p, grp_ts, tile);
+          m0 = g.row0;
+          t = g.nt;
+          src += static_cast<size_t>(g.e) * p.expert_words;
+        } else {
+          m0 = (tile % p.tiles_t) * BT;
+          t = tile / p.tiles_t;
+        }
+        src += static_cast<size_t>(t) * KS * BK::WORDS;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait(&empty[s], ph ^ 1u)) { ok = false; break; }
           mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + BK::BYTES));
@@ -766,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
           mma_commit(&acc_full[b]);
         }
       } else
-      for (int tile = tile0; ok && tile < p.tiles; tile += tstep, ++li) {
+      for (int tile = tile0; ok && tile < ntiles; tile += tstep, ++li) {
         const int b = li % NACC;
         if (!wait(&acc_empty[b], static_cast<uint32_t>(((li / NACC) & 1) ^ 1))) { ok = false; break; }
         tc_fence_after();
@@ -813,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
     const int h = (warp - 2) >> 2;
     const int c = 32 * q + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-    const int my_tiles = tile0 < p.tiles ? (p.tiles - 1 - tile0) / tstep + 1 : 0;
+    const int my_tiles = tile0 < ntiles ? (ntiles - 1 - tile0) / tstep + 1 : 0;
     const long long total =  // the CTA's stages
         SK ? sk_bound(p.units, blockIdx.x + 1, gridDim.x) - sk_bound(p.units, blockIdx.x, gridDim.x)
            : static_cast<long long>(my_tiles) * (kb1 - kb0);
@@ -891,6 +971,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
         const int b = li % NACC;
         const int m0 = (tile % p.tiles_t) * BT;
         const int n = (tile / p.tiles_t) * kTN + nl;
+        const int mlim = p.M;
         if (!wait(&acc_full[b], static_cast<uint32_t>((li / NACC) & 1))) break;
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT);
@@ -991,7 +1072,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
                                          __ldcg(slot + static_cast<size_t>(32 * cc + j) * kTN + nl));
             }
           }
-          store_y32<kBF>(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
+          store_y32<kBF>(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane, mlim);
           if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
         }
         if (!chunks_met) break;
@@ -1004,11 +1085,21 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
         if (!met) break;
       }
     } else
-    for (int tile = tile0; tile < p.tiles; tile += tstep, ++li) {
+    for (int tile = tile0; tile < ntiles; tile += tstep, ++li) {
       const int b = li % NACC;
-      const int m0 = (tile % p.tiles_t) * BT;
-      const int n = (tile / p.tiles_t) * kTN + nl;
-      const float bias = (p.bias != nullptr && n < p.N) ? load_bias<kBF>(p.bias, n) : 0.f;
+      int m0, n, mlim = p.M;
+      const __half* bias_row = p.bias;
+      if constexpr (GRP) {
+        const GrpTile g = grp_tile(p, grp_ts, tile);
+        m0 = g.row0;
+        n = g.nt * kTN + nl;
+        mlim = g.rowb;  // the next expert's rows are computed and discarded
+        if (bias_row != nullptr) bias_row += static_cast<size_t>(g.e) * p.N;
+      } else {
+        m0 = (tile % p.tiles_t) * BT;
+        n = (tile / p.tiles_t) * kTN + nl;
+      }
+      const float bias = (bias_row != nullptr && n < p.N) ? load_bias<kBF>(bias_row, n) : 0.f;
       if (!wait(&acc_full[b], static_cast<uint32_t>((li / NACC) & 1))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT);
@@ -1042,7 +1133,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
               cur[j + 3] = __float_as_uint(__uint_as_float(cur[j + 3]) + q4.w);
             }
           }
-          store_y32<kBF>(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane);
+          store_y32<kBF>(p, ystage, cur, bias, m0 + 32 * cc, n - lane, lane, mlim);
         };
         if constexpr (CF::kNarrow) {  // one or two chunks: no prefetch (register budget)
 #pragma unroll 1
@@ -1059,8 +1150,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int na = c0 + 16 * h + (lane >> 2), nb = na + 8;
-            ba[h] = (p.bias != nullptr && na < p.N) ? load_bias<kBF>(p.bias, na) : 0.f;
-            bb[h] = (p.bias != nullptr && nb < p.N) ? load_bias<kBF>(p.bias, nb) : 0.f;
+            ba[h] = (bias_row != nullptr && na < p.N) ? load_bias<kBF>(bias_row, na) : 0.f;
+            bb[h] = (bias_row != nullptr && nb < p.N) ? load_bias<kBF>(bias_row, nb) : 0.f;
           }
           const uint32_t fbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT);
           uint32_t va[32], vb[32];
@@ -1075,7 +1166,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
               tmem_ld16x256_nowait(fbase + 32 * (cc + 1), nxt);
               tmem_ld16x256_nowait(fbase + (16u << 16) + 32 * (cc + 1), nxt + 16);
             }
-            store_y32_frag<kBF>(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane);
+            store_y32_frag<kBF>(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane, mlim);
             if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
           }
         } else {
@@ -1336,6 +1427,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
     for (int tile = pair; tile < p.tiles; tile += npairs, ++li) {
       const int m0 = (tile % p.tiles_t) * BT;
       const int n = ((tile / p.tiles_t) * 2 + static_cast<int>(rank)) * kTN + nl;
+      const int mlim = p.M;
       const float bias = (p.bias != nullptr && n < p.N) ? load_bias<kBF>(p.bias, n) : 0.f;
       if (!wait(acc_full, static_cast<uint32_t>(li & 1))) break;
       tc_fence_after();
@@ -1361,7 +1453,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
             tmem_ld16x256_nowait(taddr + 32 * (cc + 1), nxt);
             tmem_ld16x256_nowait(taddr + (16u << 16) + 32 * (cc + 1), nxt + 16);
           }
-          store_y32_frag<kBF>(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane);
+          store_y32_frag<kBF>(p, ystage, cur, ba, bb, m0 + 32 * cc, c0, lane, mlim);
           if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
         }
       } else {
@@ -1372,7 +1464,7 @@ __global__ void __launch_bounds__(kThreads, 1) packed_pair_kernel(const __grid_c
           uint32_t (&cur)[32] = (cc & 1) ? vb : va;
           uint32_t (&nxt)[32] = (cc & 1) ? va : vb;
           if (cc + 1 < BT / 32) tmem_ld32_nowait(taddr + 32 * (cc + 1), nxt);
-          store_y32<kBF>(p, nullptr, cur, bias, m0 + 32 * cc, n - lane, lane);
+          store_y32<kBF>(p, nullptr, cur, bias, m0 + 32 * cc, n - lane, lane, mlim);
           if (cc + 1 < BT / 32) tmem_wait_ld(nxt);
         }
       }
@@ -1627,6 +1719,45 @@ cudaError_t launch_repack(const uint32_t* qw, const uint32_t* qz, const __half* 
 }
 
 size_t packed_workspace_flag_bytes(int sms) { return sk_flag_bytes(sms); }
+
+cudaError_t launch_packed_grouped(const GemmProblem& p, const void* packed) {
+  using CF = Cfg<256, 1, 4>;
+  static_assert(CF::USED + kGrpBytes <= kSmemCap, "grouped: tile-start table after the ring");
+  constexpr int kSmem = CF::SMEM + kGrpBytes;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(packed_kernel<256, 1, false, false, 4, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  PackedParams pp{};
+  pp.packed = static_cast<const uint32_t*>(packed);
+  pp.bias = p.bias;
+  pp.y = p.y;
+  cudaError_t e = status_word_ptr(&pp.status);
+  if (e != cudaSuccess) return e;
+  pp.M = p.M; pp.K = p.K; pp.N = p.N;
+  pp.y_vec = (aligned(p.y, 16) && p.N % 8 == 0) ? 1 : 0;
+  const char* why = nullptr;
+  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, 256,
+                    CU_TENSOR_MAP_SWIZZLE_128B, &why))
+    return cudaErrorInvalidValue;
+  const int NT = (p.N + kTN - 1) / kTN, KS = p.K / kTK;
+  pp.offsets = p.offsets;
+  pp.E = p.E;
+  pp.grp_nt = NT;
+  pp.expert_words = static_cast<size_t>(NT) * KS * Blk<4>::WORDS;
+  const long long tmax = (static_cast<long long>(p.M + 255) / 256 + p.E) * NT;  // tiles at most
+  if (tmax > 0x7fffffffLL) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long grid = tmax < sms ? tmax : sms;
+  packed_kernel<256, 1, false, false, 4, true><<<static_cast<unsigned>(grid), kThreads, kSmem, p.stream>>>(pp);
+  return cudaGetLastError();
+}
 
 size_t packed_workspace_bytes(int sms) {
   return sk_flag_bytes(sms) + static_cast<size_t>(sms) * kSkSlotBytes;
