@@ -277,6 +277,12 @@ def test_packed_layout_argument_checks_are_host_side(lib):
     assert g8(A, B, None, 0, 256, 260, 128, B, None, 0, None) == 0
     e = lib.awq_gemm_packed_ex
     assert e(A, B, None, 4, 256, 64, 128, B, 1, None, 0, None) == INVALID   # fp32 activations
+    gp = lib.awq_gemm_packed_grouped
+    # (x, packed, bias, offsets, R, E, K, N, G, y, stream)
+    assert gp(A, B, None, A, 8, 0, 256, 64, 128, B, None) == INVALID          # E >= 1
+    assert gp(A, B, None, A, 8, 257, 256, 64, 128, B, None) == INVALID        # E <= 256
+    assert gp(A, B, None, A, 8, 4, 96, 64, 32, B, None) == SHAPE              # K % 64
+    assert gp(A, B, None, A, 0, 4, 256, 64, 128, B, None) == 0                # R == 0: no launch
     z = lib.awq_gemm_packed_noalloc
     # (x, packed, bias, M, K, N, G, y, stream): the packed linear's checks, before any scratch use
     assert z(A, B, None, 4, 96, 64, 32, B, None) == SHAPE
@@ -290,5 +296,6 @@ def test_packed_layout_argument_checks_are_host_side(lib):
         assert lib.awq_gemm_packed_workspace_size(ctypes.byref(n)) == DEVICE
         assert z(A, B, None, 4, 256, 64, 128, B, None) == DEVICE
         assert g8(A, B, None, 4, 256, 260, 128, B, None, 0, None) == DEVICE
+        assert gp(A, B, None, A, 8, 4, 256, 64, 128, B, None) == DEVICE
         assert r8(A, A, A, 256, 64, 128, B, None) == DEVICE
         assert e(A, B, None, 4, 256, 64, 128, B, 2, None, 0, None) == DEVICE
