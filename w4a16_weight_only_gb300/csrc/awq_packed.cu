@@ -1,5 +1,6 @@
-// Tile-packed layout: the one-off repack (awq_repack) and the tensor-core linear that reads
-// it (awq_gemm_packed).
+// Tile-packed layout: the one-off repack (awq_repack, awq_repack_w8) and the tensor-core
+// linear that reads it (awq_gemm_packed and its workspace, bf16, 8-bit, no-allocation and
+// grouped forms).
 //
 // Layout (this library's kernel-native order; repacking the AWQ order away for a kernel is
 // the prior art of the vLLM article, section 5.1, and of the GPTQModel wiki, "Marlin and
@@ -28,9 +29,19 @@
 // Warp roles (448 threads): warp 0 producer (one TMA copy of the activation tile and one
 // bulk copy of the packed block per stage), warp 1 TMEM allocation and the MMA-issuing
 // thread, warps 2-9 dequant (warp w: TMEM lanes 32 (w % 4) .., K half (w - 2) / 4), warps
-// 10-13 epilogue (tcgen05.ld, + bias, fp16 stores).  Every wait is bounded in wall time;
+// 10-13 epilogue (tcgen05.ld, + bias, rounding, stores).  Every wait is bounded in wall time;
 // on give-up the kernel sets the device status word, every role leaves its loop, issued
 // copies and MMAs are drained (bounded) and TMEM is freed.
+//
+// Variants, all of the same kernel body: token tiles of 32 / 64 / 128 rows with a K split over
+// a cluster (few rows), 256-row tiles (one accumulator; y staged through shared memory as
+// 16-byte stores), stream-K over one CTA per SM with a caller workspace (tiles that fill the
+// SMs poorly), a two-CTA cta_group::2 kernel (long K), bf16 activations and scales, 8-bit codes
+// (their own block layout, below), and a grouped mode over stacked experts' layouts.
+//
+// 8-bit codes: the same tiles and meta words (8-bit zeros), 2176-word blocks: word
+// 1024 h + 512 k + 4 c + j holds column c's codes for rows 32 h + 16 k + 4 j + 0..3, one
+// byte each, so a dequant thread's 32 rows are two 16-byte loads.
 #include <mutex>
 
 #include "awq_internal.cuh"
