@@ -1021,14 +1021,21 @@ def run_grouped_sweep(awq, timed, hbm, hbm_kind):
         fp = lambda: awq.awq_gemm_packed_grouped(x, pk, offs, K, N, None, G, out=y)
         timed(fp, 3)
         t_p = timed(fp, 10)
+        # the same experts and rows in bf16 (scales and x cast on the device, experts repacked)
+        xb, yb = x.to(torch.bfloat16), torch.empty((R, N), dtype=torch.bfloat16, device="cuda")
+        pkb = awq.awq_repack_experts(qw, qz, sc.to(torch.bfloat16), G)
+        fb = lambda: awq.awq_gemm_packed_grouped(xb, pkb, offs, K, N, None, G, out=yb)
+        timed(fb, 3)
+        t_b = timed(fb, 10)
         awq.device_status()
         print(json.dumps({"workload": f"moe_prefill_e{E}_top{topk}_t{T}_{K}x{N}", "E": E, "topk": topk,
                           "tokens": T, "rows": R, "K": K, "N": N, "group_size": G,
                           "grouped_decode_us": t_dec, "grouped_decode_TFLOP_s": flop / t_dec / 1e6,
                           "packed_us": t_p, "packed_TFLOP_s": flop / t_p / 1e6,
                           "packed_frac_tensor": flop / t_p / 1e6 / tflops, "repack_experts_us": t_rp,
+                          "packed_bf16_us": t_b, "packed_bf16_TFLOP_s": flop / t_b / 1e6,
                           "tensor_peak_TFLOP_s": tflops}), flush=True)
-        del x, qw, qz, sc, y, pk
+        del x, qw, qz, sc, y, pk, xb, yb, pkb
         torch.cuda.empty_cache()
 
 

@@ -413,18 +413,19 @@ awq_status_t awq_gemm_packed_ex(const void* x, const void* packed, const void* b
  * tile-packed weights, for routed batches of prefill size (vLLM article, section 5.4: routed
  * expert layers).  packed holds E tile-packed layouts of 4-bit experts back to back, expert
  * e's at byte e * awq_repack_size(K, N, group_size) (awq_repack of qweight[e], qzeros[e],
- * scales[e] into that slice); x_f16 fp16 [R, K] routed rows sorted by expert, expert_offsets
- * DEVICE int32 [E + 1] as for awq_gemm_grouped (read on the device only), bias_f16 fp16
- * [E, N] or NULL, y_f16 fp16 [R, N].  One persistent launch over (expert, 256-row tile,
+ * scales[e] into that slice); x [R, K] routed rows sorted by expert, expert_offsets DEVICE
+ * int32 [E + 1] as for awq_gemm_grouped (read on the device only), bias [E, N] or NULL,
+ * y [R, N]; x, bias, y (and the scales the layouts were written from) fp16 (dtype
+ * AWQ_DTYPE_F16) or bf16 (AWQ_DTYPE_BF16, as awq_gemm_packed_ex).  One persistent launch over (expert, 256-row tile,
  * column tile); a tile's rows of the next expert are computed and discarded.  Requirements:
  * those of awq_gemm_packed, 1 <= E <= 256, E*K*N < 2^40.  Offsets outside [0, R] or not
  * rising give unspecified values in y but never an access outside x, y, bias or packed.
  * R == 0 or N == 0: AWQ_OK, no launch.
  */
-awq_status_t awq_gemm_packed_grouped(const void* x_f16, const void* packed, const void* bias_f16,
+awq_status_t awq_gemm_packed_grouped(const void* x, const void* packed, const void* bias,
                                      const int32_t* expert_offsets, int64_t R, int64_t E,
-                                     int64_t K, int64_t N, int64_t group_size, void* y_f16,
-                                     awq_stream_t stream);
+                                     int64_t K, int64_t N, int64_t group_size, void* y,
+                                     awq_dtype_t dtype, awq_stream_t stream);
 
 awq_status_t awq_repack_w8_size(int64_t K, int64_t N, int64_t group_size, size_t* bytes);
 awq_status_t awq_repack_w8(const int32_t* qweight, const int32_t* qzeros, const void* scales_f16,

@@ -167,15 +167,19 @@ def workload_inputs(name: str, dtype: str = "f16") -> dict:
 
 
 def moe_inputs(seed: int, T: int, topk: int, E: int, K: int, N: int, group_size: int = 128,
-               bias: bool = False) -> dict:
+               bias: bool = False, dtype: str = "f16") -> dict:
     """Synthetic mixture-of-experts layer: E experts' AWQ linears (each drawn as
     awq_linear, seeds seed + 1 + e) and T tokens each routed to topk distinct experts
     drawn uniformly; the routed rows (token copies) are sorted by expert (stable), so
     expert e owns rows offsets[e] .. offsets[e+1]-1.  Returns x [T*topk, K] fp16,
     qweight [E, K, N/8], qzeros [E, K/G, N/8], scales [E, K/G, N], bias [E, N] or None,
-    offsets int32 [E+1], token_of_row, plus the sizes."""
+    offsets int32 [E+1], token_of_row, plus the sizes.  dtype="bf16": x, scales and bias
+    rounded to bf16 instead (fp32 arrays holding bf16 values, as awq_linear)."""
+    if dtype not in ("f16", "bf16"):
+        raise ValueError("dtype must be 'f16' or 'bf16'")
+    half = np.float16 if dtype == "f16" else _to_bf16
     rng = np.random.Generator(np.random.PCG64(seed))
-    tokens = rng.standard_normal((T, K), dtype=np.float32).astype(np.float16)
+    tokens = half(rng.standard_normal((T, K), dtype=np.float32))
     choice = np.stack([rng.permutation(E)[:topk] for _ in range(T)])   # [T, topk]
     expert_of_row = choice.reshape(-1)
     token_of_row = np.repeat(np.arange(T), topk)
@@ -183,7 +187,7 @@ def moe_inputs(seed: int, T: int, topk: int, E: int, K: int, N: int, group_size:
     expert_of_row, token_of_row = expert_of_row[order], token_of_row[order]
     counts = np.bincount(expert_of_row, minlength=E)
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
-    ex = [awq_linear(seed + 1 + e, 1, K, N, group_size=group_size, bias=bias) for e in range(E)]
+    ex = [awq_linear(seed + 1 + e, 1, K, N, group_size=group_size, bias=bias, dtype=dtype) for e in range(E)]
     return {"x": np.ascontiguousarray(tokens[token_of_row]),
             "qweight": np.ascontiguousarray(np.stack([d["qweight"] for d in ex])),
             "qzeros": np.ascontiguousarray(np.stack([d["qzeros"] for d in ex])),

@@ -105,3 +105,56 @@ def test_grouped_packed_exact_case_bitwise(awq):
     y = run_packed(awq, d)
     want = oracle.gemm_grouped(d["x"], d["qweight"], d["qzeros"], d["scales"], None, G, d["offsets"])
     assert np.array_equal(y.view(np.uint16), want.astype(np.float16).view(np.uint16))
+
+
+# bf16 (experts repacked from bf16 scales; x, bias, y bf16).  The packed kernel rounds each
+# dequantized weight once to bf16 for the tensor core, so the reference is the fp64 GEMM of
+# the oracle's bf16-rounded dequant, expert by expert, under the same 1e-2 criterion.
+def run_packed_bf16(awq, d):
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).cuda()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    pk = awq.awq_repack_experts(dev(d["qweight"]), dev(d["qzeros"]), bf(d["scales"]), d["group_size"])
+    y = awq.awq_gemm_packed_grouped(bf(d["x"]), pk, dev(d["offsets"]), d["K"], d["N"],
+                                    None if d["bias"] is None else bf(d["bias"]), group_size=d["group_size"])
+    torch.cuda.synchronize()
+    assert y.dtype == torch.bfloat16
+    return y.float().cpu().numpy()
+
+
+def reference_bf16_rounded(d):
+    off, G = d["offsets"], d["group_size"]
+    y = np.zeros((d["x"].shape[0], d["N"]))
+    for e in range(len(off) - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        W = oracle.dequant_bf16(d["qweight"][e], d["qzeros"][e], d["scales"][e], G).astype(np.float64)
+        y[r0:r1] = d["x"][r0:r1].astype(np.float64) @ W
+        if d["bias"] is not None:
+            y[r0:r1] += d["bias"][e].astype(np.float64)
+    return y
+
+
+@pytest.mark.parametrize("T,topk,E,K,N,G,bias", [(600, 2, 8, 1024, 520, 128, True), (700, 2, 16, 512, 384, -1, False)])
+def test_grouped_packed_bf16_vs_oracle(awq, T, topk, E, K, N, G, bias):
+    d = synth.moe_inputs(32000 + T + E, T, topk, E, K, N, group_size=G, bias=bias, dtype="bf16")
+    y = run_packed_bf16(awq, d)
+    assert np.isfinite(y).all()
+    ok, worst = oracle.within_tolerance(y.astype(np.float64), reference_bf16_rounded(d), 1e-2)
+    assert ok, f"worst |err|/(1e-2*max(1,|ref|)) = {worst:.3f}"
+    assert np.array_equal(run_packed_bf16(awq, d).view(np.uint32), y.view(np.uint32))
+
+
+def test_grouped_packed_bf16_exact_case_bitwise(awq):
+    # exact-arithmetic inputs as in the fp16 case: y is the oracle's value rounded once to bf16
+    E, K, N, G, R = 4, 1024, 384, 128, 700
+    ex = [synth.awq_linear(32600 + e, 1, K, N, group_size=G, bias=True, x_kind="smallint", scale_kind="pow2",
+                           bias_kind="dyadic", dtype="bf16") for e in range(E)]
+    x = synth.awq_linear(32650, R, K, N, group_size=G, x_kind="smallint", scale_kind="pow2", dtype="bf16")["x"]
+    d = {"x": x, "qweight": np.stack([a["qweight"] for a in ex]), "qzeros": np.stack([a["qzeros"] for a in ex]),
+         "scales": np.stack([a["scales"] for a in ex]), "bias": np.stack([a["bias"] for a in ex]), "group_size": G,
+         "K": K, "N": N, "offsets": np.array([0, 0, 300, 557, R], dtype=np.int32)}
+    y = run_packed_bf16(awq, d)
+    want = oracle.round_to_bf16(oracle.gemm_grouped(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G,
+                                                     d["offsets"]).astype(np.float32))
+    assert np.array_equal(y.view(np.uint32), want.view(np.uint32))

@@ -51,7 +51,7 @@ SIGNATURES = {
     "awq_gemm_packed_noalloc": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "awq_gemm_packed_ex": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _i32, _vp, ctypes.c_size_t, _vp]),
     "awq_repack_w8_size": (_i32, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
-    "awq_gemm_packed_grouped": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "awq_gemm_packed_grouped": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp, _i32, _vp]),
     "awq_repack_w8": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     "awq_gemm_packed_w8": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, ctypes.c_size_t, _vp]),
 }
@@ -575,8 +575,8 @@ def awq_gemm_packed_noalloc(x, packed, bias, K, N, group_size=128, out=None, str
 
 
 def awq_repack_experts(qweight, qzeros, scales, group_size=128, stream=None):
-    """E experts' 4-bit weights (qweight int32 [E, K, N/8], qzeros [E, K/G, N/8], fp16 scales
-    [E, K/G, N]) into one int32 device tensor of E stacked tile-packed layouts, expert e's at
+    """E experts' 4-bit weights (qweight int32 [E, K, N/8], qzeros [E, K/G, N/8], fp16 or bf16
+    scales [E, K/G, N]) into one int32 device tensor of E stacked tile-packed layouts, expert e's at
     word e * awq_repack_size(K, N, group_size) / 4 (one awq_repack launch per expert)."""
     E, K, C = qweight.shape
     N = 8 * C
@@ -590,13 +590,16 @@ def awq_repack_experts(qweight, qzeros, scales, group_size=128, stream=None):
 
 def awq_gemm_packed_grouped(x, packed, offsets, K, N, bias=None, group_size=128, out=None, stream=None):
     """Grouped (mixture-of-experts) linear on stacked tile-packed experts (awq_repack_experts)
-    via the library's awq_gemm_packed_grouped: rows offsets[e]..offsets[e+1]-1 of x fp16 [R, K]
-    through expert e; offsets int32 [E+1] on the device, bias fp16 [E, N] or None.  Returns fp16
-    [R, N]."""
+    via the library's awq_gemm_packed_grouped: rows offsets[e]..offsets[e+1]-1 of x [R, K]
+    through expert e; offsets int32 [E+1] on the device, bias [E, N] or None; x, bias and the
+    result fp16, or bf16 (experts repacked from bf16 scales).  Returns [R, N] in x's dtype."""
     lib = load_library()
     R = x.shape[0]
     dev = _cuda_index(x, "x")
-    _need(x, "x", torch.float16, (R, K), dev)
+    dt = x.dtype
+    if dt not in (torch.float16, torch.bfloat16):
+        raise TypeError("x must be float16 or bfloat16")
+    _need(x, "x", dt, (R, K), dev)
     words = awq_repack_size(K, N, group_size) // 4
     if packed.numel() % words != 0:
         raise ValueError("packed must hold whole experts' tile-packed layouts")
@@ -604,11 +607,12 @@ def awq_gemm_packed_grouped(x, packed, offsets, K, N, bias=None, group_size=128,
     _need(packed, "packed", torch.int32, (E * words,), dev)
     _need(offsets, "offsets", torch.int32, (E + 1,), dev)
     if bias is not None:
-        _need(bias, "bias", torch.float16, (E, N), dev)
+        _need(bias, "bias", dt, (E, N), dev)
     if out is None:
-        out = torch.empty((R, N), dtype=torch.float16, device=dev)
+        out = torch.empty((R, N), dtype=dt, device=dev)
     else:
-        _need(out, "out", torch.float16, (R, N), dev)
+        _need(out, "out", dt, (R, N), dev)
     _check(lib.awq_gemm_packed_grouped(_ptr(x), _ptr(packed), _ptr(bias), _ptr(offsets), R, E, K, N,
-                                       group_size, _ptr(out), _stream(stream)))
+                                       group_size, _ptr(out), DTYPE_BF16 if dt is torch.bfloat16 else DTYPE_F16,
+                                       _stream(stream)))
     return out

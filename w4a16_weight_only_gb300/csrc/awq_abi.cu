@@ -612,14 +612,18 @@ awq_status_t awq_gemm_packed_w8(const void* x_f16, const void* packed, const voi
   return ok();
 }
 
-awq_status_t awq_gemm_packed_grouped(const void* x_f16, const void* packed, const void* bias_f16,
+awq_status_t awq_gemm_packed_grouped(const void* x, const void* packed, const void* bias,
                                      const int32_t* expert_offsets, int64_t R, int64_t E, int64_t K,
-                                     int64_t N, int64_t group_size, void* y_f16, awq_stream_t stream) {
+                                     int64_t N, int64_t group_size, void* y, awq_dtype_t dtype,
+                                     awq_stream_t stream) {
+  if (dtype != AWQ_DTYPE_F16 && dtype != AWQ_DTYPE_BF16)
+    return fail(AWQ_ERR_INVALID_ARGUMENT, "dtype must be AWQ_DTYPE_F16 or AWQ_DTYPE_BF16");
   if (E <= 0 || E > awq::kPackedGroupedMaxE)
     return fail(AWQ_ERR_INVALID_ARGUMENT, "E must be in 1..%d (got %lld)", awq::kPackedGroupedMaxE, (long long)E);
   awq::GemmProblem p{};
   bool launch = false;
-  awq_status_t st = packed_problem(x_f16, packed, bias_f16, R, K, N, group_size, y_f16, stream, &p, &launch);
+  awq_status_t st = packed_problem(x, packed, bias, R, K, N, group_size, y, stream, &p, &launch,
+                                   dtype == AWQ_DTYPE_BF16);
   if (st != AWQ_OK || !launch) return st;
   if (K * N * E >= kProdLimit) return fail(AWQ_ERR_UNSUPPORTED_SHAPE, "E*K*N must be below 2^40");
   if (!expert_offsets) return fail(AWQ_ERR_INVALID_ARGUMENT, "null expert_offsets");

@@ -103,7 +103,7 @@ cudaError_t launch_repack8(const uint32_t* qw, const uint32_t* qz, const __half*
 // with M > 128 whose tiles fill the SMs poorly run the stream-K kernel.
 size_t packed_workspace_bytes(int sms);
 size_t packed_workspace_flag_bytes(int sms);  // the leading flag area of that workspace
-// Grouped (mixture-of-experts) linear on E stacked 4-bit packed layouts, fp16: p.offsets
+// Grouped (mixture-of-experts) linear on E stacked 4-bit packed layouts, fp16 or bf16 (p.bf16): p.offsets
 // (device, E + 1) and p.E (1 .. kPackedGroupedMaxE) as for launch_decode_grouped, p.M = R.
 constexpr int kPackedGroupedMaxE = 256;
 cudaError_t launch_packed_grouped(const GemmProblem& p, const void* packed);

@@ -1731,14 +1731,16 @@ cudaError_t launch_repack(const uint32_t* qw, const uint32_t* qz, const __half* 
 
 size_t packed_workspace_flag_bytes(int sms) { return sk_flag_bytes(sms); }
 
-cudaError_t launch_packed_grouped(const GemmProblem& p, const void* packed) {
+namespace {
+template <bool kBF>
+cudaError_t launch_grouped_t(const GemmProblem& p, const void* packed) {
   using CF = Cfg<256, 1, 4>;
   static_assert(CF::USED + kGrpBytes <= kSmemCap, "grouped: tile-start table after the ring");
   constexpr int kSmem = CF::SMEM + kGrpBytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(packed_kernel<256, 1, false, false, 4, true>,
+    attr_err = cudaFuncSetAttribute(packed_kernel<256, 1, false, kBF, 4, true>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -1751,8 +1753,8 @@ cudaError_t launch_packed_grouped(const GemmProblem& p, const void* packed) {
   pp.M = p.M; pp.K = p.K; pp.N = p.N;
   pp.y_vec = (aligned(p.y, 16) && p.N % 8 == 0) ? 1 : 0;
   const char* why = nullptr;
-  if (!make_tmap_2d(&pp.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, 256,
-                    CU_TENSOR_MAP_SWIZZLE_128B, &why))
+  if (!make_tmap_2d(&pp.tm_x, kBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    p.x, p.K, p.M, kTK, 256, CU_TENSOR_MAP_SWIZZLE_128B, &why))
     return cudaErrorInvalidValue;
   const int NT = (p.N + kTN - 1) / kTN, KS = p.K / kTK;
   pp.offsets = p.offsets;
@@ -1766,8 +1768,13 @@ cudaError_t launch_packed_grouped(const GemmProblem& p, const void* packed) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long grid = tmax < sms ? tmax : sms;
-  packed_kernel<256, 1, false, false, 4, true><<<static_cast<unsigned>(grid), kThreads, kSmem, p.stream>>>(pp);
+  packed_kernel<256, 1, false, kBF, 4, true><<<static_cast<unsigned>(grid), kThreads, kSmem, p.stream>>>(pp);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_packed_grouped(const GemmProblem& p, const void* packed) {
+  return p.bf16 ? launch_grouped_t<true>(p, packed) : launch_grouped_t<false>(p, packed);
 }
 
 size_t packed_workspace_bytes(int sms) {
