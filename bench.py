@@ -814,6 +814,22 @@ def run_sweep(args, local):
                          "mode": "static weights (prepared layers)",
                          "default_order_us": t_def, "default_order_GB_s": nbytes / t_def / 1e3,
                          "weight_copies": R, "launches_per_graph": calls})
+            if K % 64 == 0 and (G == -1 or G % 64 == 0):
+                # the tile-packed copies (what AwqLinear(packed=True) calls), replayed the same
+                # way; GB/s of the same algorithmic bytes, so the times compare directly
+                pks = [awq.awq_repack(w[0], w[1], w[2], G, stream=stream) for w in sets]
+                torch.cuda.synchronize()
+                with torch.cuda.stream(stream):
+                    for i in range(3 * R):
+                        awq.awq_gemm_packed(x, pks[i % R], bias, K, N, G, out=y, stream=stream)
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        for i in range(calls):
+                            awq.awq_gemm_packed(x, pks[i % R], bias, K, N, G, out=y, stream=stream)
+                t_p = sorted(timed(g.replay, 1) / calls for _ in range(5))[2]
+                del g, pks
+                line.update({"packed_us": t_p, "packed_GB_s": nbytes / t_p / 1e3,
+                             "packed_frac_hbm": nbytes / t_p / 1e3 / hbm})
             del sets
         else:
             fn = lambda: awq.awq_gemm(x, qw, qz, sc, bias, group_size=G, out=y, stream=stream)

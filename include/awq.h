@@ -312,7 +312,8 @@ awq_path_t awq_gemm_select_path_ex(int64_t M, int64_t K, int64_t N, int64_t grou
  *   [M, N]; fp32 accumulation, a fixed summation order: repeated calls are bitwise
  *   identical; |y - y_exact| <= 1e-2 * max(1, |y_exact|)).  A tcgen05 kernel whose
  *   dequantized weights stay in tensor memory; built for prefill-sized M (any M >= 1 runs;
- *   small M is faster through awq_gemm on the checkpoint layout).  M == 0 or N == 0:
+ *   below 128 rows awq_gemm on the checkpoint layout is mostly faster, except near 32 rows
+ *   on wide linears).  M == 0 or N == 0:
  *   AWQ_OK, no launch.  One kernel launch otherwise, asynchronous on `stream`, plain stream
  *   order.
  */

@@ -168,7 +168,8 @@ def test_bf16_rejects_mixed_dtypes(awq):
 # AWQ_DTYPE_BF16): the kernels round each dequantized weight once to bf16, so the reference is
 # the fp64 GEMM of the oracle's bf16-rounded dequant.  Shapes: narrow split tiles, the 256-row
 # kernel with ragged rows and columns, stream-K (through a workspace), the pair kernel (K = 8192).
-PACKED_BF = [(40, 1024, 512, 128, True, None), (300, 1024, 264, 64, True, None),
+PACKED_BF = [(1, 1024, 520, 128, True, None), (16, 2048, 264, 64, True, None), (32, 4096, 1032, -1, False, None),
+             (40, 1024, 512, 128, True, None), (300, 1024, 264, 64, True, None),
              (257, 4096, 2048, 128, True, "ws"), (300, 8192, 512, 128, False, None),
              (700, 512, 1032, -1, True, None)]
 
@@ -209,7 +210,8 @@ def test_gemm_packed_bf16_vs_oracle(awq, M, K, N, G, bias, ws):
     assert torch.equal(y, y2)
 
 
-@pytest.mark.parametrize("M,K,N,ws", [(300, 2048, 384, None), (257, 4096, 2048, "ws"), (64, 2048, 384, None)])
+@pytest.mark.parametrize("M,K,N,ws", [(300, 2048, 384, None), (257, 4096, 2048, "ws"), (64, 2048, 384, None),
+                                      (32, 4096, 520, None), (5, 2048, 384, None)])
 def test_gemm_packed_bf16_exact_case_bitwise(awq, M, K, N, ws):
     # exact-arithmetic inputs: every weight (c - z) * 2^k and every partial sum is exact, so y
     # is the oracle's value rounded once to bf16 whatever the kernel's summation order

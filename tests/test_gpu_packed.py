@@ -97,21 +97,6 @@ def test_gemm_packed_long_k_pairs(awq, M, K, N):
                  f"packed M={M} K={K} N={N}")
 
 
-@pytest.mark.parametrize("M,K,N", [(300, 8192, 512), (256, 8192, 256), (512, 8192, 384), (260, 4096, 512)])
-def test_gemm_packed_long_k_pairs(awq, M, K, N):
-    # K >= 8192 with an even number of 128-column tiles runs the two-CTA (cta_group::2) kernel,
-    # an odd number (N = 384) and K = 4096 the single-CTA one; exact-arithmetic inputs make
-    # both bitwise checkable, random ones check the tolerance
-    d = synth.awq_linear(23200 + M + N, M, K, N, group_size=128, bias=True, x_kind="smallint",
-                         scale_kind="pow2", bias_kind="dyadic")
-    y = run(awq, d)
-    want = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128).astype(np.float16)
-    assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
-    d = synth.awq_linear(23300 + M + N, M, K, N, group_size=128, bias=True)
-    assert_close(run(awq, d), oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128),
-                 f"packed M={M} K={K} N={N}")
-
-
 # narrow token tiles (32 / 64 / 128 rows) with K split over clusters of 2 or 4 CTAs, chosen by
 # tile count: 8 tiles of 32 rows (4-way), 4 of 64 (2-way), 8 of 128 (2-way), an uneven split
 # (K = 4160: 65 stages), a persistent unsplit launch (N = 28672: 224 tiles)
@@ -142,6 +127,35 @@ def test_gemm_packed_narrow_split_exact_bitwise(awq, M):
                          scale_kind="pow2", bias_kind="dyadic")
     y = run(awq, d)
     want = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 128).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
+
+
+# Small batches (M <= 32: 16- or 32-row token tiles, several CTAs per SM, K split over a
+# cluster of 1 .. 16 CTAs, each rank finishing a slice of the columns): one stage in all (no
+# split), two, five (a 5-CTA cluster), a 16-CTA cluster (few column tiles), ragged column
+# tiles, G = 64 / 128 / -1, the 7B shapes
+SMALLB = [(1, 64, 128, 64, True), (2, 128, 136, 64, False), (5, 320, 264, 64, True), (16, 4096, 512, 128, True),
+          (17, 1024, 1032, -1, True), (31, 2048, 384, 128, False), (32, 4096, 11008, 128, True),
+          (16, 11008, 4096, 128, False), (8, 4096, 4096, 128, True)]
+
+
+@pytest.mark.parametrize("M,K,N,G,bias", SMALLB)
+def test_gemm_packed_small_batch(awq, M, K, N, G, bias):
+    d = synth.awq_linear(24000 + M + K + N, M, K, N, group_size=G, bias=bias)
+    y = run(awq, d)
+    assert_close(y, oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], G),
+                 f"packed small M={M} K={K} N={N} G={G}")
+    assert np.array_equal(run(awq, d).view(np.uint16), y.view(np.uint16))  # fixed reduction order
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 4096, 520), (16, 4096, 520), (17, 1024, 4096), (32, 4096, 520), (32, 320, 136)])
+def test_gemm_packed_small_batch_exact_bitwise(awq, M, K, N):
+    # exact-arithmetic inputs: every rank's partial sums are exact in fp32, so y is the
+    # oracle's value rounded once to fp16 whatever the cluster size
+    d = synth.awq_linear(24500 + M + K, M, K, N, group_size=64, bias=True, x_kind="smallint",
+                         scale_kind="pow2", bias_kind="dyadic")
+    y = run(awq, d)
+    want = oracle.gemm(d["x"], d["qweight"], d["qzeros"], d["scales"], d["bias"], 64).astype(np.float16)
     assert np.array_equal(y.view(np.uint16), want.view(np.uint16))
 
 

@@ -37,7 +37,9 @@
 // a cluster (few rows), 256-row tiles (one accumulator; y staged through shared memory as
 // 16-byte stores), stream-K over one CTA per SM with a caller workspace (tiles that fill the
 // SMs poorly), a two-CTA cta_group::2 kernel (long K), bf16 activations and scales, 8-bit codes
-// (their own block layout, below), and a grouped mode over stacked experts' layouts.
+// (their own block layout, below), and a grouped mode over stacked experts' layouts.  4-bit
+// launches of at most 32 rows take a kernel of their own (packed_small_kernel: four
+// independent pipelines per CTA, below).
 //
 // 8-bit codes: the same tiles and meta words (8-bit zeros), 2176-word blocks: word
 // 1024 h + 512 k + 4 c + j holds column c's codes for rows 32 h + 16 k + 4 j + 0..3, one
@@ -378,7 +380,8 @@ constexpr uint32_t idesc_ts() {
 // shared memory holds, per slot, the activation tile and the packed block (one ring: slot s
 // carries stage j's activations, packed block and A operand, j = s mod ST), plus, in rank 0 of
 // a split, the other ranks' partial sums.  Narrow tiles (BT <= 64) allocate 256 TMEM columns
-// and at most half an SM's shared memory, so two CTAs share an SM.
+// and at most half an SM's shared memory, so two CTAs share an SM (per-CTA %smid and
+// globaltimer stamps show two resident at once; the occupancy calculator reports one).
 template <int BT, int SPLIT, int BITS = 4>
 struct Cfg {
   static constexpr int NACC = BT >= 256 ? 1 : 2;
@@ -1212,6 +1215,307 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
   }
 }
 
+// ------------------------------------------------------------ small batches ----
+// Token tiles of 16 or 32 rows (M <= 32, 4-bit codes).  A 32-row tile gives the tensor core
+// about 32 cycles of work a stage, far less than the issue cost of the stage's own async
+// instructions on one thread (each tcgen05.mma, commit, bulk copy or barrier wait takes
+// some 60-100 cycles to issue, measured with clock stamps), so one pipeline per SM leaves
+// the SM idle.  A CTA here (one per SM: it takes all 512 TMEM columns and nearly all shared
+// memory) runs P independent pipelines side by side, each with its own producer
+// thread (one TMA copy and one bulk copy per stage), MMA-issuing thread, four dequant warps
+// (one per TMEM lane quadrant), ring of ST shared-memory stages, SA A slots and accumulator
+// in its own 128 TMEM columns.  Pipeline j takes the j-th quarter of the CTA's K stages; the
+// dequant warps of pipeline 0 add the P accumulators in order.  The K loop of one 128-column
+// tile is further split over a cluster of CS CTAs (1 .. 16, set at launch so the grid is
+// resident in one wave); rank r finishes output columns [128 r / CS, 128 (r + 1) / CS): the
+// other ranks push their fp32 sums of those columns into its shared memory (st.async,
+// counted on one barrier) and it adds all CS partials in rank order (bitwise repeatable),
+// adds the bias and stores y.
+constexpr int kSmallPipes = 4;
+constexpr int kSmallThreads = kSmallPipes * 6 * 32;
+constexpr int kSmallMaxCS = 16;
+template <int BT>
+struct SmallCfg {
+  static_assert(BT == 16 || BT == 32, "token tiles of 16 or 32 rows");
+  static constexpr int P = kSmallPipes;
+  static constexpr int COLS = 512;                    // 128 per pipeline
+  static constexpr int SA = 3;                        // A slots per pipeline, after its accumulator
+  static constexpr int X_BYTES = BT * kTK * 2;        // 1024-byte multiple (SW128 atoms)
+  static constexpr int RECV_PITCH = BT + 4;           // floats per received column
+  static constexpr int RECV_BYTES = (kTN + kSmallMaxCS) * RECV_PITCH * 4;
+  static constexpr int ST0 = (kSmemCap - 2048 - RECV_BYTES) / (P * (X_BYTES + kBlockBytes));
+  static constexpr int ST = ST0 < 8 ? ST0 : 8;        // ring stages per pipeline
+  static constexpr int X_OFF = 0;                     // x ring of pipeline j, stage s: (j ST + s) X_BYTES
+  static constexpr int B_OFF = P * ST * X_BYTES;
+  static constexpr int BAR_OFF = B_OFF + P * ST * kBlockBytes;
+  // per pipeline: full_t[ST], empty_t[ST], full_a[SA], acc_full; then recv
+  static constexpr int ACC = 2 * ST + SA;             // acc_full's index in a pipeline's barriers
+  static constexpr int NB = ACC + 1;
+  static constexpr int MISC_OFF = BAR_OFF + (P * NB + 1) * 8;
+  static constexpr int RECV_OFF = ((MISC_OFF + 8 + 15) / 16) * 16;
+  static constexpr int SMEM = 1024 + RECV_OFF + RECV_BYTES;
+  static_assert(ST > SA && SMEM <= kSmemCap, "resources");
+  static_assert(32 + SA * 32 <= COLS / P, "TMEM columns");
+};
+
+template <int BT, bool kBF>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    packed_small_kernel(const __grid_constant__ PackedParams p) {
+  using CF = SmallCfg<BT>;
+  constexpr int ST = CF::ST, SA = CF::SA, P = CF::P, NB = CF::NB;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + CF::BAR_OFF);
+  uint64_t* recv_bar = bars_all + P * NB;  // the other ranks' sums of this rank's columns landed
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + CF::MISC_OFF + 4);
+  float* recv = reinterpret_cast<float*>(smem + CF::RECV_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int pipe = warp / 6, role = warp % 6;  // role 0 producer, 1 MMA issuer, 2-5 dequant
+  const int KS = p.K / kTK;
+  const int cs = static_cast<int>(cluster_nctarank());
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int tile = static_cast<int>(blockIdx.x) / cs;  // token tiles fastest
+  const int m0 = (tile % p.tiles_t) * BT;
+  const int nt = tile / p.tiles_t;
+  const int kr0 = KS * rank / cs, kr = KS * (rank + 1) / cs - kr0;  // this rank's stages; KS * 16 < 2^31
+  const int kb0 = kr0 + kr * pipe / P, nst = kr0 + kr * (pipe + 1) / P - kb0;  // this pipeline's
+  const int own_lo = kTN * rank / cs, own_hi = kTN * (rank + 1) / cs;
+  // this pipeline's barriers, ring and TMEM columns
+  uint64_t* bars = bars_all + pipe * NB;
+  uint64_t* full_t = bars;             // activation tile + packed block of the slot landed
+  uint64_t* empty_t = bars + ST;       // slot free: block read by the dequant warps, MMAs done
+  uint64_t* full_a = bars + 2 * ST;    // A slot dequantized
+  uint64_t* acc_full = bars + CF::ACC;  // every MMA of the pipeline done
+  unsigned char* xring = smem + CF::X_OFF + pipe * ST * CF::X_BYTES;
+  unsigned char* bring = smem + CF::B_OFF + pipe * ST * kBlockBytes;
+
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < P; ++j) {
+      uint64_t* b = bars_all + j * NB;
+      for (int s = 0; s < ST; ++s) {
+        mbar_init(&b[s], 1);
+        mbar_init(&b[ST + s], 4 + 1);  // four dequant warps (block read) + the MMA commit
+      }
+      for (int a = 0; a < SA; ++a) mbar_init(&b[2 * ST + a], 4);
+      mbar_init(&b[CF::ACC], 1);
+    }
+    mbar_init(recv_bar, 1);
+    if (cs > 1)  // the other ranks' sums of this rank's columns, one phase
+      mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((cs - 1) * (own_hi - own_lo) * BT * 4));
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(const_cast<uint32_t*>(tmem_slot))), "n"(CF::COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  if (cs > 1) cluster_sync_all();  // every rank's recv barrier exists before any push
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tcol = tmem_base + static_cast<uint32_t>(pipe * (CF::COLS / P));  // accumulator
+
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(bar, parity, p.status, kStatusPackedTimeout, kWaitLimitNs)) return true;
+    *abort_flag = 1u;
+    return false;
+  };
+
+  if (role == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_x);
+      const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
+      const uint32_t* src = p.packed + (static_cast<size_t>(nt) * KS + kb0) * kBlockWords;
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < nst; ++i) {
+        const int s = i % ST;
+        if (!wait(&empty_t[s], static_cast<uint32_t>((i / ST) & 1) ^ 1u)) { ok = false; break; }
+        mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + kBlockBytes));
+        tma_load_2d_hint(xring + s * CF::X_BYTES, &p.tm_x, &full_t[s], (kb0 + i) * kTK, m0, pol_x);
+        bulk_load(bring + s * kBlockBytes, src + static_cast<size_t>(i) * kBlockWords, kBlockBytes, &full_t[s],
+                  pol_w);
+        ++issued;
+      }
+      if (!ok)  // every issued stage's copies land before the CTA may exit
+        for (int i = issued - 1; i >= 0 && i >= issued - ST; --i)
+          mbar_wait_bounded(&full_t[i % ST], static_cast<uint32_t>((i / ST) & 1), p.status, kStatusPackedTimeout,
+                            kWaitLimitNs);
+    }
+  } else if (role == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_ts<BT>() | (kBF ? kIdescBF : 0u);
+      const uint32_t xbase = sbase + static_cast<uint32_t>(xring - smem);
+      // Stages in pairs: one wait on the later stage's full_a covers both (every dequant warp
+      // arrives in stage order, and each arrival releases its TMEM stores of earlier stages).
+      // One commit per stage frees its ring slot; the dequant warps take that as the signal
+      // that the A slot of the same stage is free too.
+      for (int i = 0; i < nst; i += 2) {
+        const int n2 = nst - i < 2 ? nst - i : 2, il = i + n2 - 1;
+        if (!wait(&full_a[il % SA], static_cast<uint32_t>((il / SA) & 1))) break;
+        tc_fence_after();
+        for (int h = 0; h < n2; ++h) {
+          const int s = (i + h) % ST, a = (i + h) % SA;
+          const uint32_t aaddr = tcol + 32u + static_cast<uint32_t>(32 * a);
+          const uint64_t bdesc = sw128_kmajor_desc(xbase + s * CF::X_BYTES);
+#pragma unroll
+          for (int ks = 0; ks < kTK / 16; ++ks)  // K += 16: A 8 TMEM columns, B 32 bytes
+            mma_ts(tcol, aaddr + 8u * ks, bdesc + 2u * ks, idesc, (i + h > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(&empty_t[s]);
+        }
+      }
+      // completes once every MMA issued above is done (after a give-up too: TMEM is freed
+      // only after this wait)
+      mma_commit(acc_full);
+      mbar_wait_bounded(acc_full, 0u, p.status, kStatusPackedTimeout, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ dequant, finish
+    // Thread = output column c of the tile (TMEM lane): per stage its codes of both K halves
+    // (two 16-byte loads) and its meta word, 32 element pairs stored to the stage's A slot.
+    const int q = warp & 3;  // TMEM lanes 32 q .. 32 q + 31
+    const int c = 32 * q + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    bool ok = true;
+    for (int i = 0; i < nst; ++i) {
+      const int s = i % ST, a = i % SA;
+      if (!wait(&full_t[s], static_cast<uint32_t>((i / ST) & 1))) { ok = false; break; }
+      StageCodes<4> c0, c1;
+      const unsigned char* blk = bring + s * kBlockBytes;
+      load_codes<4>(blk, 0, c, c0);
+      c1.a = *reinterpret_cast<const uint4*>(blk + 16 * (128 + c));
+      c1.meta = c0.meta;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_t[s]);  // the block is read; the MMAs commit the rest
+      // A slot a was last read by stage i - SA, whose MMAs complete the phase of its ring slot
+      // (that slot cannot move on before this warp's arrival for stage i - SA + ST > i)
+      if (i >= SA && !wait(&empty_t[(i - SA) % ST], static_cast<uint32_t>(((i - SA) / ST) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();  // the TMEM stores below come after the slot's previous MMAs
+      uint32_t v[16];
+      convert_codes<4, kBF>(c0, v);
+      tmem_st16(tcol + lane_addr + 32u + static_cast<uint32_t>(32 * a), v);
+      convert_codes<4, kBF>(c1, v);
+      tmem_st16(tcol + lane_addr + 48u + static_cast<uint32_t>(32 * a), v);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full_a[a]);
+    }
+    if (pipe == 0) {
+      // Finish: column c's BT sums over the pipelines (in order), pushed to the rank that
+      // finishes column c, or added there.
+      float acc[BT];
+#pragma unroll
+      for (int j = 0; j < BT; ++j) acc[j] = 0.f;
+      for (int j = 0; j < P; ++j) {
+        if (ok) ok = wait(bars_all + j * NB + CF::ACC, 0u);
+        tc_fence_after();
+        const int nj = kr0 + kr * (j + 1) / P - (kr0 + kr * j / P);  // pipeline j's stages
+        uint32_t v[32];
+        const uint32_t ta = tmem_base + static_cast<uint32_t>(j * (CF::COLS / P)) + lane_addr;
+        if constexpr (BT == 32) {
+          tmem_ld32_nowait(ta, v);
+        } else {
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+              : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+              : "r"(ta)
+              : "memory");
+#pragma unroll
+          for (int jj = 16; jj < 32; ++jj) v[jj] = 0u;
+        }
+        tmem_wait_ld(v);
+        if (ok && nj > 0) {
+#pragma unroll
+          for (int jj = 0; jj < BT; ++jj) acc[jj] += __uint_as_float(v[jj]);
+        }
+      }
+      const int wmax = (kTN + cs - 1) / cs;
+      const bool mine = c >= own_lo && c < own_hi;
+      if (!mine) {
+        int r = c * cs / kTN;  // the rank whose columns hold c
+        while (kTN * (r + 1) / cs <= c) ++r;
+        while (kTN * r / cs > c) --r;
+        const uint32_t rbar = cluster_addr(recv_bar, static_cast<uint32_t>(r));
+        const uint32_t rdst = cluster_addr(recv + (rank * wmax + (c - kTN * r / cs)) * CF::RECV_PITCH,
+                                           static_cast<uint32_t>(r));
+#pragma unroll
+        for (int j = 0; j < BT; j += 4)
+          st_async_v4_at(rdst + static_cast<uint32_t>(4 * j), rbar, __float_as_uint(acc[j]),
+                         __float_as_uint(acc[j + 1]), __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
+      } else {
+        bool have = true;
+        if (cs > 1) {
+          have = mbar_try_wait_cl(recv_bar, 0u);
+          if (!have && *abort_flag == 0u) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!(have = mbar_try_wait_cl(recv_bar, 0u))) {
+              if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                atomicOr(p.status, kStatusPackedTimeout);
+                *abort_flag = 1u;
+                break;
+              }
+            }
+          }
+        }
+        const int n = nt * kTN + c;
+        if (have && n < p.N) {
+          float sum[BT];
+#pragma unroll
+          for (int j = 0; j < BT; ++j) sum[j] = 0.f;
+          for (int r = 0; r < cs; ++r) {  // rank order
+            if (r == rank) {
+#pragma unroll
+              for (int j = 0; j < BT; ++j) sum[j] += acc[j];
+            } else {
+              const float* src = recv + (r * wmax + (c - own_lo)) * CF::RECV_PITCH;
+#pragma unroll
+              for (int j = 0; j < BT; j += 4) {
+                const float4 q4 = *reinterpret_cast<const float4*>(src + j);
+                sum[j] += q4.x;
+                sum[j + 1] += q4.y;
+                sum[j + 2] += q4.z;
+                sum[j + 3] += q4.w;
+              }
+            }
+          }
+          const float bias = p.bias != nullptr ? load_bias<kBF>(p.bias, n) : 0.f;
+          uint16_t* yp = reinterpret_cast<uint16_t*>(p.y) + static_cast<size_t>(m0) * p.N + n;
+#pragma unroll
+          for (int j = 0; j < BT; ++j)
+            if (m0 + j < p.M) yp[static_cast<size_t>(j) * p.N] = float_to_elem<kBF>(sum[j] + bias);
+        }
+      }
+    }
+  }
+
+  // no rank leaves while another may still push into its shared memory (its owners waited,
+  // bounded, for every push), and TMEM is freed after every MMA completed
+  __syncthreads();
+  if (cs > 1) cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(CF::COLS)
+                 : "memory");
+  }
+}
+
 // ------------------------------------------------------------------ pair mode ----
 // Large M: a cluster of two CTAs shares one tile of 256 output columns (M = 256 of
 // tcgen05.mma.cta_group::2: each CTA dequantizes its own 128 columns, its own column tile of
@@ -1590,6 +1894,70 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
   return cudaGetLastError();
 }
 
+// Small-batch launch (M <= 32, 4-bit): the largest cluster size (K split) whose grid of
+// tiles x CS CTAs is resident in one wave (occupancy API, cached per device and size), at
+// most kSmallMaxCS and at most the stage count, so every rank has a stage.
+template <int BT, bool kBF>
+cudaError_t launch_small(const PackedParams& base, const GemmProblem& p) {
+  using CF = SmallCfg<BT>;
+  auto kern = packed_small_kernel<BT, kBF>;
+  static std::mutex mu;
+  static int fits[64][kSmallMaxCS + 1];  // resident CTAs at cluster size cs (0: not yet asked)
+  static bool attr_set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  PackedParams pp = base;
+  const char* why = nullptr;
+  if (!make_tmap_2d(&pp.tm_x, kBF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x, p.K, p.M, kTK, BT,
+                    CU_TENSOR_MAP_SWIZZLE_128B, &why))
+    return cudaErrorInvalidValue;
+  pp.tiles_t = (p.M + BT - 1) / BT;
+  const long long tiles = static_cast<long long>(pp.tiles_t) * ((p.N + kTN - 1) / kTN);
+  if (tiles * kSmallMaxCS > 0x7fffffffLL) return cudaErrorInvalidValue;
+  pp.tiles = static_cast<int>(tiles);
+  const int KS = p.K / kTK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kSmallThreads, 1, 1);
+  cfg.dynamicSmemBytes = CF::SMEM;
+  cfg.stream = p.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int cs = 1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+    for (int c = 2; c <= kSmallMaxCS && c <= KS; ++c) {
+      if (fits[dev][c] == 0) {
+        int n = 0;
+        cfg.gridDim = dim3(static_cast<unsigned>(c), 1, 1);
+        attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+          (void)cudaGetLastError();
+          n = 0;
+        }
+        fits[dev][c] = n > 0 ? n * c : -1;
+      }
+      if (fits[dev][c] > 0 && tiles * c <= fits[dev][c]) cs = c;
+    }
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * cs), 1, 1);
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  e = cudaLaunchKernelEx(&cfg, kern, pp);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // Stream-K launch (256-row tiles): one CTA per SM, at least kSkMinUnits stages each.
 size_t sk_flag_bytes(int sms) { return (static_cast<size_t>(sms) * 4 + 255) / 256 * 256; }
 
@@ -1645,7 +2013,7 @@ bool use_stream_k(int M, int K, int N, int sms, bool pair) {
 // Token tile and K split of a launch with M <= 128 rows: the narrowest tile holding M rows
 // (32, 64 or 128), and the largest split (2 or 4 for 32 rows, 2 for 64 and 128) that keeps
 // every CTA resident in one wave (two CTAs per SM below 128-row tiles) with at least four
-// stages each.
+// stages each.  (4-bit launches of at most 32 rows take the small-batch kernel instead.)
 struct PackedPlan {
   int bt = 256, split = 1;
 };
@@ -1669,6 +2037,7 @@ template <bool kBF, int BITS>
 cudaError_t launch_planned(const PackedParams& pp, const GemmProblem& p, void* workspace, size_t workspace_bytes,
                            int sms) {
   const PackedPlan pl = packed_plan(p.M, p.K, p.N, sms);
+  if (BITS == 4 && p.M <= 32) return p.M <= 16 ? launch_small<16, kBF>(pp, p) : launch_small<32, kBF>(pp, p);
   if (pl.bt == 32)
     return pl.split == 4 ? launch_bt<32, 4, kBF, BITS>(pp, p) : pl.split == 2 ? launch_bt<32, 2, kBF, BITS>(pp, p) : launch_bt<32, 1, kBF, BITS>(pp, p);
   if (pl.bt == 64) return pl.split == 2 ? launch_bt<64, 2, kBF, BITS>(pp, p) : launch_bt<64, 1, kBF, BITS>(pp, p);
