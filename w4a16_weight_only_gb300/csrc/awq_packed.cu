@@ -1220,8 +1220,9 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
 // about 32 cycles of work a stage, far less than the issue cost of the stage's own async
 // instructions on one thread (each tcgen05.mma, commit, bulk copy or barrier wait takes
 // some 60-100 cycles to issue, measured with clock stamps), so one pipeline per SM leaves
-// the SM idle.  A CTA here (one per SM: it takes all 512 TMEM columns and nearly all shared
-// memory) runs P independent pipelines side by side, each with its own producer
+// the SM idle.  A CTA here runs P independent pipelines side by side (P = 4: one CTA per SM,
+// all 512 TMEM columns and nearly all shared memory; P = 2: two CTAs per SM, half of each,
+// which lets more CTAs split a tile count that fills the SMs poorly), each with its own producer
 // thread (one TMA copy and one bulk copy per stage), MMA-issuing thread, four dequant warps
 // (one per TMEM lane quadrant), ring of ST shared-memory stages, SA A slots and accumulator
 // in its own 128 TMEM columns.  Pipeline j takes the j-th quarter of the CTA's K stages; the
@@ -1231,19 +1232,22 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
 // other ranks push their fp32 sums of those columns into its shared memory (st.async,
 // counted on one barrier) and it adds all CS partials in rank order (bitwise repeatable),
 // adds the bias and stores y.
-constexpr int kSmallPipes = 4;
-constexpr int kSmallThreads = kSmallPipes * 6 * 32;
 constexpr int kSmallMaxCS = 16;
-template <int BT>
+template <int BT, int NP>
 struct SmallCfg {
   static_assert(BT == 16 || BT == 32, "token tiles of 16 or 32 rows");
-  static constexpr int P = kSmallPipes;
-  static constexpr int COLS = 512;                    // 128 per pipeline
+  static_assert(NP == 2 || NP == 4, "two or four pipelines");
+  static constexpr int P = NP;
+  static constexpr int THREADS = P * 6 * 32;
+  static constexpr int PER_SM = 4 / P;                // CTAs per SM
+  static constexpr int COLS = 128 * P;                // 128 per pipeline
   static constexpr int SA = 3;                        // A slots per pipeline, after its accumulator
   static constexpr int X_BYTES = BT * kTK * 2;        // 1024-byte multiple (SW128 atoms)
   static constexpr int RECV_PITCH = BT + 4;           // floats per received column
   static constexpr int RECV_BYTES = (kTN + kSmallMaxCS) * RECV_PITCH * 4;
-  static constexpr int ST0 = (kSmemCap - 2048 - RECV_BYTES) / (P * (X_BYTES + kBlockBytes));
+  // an SM's shared memory over its CTAs, less the per-CTA reservation
+  static constexpr int CAP = P == 4 ? kSmemCap : 228 * 1024 / PER_SM - 1024;
+  static constexpr int ST0 = (CAP - 2048 - RECV_BYTES) / (P * (X_BYTES + kBlockBytes));
   static constexpr int ST = ST0 < 8 ? ST0 : 8;        // ring stages per pipeline
   static constexpr int X_OFF = 0;                     // x ring of pipeline j, stage s: (j ST + s) X_BYTES
   static constexpr int B_OFF = P * ST * X_BYTES;
@@ -1254,14 +1258,14 @@ struct SmallCfg {
   static constexpr int MISC_OFF = BAR_OFF + (P * NB + 1) * 8;
   static constexpr int RECV_OFF = ((MISC_OFF + 8 + 15) / 16) * 16;
   static constexpr int SMEM = 1024 + RECV_OFF + RECV_BYTES;
-  static_assert(ST > SA && SMEM <= kSmemCap, "resources");
+  static_assert(ST > SA && SMEM <= CAP, "resources");
   static_assert(32 + SA * 32 <= COLS / P, "TMEM columns");
 };
 
-template <int BT, bool kBF>
-__global__ void __launch_bounds__(kSmallThreads, 1)
+template <int BT, int NP, bool kBF>
+__global__ void __launch_bounds__(SmallCfg<BT, NP>::THREADS, SmallCfg<BT, NP>::PER_SM)
     packed_small_kernel(const __grid_constant__ PackedParams p) {
-  using CF = SmallCfg<BT>;
+  using CF = SmallCfg<BT, NP>;
   constexpr int ST = CF::ST, SA = CF::SA, P = CF::P, NB = CF::NB;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -1894,18 +1898,105 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
   return cudaGetLastError();
 }
 
-// Small-batch launch (M <= 32, 4-bit): the largest cluster size (K split) whose grid of
-// tiles x CS CTAs is resident in one wave (occupancy API, cached per device and size), at
-// most kSmallMaxCS and at most the stage count, so every rank has a stage.
+// Small-batch launch (M <= 32, 4-bit).  Clusters of c CTAs placeable at one CTA per SM come
+// from the occupancy API on the four-pipeline kernel (whose resources allow one per SM; the
+// API reports one per SM for every kernel that allocates tensor memory, so the two-pipeline
+// kernel counts twice that, as measured).  Per variant the cluster size is the largest
+// (at most kSmallMaxCS and the stage count) whose grid of tiles x c CTAs is resident in one
+// wave; the variant is the one whose busiest SM has the least work: four pipelines each take
+// about 800 cycles a stage when four share an SM, two alone about 650.
+struct SmallPlan {
+  int np = 4, cs = 1;
+};
+template <int BT, int NP, bool kBF>
+cudaError_t small_attrs(int dev) {
+  using CF = SmallCfg<BT, NP>;
+  static std::mutex mu;
+  static bool set[64];
+  std::lock_guard<std::mutex> lock(mu);
+  if (set[dev]) return cudaSuccess;
+  auto kern = packed_small_kernel<BT, NP, kBF>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) set[dev] = true;
+  return e;
+}
+template <int BT, bool kBF>
+cudaError_t small_plan(int dev, long long tiles, int KS, int sms, SmallPlan* out) {
+  using C4 = SmallCfg<BT, 4>;
+  static std::mutex mu;
+  static int fits[64][kSmallMaxCS + 1];  // clusters of c CTAs x c at one CTA per SM (0: not asked)
+  cudaError_t e = small_attrs<BT, 4, kBF>(dev);
+  if (e == cudaSuccess) e = small_attrs<BT, 2, kBF>(dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int c = 1; c <= kSmallMaxCS && c <= KS; ++c) {
+    if (fits[dev][c] != 0) continue;
+    if (c == 1) { fits[dev][c] = sms; continue; }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(c), 1, 1);
+    cfg.blockDim = dim3(C4::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C4::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, packed_small_kernel<BT, 4, kBF>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    fits[dev][c] = n > 0 ? n * c : -1;
+  }
+  double best = 0.0;
+  for (int np : {4, 2}) {
+    const int per_sm = 4 / np;
+    int cs = 1;
+    for (int c = 2; c <= kSmallMaxCS && c <= KS; ++c)
+      if (fits[dev][c] > 0 && tiles * c <= static_cast<long long>(per_sm) * fits[dev][c]) cs = c;
+    const long long ctas = tiles * cs;
+    const double waves = static_cast<double>((ctas + static_cast<long long>(per_sm) * sms - 1) / (static_cast<long long>(per_sm) * sms));
+    const double stages = static_cast<double>((KS + cs - 1) / cs);
+    // cycles on the busiest SM: four pipelines at ~800 a stage; two alone at ~650
+    const bool shared = np == 4 || ctas > sms;
+    const double cost = waves * stages * (np == 4 ? 200.0 : (shared ? 400.0 : 325.0));
+    if (np == 4 || cost < best) {
+      best = cost;
+      out->np = np;
+      out->cs = cs;
+    }
+  }
+  return cudaSuccess;
+}
+
+template <int BT, int NP, bool kBF>
+cudaError_t launch_small_np(const PackedParams& pp, const GemmProblem& p, int cs) {
+  using CF = SmallCfg<BT, NP>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(pp.tiles) * cs), 1, 1);
+  cfg.blockDim = dim3(CF::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = CF::SMEM;
+  cfg.stream = p.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_small_kernel<BT, NP, kBF>, pp);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int BT, bool kBF>
 cudaError_t launch_small(const PackedParams& base, const GemmProblem& p) {
-  using CF = SmallCfg<BT>;
-  auto kern = packed_small_kernel<BT, kBF>;
-  static std::mutex mu;
-  static int fits[64][kSmallMaxCS + 1];  // resident CTAs at cluster size cs (0: not yet asked)
-  static bool attr_set[64];
-  int dev = 0;
+  int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   PackedParams pp = base;
@@ -1917,45 +2008,10 @@ cudaError_t launch_small(const PackedParams& base, const GemmProblem& p) {
   const long long tiles = static_cast<long long>(pp.tiles_t) * ((p.N + kTN - 1) / kTN);
   if (tiles * kSmallMaxCS > 0x7fffffffLL) return cudaErrorInvalidValue;
   pp.tiles = static_cast<int>(tiles);
-  const int KS = p.K / kTK;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kSmallThreads, 1, 1);
-  cfg.dynamicSmemBytes = CF::SMEM;
-  cfg.stream = p.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int cs = 1;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!attr_set[dev]) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
-      if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-      attr_set[dev] = true;
-    }
-    for (int c = 2; c <= kSmallMaxCS && c <= KS; ++c) {
-      if (fits[dev][c] == 0) {
-        int n = 0;
-        cfg.gridDim = dim3(static_cast<unsigned>(c), 1, 1);
-        attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-          (void)cudaGetLastError();
-          n = 0;
-        }
-        fits[dev][c] = n > 0 ? n * c : -1;
-      }
-      if (fits[dev][c] > 0 && tiles * c <= fits[dev][c]) cs = c;
-    }
-  }
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles * cs), 1, 1);
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-  e = cudaLaunchKernelEx(&cfg, kern, pp);
+  SmallPlan pl;
+  e = small_plan<BT, kBF>(dev, tiles, p.K / kTK, sms, &pl);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return pl.np == 2 ? launch_small_np<BT, 2, kBF>(pp, p, pl.cs) : launch_small_np<BT, 4, kBF>(pp, p, pl.cs);
 }
 
 // Stream-K launch (256-row tiles): one CTA per SM, at least kSkMinUnits stages each.
