@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
   static_assert(NW == 4 || NW == 8, "4 or 8 warps per CTA");
   constexpr uint32_t kOne2 = kBF ? 0x3F803F80u : kOnes;     // 1.0 in both halves
   constexpr uint32_t kMag = kBF ? 0x43004300u : kMagic;     // 128 (bf16) / 1024 (fp16)
+  constexpr uint32_t kMag64 = 0x54005400u;                   // fp16 64 in both halves
   constexpr float kBias = kBF ? 128.f : 0.f;                 // offset the operand carries
   using GE = Geo<TB, CWL, NW, BITS>;
   constexpr int NMMA = GE::NMMA;
@@ -521,7 +522,10 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
           } else {
 #pragma unroll
             for (int nib = 0; nib < 4; ++nib) {
-              zp[kSub ? 0 : hb][nib] = and_or(zd >> (4 * nib), 0x000F000Fu, kMag);
+              // fp16: odd nibbles stay in bits 4-7 under the exponent of 64 (the operand below)
+              zp[kSub ? 0 : hb][nib] = (kBF || !(nib & 1))
+                                           ? and_or(zd >> (4 * nib), 0x000F000Fu, kMag)
+                                           : and_or(zd >> (4 * nib - 4), 0x00F000F0u, kMag64);
               sp[kSub ? 0 : hb][nib] = prmt(sv[hb][nib >> 1], 0u, (nib & 1) ? 0x3232u : 0x1010u);
             }
           }
@@ -573,7 +577,10 @@ __global__ void __launch_bounds__(NW * 32, kMinBlocks<TB, NW>)
             const uint32_t h = and_or(s >> (4 * nib), 0x000F000Fu, kMag);
             return hmul2_bf16(hsub2_bf16(h, zp[kSub ? 0 : hb][nib]), sp[kSub ? 0 : hb][nib]);
           } else {
-            const uint32_t h = and_or(s >> (4 * nib), 0x000F000Fu, kMag);
+            // fp16 1024 + c (even nibble, bits 0-3) or 64 + c (odd nibble left in bits 4-7:
+            // the mantissa step of 64 is 1/16), exact either way; one shift serves nibbles 2, 3
+            const uint32_t h = (nib & 1) ? and_or((nib & 2) ? (s >> 8) : s, 0x00F000F0u, kMag64)
+                                         : and_or((nib & 2) ? (s >> 8) : s, 0x000F000Fu, kMag);
             return hmul2(hsub2(h, zp[kSub ? 0 : hb][nib]), sp[kSub ? 0 : hb][nib]);
           }
         };

@@ -531,13 +531,29 @@ __device__ __forceinline__ void convert_codes(const StageCodes<BITS>& cd, uint32
       v[2 * q] = dq_mul<kBF>(dq_sub<kBF>(prmt(w[q], kMag, 0x7150u), zz), ss);
       v[2 * q + 1] = dq_mul<kBF>(dq_sub<kBF>(prmt(w[q], kMag, 0x7352u), zz), ss);
     }
-  } else {
+  } else if constexpr (kBF) {
     const uint32_t w[4] = {cd.a.x, cd.a.y, cd.a.z, cd.a.w};
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
       for (int ii = 0; ii < 4; ++ii)
         v[4 * jj + ii] = dq_mul<kBF>(dq_sub<kBF>(and_or(w[jj] >> (4 * ii), 0x000F000Fu, kMag), zz), ss);
+  } else {
+    // fp16: a nibble in bits 4-7 of a half lies inside the mantissa, so or'ed under the
+    // exponent of 64 (mantissa step 1/16) it reads exactly 64 + c; pairs 1 and 3 then need
+    // no shift of their own (one shift by 8 serves pairs 2 and 3), and subtracting 64 + z
+    // leaves the same exact c - z
+    constexpr uint32_t kMag64 = 0x54005400u;                            // fp16 64 in both halves
+    const uint32_t zz64 = kMag64 | (((cd.meta >> 16) * 0x00010001u) << 4);  // (64 + z)
+    const uint32_t w[4] = {cd.a.x, cd.a.y, cd.a.z, cd.a.w};
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t hi = w[jj] >> 8;
+      v[4 * jj + 0] = dq_mul<false>(dq_sub<false>(and_or(w[jj], 0x000F000Fu, kMag), zz), ss);
+      v[4 * jj + 1] = dq_mul<false>(dq_sub<false>(and_or(w[jj], 0x00F000F0u, kMag64), zz64), ss);
+      v[4 * jj + 2] = dq_mul<false>(dq_sub<false>(and_or(hi, 0x000F000Fu, kMag), zz), ss);
+      v[4 * jj + 3] = dq_mul<false>(dq_sub<false>(and_or(hi, 0x00F000F0u, kMag64), zz64), ss);
+    }
   }
 }
 

@@ -604,15 +604,21 @@ __global__ void __launch_bounds__(kThreads, BT < kBT ? 2 : 1) prefill_kernel(con
           const uint32_t sp[4] = {s4.x, s4.y, s4.z, s4.w};  // (s[2j], s[2j+1])
           uint32_t zp[4];                                    // (1024+z[2j], 1024+z[2j+1])
           const uint32_t zc = cc ? zw[1] : zw[0];
+          // fp16: odd pairs are read in bits 4-7 under the exponent of 64 (mantissa step 1/16):
+          // 64 + c and 64 + z, exact as 1024 + c is; one shift serves pairs 2 and 3
+          constexpr uint32_t kMag64 = 0x54005400u;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) zp[j] = and_or(zc >> (4 * j), 0x000F000Fu, kMag);
+          for (int j = 0; j < 4; ++j)
+            zp[j] = (kBF || !(j & 1)) ? and_or(zc >> (4 * j), 0x000F000Fu, kMag)
+                                      : and_or(zc >> (4 * j - 4), 0x00F000F0u, kMag64);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             uint32_t v[4];
             const uint32_t wc = cc ? w[e][1] : w[e][0];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const uint32_t h = and_or(wc >> (4 * j), 0x000F000Fu, kMag);
+              const uint32_t h = (kBF || !(j & 1)) ? and_or(wc >> (4 * j), 0x000F000Fu, kMag)
+                                                   : and_or(wc >> (4 * j - 4), 0x00F000F0u, kMag64);
               v[j] = kBF ? hmul2_bf16(hsub2_bf16(h, zp[j]), sp[j]) : hmul2(hsub2(h, zp[j]), sp[j]);
             }
             const int k = rp + 32 * e;
