@@ -99,10 +99,10 @@ def step_flop(names):
 # `python bench.py --steps 20 --warmup 3 --no-cpu-baseline --decode-only` summarised in
 # profiles/decode_tma_70b_m1_bench_launches.md; valid only for the kernel source it was
 # measured on (SHA-256 of the files below), else reported as null.
-TRAFFIC_BYTES_PER_LAUNCH = 93_193_924
+TRAFFIC_BYTES_PER_LAUNCH = 93_185_075
 TRAFFIC_SOURCES = {
     "w4a16_weight_only_gb300/csrc/awq_decode_tma.cu":
-        "b01453c4e416019eed09b63b331e35f7da7f3a4ec5ddc4950faa12ed7a5b4818",
+        "3abd9c35b548d6d2a6de5abf5895ead1aa80163b256e434f3e0379e9d03701e0",
     "w4a16_weight_only_gb300/csrc/awq_ptx.cuh":
         "7488ac9d3e1525b7a303d4e435be38b50cdcbf4b04c725918e9c8ee96f8b2e02",
 }
