@@ -175,7 +175,11 @@ def test_repack_w8_bit_exact(awq, K, N, G):
     assert np.array_equal(pk.cpu().numpy().view(np.uint32), want)
 
 
-PACKED8 = [(40, 1024, 512, 128, True, None), (300, 1024, 260, 64, True, None),
+# M <= 32 runs the small-batch kernel (16- or 32-row tiles, several pipelines per CTA):
+# ragged N (N % 8 != 0: 2-byte y stores), G = -1, a 5-stage K split, the 7B shape
+PACKED8 = [(1, 1024, 260, 128, True, None), (16, 4096, 512, 64, True, None), (17, 320, 516, -1, False, None),
+           (32, 4096, 11008, 128, True, None),
+           (40, 1024, 512, 128, True, None), (300, 1024, 260, 64, True, None),
            (257, 4096, 2048, 128, True, "ws"), (300, 8192, 512, 128, False, None),
            (700, 512, 1028, -1, True, None)]
 
@@ -200,7 +204,8 @@ def test_gemm_packed_w8_vs_oracle(awq, M, K, N, G, bias, ws):
     assert torch.equal(y, y2)
 
 
-@pytest.mark.parametrize("M,K,N,ws", [(300, 2048, 384, None), (257, 4096, 2048, "ws"), (64, 2048, 384, None)])
+@pytest.mark.parametrize("M,K,N,ws", [(300, 2048, 384, None), (257, 4096, 2048, "ws"), (64, 2048, 384, None),
+                                      (1, 2048, 384, None), (16, 4096, 260, None), (32, 1024, 516, None)])
 def test_gemm_packed_w8_exact_case_bitwise(awq, M, K, N, ws):
     # small-integer activations, power-of-two scales: every product and partial sum is exact,
     # so y is the oracle's value rounded once to fp16 whatever the summation order

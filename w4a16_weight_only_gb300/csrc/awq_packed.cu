@@ -1232,7 +1232,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
 }
 
 // ------------------------------------------------------------ small batches ----
-// Token tiles of 16 or 32 rows (M <= 32, 4-bit codes).  A 32-row tile gives the tensor core
+// Token tiles of 16 or 32 rows (M <= 32; 4-bit codes, or 8-bit ones in their own blocks).  A 32-row tile gives the tensor core
 // about 32 cycles of work a stage, far less than the issue cost of the stage's own async
 // instructions on one thread (each tcgen05.mma, commit, bulk copy or barrier wait takes
 // some 60-100 cycles to issue, measured with clock stamps), so one pipeline per SM leaves
@@ -1249,10 +1249,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<BT, SPLIT, BITS>::kNarrow ? 2 : 
 // counted on one barrier) and it adds all CS partials in rank order (bitwise repeatable),
 // adds the bias and stores y.
 constexpr int kSmallMaxCS = 16;
-template <int BT, int NP>
+template <int BT, int NP, int BITS = 4>
 struct SmallCfg {
   static_assert(BT == 16 || BT == 32, "token tiles of 16 or 32 rows");
   static_assert(NP == 2 || NP == 4, "two or four pipelines");
+  static constexpr int BLK = Blk<BITS>::BYTES;        // packed block of a stage
   static constexpr int P = NP;
   static constexpr int THREADS = P * 6 * 32;
   static constexpr int PER_SM = 4 / P;                // CTAs per SM
@@ -1263,25 +1264,31 @@ struct SmallCfg {
   static constexpr int RECV_BYTES = (kTN + kSmallMaxCS) * RECV_PITCH * 4;
   // an SM's shared memory over its CTAs, less the per-CTA reservation
   static constexpr int CAP = P == 4 ? kSmemCap : 228 * 1024 / PER_SM - 1024;
-  static constexpr int ST0 = (CAP - 2048 - RECV_BYTES) / (P * (X_BYTES + kBlockBytes));
-  static constexpr int ST = ST0 < 8 ? ST0 : 8;        // ring stages per pipeline
+  static constexpr int ST0 = (CAP - 2048 - RECV_BYTES) / (P * (X_BYTES + BLK));
+  // the ring must be deeper than the A slots (8-bit codes with 32-row tiles leave two
+  // pipelines too little shared memory: that variant does not exist)
+  static constexpr bool FITS = ST0 > SA;
+  static constexpr int ST = !FITS ? SA + 1 : ST0 < 8 ? ST0 : 8;  // ring stages per pipeline
   static constexpr int X_OFF = 0;                     // x ring of pipeline j, stage s: (j ST + s) X_BYTES
   static constexpr int B_OFF = P * ST * X_BYTES;
-  static constexpr int BAR_OFF = B_OFF + P * ST * kBlockBytes;
+  static constexpr int BAR_OFF = B_OFF + P * ST * BLK;
   // per pipeline: full_t[ST], empty_t[ST], full_a[SA], acc_full; then recv
   static constexpr int ACC = 2 * ST + SA;             // acc_full's index in a pipeline's barriers
   static constexpr int NB = ACC + 1;
   static constexpr int MISC_OFF = BAR_OFF + (P * NB + 1) * 8;
   static constexpr int RECV_OFF = ((MISC_OFF + 8 + 15) / 16) * 16;
   static constexpr int SMEM = 1024 + RECV_OFF + RECV_BYTES;
-  static_assert(ST > SA && SMEM <= CAP, "resources");
+  static_assert(!FITS || SMEM <= CAP, "resources");
   static_assert(32 + SA * 32 <= COLS / P, "TMEM columns");
 };
 
-template <int BT, int NP, bool kBF>
-__global__ void __launch_bounds__(SmallCfg<BT, NP>::THREADS, SmallCfg<BT, NP>::PER_SM)
+template <int BT, int NP, bool kBF, int BITS>
+__global__ void __launch_bounds__(SmallCfg<BT, NP, BITS>::THREADS, SmallCfg<BT, NP, BITS>::PER_SM)
     packed_small_kernel(const __grid_constant__ PackedParams p) {
-  using CF = SmallCfg<BT, NP>;
+  using CF = SmallCfg<BT, NP, BITS>;
+  using BK = Blk<BITS>;
+  static_assert(CF::FITS, "ring deeper than the A slots");
+  static_assert(BITS == 4 || !kBF, "8-bit codes: fp16 only");
   constexpr int ST = CF::ST, SA = CF::SA, P = CF::P, NB = CF::NB;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -1312,7 +1319,7 @@ __global__ void __launch_bounds__(SmallCfg<BT, NP>::THREADS, SmallCfg<BT, NP>::P
   uint64_t* full_a = bars + 2 * ST;    // A slot dequantized
   uint64_t* acc_full = bars + CF::ACC;  // every MMA of the pipeline done
   unsigned char* xring = smem + CF::X_OFF + pipe * ST * CF::X_BYTES;
-  unsigned char* bring = smem + CF::B_OFF + pipe * ST * kBlockBytes;
+  unsigned char* bring = smem + CF::B_OFF + pipe * ST * BK::BYTES;
 
   if (threadIdx.x == 0) {
     for (int j = 0; j < P; ++j) {
@@ -1355,16 +1362,15 @@ __global__ void __launch_bounds__(SmallCfg<BT, NP>::THREADS, SmallCfg<BT, NP>::P
     if (lane == 0) {
       prefetch_tmap(&p.tm_x);
       const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
-      const uint32_t* src = p.packed + (static_cast<size_t>(nt) * KS + kb0) * kBlockWords;
+      const uint32_t* src = p.packed + (static_cast<size_t>(nt) * KS + kb0) * BK::WORDS;
       int issued = 0;
       bool ok = true;
       for (int i = 0; i < nst; ++i) {
         const int s = i % ST;
         if (!wait(&empty_t[s], static_cast<uint32_t>((i / ST) & 1) ^ 1u)) { ok = false; break; }
-        mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + kBlockBytes));
+        mbar_arrive_expect_tx(&full_t[s], static_cast<uint32_t>(CF::X_BYTES + BK::BYTES));
         tma_load_2d_hint(xring + s * CF::X_BYTES, &p.tm_x, &full_t[s], (kb0 + i) * kTK, m0, pol_x);
-        bulk_load(bring + s * kBlockBytes, src + static_cast<size_t>(i) * kBlockWords, kBlockBytes, &full_t[s],
-                  pol_w);
+        bulk_load(bring + s * BK::BYTES, src + static_cast<size_t>(i) * BK::WORDS, BK::BYTES, &full_t[s], pol_w);
         ++issued;
       }
       if (!ok)  // every issued stage's copies land before the CTA may exit
@@ -1412,11 +1418,15 @@ __global__ void __launch_bounds__(SmallCfg<BT, NP>::THREADS, SmallCfg<BT, NP>::P
     for (int i = 0; i < nst; ++i) {
       const int s = i % ST, a = i % SA;
       if (!wait(&full_t[s], static_cast<uint32_t>((i / ST) & 1))) { ok = false; break; }
-      StageCodes<4> c0, c1;
-      const unsigned char* blk = bring + s * kBlockBytes;
-      load_codes<4>(blk, 0, c, c0);
-      c1.a = *reinterpret_cast<const uint4*>(blk + 16 * (128 + c));
-      c1.meta = c0.meta;
+      StageCodes<BITS> c0, c1;
+      const unsigned char* blk = bring + s * BK::BYTES;
+      load_codes<BITS>(blk, 0, c, c0);
+      if constexpr (BITS == 8) {
+        load_codes<8>(blk, 1, c, c1);
+      } else {
+        c1.a = *reinterpret_cast<const uint4*>(blk + 16 * (128 + c));
+        c1.meta = c0.meta;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_t[s]);  // the block is read; the MMAs commit the rest
       // A slot a was last read by stage i - SA, whose MMAs complete the phase of its ring slot
@@ -1427,9 +1437,9 @@ __global__ void __launch_bounds__(SmallCfg<BT, NP>::THREADS, SmallCfg<BT, NP>::P
       }
       tc_fence_after();  // the TMEM stores below come after the slot's previous MMAs
       uint32_t v[16];
-      convert_codes<4, kBF>(c0, v);
+      convert_codes<BITS, kBF>(c0, v);
       tmem_st16(tcol + lane_addr + 32u + static_cast<uint32_t>(32 * a), v);
-      convert_codes<4, kBF>(c1, v);
+      convert_codes<BITS, kBF>(c1, v);
       tmem_st16(tcol + lane_addr + 48u + static_cast<uint32_t>(32 * a), v);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
@@ -1924,26 +1934,28 @@ cudaError_t launch_bt(const PackedParams& base, const GemmProblem& p) {
 struct SmallPlan {
   int np = 4, cs = 1;
 };
-template <int BT, int NP, bool kBF>
+template <int BT, int NP, bool kBF, int BITS>
 cudaError_t small_attrs(int dev) {
-  using CF = SmallCfg<BT, NP>;
+  using CF = SmallCfg<BT, NP, BITS>;
   static std::mutex mu;
   static bool set[64];
   std::lock_guard<std::mutex> lock(mu);
   if (set[dev]) return cudaSuccess;
-  auto kern = packed_small_kernel<BT, NP, kBF>;
+  auto kern = packed_small_kernel<BT, NP, kBF, BITS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) set[dev] = true;
   return e;
 }
-template <int BT, bool kBF>
+template <int BT, bool kBF, int BITS>
 cudaError_t small_plan(int dev, long long tiles, int KS, int sms, SmallPlan* out) {
-  using C4 = SmallCfg<BT, 4>;
+  using C4 = SmallCfg<BT, 4, BITS>;
+  constexpr bool kTwo = SmallCfg<BT, 2, BITS>::FITS;
   static std::mutex mu;
   static int fits[64][kSmallMaxCS + 1];  // clusters of c CTAs x c at one CTA per SM (0: not asked)
-  cudaError_t e = small_attrs<BT, 4, kBF>(dev);
-  if (e == cudaSuccess) e = small_attrs<BT, 2, kBF>(dev);
+  cudaError_t e = small_attrs<BT, 4, kBF, BITS>(dev);
+  if constexpr (kTwo)
+    if (e == cudaSuccess) e = small_attrs<BT, 2, kBF, BITS>(dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   for (int c = 1; c <= kSmallMaxCS && c <= KS; ++c) {
@@ -1961,7 +1973,7 @@ cudaError_t small_plan(int dev, long long tiles, int KS, int sms, SmallPlan* out
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, packed_small_kernel<BT, 4, kBF>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, packed_small_kernel<BT, 4, kBF, BITS>, &cfg) != cudaSuccess) {
       (void)cudaGetLastError();
       n = 0;
     }
@@ -1969,6 +1981,7 @@ cudaError_t small_plan(int dev, long long tiles, int KS, int sms, SmallPlan* out
   }
   double best = 0.0;
   for (int np : {4, 2}) {
+    if (np == 2 && !kTwo) continue;
     const int per_sm = 4 / np;
     int cs = 1;
     for (int c = 2; c <= kSmallMaxCS && c <= KS; ++c)
@@ -1988,9 +2001,9 @@ cudaError_t small_plan(int dev, long long tiles, int KS, int sms, SmallPlan* out
   return cudaSuccess;
 }
 
-template <int BT, int NP, bool kBF>
+template <int BT, int NP, bool kBF, int BITS>
 cudaError_t launch_small_np(const PackedParams& pp, const GemmProblem& p, int cs) {
-  using CF = SmallCfg<BT, NP>;
+  using CF = SmallCfg<BT, NP, BITS>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(pp.tiles) * cs), 1, 1);
   cfg.blockDim = dim3(CF::THREADS, 1, 1);
@@ -2003,12 +2016,12 @@ cudaError_t launch_small_np(const PackedParams& pp, const GemmProblem& p, int cs
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_small_kernel<BT, NP, kBF>, pp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, packed_small_kernel<BT, NP, kBF, BITS>, pp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int BT, bool kBF>
+template <int BT, bool kBF, int BITS>
 cudaError_t launch_small(const PackedParams& base, const GemmProblem& p) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -2025,9 +2038,11 @@ cudaError_t launch_small(const PackedParams& base, const GemmProblem& p) {
   if (tiles * kSmallMaxCS > 0x7fffffffLL) return cudaErrorInvalidValue;
   pp.tiles = static_cast<int>(tiles);
   SmallPlan pl;
-  e = small_plan<BT, kBF>(dev, tiles, p.K / kTK, sms, &pl);
+  e = small_plan<BT, kBF, BITS>(dev, tiles, p.K / kTK, sms, &pl);
   if (e != cudaSuccess) return e;
-  return pl.np == 2 ? launch_small_np<BT, 2, kBF>(pp, p, pl.cs) : launch_small_np<BT, 4, kBF>(pp, p, pl.cs);
+  if constexpr (SmallCfg<BT, 2, BITS>::FITS)
+    if (pl.np == 2) return launch_small_np<BT, 2, kBF, BITS>(pp, p, pl.cs);
+  return launch_small_np<BT, 4, kBF, BITS>(pp, p, pl.cs);
 }
 
 // Stream-K launch (256-row tiles): one CTA per SM, at least kSkMinUnits stages each.
@@ -2085,7 +2100,7 @@ bool use_stream_k(int M, int K, int N, int sms, bool pair) {
 // Token tile and K split of a launch with M <= 128 rows: the narrowest tile holding M rows
 // (32, 64 or 128), and the largest split (2 or 4 for 32 rows, 2 for 64 and 128) that keeps
 // every CTA resident in one wave (two CTAs per SM below 128-row tiles) with at least four
-// stages each.  (4-bit launches of at most 32 rows take the small-batch kernel instead.)
+// stages each.  (Launches of at most 32 rows take the small-batch kernel instead.)
 struct PackedPlan {
   int bt = 256, split = 1;
 };
@@ -2109,7 +2124,7 @@ template <bool kBF, int BITS>
 cudaError_t launch_planned(const PackedParams& pp, const GemmProblem& p, void* workspace, size_t workspace_bytes,
                            int sms) {
   const PackedPlan pl = packed_plan(p.M, p.K, p.N, sms);
-  if (BITS == 4 && p.M <= 32) return p.M <= 16 ? launch_small<16, kBF>(pp, p) : launch_small<32, kBF>(pp, p);
+  if (p.M <= 32) return p.M <= 16 ? launch_small<16, kBF, BITS>(pp, p) : launch_small<32, kBF, BITS>(pp, p);
   if (pl.bt == 32)
     return pl.split == 4 ? launch_bt<32, 4, kBF, BITS>(pp, p) : pl.split == 2 ? launch_bt<32, 2, kBF, BITS>(pp, p) : launch_bt<32, 1, kBF, BITS>(pp, p);
   if (pl.bt == 64) return pl.split == 2 ? launch_bt<64, 2, kBF, BITS>(pp, p) : launch_bt<64, 1, kBF, BITS>(pp, p);
