@@ -884,7 +884,8 @@ def w8_bytes(M, K, N, G, bias):
 def run_w8_sweep(awq, timed, hbm, hbm_kind):
     """awq_gemm_w8 (8-bit codes) on the 7B decode linears, a 16-row batch and a 70B MLP
     linear: HBM GB/s over CUDA-graph replays of rotating weight copies (together > 3x L2),
-    for the automatic path and for the plain generic kernel."""
+    for the automatic path, for the plain generic kernel, and for awq_gemm_packed on the
+    8-bit tile-packed copies."""
     import torch
     stream = torch.cuda.Stream()
     for (M, K, N) in ((1, 4096, 4096), (1, 4096, 11008), (1, 11008, 4096), (16, 4096, 11008),
@@ -918,6 +919,21 @@ def run_w8_sweep(awq, timed, hbm, hbm_kind):
             line.update({key + "us": t, key + "GB_s": nbytes / t / 1e3,
                          key + "frac_hbm": nbytes / t / 1e3 / hbm})
             del g
+        # the 8-bit tile-packed copies (the small-batch kernel), replayed the same way
+        pks = [awq.awq_repack(s[0], s[1], s[2], G, stream=stream, bits=8) for s in sets]
+        calls = max(R, (240 // R) * R)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for i in range(2 * R):
+                awq.awq_gemm_packed(x, pks[i % R], bias, K, N, G, out=y, stream=stream, bits=8)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(calls):
+                    awq.awq_gemm_packed(x, pks[i % R], bias, K, N, G, out=y, stream=stream, bits=8)
+        t = sorted(timed(g.replay, 1) / calls for _ in range(5))[2]
+        awq.device_status()
+        line.update({"packed_us": t, "packed_GB_s": nbytes / t / 1e3, "packed_frac_hbm": nbytes / t / 1e3 / hbm})
+        del g, pks
         print(json.dumps(line), flush=True)
         del sets, w, x, y
         torch.cuda.empty_cache()
