@@ -17,6 +17,12 @@ INVALID, SHAPE, MISALIGNED, DEVICE = 1, 2, 3, 4
 
 @pytest.fixture(scope="module")
 def lib():
+    # The calls below pass fake device addresses: where a CUDA device is present, a call
+    # with valid arguments would launch a kernel on them, so these checks run only where
+    # there is none (the GPU tests cover the same entry points with real buffers).
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only checks with fake device addresses; a CUDA device is present")
     from w4a16_weight_only_gb300 import build
     build.build()
     from w4a16_weight_only_gb300 import _binding
