@@ -96,8 +96,8 @@ def step_flop(names):
 
 # DRAM traffic of the decode kernel per launch (dram__bytes_read.sum + dram__bytes_write.sum),
 # averaged over the three linears of one headline step, from the ncu launch list of
-# `python bench.py --steps 20 --warmup 3 --no-cpu-baseline --decode-only` summarised in
-# profiles/decode_tma_70b_m1_bench_launches.md; valid only for the kernel source it was
+# `python bench.py --steps 20 --warmup 3 --no-cpu-baseline --decode-only` (its summary is
+# the decode launch-list profile under profiles/); valid only for the kernel source it was
 # measured on (SHA-256 of the files below), else reported as null.
 TRAFFIC_BYTES_PER_LAUNCH = 93_185_075
 TRAFFIC_SOURCES = {
